@@ -1,0 +1,91 @@
+"""Seeded synthetic inputs for the attention workloads.
+
+This module holds no attention arithmetic: it only draws random tensors, so both
+the oracle side (tests) and the CUDA side may use it.
+
+Recipe (all workloads): a CPU ``torch.Generator`` seeded with ``seed``; fp32
+standard normal draws in the order Q, K, V, dO; each then rounded to bf16
+(round to nearest even).  Layout ``[B, N, H, d]``.  The grouped-query workload
+adds outliers: one channel index c in [0, d) is drawn from the same generator
+after the four tensors, and Q[..., c] and K[..., c] are multiplied by 20 before
+the bf16 rounding (1% of d=128 channels, rounded to one channel, shared by all
+heads and tokens).
+
+Large workloads can be drawn on the GPU instead (``device='cuda'``, a CUDA
+generator with the same seed); those values differ from the CPU draws and are
+used only where the reference values are computed from the very same tensors.
+"""
+
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    outliers: bool = False
+    seed: int = 0
+    decode: bool = False
+    extra: dict = field(default_factory=dict, compare=False, hash=False)
+
+    @property
+    def scale(self):
+        return 1.0 / (self.d ** 0.5)
+
+
+# The five workloads of the benchmark plan, by what they are.
+TINY = Workload("tiny_b1_h1_n256_d64", 1, 1, 1, 256, 256, 64, False)
+MHA_N2048_D64 = Workload("mha_b4_h16_n2048_d64", 4, 16, 16, 2048, 2048, 64, False)
+CAUSAL_N4096_D128 = Workload("causal_b2_h16_n4096_d128", 2, 16, 16, 4096, 4096, 128, True)
+GQA_N8192_D128 = Workload("gqa_causal_b1_hq32_hkv8_n8192_d128_outliers", 1, 32, 8, 8192, 8192, 128,
+                          True, outliers=True)
+DECODE_Q1 = Workload("decode_b8_hq32_hkv8_q1_kv131072_d128", 8, 32, 8, 1, 131072, 128, False, decode=True)
+DECODE_Q4 = Workload("decode_b8_hq32_hkv8_q4_kv131072_d128", 8, 32, 8, 4, 131072, 128, False, decode=True)
+
+ALL = [TINY, MHA_N2048_D64, CAUSAL_N4096_D128, GQA_N8192_D128, DECODE_Q1, DECODE_Q4]
+
+
+def make(w, device="cpu", with_do=True, seed=None):
+    """Draw (q, k, v, do) bf16 tensors for workload ``w`` on ``device``.
+
+    Returns a dict with keys q, k, v, do (do is None when ``with_do`` is False
+    or for decode workloads), and ``outlier_channel`` (int or None).
+    """
+    seed = w.seed if seed is None else seed
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def draw(n, h):
+        return torch.randn((w.B, n, h, w.d), generator=gen, dtype=torch.float32, device=device)
+
+    q = draw(w.Nq, w.Hq)
+    k = draw(w.Nk, w.Hkv)
+    v = draw(w.Nk, w.Hkv)
+    do = draw(w.Nq, w.Hq) if (with_do and not w.decode) else None
+    ch = None
+    if w.outliers:
+        ch = int(torch.randint(0, w.d, (1,), generator=gen, device=device).item())
+        q[..., ch] *= 20.0
+        k[..., ch] *= 20.0
+    out = {
+        "q": q.to(torch.bfloat16),
+        "k": k.to(torch.bfloat16),
+        "v": v.to(torch.bfloat16),
+        "do": None if do is None else do.to(torch.bfloat16),
+        "outlier_channel": ch,
+    }
+    return out
+
+
+def shape_inputs(B, Hq, Hkv, Nq, Nk, d, seed=0, device="cpu", with_do=True):
+    """Draw (q, k, v, do) for an arbitrary shape with the same recipe (no outliers)."""
+    w = Workload("custom", B, Hq, Hkv, Nq, Nk, d, False, seed=seed)
+    return make(w, device=device, with_do=with_do)

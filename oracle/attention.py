@@ -1,0 +1,290 @@
+"""fp64 CPU oracle: scaled-dot-product attention, its gradients, and FlashDecoding.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).  Plain numpy in float64.
+
+Tensor layout everywhere: ``[B, N, H, d]`` (batch, sequence, head, head dim), as
+in the ``flash_attn_func`` interface of "第18章 FlashAttention" §18.7.1.  K and V
+carry ``Hkv`` heads; query head ``h`` reads KV head ``h // (Hq // Hkv)``
+(consecutive grouping; §18.2.2 says groups of query heads share one K/V head but
+not which ones, so the plainest grouping is taken).  LSE is ``[B, Hq, Nq]``.
+
+Definitions followed (one bullet per function below):
+  * forward: S = scale * Q K^T, causal S_ij = -inf for j > i, P = softmax(S)
+    row-wise with the max subtracted first (safe softmax), O = P V,
+    LSE_i = m_i + ln(sum_j exp(S_ij - m_i)).  "第18章" §18.1.1 code listing and
+    §18.2.1 (score, scaling, softmax), §18.2.2 (causal mask), §18.4.2 (safe
+    softmax), Fig. 18-6 (the saved statistic is the log-sum-exp).
+  * backward: dV = P^T dO, dP = dO V^T, D = rowsum(P * dP), dS = P * (dP - D),
+    dQ = scale dS K, dK = scale dS^T Q; for grouped heads dK/dV sum over the
+    group (chain rule through the broadcast).  §18.2.4 and §18.4.4 gradient
+    formulas; D is taken over the whole row, as its definition states.
+  * tiled forward: the outer/inner loop with running max m and sum l of
+    §18.4.1 and the online update of §18.4.2; CMU 11-868 L21 notes slide 12
+    (two-block rescaling) and its Algorithm-1 remark.
+  * FlashDecoding: each KV split t yields (m_t, l_t, O_t) with O_t the
+    unnormalised local output; the combine is O = sum_t O_t e^{m_t - m} /
+    sum_t l_t e^{m_t - m}.  §18.8.2 and lecture slides 57-60.
+
+Large inputs are processed in blocks of whole query rows; every row's softmax
+is still complete inside one block, so this is the plain definition, not a
+tiling of it.
+"""
+
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+def _f64(x):
+    """Widen any array-like (numpy, or a torch tensor via numpy()) to float64."""
+    if hasattr(x, "detach"):  # torch tensor: bf16 -> fp32 -> fp64 is exact
+        import torch  # local import: the oracle itself does not need torch
+
+        x = x.detach().to("cpu", torch.float32).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def _check_shapes(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("q, k, v must be [B, N, H, d]")
+    B, Nq, Hq, d = q.shape
+    Bk, Nk, Hkv, dk = k.shape
+    if v.shape != k.shape or Bk != B or dk != d:
+        raise ValueError("k and v must be [B, Nk, Hkv, d] matching q")
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv (grouped-query attention)")
+    return B, Nq, Nk, Hq, Hkv, d
+
+
+def causal_mask(rows, Nk):
+    """Boolean matrix, True where key j is NOT visible to query row i (j > i).
+
+    "第18章" §18.2.2: M_ij = -inf for j > i (top-left aligned; the causal
+    configurations all have Nq == Nk).
+    """
+    rows = np.asarray(rows)
+    return np.arange(Nk)[None, :] > rows[:, None]
+
+
+def _scores(Qr, Kh, scale, rows, causal):
+    S = scale * (Qr @ Kh.T)
+    if causal:
+        S = np.where(causal_mask(rows, Kh.shape[0]), NEG_INF, S)
+    return S
+
+
+def _softmax_rows(S):
+    """Safe softmax of each row (§18.4.2 'Safe Softmax'): max, exp, normalise."""
+    m = S.max(axis=1, keepdims=True)
+    if not np.all(np.isfinite(m)):
+        raise ValueError("a query row sees no key (fully masked row)")
+    E = np.exp(S - m)
+    l = E.sum(axis=1, keepdims=True)
+    return E / l, m[:, 0], l[:, 0]
+
+
+def attention_forward(q, k, v, scale, causal=False, row_block=2048, heads=None, rows=None):
+    """Plain attention forward.  Returns (O [B,Nq,Hq,d], LSE [B,Hq,Nq]).
+
+    ``heads`` (list of (b, h)) and ``rows`` (array of query rows) restrict which
+    outputs are computed; entries not computed are NaN.  Restriction only skips
+    rows: each computed row is the full definition.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Nq, Nk, Hq, Hkv, d = _check_shapes(q, k, v)
+    if causal and Nq != Nk:
+        raise ValueError("causal attention is defined here for Nq == Nk only")
+    g = Hq // Hkv
+    o = np.full((B, Nq, Hq, d), np.nan)
+    lse = np.full((B, Hq, Nq), np.nan)
+    all_rows = np.arange(Nq) if rows is None else np.asarray(rows)
+    for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(Hq)]):
+        kv = h // g
+        Kh, Vh = k[b, :, kv, :], v[b, :, kv, :]
+        for r0 in range(0, len(all_rows), row_block):
+            rr = all_rows[r0:r0 + row_block]
+            S = _scores(q[b, rr, h, :], Kh, scale, rr, causal)
+            P, m, l = _softmax_rows(S)
+            o[b, rr, h, :] = P @ Vh
+            lse[b, h, rr] = m + np.log(l)
+    return o, lse
+
+
+def attention_backward(q, k, v, do, scale, causal=False, row_block=1024, heads=None):
+    """Plain attention backward with S and P materialised.
+
+    Returns (dQ [B,Nq,Hq,d], dK [B,Nk,Hkv,d], dV [B,Nk,Hkv,d]).  With ``heads``
+    given, only those query heads contribute (dQ of other heads is NaN and dK/dV
+    hold only the listed heads' contributions).
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Nq, Nk, Hq, Hkv, d = _check_shapes(q, k, v)
+    if do.shape != q.shape:
+        raise ValueError("dO must have the shape of O")
+    if causal and Nq != Nk:
+        raise ValueError("causal attention is defined here for Nq == Nk only")
+    g = Hq // Hkv
+    dq = np.full(q.shape, np.nan)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(Hq)]):
+        kv = h // g
+        Kh, Vh = k[b, :, kv, :], v[b, :, kv, :]
+        for r0 in range(0, Nq, row_block):
+            rr = np.arange(r0, min(Nq, r0 + row_block))
+            Qr, dOr = q[b, rr, h, :], do[b, rr, h, :]
+            S = _scores(Qr, Kh, scale, rr, causal)
+            P, _, _ = _softmax_rows(S)
+            dv[b, :, kv, :] += P.T @ dOr                 # dV = P^T dO
+            dP = dOr @ Vh.T                              # dP = dO V^T
+            D = np.sum(P * dP, axis=1, keepdims=True)    # D = rowsum(P o dP), full row
+            dS = P * (dP - D)                            # softmax Jacobian
+            dq[b, rr, h, :] = scale * (dS @ Kh)          # dQ = scale dS K
+            dk[b, :, kv, :] += scale * (dS.T @ Qr)       # dK = scale dS^T Q
+    return dq, dk, dv
+
+
+def attention_backward_sampled(q, k, v, do, scale, causal, b, h, q_rows, k_rows, row_block=1024):
+    """Backward of one query head (b, h), returning only sampled output rows.
+
+    Returns (dQ[q_rows], dK_h[k_rows], dV_h[k_rows]) where dK_h/dV_h are the
+    contributions of head h alone (sum them over a group for grouped heads).
+    The full rows of S, P, dP and dS are formed exactly as in
+    ``attention_backward``; only the rows kept at the end differ.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Nq, Nk, Hq, Hkv, d = _check_shapes(q, k, v)
+    kv = h // (Hq // Hkv)
+    Kh, Vh = k[b, :, kv, :], v[b, :, kv, :]
+    q_rows, k_rows = np.asarray(q_rows), np.asarray(k_rows)
+    dq = np.zeros((len(q_rows), d))
+    dk = np.zeros((len(k_rows), d))
+    dv = np.zeros((len(k_rows), d))
+    pos = {int(r): i for i, r in enumerate(q_rows)}
+    for r0 in range(0, Nq, row_block):
+        rr = np.arange(r0, min(Nq, r0 + row_block))
+        Qr, dOr = q[b, rr, h, :], do[b, rr, h, :]
+        S = _scores(Qr, Kh, scale, rr, causal)
+        P, _, _ = _softmax_rows(S)
+        dP = dOr @ Vh.T
+        D = np.sum(P * dP, axis=1, keepdims=True)
+        dS = P * (dP - D)
+        dv += P[:, k_rows].T @ dOr
+        dk += scale * (dS[:, k_rows].T @ Qr)
+        for i, r in enumerate(rr):
+            if int(r) in pos:
+                dq[pos[int(r)]] = scale * (dS[i] @ Kh)
+    return dq, dk, dv
+
+
+def tiled_forward_head(Qh, Kh, Vh, scale, block_r, block_c, causal=False):
+    """One head of the tiled forward with online softmax, in the pages' order.
+
+    "第18章" §18.4.1 (outer loop over Q blocks of B_r rows, inner loop over K/V
+    blocks of B_c rows, running state m, l, O) and §18.4.2 (online update:
+    m_new = max(m, m~), l_new = e^{m-m_new} l + e^{m~-m_new} l~, and the output
+    rescaled by the same factors; final O / l).  Block sizes may be anything;
+    the result must equal the plain definition (the theorem of §18.4.2).
+    Returns (O [Nq, d], LSE [Nq]).
+    """
+    Qh, Kh, Vh = _f64(Qh), _f64(Kh), _f64(Vh)
+    Nq, d = Qh.shape
+    Nk = Kh.shape[0]
+    O = np.zeros((Nq, d))
+    LSE = np.zeros(Nq)
+    for i0 in range(0, Nq, block_r):
+        rows = np.arange(i0, min(Nq, i0 + block_r))
+        Qi = Qh[rows]
+        m = np.full(len(rows), NEG_INF)
+        l = np.zeros(len(rows))
+        Oi = np.zeros((len(rows), d))
+        for j0 in range(0, Nk, block_c):
+            cols = np.arange(j0, min(Nk, j0 + block_c))
+            Sij = scale * (Qi @ Kh[cols].T)
+            if causal:
+                Sij = np.where(cols[None, :] > rows[:, None], NEG_INF, Sij)
+            m_tilde = Sij.max(axis=1)
+            live = np.isfinite(m_tilde)        # rows with at least one visible key here
+            safe_mt = np.where(live, m_tilde, 0.0)
+            P_tilde = np.where(live[:, None], np.exp(Sij - safe_mt[:, None]), 0.0)
+            l_tilde = P_tilde.sum(axis=1)
+            m_new = np.maximum(m, m_tilde)
+            a_old = np.where(np.isfinite(m), np.exp(m - np.where(np.isfinite(m_new), m_new, 0.0)), 0.0)
+            a_new = np.where(live, np.exp(m_tilde - np.where(np.isfinite(m_new), m_new, 0.0)), 0.0)
+            l = a_old * l + a_new * l_tilde
+            Oi = a_old[:, None] * Oi + a_new[:, None] * (P_tilde @ Vh[cols])
+            m = m_new
+        O[rows] = Oi / l[:, None]
+        LSE[rows] = m + np.log(l)
+    return O, LSE
+
+
+def two_block_output(Qh, K1, V1, K2, V2, scale):
+    """Two-block rescaling of lecture slide 12, with exp taken without a max.
+
+    l1 = rowsum(exp(S1)), O1 = exp(S1) V1 / l1; l2 = l1 + rowsum(exp(S2));
+    O2 = (l1 / l2) O1 + exp(S2) V2 / l2.  Only for small scores (no max shift).
+    """
+    Qh, K1, V1, K2, V2 = map(_f64, (Qh, K1, V1, K2, V2))
+    A1 = np.exp(scale * (Qh @ K1.T))
+    A2 = np.exp(scale * (Qh @ K2.T))
+    l1 = A1.sum(axis=1, keepdims=True)
+    O1 = (A1 @ V1) / l1
+    l2 = l1 + A2.sum(axis=1, keepdims=True)
+    return (l1 / l2) * O1 + (A2 @ V2) / l2
+
+
+def decode_partials(q, k, v, scale, splits, heads=None):
+    """FlashDecoding step 2 ("第18章" §18.8.2): per KV split, local statistics.
+
+    ``splits`` is a list of (start, end) key ranges.  Returns (m, l, O_t) with
+    shapes [B, Hq, Nq, T], [B, Hq, Nq, T] and [B, Hq, Nq, T, d], where O_t is the
+    unnormalised local output sum_j e^{s_j - m_t} v_j.  An empty split has
+    m = -inf, l = 0, O_t = 0.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Nq, Nk, Hq, Hkv, d = _check_shapes(q, k, v)
+    g = Hq // Hkv
+    T = len(splits)
+    m = np.full((B, Hq, Nq, T), NEG_INF)
+    l = np.zeros((B, Hq, Nq, T))
+    Ot = np.zeros((B, Hq, Nq, T, d))
+    for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(Hq)]):
+        kv = h // g
+        for t, (s0, s1) in enumerate(splits):
+            if s1 <= s0:
+                continue
+            s = scale * (q[b, :, h, :] @ k[b, s0:s1, kv, :].T)   # [Nq, keys]
+            mt = s.max(axis=1)
+            e = np.exp(s - mt[:, None])
+            m[b, h, :, t] = mt
+            l[b, h, :, t] = e.sum(axis=1)
+            Ot[b, h, :, t, :] = e @ v[b, s0:s1, kv, :]
+    return m, l, Ot
+
+
+def decode_combine(m, l, Ot):
+    """FlashDecoding step 3: O = sum_t O_t e^{m_t - m} / sum_t l_t e^{m_t - m}.
+
+    Returns (O [B, Hq, Nq, d], LSE [B, Hq, Nq]) with LSE = m + ln sum_t l_t e^{m_t-m}.
+    """
+    mg = m.max(axis=-1)
+    w = np.where(np.isfinite(m), np.exp(m - mg[..., None]), 0.0)
+    den = np.sum(l * w, axis=-1)
+    O = np.sum(Ot * w[..., None], axis=-2) / den[..., None]
+    return O, mg + np.log(den)
+
+
+def flops_forward(B, Hq, Nq, Nk, d, causal):
+    """Counted forward FLOPs: two matmuls of 2*Nq*Nk*d each per head, halved for causal.
+
+    "第18章" §18.2.3 (about 4N^2 d for the two products) and §18.5.2 (causal
+    roughly halves it).  Softmax FLOPs are not counted.
+    """
+    f = 4.0 * B * Hq * Nq * Nk * d
+    return f / 2 if causal else f
+
+
+def flops_backward(B, Hq, Nq, Nk, d, causal):
+    """Counted backward FLOPs: 2.5x the forward (five matmuls instead of two)."""
+    return 2.5 * flops_forward(B, Hq, Nq, Nk, d, causal)

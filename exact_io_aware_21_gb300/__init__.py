@@ -1,0 +1,19 @@
+"""exact_io_aware_21_gb300: exact IO-aware attention (FlashAttention) for GB300 (sm_103a).
+
+The compute path is a C-ABI CUDA library (``libfa_gb300.so``, header
+``include/fa.h``); this package is its thin Python binding.  The library is
+loaded on first use and every op raises if it is missing: there is no CPU
+fallback.
+"""
+
+from .binding import (  # noqa: F401
+    FAError,
+    fa_bwd,
+    fa_decode,
+    fa_fwd,
+    forward,
+    backward,
+    decode,
+    library,
+    library_path,
+)

@@ -1,0 +1,182 @@
+"""Thin ctypes binding of libfa_gb300.so (C ABI in include/fa.h).
+
+Argument marshalling only: torch tensors are turned into (pointer, strides)
+descriptors, the workspace and outputs are allocated with torch on the tensors'
+device, and the current torch CUDA stream is passed down.  Every step of the
+attention computation runs in the library's kernels; if the library is not
+built, every call raises ``FAError`` (there is no fallback).
+"""
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+FA_OK = 0
+
+
+class FAError(RuntimeError):
+    """An error code returned by the C ABI (message from fa_strerror)."""
+
+    def __init__(self, code, msg):
+        super().__init__(f"fa error {code}: {msg}")
+        self.code = code
+
+
+class FaTensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("stride_b", ctypes.c_int64), ("stride_n", ctypes.c_int64),
+                ("stride_h", ctypes.c_int64)]
+
+
+class FaShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("Nq", ctypes.c_int),
+                ("Nk", ctypes.c_int), ("d", ctypes.c_int), ("scale", ctypes.c_float), ("causal", ctypes.c_int)]
+
+
+# name -> (restype, argtypes); mirrors include/fa.h
+_PT = ctypes.POINTER(FaTensor)
+_PS = ctypes.POINTER(FaShape)
+_VP = ctypes.c_void_p
+_I = ctypes.c_int
+_PI = ctypes.POINTER(ctypes.c_int)
+_SZ = ctypes.c_size_t
+SIGNATURES = {
+    "fa_fwd_workspace_size": (_SZ, [_PS]),
+    "fa_fwd": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _VP, _SZ, _VP]),
+    "fa_bwd_workspace_size": (_SZ, [_PS]),
+    "fa_bwd": (_I, [_PT, _PT, _PT, _PT, _VP, _PT, _PT, _PT, _PT, _PS, _VP, _SZ, _VP]),
+    "fa_decode_num_splits": (_I, [_PS, _I]),
+    "fa_decode_workspace_size": (_SZ, [_PS, _I]),
+    "fa_decode": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _I, _VP, _SZ, _VP]),
+    "fa_decode_partials_layout": (_I, [_PS, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
+    "fa_get_device_status": (_I, [_VP, _VP, _PI]),
+    "fa_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
+    "fa_strerror": (ctypes.c_char_p, [_I]),
+    "fa_last_cuda_error": (_I, []),
+    "fa_tile_class": (_I, [_PS, _I, _I]),
+    "fa_fwd_num_units": (_I, [_PS]),
+    "fa_fwd_unit": (_I, [_PS, _I, _PI, _PI, _PI]),
+    "fa_dkdv_num_units": (_I, [_PS]),
+    "fa_dkdv_unit": (_I, [_PS, _I, _PI, _PI, _PI]),
+    "fa_dq_num_units": (_I, [_PS]),
+    "fa_dq_unit": (_I, [_PS, _I, _PI, _PI, _PI]),
+    "fa_decode_split_range": (_I, [_PS, _I, _I, _PI, _PI]),
+    "fa_selftest_mma": (_I, [_I, _I, _VP, _VP, _VP, _VP, _VP]),
+}
+
+
+def library_path():
+    return os.path.join(_HERE, "_build", "libfa_gb300.so")
+
+
+def library():
+    """Load libfa_gb300.so (once).  Raises FAError if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise FAError(-1, f"{path} is missing: build it with `python -m exact_io_aware_21_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def check(rc):
+    if rc != FA_OK:
+        lib = library()
+        msg = lib.fa_strerror(rc).decode()
+        if rc in (5, 7):
+            msg += f" (cuda error {lib.fa_last_cuda_error()})"
+        raise FAError(rc, msg)
+
+
+def shape(B, Hq, Hkv, Nq, Nk, d, scale=None, causal=False):
+    return FaShape(B, Hq, Hkv, Nq, Nk, d, 1.0 / math.sqrt(d) if scale is None else float(scale), int(bool(causal)))
+
+
+def tdesc(t):
+    """[B, N, H, d] bf16 CUDA tensor -> FaTensor (strides in elements)."""
+    if t.dim() != 4 or t.dtype != torch.bfloat16 or not t.is_cuda or t.stride(-1) != 1:
+        raise FAError(1, "expected a 4-D bf16 CUDA tensor [B, N, H, d] with unit head-dim stride")
+    return FaTensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ws(nbytes, device):
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------- C-ABI mirrors
+def fa_fwd(q, k, v, o, lse, s, workspace):
+    lib = library()
+    check(lib.fa_fwd(tdesc(q), tdesc(k), tdesc(v), tdesc(o), lse.data_ptr(), ctypes.byref(s),
+                     workspace.data_ptr(), workspace.numel(), _stream(q)))
+
+
+def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, s, workspace):
+    lib = library()
+    check(lib.fa_bwd(tdesc(q), tdesc(k), tdesc(v), tdesc(o), lse.data_ptr(), tdesc(do), tdesc(dq), tdesc(dk),
+                     tdesc(dv), ctypes.byref(s), workspace.data_ptr(), workspace.numel(), _stream(q)))
+
+
+def fa_decode(q, kc, vc, o, lse, s, num_splits, workspace):
+    lib = library()
+    check(lib.fa_decode(tdesc(q), tdesc(kc), tdesc(vc), tdesc(o), lse.data_ptr(), ctypes.byref(s), int(num_splits),
+                        workspace.data_ptr(), workspace.numel(), _stream(q)))
+
+
+def device_status(workspace):
+    """Synchronise and return (rc, status bits) recorded in the workspace."""
+    lib = library()
+    st = ctypes.c_int(0)
+    rc = lib.fa_get_device_status(workspace.data_ptr(), _stream(workspace), ctypes.byref(st))
+    return rc, st.value
+
+
+# ---------------------------------------------------------------- convenience API
+def _dims(q, k, scale, causal):
+    B, Nq, Hq, d = q.shape
+    _, Nk, Hkv, _ = k.shape
+    return shape(B, Hq, Hkv, Nq, Nk, d, scale, causal)
+
+
+def forward(q, k, v, causal=False, scale=None):
+    """O, LSE = attention(q, k, v).  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] bf16 on CUDA."""
+    s = _dims(q, k, scale, causal)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
+    ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q.device)
+    fa_fwd(q, k, v, o, lse, s, ws)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, causal=False, scale=None):
+    """dQ, dK, dV of attention given O and LSE from ``forward`` and the upstream dO."""
+    s = _dims(q, k, scale, causal)
+    dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device)
+    dv = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device)
+    ws = _ws(library().fa_bwd_workspace_size(ctypes.byref(s)), q.device)
+    fa_bwd(q, k, v, o, lse, do, dq, dk, dv, s, ws)
+    return dq, dk, dv
+
+
+def decode(q, k_cache, v_cache, scale=None, num_splits=0):
+    """Split-KV decode: O, LSE for a short query q [B,Nq,Hq,d] against the cache."""
+    s = _dims(q, k_cache, scale, False)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
+    ws = _ws(library().fa_decode_workspace_size(ctypes.byref(s), int(num_splits)), q.device)
+    fa_decode(q, k_cache, v_cache, o, lse, s, num_splits, ws)
+    return o, lse

@@ -1,0 +1,408 @@
+// C ABI of libfa_gb300.so (declared in include/fa.h): argument checks, TMA
+// descriptor encoding, workspace layout, and the launches.  No allocation, no
+// synchronisation and no host-side compute fallback: every attention result
+// comes from the kernels in fa_fwd.cu, fa_bwd.cu and fa_decode.cu.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_kernels.h"
+#include "fa_plan.h"
+#include "fa_status.h"
+
+using namespace fa;
+
+namespace {
+
+unsigned long long g_timeout_ns = 10ull * 1000 * 1000 * 1000;
+int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e, int code) {
+  g_last_cuda_error = static_cast<int>(e);
+  return code;
+}
+
+// ---- device facts ---------------------------------------------------------------
+struct DevInfo {
+  int ok = -1;  // -1 unknown, 0 not sm_103, 1 sm_103
+  int sms = 0;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+int device_info(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, FA_ERR_CUDA);
+  if (dev < 0 || dev >= 64) return FA_ERR_ARCH;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (d.ok < 0) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, FA_ERR_CUDA);
+    d.ok = (major == 10 && minor == 3) ? 1 : 0;
+  }
+  if (d.ok != 1) return FA_ERR_ARCH;
+  *sms = d.sms;
+  return FA_OK;
+}
+
+// ---- TMA descriptor encoding ------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D map over a bf16 [B, N, H, d] tensor: dims (d, H, N, B); box 64 x 1 x 128 x 1,
+// 128-byte swizzle; rows past N read as zero.
+int make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int64_t sb, int64_t sn, int64_t sh) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return FA_ERR_CUDA;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(sn) * 2,
+                           static_cast<cuuint64_t>(sb) * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(TILE), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ALIGN;
+}
+
+// ---- argument checks ----------------------------------------------------------------
+int check_shape(const fa_shape_t* s) {
+  if (!s) return FA_ERR_INVALID;
+  if (s->B <= 0 || s->Hq <= 0 || s->Hkv <= 0 || s->Nq <= 0 || s->Nk <= 0) return FA_ERR_INVALID;
+  if (s->Hq % s->Hkv != 0) return FA_ERR_INVALID;
+  if (s->d != 64 && s->d != 128) return FA_ERR_INVALID;
+  if (!(s->scale > 0.f) || !isfinite(s->scale)) return FA_ERR_INVALID;
+  if (s->causal != 0 && s->causal != 1) return FA_ERR_INVALID;
+  if (s->causal && s->Nq != s->Nk) return FA_ERR_INVALID;
+  // index arithmetic inside the kernels is 32-bit per (head, row) and 64-bit per element
+  if (static_cast<int64_t>(s->B) * s->Hq * s->Nq > (1ll << 31) - 1) return FA_ERR_INVALID;
+  if (static_cast<int64_t>(s->Nk) > (1ll << 30)) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+int check_tensor(const fa_tensor_t* t) {
+  if (!t || !t->ptr) return FA_ERR_INVALID;
+  if (t->stride_b < 0 || t->stride_n < 0 || t->stride_h < 0) return FA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(t->ptr) & 15) != 0) return FA_ERR_ALIGN;
+  if ((t->stride_b % 8) || (t->stride_n % 8) || (t->stride_h % 8)) return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
+int check_ws(const void* ws, size_t have, size_t need) {
+  if (!ws || have < need) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 15) != 0) return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
+Dims dims_of(const fa_shape_t* s) { return Dims{s->B, s->Hq, s->Hkv, s->Nq, s->Nk, s->causal}; }
+
+OutRows rows_of(const fa_tensor_t* t) { return OutRows{t->ptr, t->stride_b, t->stride_n, t->stride_h}; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Every call starts by clearing the workspace header (status word and unit
+// counters), so the status read later belongs to the most recent call.
+int clear_header(void* ws, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(ws, 0, FA_WS_HEADER_BYTES, st);
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_CUDA);
+}
+
+int nq_pad(const fa_shape_t* s) { return cdiv(s->Nq, TILE) * TILE; }
+
+// decode: resolve the requested split count (0 = auto) to the number used
+int decode_splits_resolved(const fa_shape_t* s, int requested, int sms) {
+  const int tiles = cdiv(s->Nk, TILE);
+  int S = requested;
+  if (S <= 0) {
+    // one CTA per SM at a time: minimise (waves x (tiles per split + pipeline
+    // ramp of ~2 tiles)), with a small charge per split for the combine
+    const int units = s->B * s->Hkv;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int c = 1; c <= 256 && c <= tiles; ++c) {
+      const int ctas = units * c;
+      const int waves = cdiv(ctas, sms > 0 ? sms : 1);
+      const double cost = static_cast<double>(waves) * (cdiv(tiles, c) + 2) + 0.01 * c;
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = c;
+      }
+    }
+    S = best;
+  }
+  if (S > tiles) S = tiles;
+  return decode_nsplits(s->Nk, S);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID: return "invalid argument (null pointer, size, Hq % Hkv, head dim, causal with Nq != Nk)";
+    case FA_ERR_ALIGN: return "misaligned tensor (pointer must be 16-byte aligned, strides multiples of 8 elements)";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_ARCH: return "current CUDA device is not an sm_103 (GB300) GPU";
+    case FA_ERR_LAUNCH: return "kernel launch failed";
+    case FA_ERR_TIMEOUT: return "a device-side bounded wait ran out";
+    case FA_ERR_CUDA: return "CUDA runtime or driver call failed";
+    default: return "unknown error";
+  }
+}
+
+int fa_last_cuda_error(void) { return g_last_cuda_error; }
+
+void fa_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns > 0 ? ns : 1; }
+
+// ------------------------------------------------------------------------ plans
+int fa_tile_class(const fa_shape_t* s, int qt, int kt) {
+  if (check_shape(s) != FA_OK) return -1;
+  const Dims d = dims_of(s);
+  if (qt < 0 || kt < 0 || qt >= q_tiles(d) || kt >= k_tiles(d)) return -1;
+  return tile_class(d, qt, kt);
+}
+
+int fa_fwd_num_units(const fa_shape_t* s) { return check_shape(s) == FA_OK ? fwd_units(dims_of(s)) : -1; }
+int fa_dkdv_num_units(const fa_shape_t* s) { return check_shape(s) == FA_OK ? dkdv_units(dims_of(s)) : -1; }
+int fa_dq_num_units(const fa_shape_t* s) { return check_shape(s) == FA_OK ? dq_units(dims_of(s)) : -1; }
+
+int fa_fwd_unit(const fa_shape_t* s, int i, int* b, int* h, int* p) {
+  if (check_shape(s) != FA_OK || !b || !h || !p) return FA_ERR_INVALID;
+  const Dims d = dims_of(s);
+  if (i < 0 || i >= fwd_units(d)) return FA_ERR_INVALID;
+  fwd_unit(d, i, *b, *h, *p);
+  return FA_OK;
+}
+
+int fa_dkdv_unit(const fa_shape_t* s, int i, int* b, int* kvh, int* kt) {
+  if (check_shape(s) != FA_OK || !b || !kvh || !kt) return FA_ERR_INVALID;
+  const Dims d = dims_of(s);
+  if (i < 0 || i >= dkdv_units(d)) return FA_ERR_INVALID;
+  dkdv_unit(d, i, *b, *kvh, *kt);
+  return FA_OK;
+}
+
+int fa_dq_unit(const fa_shape_t* s, int i, int* b, int* h, int* qt) {
+  if (check_shape(s) != FA_OK || !b || !h || !qt) return FA_ERR_INVALID;
+  const Dims d = dims_of(s);
+  if (i < 0 || i >= dq_units(d)) return FA_ERR_INVALID;
+  dq_unit(d, i, *b, *h, *qt);
+  return FA_OK;
+}
+
+int fa_decode_split_range(const fa_shape_t* s, int num_splits, int i, int* start, int* end) {
+  if (check_shape(s) != FA_OK || num_splits <= 0 || !start || !end) return FA_ERR_INVALID;
+  const int n = decode_nsplits(s->Nk, num_splits);
+  if (i < 0 || i >= n) return FA_ERR_INVALID;
+  const int chunk = decode_chunk(s->Nk, num_splits);
+  *start = i * chunk;
+  *end = imin(s->Nk, (i + 1) * chunk);
+  return FA_OK;
+}
+
+// ------------------------------------------------------------------------ status
+int fa_get_device_status(void* ws, void* stream, int* status) {
+  if (!ws || !status) return FA_ERR_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, FA_ERR_CUDA);
+  int v = 0;
+  e = cudaMemcpy(&v, static_cast<char*>(ws) + FA_WS_STATUS_OFFSET, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, FA_ERR_CUDA);
+  e = cudaMemset(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, FA_ERR_CUDA);
+  *status = v;
+  return (v & FA_STATUS_TIMEOUT_MASK) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+// ------------------------------------------------------------------------ forward
+size_t fa_fwd_workspace_size(const fa_shape_t* s) { return check_shape(s) == FA_OK ? FA_WS_HEADER_BYTES : 0; }
+
+int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
+           const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_shape(s)) || (rc = check_tensor(q)) || (rc = check_tensor(k)) || (rc = check_tensor(v)) ||
+      (rc = check_tensor(o)))
+    return rc;
+  if (!lse) return FA_ERR_INVALID;
+  if ((rc = check_ws(ws, ws_bytes, fa_fwd_workspace_size(s)))) return rc;
+  int sms = 0;
+  if ((rc = device_info(&sms))) return rc;
+  FwdLaunch a;
+  memset(&a, 0, sizeof(a));
+  a.dims = dims_of(s);
+  a.d = s->d;
+  a.scale = s->scale;
+  if ((rc = make_map(&a.tm_q, q->ptr, s->B, s->Nq, s->Hq, s->d, q->stride_b, q->stride_n, q->stride_h)) ||
+      (rc = make_map(&a.tm_k, k->ptr, s->B, s->Nk, s->Hkv, s->d, k->stride_b, k->stride_n, k->stride_h)) ||
+      (rc = make_map(&a.tm_v, v->ptr, s->B, s->Nk, s->Hkv, s->d, v->stride_b, v->stride_n, v->stride_h)))
+    return rc;
+  a.o = rows_of(o);
+  a.lse = lse;
+  a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
+  a.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_COUNTER_OFFSET);
+  a.timeout_ns = g_timeout_ns;
+  a.num_sms = sms;
+  if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
+  cudaError_t e = launch_fwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
+}
+
+// ------------------------------------------------------------------------ backward
+size_t fa_bwd_workspace_size(const fa_shape_t* s) {
+  if (check_shape(s) != FA_OK) return 0;
+  const size_t rows = static_cast<size_t>(s->B) * s->Hq * nq_pad(s);
+  return FA_WS_HEADER_BYTES + 2 * round_up(rows * sizeof(float), 256);
+}
+
+int fa_bwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o,
+           const float* lse, const fa_tensor_t* dout, const fa_tensor_t* dq, const fa_tensor_t* dk,
+           const fa_tensor_t* dv, const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_shape(s)) || (rc = check_tensor(q)) || (rc = check_tensor(k)) || (rc = check_tensor(v)) ||
+      (rc = check_tensor(o)) || (rc = check_tensor(dout)) || (rc = check_tensor(dq)) || (rc = check_tensor(dk)) ||
+      (rc = check_tensor(dv)))
+    return rc;
+  if (!lse) return FA_ERR_INVALID;
+  if ((rc = check_ws(ws, ws_bytes, fa_bwd_workspace_size(s)))) return rc;
+  int sms = 0;
+  if ((rc = device_info(&sms))) return rc;
+  BwdLaunch a;
+  memset(&a, 0, sizeof(a));
+  a.dims = dims_of(s);
+  a.d = s->d;
+  a.scale = s->scale;
+  if ((rc = make_map(&a.tm_q, q->ptr, s->B, s->Nq, s->Hq, s->d, q->stride_b, q->stride_n, q->stride_h)) ||
+      (rc = make_map(&a.tm_k, k->ptr, s->B, s->Nk, s->Hkv, s->d, k->stride_b, k->stride_n, k->stride_h)) ||
+      (rc = make_map(&a.tm_v, v->ptr, s->B, s->Nk, s->Hkv, s->d, v->stride_b, v->stride_n, v->stride_h)) ||
+      (rc = make_map(&a.tm_do, dout->ptr, s->B, s->Nq, s->Hq, s->d, dout->stride_b, dout->stride_n,
+                     dout->stride_h)))
+    return rc;
+  a.o = rows_of(o);
+  a.dout = rows_of(dout);
+  a.dq = rows_of(dq);
+  a.dk = rows_of(dk);
+  a.dv = rows_of(dv);
+  a.lse = lse;
+  a.nq_pad = nq_pad(s);
+  const size_t rows = static_cast<size_t>(s->B) * s->Hq * a.nq_pad;
+  char* base = static_cast<char*>(ws);
+  a.lse2 = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES);
+  a.delta = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES + round_up(rows * sizeof(float), 256));
+  a.status = reinterpret_cast<int*>(base + FA_WS_STATUS_OFFSET);
+  a.counters = reinterpret_cast<int*>(base + FA_WS_COUNTER_OFFSET);
+  a.timeout_ns = g_timeout_ns;
+  a.num_sms = sms;
+  if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
+  cudaError_t e = launch_bwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
+}
+
+// ------------------------------------------------------------------------ decode
+int fa_decode_num_splits(const fa_shape_t* s, int num_splits) {
+  if (check_shape(s) != FA_OK) return -1;
+  int sms = 148;
+  if (num_splits <= 0 && device_info(&sms) != FA_OK) sms = 148;
+  return decode_splits_resolved(s, num_splits, sms);
+}
+
+int fa_decode_partials_layout(const fa_shape_t* s, int num_splits, size_t* lse_off, size_t* o_off) {
+  const int S = fa_decode_num_splits(s, num_splits);
+  if (S <= 0 || !lse_off || !o_off) return FA_ERR_INVALID;
+  const size_t rows = static_cast<size_t>(s->B) * s->Hq * s->Nq * S;
+  *lse_off = FA_WS_HEADER_BYTES;
+  *o_off = FA_WS_HEADER_BYTES + round_up(rows * sizeof(float), 256);
+  return FA_OK;
+}
+
+size_t fa_decode_workspace_size(const fa_shape_t* s, int num_splits) {
+  const int S = fa_decode_num_splits(s, num_splits);
+  if (S <= 0) return 0;
+  const size_t rows = static_cast<size_t>(s->B) * s->Hq * s->Nq * S;
+  return FA_WS_HEADER_BYTES + round_up(rows * sizeof(float), 256) + round_up(rows * s->d * sizeof(float), 256);
+}
+
+int fa_decode(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor_t* vc, const fa_tensor_t* o,
+              float* lse, const fa_shape_t* s, int num_splits, void* ws, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_shape(s)) || (rc = check_tensor(q)) || (rc = check_tensor(kc)) || (rc = check_tensor(vc)) ||
+      (rc = check_tensor(o)))
+    return rc;
+  if (!lse || s->causal) return FA_ERR_INVALID;
+  if ((s->Hq / s->Hkv) * s->Nq > 16) return FA_ERR_INVALID;  // packed rows must fit one 16-row tile
+  int sms = 0;
+  if ((rc = device_info(&sms))) return rc;
+  const int S = decode_splits_resolved(s, num_splits, sms);
+  if ((rc = check_ws(ws, ws_bytes, fa_decode_workspace_size(s, num_splits)))) return rc;
+  DecodeLaunch a;
+  memset(&a, 0, sizeof(a));
+  a.dims = dims_of(s);
+  a.d = s->d;
+  a.scale = s->scale;
+  if ((rc = make_map(&a.tm_k, kc->ptr, s->B, s->Nk, s->Hkv, s->d, kc->stride_b, kc->stride_n, kc->stride_h)) ||
+      (rc = make_map(&a.tm_v, vc->ptr, s->B, s->Nk, s->Hkv, s->d, vc->stride_b, vc->stride_n, vc->stride_h)))
+    return rc;
+  a.q = q->ptr;
+  a.q_sb = q->stride_b;
+  a.q_sn = q->stride_n;
+  a.q_sh = q->stride_h;
+  a.o = rows_of(o);
+  a.lse = lse;
+  size_t lo = 0, oo = 0;
+  fa_decode_partials_layout(s, num_splits, &lo, &oo);
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(ws) + lo);
+  a.o_part = reinterpret_cast<float*>(static_cast<char*>(ws) + oo);
+  a.num_splits = S;
+  // the chunk that yields exactly S splits
+  a.chunk = decode_chunk(s->Nk, S);
+  a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
+  a.timeout_ns = g_timeout_ns;
+  if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
+  cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
+}
+
+// ------------------------------------------------------------------------ self-test
+int fa_selftest_mma(int mode, int nk, const void* a, const void* b, float* c, void* ws, void* stream) {
+  if ((mode != 0 && mode != 1) || (nk != 64 && nk != 128) || !a || !b || !c) return FA_ERR_INVALID;
+  int sms = 0, rc;
+  if ((rc = check_ws(ws, FA_WS_HEADER_BYTES, FA_WS_HEADER_BYTES))) return rc;
+  if ((rc = device_info(&sms))) return rc;
+  CUtensorMap ta, tb;
+  // mode 0: a, b are [128 x k] row-major.  mode 1: a [128 x 128] is read by
+  // threads (the map over it is unused), b is [128 x n] row-major.
+  if ((rc = make_map(&ta, mode == 0 ? a : b, 1, 128, 1, nk, 128 * nk, nk, nk)) ||
+      (rc = make_map(&tb, b, 1, 128, 1, nk, 128 * nk, nk, nk)))
+    return rc;
+  int* status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
+  if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
+  cudaError_t e = launch_selftest_mma(mode, nk, ta, tb, a, c, status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
+}
+
+}  // extern "C"

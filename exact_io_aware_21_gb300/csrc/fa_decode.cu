@@ -1,0 +1,379 @@
+// Split-KV decode (FlashDecoding) and its log-sum-exp weighted combine.
+//
+// Method ("第18章 FlashAttention" §18.8.2; "CMU 11-868 L21" notes, slides
+// 57-60): with a short query and a long KV cache, the cache is cut along its
+// length into chunks that run in parallel; each chunk yields its own softmax
+// statistics and partial output, and a second kernel merges them with weights
+// e^{m_t - m}.  The query heads that share one K/V head, times the query
+// positions, are packed into the rows of one matrix tile (GQA packing), so
+// each K/V byte is read from HBM once for all of them.
+//
+// GB300 design.  The work is HBM-bound (4-16 flop per byte), so the kernel is
+// built around the copy engine: one CTA per (split, K/V head, batch); a
+// producer warp streams 128-key K and V tiles with TMA (16-byte aligned,
+// 128-byte-swizzled boxes of 64 channels x 128 keys) through a ring of
+// shared-memory stages; 8 compute warps each own 16 keys of every tile.  The
+// packed rows (Hq/Hkv * Nq <= 16) form exactly one 16-row matrix tile, which
+// is what the warp-level mma.sync m16n8k16 handles: the scores, the online
+// softmax and P stay in registers, and no cross-warp exchange is needed until
+// the split ends.  (A 128-row tcgen05 product would be 87% padding here.)
+// The warps' states are merged through shared memory into the split's
+// (LSE_s, O_s); the combine kernel then merges the splits.
+#include <math.h>
+
+#include "fa_kernels.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float LN2 = 0.69314718055994530942f;
+constexpr int WARPS = 8;              // compute warps, 16 keys of each tile apiece
+constexpr int THREADS = 32 * (WARPS + 1);
+
+template <int D>
+struct DecLayout {
+  static constexpr int TB = TILE * D * 2;   // one K or V tile
+  static constexpr int STAGES = D == 64 ? 6 : 3;
+  static constexpr int OFF_KV = 0;          // stage s: K at s*2*TB, V at s*2*TB + TB
+  static constexpr int OFF_BAR = STAGES * 2 * TB;
+  static constexpr int BYTES = OFF_BAR + 2 * STAGES * 8 + 64;
+  static constexpr int ALLOC = BYTES + 1024;
+  // after the pipeline ends the stage memory holds the per-warp states:
+  // m[WARPS][16], l[WARPS][16], o[WARPS][16][D]  (fp32)
+  static_assert(WARPS * 16 * (2 + D) * 4 <= STAGES * 2 * TB, "merge area");
+};
+
+struct DecParams {
+  Dims dims;
+  int d;
+  float scale_log2;
+  const __nv_bfloat16* q;
+  int64_t q_sb, q_sn, q_sh;
+  float* lse_part;
+  float* o_part;
+  int num_splits, chunk;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+// Byte offset of (key, channel) inside a TMA tile of 128 keys x D channels
+// stored as D/64 boxes of [128 keys][128 bytes] with the 128-byte swizzle
+// (16-byte chunk index XOR key % 8).
+__device__ __forceinline__ uint32_t swz(int key, int ch) {
+  return (ch >> 6) * (TILE * 128) + key * 128 + ((((ch & 63) >> 3) ^ (key & 7)) << 4) + ((ch & 7) << 1);
+}
+
+template <int D>
+__global__ void __launch_bounds__(THREADS, 1)
+    fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                           const DecParams p) {
+  using L = DecLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* empty = full + L::STAGES;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const Dims& s = p.dims;
+  const int g = s.Hq / s.Hkv;
+  const int rows = g * s.Nq;
+  const int k0 = split * p.chunk;
+  const int k1 = imin(s.Nk, k0 + p.chunk);
+  const int ntiles = cdiv(k1 - k0, TILE);
+  const int warp = threadIdx.x >> 5, lane = lane_id();
+  const Ctl ctl{p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < L::STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], WARPS);
+    }
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  __syncthreads();
+
+  if (warp == WARPS) {  // ---------------------------------------------- producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t % L::STAGES;
+        if (!mbar_wait(&empty[st], ((t / L::STAGES) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
+        mbar_arrive_expect_tx(&full[st], 2 * L::TB);
+        uint8_t* dst = smem + L::OFF_KV + st * 2 * L::TB;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(dst + c * (TILE * 128), &tm_k, &full[st], c * 64, kvh, k0 + t * TILE, b);
+          tma_load_4d(dst + L::TB + c * (TILE * 128), &tm_v, &full[st], c * 64, kvh, k0 + t * TILE, b);
+        }
+        ++issued;
+      }
+      // wait for the copies in flight before the CTA may exit
+      for (int t = imax(0, issued - L::STAGES); t < issued; ++t)
+        mbar_wait(&full[t % L::STAGES], (t / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+    }
+    __syncthreads();  // pairs with the compute warps' barrier before the merge
+    __syncthreads();
+    return;
+  }
+
+  // -------------------------------------------------------------- compute warps
+  const int gq = lane >> 2, tq = lane & 3;  // fragment row group / column pair
+  // Q as m16n8k16 A fragments (rows r = qpos * g + head-in-group, zero above `rows`).
+  uint32_t qa[D / 16][4];
+  {
+    const int ra = gq, rb = gq + 8;
+    const __nv_bfloat16* qpa = nullptr;
+    const __nv_bfloat16* qpb = nullptr;
+    if (ra < rows) qpa = p.q + b * p.q_sb + (ra / g) * p.q_sn + (kvh * g + ra % g) * p.q_sh;
+    if (rb < rows) qpb = p.q + b * p.q_sb + (rb / g) * p.q_sn + (kvh * g + rb % g) * p.q_sh;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int c0 = ks * 16 + 2 * tq;
+      qa[ks][0] = qpa ? *reinterpret_cast<const uint32_t*>(qpa + c0) : 0u;
+      qa[ks][1] = qpb ? *reinterpret_cast<const uint32_t*>(qpb + c0) : 0u;
+      qa[ks][2] = qpa ? *reinterpret_cast<const uint32_t*>(qpa + c0 + 8) : 0u;
+      qa[ks][3] = qpb ? *reinterpret_cast<const uint32_t*>(qpb + c0 + 8) : 0u;
+    }
+  }
+  const float c = p.scale_log2;
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  float o[D / 8][4];
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+  const int mat = lane >> 3, mrow = lane & 7;  // ldmatrix: which 8x8 matrix this lane addresses
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t % L::STAGES;
+    ok = mbar_wait(&full[st], (t / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+    if (!__all_sync(0xffffffffu, ok)) {
+      ok = false;
+      break;
+    }
+    const uint32_t kb = smem_u32(smem + L::OFF_KV + st * 2 * L::TB);
+    const uint32_t vb = kb + L::TB;
+    const int key_base = 16 * warp;  // this warp's 16 keys within the tile
+
+    // S = Q K^T for 16 rows x 16 keys (two n8 tiles)
+    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      // matrices: (keys 0-7, ch lo), (keys 0-7, ch hi), (keys 8-15, ch lo), (keys 8-15, ch hi)
+      const int key = key_base + 8 * (mat >> 1) + mrow;
+      const int ch = ks * 16 + 8 * (mat & 1);
+      uint32_t b00, b01, b10, b11;
+      ldsm_x4(kb + swz(key, ch), b00, b01, b10, b11);
+      mma_16816(sacc[0], qa[ks], b00, b01);
+      mma_16816(sacc[1], qa[ks], b10, b11);
+    }
+    // mask keys outside [k0, k1)
+    const int key0 = k0 + t * TILE + key_base;
+    float sv[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int key = key0 + 8 * nt + 2 * tq + (i & 1);
+        sv[nt][i] = key < k1 ? sacc[nt][i] : -INFINITY;
+      }
+    // online softmax for rows gq (i = 0,1) and gq+8 (i = 2,3)
+    uint32_t pa[4];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      float mx = fmaxf(fmaxf(sv[0][2 * hr], sv[0][2 * hr + 1]), fmaxf(sv[1][2 * hr], sv[1][2 * hr + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_tile = mx * c;
+      const float m_new = fmaxf(m_run[hr], m_tile);
+      const float alpha = (m_new == m_run[hr]) ? 1.f : ex2(m_run[hr] - m_new);
+      const float mu = (m_new == -INFINITY) ? 0.f : m_new;
+      const float p00 = ex2(fmaf(sv[0][2 * hr], c, -mu)), p01 = ex2(fmaf(sv[0][2 * hr + 1], c, -mu));
+      const float p10 = ex2(fmaf(sv[1][2 * hr], c, -mu)), p11 = ex2(fmaf(sv[1][2 * hr + 1], c, -mu));
+      l_run[hr] = l_run[hr] * alpha + (p00 + p01 + p10 + p11);
+      m_run[hr] = m_new;
+      pa[hr] = pack_bf16(p00, p01);      // a0 (row gq) / a1 (row gq+8): keys 2tq, 2tq+1
+      pa[2 + hr] = pack_bf16(p10, p11);  // a2 / a3: keys 8+2tq, 9+2tq
+      if (alpha != 1.f) {
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+          o[nt][2 * hr] *= alpha;
+          o[nt][2 * hr + 1] *= alpha;
+        }
+      }
+    }
+    // O += P V: B fragments of V (16 keys x 8 channels) via transposed ldmatrix
+#pragma unroll
+    for (int np = 0; np < D / 16; ++np) {
+      // matrices: (keys 0-7, ch n0..), (keys 8-15, ch n0..), (keys 0-7, ch n0+8..), (keys 8-15, ch n0+8..)
+      const int key = key_base + 8 * (mat & 1) + mrow;
+      const int ch = np * 16 + 8 * (mat >> 1);
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_t(vb + swz(key, ch), v0, v1, v2, v3);
+      mma_16816(o[2 * np], pa, v0, v1);
+      mma_16816(o[2 * np + 1], pa, v2, v3);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+
+  // ---------------------------------------------------------- merge the 8 warps
+  // row sums are spread over the 4 lanes of a quad
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
+    l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
+  }
+  // all compute warps and the producer must be past the pipeline before the
+  // stage memory is reused
+  __syncthreads();
+  float* sm = reinterpret_cast<float*>(smem);
+  float* sm_m = sm;                       // [WARPS][16]
+  float* sm_l = sm + WARPS * 16;          // [WARPS][16]
+  float* sm_o = sm + 2 * WARPS * 16;      // [WARPS][16][D]
+  if (tq == 0) {
+    sm_m[warp * 16 + gq] = m_run[0];
+    sm_m[warp * 16 + gq + 8] = m_run[1];
+    sm_l[warp * 16 + gq] = l_run[0];
+    sm_l[warp * 16 + gq + 8] = l_run[1];
+  }
+#pragma unroll
+  for (int nt = 0; nt < D / 8; ++nt) {
+    const int ch = nt * 8 + 2 * tq;
+    sm_o[(warp * 16 + gq) * D + ch] = o[nt][0];
+    sm_o[(warp * 16 + gq) * D + ch + 1] = o[nt][1];
+    sm_o[(warp * 16 + gq + 8) * D + ch] = o[nt][2];
+    sm_o[(warp * 16 + gq + 8) * D + ch + 1] = o[nt][3];
+  }
+  __syncthreads();
+  if (!ok) return;
+  // 256 threads: thread -> (row, channel range)
+  const int tid = threadIdx.x;  // < 256
+  constexpr int PER = 16 * D / 256;  // channels per thread
+  const int row = tid / (D / PER);
+  const int chb = (tid % (D / PER)) * PER;
+  if (row < rows) {
+    float mstar = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) mstar = fmaxf(mstar, sm_m[w * 16 + row]);
+    const float mref = mstar == -INFINITY ? 0.f : mstar;
+    float wsum = 0.f, wt[WARPS];
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+      const float mw = sm_m[w * 16 + row];
+      wt[w] = mw == -INFINITY ? 0.f : ex2(mw - mref);
+      wsum += wt[w] * sm_l[w * 16 + row];
+    }
+    const float inv = 1.f / wsum;
+    const int qpos = row / g, hq = kvh * g + row % g;
+    const int64_t prow = ((static_cast<int64_t>(b) * s.Hq + hq) * s.Nq + qpos) * p.num_splits + split;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < WARPS; ++w) acc += wt[w] * sm_o[(w * 16 + row) * D + chb + i];
+      p.o_part[prow * D + chb + i] = acc * inv;
+    }
+    if (chb == 0) p.lse_part[prow] = (mref + __log2f(wsum)) * LN2;
+  }
+}
+
+// One warp per output row: LSE = ln sum_s e^{LSE_s}; O = sum_s e^{LSE_s - LSE} O_s.
+template <int D>
+__global__ void __launch_bounds__(128) fa_decode_combine_kernel(const float* __restrict__ lse_part,
+                                                                const float* __restrict__ o_part, OutRows o,
+                                                                float* __restrict__ lse, int rows_total, int Hq,
+                                                                int Nq, int S) {
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows_total) return;
+  const float* lp = lse_part + static_cast<int64_t>(row) * S;
+  float mx = -INFINITY;
+  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lp[s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  float den = 0.f;
+  for (int s = lane; s < S; s += 32) den += __expf(lp[s] - mx);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  const float lse_row = mx + __logf(den);
+  constexpr int PER = D / 32;
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  const float* op = o_part + static_cast<int64_t>(row) * S * D;
+  for (int s = 0; s < S; ++s) {
+    const float w = __expf(lp[s] - lse_row);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] += w * op[s * D + lane * PER + i];
+  }
+  // row = (b * Hq + h) * Nq + qpos
+  const int qpos = row % Nq, bh = row / Nq, h = bh % Hq, b = bh / Hq;
+  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(o.ptr) + b * o.sb + static_cast<int64_t>(qpos) * o.sn +
+                       h * o.sh + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER; i += 2) *reinterpret_cast<uint32_t*>(dst + i) = pack_bf16(acc[i], acc[i + 1]);
+  if (lane == 0) lse[row] = lse_row;
+}
+
+template <int D>
+cudaError_t launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
+  using L = DecLayout<D>;
+  auto kern = fa_decode_split_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  if (e != cudaSuccess) return e;
+  DecParams p;
+  p.dims = a.dims;
+  p.d = a.d;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.q_sb = a.q_sb;
+  p.q_sn = a.q_sn;
+  p.q_sh = a.q_sh;
+  p.lse_part = a.lse_part;
+  p.o_part = a.o_part;
+  p.num_splits = a.num_splits;
+  p.chunk = a.chunk;
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  dim3 grid(a.num_splits, a.dims.Hkv, a.dims.B);
+  kern<<<grid, THREADS, L::ALLOC, st>>>(a.tm_k, a.tm_v, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int rows_total = a.dims.B * a.dims.Hq * a.dims.Nq;
+  fa_decode_combine_kernel<D><<<cdiv(rows_total, 4), 128, 0, st>>>(a.lse_part, a.o_part, a.o, a.lse, rows_total,
+                                                                   a.dims.Hq, a.dims.Nq, a.num_splits);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t st) {
+  return a.d == 64 ? launch_decode_t<64>(a, st) : launch_decode_t<128>(a, st);
+}
+
+}  // namespace fa

@@ -1,0 +1,451 @@
+// Forward kernel: exact attention, tile by tile with an online softmax.
+//
+// Method ("第18章 FlashAttention" §18.4.1-§18.4.3; "CMU 11-868 L21" notes,
+// slides 9-12 and the Algorithm-1 remark): each query tile keeps a running row
+// max m and row sum l; every key tile's scores S = Q K^T are exponentiated
+// against the running max, the partial output is rescaled when the max moves,
+// and at the end O / l and LSE = m + ln l are written.  S and P never leave the
+// chip.  Causal work skips key tiles above the diagonal and masks the diagonal
+// tile element by element (§18.5.2).
+//
+// GB300 design (one persistent CTA per SM, 12 warps):
+//   warp 0      TMA producer: claims work units (an atomic counter, longest
+//               first), loads the two Q tiles of the unit and streams K_j, V_j
+//               through a ring of shared-memory stages.
+//   warp 1      MMA issuer (one thread) and TMEM owner: S_t = Q_t K_j^T and
+//               O_t += P_t V_j with tcgen05.mma, accumulators in TMEM.
+//   warps 4-7   softmax for query tile 0 of the unit (thread = row = TMEM lane)
+//   warps 8-11  softmax for query tile 1
+// The two query tiles share every K/V stage and ping-pong on the tensor core:
+// while one warpgroup exponentiates S_0, the tensor core computes S_1 or P_0 V.
+// TMEM (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,256+d) O_1 [256+d,256+2d);
+// P_t is written as bf16 over the first 64 columns of S_t and read from TMEM by
+// the P V product.
+// Rescaling is skipped while the running max has grown by at most TAU (log2
+// units): the stale max stays the reference for both O and l, so the result is
+// unchanged (lecture slides 51-52 describe skipping most rescalings).
+#include <math.h>
+
+#include "fa_kernels.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float TAU = 8.0f;
+constexpr float LN2 = 0.69314718055994530942f;
+
+template <int D>
+struct FwdLayout {
+  static constexpr int QB = TILE * D * 2;    // one Q tile (bytes)
+  static constexpr int TB = TILE * D * 2;    // one K or V tile
+  static constexpr int STAGES = D == 64 ? 6 : 4;
+  static constexpr int CH = D / 64;          // 64-column swizzle atoms per tile row
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = 2 * QB;
+  static constexpr int OFF_BAR = OFF_KV + STAGES * TB;
+  // barriers: unit_full[2] unit_empty[2] q_full q_empty kv_full[S] kv_empty[S]
+  //           s_full[2] p_full[2] o_full[2] o_empty[2]
+  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 8;
+  static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_TMEM = OFF_UNIT + 16;
+  static constexpr int BYTES = OFF_TMEM + 16;
+  static constexpr int ALLOC = BYTES + 1024;
+};
+
+struct FwdParams {
+  Dims dims;
+  float scale_log2;
+  OutRows o;
+  float* lse;
+  int* status;
+  int* counter;
+  unsigned long long timeout_ns;
+  int total_units;
+};
+
+struct Bars {
+  uint64_t *unit_full, *unit_empty, *q_full, *q_empty, *kv_full, *kv_empty, *s_full, *p_full, *o_full, *o_empty;
+};
+
+template <int D>
+__device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
+  using L = FwdLayout<D>;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  Bars r;
+  r.unit_full = b;
+  r.unit_empty = b + 2;
+  r.q_full = b + 4;
+  r.q_empty = b + 5;
+  r.kv_full = b + 6;
+  r.kv_empty = r.kv_full + L::STAGES;
+  r.s_full = r.kv_empty + L::STAGES;
+  r.p_full = r.s_full + 2;
+  r.o_full = r.p_full + 2;
+  r.o_empty = r.o_full + 2;
+  return r;
+}
+
+__device__ __forceinline__ void unit_tiles(const Dims& s, int p, int (&n)[2]) {
+  const int nq = q_tiles(s);
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = 2 * p + t;
+    n[t] = qt < nq ? kv_tiles_for_q(s, qt) : 0;
+  }
+}
+
+// ------------------------------------------------------------------ producer
+template <int D>
+__device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, const CUtensorMap* tm_q,
+                             const CUtensorMap* tm_k, const CUtensorMap* tm_v, const FwdParams& p,
+                             const Ctl& ctl) {
+  using L = FwdLayout<D>;
+  const int g = p.dims.Hq / p.dims.Hkv;
+  uint32_t seq = 0;       // K/V tiles issued so far (ring sequence number)
+  int q_armed = -1;       // last unit index whose Q load was issued
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!mbar_wait(&bar.unit_empty[slot], ((it >> 1) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
+    const int u = atomicAdd(p.counter, 1);
+    unit_slot[slot] = u;
+    mbar_arrive(&bar.unit_full[slot]);
+    if (u >= p.total_units) break;
+    int b, h, pr, n[2];
+    fwd_unit(p.dims, u, b, h, pr);
+    unit_tiles(p.dims, pr, n);
+    const int nmax = imax(n[0], n[1]);
+    const int kvh = h / g;
+
+    if (!mbar_wait(bar.q_empty, (it & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
+    mbar_arrive_expect_tx(bar.q_full, 2 * L::QB);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int c = 0; c < L::CH; ++c)
+        tma_load_4d(smem + L::OFF_Q + t * L::QB + c * (TILE * 128), tm_q, bar.q_full, c * 64, h,
+                    (2 * pr + t) * TILE, b);
+    q_armed = it;
+
+    bool ok = true;
+    for (int j = 0; j < nmax && ok; ++j) {
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const int s = seq % L::STAGES;
+        const uint32_t ph = (seq / L::STAGES) & 1;
+        if (!mbar_wait(&bar.kv_empty[s], ph ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&bar.kv_full[s], L::TB);
+#pragma unroll
+        for (int c = 0; c < L::CH; ++c)
+          tma_load_4d(smem + L::OFF_KV + s * L::TB + c * (TILE * 128), kv ? tm_v : tm_k, &bar.kv_full[s], c * 64,
+                      kvh, j * TILE, b);
+        ++seq;
+      }
+    }
+    if (!ok) break;
+  }
+  // Let every copy still in flight land before the CTA can exit.
+  for (int s = 0; s < L::STAGES; ++s) {
+    if (seq > static_cast<uint32_t>(s)) {
+      const uint32_t last = seq - 1 - ((seq - 1 - s) % L::STAGES);  // last sequence number on stage s
+      mbar_wait(&bar.kv_full[s], (last / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+    }
+  }
+  if (q_armed >= 0) mbar_wait(bar.q_full, q_armed & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <int D>
+__device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
+                        const Ctl& ctl) {
+  using L = FwdLayout<D>;
+  constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);  // Q K^T, both K-major
+  constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);     // P V, V is N-major
+  const uint32_t q_base = smem_u32(smem + L::OFF_Q);
+  const uint32_t kv_base = smem_u32(smem + L::OFF_KV);
+  uint32_t seq = 0;
+  uint32_t pph[2] = {0, 0};
+  uint32_t active[2] = {0, 0};
+
+  auto issue_s = [&](int t, int stage) {
+    const uint32_t d_tmem = tmem + t * 128;
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+      const uint32_t off = (k / 4) * (TILE * 128) + (k % 4) * 32;
+      const uint64_t a = sdesc_sw128(q_base + t * L::QB + off, 16, 1024);
+      const uint64_t bd = sdesc_sw128(kv_base + stage * L::TB + off, 16, 1024);
+      mma_ss(d_tmem, a, bd, IDESC_S, k > 0);
+    }
+  };
+  auto issue_pv = [&](int t, int stage, bool acc) {
+    const uint32_t d_tmem = tmem + 256 + t * D;
+    const uint32_t p_tmem = tmem + t * 128;
+#pragma unroll
+    for (int k = 0; k < TILE / 16; ++k) {
+      const uint64_t bd = sdesc_sw128(kv_base + stage * L::TB + k * 16 * 128, TILE * 128, 1024);
+      mma_ts(d_tmem, p_tmem + k * 8, bd, IDESC_O, (acc || k > 0) ? 1u : 0u);
+    }
+  };
+
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) return;
+    const int u = unit_slot[slot];
+    mbar_arrive(&bar.unit_empty[slot]);
+    if (u >= p.total_units) return;
+    int b, h, pr, n[2];
+    fwd_unit(p.dims, u, b, h, pr);
+    unit_tiles(p.dims, pr, n);
+    const int nmax = imax(n[0], n[1]);
+
+    if (!mbar_wait(bar.q_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+    // K_0
+    {
+      const int s = seq % L::STAGES;
+      if (!mbar_wait(&bar.kv_full[s], (seq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+      tc_fence_after();
+      for (int t = 0; t < 2; ++t)
+        if (n[t] > 0) {
+          issue_s(t, s);
+          mma_commit(&bar.s_full[t]);
+        }
+      if (nmax == 1) mma_commit(bar.q_empty);
+      mma_commit(&bar.kv_empty[s]);
+    }
+    for (int j = 0; j < nmax; ++j) {
+      const uint32_t vseq = seq + 2 * j + 1, kseq = seq + 2 * j + 2;
+      const int vs = vseq % L::STAGES, ks = kseq % L::STAGES;
+      const bool need_k = j + 1 < nmax;
+      if (!mbar_wait(&bar.kv_full[vs], (vseq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+      if (need_k && !mbar_wait(&bar.kv_full[ks], (kseq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+      for (int t = 0; t < 2; ++t) {
+        if (j >= n[t]) continue;
+        if (j == 0 && !mbar_wait(&bar.o_empty[t], (active[t] & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+        if (!mbar_wait(&bar.p_full[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
+        pph[t] ^= 1;
+        tc_fence_after();
+        issue_pv(t, vs, j > 0);
+        if (j == n[t] - 1) mma_commit(&bar.o_full[t]);
+        if (j + 1 < n[t]) {
+          issue_s(t, ks);
+          mma_commit(&bar.s_full[t]);
+        }
+      }
+      mma_commit(&bar.kv_empty[vs]);
+      if (need_k) {
+        if (j + 1 == nmax - 1) mma_commit(bar.q_empty);
+        mma_commit(&bar.kv_empty[ks]);
+      }
+    }
+    for (int t = 0; t < 2; ++t)
+      if (n[t] > 0) ++active[t];
+    seq += 2 * nmax;
+  }
+}
+
+// ------------------------------------------------------------------ softmax
+template <int D, bool CAUSAL>
+__device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
+                            const Ctl& ctl) {
+  const int wq = (threadIdx.x >> 5) & 3;  // warp within the warpgroup = TMEM lane quarter
+  const int r = wq * 32 + lane_id();      // row of the query tile
+  const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tmem + lanes + t * 128;
+  const uint32_t tO = tmem + lanes + 256 + t * D;
+  const float c = p.scale_log2;
+  const Dims& s = p.dims;
+  uint32_t sph = 0, active = 0;
+
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    bool ok = mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const int u = unit_slot[slot];
+    mbar_arrive(&bar.unit_empty[slot]);
+    if (u >= p.total_units) return;
+    int b, h, pr, n2[2];
+    fwd_unit(s, u, b, h, pr);
+    unit_tiles(s, pr, n2);
+    const int n = n2[t];
+    if (n == 0) continue;
+    const int qt = 2 * pr + t;
+    const int q_row = qt * TILE + r;
+
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < n; ++j) {
+      ok = mbar_wait(&bar.s_full[t], sph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+      sph ^= 1;
+      if (!__all_sync(0xffffffffu, ok)) return;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld128(tS, sr);
+
+      float sv[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i]);
+      if (j == n - 1 && (CAUSAL || (s.Nk % TILE) != 0)) {
+        int lim = s.Nk - j * TILE;
+        if (CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= lim) sv[i] = -INFINITY;
+      }
+      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+#pragma unroll
+      for (int i = 4; i < 128; i += 4) {
+        mx0 = fmaxf(mx0, sv[i]);
+        mx1 = fmaxf(mx1, sv[i + 1]);
+        mx2 = fmaxf(mx2, sv[i + 2]);
+        mx3 = fmaxf(mx3, sv[i + 3]);
+      }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float m_new = (m_tile > m_run + TAU) ? m_tile : m_run;
+      const float alpha = ex2(m_run - m_new);
+      const float neg_m = -m_new;
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float p0 = ex2(fmaf(sv[2 * i], c, neg_m));
+        const float p1 = ex2(fmaf(sv[2 * i + 1], c, neg_m));
+        sum0 += p0;
+        sum1 += p1;
+        pk[i] = pack_bf16(p0, p1);
+      }
+      l_run = l_run * alpha + (sum0 + sum1);
+      tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc * 32, o);
+
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + cc * 32, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar.p_full[t]);
+      m_run = m_new;
+    }
+
+    // epilogue: O / l -> bf16, LSE
+    ok = mbar_wait(&bar.o_full[t], active & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+    ++active;
+    if (!__all_sync(0xffffffffu, ok)) return;
+    tc_fence_after();
+    const float inv_l = 1.f / l_run;
+    const bool live = q_row < s.Nq;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o.ptr) + b * p.o.sb +
+                          static_cast<int64_t>(q_row) * p.o.sn + h * p.o.sh;
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+      uint32_t o[32];
+      tmem_ld32(tO + cc * 32, o);
+
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      }
+    }
+    if (live) p.lse[(static_cast<int64_t>(b) * s.Hq + h) * s.Nq + q_row] = (m_run + __log2f(l_run)) * LN2;
+    tc_fence_before();
+    mbar_arrive(&bar.o_empty[t]);
+  }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using L = FwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const Bars bar = carve_bars<D>(smem);
+  int* unit_slot = reinterpret_cast<int*>(smem + L::OFF_UNIT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
+  const int warp = threadIdx.x >> 5;
+  const Ctl ctl{p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar.unit_full[0], 1);
+    mbar_init(&bar.unit_full[1], 1);
+    mbar_init(&bar.unit_empty[0], 1 + 256);
+    mbar_init(&bar.unit_empty[1], 1 + 256);
+    mbar_init(bar.q_full, 1);
+    mbar_init(bar.q_empty, 1);
+    for (int s = 0; s < L::STAGES; ++s) {
+      mbar_init(&bar.kv_full[s], 1);
+      mbar_init(&bar.kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar.s_full[t], 1);
+      mbar_init(&bar.p_full[t], 128);
+      mbar_init(&bar.o_full[t], 1);
+      mbar_init(&bar.o_empty[t], 128);
+    }
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane_id() == 0) fwd_producer<D>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
+  } else if (warp == 1) {
+    if (lane_id() == 0) fwd_mma<D>(smem, bar, unit_slot, tmem, p, ctl);
+  } else if (warp >= 4) {
+    fwd_softmax<D, CAUSAL>((warp - 4) >> 2, bar, unit_slot, tmem, p, ctl);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
+  using L = FwdLayout<D>;
+  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  if (e != cudaSuccess) return e;
+  FwdParams p;
+  p.dims = a.dims;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.status = a.status;
+  p.counter = a.counter;
+  p.timeout_ns = a.timeout_ns;
+  p.total_units = fwd_units(a.dims);
+  const int grid = imax(1, imin(p.total_units, a.num_sms));
+  kern<<<grid, 384, L::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
+  if (a.d == 64) return a.dims.causal ? launch_fwd_t<64, true>(a, st) : launch_fwd_t<64, false>(a, st);
+  return a.dims.causal ? launch_fwd_t<128, true>(a, st) : launch_fwd_t<128, false>(a, st);
+}
+
+}  // namespace fa

@@ -1,0 +1,69 @@
+// Launch interfaces between the C-ABI layer (fa_api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fa_plan.h"
+
+namespace fa {
+
+struct OutRows {           // a bf16 [B, N, H, d] tensor written row by row
+  void* ptr;
+  int64_t sb, sn, sh;
+};
+
+struct FwdLaunch {
+  Dims dims;
+  int d;
+  float scale;
+  CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps, box 64 x 1 x 128 x 1, 128B swizzle
+  OutRows o;
+  float* lse;
+  int* status;
+  int* counter;
+  unsigned long long timeout_ns;
+  int num_sms;
+};
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
+
+struct BwdLaunch {
+  Dims dims;
+  int d;
+  float scale;
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  OutRows o, dout, dq, dk, dv;
+  const float* lse;
+  float* lse2;     // workspace [B*Hq, Nq_pad] : LSE * log2(e)  (+inf in padding)
+  float* delta;    // workspace [B*Hq, Nq_pad] : D = rowsum(dO o O)
+  int nq_pad;
+  int* status;
+  int* counters;   // [2]
+  unsigned long long timeout_ns;
+  int num_sms;
+};
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st);
+
+struct DecodeLaunch {
+  Dims dims;       // causal = 0
+  int d;
+  float scale;
+  CUtensorMap tm_k, tm_v;
+  const void* q;
+  int64_t q_sb, q_sn, q_sh;
+  OutRows o;
+  float* lse;
+  float* lse_part;  // [B, Hq, Nq, S]
+  float* o_part;    // [B, Hq, Nq, S, d]
+  int num_splits;
+  int chunk;        // keys per split (multiple of 128)
+  int* status;
+  unsigned long long timeout_ns;
+};
+cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t st);
+
+cudaError_t launch_selftest_mma(int mode, int n_or_k, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                const void* a_rows, float* c, int* status, cudaStream_t st);
+
+}  // namespace fa

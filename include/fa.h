@@ -1,0 +1,192 @@
+/*
+ * fa.h -- C ABI of libfa_gb300.so: exact IO-aware attention (FlashAttention)
+ * for one GB300 GPU (sm_103a).
+ *
+ * The method: scaled-dot-product attention computed tile by tile with an online
+ * softmax, so the Nq x Nk score matrix never reaches HBM ("第18章 FlashAttention",
+ * §18.4.1-§18.4.3; "CMU 11-868 L21 FlashAttention" notes, slides 9-12); a
+ * backward pass that rebuilds P on chip from the saved log-sum-exp instead of
+ * storing it (§18.4.4; lecture slide 14); and split-KV decoding
+ * (FlashDecoding) with a log-sum-exp weighted combine (§18.8.2; slides 57-60).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are bf16, layout [B, N, H, d] (batch, sequence, head, head dim) as
+ *    in the flash_attn_func interface of §18.7.1.  Each is passed as an
+ *    fa_tensor_t: a device pointer plus the batch / sequence / head strides in
+ *    ELEMENTS; the head-dim stride is 1.  Pointers must be 16-byte aligned and
+ *    the three strides multiples of 8 elements (16 bytes): the kernels move
+ *    tiles with the Tensor Memory Accelerator, which requires both.
+ *  - LSE is fp32, contiguous [B, Hq, Nq], natural log, in units of the scaled
+ *    scores: LSE_i = ln sum_j exp(scale * q_i . k_j).
+ *  - Grouped-query attention: Hq must be a multiple of Hkv; query head h reads
+ *    K/V head h / (Hq / Hkv) (§18.2.2; consecutive grouping).
+ *  - d is 64 or 128.  scale must be finite and > 0 (callers usually pass
+ *    1/sqrt(d), §18.2.1).
+ *  - causal != 0 masks key j for query i when j > i (§18.2.2, top-left
+ *    aligned) and requires Nq == Nk.
+ *  - Ownership: the caller allocates and owns every device buffer, including
+ *    the workspace (size from the matching *_workspace_size call).  The library
+ *    never allocates, frees or synchronises in the compute calls; work is
+ *    enqueued on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *    the call returns before it finishes.
+ *  - Errors: the return value is FA_OK or an FA_ERR_* code; fa_strerror()
+ *    describes it.  Argument errors are detected before anything is enqueued.
+ *    Errors found on the GPU (a bounded wait that ran out) are recorded in the
+ *    workspace and returned by fa_get_device_status().  Each compute call
+ *    first clears the workspace's 256-byte header (status word and work
+ *    counters) on its stream, so the status belongs to the latest call, and
+ *    calls that share one workspace must not run concurrently.
+ *  - Every device buffer must live on the current CUDA device, which must be
+ *    an sm_103 part (FA_ERR_ARCH otherwise).
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  FA_OK = 0,
+  FA_ERR_INVALID = 1,   /* null pointer, bad size, Hq % Hkv != 0, d not 64/128, causal with Nq != Nk */
+  FA_ERR_ALIGN = 2,     /* pointer not 16-byte aligned or stride not a multiple of 8 elements */
+  FA_ERR_WORKSPACE = 3, /* workspace missing or smaller than the *_workspace_size answer */
+  FA_ERR_ARCH = 4,      /* current device is not sm_103 */
+  FA_ERR_LAUNCH = 5,    /* a kernel launch failed (the CUDA error is in fa_last_cuda_error) */
+  FA_ERR_TIMEOUT = 6,   /* a device-side bounded wait ran out (see fa_get_device_status) */
+  FA_ERR_CUDA = 7       /* another CUDA runtime/driver call failed */
+};
+
+typedef struct {
+  void* ptr;          /* device pointer to the element [0, 0, 0, 0] (bf16) */
+  int64_t stride_b;   /* elements between consecutive batch entries */
+  int64_t stride_n;   /* elements between consecutive sequence positions */
+  int64_t stride_h;   /* elements between consecutive heads; head-dim stride is 1 */
+} fa_tensor_t;
+
+typedef struct {
+  int B;        /* batch */
+  int Hq;       /* query heads */
+  int Hkv;      /* key/value heads; Hq % Hkv == 0 */
+  int Nq;       /* query length */
+  int Nk;       /* key/value length */
+  int d;        /* head dim: 64 or 128 */
+  float scale;  /* softmax scale applied to q.k (e.g. 1/sqrt(d)) */
+  int causal;   /* 0 or 1 */
+} fa_shape_t;
+
+/* ---------------------------------------------------------------------------
+ * Forward.  "第18章" §18.4.1 (tiling: Q tiles outer, K/V tiles inner, running
+ * max m and sum l), §18.4.2 (online update), §18.4.3 (kernel: O rescaled, final
+ * O / l, m and l saved); Fig. 18-6 (the saved statistic is the log-sum-exp);
+ * §18.5.2 (causal: key tiles above the diagonal skipped, the diagonal tile
+ * masked element by element); lecture slides 26-46 (persistent kernel,
+ * longest-first order of causal work).
+ *   q   [B, Nq, Hq, d]  in
+ *   k,v [B, Nk, Hkv, d] in
+ *   o   [B, Nq, Hq, d]  out (bf16, round to nearest even)
+ *   lse [B, Hq, Nq]     out (fp32, contiguous)
+ * Needs fa_fwd_workspace_size(shape) bytes of workspace (16-byte aligned).
+ * ------------------------------------------------------------------------- */
+size_t fa_fwd_workspace_size(const fa_shape_t* shape);
+int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
+           const fa_shape_t* shape, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Backward.  §18.4.4: P rebuilt per tile from the saved statistics with no
+ * rescaling, dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = scale dS K,
+ * dK = scale dS^T Q; Fig. 18-17 (dependency chain).  D_i is the full-row
+ * rowsum(P o dP), which equals dO_i . O_i and is computed once before the
+ * tile loops (the per-block D of the printed pseudocode is not used).  dK/dV
+ * of a shared K/V head sum the contributions of its query heads.  Three
+ * kernels, no atomics: preprocess (D), dK/dV (one key tile per work unit),
+ * dQ (one query tile per work unit); results are deterministic.
+ *   q, o, dout [B, Nq, Hq, d] in;  k, v [B, Nk, Hkv, d] in;  lse in (from fa_fwd)
+ *   dq [B, Nq, Hq, d] out;  dk, dv [B, Nk, Hkv, d] out  (bf16)
+ * ------------------------------------------------------------------------- */
+size_t fa_bwd_workspace_size(const fa_shape_t* shape);
+int fa_bwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o,
+           const float* lse, const fa_tensor_t* dout, const fa_tensor_t* dq, const fa_tensor_t* dk,
+           const fa_tensor_t* dv, const fa_shape_t* shape, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Split-KV decode (FlashDecoding).  §18.8.2: the KV cache is cut along its
+ * length into chunks processed in parallel, each producing (m_t, l_t, O_t),
+ * merged by O = sum_t O_t e^{m_t-m} / sum_t l_t e^{m_t-m}; lecture slides
+ * 57-60: the query heads sharing a K/V head (and the query positions) are
+ * packed into one matrix tile.  Non-causal: every query row sees all Nk keys.
+ *   q      [B, Nq, Hq, d]   in  (Nq small: Hq/Hkv * Nq <= 16)
+ *   kcache [B, Nk, Hkv, d]  in;  vcache likewise
+ *   o      [B, Nq, Hq, d]   out (bf16);  lse [B, Hq, Nq] out (fp32)
+ * num_splits: requested number of KV splits, 0 = choose from the GPU's SM
+ * count.  Splits are whole 128-key tiles: chunk = ceil(ceil(Nk/128)/S)*128
+ * keys, split s = [s*chunk, min((s+1)*chunk, Nk)); the number used is
+ * fa_decode_num_splits().  shape->causal must be 0.
+ * ------------------------------------------------------------------------- */
+int fa_decode_num_splits(const fa_shape_t* shape, int num_splits);
+size_t fa_decode_workspace_size(const fa_shape_t* shape, int num_splits);
+int fa_decode(const fa_tensor_t* q, const fa_tensor_t* kcache, const fa_tensor_t* vcache, const fa_tensor_t* o,
+              float* lse, const fa_shape_t* shape, int num_splits, void* workspace, size_t workspace_bytes,
+              void* stream);
+/* Where fa_decode leaves the per-split partials inside its workspace (for
+ * tests): lse_part [B, Hq, Nq, S] fp32 (natural log) and o_part
+ * [B, Hq, Nq, S, d] fp32 (normalised by the split's own sum).  Byte offsets. */
+int fa_decode_partials_layout(const fa_shape_t* shape, int num_splits, size_t* lse_offset, size_t* o_offset);
+
+/* ---------------------------------------------------------------------------
+ * Device status.  Synchronises `stream`, returns the error bits the kernels
+ * recorded in `workspace` (0 = none) through *status, and clears them.
+ * Returns FA_ERR_TIMEOUT when a bounded wait ran out, FA_OK otherwise.
+ * ------------------------------------------------------------------------- */
+int fa_get_device_status(void* workspace, void* stream, int* status);
+
+/* Time budget of every device-side wait, in nanoseconds (default 10 s).  A
+ * wait that runs out records an error and the kernel returns early.  */
+void fa_set_wait_timeout_ns(unsigned long long ns);
+
+const char* fa_strerror(int code);
+/* The last CUDA runtime error code seen by the library (cudaError_t value). */
+int fa_last_cuda_error(void);
+
+/* ---------------------------------------------------------------------------
+ * Host-side plans (integer, no GPU needed): exactly what the kernels use.
+ * ------------------------------------------------------------------------- */
+/* Causal class of query tile qt x key tile kt (128 x 128): 0 = skipped
+ * (fully masked), 1 = fully visible, 2 = partial (masked element by element);
+ * §18.5.2, Fig. 18-20.  Non-causal shapes answer 1.  -1 on bad arguments. */
+int fa_tile_class(const fa_shape_t* shape, int q_tile, int kv_tile);
+/* Work units in the order the kernels hand them out (longest first for causal
+ * shapes; lecture slides 27-46).  Forward unit = (b, h, pair p: query tiles 2p
+ * and 2p+1).  dK/dV unit = (b, kv head, key tile).  dQ unit = (b, h, query
+ * tile).  *_num_units gives the count; *_unit writes the index-th unit. */
+int fa_fwd_num_units(const fa_shape_t* shape);
+int fa_fwd_unit(const fa_shape_t* shape, int index, int* b, int* h, int* p);
+int fa_dkdv_num_units(const fa_shape_t* shape);
+int fa_dkdv_unit(const fa_shape_t* shape, int index, int* b, int* kvh, int* kv_tile);
+int fa_dq_num_units(const fa_shape_t* shape);
+int fa_dq_unit(const fa_shape_t* shape, int index, int* b, int* h, int* q_tile);
+/* Key range [start, end) of decode split s. */
+int fa_decode_split_range(const fa_shape_t* shape, int num_splits, int s, int* start, int* end);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics: one 128-row tcgen05 matrix product through the same TMA,
+ * descriptor and TMEM code the attention kernels use (no counterpart on the
+ * pages; it isolates the tensor-core building blocks).
+ *   mode 0: c[128 x 128] = a[128 x k] * b[128 x k]^T   (both K-major, k = 64|128)
+ *   mode 1: c[128 x n]   = a[128 x 128] * b[128 x n]   (a staged in TMEM,
+ *                                                       b row-major, n = 64|128)
+ * a, b: device bf16, row-major; c: device fp32 row-major.
+ * workspace: at least 256 bytes of device memory (its first word records a
+ * timed-out wait, as for the attention calls).
+ */
+int fa_selftest_mma(int mode, int n_or_k, const void* a, const void* b, float* c, void* workspace, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,155 @@
+"""The C-ABI library loads, exports every declared symbol, and its host plans
+equal the oracle's plans exactly (no GPU needed: no compute call is made)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_io_aware_21_gb300 as fa
+from exact_io_aware_21_gb300.binding import SIGNATURES, FaShape, FaTensor, shape
+from oracle import plan as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fa.library_path()):
+        from exact_io_aware_21_gb300 import build
+
+        build.build()
+    return fa.library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_]+\s*\*?\s*(fa_[a-z0-9_]+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(SIGNATURES), "binding signatures must mirror the header"
+
+
+def test_strerror(lib):
+    assert lib.fa_strerror(0) == b"ok"
+    for code in range(1, 8):
+        assert len(lib.fa_strerror(code)) > 5
+
+
+def S(B, Hq, Hkv, Nq, Nk, d=128, causal=False):
+    return ctypes.byref(shape(B, Hq, Hkv, Nq, Nk, d, causal=causal))
+
+
+@pytest.mark.parametrize("N", [128, 200, 1000, 4096])
+@pytest.mark.parametrize("causal", [False, True])
+def test_tile_classes_match_oracle(lib, N, causal):
+    want = P.tile_classes(N, N, 128, 128, causal)
+    for i, row in enumerate(want):
+        for j, c in enumerate(row):
+            assert lib.fa_tile_class(S(1, 1, 1, N, N, causal=causal), i, j) == c
+
+
+def test_noncausal_rectangular_classes(lib):
+    assert lib.fa_tile_class(S(1, 1, 1, 100, 700), 0, 5) == P.FULL
+    assert lib.fa_tile_class(S(1, 1, 1, 100, 700), 0, 6) == -1   # out of range
+
+
+def units(lib, kind, s, n):
+    out = []
+    b, x, y = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    fn = getattr(lib, f"fa_{kind}_unit")
+    for i in range(n):
+        assert fn(s, i, ctypes.byref(b), ctypes.byref(x), ctypes.byref(y)) == 0
+        out.append((b.value, x.value, y.value))
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,N", [(2, 4, 2, 128), (2, 4, 4, 300), (1, 8, 2, 1000), (2, 16, 16, 4096),
+                                        (1, 32, 8, 8192)])
+def test_unit_orders_match_oracle(lib, causal, B, Hq, Hkv, N):
+    s = S(B, Hq, Hkv, N, N, causal=causal)
+    n = lib.fa_fwd_num_units(s)
+    assert units(lib, "fwd", s, n) == P.fwd_unit_order(B, Hq, N, N, causal)
+    n = lib.fa_dkdv_num_units(s)
+    assert units(lib, "dkdv", s, n) == P.dkdv_unit_order(B, Hkv, N, N, causal)
+    n = lib.fa_dq_num_units(s)
+    assert units(lib, "dq", s, n) == P.dq_unit_order(B, Hq, N, N, causal)
+
+
+@pytest.mark.parametrize("Nk", [1, 127, 128, 129, 1000, 131072])
+@pytest.mark.parametrize("req", [1, 3, 19, 64])
+def test_decode_split_ranges_match_oracle(lib, Nk, req):
+    s = S(8, 32, 8, 1, Nk)
+    want = P.decode_splits(Nk, req)
+    assert lib.fa_decode_num_splits(s, req) == len(want)
+    a, b = ctypes.c_int(), ctypes.c_int()
+    got = []
+    for i in range(len(want)):
+        assert lib.fa_decode_split_range(s, req, i, ctypes.byref(a), ctypes.byref(b)) == 0
+        got.append((a.value, b.value))
+    assert got == want
+    assert lib.fa_decode_split_range(s, req, len(want), ctypes.byref(a), ctypes.byref(b)) != 0
+
+
+def test_decode_auto_splits_positive(lib):
+    n = lib.fa_decode_num_splits(S(8, 32, 8, 4, 131072), 0)
+    assert 1 <= n <= 1024
+
+
+FAKE = 0x10000  # never dereferenced: argument checks fail first
+
+
+def tens(ptr=FAKE, sb=8 * 1024, sn=8 * 16, sh=8 * 2):
+    return ctypes.byref(FaTensor(ptr, sb, sn, sh))
+
+
+@pytest.mark.parametrize("bad", [
+    dict(Hq=3, Hkv=2), dict(d=96), dict(B=0), dict(Nq=0), dict(causal=True, Nq=10, Nk=20), dict(scale=0.0),
+    dict(scale=float("nan")), dict(scale=-1.0)])
+def test_invalid_shapes_rejected_before_any_gpu_work(lib, bad):
+    kw = dict(B=1, Hq=2, Hkv=2, Nq=16, Nk=16, d=64, causal=False, scale=None)
+    kw.update(bad)
+    s = shape(**kw)
+    if bad.get("scale", 1.0) != bad.get("scale", 1.0) or "scale" in bad:
+        s.scale = bad["scale"]
+    rc = lib.fa_fwd(tens(), tens(), tens(), tens(), FAKE, ctypes.byref(s), FAKE, 1 << 20, None)
+    assert rc == 1  # FA_ERR_INVALID
+
+
+def test_misaligned_and_workspace_errors(lib):
+    s = ctypes.byref(shape(1, 2, 2, 16, 16, 64))
+    assert lib.fa_fwd(tens(FAKE + 2), tens(), tens(), tens(), FAKE, s, FAKE, 1 << 20, None) == 2
+    assert lib.fa_fwd(tens(sn=12), tens(), tens(), tens(), FAKE, s, FAKE, 1 << 20, None) == 2
+    assert lib.fa_fwd(tens(), tens(), tens(), tens(), FAKE, s, FAKE, 8, None) == 3
+    assert lib.fa_fwd(tens(), tens(), tens(), tens(), None, s, FAKE, 1 << 20, None) == 1
+    assert lib.fa_fwd(None, tens(), tens(), tens(), FAKE, s, FAKE, 1 << 20, None) == 1
+    # decode: causal and too many packed rows are rejected
+    sd = shape(1, 32, 1, 1, 100, 64)
+    assert lib.fa_decode(tens(), tens(), tens(), tens(), FAKE, ctypes.byref(sd), 1, FAKE, 1 << 30, None) == 1
+
+
+def test_workspace_sizes(lib):
+    s = S(2, 16, 16, 4096, 4096, causal=True)
+    assert lib.fa_fwd_workspace_size(s) >= 256
+    assert lib.fa_bwd_workspace_size(s) >= 256 + 2 * 2 * 16 * 4096 * 4
+    sd = S(8, 32, 8, 4, 131072)
+    n = lib.fa_decode_num_splits(sd, 19)
+    assert lib.fa_decode_workspace_size(sd, 19) >= 256 + 8 * 32 * 4 * n * (128 + 1) * 4
+    lo, oo = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.fa_decode_partials_layout(sd, 19, ctypes.byref(lo), ctypes.byref(oo)) == 0
+    assert lo.value == 256 and oo.value >= lo.value + 8 * 32 * 4 * n * 4
+
+
+def test_binding_rejects_non_cuda_tensors():
+    import torch
+
+    with pytest.raises(fa.FAError):
+        fa.binding.tdesc(torch.zeros(1, 2, 2, 64, dtype=torch.bfloat16))

@@ -1,0 +1,160 @@
+"""GPU parity of the forward kernel against the fp64 oracle (through the C ABI).
+
+Covers: the tensor-core building blocks (self-test), small shapes spanning
+several tiles with ragged tails, d = 64 and 128, causal and non-causal, grouped
+heads, Nq != Nk, strided views, the bit-exact causal mask, and the workloads of
+the benchmark at full size on sampled rows.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_21_gb300 as fa
+from exact_io_aware_21_gb300 import inputs
+from oracle import attention as A
+from parity import assert_fwd, f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fa.library()
+    fa.library().fa_set_wait_timeout_ns(10_000_000_000)
+
+
+def status_ok(ws):
+    rc, st = fa.binding.device_status(ws)
+    assert rc == 0 and st == 0, f"device status {st:#x}"
+
+
+# ------------------------------------------------------------------ building blocks
+@pytest.mark.parametrize("k", [64, 128])
+def test_selftest_qk_form(k):
+    g = torch.Generator().manual_seed(k)
+    a = torch.randn(128, k, generator=g).to(torch.bfloat16)
+    b = torch.randn(128, k, generator=g).to(torch.bfloat16)
+    c = torch.zeros(128, 128, dtype=torch.float32, device=DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    fa.binding.check(fa.library().fa_selftest_mma(0, k, a.to(DEV).data_ptr(), b.to(DEV).data_ptr(), c.data_ptr(),
+                                                  ws.data_ptr(), None))
+    torch.cuda.synchronize()
+    ref = f64(a) @ f64(b).T
+    np.testing.assert_allclose(f64(c), ref, rtol=1e-5, atol=1e-4)
+    status_ok(ws)
+
+
+@pytest.mark.parametrize("n", [64, 128])
+def test_selftest_pv_form(n):
+    g = torch.Generator().manual_seed(100 + n)
+    a = torch.rand(128, 128, generator=g).to(torch.bfloat16)
+    b = torch.randn(128, n, generator=g).to(torch.bfloat16)
+    c = torch.zeros(128, n, dtype=torch.float32, device=DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    fa.binding.check(fa.library().fa_selftest_mma(1, n, a.to(DEV).data_ptr(), b.to(DEV).data_ptr(), c.data_ptr(),
+                                                  ws.data_ptr(), None))
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(f64(c), f64(a) @ f64(b), rtol=1e-5, atol=1e-4)
+    status_ok(ws)
+
+
+# ------------------------------------------------------------------ small shapes
+def run_fwd(x, causal, scale):
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def test_tiny_workload():
+    w = inputs.TINY
+    x = inputs.make(w)
+    o, lse = run_fwd(x, w.causal, w.scale)
+    o_ref, lse_ref = A.attention_forward(x["q"], x["k"], x["v"], w.scale, w.causal)
+    assert_fwd(o, lse, o_ref, lse_ref, w.name)
+
+
+CASES = [
+    # B, Hq, Hkv, Nq, Nk, d, causal
+    (1, 1, 1, 128, 128, 64, False),
+    (1, 2, 2, 256, 256, 128, True),
+    (2, 3, 3, 300, 300, 64, True),      # ragged: 3 query tiles, odd pair count
+    (1, 4, 2, 1000, 1000, 128, True),   # grouped heads, ragged
+    (2, 2, 1, 513, 513, 64, False),
+    (1, 2, 2, 200, 700, 128, False),    # Nq != Nk
+    (1, 2, 2, 700, 130, 64, False),
+    (1, 1, 1, 1, 1, 128, True),         # one row, one key
+    (1, 1, 1, 127, 127, 64, True),
+    (1, 1, 1, 129, 129, 128, True),
+    (1, 8, 1, 384, 384, 128, False),    # multi-query
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal", CASES)
+def test_small_shapes(B, Hq, Hkv, Nq, Nk, d, causal):
+    x = inputs.shape_inputs(B, Hq, Hkv, Nq, Nk, d, seed=Nq * 7 + Nk + d, with_do=False)
+    scale = 1 / np.sqrt(d)
+    o, lse = run_fwd(x, causal, scale)
+    o_ref, lse_ref = A.attention_forward(x["q"], x["k"], x["v"], scale, causal)
+    assert_fwd(o, lse, o_ref, lse_ref, f"{B}x{Hq}/{Hkv}x{Nq}x{Nk}x{d} causal={causal}")
+
+
+def test_strided_views_and_custom_scale():
+    """Q/K/V as slices of a packed [B, N, 3, H, d] buffer (head stride != d)."""
+    B, N, H, d = 2, 300, 2, 128
+    g = torch.Generator().manual_seed(5)
+    qkv = torch.randn(B, N, 3, H, d, generator=g).to(torch.bfloat16)
+    dq = qkv.to(DEV)
+    q, k, v = dq[:, :, 0], dq[:, :, 1], dq[:, :, 2]
+    o, lse = fa.forward(q, k, v, causal=True, scale=0.05)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = A.attention_forward(qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2], 0.05, True)
+    assert_fwd(o, lse, o_ref, lse_ref, "strided")
+
+
+@pytest.mark.parametrize("N,d", [(1000, 64), (4096, 128), (300, 128)])
+def test_causal_mask_bit_exact(N, d):
+    """Q = 0: every visible score is 0, so exp(LSE_i) counts the visible keys: i + 1."""
+    B, H = 1, 2
+    q = torch.zeros(B, N, H, d, dtype=torch.bfloat16, device=DEV)
+    k = torch.randn(B, N, H, d, device=DEV).to(torch.bfloat16)
+    v = torch.randn(B, N, H, d, device=DEV).to(torch.bfloat16)
+    _, lse = fa.forward(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    counts = np.rint(np.exp(f64(lse))).astype(np.int64)
+    assert np.array_equal(counts, np.broadcast_to(np.arange(1, N + 1), counts.shape))
+    _, lse = fa.forward(q, k, v, causal=False)
+    torch.cuda.synchronize()
+    assert np.array_equal(np.rint(np.exp(f64(lse))).astype(np.int64), np.full((B, H, N), N))
+
+
+def test_deterministic():
+    x = inputs.shape_inputs(1, 4, 2, 1000, 1000, 128, seed=3, with_do=False)
+    a = run_fwd(x, True, 0.1)
+    b = run_fwd(x, True, 0.1)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# ------------------------------------------------------------------ full-size workloads
+def sampled_check(w, n_heads=3, n_rows=96, seed=11):
+    x = inputs.make(w, with_do=False)
+    o, lse = run_fwd(x, w.causal, w.scale)
+    rng = np.random.default_rng(seed)
+    heads = [(int(rng.integers(w.B)), int(rng.integers(w.Hq))) for _ in range(n_heads)]
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, w.Nq - 1], rng.integers(0, w.Nq, n_rows)]))
+    o_ref, lse_ref = A.attention_forward(x["q"], x["k"], x["v"], w.scale, w.causal, heads=heads, rows=rows)
+    for b, h in heads:
+        assert_fwd(o[b, rows, h], lse[b, h, rows], o_ref[b, rows, h], lse_ref[b, h, rows], f"{w.name} b{b} h{h}")
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w", [inputs.MHA_N2048_D64, inputs.CAUSAL_N4096_D128, inputs.GQA_N8192_D128],
+                         ids=lambda w: w.name)
+def test_full_workload_sampled(w):
+    sampled_check(w)

@@ -1,6 +1,761 @@
-// Backward kernels (placeholder until the tcgen05 backward lands).
+// Backward kernels: attention gradients with P rebuilt on chip.
+//
+// Method ("第18章 FlashAttention" §18.4.4, Fig. 18-17; "CMU 11-868 L21" notes,
+// slide 14): the forward pass saved only O and the row statistic (here the
+// log-sum-exp); the backward pass recomputes S = Q K^T tile by tile, rebuilds
+// P = exp(scale S - LSE) with no rescaling, and forms dV = P^T dO,
+// dP = dO V^T, dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+// D_i = rowsum(P o dP) over the whole row equals dO_i . O_i, so it is computed
+// once, before the tile loops, by the preprocess kernel.
+//
+// GB300 design: three kernels and no atomics, so results are deterministic.
+//   preprocess  D = rowsum(dO o O) and LSE * log2(e), both padded to whole
+//               128-row tiles (+inf / 0 in the padding, which zeroes P there).
+//   dK/dV       one CTA per SM, persistent; a unit is one 128-key tile of one
+//               K/V head; it loops over the query heads of the group and their
+//               query tiles (causal: only tiles at or below the diagonal).
+//               TMEM: S^T [0,128) dP^T [128,256) dV [256,256+d) dK [256+d,..);
+//               P^T and dS^T are written back over S^T and dP^T as bf16 and
+//               feed the dV and dK products from TMEM.
+//   dQ          a unit is one 128-row query tile; it loops over key tiles.
+//               TMEM: S double-buffered [0,256), dP [256,384), dQ [384,384+d);
+//               dS is written over dP as bf16 and feeds dQ += dS K.
+// Warp roles as in the forward kernel: warp 0 loads with TMA, one thread of
+// warp 1 issues tcgen05 MMAs, warps 4-7 do the elementwise work with one TMEM
+// lane (one row) per thread.
+#include <math.h>
+
 #include "fa_kernels.h"
+#include "sm103.cuh"
 
 namespace fa {
-cudaError_t launch_bwd(const BwdLaunch&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+struct BwdParams {
+  Dims dims;
+  float scale;       // softmax scale
+  float scale_log2;  // scale * log2(e)
+  OutRows o, dout, dq, dk, dv;
+  const float* lse;
+  float* lse2;
+  float* delta;
+  int nq_pad;
+  int* status;
+  int* counter;
+  unsigned long long timeout_ns;
+  int total_units;
+};
+
+// ================================================================== preprocess
+// threads per row = D / 8 (one 16-byte chunk of dO and of O each)
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
+  constexpr int TPR = D / 8;
+  const int64_t row = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / TPR;
+  const int part = threadIdx.x % TPR;
+  const int64_t rows = static_cast<int64_t>(p.dims.B) * p.dims.Hq * p.nq_pad;
+  if (row >= rows) return;
+  const int q = static_cast<int>(row % p.nq_pad);
+  const int bh = static_cast<int>(row / p.nq_pad);
+  const int b = bh / p.dims.Hq, h = bh % p.dims.Hq;
+  float acc = 0.f;
+  if (q < p.dims.Nq) {
+    const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.o.ptr) + b * p.o.sb +
+                             static_cast<int64_t>(q) * p.o.sn + h * p.o.sh + part * 8;
+    const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout.ptr) + b * p.dout.sb +
+                             static_cast<int64_t>(q) * p.dout.sn + h * p.dout.sh + part * 8;
+    const uint4 ov = *reinterpret_cast<const uint4*>(o);
+    const uint4 gv = *reinterpret_cast<const uint4*>(g);
+    const uint32_t* ou = reinterpret_cast<const uint32_t*>(&ov);
+    const uint32_t* gu = reinterpret_cast<const uint32_t*>(&gv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = unpack_bf16(ou[i]), c = unpack_bf16(gu[i]);
+      acc = fmaf(a.x, c.x, acc);
+      acc = fmaf(a.y, c.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
+  if (part == 0) {
+    p.delta[row] = acc;
+    p.lse2[row] = q < p.dims.Nq ? p.lse[static_cast<int64_t>(bh) * p.dims.Nq + q] * LOG2E : INFINITY;
+  }
+}
+
+// ================================================================== shared helpers
+template <int D>
+__device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
+  constexpr uint32_t IDESC = idesc_bf16(128, 128, false, false);
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    const uint32_t off = (k / 4) * (TILE * 128) + (k % 4) * 32;
+    mma_ss(d_tmem, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), IDESC, k > 0);
+  }
+}
+
+// D[128 x D] (+)= A[tmem, 128 x 128 bf16] * B[smem tile 128 x D, N-major]
+template <int D>
+__device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, bool acc) {
+  constexpr uint32_t IDESC = idesc_bf16(128, D, false, true);
+#pragma unroll
+  for (int k = 0; k < TILE / 16; ++k)
+    mma_ts(d_tmem, a_tmem + k * 8, sdesc_sw128(b_base + k * 16 * 128, TILE * 128, 1024), IDESC,
+           (acc || k > 0) ? 1u : 0u);
+}
+
+// store one 128-column... row of D fp32 accumulator columns as bf16 (times mul)
+template <int D>
+__device__ __forceinline__ void store_row_bf16(uint32_t t_acc, float mul, __nv_bfloat16* dst, bool live) {
+#pragma unroll
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t v[32];
+    tmem_ld32(t_acc + cc * 32, v);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+    if (live) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+  }
+}
+
+// ================================================================== dK / dV
+template <int D>
+struct DkvLayout {
+  static constexpr int TB = TILE * D * 2;
+  static constexpr int STAGES = D == 64 ? 4 : 2;
+  static constexpr int STAGE = 2 * TB + 1024;  // Q_i, dO_i, lse2[128], delta[128]
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TB;
+  static constexpr int OFF_ST = 2 * TB;
+  static constexpr int OFF_BAR = OFF_ST + STAGES * STAGE;
+  // unit_full[2] unit_empty[2] kv_full kv_empty st_full[S] st_empty[S] s_full dp_full p_full ds_full acc_full
+  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 5;
+  static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_TMEM = OFF_UNIT + 16;
+  static constexpr int ALLOC = OFF_TMEM + 16 + 1024;
+};
+
+struct DkvBars {
+  uint64_t *unit_full, *unit_empty, *kv_full, *kv_empty, *st_full, *st_empty, *s_full, *dp_full, *p_full, *ds_full,
+      *acc_full;
+};
+
+template <int D>
+__device__ __forceinline__ DkvBars dkv_bars(uint8_t* smem) {
+  using L = DkvLayout<D>;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  DkvBars r;
+  r.unit_full = b;
+  r.unit_empty = b + 2;
+  r.kv_full = b + 4;
+  r.kv_empty = b + 5;
+  r.st_full = b + 6;
+  r.st_empty = r.st_full + L::STAGES;
+  r.s_full = r.st_empty + L::STAGES;
+  r.dp_full = r.s_full + 1;
+  r.p_full = r.s_full + 2;
+  r.ds_full = r.s_full + 3;
+  r.acc_full = r.s_full + 4;
+  return r;
+}
+
+struct DkvUnit {
+  int b, kvh, kt, q0, nqi, n_it;
+};
+
+__device__ __forceinline__ DkvUnit dkv_decode(const Dims& s, int u) {
+  DkvUnit r;
+  dkdv_unit(s, u, r.b, r.kvh, r.kt);
+  r.q0 = q_tile_begin(s, r.kt);
+  r.nqi = q_tiles(s) - r.q0;
+  r.n_it = (s.Hq / s.Hkv) * r.nqi;
+  return r;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(256, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p) {
+  using L = DkvLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const DkvBars bar = dkv_bars<D>(smem);
+  int* unit_slot = reinterpret_cast<int*>(smem + L::OFF_UNIT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
+  const int warp = threadIdx.x >> 5;
+  const Ctl ctl{p.status, p.timeout_ns};
+  const Dims& s = p.dims;
+  const int g = s.Hq / s.Hkv;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.unit_full[i], 1);
+      mbar_init(&bar.unit_empty[i], 1 + 128);
+    }
+    mbar_init(bar.kv_full, 1);
+    mbar_init(bar.kv_empty, 1);
+    for (int i = 0; i < L::STAGES; ++i) {
+      mbar_init(&bar.st_full[i], 1);
+      mbar_init(&bar.st_empty[i], 1);
+    }
+    mbar_init(bar.s_full, 1);
+    mbar_init(bar.dp_full, 1);
+    mbar_init(bar.p_full, 128);
+    mbar_init(bar.ds_full, 128);
+    mbar_init(bar.acc_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane_id() == 0) {  // ---------------------------------------------- producer
+      uint32_t sq = 0;
+      int kv_armed = -1;
+      for (int it = 0;; ++it) {
+        const int slot = it & 1;
+        if (!mbar_wait(&bar.unit_empty[slot], ((it >> 1) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
+        const int u = atomicAdd(p.counter, 1);
+        unit_slot[slot] = u;
+        mbar_arrive(&bar.unit_full[slot]);
+        if (u >= p.total_units) break;
+        const DkvUnit w = dkv_decode(s, u);
+        if (!mbar_wait(bar.kv_empty, (it & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
+        mbar_arrive_expect_tx(bar.kv_full, 2 * L::TB);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(smem + L::OFF_K + c * (TILE * 128), &tm_k, bar.kv_full, c * 64, w.kvh, w.kt * TILE, w.b);
+          tma_load_4d(smem + L::OFF_V + c * (TILE * 128), &tm_v, bar.kv_full, c * 64, w.kvh, w.kt * TILE, w.b);
+        }
+        kv_armed = it;
+        bool ok = true;
+        for (int k = 0; k < w.n_it; ++k, ++sq) {
+          const int st = sq % L::STAGES;
+          if (!mbar_wait(&bar.st_empty[st], ((sq / L::STAGES) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
+            ok = false;
+            break;
+          }
+          const int hq = w.kvh * g + k / w.nqi, qi = w.q0 + k % w.nqi;
+          uint8_t* base = smem + L::OFF_ST + st * L::STAGE;
+          const int64_t row0 = (static_cast<int64_t>(w.b) * s.Hq + hq) * p.nq_pad + qi * TILE;
+          mbar_arrive_expect_tx(&bar.st_full[st], 2 * L::TB + 1024);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(base + c * (TILE * 128), &tm_q, &bar.st_full[st], c * 64, hq, qi * TILE, w.b);
+            tma_load_4d(base + L::TB + c * (TILE * 128), &tm_do, &bar.st_full[st], c * 64, hq, qi * TILE, w.b);
+          }
+          bulk_load(base + 2 * L::TB, p.lse2 + row0, 512, &bar.st_full[st]);
+          bulk_load(base + 2 * L::TB + 512, p.delta + row0, 512, &bar.st_full[st]);
+        }
+        if (!ok) break;
+      }
+      // copies in flight land before exit
+      for (int i = 0; i < L::STAGES; ++i)
+        if (sq > static_cast<uint32_t>(i)) {
+          const uint32_t last = sq - 1 - ((sq - 1 - i) % L::STAGES);
+          mbar_wait(&bar.st_full[i], (last / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+        }
+      if (kv_armed >= 0) mbar_wait(bar.kv_full, kv_armed & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+    }
+  } else if (warp == 1) {
+    if (lane_id() == 0) {  // ---------------------------------------------- MMA issuer
+      const uint32_t kb = smem_u32(smem + L::OFF_K), vb = smem_u32(smem + L::OFF_V);
+      const uint32_t stb = smem_u32(smem + L::OFF_ST);
+      const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+      uint32_t sq = 0, pph = 0, dph = 0;
+      for (int it = 0;; ++it) {
+        const int slot = it & 1;
+        if (!mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
+        const int u = unit_slot[slot];
+        mbar_arrive(&bar.unit_empty[slot]);
+        if (u >= p.total_units) break;
+        const DkvUnit w = dkv_decode(s, u);
+        if (!mbar_wait(bar.kv_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA)) break;
+        bool ok = mbar_wait(&bar.st_full[sq % L::STAGES], (sq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint32_t qb = stb + (sq % L::STAGES) * L::STAGE;
+          issue_ss<D>(tS, kb, qb);           // S^T = K Q^T
+          mma_commit(bar.s_full);
+          issue_ss<D>(tP, vb, qb + L::TB);   // dP^T = V dO^T
+          mma_commit(bar.dp_full);
+        }
+        for (int k = 0; k < w.n_it && ok; ++k) {
+          const uint32_t cur = stb + ((sq + k) % L::STAGES) * L::STAGE;
+          ok = mbar_wait(bar.p_full, pph, ctl, FA_STATUS_TIMEOUT_MMA);
+          pph ^= 1;
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts<D>(tdV, tS, cur + L::TB, k > 0);   // dV += P^T dO
+          const bool more = k + 1 < w.n_it;
+          uint32_t nxt = 0;
+          if (more) {
+            const uint32_t nsq = sq + k + 1;
+            ok = mbar_wait(&bar.st_full[nsq % L::STAGES], (nsq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+            if (!ok) break;
+            tc_fence_after();
+            nxt = stb + (nsq % L::STAGES) * L::STAGE;
+            issue_ss<D>(tS, kb, nxt);
+            mma_commit(bar.s_full);
+          }
+          ok = mbar_wait(bar.ds_full, dph, ctl, FA_STATUS_TIMEOUT_MMA);
+          dph ^= 1;
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts<D>(tdK, tP, cur, k > 0);           // dK += dS^T Q
+          mma_commit(&bar.st_empty[(sq + k) % L::STAGES]);
+          if (more) {
+            issue_ss<D>(tP, vb, nxt + L::TB);
+            mma_commit(bar.dp_full);
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar.acc_full);
+        mma_commit(bar.kv_empty);
+        sq += w.n_it;
+      }
+    }
+  } else if (warp >= 4) {  // -------------------------------------------------- gradient warps
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane_id();  // key row within the tile
+    const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lanes, tP = tmem + lanes + 128, tdV = tmem + lanes + 256,
+                   tdK = tmem + lanes + 256 + D;
+    const float c = p.scale_log2;
+    uint32_t sq = 0, sph = 0, dph = 0;
+    for (int it = 0;; ++it) {
+      const int slot = it & 1;
+      bool ok = mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int u = unit_slot[slot];
+      mbar_arrive(&bar.unit_empty[slot]);
+      if (u >= p.total_units) break;
+      const DkvUnit w = dkv_decode(s, u);
+      const int key = w.kt * TILE + r;
+      for (int k = 0; k < w.n_it && ok; ++k) {
+        const uint32_t q = sq + k;
+        const uint8_t* stage = smem + L::OFF_ST + (q % L::STAGES) * L::STAGE;
+        const float* l2 = reinterpret_cast<const float*>(stage + 2 * L::TB);
+        const float* dl = l2 + 128;
+        const int qi = w.q0 + k % w.nqi;
+        ok = mbar_wait(&bar.st_full[q % L::STAGES], (q / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+        ok = ok && mbar_wait(bar.s_full, sph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+        sph ^= 1;
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // P^T[key, query] = exp2(S * scale*log2e - LSE2[query]); causal: 0 where query < key.
+        // S^T is read 32 columns at a time; each 16-column bf16 result goes back over
+        // columns that have already been read.
+        int lim = 0;  // columns below lim are masked (diagonal tile only)
+        if (CAUSAL && tile_class(s, qi, w.kt) == 2) lim = key - qi * TILE;
+        uint32_t pk[64];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t sr[32];
+          tmem_ld32(tS + 32 * cc, sr);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int col = 32 * cc + 4 * j;
+            const float4 l4 = *reinterpret_cast<const float4*>(l2 + col);
+            float p0 = ex2(fmaf(__uint_as_float(sr[4 * j + 0]), c, -l4.x));
+            float p1 = ex2(fmaf(__uint_as_float(sr[4 * j + 1]), c, -l4.y));
+            float p2 = ex2(fmaf(__uint_as_float(sr[4 * j + 2]), c, -l4.z));
+            float p3 = ex2(fmaf(__uint_as_float(sr[4 * j + 3]), c, -l4.w));
+            if (CAUSAL) {
+              if (col + 0 < lim) p0 = 0.f;
+              if (col + 1 < lim) p1 = 0.f;
+              if (col + 2 < lim) p2 = 0.f;
+              if (col + 3 < lim) p3 = 0.f;
+            }
+            pk[16 * cc + 2 * j] = pack_bf16(p0, p1);
+            pk[16 * cc + 2 * j + 1] = pack_bf16(p2, p3);
+          }
+          tmem_st16(tS + 16 * cc, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * cc]));
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar.p_full);
+
+        ok = mbar_wait(bar.dp_full, dph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+        dph ^= 1;
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // dS^T = P^T o (dP^T - D[query])
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t sr[32];
+          tmem_ld32(tP + 32 * cc, sr);
+          uint32_t dk[16];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int col = 32 * cc + 4 * j;
+            const float4 d4 = *reinterpret_cast<const float4*>(dl + col);
+            const float2 pa = unpack_bf16(pk[16 * cc + 2 * j]), pb = unpack_bf16(pk[16 * cc + 2 * j + 1]);
+            dk[2 * j] = pack_bf16(pa.x * (__uint_as_float(sr[4 * j + 0]) - d4.x),
+                                  pa.y * (__uint_as_float(sr[4 * j + 1]) - d4.y));
+            dk[2 * j + 1] = pack_bf16(pb.x * (__uint_as_float(sr[4 * j + 2]) - d4.z),
+                                      pb.y * (__uint_as_float(sr[4 * j + 3]) - d4.w));
+          }
+          tmem_st16(tP + 16 * cc, dk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar.ds_full);
+      }
+      if (!ok) break;
+      ok = mbar_wait(bar.acc_full, it & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const bool live = key < s.Nk;
+      __nv_bfloat16* dvr = reinterpret_cast<__nv_bfloat16*>(p.dv.ptr) + w.b * p.dv.sb +
+                           static_cast<int64_t>(key) * p.dv.sn + w.kvh * p.dv.sh;
+      __nv_bfloat16* dkr = reinterpret_cast<__nv_bfloat16*>(p.dk.ptr) + w.b * p.dk.sb +
+                           static_cast<int64_t>(key) * p.dk.sn + w.kvh * p.dk.sh;
+      store_row_bf16<D>(tdV, 1.f, dvr, live);
+      store_row_bf16<D>(tdK, p.scale, dkr, live);
+      sq += w.n_it;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================== dQ
+template <int D>
+struct DqLayout {
+  static constexpr int TB = TILE * D * 2;
+  static constexpr int STAGES = D == 64 ? 4 : 2;  // K_j + V_j per stage
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = TB;
+  static constexpr int OFF_KV = 2 * TB;
+  static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * TB;
+  // unit_full[2] unit_empty[2] q_full q_empty kv_full[S] kv_empty[S] s_full[2] dp_full ds_full acc_full
+  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 5;
+  static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_TMEM = OFF_UNIT + 16;
+  static constexpr int ALLOC = OFF_TMEM + 16 + 1024;
+};
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(256, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdParams p) {
+  using L = DqLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bb = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* unit_full = bb;
+  uint64_t* unit_empty = bb + 2;
+  uint64_t* q_full = bb + 4;
+  uint64_t* q_empty = bb + 5;
+  uint64_t* kv_full = bb + 6;
+  uint64_t* kv_empty = kv_full + L::STAGES;
+  uint64_t* s_full = kv_empty + L::STAGES;  // [2]
+  uint64_t* dp_full = s_full + 2;
+  uint64_t* ds_full = s_full + 3;
+  uint64_t* acc_full = s_full + 4;
+  int* unit_slot = reinterpret_cast<int*>(smem + L::OFF_UNIT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
+  const int warp = threadIdx.x >> 5;
+  const Ctl ctl{p.status, p.timeout_ns};
+  const Dims& s = p.dims;
+  const int g = s.Hq / s.Hkv;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&unit_full[i], 1);
+      mbar_init(&unit_empty[i], 1 + 128);
+      mbar_init(&s_full[i], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int i = 0; i < L::STAGES; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, 128);
+    mbar_init(acc_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane_id() == 0) {  // ---------------------------------------------- producer
+      uint32_t kq = 0;
+      int q_armed = -1;
+      for (int it = 0;; ++it) {
+        const int slot = it & 1;
+        if (!mbar_wait(&unit_empty[slot], ((it >> 1) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
+        const int u = atomicAdd(p.counter, 1);
+        unit_slot[slot] = u;
+        mbar_arrive(&unit_full[slot]);
+        if (u >= p.total_units) break;
+        int b, h, qt;
+        dq_unit(s, u, b, h, qt);
+        const int n = kv_tiles_for_q(s, qt), kvh = h / g;
+        if (!mbar_wait(q_empty, (it & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
+        mbar_arrive_expect_tx(q_full, 2 * L::TB);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(smem + L::OFF_Q + c * (TILE * 128), &tm_q, q_full, c * 64, h, qt * TILE, b);
+          tma_load_4d(smem + L::OFF_DO + c * (TILE * 128), &tm_do, q_full, c * 64, h, qt * TILE, b);
+        }
+        q_armed = it;
+        bool ok = true;
+        for (int j = 0; j < n; ++j, ++kq) {
+          const int st = kq % L::STAGES;
+          if (!mbar_wait(&kv_empty[st], ((kq / L::STAGES) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
+            ok = false;
+            break;
+          }
+          uint8_t* base = smem + L::OFF_KV + st * 2 * L::TB;
+          mbar_arrive_expect_tx(&kv_full[st], 2 * L::TB);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(base + c * (TILE * 128), &tm_k, &kv_full[st], c * 64, kvh, j * TILE, b);
+            tma_load_4d(base + L::TB + c * (TILE * 128), &tm_v, &kv_full[st], c * 64, kvh, j * TILE, b);
+          }
+        }
+        if (!ok) break;
+      }
+      for (int i = 0; i < L::STAGES; ++i)
+        if (kq > static_cast<uint32_t>(i)) {
+          const uint32_t last = kq - 1 - ((kq - 1 - i) % L::STAGES);
+          mbar_wait(&kv_full[i], (last / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+        }
+      if (q_armed >= 0) mbar_wait(q_full, q_armed & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+    }
+  } else if (warp == 1) {
+    if (lane_id() == 0) {  // ---------------------------------------------- MMA issuer
+      const uint32_t qb = smem_u32(smem + L::OFF_Q), dob = smem_u32(smem + L::OFF_DO);
+      const uint32_t kvb = smem_u32(smem + L::OFF_KV);
+      const uint32_t tP = tmem + 256, tdQ = tmem + 384;
+      uint32_t kq = 0, dsph = 0;
+      auto kvwait = [&](uint32_t idx) {
+        return mbar_wait(&kv_full[idx % L::STAGES], (idx / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+      };
+      auto kbase = [&](uint32_t idx) { return kvb + (idx % L::STAGES) * 2 * L::TB; };
+      for (int it = 0;; ++it) {
+        const int slot = it & 1;
+        if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
+        const int u = unit_slot[slot];
+        mbar_arrive(&unit_empty[slot]);
+        if (u >= p.total_units) break;
+        int b, h, qt;
+        dq_unit(s, u, b, h, qt);
+        const int n = kv_tiles_for_q(s, qt);
+        bool ok = mbar_wait(q_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA) && kvwait(kq);
+        if (!ok) break;
+        tc_fence_after();
+        issue_ss<D>(tmem + 0, qb, kbase(kq));            // S_0 = Q K_0^T
+        mma_commit(&s_full[0]);
+        issue_ss<D>(tP, dob, kbase(kq) + L::TB);          // dP_0 = dO V_0^T
+        mma_commit(dp_full);
+        if (n > 1) {
+          if (!kvwait(kq + 1)) break;
+          tc_fence_after();
+          issue_ss<D>(tmem + 128, qb, kbase(kq + 1));
+          mma_commit(&s_full[1]);
+        }
+        for (int j = 0; j < n && ok; ++j) {
+          ok = mbar_wait(ds_full, dsph, ctl, FA_STATUS_TIMEOUT_MMA);
+          dsph ^= 1;
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts<D>(tdQ, tP, kbase(kq + j), j > 0);       // dQ += dS K_j
+          mma_commit(&kv_empty[(kq + j) % L::STAGES]);
+          if (j + 1 < n) {
+            issue_ss<D>(tP, dob, kbase(kq + j + 1) + L::TB);  // dP_{j+1}
+            mma_commit(dp_full);
+          }
+          if (j + 2 < n) {
+            ok = kvwait(kq + j + 2);
+            if (!ok) break;
+            tc_fence_after();
+            issue_ss<D>(tmem + (j & 1) * 128, qb, kbase(kq + j + 2));
+            mma_commit(&s_full[j & 1]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(acc_full);
+        mma_commit(q_empty);
+        kq += n;
+      }
+    }
+  } else if (warp >= 4) {  // -------------------------------------------------- gradient warps
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane_id();
+    const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tP = tmem + lanes + 256, tdQ = tmem + lanes + 384;
+    const float c = p.scale_log2;
+    uint32_t sph[2] = {0, 0}, dph = 0;
+    for (int it = 0;; ++it) {
+      const int slot = it & 1;
+      bool ok = mbar_wait(&unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int u = unit_slot[slot];
+      mbar_arrive(&unit_empty[slot]);
+      if (u >= p.total_units) break;
+      int b, h, qt;
+      dq_unit(s, u, b, h, qt);
+      const int n = kv_tiles_for_q(s, qt);
+      const int q_row = qt * TILE + r;
+      const int64_t srow = (static_cast<int64_t>(b) * s.Hq + h) * p.nq_pad + q_row;
+      const float l2 = p.lse2[srow], dl = p.delta[srow];
+      for (int j = 0; j < n && ok; ++j) {
+        const int bi = j & 1;
+        ok = mbar_wait(&s_full[bi], sph[bi], ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+        sph[bi] ^= 1;
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        int lim = 128;  // keys at or beyond lim (tile-local) are masked
+        if (j == n - 1) {
+          lim = imin(lim, s.Nk - j * TILE);
+          if (CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
+        }
+        uint32_t pk[64];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t sr[32];
+          tmem_ld32(tmem + lanes + bi * 128 + 32 * cc, sr);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = 32 * cc + 2 * i;
+            float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), c, -l2));
+            float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), c, -l2));
+            if (col >= lim) p0 = 0.f;
+            if (col + 1 >= lim) p1 = 0.f;
+            pk[16 * cc + i] = pack_bf16(p0, p1);
+          }
+        }
+        ok = mbar_wait(dp_full, dph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+        dph ^= 1;
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // dS = P o (dP - D_row), written as bf16 over the dP columns already read
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t sr[32];
+          tmem_ld32(tP + 32 * cc, sr);
+          uint32_t ds[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 pp = unpack_bf16(pk[16 * cc + i]);
+            ds[i] = pack_bf16(pp.x * (__uint_as_float(sr[2 * i]) - dl), pp.y * (__uint_as_float(sr[2 * i + 1]) - dl));
+          }
+          tmem_st16(tP + 16 * cc, ds);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+      }
+      if (!ok) break;
+      ok = mbar_wait(acc_full, it & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      __nv_bfloat16* dqr = reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sb +
+                           static_cast<int64_t>(q_row) * p.dq.sn + h * p.dq.sh;
+      store_row_bf16<D>(tdQ, p.scale, dqr, q_row < s.Nq);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
+  BwdParams p;
+  p.dims = a.dims;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * LOG2E;
+  p.o = a.o;
+  p.dout = a.dout;
+  p.dq = a.dq;
+  p.dk = a.dk;
+  p.dv = a.dv;
+  p.lse = a.lse;
+  p.lse2 = a.lse2;
+  p.delta = a.delta;
+  p.nq_pad = a.nq_pad;
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  // 1) preprocess
+  {
+    const int64_t threads = static_cast<int64_t>(a.dims.B) * a.dims.Hq * a.nq_pad * (D / 8);
+    bwd_preprocess_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // 2) dK / dV
+  {
+    auto kern = bwd_dkdv_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<D>::ALLOC);
+    if (e != cudaSuccess) return e;
+    p.counter = a.counters;
+    p.total_units = dkdv_units(a.dims);
+    kern<<<imax(1, imin(p.total_units, a.num_sms)), 256, DkvLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
+                                                                                     a.tm_do, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // 3) dQ
+  {
+    auto kern = bwd_dq_kernel<D, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::ALLOC);
+    if (e != cudaSuccess) return e;
+    p.counter = a.counters + 1;
+    p.total_units = dq_units(a.dims);
+    kern<<<imax(1, imin(p.total_units, a.num_sms)), 256, DqLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
+                                                                                   a.tm_do, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st) {
+  if (a.d == 64) return a.dims.causal ? launch_bwd_t<64, true>(a, st) : launch_bwd_t<64, false>(a, st);
+  return a.dims.causal ? launch_bwd_t<128, true>(a, st) : launch_bwd_t<128, false>(a, st);
+}
+
 }  // namespace fa

@@ -41,7 +41,8 @@ def test_selftest_qk_form(k):
     b = torch.randn(128, k, generator=g).to(torch.bfloat16)
     c = torch.zeros(128, 128, dtype=torch.float32, device=DEV)
     ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
-    fa.binding.check(fa.library().fa_selftest_mma(0, k, a.to(DEV).data_ptr(), b.to(DEV).data_ptr(), c.data_ptr(),
+    da, db = a.to(DEV), b.to(DEV)   # keep the device copies alive during the call
+    fa.binding.check(fa.library().fa_selftest_mma(0, k, da.data_ptr(), db.data_ptr(), c.data_ptr(),
                                                   ws.data_ptr(), None))
     torch.cuda.synchronize()
     ref = f64(a) @ f64(b).T
@@ -56,7 +57,8 @@ def test_selftest_pv_form(n):
     b = torch.randn(128, n, generator=g).to(torch.bfloat16)
     c = torch.zeros(128, n, dtype=torch.float32, device=DEV)
     ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
-    fa.binding.check(fa.library().fa_selftest_mma(1, n, a.to(DEV).data_ptr(), b.to(DEV).data_ptr(), c.data_ptr(),
+    da, db = a.to(DEV), b.to(DEV)
+    fa.binding.check(fa.library().fa_selftest_mma(1, n, da.data_ptr(), db.data_ptr(), c.data_ptr(),
                                                   ws.data_ptr(), None))
     torch.cuda.synchronize()
     np.testing.assert_allclose(f64(c), f64(a) @ f64(b), rtol=1e-5, atol=1e-4)

@@ -46,9 +46,10 @@ _PI = ctypes.POINTER(ctypes.c_int)
 _SZ = ctypes.c_size_t
 SIGNATURES = {
     "fa_fwd_workspace_size": (_SZ, [_PS]),
-    "fa_fwd": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _VP, _SZ, _VP]),
+    "fa_fwd": (_I, [_PT, _PT, _PT, _PT, _VP, _PT, _PS, _VP, _SZ, _VP]),
     "fa_bwd_workspace_size": (_SZ, [_PS]),
-    "fa_bwd": (_I, [_PT, _PT, _PT, _PT, _VP, _PT, _PT, _PT, _PT, _PS, _VP, _SZ, _VP]),
+    "fa_bwd": (_I, [_PT, _PT, _PT, _PT, _VP, _PT, _PT, _PT, _PT, _PT, _PS, _VP, _SZ, _VP]),
+    "fa_bwd_part": (_I, [_I, _PT, _PT, _PT, _PT, _VP, _PT, _PT, _PT, _PT, _PT, _PS, _VP, _SZ, _VP]),
     "fa_decode_num_splits": (_I, [_PS, _I]),
     "fa_decode_workspace_size": (_SZ, [_PS, _I]),
     "fa_decode": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _I, _VP, _SZ, _VP]),
@@ -118,16 +119,27 @@ def _ws(nbytes, device):
 
 
 # ---------------------------------------------------------------- C-ABI mirrors
-def fa_fwd(q, k, v, o, lse, s, workspace):
+def _opt(t):
+    return None if t is None else ctypes.byref(tdesc(t))
+
+
+def fa_fwd(q, k, v, o, lse, s, workspace, o_res=None):
     lib = library()
-    check(lib.fa_fwd(tdesc(q), tdesc(k), tdesc(v), tdesc(o), lse.data_ptr(), ctypes.byref(s),
+    check(lib.fa_fwd(tdesc(q), tdesc(k), tdesc(v), tdesc(o), lse.data_ptr(), _opt(o_res), ctypes.byref(s),
                      workspace.data_ptr(), workspace.numel(), _stream(q)))
 
 
-def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, s, workspace):
+def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, s, workspace, o_res=None):
     lib = library()
-    check(lib.fa_bwd(tdesc(q), tdesc(k), tdesc(v), tdesc(o), lse.data_ptr(), tdesc(do), tdesc(dq), tdesc(dk),
-                     tdesc(dv), ctypes.byref(s), workspace.data_ptr(), workspace.numel(), _stream(q)))
+    check(lib.fa_bwd(tdesc(q), tdesc(k), tdesc(v), tdesc(o), lse.data_ptr(), _opt(o_res), tdesc(do), tdesc(dq),
+                     tdesc(dk), tdesc(dv), ctypes.byref(s), workspace.data_ptr(), workspace.numel(), _stream(q)))
+
+
+def fa_bwd_part(part, q, k, v, o, lse, do, dq, dk, dv, s, workspace, o_res=None):
+    lib = library()
+    check(lib.fa_bwd_part(int(part), tdesc(q), tdesc(k), tdesc(v), tdesc(o), lse.data_ptr(), _opt(o_res),
+                          tdesc(do), tdesc(dq), tdesc(dk), tdesc(dv), ctypes.byref(s), workspace.data_ptr(),
+                          workspace.numel(), _stream(q)))
 
 
 def fa_decode(q, kc, vc, o, lse, s, num_splits, workspace):
@@ -151,24 +163,29 @@ def _dims(q, k, scale, causal):
     return shape(B, Hq, Hkv, Nq, Nk, d, scale, causal)
 
 
-def forward(q, k, v, causal=False, scale=None):
-    """O, LSE = attention(q, k, v).  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] bf16 on CUDA."""
+def forward(q, k, v, causal=False, scale=None, residual=False):
+    """O, LSE = attention(q, k, v).  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] bf16 on CUDA.
+
+    With ``residual=True`` also returns O's bf16 rounding residual, which
+    ``backward`` uses to form D accurately (see fa_bwd in include/fa.h).
+    """
     s = _dims(q, k, scale, causal)
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
+    res = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
     ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q.device)
-    fa_fwd(q, k, v, o, lse, s, ws)
-    return o, lse
+    fa_fwd(q, k, v, o, lse, s, ws, res)
+    return (o, lse, res) if residual else (o, lse)
 
 
-def backward(q, k, v, o, lse, do, causal=False, scale=None):
-    """dQ, dK, dV of attention given O and LSE from ``forward`` and the upstream dO."""
+def backward(q, k, v, o, lse, do, causal=False, scale=None, o_residual=None):
+    """dQ, dK, dV of attention given O, LSE (and optionally O's residual) from ``forward``."""
     s = _dims(q, k, scale, causal)
     dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device)
     dv = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device)
     ws = _ws(library().fa_bwd_workspace_size(ctypes.byref(s)), q.device)
-    fa_bwd(q, k, v, o, lse, do, dq, dk, dv, s, ws)
+    fa_bwd(q, k, v, o, lse, do, dq, dk, dv, s, ws, o_residual)
     return dq, dk, dv
 
 

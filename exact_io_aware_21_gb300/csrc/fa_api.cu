@@ -244,10 +244,10 @@ int fa_get_device_status(void* ws, void* stream, int* status) {
 size_t fa_fwd_workspace_size(const fa_shape_t* s) { return check_shape(s) == FA_OK ? FA_WS_HEADER_BYTES : 0; }
 
 int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
-           const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
+           const fa_tensor_t* o_res, const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
   int rc;
   if ((rc = check_shape(s)) || (rc = check_tensor(q)) || (rc = check_tensor(k)) || (rc = check_tensor(v)) ||
-      (rc = check_tensor(o)))
+      (rc = check_tensor(o)) || (o_res && (rc = check_tensor(o_res))))
     return rc;
   if (!lse) return FA_ERR_INVALID;
   if ((rc = check_ws(ws, ws_bytes, fa_fwd_workspace_size(s)))) return rc;
@@ -263,6 +263,7 @@ int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
       (rc = make_map(&a.tm_v, v->ptr, s->B, s->Nk, s->Hkv, s->d, v->stride_b, v->stride_n, v->stride_h)))
     return rc;
   a.o = rows_of(o);
+  a.o_res = o_res ? rows_of(o_res) : OutRows{nullptr, 0, 0, 0};
   a.lse = lse;
   a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
   a.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_COUNTER_OFFSET);
@@ -280,13 +281,14 @@ size_t fa_bwd_workspace_size(const fa_shape_t* s) {
   return FA_WS_HEADER_BYTES + 2 * round_up(rows * sizeof(float), 256);
 }
 
-int fa_bwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o,
-           const float* lse, const fa_tensor_t* dout, const fa_tensor_t* dq, const fa_tensor_t* dk,
-           const fa_tensor_t* dv, const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
+static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v,
+                    const fa_tensor_t* o, const float* lse, const fa_tensor_t* o_res, const fa_tensor_t* dout,
+                    const fa_tensor_t* dq, const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* s,
+                    void* ws, size_t ws_bytes, void* stream) {
   int rc;
   if ((rc = check_shape(s)) || (rc = check_tensor(q)) || (rc = check_tensor(k)) || (rc = check_tensor(v)) ||
       (rc = check_tensor(o)) || (rc = check_tensor(dout)) || (rc = check_tensor(dq)) || (rc = check_tensor(dk)) ||
-      (rc = check_tensor(dv)))
+      (rc = check_tensor(dv)) || (o_res && (rc = check_tensor(o_res))))
     return rc;
   if (!lse) return FA_ERR_INVALID;
   if ((rc = check_ws(ws, ws_bytes, fa_bwd_workspace_size(s)))) return rc;
@@ -304,6 +306,7 @@ int fa_bwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
                      dout->stride_h)))
     return rc;
   a.o = rows_of(o);
+  a.o_res = o_res ? rows_of(o_res) : OutRows{nullptr, 0, 0, 0};
   a.dout = rows_of(dout);
   a.dq = rows_of(dq);
   a.dk = rows_of(dk);
@@ -318,9 +321,25 @@ int fa_bwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
   a.counters = reinterpret_cast<int*>(base + FA_WS_COUNTER_OFFSET);
   a.timeout_ns = g_timeout_ns;
   a.num_sms = sms;
+  a.parts = parts;
   if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
   cudaError_t e = launch_bwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
+}
+
+int fa_bwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o,
+           const float* lse, const fa_tensor_t* o_res, const fa_tensor_t* dout, const fa_tensor_t* dq,
+           const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* s, void* ws, size_t ws_bytes,
+           void* stream) {
+  return bwd_impl(7, q, k, v, o, lse, o_res, dout, dq, dk, dv, s, ws, ws_bytes, stream);
+}
+
+int fa_bwd_part(int part, const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o,
+                const float* lse, const fa_tensor_t* o_res, const fa_tensor_t* dout, const fa_tensor_t* dq,
+                const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* s, void* ws, size_t ws_bytes,
+                void* stream) {
+  if (part < 0 || part > 2) return FA_ERR_INVALID;
+  return bwd_impl(1 << part, q, k, v, o, lse, o_res, dout, dq, dk, dv, s, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------------ decode

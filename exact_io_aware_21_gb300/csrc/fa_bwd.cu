@@ -44,7 +44,7 @@ struct BwdParams {
   Dims dims;
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
-  OutRows o, dout, dq, dk, dv;
+  OutRows o, o_res, dout, dq, dk, dv;
   const float* lse;
   float* lse2;
   float* delta;
@@ -82,6 +82,18 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
       const float2 a = unpack_bf16(ou[i]), c = unpack_bf16(gu[i]);
       acc = fmaf(a.x, c.x, acc);
       acc = fmaf(a.y, c.y, acc);
+    }
+    if (p.o_res.ptr != nullptr) {  // D = dO . (O + residual)
+      const __nv_bfloat16* rr = reinterpret_cast<const __nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
+                                static_cast<int64_t>(q) * p.o_res.sn + h * p.o_res.sh + part * 8;
+      const uint4 rv = *reinterpret_cast<const uint4*>(rr);
+      const uint32_t* ru = reinterpret_cast<const uint32_t*>(&rv);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = unpack_bf16(ru[i]), c = unpack_bf16(gu[i]);
+        acc = fmaf(a.x, c.x, acc);
+        acc = fmaf(a.y, c.y, acc);
+      }
     }
   }
 #pragma unroll
@@ -709,6 +721,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   p.scale = a.scale;
   p.scale_log2 = a.scale * LOG2E;
   p.o = a.o;
+  p.o_res = a.o_res;
   p.dout = a.dout;
   p.dq = a.dq;
   p.dk = a.dk;
@@ -720,14 +733,14 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
   // 1) preprocess
-  {
+  if (a.parts & 1) {
     const int64_t threads = static_cast<int64_t>(a.dims.B) * a.dims.Hq * a.nq_pad * (D / 8);
     bwd_preprocess_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   // 2) dK / dV
-  {
+  if (a.parts & 2) {
     auto kern = bwd_dkdv_kernel<D, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<D>::ALLOC);
     if (e != cudaSuccess) return e;
@@ -738,7 +751,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // 3) dQ
-  {
+  if (a.parts & 4) {
     auto kern = bwd_dq_kernel<D, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::ALLOC);
     if (e != cudaSuccess) return e;

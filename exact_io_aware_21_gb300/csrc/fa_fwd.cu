@@ -57,6 +57,7 @@ struct FwdParams {
   Dims dims;
   float scale_log2;
   OutRows o;
+  OutRows o_res;
   float* lse;
   int* status;
   int* counter;
@@ -344,6 +345,10 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     const bool live = q_row < s.Nq;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o.ptr) + b * p.o.sb +
                           static_cast<int64_t>(q_row) * p.o.sn + h * p.o.sh;
+    __nv_bfloat16* rrow = p.o_res.ptr == nullptr
+                              ? nullptr
+                              : reinterpret_cast<__nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
+                                    static_cast<int64_t>(q_row) * p.o_res.sn + h * p.o_res.sh;
 #pragma unroll
     for (int cc = 0; cc < D / 32; ++cc) {
       uint32_t o[32];
@@ -357,6 +362,17 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
         uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      }
+      if (rrow != nullptr && live) {  // rounding residual: bf16(O - bf16(O))
+        uint32_t rz[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 hv = unpack_bf16(w[i]);
+          rz[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l - hv.x, __uint_as_float(o[2 * i + 1]) * inv_l - hv.y);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(rrow + cc * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(rz[4 * i], rz[4 * i + 1], rz[4 * i + 2], rz[4 * i + 3]);
       }
     }
     if (live) p.lse[(static_cast<int64_t>(b) * s.Hq + h) * s.Nq + q_row] = (m_run + __log2f(l_run)) * LN2;
@@ -431,6 +447,7 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   p.dims = a.dims;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.o = a.o;
+  p.o_res = a.o_res;
   p.lse = a.lse;
   p.status = a.status;
   p.counter = a.counter;

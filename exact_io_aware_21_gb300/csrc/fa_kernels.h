@@ -20,6 +20,7 @@ struct FwdLaunch {
   float scale;
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps, box 64 x 1 x 128 x 1, 128B swizzle
   OutRows o;
+  OutRows o_res;   // ptr == nullptr: residual not written
   float* lse;
   int* status;
   int* counter;
@@ -33,7 +34,7 @@ struct BwdLaunch {
   int d;
   float scale;
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
-  OutRows o, dout, dq, dk, dv;
+  OutRows o, o_res, dout, dq, dk, dv;  // o_res.ptr may be nullptr
   const float* lse;
   float* lse2;     // workspace [B*Hq, Nq_pad] : LSE * log2(e)  (+inf in padding)
   float* delta;    // workspace [B*Hq, Nq_pad] : D = rowsum(dO o O)
@@ -42,6 +43,7 @@ struct BwdLaunch {
   int* counters;   // [2]
   unsigned long long timeout_ns;
   int num_sms;
+  int parts;       // bit 0: preprocess, bit 1: dK/dV, bit 2: dQ
 };
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st);
 

@@ -90,11 +90,15 @@ typedef struct {
  *   k,v [B, Nk, Hkv, d] in
  *   o   [B, Nq, Hq, d]  out (bf16, round to nearest even)
  *   lse [B, Hq, Nq]     out (fp32, contiguous)
+ *   o_residual [B, Nq, Hq, d]  optional out (NULL = not written): the bf16
+ *       rounding residual of O, i.e. bf16(O_fp32 - O).  O + o_residual carries
+ *       about 16 significant bits; fa_bwd uses it for D (see there).
  * Needs fa_fwd_workspace_size(shape) bytes of workspace (16-byte aligned).
  * ------------------------------------------------------------------------- */
 size_t fa_fwd_workspace_size(const fa_shape_t* shape);
 int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
-           const fa_shape_t* shape, void* workspace, size_t workspace_bytes, void* stream);
+           const fa_tensor_t* o_residual, const fa_shape_t* shape, void* workspace, size_t workspace_bytes,
+           void* stream);
 
 /* ---------------------------------------------------------------------------
  * Backward.  §18.4.4: P rebuilt per tile from the saved statistics with no
@@ -106,12 +110,27 @@ int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
  * kernels, no atomics: preprocess (D), dK/dV (one key tile per work unit),
  * dQ (one query tile per work unit); results are deterministic.
  *   q, o, dout [B, Nq, Hq, d] in;  k, v [B, Nk, Hkv, d] in;  lse in (from fa_fwd)
+ *   o_residual  optional in (NULL = none): the residual written by fa_fwd.
+ *       D is then dO . (O + o_residual).  Without it D is dO . O with O in
+ *       bf16; when attention is nearly one-hot, dP - D is a difference of
+ *       nearly equal terms and O's rounding shows up in dQ and dK (a few
+ *       percent on inputs with outlier channels).
  *   dq [B, Nq, Hq, d] out;  dk, dv [B, Nk, Hkv, d] out  (bf16)
  * ------------------------------------------------------------------------- */
 size_t fa_bwd_workspace_size(const fa_shape_t* shape);
 int fa_bwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o,
-           const float* lse, const fa_tensor_t* dout, const fa_tensor_t* dq, const fa_tensor_t* dk,
-           const fa_tensor_t* dv, const fa_shape_t* shape, void* workspace, size_t workspace_bytes, void* stream);
+           const float* lse, const fa_tensor_t* o_residual, const fa_tensor_t* dout, const fa_tensor_t* dq,
+           const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* shape, void* workspace,
+           size_t workspace_bytes, void* stream);
+/* The three backward launches one at a time, for callers that time or
+ * schedule them separately: part 0 = preprocess (D and the padded LSE, kept in
+ * the workspace), 1 = dK/dV, 2 = dQ.  Parts 1 and 2 read what part 0 left in
+ * the same workspace; running parts 0, 1, 2 in order on one stream is exactly
+ * fa_bwd.  Same arguments and errors as fa_bwd; FA_ERR_INVALID for another part. */
+int fa_bwd_part(int part, const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o,
+                const float* lse, const fa_tensor_t* o_residual, const fa_tensor_t* dout, const fa_tensor_t* dq,
+                const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* shape, void* workspace,
+                size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Split-KV decode (FlashDecoding).  §18.8.2: the KV cache is cut along its

@@ -110,12 +110,14 @@ def attention_forward(q, k, v, scale, causal=False, row_block=2048, heads=None, 
     return o, lse
 
 
-def attention_backward(q, k, v, do, scale, causal=False, row_block=1024, heads=None):
+def attention_backward(q, k, v, do, scale, causal=False, row_block=1024, heads=None, rows=None):
     """Plain attention backward with S and P materialised.
 
     Returns (dQ [B,Nq,Hq,d], dK [B,Nk,Hkv,d], dV [B,Nk,Hkv,d]).  With ``heads``
     given, only those query heads contribute (dQ of other heads is NaN and dK/dV
-    hold only the listed heads' contributions).
+    hold only the listed heads' contributions).  With ``rows`` given, only those
+    query rows are processed: dQ of other rows is NaN and dK/dV hold the sum of
+    the listed rows' contributions (dK and dV are sums over query rows).
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, Nq, Nk, Hq, Hkv, d = _check_shapes(q, k, v)
@@ -130,8 +132,9 @@ def attention_backward(q, k, v, do, scale, causal=False, row_block=1024, heads=N
     for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(Hq)]):
         kv = h // g
         Kh, Vh = k[b, :, kv, :], v[b, :, kv, :]
-        for r0 in range(0, Nq, row_block):
-            rr = np.arange(r0, min(Nq, r0 + row_block))
+        all_rows = np.arange(Nq) if rows is None else np.asarray(rows)
+        for r0 in range(0, len(all_rows), row_block):
+            rr = all_rows[r0:r0 + row_block]
             Qr, dOr = q[b, rr, h, :], do[b, rr, h, :]
             S = _scores(Qr, Kh, scale, rr, causal)
             P, _, _ = _softmax_rows(S)

@@ -120,17 +120,21 @@ def test_invalid_shapes_rejected_before_any_gpu_work(lib, bad):
     s = shape(**kw)
     if bad.get("scale", 1.0) != bad.get("scale", 1.0) or "scale" in bad:
         s.scale = bad["scale"]
-    rc = lib.fa_fwd(tens(), tens(), tens(), tens(), FAKE, ctypes.byref(s), FAKE, 1 << 20, None)
+    rc = lib.fa_fwd(tens(), tens(), tens(), tens(), FAKE, None, ctypes.byref(s), FAKE, 1 << 20, None)
     assert rc == 1  # FA_ERR_INVALID
 
 
 def test_misaligned_and_workspace_errors(lib):
     s = ctypes.byref(shape(1, 2, 2, 16, 16, 64))
-    assert lib.fa_fwd(tens(FAKE + 2), tens(), tens(), tens(), FAKE, s, FAKE, 1 << 20, None) == 2
-    assert lib.fa_fwd(tens(sn=12), tens(), tens(), tens(), FAKE, s, FAKE, 1 << 20, None) == 2
-    assert lib.fa_fwd(tens(), tens(), tens(), tens(), FAKE, s, FAKE, 8, None) == 3
-    assert lib.fa_fwd(tens(), tens(), tens(), tens(), None, s, FAKE, 1 << 20, None) == 1
-    assert lib.fa_fwd(None, tens(), tens(), tens(), FAKE, s, FAKE, 1 << 20, None) == 1
+    assert lib.fa_fwd(tens(FAKE + 2), tens(), tens(), tens(), FAKE, None, s, FAKE, 1 << 20, None) == 2
+    assert lib.fa_fwd(tens(sn=12), tens(), tens(), tens(), FAKE, None, s, FAKE, 1 << 20, None) == 2
+    assert lib.fa_fwd(tens(), tens(), tens(), tens(), FAKE, None, s, FAKE, 8, None) == 3
+    assert lib.fa_fwd(tens(), tens(), tens(), tens(), FAKE, tens(FAKE + 4), s, FAKE, 1 << 20, None) == 2
+    assert lib.fa_fwd(tens(), tens(), tens(), tens(), None, None, s, FAKE, 1 << 20, None) == 1
+    assert lib.fa_fwd(None, tens(), tens(), tens(), FAKE, None, s, FAKE, 1 << 20, None) == 1
+    # bwd_part: unknown part
+    assert lib.fa_bwd_part(3, tens(), tens(), tens(), tens(), FAKE, None, tens(), tens(), tens(), tens(), s, FAKE,
+                           1 << 20, None) == 1
     # decode: causal and too many packed rows are rejected
     sd = shape(1, 32, 1, 1, 100, 64)
     assert lib.fa_decode(tens(), tens(), tens(), tens(), FAKE, ctypes.byref(sd), 1, FAKE, 1 << 30, None) == 1

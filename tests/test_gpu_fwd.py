@@ -66,11 +66,11 @@ def test_selftest_pv_form(n):
 
 
 # ------------------------------------------------------------------ small shapes
-def run_fwd(x, causal, scale):
+def run_fwd(x, causal, scale, residual=False):
     q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
-    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    out = fa.forward(q, k, v, causal=causal, scale=scale, residual=residual)
     torch.cuda.synchronize()
-    return o, lse
+    return out
 
 
 def test_tiny_workload():
@@ -135,6 +135,21 @@ def test_causal_mask_bit_exact(N, d):
     assert np.array_equal(np.rint(np.exp(f64(lse))).astype(np.int64), np.full((B, H, N), N))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_residual_output(d):
+    """The optional residual is bf16(O_fp32 - O): O + residual tracks the oracle far
+    beyond bf16, and asking for it leaves O and LSE unchanged."""
+    x = inputs.shape_inputs(1, 2, 1, 500, 500, d, seed=21, with_do=False)
+    o1, l1 = run_fwd(x, True, 0.1)
+    o, lse, res = run_fwd(x, True, 0.1, residual=True)
+    assert torch.equal(o, o1) and torch.equal(lse, l1)
+    o_ref, lse_ref = A.attention_forward(x["q"], x["k"], x["v"], 0.1, True)
+    assert_fwd(o, lse, o_ref, lse_ref, "residual", o_res=res)
+    err_hi = np.abs(f64(o) - o_ref).max()
+    err_lo = np.abs(f64(o) + f64(res) - o_ref).max()
+    assert err_lo < err_hi / 8
+
+
 def test_deterministic():
     x = inputs.shape_inputs(1, 4, 2, 1000, 1000, 128, seed=3, with_do=False)
     a = run_fwd(x, True, 0.1)
@@ -145,13 +160,14 @@ def test_deterministic():
 # ------------------------------------------------------------------ full-size workloads
 def sampled_check(w, n_heads=3, n_rows=96, seed=11):
     x = inputs.make(w, with_do=False)
-    o, lse = run_fwd(x, w.causal, w.scale)
+    o, lse, res = run_fwd(x, w.causal, w.scale, residual=True)
     rng = np.random.default_rng(seed)
     heads = [(int(rng.integers(w.B)), int(rng.integers(w.Hq))) for _ in range(n_heads)]
     rows = np.unique(np.concatenate([[0, 1, 127, 128, w.Nq - 1], rng.integers(0, w.Nq, n_rows)]))
     o_ref, lse_ref = A.attention_forward(x["q"], x["k"], x["v"], w.scale, w.causal, heads=heads, rows=rows)
     for b, h in heads:
-        assert_fwd(o[b, rows, h], lse[b, h, rows], o_ref[b, rows, h], lse_ref[b, h, rows], f"{w.name} b{b} h{h}")
+        assert_fwd(o[b, rows, h], lse[b, h, rows], o_ref[b, rows, h], lse_ref[b, h, rows], f"{w.name} b{b} h{h}",
+                   o_res=res[b, rows, h])
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
 
 

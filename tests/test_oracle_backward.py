@@ -122,3 +122,16 @@ def test_row_block_does_not_change_result():
     b = A.attention_backward(q, k, v, do, 0.3, True, row_block=1000)
     for x, y in zip(a, b):
         np.testing.assert_allclose(x, y, atol=1e-13)
+
+
+def test_row_restriction_sums_to_full():
+    """dK, dV are sums over query rows: two disjoint row sets add up to the full result."""
+    q, k, v, do = rand(1, 40, 2, 8), rand(1, 40, 1, 8), rand(1, 40, 1, 8), rand(1, 40, 2, 8)
+    full = A.attention_backward(q, k, v, do, 0.3, True)
+    a = A.attention_backward(q, k, v, do, 0.3, True, rows=np.arange(0, 13))
+    b = A.attention_backward(q, k, v, do, 0.3, True, rows=np.arange(13, 40), row_block=5)
+    np.testing.assert_allclose(a[1] + b[1], full[1], atol=1e-13)
+    np.testing.assert_allclose(a[2] + b[2], full[2], atol=1e-13)
+    np.testing.assert_allclose(a[0][:, :13], full[0][:, :13], atol=1e-14)
+    np.testing.assert_allclose(b[0][:, 13:], full[0][:, 13:], atol=1e-14)
+    assert np.isnan(a[0][:, 13:]).all()

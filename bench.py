@@ -1,0 +1,538 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on GB300; prints ONE JSON line.
+
+A step is one pass of the whole hot path over synthetic inputs already resident
+in HBM:
+  training legs  forward + backward (preprocess, dK/dV, dQ) of
+                 causal_b2_h16_n4096_d128   (B=2, H=16, N=4096, d=128, causal)
+                 gqa_causal_b1_hq32_hkv8_n8192_d128_outliers
+  decode legs    split-KV decode + combine of
+                 decode_b8_hq32_hkv8_q1_kv131072_d128 and the q4 variant
+``value`` = counted forward + backward FLOPs of the training legs divided by
+their device time (TFLOPS; forward 4*B*H*Nq*Nk*d, halved when causal, backward
+2.5x that).  Decode legs report KV-read GB/s.  L2 is flushed (256 MiB write)
+before every launch group, outside its events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+data (weak scaling, no collective on the data path); the step time is the max
+over ranks and rank 0 prints.  ``--impl reference`` times the fp64 CPU oracle on
+this host's cores on a bounded sample of the same workloads.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+TRAIN = ("causal_b2_h16_n4096_d128", "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers")
+DECODE = ("decode_b8_hq32_hkv8_q1_kv131072_d128", "decode_b8_hq32_hkv8_q4_kv131072_d128")
+WORKLOAD = " + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode)"
+METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------- helpers
+def workloads():
+    from exact_io_aware_21_gb300 import inputs
+
+    by = {w.name: w for w in inputs.ALL}
+    return [by[n] for n in TRAIN], [by[n] for n in DECODE]
+
+
+def fwd_flops(w):
+    f = 4.0 * w.B * w.Hq * w.Nq * w.Nk * w.d
+    return f / 2 if w.causal else f
+
+
+def kv_bytes(w):
+    return 2.0 * w.B * w.Hkv * w.Nk * w.d * 2
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def aggregate(local_ms, local_work, world):
+    """(max over ranks of the step time, sum over ranks of the work)."""
+    if world <= 1:
+        return local_ms, local_work
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    w = torch.tensor([local_work], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(w, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(w.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples, kept for a time window."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_id), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    @staticmethod
+    def _num(x):
+        try:
+            return float(x)
+        except ValueError:
+            return None
+
+    def summary(self, t0, t1):
+        rows = [s for t, s in self.samples if t0 <= t <= t1 + 0.15 and len(s) >= 7]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [self._num(r[0]) for r in rows if self._num(r[0]) is not None]
+        reasons = sorted({self.NAMES[i] for r in rows for i in range(4) if r[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self._num(rows[0][1]),
+                "power_w_max": max((self._num(r[2]) or 0.0) for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def gpu_id_for(device):
+    try:
+        return f"GPU-{torch.cuda.get_device_properties(device).uuid}"
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[device.index or 0] if vis else (device.index or 0)
+
+
+# ----------------------------------------------------------------------------- oracle samples
+_SAMPLE_CACHE = {}
+
+
+def _head_inputs(w):
+    """Head (0, 0) of the workload's inputs (the same seeded recipe), as numpy."""
+    if w.name not in _SAMPLE_CACHE:
+        from exact_io_aware_21_gb300 import inputs
+
+        x = inputs.make(w)
+        kvh = 0
+        _SAMPLE_CACHE[w.name] = {
+            "q": x["q"][:1, :, :1].float().numpy(), "k": x["k"][:1, :, kvh:kvh + 1].float().numpy(),
+            "v": x["v"][:1, :, kvh:kvh + 1].float().numpy(), "do": x["do"][:1, :, :1].float().numpy()}
+    return _SAMPLE_CACHE[w.name]
+
+
+def oracle_sample_step(w, rows):
+    """fp64 oracle forward + backward of head (0, 0) restricted to query ``rows``.
+
+    Returns the counted FLOPs of that share of the workload: the workload's
+    counted fwd+bwd FLOPs times the fraction of visible (row, key) pairs covered.
+    """
+    from oracle import attention as A
+
+    x = _head_inputs(w)
+    A.attention_forward(x["q"], x["k"], x["v"], w.scale, w.causal, rows=rows)
+    A.attention_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, rows=rows)
+    vis = sum(int(r) + 1 for r in rows) if w.causal else len(rows) * w.Nk
+    total = (w.Nq * (w.Nq + 1) / 2 if w.causal else w.Nq * w.Nk) * w.B * w.Hq
+    return 3.5 * fwd_flops(w) * vis / total
+
+
+def rows_for(w, seconds, probe=256):
+    """Number of (longest) query rows of one head whose oracle fwd+bwd takes ~``seconds``."""
+    import numpy as np
+
+    t0 = time.perf_counter()
+    oracle_sample_step(w, np.arange(w.Nq - probe, w.Nq))
+    dt = time.perf_counter() - t0
+    return int(max(32, min(w.Nq, probe * seconds / max(dt, 1e-6))))
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_run(train, seconds_per_step, steps, warmup):
+    """Time ``steps`` oracle steps; each step = a row block of head (0,0) of every training workload."""
+    import numpy as np
+
+    n = {w.name: rows_for(w, seconds_per_step / len(train)) for w in train}
+    times, flops = [], 0.0
+    for i in range(warmup + steps):
+        t0 = time.perf_counter()
+        f = 0.0
+        for w in train:
+            m = n[w.name]
+            r0 = (w.Nq - m) - (i * m) % max(1, w.Nq - m + 1)
+            f += oracle_sample_step(w, np.arange(r0, r0 + m))
+        dt = time.perf_counter() - t0
+        if i >= warmup:
+            times.append(dt)
+            flops += f
+    desc = ", ".join(f"{w.name}: {n[w.name]} query rows of head (0,0)" for w in train)
+    return flops / sum(times) / 1e12, sum(times) / steps, desc
+
+
+def run_cpu_baseline(train, budget_s):
+    value, _, desc = oracle_run(train, budget_s, 1, 0)
+    return {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{desc}; fwd+bwd in fp64 numpy, about {budget_s:.0f} s"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    _, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    train, _ = workloads()
+    per_step = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
+    value, s_per_step, desc = oracle_run(train, per_step, args.steps, args.warmup)
+    cpu = {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+           "sample": f"per step {desc}; fwd+bwd in fp64 numpy"}
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), bf16-rounded; outlier channel x20 in the GQA workload)",
+        "config": {"workload": WORKLOAD, "sample": f"per step: {desc}, fwd+bwd (decode legs not sampled)",
+                   "parallelism": "host cores"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+class Leg:
+    def __init__(self, name, kind, w, fns, work):
+        self.name, self.kind, self.w, self.fns, self.work = name, kind, w, fns, work
+        self.ms = {k: 0.0 for k, _ in fns}
+
+
+KERNELS_PER_CALL = {"fwd": 1, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2}
+
+
+def kernel_flops(part, w):
+    """Algorithmic FLOPs of one launch: the counted matmuls that launch performs.
+
+    forward: S = QK^T and O = PV; dK/dV: S^T, dP^T, dV, dK (4 of the 5 backward
+    matmuls); dQ: the dQ matmul only (its recomputed S and dP are not counted)."""
+    f = fwd_flops(w)
+    return {"fwd": f, "bwd_dkdv": 2.0 * f, "bwd_dq": 0.5 * f}.get(part)
+
+
+def make_legs(device, seed):
+    import ctypes
+
+    import exact_io_aware_21_gb300 as fa
+    from exact_io_aware_21_gb300 import binding as B
+    from exact_io_aware_21_gb300 import inputs
+
+    lib = fa.library()
+    train, dec = workloads()
+    legs, state = [], {}
+    for w in train:
+        x = inputs.make(w, device=device, seed=w.seed + seed)
+        s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal)
+        st = dict(x=x, s=s, o=torch.empty_like(x["q"]), ores=torch.empty_like(x["q"]),
+                  lse=torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=device),
+                  dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
+                  wsf=torch.zeros(lib.fa_fwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=device),
+                  wsb=torch.zeros(lib.fa_bwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=device))
+        state[w.name] = st
+
+        def fwd(st=st):
+            x = st["x"]
+            B.fa_fwd(x["q"], x["k"], x["v"], st["o"], st["lse"], st["s"], st["wsf"], st["ores"])
+
+        def part(i, st=st):
+            x = st["x"]
+            B.fa_bwd_part(i, x["q"], x["k"], x["v"], st["o"], st["lse"], x["do"], st["dq"], st["dk"], st["dv"],
+                          st["s"], st["wsb"], st["ores"])
+
+        fns = [("fwd", fwd), ("bwd_pre", lambda part=part: part(0)), ("bwd_dkdv", lambda part=part: part(1)),
+               ("bwd_dq", lambda part=part: part(2))]
+        legs.append(Leg(w.name, "train", w, fns, 3.5 * fwd_flops(w)))
+    for w in dec:
+        x = inputs.make(w, device=device, with_do=False, seed=w.seed + seed)
+        s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, False)
+        S = lib.fa_decode_num_splits(ctypes.byref(s), 0)
+        st = dict(x=x, s=s, S=S, o=torch.empty_like(x["q"]),
+                  lse=torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=device),
+                  ws=torch.zeros(lib.fa_decode_workspace_size(ctypes.byref(s), S), dtype=torch.uint8,
+                                 device=device))
+        state[w.name] = st
+
+        def dec_fn(st=st):
+            x = st["x"]
+            B.fa_decode(x["q"], x["k"], x["v"], st["o"], st["lse"], st["s"], st["S"], st["ws"])
+
+        legs.append(Leg(w.name, "decode", w, [("decode", dec_fn)], kv_bytes(w)))
+    return legs, state
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            ent = json.load(f)[kernel][workload]
+        src = os.path.join(ROOT, "exact_io_aware_21_gb300", "csrc", ent["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return ent["bytes_per_launch"] if sha == ent["source_sha256_16"] else None
+    except Exception:
+        return None
+
+
+def run_e2e(legs, state, device, steps, world):
+    """Training legs through the public API with host buffers: H2D inputs, fwd, bwd, D2H grads."""
+    from exact_io_aware_21_gb300 import binding as B
+
+    host, h2d, d2h = {}, 0, 0
+    for l in legs:
+        if l.kind != "train":
+            continue
+        st = state[l.name]
+        src = {k: v for k, v in st["x"].items() if torch.is_tensor(v)}
+        hx = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in src.items()}
+        for k in hx:
+            hx[k].copy_(src[k])
+        hg = {k: torch.empty(st[k].shape, dtype=st[k].dtype, pin_memory=True) for k in ("dq", "dk", "dv")}
+        dx = {k: torch.empty_like(v) for k, v in src.items()}
+        host[l.name] = (hx, hg, dx)
+        h2d += sum(t.numel() * t.element_size() for t in hx.values())
+        d2h += sum(t.numel() * t.element_size() for t in hg.values())
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        for l in legs:
+            if l.kind != "train":
+                continue
+            st = state[l.name]
+            hx, hg, dx = host[l.name]
+            for k in hx:
+                dx[k].copy_(hx[k], non_blocking=True)
+            B.fa_fwd(dx["q"], dx["k"], dx["v"], st["o"], st["lse"], st["s"], st["wsf"], st["ores"])
+            B.fa_bwd(dx["q"], dx["k"], dx["v"], st["o"], st["lse"], dx["do"], st["dq"], st["dk"], st["dv"], st["s"],
+                     st["wsb"], st["ores"])
+            for k in hg:
+                hg[k].copy_(st[k], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms, flops = aggregate(e0.elapsed_time(e1) / steps, sum(l.work for l in legs if l.kind == "train"), world)
+    return {"value": flops / ms / 1e9, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms,
+            "what": "fwd+bwd of the training workloads via fa_fwd/fa_bwd with pinned host inputs and gradients"}
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    import exact_io_aware_21_gb300 as fa
+
+    fa.library()  # raises if the CUDA library is not built: there is no fallback
+    peaks, peak_src = load_peaks()
+    legs, state = make_legs(device, seed=1000 * rank)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    def one_step(record):
+        for leg in legs:
+            for part, fn in leg.fns:
+                flush.fill_(1)
+                if record is None:
+                    fn()
+                    continue
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                record.append((leg, part, e0, e1))
+
+    for _ in range(args.warmup):
+        one_step(None)
+    torch.cuda.synchronize()
+    for st in state.values():  # every workspace must report a clean device status
+        for key in ("wsf", "wsb", "ws"):
+            if key in st:
+                rc, bits = fa.binding.device_status(st[key])
+                if rc != 0:
+                    raise RuntimeError(f"device status {bits:#x} after warm-up")
+
+    sampler = ClockSampler(gpu_id_for(device)) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    recs = []
+    for _ in range(args.steps):
+        one_step(recs)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall1 = time.time()
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    for leg, part, e0, e1 in recs:
+        leg.ms[part] += e0.elapsed_time(e1) / args.steps
+    leg_ms = {l.name: sum(l.ms.values()) for l in legs}
+    step_ms = sum(leg_ms.values())
+    train_ms = sum(leg_ms[l.name] for l in legs if l.kind == "train")
+    max_train_ms, total_flops = aggregate(train_ms, sum(l.work for l in legs if l.kind == "train"), world)
+    max_step_ms, _ = aggregate(step_ms, 0.0, world)
+    sus = peaks["bf16_tflops_sustained"]
+
+    legs_out = {}
+    for l in legs:
+        if l.kind == "train":
+            f = fwd_flops(l.w)
+            bwd_ms = l.ms["bwd_pre"] + l.ms["bwd_dkdv"] + l.ms["bwd_dq"]
+            legs_out[l.name] = {
+                "fwd_ms": l.ms["fwd"], "fwd_tflops": f / l.ms["fwd"] / 1e9,
+                "fwd_frac_of_sustained_peak": f / l.ms["fwd"] / 1e9 / sus,
+                "bwd_ms": bwd_ms, "bwd_tflops": 2.5 * f / bwd_ms / 1e9,
+                "bwd_frac_of_sustained_peak": 2.5 * f / bwd_ms / 1e9 / sus,
+                "bwd_parts_ms": {k: l.ms[k] for k in ("bwd_pre", "bwd_dkdv", "bwd_dq")}}
+        else:
+            ms = l.ms["decode"]
+            legs_out[l.name] = {"ms": ms, "gbs": l.work / ms / 1e6, "frac_of_hbm_peak": l.work / ms / 1e6 /
+                                peaks["hbm_gbs"], "num_splits": state[l.name]["S"]}
+
+    # roofline of the dominant kernel: the launch with the largest share of the step
+    dl, dp = max(((l, p) for l in legs for p, _ in l.fns if p != "bwd_pre"), key=lambda lp: lp[0].ms[lp[1]])
+    if dp == "decode":
+        ach = dl.work / dl.ms[dp] / 1e6
+        roof = {"kernel": "fa_decode_split_kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": ach / peaks["hbm_gbs"]}
+    else:
+        ach = kernel_flops(dp, dl.w) / dl.ms[dp] / 1e9
+        kname = {"fwd": "fa_fwd_kernel", "bwd_dkdv": "bwd_dkdv_kernel", "bwd_dq": "bwd_dq_kernel"}[dp]
+        roof = {"kernel": kname, "bound": "tensor", "achieved": ach, "peak": sus, "unit": "TFLOP/s",
+                "frac": ach / sus, "frac_of_burst_peak": ach / peaks["bf16_tflops"]}
+    roof.update({"workload": dl.name, "share_of_step": dl.ms[dp] / step_ms,
+                 "peak_source": f"{peak_src}: " + ("MEASURED_PEAKS.json" if peak_src == "measured"
+                                                   else "profiling-recipe fallback"),
+                 "traffic": traffic_for(roof["kernel"], dl.name)})
+
+    e2e = run_e2e(legs, state, device, args.steps, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline([l.w for l in legs if l.kind == "train"], args.cpu_seconds)
+
+    line = {
+        "metric": METRIC,
+        "value": total_flops / max_train_ms / 1e9,
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": max_step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), bf16-rounded; outlier channel x20 in the GQA workload)",
+        "config": {
+            "workload": WORKLOAD,
+            "value_counts": "fwd+bwd FLOPs of the two training workloads / their device time",
+            "l2": "flushed (256 MiB write) before every launch group, outside its events",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "legs": legs_out,
+        },
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * sum(KERNELS_PER_CALL[p] for l in legs for p, _ in l.fns),
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description="exact attention hot-path benchmark (one JSON line)")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    return run_reference(args) if args.impl == "reference" else run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -523,7 +523,7 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description="exact attention hot-path benchmark (one JSON line)")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

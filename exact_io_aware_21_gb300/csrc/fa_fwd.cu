@@ -21,9 +21,12 @@
 // TMEM (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,256+d) O_1 [256+d,256+2d);
 // P_t is written as bf16 over the first 64 columns of S_t and read from TMEM by
 // the P V product.
-// Rescaling is skipped while the running max has grown by at most TAU (log2
-// units): the stale max stays the reference for both O and l, so the result is
-// unchanged (lecture slides 51-52 describe skipping most rescalings).
+// The running max is the exact row max so far (TAU = 0): the dominant P of a
+// nearly one-hot row is then exactly 1.0 in bf16, so O's error scales with the
+// rest of the row, which keeps D = dO . O consistent in the backward.  The
+// rescale of O is skipped for a warp whose 32 rows kept their max.  (A stale
+// reference within TAU > 0 of the max, as lecture slides 51-52 describe, is
+// exact for O / l but rounds the dominant P; see the design notes.)
 #include <math.h>
 
 #include "fa_kernels.h"
@@ -32,7 +35,7 @@
 namespace fa {
 namespace {
 
-constexpr float TAU = 8.0f;
+constexpr float TAU = 0.0f;
 constexpr float LN2 = 0.69314718055994530942f;
 
 template <int D>

@@ -54,6 +54,8 @@ SIGNATURES = {
     "fa_decode_workspace_size": (_SZ, [_PS, _I]),
     "fa_decode": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _I, _VP, _SZ, _VP]),
     "fa_decode_partials_layout": (_I, [_PS, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
+    "fa_decode_noalloc_max_bytes": (_SZ, []),
+    "fa_decode_noalloc": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _I, _VP]),
     "fa_get_device_status": (_I, [_VP, _VP, _PI]),
     "fa_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
     "fa_strerror": (ctypes.c_char_p, [_I]),

@@ -171,6 +171,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_LAUNCH: return "kernel launch failed";
     case FA_ERR_TIMEOUT: return "a device-side bounded wait ran out";
     case FA_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case FA_ERR_TOO_LARGE: return "problem needs more scratch than the fixed no-allocation array holds";
     default: return "unknown error";
   }
 }

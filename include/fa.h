@@ -58,7 +58,8 @@ enum {
   FA_ERR_ARCH = 4,      /* current device is not sm_103 */
   FA_ERR_LAUNCH = 5,    /* a kernel launch failed (the CUDA error is in fa_last_cuda_error) */
   FA_ERR_TIMEOUT = 6,   /* a device-side bounded wait ran out (see fa_get_device_status) */
-  FA_ERR_CUDA = 7       /* another CUDA runtime/driver call failed */
+  FA_ERR_CUDA = 7,      /* another CUDA runtime/driver call failed */
+  FA_ERR_TOO_LARGE = 8  /* the problem needs more scratch than fa_decode_noalloc's fixed array holds */
 };
 
 typedef struct {
@@ -155,6 +156,35 @@ int fa_decode(const fa_tensor_t* q, const fa_tensor_t* kcache, const fa_tensor_t
  * tests): lse_part [B, Hq, Nq, S] fp32 (natural log) and o_part
  * [B, Hq, Nq, S, d] fp32 (normalised by the split's own sum).  Byte offsets. */
 int fa_decode_partials_layout(const fa_shape_t* shape, int num_splits, size_t* lse_offset, size_t* o_offset);
+
+/* ---------------------------------------------------------------------------
+ * Decode without allocation.  No counterpart on the pages: this is a service
+ * to callers that cannot allocate device memory, such as an inference server
+ * that reserves all device memory for its own pool at start-up and forbids
+ * later cudaMalloc calls (they synchronise the device and fragment the pool),
+ * or a plug-in that receives only the tensors of the call.
+ * fa_decode_noalloc computes exactly what fa_decode computes, with the same
+ * arguments minus the workspace: its scratch (the per-split partials and the
+ * status header) lives in one array of FA_DECODE_SCRATCH_BYTES compiled into
+ * the library, which every GPU that loads the library holds until the process
+ * exits.  The library allocates nothing in this call.
+ *  - Limit: fa_decode_workspace_size(shape, num_splits) must not exceed
+ *    FA_DECODE_SCRATCH_BYTES (8 MiB; for d = 128 about
+ *    B*Hq*Nq*splits*516 bytes); otherwise the call returns FA_ERR_TOO_LARGE
+ *    and enqueues nothing.  Request fewer splits to fit.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array, which keeps the last call's contents.
+ *    Calls whose work overlaps on the GPU (other streams, other host threads)
+ *    race on it: order them on one stream.
+ *  - fa_get_device_status() cannot reach this array; a timed-out wait still
+ *    ends the kernels, but its status bit is not reported.
+ * ------------------------------------------------------------------------- */
+#define FA_DECODE_SCRATCH_BYTES ((size_t)8 << 20)
+size_t fa_decode_noalloc_max_bytes(void);
+int fa_decode_noalloc(const fa_tensor_t* q, const fa_tensor_t* kcache, const fa_tensor_t* vcache,
+                      const fa_tensor_t* o, float* lse, const fa_shape_t* shape, int num_splits, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Device status.  Synchronises `stream`, returns the error bits the kernels

@@ -20,9 +20,14 @@
 //   dQ          a unit is one 128-row query tile; it loops over key tiles.
 //               TMEM: S double-buffered [0,256), dP [256,384), dQ [384,384+d);
 //               dS is written over dP as bf16 and feeds dQ += dS K.
-// Warp roles as in the forward kernel: warp 0 loads with TMA, one thread of
-// warp 1 issues tcgen05 MMAs, warps 4-7 do the elementwise work with one TMEM
-// lane (one row) per thread.
+// Warp roles: warp 0 loads with TMA, one thread of warp 1 issues tcgen05 MMAs,
+// and two warpgroups (warps 4-7 and 8-11) do the elementwise work: both hold
+// the same 128 rows (one TMEM lane per thread) and split the 128 columns,
+// warpgroup 0 taking columns 0-63 and warpgroup 1 columns 64-127.  Each writes
+// its bf16 half (P^T or dS) back into TMEM columns it has itself already read:
+// the half for columns 0-63 at column offset 0, the half for 64-127 at offset
+// 64, so the two warpgroups never wait for each other; the MMAs that read that
+// operand from TMEM address its second half 64 columns on.
 #include <math.h>
 
 #include "fa_kernels.h"
@@ -115,21 +120,27 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a_base, uint3
   }
 }
 
-// D[128 x D] (+)= A[tmem, 128 x 128 bf16] * B[smem tile 128 x D, N-major]
+// D[128 x D] (+)= A[tmem, 128 x 128 bf16] * B[smem tile 128 x D, N-major].
+// A's K columns 0-63 are packed at TMEM columns [0, 32), K columns 64-127 at
+// [64, 96) (one half per elementwise warpgroup).
 template <int D>
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, bool acc) {
   constexpr uint32_t IDESC = idesc_bf16(128, D, false, true);
 #pragma unroll
   for (int k = 0; k < TILE / 16; ++k)
-    mma_ts(d_tmem, a_tmem + k * 8, sdesc_sw128(b_base + k * 16 * 128, TILE * 128, 1024), IDESC,
-           (acc || k > 0) ? 1u : 0u);
+    mma_ts(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), sdesc_sw128(b_base + k * 16 * 128, TILE * 128, 1024),
+           IDESC, (acc || k > 0) ? 1u : 0u);
 }
 
-// store one 128-column... row of D fp32 accumulator columns as bf16 (times mul)
-template <int D>
-__device__ __forceinline__ void store_row_bf16(uint32_t t_acc, float mul, __nv_bfloat16* dst, bool live) {
+// Store columns [col0, col0 + NC) of a row of fp32 accumulator columns as bf16
+// (times mul); dst points at the row's first element.
+template <int NC>
+__device__ __forceinline__ void store_cols_bf16(uint32_t t_acc, int col0, float mul, __nv_bfloat16* dst,
+                                                bool live) {
+  dst += col0;
+  t_acc += col0;
 #pragma unroll
-  for (int cc = 0; cc < D / 32; ++cc) {
+  for (int cc = 0; cc < NC / 32; ++cc) {
     uint32_t v[32];
     tmem_ld32(t_acc + cc * 32, v);
     uint32_t w[16];
@@ -198,7 +209,7 @@ __device__ __forceinline__ DkvUnit dkv_decode(const Dims& s, int u) {
 }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdParams p) {
@@ -216,7 +227,7 @@ __global__ void __launch_bounds__(256, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.unit_full[i], 1);
-      mbar_init(&bar.unit_empty[i], 1 + 128);
+      mbar_init(&bar.unit_empty[i], 1 + 256);
     }
     mbar_init(bar.kv_full, 1);
     mbar_init(bar.kv_empty, 1);
@@ -226,8 +237,8 @@ __global__ void __launch_bounds__(256, 1)
     }
     mbar_init(bar.s_full, 1);
     mbar_init(bar.dp_full, 1);
-    mbar_init(bar.p_full, 128);
-    mbar_init(bar.ds_full, 128);
+    mbar_init(bar.p_full, 256);
+    mbar_init(bar.ds_full, 256);
     mbar_init(bar.acc_full, 1);
     fence_barrier_init();
   }
@@ -345,7 +356,8 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp >= 4) {  // -------------------------------------------------- gradient warps
     const int wq = warp & 3;
-    const int r = wq * 32 + lane_id();  // key row within the tile
+    const int c0 = ((warp - 4) >> 2) * 64;  // this warpgroup's first column
+    const int r = wq * 32 + lane_id();      // key row within the tile
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lanes, tP = tmem + lanes + 128, tdV = tmem + lanes + 256,
                    tdK = tmem + lanes + 256 + D;
@@ -376,17 +388,17 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         // P^T[key, query] = exp2(S * scale*log2e - LSE2[query]); causal: 0 where query < key.
         // S^T is read 32 columns at a time; each 16-column bf16 result goes back over
-        // columns that have already been read.
+        // columns this warpgroup has already read.
         int lim = 0;  // columns below lim are masked (diagonal tile only)
         if (CAUSAL && tile_class(s, qi, w.kt) == 2) lim = key - qi * TILE;
-        uint32_t pk[64];
+        uint32_t pk[32];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t sr[32];
-          tmem_ld32(tS + 32 * cc, sr);
+          tmem_ld32(tS + c0 + 32 * cc, sr);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const int col = 32 * cc + 4 * j;
+            const int col = c0 + 32 * cc + 4 * j;
             const float4 l4 = *reinterpret_cast<const float4*>(l2 + col);
             float p0 = ex2(fmaf(__uint_as_float(sr[4 * j + 0]), c, -l4.x));
             float p1 = ex2(fmaf(__uint_as_float(sr[4 * j + 1]), c, -l4.y));
@@ -401,7 +413,7 @@ __global__ void __launch_bounds__(256, 1)
             pk[16 * cc + 2 * j] = pack_bf16(p0, p1);
             pk[16 * cc + 2 * j + 1] = pack_bf16(p2, p3);
           }
-          tmem_st16(tS + 16 * cc, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * cc]));
+          tmem_st16(tS + c0 + 16 * cc, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * cc]));
         }
         tmem_wait_st();
         tc_fence_before();
@@ -416,13 +428,13 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         // dS^T = P^T o (dP^T - D[query])
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t sr[32];
-          tmem_ld32(tP + 32 * cc, sr);
+          tmem_ld32(tP + c0 + 32 * cc, sr);
           uint32_t dk[16];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const int col = 32 * cc + 4 * j;
+            const int col = c0 + 32 * cc + 4 * j;
             const float4 d4 = *reinterpret_cast<const float4*>(dl + col);
             const float2 pa = unpack_bf16(pk[16 * cc + 2 * j]), pb = unpack_bf16(pk[16 * cc + 2 * j + 1]);
             dk[2 * j] = pack_bf16(pa.x * (__uint_as_float(sr[4 * j + 0]) - d4.x),
@@ -430,7 +442,7 @@ __global__ void __launch_bounds__(256, 1)
             dk[2 * j + 1] = pack_bf16(pb.x * (__uint_as_float(sr[4 * j + 2]) - d4.z),
                                       pb.y * (__uint_as_float(sr[4 * j + 3]) - d4.w));
           }
-          tmem_st16(tP + 16 * cc, dk);
+          tmem_st16(tP + c0 + 16 * cc, dk);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -445,8 +457,8 @@ __global__ void __launch_bounds__(256, 1)
                            static_cast<int64_t>(key) * p.dv.sn + w.kvh * p.dv.sh;
       __nv_bfloat16* dkr = reinterpret_cast<__nv_bfloat16*>(p.dk.ptr) + w.b * p.dk.sb +
                            static_cast<int64_t>(key) * p.dk.sn + w.kvh * p.dk.sh;
-      store_row_bf16<D>(tdV, 1.f, dvr, live);
-      store_row_bf16<D>(tdK, p.scale, dkr, live);
+      store_cols_bf16<D / 2>(tdV, (c0 / 64) * (D / 2), 1.f, dvr, live);
+      store_cols_bf16<D / 2>(tdK, (c0 / 64) * (D / 2), p.scale, dkr, live);
       sq += w.n_it;
     }
   }
@@ -475,7 +487,7 @@ struct DqLayout {
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdParams p) {
@@ -503,7 +515,7 @@ __global__ void __launch_bounds__(256, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&unit_full[i], 1);
-      mbar_init(&unit_empty[i], 1 + 128);
+      mbar_init(&unit_empty[i], 1 + 256);
       mbar_init(&s_full[i], 1);
     }
     mbar_init(q_full, 1);
@@ -513,7 +525,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&kv_empty[i], 1);
     }
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 128);
+    mbar_init(ds_full, 256);
     mbar_init(acc_full, 1);
     fence_barrier_init();
   }
@@ -626,6 +638,7 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp >= 4) {  // -------------------------------------------------- gradient warps
     const int wq = warp & 3;
+    const int c0 = ((warp - 4) >> 2) * 64;  // this warpgroup's first key column
     const int r = wq * 32 + lane_id();
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tP = tmem + lanes + 256, tdQ = tmem + lanes + 384;
@@ -658,14 +671,14 @@ __global__ void __launch_bounds__(256, 1)
           lim = imin(lim, s.Nk - j * TILE);
           if (CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
         }
-        uint32_t pk[64];
+        uint32_t pk[32];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t sr[32];
-          tmem_ld32(tmem + lanes + bi * 128 + 32 * cc, sr);
+          tmem_ld32(tmem + lanes + bi * 128 + c0 + 32 * cc, sr);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int col = 32 * cc + 2 * i;
+            const int col = c0 + 32 * cc + 2 * i;
             float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), c, -l2));
             float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), c, -l2));
             if (col >= lim) p0 = 0.f;
@@ -682,16 +695,16 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         // dS = P o (dP - D_row), written as bf16 over the dP columns already read
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t sr[32];
-          tmem_ld32(tP + 32 * cc, sr);
+          tmem_ld32(tP + c0 + 32 * cc, sr);
           uint32_t ds[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const float2 pp = unpack_bf16(pk[16 * cc + i]);
             ds[i] = pack_bf16(pp.x * (__uint_as_float(sr[2 * i]) - dl), pp.y * (__uint_as_float(sr[2 * i + 1]) - dl));
           }
-          tmem_st16(tP + 16 * cc, ds);
+          tmem_st16(tP + c0 + 16 * cc, ds);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -703,7 +716,7 @@ __global__ void __launch_bounds__(256, 1)
       tc_fence_after();
       __nv_bfloat16* dqr = reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sb +
                            static_cast<int64_t>(q_row) * p.dq.sn + h * p.dq.sh;
-      store_row_bf16<D>(tdQ, p.scale, dqr, q_row < s.Nq);
+      store_cols_bf16<D / 2>(tdQ, (c0 / 64) * (D / 2), p.scale, dqr, q_row < s.Nq);
     }
   }
   tc_fence_before();
@@ -746,7 +759,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     p.counter = a.counters;
     p.total_units = dkdv_units(a.dims);
-    kern<<<imax(1, imin(p.total_units, a.num_sms)), 256, DkvLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
+    kern<<<imax(1, imin(p.total_units, a.num_sms)), 384, DkvLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
                                                                                      a.tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -757,7 +770,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     p.counter = a.counters + 1;
     p.total_units = dq_units(a.dims);
-    kern<<<imax(1, imin(p.total_units, a.num_sms)), 256, DqLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
+    kern<<<imax(1, imin(p.total_units, a.num_sms)), 384, DqLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
                                                                                    a.tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

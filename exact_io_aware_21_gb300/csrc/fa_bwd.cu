@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.unit_full[i], 1);
-      mbar_init(&bar.unit_empty[i], 1 + 256);
+      mbar_init(&bar.unit_empty[i], 1 + 8);
     }
     mbar_init(bar.kv_full, 1);
     mbar_init(bar.kv_empty, 1);
@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(bar.s_full, 1);
     mbar_init(bar.dp_full, 1);
-    mbar_init(bar.p_full, 256);
-    mbar_init(bar.ds_full, 256);
+    mbar_init(bar.p_full, 8);
+    mbar_init(bar.ds_full, 8);
     mbar_init(bar.acc_full, 1);
     fence_barrier_init();
   }
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
       if (!__all_sync(0xffffffffu, ok)) break;
       const int u = unit_slot[slot];
-      mbar_arrive(&bar.unit_empty[slot]);
+      warp_arrive(&bar.unit_empty[slot]);
       if (u >= p.total_units) break;
       const DkvUnit w = dkv_decode(s, u);
       const int key = w.kt * TILE + r;
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar.p_full);
+        warp_arrive(bar.p_full);
 
         ok = mbar_wait(bar.dp_full, dph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
         dph ^= 1;
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(bar.ds_full);
+        warp_arrive(bar.ds_full);
       }
       if (!ok) break;
       ok = mbar_wait(bar.acc_full, it & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&unit_full[i], 1);
-      mbar_init(&unit_empty[i], 1 + 256);
+      mbar_init(&unit_empty[i], 1 + 8);
       mbar_init(&s_full[i], 1);
     }
     mbar_init(q_full, 1);
@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&kv_empty[i], 1);
     }
     mbar_init(dp_full, 1);
-    mbar_init(ds_full, 256);
+    mbar_init(ds_full, 8);
     mbar_init(acc_full, 1);
     fence_barrier_init();
   }
@@ -649,7 +649,7 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = mbar_wait(&unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
       if (!__all_sync(0xffffffffu, ok)) break;
       const int u = unit_slot[slot];
-      mbar_arrive(&unit_empty[slot]);
+      warp_arrive(&unit_empty[slot]);
       if (u >= p.total_units) break;
       int b, h, qt;
       dq_unit(s, u, b, h, qt);
@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(ds_full);
+        warp_arrive(ds_full);
       }
       if (!ok) break;
       ok = mbar_wait(acc_full, it & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);

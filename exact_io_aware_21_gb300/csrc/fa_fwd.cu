@@ -268,7 +268,7 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     bool ok = mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
     if (!__all_sync(0xffffffffu, ok)) return;
     const int u = unit_slot[slot];
-    mbar_arrive(&bar.unit_empty[slot]);
+    warp_arrive(&bar.unit_empty[slot]);
     if (u >= p.total_units) return;
     int b, h, pr, n2[2];
     fwd_unit(s, u, b, h, pr);
@@ -335,7 +335,7 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar.p_full[t]);
+      warp_arrive(&bar.p_full[t]);
       m_run = m_new;
     }
 
@@ -380,7 +380,7 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     }
     if (live) p.lse[(static_cast<int64_t>(b) * s.Hq + h) * s.Nq + q_row] = (m_run + __log2f(l_run)) * LN2;
     tc_fence_before();
-    mbar_arrive(&bar.o_empty[t]);
+    warp_arrive(&bar.o_empty[t]);
   }
 }
 
@@ -400,8 +400,8 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar.unit_full[0], 1);
     mbar_init(&bar.unit_full[1], 1);
-    mbar_init(&bar.unit_empty[0], 1 + 256);
-    mbar_init(&bar.unit_empty[1], 1 + 256);
+    mbar_init(&bar.unit_empty[0], 1 + 8);
+    mbar_init(&bar.unit_empty[1], 1 + 8);
     mbar_init(bar.q_full, 1);
     mbar_init(bar.q_empty, 1);
     for (int s = 0; s < L::STAGES; ++s) {
@@ -410,9 +410,9 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar.s_full[t], 1);
-      mbar_init(&bar.p_full[t], 128);
+      mbar_init(&bar.p_full[t], 4);
       mbar_init(&bar.o_full[t], 1);
-      mbar_init(&bar.o_empty[t], 128);
+      mbar_init(&bar.o_empty[t], 4);
     }
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);

@@ -316,8 +316,8 @@ static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const
   a.nq_pad = nq_pad(s);
   const size_t rows = static_cast<size_t>(s->B) * s->Hq * a.nq_pad;
   char* base = static_cast<char*>(ws);
-  a.lse2 = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES);
-  a.delta = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES + round_up(rows * sizeof(float), 256));
+  a.neg_lse2 = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES);
+  a.neg_delta = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES + round_up(rows * sizeof(float), 256));
   a.status = reinterpret_cast<int*>(base + FA_WS_STATUS_OFFSET);
   a.counters = reinterpret_cast<int*>(base + FA_WS_COUNTER_OFFSET);
   a.timeout_ns = g_timeout_ns;

@@ -51,8 +51,8 @@ struct BwdParams {
   float scale_log2;  // scale * log2(e)
   OutRows o, o_res, dout, dq, dk, dv;
   const float* lse;
-  float* lse2;
-  float* delta;
+  float* neg_lse2;   // -LSE * log2(e) per query row (-inf in padding)
+  float* neg_delta;  // -D per query row
   int nq_pad;
   int* status;
   int* counter;
@@ -104,8 +104,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
   if (part == 0) {
-    p.delta[row] = acc;
-    p.lse2[row] = q < p.dims.Nq ? p.lse[static_cast<int64_t>(bh) * p.dims.Nq + q] * LOG2E : INFINITY;
+    p.neg_delta[row] = -acc;
+    p.neg_lse2[row] = q < p.dims.Nq ? -p.lse[static_cast<int64_t>(bh) * p.dims.Nq + q] * LOG2E : -INFINITY;
   }
 }
 
@@ -159,7 +159,7 @@ template <int D>
 struct DkvLayout {
   static constexpr int TB = TILE * D * 2;
   static constexpr int STAGES = D == 64 ? 4 : 2;
-  static constexpr int STAGE = 2 * TB + 1024;  // Q_i, dO_i, lse2[128], delta[128]
+  static constexpr int STAGE = 2 * TB + 1024;  // Q_i, dO_i, -lse2[128], -D[128]
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TB;
   static constexpr int OFF_ST = 2 * TB;
@@ -282,8 +282,8 @@ __global__ void __launch_bounds__(384, 1)
             tma_load_4d(base + c * (TILE * 128), &tm_q, &bar.st_full[st], c * 64, hq, qi * TILE, w.b);
             tma_load_4d(base + L::TB + c * (TILE * 128), &tm_do, &bar.st_full[st], c * 64, hq, qi * TILE, w.b);
           }
-          bulk_load(base + 2 * L::TB, p.lse2 + row0, 512, &bar.st_full[st]);
-          bulk_load(base + 2 * L::TB + 512, p.delta + row0, 512, &bar.st_full[st]);
+          bulk_load(base + 2 * L::TB, p.neg_lse2 + row0, 512, &bar.st_full[st]);
+          bulk_load(base + 2 * L::TB + 512, p.neg_delta + row0, 512, &bar.st_full[st]);
         }
         if (!ok) break;
       }
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lanes, tP = tmem + lanes + 128, tdV = tmem + lanes + 256,
                    tdK = tmem + lanes + 256 + D;
-    const float c = p.scale_log2;
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     uint32_t sq = 0, sph = 0, dph = 0;
     for (int it = 0;; ++it) {
       const int slot = it & 1;
@@ -375,9 +375,10 @@ __global__ void __launch_bounds__(384, 1)
       for (int k = 0; k < w.n_it && ok; ++k) {
         const uint32_t q = sq + k;
         const uint8_t* stage = smem + L::OFF_ST + (q % L::STAGES) * L::STAGE;
-        const float* l2 = reinterpret_cast<const float*>(stage + 2 * L::TB);
-        const float* dl = l2 + 128;
+        const float* nl2 = reinterpret_cast<const float*>(stage + 2 * L::TB);  // -LSE2[query]
+        const float* nd = nl2 + 128;                                            // -D[query]
         const int qi = w.q0 + k % w.nqi;
+        const bool diag = CAUSAL && tile_class(s, qi, w.kt) == 2;
         ok = mbar_wait(&bar.st_full[q % L::STAGES], (q / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
         ok = ok && mbar_wait(bar.s_full, sph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
         sph ^= 1;
@@ -387,33 +388,35 @@ __global__ void __launch_bounds__(384, 1)
         }
         tc_fence_after();
         // P^T[key, query] = exp2(S * scale*log2e - LSE2[query]); causal: 0 where query < key.
+        // Elementwise math runs on packed f32x2 operations: scalar FP32 issue at this rate
+        // from the other sub-partitions starves the tensor pipe, packed issue does not.
         // S^T is read 32 columns at a time; each 16-column bf16 result goes back over
-        // columns this warpgroup has already read.
-        int lim = 0;  // columns below lim are masked (diagonal tile only)
-        if (CAUSAL && tile_class(s, qi, w.kt) == 2) lim = key - qi * TILE;
-        uint32_t pk[32];
+        // columns this warpgroup has already read.  P stays in registers (fp32) for dS.
+        float pf[64];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t sr[32];
           tmem_ld32(tS + c0 + 32 * cc, sr);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const int col = c0 + 32 * cc + 4 * j;
-            const float4 l4 = *reinterpret_cast<const float4*>(l2 + col);
-            float p0 = ex2(fmaf(__uint_as_float(sr[4 * j + 0]), c, -l4.x));
-            float p1 = ex2(fmaf(__uint_as_float(sr[4 * j + 1]), c, -l4.y));
-            float p2 = ex2(fmaf(__uint_as_float(sr[4 * j + 2]), c, -l4.z));
-            float p3 = ex2(fmaf(__uint_as_float(sr[4 * j + 3]), c, -l4.w));
-            if (CAUSAL) {
-              if (col + 0 < lim) p0 = 0.f;
-              if (col + 1 < lim) p1 = 0.f;
-              if (col + 2 < lim) p2 = 0.f;
-              if (col + 3 < lim) p3 = 0.f;
-            }
-            pk[16 * cc + 2 * j] = pack_bf16(p0, p1);
-            pk[16 * cc + 2 * j + 1] = pack_bf16(p2, p3);
+            const float4 l4 = *reinterpret_cast<const float4*>(nl2 + c0 + 32 * cc + 4 * j);
+            const float2 x01 = __ffma2_rn(f32x2(sr[4 * j], sr[4 * j + 1]), c2, make_float2(l4.x, l4.y));
+            const float2 x23 = __ffma2_rn(f32x2(sr[4 * j + 2], sr[4 * j + 3]), c2, make_float2(l4.z, l4.w));
+            pf[32 * cc + 4 * j + 0] = ex2(x01.x);
+            pf[32 * cc + 4 * j + 1] = ex2(x01.y);
+            pf[32 * cc + 4 * j + 2] = ex2(x23.x);
+            pf[32 * cc + 4 * j + 3] = ex2(x23.y);
           }
-          tmem_st16(tS + c0 + 16 * cc, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * cc]));
+          if (CAUSAL && diag) {  // columns below lim (queries before this key) are masked
+            const int lim = key - qi * TILE - c0 - 32 * cc;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < lim) pf[32 * cc + i] = 0.f;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pf[32 * cc + 2 * i], pf[32 * cc + 2 * i + 1]);
+          tmem_st16(tS + c0 + 16 * cc, pk);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -434,13 +437,14 @@ __global__ void __launch_bounds__(384, 1)
           uint32_t dk[16];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const int col = c0 + 32 * cc + 4 * j;
-            const float4 d4 = *reinterpret_cast<const float4*>(dl + col);
-            const float2 pa = unpack_bf16(pk[16 * cc + 2 * j]), pb = unpack_bf16(pk[16 * cc + 2 * j + 1]);
-            dk[2 * j] = pack_bf16(pa.x * (__uint_as_float(sr[4 * j + 0]) - d4.x),
-                                  pa.y * (__uint_as_float(sr[4 * j + 1]) - d4.y));
-            dk[2 * j + 1] = pack_bf16(pb.x * (__uint_as_float(sr[4 * j + 2]) - d4.z),
-                                      pb.y * (__uint_as_float(sr[4 * j + 3]) - d4.w));
+            const float4 d4 = *reinterpret_cast<const float4*>(nd + c0 + 32 * cc + 4 * j);
+            const float* pj = pf + 32 * cc + 4 * j;
+            const float2 a = __fmul2_rn(make_float2(pj[0], pj[1]),
+                                        __fadd2_rn(f32x2(sr[4 * j], sr[4 * j + 1]), make_float2(d4.x, d4.y)));
+            const float2 b = __fmul2_rn(make_float2(pj[2], pj[3]),
+                                        __fadd2_rn(f32x2(sr[4 * j + 2], sr[4 * j + 3]), make_float2(d4.z, d4.w)));
+            dk[2 * j] = pack_bf16(a.x, a.y);
+            dk[2 * j + 1] = pack_bf16(b.x, b.y);
           }
           tmem_st16(tP + c0 + 16 * cc, dk);
         }
@@ -642,7 +646,7 @@ __global__ void __launch_bounds__(384, 1)
     const int r = wq * 32 + lane_id();
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tP = tmem + lanes + 256, tdQ = tmem + lanes + 384;
-    const float c = p.scale_log2;
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     uint32_t sph[2] = {0, 0}, dph = 0;
     for (int it = 0;; ++it) {
       const int slot = it & 1;
@@ -656,7 +660,8 @@ __global__ void __launch_bounds__(384, 1)
       const int n = kv_tiles_for_q(s, qt);
       const int q_row = qt * TILE + r;
       const int64_t srow = (static_cast<int64_t>(b) * s.Hq + h) * p.nq_pad + q_row;
-      const float l2 = p.lse2[srow], dl = p.delta[srow];
+      const float2 nl2 = make_float2(p.neg_lse2[srow], p.neg_lse2[srow]);
+      const float2 nd2 = make_float2(p.neg_delta[srow], p.neg_delta[srow]);
       for (int j = 0; j < n && ok; ++j) {
         const int bi = j & 1;
         ok = mbar_wait(&s_full[bi], sph[bi], ctl, FA_STATUS_TIMEOUT_SOFTMAX);
@@ -666,25 +671,27 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         tc_fence_after();
-        int lim = 128;  // keys at or beyond lim (tile-local) are masked
-        if (j == n - 1) {
-          lim = imin(lim, s.Nk - j * TILE);
-          if (CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
-        }
-        uint32_t pk[32];
+        // P = exp2(S * scale*log2e - LSE2[row]), on packed f32x2 operations (see the
+        // dK/dV kernel); only the last key tile can hold masked keys.
+        float pf[64];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t sr[32];
           tmem_ld32(tmem + lanes + bi * 128 + c0 + 32 * cc, sr);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int col = c0 + 32 * cc + 2 * i;
-            float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), c, -l2));
-            float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), c, -l2));
-            if (col >= lim) p0 = 0.f;
-            if (col + 1 >= lim) p1 = 0.f;
-            pk[16 * cc + i] = pack_bf16(p0, p1);
+            const float2 x = __ffma2_rn(f32x2(sr[2 * i], sr[2 * i + 1]), c2, nl2);
+            pf[32 * cc + 2 * i] = ex2(x.x);
+            pf[32 * cc + 2 * i + 1] = ex2(x.y);
           }
+        }
+        if (j == n - 1) {  // keys at or beyond lim (tile-local) are masked
+          int lim = imin(TILE, s.Nk - j * TILE);
+          if (CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
+          lim -= c0;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i >= lim) pf[i] = 0.f;
         }
         ok = mbar_wait(dp_full, dph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
         dph ^= 1;
@@ -701,8 +708,9 @@ __global__ void __launch_bounds__(384, 1)
           uint32_t ds[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float2 pp = unpack_bf16(pk[16 * cc + i]);
-            ds[i] = pack_bf16(pp.x * (__uint_as_float(sr[2 * i]) - dl), pp.y * (__uint_as_float(sr[2 * i + 1]) - dl));
+            const float2 g = __fmul2_rn(make_float2(pf[32 * cc + 2 * i], pf[32 * cc + 2 * i + 1]),
+                                        __fadd2_rn(f32x2(sr[2 * i], sr[2 * i + 1]), nd2));
+            ds[i] = pack_bf16(g.x, g.y);
           }
           tmem_st16(tP + c0 + 16 * cc, ds);
         }
@@ -740,8 +748,8 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   p.dk = a.dk;
   p.dv = a.dv;
   p.lse = a.lse;
-  p.lse2 = a.lse2;
-  p.delta = a.delta;
+  p.neg_lse2 = a.neg_lse2;
+  p.neg_delta = a.neg_delta;
   p.nq_pad = a.nq_pad;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;

@@ -36,8 +36,8 @@ struct BwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
   OutRows o, o_res, dout, dq, dk, dv;  // o_res.ptr may be nullptr
   const float* lse;
-  float* lse2;     // workspace [B*Hq, Nq_pad] : LSE * log2(e)  (+inf in padding)
-  float* delta;    // workspace [B*Hq, Nq_pad] : D = rowsum(dO o O)
+  float* neg_lse2;   // workspace [B*Hq, Nq_pad] : -LSE * log2(e)  (-inf in padding)
+  float* neg_delta;  // workspace [B*Hq, Nq_pad] : -D, D = rowsum(dO o O)
   int nq_pad;
   int* status;
   int* counters;   // [2]

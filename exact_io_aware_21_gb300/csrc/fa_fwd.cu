@@ -260,6 +260,7 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
   const uint32_t tS = tmem + lanes + t * 128;
   const uint32_t tO = tmem + lanes + 256 + t * D;
   const float c = p.scale_log2;
+  const float2 c2 = make_float2(c, c);
   const Dims& s = p.dims;
   uint32_t sph = 0, active = 0;
 
@@ -297,39 +298,48 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
         for (int i = 0; i < 128; ++i)
           if (i >= lim) sv[i] = -INFINITY;
       }
-      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+      // Row max (three-input max), then exp2 and row sum on packed f32x2 operations:
+      // scalar FP32 issue at this rate from several sub-partitions slows the tensor pipe.
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int i = 4; i < 128; i += 4) {
-        mx0 = fmaxf(mx0, sv[i]);
-        mx1 = fmaxf(mx1, sv[i + 1]);
-        mx2 = fmaxf(mx2, sv[i + 2]);
-        mx3 = fmaxf(mx3, sv[i + 3]);
+      for (int i = 0; i < 128; i += 8) {
+        mx0 = fmax3(mx0, sv[i], sv[i + 1]);
+        mx1 = fmax3(mx1, sv[i + 2], sv[i + 3]);
+        mx2 = fmax3(mx2, sv[i + 4], sv[i + 5]);
+        mx3 = fmax3(mx3, sv[i + 6], sv[i + 7]);
       }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const float m_tile = fmaxf(fmax3(mx0, mx1, mx2), mx3) * c;
       const float m_new = (m_tile > m_run + TAU) ? m_tile : m_run;
       const float alpha = ex2(m_run - m_new);
-      const float neg_m = -m_new;
-      float sum0 = 0.f, sum1 = 0.f;
+      const float2 neg_m2 = make_float2(-m_new, -m_new);
+      float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
       uint32_t pk[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2(fmaf(sv[2 * i], c, neg_m));
-        const float p1 = ex2(fmaf(sv[2 * i + 1], c, neg_m));
-        sum0 += p0;
-        sum1 += p1;
-        pk[i] = pack_bf16(p0, p1);
+      for (int i = 0; i < 64; i += 2) {
+        const float2 x0 = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), c2, neg_m2);
+        const float2 x1 = __ffma2_rn(make_float2(sv[2 * i + 2], sv[2 * i + 3]), c2, neg_m2);
+        const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+        const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+        sum0 = __fadd2_rn(sum0, p0);
+        sum1 = __fadd2_rn(sum1, p1);
+        pk[i] = pack_bf16(p0.x, p0.y);
+        pk[i + 1] = pack_bf16(p1.x, p1.y);
       }
-      l_run = l_run * alpha + (sum0 + sum1);
+      l_run = l_run * alpha + ((sum0.x + sum0.y) + (sum1.x + sum1.y));
       tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32(tO + cc * 32, o);
-
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          for (int i = 0; i < 16; ++i) {
+            const float2 v = __fmul2_rn(f32x2(o[2 * i], o[2 * i + 1]), a2);
+            o[2 * i] = __float_as_uint(v.x);
+            o[2 * i + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(tO + cc * 32, o);
         }
       }

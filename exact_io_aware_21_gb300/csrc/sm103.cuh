@@ -276,6 +276,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Two fp32 values held as raw bits (e.g. TMEM load results) as a float2 operand.
 __device__ __forceinline__ float2 f32x2(uint32_t lo, uint32_t hi) {
   return make_float2(__uint_as_float(lo), __uint_as_float(hi));

@@ -132,25 +132,38 @@ __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint3
            IDESC, (acc || k > 0) ? 1u : 0u);
 }
 
-// Store columns [col0, col0 + NC) of a row of fp32 accumulator columns as bf16
-// (times mul); dst points at the row's first element.
+// Half of issue_ts: the four K steps whose A columns come from chunk `half` of
+// each elementwise warpgroup (K steps 0,1,4,5 for half 0; 2,3,6,7 for half 1),
+// so the product can start on the columns written first.
+template <int D, int HALF>
+__device__ __forceinline__ void issue_ts_half(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, bool acc) {
+  constexpr uint32_t IDESC = idesc_bf16(128, D, false, true);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int k = (i & 1) + 2 * HALF + (i >> 1) * 4;
+    mma_ts(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), sdesc_sw128(b_base + k * 16 * 128, TILE * 128, 1024),
+           IDESC, (acc || i > 0) ? 1u : 0u);
+  }
+}
+
+// Store accumulator columns [col0, col0 + NC) of the warp's 32 TMEM lanes as bf16
+// rows (times mul): dst0 = element (lane 0's row, column 0); rows at or beyond
+// `live` (counted from lane 0) are skipped.
 template <int NC>
-__device__ __forceinline__ void store_cols_bf16(uint32_t t_acc, int col0, float mul, __nv_bfloat16* dst,
-                                                bool live) {
-  dst += col0;
-  t_acc += col0;
+__device__ __forceinline__ void store_acc_rows(uint32_t t_acc, int col0, float mul, __nv_bfloat16* dst0,
+                                               int64_t stride, int live, uint8_t* scratch) {
+  const float2 m2 = make_float2(mul, mul);
 #pragma unroll
   for (int cc = 0; cc < NC / 32; ++cc) {
     uint32_t v[32];
-    tmem_ld32(t_acc + cc * 32, v);
+    tmem_ld32(t_acc + col0 + cc * 32, v);
     uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = pack_bf16(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-    if (live) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    for (int i = 0; i < 16; ++i) {
+      const float2 f = __fmul2_rn(f32x2(v[2 * i], v[2 * i + 1]), m2);
+      w[i] = pack_bf16(f.x, f.y);
     }
+    store_rows32_bf16(w, scratch, dst0 + col0 + cc * 32, stride, live);
   }
 }
 
@@ -164,11 +177,13 @@ struct DkvLayout {
   static constexpr int OFF_V = TB;
   static constexpr int OFF_ST = 2 * TB;
   static constexpr int OFF_BAR = OFF_ST + STAGES * STAGE;
-  // unit_full[2] unit_empty[2] kv_full kv_empty st_full[S] st_empty[S] s_full dp_full p_full ds_full acc_full
-  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 5;
+  // unit_full[2] unit_empty[2] kv_full kv_empty st_full[S] st_empty[S] s_full dp_full p_full[2] ds_full[2]
+  // acc_full
+  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 7;
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
-  static constexpr int ALLOC = OFF_TMEM + 16 + 1024;
+  static constexpr int OFF_SCR = (OFF_TMEM + 16 + 127) / 128 * 128;  // row-store scratch, one per gradient warp
+  static constexpr int ALLOC = OFF_SCR + 8 * ROW_SCRATCH_BYTES + 1024;
 };
 
 struct DkvBars {
@@ -189,9 +204,9 @@ __device__ __forceinline__ DkvBars dkv_bars(uint8_t* smem) {
   r.st_empty = r.st_full + L::STAGES;
   r.s_full = r.st_empty + L::STAGES;
   r.dp_full = r.s_full + 1;
-  r.p_full = r.s_full + 2;
-  r.ds_full = r.s_full + 3;
-  r.acc_full = r.s_full + 4;
+  r.p_full = r.s_full + 2;   // [2]: one per 32-column chunk of each warpgroup's half
+  r.ds_full = r.s_full + 4;  // [2]
+  r.acc_full = r.s_full + 6;
   return r;
 }
 
@@ -237,8 +252,10 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(bar.s_full, 1);
     mbar_init(bar.dp_full, 1);
-    mbar_init(bar.p_full, 8);
-    mbar_init(bar.ds_full, 8);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar.p_full[i], 8);
+      mbar_init(&bar.ds_full[i], 8);
+    }
     mbar_init(bar.acc_full, 1);
     fence_barrier_init();
   }
@@ -318,14 +335,20 @@ __global__ void __launch_bounds__(384, 1)
           mma_commit(bar.s_full);
           issue_ss<D>(tP, vb, qb + L::TB);   // dP^T = V dO^T
           mma_commit(bar.dp_full);
+          if (w.n_it == 1) mma_commit(bar.kv_empty);  // K and V are read by S and dP only
         }
         for (int k = 0; k < w.n_it && ok; ++k) {
           const uint32_t cur = stb + ((sq + k) % L::STAGES) * L::STAGE;
-          ok = mbar_wait(bar.p_full, pph, ctl, FA_STATUS_TIMEOUT_MMA);
+          // dV += P^T dO, each half as soon as its P columns are in TMEM
+          ok = mbar_wait(&bar.p_full[0], pph, ctl, FA_STATUS_TIMEOUT_MMA);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts_half<D, 0>(tdV, tS, cur + L::TB, k > 0);
+          ok = mbar_wait(&bar.p_full[1], pph, ctl, FA_STATUS_TIMEOUT_MMA);
           pph ^= 1;
           if (!ok) break;
           tc_fence_after();
-          issue_ts<D>(tdV, tS, cur + L::TB, k > 0);   // dV += P^T dO
+          issue_ts_half<D, 1>(tdV, tS, cur + L::TB, true);
           const bool more = k + 1 < w.n_it;
           uint32_t nxt = 0;
           if (more) {
@@ -337,25 +360,33 @@ __global__ void __launch_bounds__(384, 1)
             issue_ss<D>(tS, kb, nxt);
             mma_commit(bar.s_full);
           }
-          ok = mbar_wait(bar.ds_full, dph, ctl, FA_STATUS_TIMEOUT_MMA);
+          // dK += dS^T Q, by halves as for dV
+          ok = mbar_wait(&bar.ds_full[0], dph, ctl, FA_STATUS_TIMEOUT_MMA);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ts_half<D, 0>(tdK, tP, cur, k > 0);
+          ok = mbar_wait(&bar.ds_full[1], dph, ctl, FA_STATUS_TIMEOUT_MMA);
           dph ^= 1;
           if (!ok) break;
           tc_fence_after();
-          issue_ts<D>(tdK, tP, cur, k > 0);           // dK += dS^T Q
+          issue_ts_half<D, 1>(tdK, tP, cur, true);
           mma_commit(&bar.st_empty[(sq + k) % L::STAGES]);
           if (more) {
             issue_ss<D>(tP, vb, nxt + L::TB);
             mma_commit(bar.dp_full);
+            // The unit's last S and dP are issued: K and V can be refilled with the
+            // next unit's tiles while its last dV and dK run.
+            if (k + 2 == w.n_it) mma_commit(bar.kv_empty);
           }
         }
         if (!ok) break;
         mma_commit(bar.acc_full);
-        mma_commit(bar.kv_empty);
         sq += w.n_it;
       }
     }
   } else if (warp >= 4) {  // -------------------------------------------------- gradient warps
     const int wq = warp & 3;
+    uint8_t* scratch = smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES;
     const int c0 = ((warp - 4) >> 2) * 64;  // this warpgroup's first column
     const int r = wq * 32 + lane_id();      // key row within the tile
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
@@ -390,37 +421,41 @@ __global__ void __launch_bounds__(384, 1)
         // P^T[key, query] = exp2(S * scale*log2e - LSE2[query]); causal: 0 where query < key.
         // Elementwise math runs on packed f32x2 operations: scalar FP32 issue at this rate
         // from the other sub-partitions starves the tensor pipe, packed issue does not.
-        // S^T is read 32 columns at a time; each 16-column bf16 result goes back over
-        // columns this warpgroup has already read.  P stays in registers (fp32) for dS.
+        // This warpgroup's 64 columns of S^T are read at once; P goes back as bf16 over
+        // them in two 32-column chunks, each announced on its own barrier so that the
+        // dV product starts on the first chunk.  P stays in registers (fp32) for dS.
         float pf[64];
+        {
+          uint32_t sr[64];
+          tmem_ld64(tS + c0, sr);
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t sr[32];
-          tmem_ld32(tS + c0 + 32 * cc, sr);
+          for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 l4 = *reinterpret_cast<const float4*>(nl2 + c0 + 32 * cc + 4 * j);
-            const float2 x01 = __ffma2_rn(f32x2(sr[4 * j], sr[4 * j + 1]), c2, make_float2(l4.x, l4.y));
-            const float2 x23 = __ffma2_rn(f32x2(sr[4 * j + 2], sr[4 * j + 3]), c2, make_float2(l4.z, l4.w));
-            pf[32 * cc + 4 * j + 0] = ex2(x01.x);
-            pf[32 * cc + 4 * j + 1] = ex2(x01.y);
-            pf[32 * cc + 4 * j + 2] = ex2(x23.x);
-            pf[32 * cc + 4 * j + 3] = ex2(x23.y);
+            for (int j = 0; j < 8; ++j) {
+              const int e = 32 * cc + 4 * j;
+              const float4 l4 = *reinterpret_cast<const float4*>(nl2 + c0 + e);
+              const float2 x01 = __ffma2_rn(f32x2(sr[e], sr[e + 1]), c2, make_float2(l4.x, l4.y));
+              const float2 x23 = __ffma2_rn(f32x2(sr[e + 2], sr[e + 3]), c2, make_float2(l4.z, l4.w));
+              pf[e + 0] = ex2(x01.x);
+              pf[e + 1] = ex2(x01.y);
+              pf[e + 2] = ex2(x23.x);
+              pf[e + 3] = ex2(x23.y);
+            }
+            if (CAUSAL && diag) {  // columns below lim (queries before this key) are masked
+              const int lim = key - qi * TILE - c0 - 32 * cc;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < lim) pf[32 * cc + i] = 0.f;
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pf[32 * cc + 2 * i], pf[32 * cc + 2 * i + 1]);
+            tmem_st16(tS + c0 + 16 * cc, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(&bar.p_full[cc]);
           }
-          if (CAUSAL && diag) {  // columns below lim (queries before this key) are masked
-            const int lim = key - qi * TILE - c0 - 32 * cc;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < lim) pf[32 * cc + i] = 0.f;
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pf[32 * cc + 2 * i], pf[32 * cc + 2 * i + 1]);
-          tmem_st16(tS + c0 + 16 * cc, pk);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        warp_arrive(bar.p_full);
 
         ok = mbar_wait(bar.dp_full, dph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
         dph ^= 1;
@@ -429,40 +464,42 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         tc_fence_after();
-        // dS^T = P^T o (dP^T - D[query])
+        // dS^T = P^T o (dP^T - D[query]), in the same two chunks
+        {
+          uint32_t sr[64];
+          tmem_ld64(tP + c0, sr);
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t sr[32];
-          tmem_ld32(tP + c0 + 32 * cc, sr);
-          uint32_t dk[16];
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t dk[16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 d4 = *reinterpret_cast<const float4*>(nd + c0 + 32 * cc + 4 * j);
-            const float* pj = pf + 32 * cc + 4 * j;
-            const float2 a = __fmul2_rn(make_float2(pj[0], pj[1]),
-                                        __fadd2_rn(f32x2(sr[4 * j], sr[4 * j + 1]), make_float2(d4.x, d4.y)));
-            const float2 b = __fmul2_rn(make_float2(pj[2], pj[3]),
-                                        __fadd2_rn(f32x2(sr[4 * j + 2], sr[4 * j + 3]), make_float2(d4.z, d4.w)));
-            dk[2 * j] = pack_bf16(a.x, a.y);
-            dk[2 * j + 1] = pack_bf16(b.x, b.y);
+            for (int j = 0; j < 8; ++j) {
+              const int e = 32 * cc + 4 * j;
+              const float4 d4 = *reinterpret_cast<const float4*>(nd + c0 + e);
+              const float2 a = __fmul2_rn(make_float2(pf[e], pf[e + 1]),
+                                          __fadd2_rn(f32x2(sr[e], sr[e + 1]), make_float2(d4.x, d4.y)));
+              const float2 b = __fmul2_rn(make_float2(pf[e + 2], pf[e + 3]),
+                                          __fadd2_rn(f32x2(sr[e + 2], sr[e + 3]), make_float2(d4.z, d4.w)));
+              dk[2 * j] = pack_bf16(a.x, a.y);
+              dk[2 * j + 1] = pack_bf16(b.x, b.y);
+            }
+            tmem_st16(tP + c0 + 16 * cc, dk);
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(&bar.ds_full[cc]);
           }
-          tmem_st16(tP + c0 + 16 * cc, dk);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        warp_arrive(bar.ds_full);
       }
       if (!ok) break;
       ok = mbar_wait(bar.acc_full, it & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const bool live = key < s.Nk;
-      __nv_bfloat16* dvr = reinterpret_cast<__nv_bfloat16*>(p.dv.ptr) + w.b * p.dv.sb +
-                           static_cast<int64_t>(key) * p.dv.sn + w.kvh * p.dv.sh;
-      __nv_bfloat16* dkr = reinterpret_cast<__nv_bfloat16*>(p.dk.ptr) + w.b * p.dk.sb +
-                           static_cast<int64_t>(key) * p.dk.sn + w.kvh * p.dk.sh;
-      store_cols_bf16<D / 2>(tdV, (c0 / 64) * (D / 2), 1.f, dvr, live);
-      store_cols_bf16<D / 2>(tdK, (c0 / 64) * (D / 2), p.scale, dkr, live);
+      const int key0 = w.kt * TILE + wq * 32;  // this warp's first key row
+      __nv_bfloat16* dv0 = reinterpret_cast<__nv_bfloat16*>(p.dv.ptr) + w.b * p.dv.sb +
+                           static_cast<int64_t>(key0) * p.dv.sn + w.kvh * p.dv.sh;
+      __nv_bfloat16* dk0 = reinterpret_cast<__nv_bfloat16*>(p.dk.ptr) + w.b * p.dk.sb +
+                           static_cast<int64_t>(key0) * p.dk.sn + w.kvh * p.dk.sh;
+      store_acc_rows<D / 2>(tdV, (c0 / 64) * (D / 2), 1.f, dv0, p.dv.sn, s.Nk - key0, scratch);
+      store_acc_rows<D / 2>(tdK, (c0 / 64) * (D / 2), p.scale, dk0, p.dk.sn, s.Nk - key0, scratch);
       sq += w.n_it;
     }
   }
@@ -487,7 +524,8 @@ struct DqLayout {
   static constexpr int NBAR = 4 + 2 + 2 * STAGES + 5;
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
-  static constexpr int ALLOC = OFF_TMEM + 16 + 1024;
+  static constexpr int OFF_SCR = (OFF_TMEM + 16 + 127) / 128 * 128;  // row-store scratch, one per dQ warp
+  static constexpr int ALLOC = OFF_SCR + 8 * ROW_SCRATCH_BYTES + 1024;
 };
 
 template <int D, bool CAUSAL>
@@ -642,6 +680,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp >= 4) {  // -------------------------------------------------- gradient warps
     const int wq = warp & 3;
+    uint8_t* scratch = smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES;
     const int c0 = ((warp - 4) >> 2) * 64;  // this warpgroup's first key column
     const int r = wq * 32 + lane_id();
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
@@ -722,9 +761,10 @@ __global__ void __launch_bounds__(384, 1)
       ok = mbar_wait(acc_full, it & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      __nv_bfloat16* dqr = reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sb +
-                           static_cast<int64_t>(q_row) * p.dq.sn + h * p.dq.sh;
-      store_cols_bf16<D / 2>(tdQ, (c0 / 64) * (D / 2), p.scale, dqr, q_row < s.Nq);
+      const int q0 = qt * TILE + wq * 32;  // this warp's first query row
+      __nv_bfloat16* dq0 = reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sb +
+                           static_cast<int64_t>(q0) * p.dq.sn + h * p.dq.sh;
+      store_acc_rows<D / 2>(tdQ, (c0 / 64) * (D / 2), p.scale, dq0, p.dq.sn, s.Nq - q0, scratch);
     }
   }
   tc_fence_before();

@@ -52,7 +52,8 @@ struct FwdLayout {
   static constexpr int NBAR = 4 + 2 + 2 * STAGES + 8;
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
-  static constexpr int BYTES = OFF_TMEM + 16;
+  static constexpr int OFF_SCR = (OFF_TMEM + 16 + 127) / 128 * 128;  // row-store scratch, one per softmax warp
+  static constexpr int BYTES = OFF_SCR + 8 * ROW_SCRATCH_BYTES;
   static constexpr int ALLOC = BYTES + 1024;
 };
 
@@ -253,7 +254,7 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
 // ------------------------------------------------------------------ softmax
 template <int D, bool CAUSAL>
 __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
-                            const Ctl& ctl) {
+                            const Ctl& ctl, uint8_t* scratch) {
   const int wq = (threadIdx.x >> 5) & 3;  // warp within the warpgroup = TMEM lane quarter
   const int r = wq * 32 + lane_id();      // row of the query tile
   const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
@@ -355,37 +356,36 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     if (!__all_sync(0xffffffffu, ok)) return;
     tc_fence_after();
     const float inv_l = 1.f / l_run;
+    const float2 il2 = make_float2(inv_l, inv_l);
     const bool live = q_row < s.Nq;
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o.ptr) + b * p.o.sb +
-                          static_cast<int64_t>(q_row) * p.o.sn + h * p.o.sh;
-    __nv_bfloat16* rrow = p.o_res.ptr == nullptr
-                              ? nullptr
-                              : reinterpret_cast<__nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
-                                    static_cast<int64_t>(q_row) * p.o_res.sn + h * p.o_res.sh;
+    const int q0 = qt * TILE + wq * 32;  // this warp's first row
+    __nv_bfloat16* o0 = reinterpret_cast<__nv_bfloat16*>(p.o.ptr) + b * p.o.sb + static_cast<int64_t>(q0) * p.o.sn +
+                        h * p.o.sh;
+    __nv_bfloat16* r0 = p.o_res.ptr == nullptr
+                            ? nullptr
+                            : reinterpret_cast<__nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
+                                  static_cast<int64_t>(q0) * p.o_res.sn + h * p.o_res.sh;
 #pragma unroll
     for (int cc = 0; cc < D / 32; ++cc) {
       uint32_t o[32];
       tmem_ld32(tO + cc * 32, o);
 
+      float2 ov[16];
       uint32_t w[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-      if (live) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      for (int i = 0; i < 16; ++i) {
+        ov[i] = __fmul2_rn(f32x2(o[2 * i], o[2 * i + 1]), il2);
+        w[i] = pack_bf16(ov[i].x, ov[i].y);
       }
-      if (rrow != nullptr && live) {  // rounding residual: bf16(O - bf16(O))
+      store_rows32_bf16(w, scratch, o0 + cc * 32, p.o.sn, s.Nq - q0);
+      if (r0 != nullptr) {  // rounding residual: bf16(O - bf16(O))
         uint32_t rz[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float2 hv = unpack_bf16(w[i]);
-          rz[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l - hv.x, __uint_as_float(o[2 * i + 1]) * inv_l - hv.y);
+          rz[i] = pack_bf16(ov[i].x - hv.x, ov[i].y - hv.y);
         }
-        uint4* dst = reinterpret_cast<uint4*>(rrow + cc * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(rz[4 * i], rz[4 * i + 1], rz[4 * i + 2], rz[4 * i + 3]);
+        store_rows32_bf16(rz, scratch, r0 + cc * 32, p.o_res.sn, s.Nq - q0);
       }
     }
     if (live) p.lse[(static_cast<int64_t>(b) * s.Hq + h) * s.Nq + q_row] = (m_run + __log2f(l_run)) * LN2;
@@ -440,7 +440,8 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 1) {
     if (lane_id() == 0) fwd_mma<D>(smem, bar, unit_slot, tmem, p, ctl);
   } else if (warp >= 4) {
-    fwd_softmax<D, CAUSAL>((warp - 4) >> 2, bar, unit_slot, tmem, p, ctl);
+    fwd_softmax<D, CAUSAL>((warp - 4) >> 2, bar, unit_slot, tmem, p, ctl,
+                           smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES);
   }
   tc_fence_before();
   __syncthreads();

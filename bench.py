@@ -14,6 +14,7 @@ their device time (TFLOPS; forward 4*B*H*Nq*Nk*d, halved when causal, backward
 before every launch group, outside its events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --profile-case WORKLOAD   # two fwd+bwd passes, for ncu captures
 
 Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
 data (weak scaling, no collective on the data path); the step time is the max
@@ -520,6 +521,24 @@ def run_ours(args):
     return 0
 
 
+def profile_case(name):
+    """Two forward + backward passes of one named workload through the public API.
+
+    A short, fixed program for ncu captures (the first pass warms up; capture the
+    second with ``-s``).  Prints nothing but "ok"."""
+    import exact_io_aware_21_gb300 as fa
+    from exact_io_aware_21_gb300 import inputs
+
+    w = {x.name: x for x in inputs.ALL}[name]
+    x = inputs.make(w, device="cuda")
+    for _ in range(2):
+        o, lse, res = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, residual=True)
+        fa.backward(x["q"], x["k"], x["v"], o, lse, x["do"], causal=w.causal, scale=w.scale, o_residual=res)
+    torch.cuda.synchronize()
+    print("ok")
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description="exact attention hot-path benchmark (one JSON line)")
     ap.add_argument("--gpus", type=int, default=1)
@@ -528,7 +547,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile-case", metavar="WORKLOAD", help="run two fwd+bwd passes of WORKLOAD and exit")
     args = ap.parse_args(argv)
+    if args.profile_case:
+        return profile_case(args.profile_case)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     return run_reference(args) if args.impl == "reference" else run_ours(args)

@@ -148,7 +148,7 @@ __device__ __forceinline__ void issue_ts_half(uint32_t d_tmem, uint32_t a_tmem, 
 
 // Store accumulator columns [col0, col0 + NC) of the warp's 32 TMEM lanes as bf16
 // rows (times mul): dst0 = element (lane 0's row, column 0); rows at or beyond
-// `live` (counted from lane 0) are skipped.
+// `live` (counted from lane 0) are skipped.  scratch == nullptr: direct stores.
 template <int NC>
 __device__ __forceinline__ void store_acc_rows(uint32_t t_acc, int col0, float mul, __nv_bfloat16* dst0,
                                                int64_t stride, int live, uint8_t* scratch) {
@@ -163,7 +163,13 @@ __device__ __forceinline__ void store_acc_rows(uint32_t t_acc, int col0, float m
       const float2 f = __fmul2_rn(f32x2(v[2 * i], v[2 * i + 1]), m2);
       w[i] = pack_bf16(f.x, f.y);
     }
-    store_rows32_bf16(w, scratch, dst0 + col0 + cc * 32, stride, live);
+    if (scratch != nullptr) {
+      store_rows32_bf16(w, scratch, dst0 + col0 + cc * 32, stride, live);
+    } else if (lane_id() < live) {  // no scratch: each lane stores its own row
+      uint4* d4 = reinterpret_cast<uint4*>(dst0 + lane_id() * stride + col0 + cc * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
   }
 }
 
@@ -515,17 +521,24 @@ __global__ void __launch_bounds__(384, 1)
 template <int D>
 struct DqLayout {
   static constexpr int TB = TILE * D * 2;
-  static constexpr int STAGES = D == 64 ? 4 : 2;  // K_j + V_j per stage
+  // K_j is read by S_j and, two iterations later, by dQ += dS_j K_j; V_j only by dP_j.
+  // Separate rings let K run three tiles deep (V two) in the same shared memory.
+  static constexpr int KST = D == 64 ? 4 : 3;
+  static constexpr int VST = 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = TB;
-  static constexpr int OFF_KV = 2 * TB;
-  static constexpr int OFF_BAR = OFF_KV + STAGES * 2 * TB;
-  // unit_full[2] unit_empty[2] q_full q_empty kv_full[S] kv_empty[S] s_full[2] dp_full ds_full acc_full
-  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 5;
+  static constexpr int OFF_K = 2 * TB;
+  static constexpr int OFF_V = OFF_K + KST * TB;
+  static constexpr int OFF_BAR = OFF_V + VST * TB;
+  // unit_full[2] unit_empty[2] q_full q_empty k_full[KST] k_empty[KST] v_full[VST] v_empty[VST] s_full[2]
+  // dp_full ds_full acc_full
+  static constexpr int NBAR = 4 + 2 + 2 * KST + 2 * VST + 5;
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
   static constexpr int OFF_SCR = (OFF_TMEM + 16 + 127) / 128 * 128;  // row-store scratch, one per dQ warp
-  static constexpr int ALLOC = OFF_SCR + 8 * ROW_SCRATCH_BYTES + 1024;
+  // At d = 128 the rings leave no room for the scratch: dQ rows are stored directly.
+  static constexpr bool SCRATCH = OFF_SCR + 8 * ROW_SCRATCH_BYTES + 1024 <= 227 * 1024;
+  static constexpr int ALLOC = (SCRATCH ? OFF_SCR + 8 * ROW_SCRATCH_BYTES : OFF_TMEM + 16) + 1024;
 };
 
 template <int D, bool CAUSAL>
@@ -541,9 +554,11 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* unit_empty = bb + 2;
   uint64_t* q_full = bb + 4;
   uint64_t* q_empty = bb + 5;
-  uint64_t* kv_full = bb + 6;
-  uint64_t* kv_empty = kv_full + L::STAGES;
-  uint64_t* s_full = kv_empty + L::STAGES;  // [2]
+  uint64_t* k_full = bb + 6;
+  uint64_t* k_empty = k_full + L::KST;
+  uint64_t* v_full = k_empty + L::KST;
+  uint64_t* v_empty = v_full + L::VST;      // arrived by a dQ warp once it has seen dP of that tile done
+  uint64_t* s_full = v_empty + L::VST;      // [2]
   uint64_t* dp_full = s_full + 2;
   uint64_t* ds_full = s_full + 3;
   uint64_t* acc_full = s_full + 4;
@@ -562,9 +577,13 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int i = 0; i < L::STAGES; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < L::KST; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < L::VST; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     mbar_init(dp_full, 1);
     mbar_init(ds_full, 8);
@@ -600,37 +619,56 @@ __global__ void __launch_bounds__(384, 1)
         q_armed = it;
         bool ok = true;
         for (int j = 0; j < n; ++j, ++kq) {
-          const int st = kq % L::STAGES;
-          if (!mbar_wait(&kv_empty[st], ((kq / L::STAGES) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
+          // K_j: its slot is free once dQ of the tile KST back is done.
+          const int ks = kq % L::KST;
+          if (!mbar_wait(&k_empty[ks], ((kq / L::KST) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
             ok = false;
             break;
           }
-          uint8_t* base = smem + L::OFF_KV + st * 2 * L::TB;
-          mbar_arrive_expect_tx(&kv_full[st], 2 * L::TB);
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_4d(base + c * (TILE * 128), &tm_k, &kv_full[st], c * 64, kvh, j * TILE, b);
-            tma_load_4d(base + L::TB + c * (TILE * 128), &tm_v, &kv_full[st], c * 64, kvh, j * TILE, b);
+          mbar_arrive_expect_tx(&k_full[ks], L::TB);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(smem + L::OFF_K + ks * L::TB + c * (TILE * 128), &tm_k, &k_full[ks], c * 64, kvh,
+                        j * TILE, b);
+          // V_j: its slot is free once dP of the tile VST back is done.
+          const int vs = kq % L::VST;
+          if (!mbar_wait(&v_empty[vs], ((kq / L::VST) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(&v_full[vs], L::TB);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(smem + L::OFF_V + vs * L::TB + c * (TILE * 128), &tm_v, &v_full[vs], c * 64, kvh,
+                        j * TILE, b);
         }
         if (!ok) break;
       }
-      for (int i = 0; i < L::STAGES; ++i)
+      // copies in flight land before exit (v_full of a slot may trail its k_full by one load)
+      for (int i = 0; i < L::KST; ++i)
         if (kq > static_cast<uint32_t>(i)) {
-          const uint32_t last = kq - 1 - ((kq - 1 - i) % L::STAGES);
-          mbar_wait(&kv_full[i], (last / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+          const uint32_t last = kq - 1 - ((kq - 1 - i) % L::KST);
+          mbar_wait(&k_full[i], (last / L::KST) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+        }
+      for (int i = 0; i < L::VST; ++i)
+        if (kq > static_cast<uint32_t>(i)) {
+          const uint32_t last = kq - 1 - ((kq - 1 - i) % L::VST);
+          mbar_wait(&v_full[i], (last / L::VST) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
         }
       if (q_armed >= 0) mbar_wait(q_full, q_armed & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
     }
   } else if (warp == 1) {
     if (lane_id() == 0) {  // ---------------------------------------------- MMA issuer
       const uint32_t qb = smem_u32(smem + L::OFF_Q), dob = smem_u32(smem + L::OFF_DO);
-      const uint32_t kvb = smem_u32(smem + L::OFF_KV);
+      const uint32_t kb0 = smem_u32(smem + L::OFF_K), vb0 = smem_u32(smem + L::OFF_V);
       const uint32_t tP = tmem + 256, tdQ = tmem + 384;
       uint32_t kq = 0, dsph = 0;
-      auto kvwait = [&](uint32_t idx) {
-        return mbar_wait(&kv_full[idx % L::STAGES], (idx / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+      auto kwait = [&](uint32_t idx) {
+        return mbar_wait(&k_full[idx % L::KST], (idx / L::KST) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
       };
-      auto kbase = [&](uint32_t idx) { return kvb + (idx % L::STAGES) * 2 * L::TB; };
+      auto vwait = [&](uint32_t idx) {
+        return mbar_wait(&v_full[idx % L::VST], (idx / L::VST) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+      };
+      auto kbase = [&](uint32_t idx) { return kb0 + (idx % L::KST) * L::TB; };
+      auto vbase = [&](uint32_t idx) { return vb0 + (idx % L::VST) * L::TB; };
       for (int it = 0;; ++it) {
         const int slot = it & 1;
         if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
@@ -640,15 +678,17 @@ __global__ void __launch_bounds__(384, 1)
         int b, h, qt;
         dq_unit(s, u, b, h, qt);
         const int n = kv_tiles_for_q(s, qt);
-        bool ok = mbar_wait(q_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA) && kvwait(kq);
+        bool ok = mbar_wait(q_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA) && kwait(kq);
         if (!ok) break;
         tc_fence_after();
         issue_ss<D>(tmem + 0, qb, kbase(kq));            // S_0 = Q K_0^T
         mma_commit(&s_full[0]);
-        issue_ss<D>(tP, dob, kbase(kq) + L::TB);          // dP_0 = dO V_0^T
+        if (!vwait(kq)) break;
+        tc_fence_after();
+        issue_ss<D>(tP, dob, vbase(kq));                  // dP_0 = dO V_0^T
         mma_commit(dp_full);
         if (n > 1) {
-          if (!kvwait(kq + 1)) break;
+          if (!kwait(kq + 1)) break;
           tc_fence_after();
           issue_ss<D>(tmem + 128, qb, kbase(kq + 1));
           mma_commit(&s_full[1]);
@@ -659,13 +699,16 @@ __global__ void __launch_bounds__(384, 1)
           if (!ok) break;
           tc_fence_after();
           issue_ts<D>(tdQ, tP, kbase(kq + j), j > 0);       // dQ += dS K_j
-          mma_commit(&kv_empty[(kq + j) % L::STAGES]);
+          mma_commit(&k_empty[(kq + j) % L::KST]);
           if (j + 1 < n) {
-            issue_ss<D>(tP, dob, kbase(kq + j + 1) + L::TB);  // dP_{j+1}
+            ok = vwait(kq + j + 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_ss<D>(tP, dob, vbase(kq + j + 1));          // dP_{j+1}
             mma_commit(dp_full);
           }
           if (j + 2 < n) {
-            ok = kvwait(kq + j + 2);
+            ok = kwait(kq + j + 2);
             if (!ok) break;
             tc_fence_after();
             issue_ss<D>(tmem + (j & 1) * 128, qb, kbase(kq + j + 2));
@@ -680,13 +723,13 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp >= 4) {  // -------------------------------------------------- gradient warps
     const int wq = warp & 3;
-    uint8_t* scratch = smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES;
+    uint8_t* scratch = L::SCRATCH ? smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES : nullptr;
     const int c0 = ((warp - 4) >> 2) * 64;  // this warpgroup's first key column
     const int r = wq * 32 + lane_id();
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tP = tmem + lanes + 256, tdQ = tmem + lanes + 384;
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-    uint32_t sph[2] = {0, 0}, dph = 0;
+    uint32_t sph[2] = {0, 0}, dph = 0, kq = 0;
     for (int it = 0;; ++it) {
       const int slot = it & 1;
       bool ok = mbar_wait(&unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
@@ -738,6 +781,7 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
+        if (warp == 4 && lane_id() == 0) mbar_arrive(&v_empty[(kq + j) % L::VST]);  // dP_j done: V_j is free
         tc_fence_after();
         // dS = P o (dP - D_row), written as bf16 over the dP columns already read
 #pragma unroll
@@ -765,6 +809,7 @@ __global__ void __launch_bounds__(384, 1)
       __nv_bfloat16* dq0 = reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sb +
                            static_cast<int64_t>(q0) * p.dq.sn + h * p.dq.sh;
       store_acc_rows<D / 2>(tdQ, (c0 / 64) * (D / 2), p.scale, dq0, p.dq.sn, s.Nq - q0, scratch);
+      kq += n;
     }
   }
   tc_fence_before();

@@ -42,14 +42,18 @@ template <int D>
 struct FwdLayout {
   static constexpr int QB = TILE * D * 2;    // one Q tile (bytes)
   static constexpr int TB = TILE * D * 2;    // one K or V tile
-  static constexpr int STAGES = D == 64 ? 6 : 4;
+  static constexpr int STAGES = D == 64 ? 6 : 4;  // K/V tile slots
+  // Slots are used in pairs: group 0 of a unit holds K_0, group j+1 holds V_j and
+  // K_{j+1} (the two tiles the step after S_j reads), so a step costs the MMA
+  // thread one wait and one release instead of two of each.
+  static constexpr int NG = STAGES / 2;
   static constexpr int CH = D / 64;          // 64-column swizzle atoms per tile row
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = 2 * QB;
   static constexpr int OFF_BAR = OFF_KV + STAGES * TB;
-  // barriers: unit_full[2] unit_empty[2] q_full q_empty kv_full[S] kv_empty[S]
+  // barriers: unit_full[2] unit_empty[2] q_full q_empty kv_full[NG] kv_empty[NG]
   //           s_full[2] p_full[2] o_full[2] o_empty[2]
-  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 8;
+  static constexpr int NBAR = 4 + 2 + 2 * NG + 8;
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
   static constexpr int OFF_SCR = (OFF_TMEM + 16 + 127) / 128 * 128;  // row-store scratch, one per softmax warp
@@ -83,8 +87,8 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   r.q_full = b + 4;
   r.q_empty = b + 5;
   r.kv_full = b + 6;
-  r.kv_empty = r.kv_full + L::STAGES;
-  r.s_full = r.kv_empty + L::STAGES;
+  r.kv_empty = r.kv_full + L::NG;
+  r.s_full = r.kv_empty + L::NG;
   r.p_full = r.s_full + 2;
   r.o_full = r.p_full + 2;
   r.o_empty = r.o_full + 2;
@@ -107,7 +111,7 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
                              const Ctl& ctl) {
   using L = FwdLayout<D>;
   const int g = p.dims.Hq / p.dims.Hkv;
-  uint32_t seq = 0;       // K/V tiles issued so far (ring sequence number)
+  uint32_t seq = 0;       // K/V groups issued so far (ring sequence number)
   int q_armed = -1;       // last unit index whose Q load was issued
   for (int it = 0;; ++it) {
     const int slot = it & 1;
@@ -133,30 +137,30 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
     q_armed = it;
 
     bool ok = true;
-    for (int j = 0; j < nmax && ok; ++j) {
+    for (int gi = 0; gi <= nmax; ++gi, ++seq) {  // group gi: V_{gi-1} (slot A), K_gi (slot B)
+      const int gs = seq % L::NG;
+      if (!mbar_wait(&bar.kv_empty[gs], ((seq / L::NG) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
+        ok = false;
+        break;
+      }
+      const bool has_v = gi > 0, has_k = gi < nmax;
+      uint8_t* base = smem + L::OFF_KV + gs * 2 * L::TB;
+      mbar_arrive_expect_tx(&bar.kv_full[gs], (has_v + has_k) * L::TB);
 #pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        const int s = seq % L::STAGES;
-        const uint32_t ph = (seq / L::STAGES) & 1;
-        if (!mbar_wait(&bar.kv_empty[s], ph ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&bar.kv_full[s], L::TB);
-#pragma unroll
-        for (int c = 0; c < L::CH; ++c)
-          tma_load_4d(smem + L::OFF_KV + s * L::TB + c * (TILE * 128), kv ? tm_v : tm_k, &bar.kv_full[s], c * 64,
-                      kvh, j * TILE, b);
-        ++seq;
+      for (int c = 0; c < L::CH; ++c) {
+        if (has_v)
+          tma_load_4d(base + c * (TILE * 128), tm_v, &bar.kv_full[gs], c * 64, kvh, (gi - 1) * TILE, b);
+        if (has_k)
+          tma_load_4d(base + L::TB + c * (TILE * 128), tm_k, &bar.kv_full[gs], c * 64, kvh, gi * TILE, b);
       }
     }
     if (!ok) break;
   }
   // Let every copy still in flight land before the CTA can exit.
-  for (int s = 0; s < L::STAGES; ++s) {
-    if (seq > static_cast<uint32_t>(s)) {
-      const uint32_t last = seq - 1 - ((seq - 1 - s) % L::STAGES);  // last sequence number on stage s
-      mbar_wait(&bar.kv_full[s], (last / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+  for (int gs = 0; gs < L::NG; ++gs) {
+    if (seq > static_cast<uint32_t>(gs)) {
+      const uint32_t last = seq - 1 - ((seq - 1 - gs) % L::NG);  // last group issued on slot pair gs
+      mbar_wait(&bar.kv_full[gs], (last / L::NG) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
     }
   }
   if (q_armed >= 0) mbar_wait(bar.q_full, q_armed & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
@@ -175,25 +179,29 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
   uint32_t pph[2] = {0, 0};
   uint32_t active[2] = {0, 0};
 
-  auto issue_s = [&](int t, int stage) {
+  auto issue_s = [&](int t, uint32_t k_addr) {
     const uint32_t d_tmem = tmem + t * 128;
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
       const uint32_t off = (k / 4) * (TILE * 128) + (k % 4) * 32;
       const uint64_t a = sdesc_sw128(q_base + t * L::QB + off, 16, 1024);
-      const uint64_t bd = sdesc_sw128(kv_base + stage * L::TB + off, 16, 1024);
+      const uint64_t bd = sdesc_sw128(k_addr + off, 16, 1024);
       mma_ss(d_tmem, a, bd, IDESC_S, k > 0);
     }
   };
-  auto issue_pv = [&](int t, int stage, bool acc) {
+  auto issue_pv = [&](int t, uint32_t v_addr, bool acc) {
     const uint32_t d_tmem = tmem + 256 + t * D;
     const uint32_t p_tmem = tmem + t * 128;
 #pragma unroll
     for (int k = 0; k < TILE / 16; ++k) {
-      const uint64_t bd = sdesc_sw128(kv_base + stage * L::TB + k * 16 * 128, TILE * 128, 1024);
+      const uint64_t bd = sdesc_sw128(v_addr + k * 16 * 128, TILE * 128, 1024);
       mma_ts(d_tmem, p_tmem + k * 8, bd, IDESC_O, (acc || k > 0) ? 1u : 0u);
     }
   };
+  auto group_wait = [&](uint32_t gq) {
+    return mbar_wait(&bar.kv_full[gq % L::NG], (gq / L::NG) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+  };
+  auto group_base = [&](uint32_t gq) { return kv_base + (gq % L::NG) * 2 * L::TB; };
 
   for (int it = 0;; ++it) {
     const int slot = it & 1;
@@ -207,47 +215,41 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
     const int nmax = imax(n[0], n[1]);
 
     if (!mbar_wait(bar.q_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
-    // K_0
+    // group 0: K_0
     {
-      const int s = seq % L::STAGES;
-      if (!mbar_wait(&bar.kv_full[s], (seq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+      if (!group_wait(seq)) return;
       tc_fence_after();
       for (int t = 0; t < 2; ++t)
         if (n[t] > 0) {
-          issue_s(t, s);
+          issue_s(t, group_base(seq) + L::TB);
           mma_commit(&bar.s_full[t]);
         }
       if (nmax == 1) mma_commit(bar.q_empty);
-      mma_commit(&bar.kv_empty[s]);
+      mma_commit(&bar.kv_empty[seq % L::NG]);
     }
     for (int j = 0; j < nmax; ++j) {
-      const uint32_t vseq = seq + 2 * j + 1, kseq = seq + 2 * j + 2;
-      const int vs = vseq % L::STAGES, ks = kseq % L::STAGES;
-      const bool need_k = j + 1 < nmax;
-      if (!mbar_wait(&bar.kv_full[vs], (vseq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
-      if (need_k && !mbar_wait(&bar.kv_full[ks], (kseq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+      const uint32_t gq = seq + 1 + j;  // group j+1: V_j, and K_{j+1} unless this is the last step
+      if (!group_wait(gq)) return;
+      const uint32_t v_addr = group_base(gq), k_addr = v_addr + L::TB;
       for (int t = 0; t < 2; ++t) {
         if (j >= n[t]) continue;
         if (j == 0 && !mbar_wait(&bar.o_empty[t], (active[t] & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
         if (!mbar_wait(&bar.p_full[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
         pph[t] ^= 1;
         tc_fence_after();
-        issue_pv(t, vs, j > 0);
+        issue_pv(t, v_addr, j > 0);
         if (j == n[t] - 1) mma_commit(&bar.o_full[t]);
         if (j + 1 < n[t]) {
-          issue_s(t, ks);
+          issue_s(t, k_addr);
           mma_commit(&bar.s_full[t]);
         }
       }
-      mma_commit(&bar.kv_empty[vs]);
-      if (need_k) {
-        if (j + 1 == nmax - 1) mma_commit(bar.q_empty);
-        mma_commit(&bar.kv_empty[ks]);
-      }
+      if (j + 1 == nmax - 1) mma_commit(bar.q_empty);
+      mma_commit(&bar.kv_empty[gq % L::NG]);
     }
     for (int t = 0; t < 2; ++t)
       if (n[t] > 0) ++active[t];
-    seq += 2 * nmax;
+    seq += nmax + 1;
   }
 }
 

@@ -183,9 +183,9 @@ struct DkvLayout {
   static constexpr int OFF_V = TB;
   static constexpr int OFF_ST = 2 * TB;
   static constexpr int OFF_BAR = OFF_ST + STAGES * STAGE;
-  // unit_full[2] unit_empty[2] kv_full kv_empty st_full[S] st_empty[S] s_full dp_full p_full[2] ds_full[2]
+  // unit_full[2] unit_empty[2] kv_full kv_empty st_full[S] st_empty[S] s_full dp_full p_full[2] ds_full
   // acc_full
-  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 7;
+  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 6;
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
   static constexpr int OFF_SCR = (OFF_TMEM + 16 + 127) / 128 * 128;  // row-store scratch, one per gradient warp
@@ -211,8 +211,8 @@ __device__ __forceinline__ DkvBars dkv_bars(uint8_t* smem) {
   r.s_full = r.st_empty + L::STAGES;
   r.dp_full = r.s_full + 1;
   r.p_full = r.s_full + 2;   // [2]: one per 32-column chunk of each warpgroup's half
-  r.ds_full = r.s_full + 4;  // [2]
-  r.acc_full = r.s_full + 6;
+  r.ds_full = r.s_full + 4;
+  r.acc_full = r.s_full + 5;
   return r;
 }
 
@@ -258,10 +258,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(bar.s_full, 1);
     mbar_init(bar.dp_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar.p_full[i], 8);
-      mbar_init(&bar.ds_full[i], 8);
-    }
+    for (int i = 0; i < 2; ++i) mbar_init(&bar.p_full[i], 8);
+    mbar_init(bar.ds_full, 8);
     mbar_init(bar.acc_full, 1);
     fence_barrier_init();
   }
@@ -366,15 +364,12 @@ __global__ void __launch_bounds__(384, 1)
             issue_ss<D>(tS, kb, nxt);
             mma_commit(bar.s_full);
           }
-          // dK += dS^T Q, by halves as for dV
-          ok = mbar_wait(&bar.ds_full[0], dph, ctl, FA_STATUS_TIMEOUT_MMA);
-          if (!ok) break;
-          tc_fence_after();
-          issue_ts_half<D, 0>(tdK, tP, cur, k > 0);
-          ok = mbar_wait(&bar.ds_full[1], dph, ctl, FA_STATUS_TIMEOUT_MMA);
+          // dK += dS^T Q (whole: a second hand-off here costs more than it overlaps)
+          ok = mbar_wait(bar.ds_full, dph, ctl, FA_STATUS_TIMEOUT_MMA);
           dph ^= 1;
           if (!ok) break;
           tc_fence_after();
+          issue_ts_half<D, 0>(tdK, tP, cur, k > 0);
           issue_ts_half<D, 1>(tdK, tP, cur, true);
           mma_commit(&bar.st_empty[(sq + k) % L::STAGES]);
           if (more) {
@@ -470,7 +465,7 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
         tc_fence_after();
-        // dS^T = P^T o (dP^T - D[query]), in the same two chunks
+        // dS^T = P^T o (dP^T - D[query]), in the same two chunks, announced together
         {
           uint32_t sr[64];
           tmem_ld64(tP + c0, sr);
@@ -490,9 +485,9 @@ __global__ void __launch_bounds__(384, 1)
             }
             tmem_st16(tP + c0 + 16 * cc, dk);
             tmem_wait_st();
-            tc_fence_before();
-            warp_arrive(&bar.ds_full[cc]);
           }
+          tc_fence_before();
+          warp_arrive(bar.ds_full);
         }
       }
       if (!ok) break;

@@ -305,6 +305,13 @@ __global__ void __launch_bounds__(384, 1)
           }
           bulk_load(base + 2 * L::TB, p.neg_lse2 + row0, 512, &bar.st_full[st]);
           bulk_load(base + 2 * L::TB + 512, p.neg_delta + row0, 512, &bar.st_full[st]);
+          if (k + 1 < w.n_it) {  // the next iteration's Q and dO into L2 while this stage waits its turn
+            const int hq1 = w.kvh * g + (k + 1) / w.nqi, qi1 = w.q0 + (k + 1) % w.nqi;
+            for (int c = 0; c < D / 64; ++c) {
+              tma_prefetch_l2_4d(&tm_q, c * 64, hq1, qi1 * TILE, w.b);
+              tma_prefetch_l2_4d(&tm_do, c * 64, hq1, qi1 * TILE, w.b);
+            }
+          }
         }
         if (!ok) break;
       }

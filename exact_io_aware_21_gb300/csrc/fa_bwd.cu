@@ -538,8 +538,11 @@ struct DqLayout {
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
   static constexpr int OFF_SCR = (OFF_TMEM + 16 + 127) / 128 * 128;  // row-store scratch, one per dQ warp
-  // At d = 128 the rings leave no room for the scratch: dQ rows are stored directly.
+  // At d = 128 the rings leave no room for a dedicated scratch: the epilogue then
+  // stages its rows in the Q tile, which every S of the unit has finished reading,
+  // and the dQ warps (not the MMA thread) release Q and dO for the next unit.
   static constexpr bool SCRATCH = OFF_SCR + 8 * ROW_SCRATCH_BYTES + 1024 <= 227 * 1024;
+  static_assert(SCRATCH || 8 * ROW_SCRATCH_BYTES <= TB, "the Q tile holds the epilogue scratch");
   static constexpr int ALLOC = (SCRATCH ? OFF_SCR + 8 * ROW_SCRATCH_BYTES : OFF_TMEM + 16) + 1024;
 };
 
@@ -578,7 +581,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&s_full[i], 1);
     }
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(q_empty, L::SCRATCH ? 1 : 8);
     for (int i = 0; i < L::KST; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
@@ -719,13 +722,13 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (!ok) break;
         mma_commit(acc_full);
-        mma_commit(q_empty);
+        if (L::SCRATCH) mma_commit(q_empty);
         kq += n;
       }
     }
   } else if (warp >= 4) {  // -------------------------------------------------- gradient warps
     const int wq = warp & 3;
-    uint8_t* scratch = L::SCRATCH ? smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES : nullptr;
+    uint8_t* scratch = smem + (L::SCRATCH ? L::OFF_SCR : L::OFF_Q) + (warp - 4) * ROW_SCRATCH_BYTES;
     const int c0 = ((warp - 4) >> 2) * 64;  // this warpgroup's first key column
     const int r = wq * 32 + lane_id();
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
@@ -811,6 +814,10 @@ __global__ void __launch_bounds__(384, 1)
       __nv_bfloat16* dq0 = reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sb +
                            static_cast<int64_t>(q0) * p.dq.sn + h * p.dq.sh;
       store_acc_rows<D / 2>(tdQ, (c0 / 64) * (D / 2), p.scale, dq0, p.dq.sn, s.Nq - q0, scratch);
+      if (!L::SCRATCH) {  // the Q tile was the scratch: order these accesses before the next TMA write
+        fence_proxy_async_smem();
+        warp_arrive(q_empty);
+      }
       kq += n;
     }
   }

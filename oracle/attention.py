@@ -24,6 +24,11 @@ Definitions followed (one bullet per function below):
   * FlashDecoding: each KV split t yields (m_t, l_t, O_t) with O_t the
     unnormalised local output; the combine is O = sum_t O_t e^{m_t - m} /
     sum_t l_t e^{m_t - m}.  §18.8.2 and lecture slides 57-60.
+  * paged, variable-length decode: a sequence's logical KV row r lives in the
+    physical page block_table[b, r // page_size], at row r % page_size
+    (PagedAttention's page table, §18.8.2 part 3 and §18.8.3); each sequence
+    attends over its own first seqlens[b] rows, non-causally, which is the
+    forward above applied to the gathered rows.
 
 Large inputs are processed in blocks of whole query rows; every row's softmax
 is still complete inside one block, so this is the plain definition, not a
@@ -276,6 +281,37 @@ def decode_combine(m, l, Ot):
     den = np.sum(l * w, axis=-1)
     O = np.sum(Ot * w[..., None], axis=-2) / den[..., None]
     return O, mg + np.log(den)
+
+
+def gather_paged(cache, block_table, b, length):
+    """Logical rows [0, length) of sequence b from a paged cache [pages, page_size, H, d]:
+    row r is at page block_table[b, r // page_size], row r % page_size."""
+    cache = np.asarray(cache)
+    page_size = cache.shape[1]
+    r = np.arange(length)
+    return cache[np.asarray(block_table)[b, r // page_size], r % page_size]
+
+
+def attention_decode_paged(q, k_cache, v_cache, block_table, seqlens, scale):
+    """Decode over a paged, variable-length KV cache.
+
+    q [B, Nq, Hq, d]; k_cache, v_cache [pages, page_size, Hkv, d]; block_table
+    [B, max_pages] int; seqlens [B] int >= 1.  Sequence b attends, non-causally,
+    over its own first seqlens[b] logical KV rows.  Returns (O [B, Nq, Hq, d],
+    LSE [B, Hq, Nq]).
+    """
+    q = _f64(q)
+    kc, vc = _f64(k_cache), _f64(v_cache)
+    B, Nq, Hq, d = q.shape
+    O = np.zeros((B, Nq, Hq, d))
+    LSE = np.zeros((B, Hq, Nq))
+    for b in range(B):
+        L = int(seqlens[b])
+        kb = gather_paged(kc, block_table, b, L)[None]
+        vb = gather_paged(vc, block_table, b, L)[None]
+        Ob, LSEb = attention_forward(q[b:b + 1], kb, vb, scale, causal=False)
+        O[b], LSE[b] = Ob[0], LSEb[0]
+    return O, LSE
 
 
 def flops_forward(B, Hq, Nq, Nk, d, causal):

@@ -7,7 +7,8 @@ in HBM:
                  causal_b2_h16_n4096_d128   (B=2, H=16, N=4096, d=128, causal)
                  gqa_causal_b1_hq32_hkv8_n8192_d128_outliers
   decode legs    split-KV decode + combine of
-                 decode_b8_hq32_hkv8_q1_kv131072_d128 and the q4 variant
+                 decode_b8_hq32_hkv8_q1_kv131072_d128 and the q4 variant, and the
+                 q1 cache in shuffled pages of 16 keys through fa_decode_paged
 ``value`` = counted forward + backward FLOPs of the training legs divided by
 their device time (TFLOPS; forward 4*B*H*Nq*Nk*d, halved when causal, backward
 2.5x that).  Decode legs report KV-read GB/s.  L2 is flushed (256 MiB write)
@@ -39,7 +40,10 @@ import torch  # noqa: E402
 
 TRAIN = ("causal_b2_h16_n4096_d128", "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers")
 DECODE = ("decode_b8_hq32_hkv8_q1_kv131072_d128", "decode_b8_hq32_hkv8_q4_kv131072_d128")
-WORKLOAD = " + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode)"
+PAGED = ("decode_b8_hq32_hkv8_q1_kv131072_d128", 16)  # the q1 decode cache in shuffled pages of 16 keys
+PAGED_NAME = PAGED[0] + "_paged16"
+WORKLOAD = (" + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode); " + PAGED_NAME +
+            " (paged decode)")
 METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -50,7 +54,7 @@ def workloads():
     from exact_io_aware_21_gb300 import inputs
 
     by = {w.name: w for w in inputs.ALL}
-    return [by[n] for n in TRAIN], [by[n] for n in DECODE]
+    return [by[n] for n in TRAIN], [by[n] for n in DECODE] + [by[PAGED[0]]]
 
 
 def fwd_flops(w):
@@ -299,7 +303,9 @@ def make_legs(device, seed):
         fns = [("fwd", fwd), ("bwd_pre", lambda part=part: part(0)), ("bwd_dkdv", lambda part=part: part(1)),
                ("bwd_dq", lambda part=part: part(2))]
         legs.append(Leg(w.name, "train", w, fns, 3.5 * fwd_flops(w)))
-    for w in dec:
+    for i, w in enumerate(dec):
+        paged = i == len(dec) - 1
+        name = PAGED_NAME if paged else w.name
         x = inputs.make(w, device=device, with_do=False, seed=w.seed + seed)
         s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, False)
         S = lib.fa_decode_num_splits(ctypes.byref(s), 0)
@@ -307,14 +313,37 @@ def make_legs(device, seed):
                   lse=torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=device),
                   ws=torch.zeros(lib.fa_decode_workspace_size(ctypes.byref(s), S), dtype=torch.uint8,
                                  device=device))
-        state[w.name] = st
+        if paged:  # every sequence at full length, its pages scattered over the cache
+            st.update(paged_cache(x, PAGED[1], seed=w.seed + seed))
+        state[name] = st
 
         def dec_fn(st=st):
             x = st["x"]
             B.fa_decode(x["q"], x["k"], x["v"], st["o"], st["lse"], st["s"], st["S"], st["ws"])
 
-        legs.append(Leg(w.name, "decode", w, [("decode", dec_fn)], kv_bytes(w)))
+        def paged_fn(st=st):
+            B.fa_decode_paged(st["x"]["q"], st["kc"], st["vc"], st["table"], st["lens"], st["o"], st["lse"],
+                              st["s"], st["S"], st["ws"])
+
+        legs.append(Leg(name, "decode", w, [("decode", paged_fn if paged else dec_fn)], kv_bytes(w)))
     return legs, state
+
+
+def paged_cache(x, page_size, seed):
+    """Move x's contiguous K/V cache into pages of `page_size` keys in a shuffled order."""
+    k, v = x.pop("k"), x.pop("v")
+    B, N, H, d = k.shape
+    npb = N // page_size
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    perm = torch.randperm(B * npb, generator=gen).to(k.device)
+    kc = torch.empty((B * npb, page_size, H, d), dtype=k.dtype, device=k.device)
+    vc = torch.empty_like(kc)
+    kc[perm] = k.reshape(B * npb, page_size, H, d)
+    del k
+    vc[perm] = v.reshape(B * npb, page_size, H, d)
+    del v
+    return dict(kc=kc, vc=vc, table=perm.to(torch.int32).reshape(B, npb).contiguous(),
+                lens=torch.full((B,), N, dtype=torch.int32, device=kc.device))
 
 
 def traffic_for(kernel, workload):

@@ -10,10 +10,12 @@ from .binding import (  # noqa: F401
     FAError,
     fa_bwd,
     fa_decode,
+    fa_decode_paged,
     fa_fwd,
     forward,
     backward,
     decode,
+    decode_paged,
     library,
     library_path,
 )

@@ -54,6 +54,7 @@ SIGNATURES = {
     "fa_decode_workspace_size": (_SZ, [_PS, _I]),
     "fa_decode": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _I, _VP, _SZ, _VP]),
     "fa_decode_partials_layout": (_I, [_PS, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
+    "fa_decode_paged": (_I, [_PT, _PT, _PT, _VP, _I, _VP, _I, _I, _PT, _VP, _PS, _I, _VP, _SZ, _VP]),
     "fa_decode_noalloc_max_bytes": (_SZ, []),
     "fa_decode_noalloc": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _I, _VP]),
     "fa_get_device_status": (_I, [_VP, _VP, _PI]),
@@ -150,6 +151,17 @@ def fa_decode(q, kc, vc, o, lse, s, num_splits, workspace):
                         workspace.data_ptr(), workspace.numel(), _stream(q)))
 
 
+def fa_decode_paged(q, kc, vc, block_table, seqlens_k, o, lse, s, num_splits, workspace):
+    """kc, vc: [num_pages, page_size, Hkv, d] bf16; block_table [B, max_pages] and
+    seqlens_k [B] int32 CUDA tensors (contiguous)."""
+    lib = library()
+    if block_table.dtype != torch.int32 or seqlens_k.dtype != torch.int32 or not block_table.is_contiguous():
+        raise FAError(1, "block_table and seqlens_k must be contiguous int32 CUDA tensors")
+    check(lib.fa_decode_paged(tdesc(q), tdesc(kc), tdesc(vc), block_table.data_ptr(), block_table.shape[1],
+                              seqlens_k.data_ptr(), kc.shape[0], kc.shape[1], tdesc(o), lse.data_ptr(),
+                              ctypes.byref(s), int(num_splits), workspace.data_ptr(), workspace.numel(), _stream(q)))
+
+
 def device_status(workspace):
     """Synchronise and return (rc, status bits) recorded in the workspace."""
     lib = library()
@@ -198,4 +210,23 @@ def decode(q, k_cache, v_cache, scale=None, num_splits=0):
     lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
     ws = _ws(library().fa_decode_workspace_size(ctypes.byref(s), int(num_splits)), q.device)
     fa_decode(q, k_cache, v_cache, o, lse, s, num_splits, ws)
+    return o, lse
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seqlens_k, max_seqlen=None, scale=None, num_splits=0):
+    """Decode against a paged, variable-length cache (see fa_decode_paged in include/fa.h).
+
+    q [B,Nq,Hq,d]; k_cache/v_cache [num_pages, page_size, Hkv, d]; block_table
+    [B, max_pages] int32; seqlens_k [B] int32.  ``max_seqlen`` bounds the
+    lengths (defaults to seqlens_k.max(), which reads it back to the host).
+    """
+    B, Nq, Hq, d = q.shape
+    Hkv = k_cache.shape[2]
+    if max_seqlen is None:
+        max_seqlen = int(seqlens_k.max().item())
+    s = shape(B, Hq, Hkv, Nq, int(max_seqlen), d, scale, False)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    ws = _ws(library().fa_decode_workspace_size(ctypes.byref(s), int(num_splits)), q.device)
+    fa_decode_paged(q, k_cache, v_cache, block_table, seqlens_k, o, lse, s, num_splits, ws)
     return o, lse

@@ -73,14 +73,15 @@ EncodeTiledFn encode_fn() {
 
 // 4-D map over a bf16 [B, N, H, d] tensor: dims (d, H, N, B); box 64 x 1 x 128 x 1,
 // 128-byte swizzle; rows past N read as zero.
-int make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int64_t sb, int64_t sn, int64_t sh) {
+int make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int64_t sb, int64_t sn, int64_t sh,
+             int box_rows = TILE) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return FA_ERR_CUDA;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(sn) * 2,
                            static_cast<cuuint64_t>(sb) * 2};
-  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(TILE), 1};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -238,7 +239,8 @@ int fa_get_device_status(void* ws, void* stream, int* status) {
   e = cudaMemset(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET, 0, sizeof(int));
   if (e != cudaSuccess) return cuda_fail(e, FA_ERR_CUDA);
   *status = v;
-  return (v & FA_STATUS_TIMEOUT_MASK) ? FA_ERR_TIMEOUT : FA_OK;
+  if (v & FA_STATUS_TIMEOUT_MASK) return FA_ERR_TIMEOUT;
+  return (v & FA_STATUS_BAD_INPUT) ? FA_ERR_INVALID : FA_OK;
 }
 
 // ------------------------------------------------------------------------ forward
@@ -402,6 +404,58 @@ int fa_decode(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor_t* vc
   a.chunk = decode_chunk(s->Nk, S);
   a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
   a.timeout_ns = g_timeout_ns;
+  if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
+  cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
+}
+
+int fa_decode_paged(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor_t* vc, const int* block_table,
+                    int max_pages, const int* seqlens_k, int num_pages, int page_size, const fa_tensor_t* o,
+                    float* lse, const fa_shape_t* s, int num_splits, void* ws, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_shape(s)) || (rc = check_tensor(q)) || (rc = check_tensor(kc)) || (rc = check_tensor(vc)) ||
+      (rc = check_tensor(o)))
+    return rc;
+  if (!lse || s->causal || !block_table || !seqlens_k || max_pages < 1 || num_pages < 1) return FA_ERR_INVALID;
+  if ((s->Hq / s->Hkv) * s->Nq > 16) return FA_ERR_INVALID;
+  // pages of 16, 32 or 64 keys stack into a 128-key tile; larger pages hold whole tiles
+  const bool small = page_size == 16 || page_size == 32 || page_size == 64;
+  if (!small && (page_size < TILE || page_size % TILE != 0)) return FA_ERR_INVALID;
+  if (static_cast<int64_t>(max_pages) * page_size < s->Nk) return FA_ERR_INVALID;
+  int sms = 0;
+  if ((rc = device_info(&sms))) return rc;
+  const int S = decode_splits_resolved(s, num_splits, sms);
+  if ((rc = check_ws(ws, ws_bytes, fa_decode_workspace_size(s, num_splits)))) return rc;
+  DecodeLaunch a;
+  memset(&a, 0, sizeof(a));
+  a.dims = dims_of(s);
+  a.d = s->d;
+  a.scale = s->scale;
+  const int box_rows = small ? page_size : TILE;
+  if ((rc = make_map(&a.tm_k, kc->ptr, num_pages, page_size, s->Hkv, s->d, kc->stride_b, kc->stride_n,
+                     kc->stride_h, box_rows)) ||
+      (rc = make_map(&a.tm_v, vc->ptr, num_pages, page_size, s->Hkv, s->d, vc->stride_b, vc->stride_n,
+                     vc->stride_h, box_rows)))
+    return rc;
+  a.q = q->ptr;
+  a.q_sb = q->stride_b;
+  a.q_sn = q->stride_n;
+  a.q_sh = q->stride_h;
+  a.o = rows_of(o);
+  a.lse = lse;
+  size_t lo = 0, oo = 0;
+  fa_decode_partials_layout(s, num_splits, &lo, &oo);
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(ws) + lo);
+  a.o_part = reinterpret_cast<float*>(static_cast<char*>(ws) + oo);
+  a.num_splits = S;
+  a.chunk = 0;  // per sequence, in the kernel
+  a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
+  a.timeout_ns = g_timeout_ns;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.seqlens = seqlens_k;
+  a.num_pages = num_pages;
+  a.page_size = page_size;
   if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
   cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);

@@ -19,6 +19,18 @@
 // the split ends.  (A 128-row tcgen05 product would be 87% padding here.)
 // The warps' states are merged through shared memory into the split's
 // (LSE_s, O_s); the combine kernel then merges the splits.
+//
+// Paged, variable-length cache (§18.8.2 part 3, §18.8.3: PagedAttention keeps
+// the cache in fixed-size physical pages and maps each sequence's logical pages
+// through a page table; each sequence has its own length).  The same kernel,
+// with the producer resolving every 128-key tile through the page table: one
+// TMA box per tile when a page holds whole tiles, else one box per page (pages
+// of 16-64 keys stack into the tile with the same 128-byte swizzle, since each
+// is a whole number of 8-row swizzle atoms).  Each sequence is split by its own
+// length; splits past its end write an empty partial (LSE -inf, O 0).  Keys past
+// the end of a sequence inside its last tile hold whatever the page (or an
+// earlier tile) left in shared memory: their scores are masked and their V rows
+// are zeroed in registers, so even NaN there cannot reach O.
 #include <math.h>
 
 #include "fa_kernels.h"
@@ -55,6 +67,10 @@ struct DecParams {
   int num_splits, chunk;
   int* status;
   unsigned long long timeout_ns;
+  const int* block_table;  // paged: [B, max_pages]
+  int max_pages;
+  const int* seqlens;      // paged: [B]
+  int num_pages, page_size;
 };
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -86,7 +102,7 @@ __device__ __forceinline__ uint32_t swz(int key, int ch) {
   return (ch >> 6) * (TILE * 128) + key * 128 + ((((ch & 63) >> 3) ^ (key & 7)) << 4) + ((ch & 7) << 1);
 }
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(THREADS, 1)
     fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecParams p) {
@@ -99,11 +115,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   const Dims& s = p.dims;
   const int g = s.Hq / s.Hkv;
   const int rows = g * s.Nq;
-  const int k0 = split * p.chunk;
-  const int k1 = imin(s.Nk, k0 + p.chunk);
-  const int ntiles = cdiv(k1 - k0, TILE);
   const int warp = threadIdx.x >> 5, lane = lane_id();
   const Ctl ctl{p.status, p.timeout_ns};
+  int len = s.Nk, chunk = p.chunk;  // this sequence's keys and its split length
+  if (PAGED) {
+    len = p.seqlens[b];
+    if (len < 1 || len > s.Nk) {
+      if (threadIdx.x == 0 && split == 0 && kvh == 0) report(ctl, FA_STATUS_BAD_INPUT);
+      len = imax(0, imin(len, s.Nk));
+    }
+    chunk = cdiv(cdiv(len, TILE), p.num_splits) * TILE;
+  }
+  const int k0 = split * chunk;
+  const int k1 = imin(len, k0 + chunk);
+  const int ntiles = k1 > k0 ? cdiv(k1 - k0, TILE) : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::STAGES; ++i) {
@@ -117,23 +142,70 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
 
   if (warp == WARPS) {  // ---------------------------------------------- producer
-    if (lane == 0) {
+    if (!PAGED) {
+      if (lane == 0) {
+        int issued = 0;
+        for (int t = 0; t < ntiles; ++t) {
+          const int st = t % L::STAGES;
+          if (!mbar_wait(&empty[st], ((t / L::STAGES) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
+          uint8_t* dst = smem + L::OFF_KV + st * 2 * L::TB;
+          const int kk = k0 + t * TILE;  // first key of the tile
+          mbar_arrive_expect_tx(&full[st], 2 * L::TB);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(dst + c * (TILE * 128), &tm_k, &full[st], c * 64, kvh, kk, b);
+            tma_load_4d(dst + L::TB + c * (TILE * 128), &tm_v, &full[st], c * 64, kvh, kk, b);
+          }
+          ++issued;
+        }
+        // wait for the copies in flight before the CTA may exit
+        for (int t = imax(0, issued - L::STAGES); t < issued; ++t)
+          mbar_wait(&full[t % L::STAGES], (t / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+      }
+    } else {
+      // The whole warp: lane i reads the page of box i of a tile and loads that box,
+      // so a tile's page-table reads go out together, one tile ahead of its loads.
+      // Boxes hold `rows_box` keys: one page (or a whole tile when pages hold whole
+      // tiles); none is loaded past the sequence's end, where the table need not be valid.
+      const int rows_box = imin(p.page_size, TILE);
+      const int64_t trow = static_cast<int64_t>(b) * p.max_pages;
+      auto page_of = [&](int t) {
+        const int off = lane * rows_box, key = k0 + t * TILE + off;
+        if (t >= ntiles || off >= TILE || key >= len) return -1;
+        int pg = p.block_table[trow + key / p.page_size];
+        if (pg < 0 || pg >= p.num_pages) {  // reads as zeros (out-of-range TMA box); reported
+          report(ctl, FA_STATUS_BAD_INPUT);
+          pg = p.num_pages;
+        }
+        return pg;
+      };
       int issued = 0;
+      int next_page = page_of(0);
       for (int t = 0; t < ntiles; ++t) {
         const int st = t % L::STAGES;
-        if (!mbar_wait(&empty[st], ((t / L::STAGES) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
-        mbar_arrive_expect_tx(&full[st], 2 * L::TB);
-        uint8_t* dst = smem + L::OFF_KV + st * 2 * L::TB;
+        const int page = next_page;
+        next_page = page_of(t + 1);
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[st], ((t / L::STAGES) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int kk = k0 + t * TILE;
+        const int nbox = imin(TILE / rows_box, cdiv(len - kk, rows_box));
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], 4 * nbox * rows_box * D);  // K and V boxes
+        __syncwarp();
+        if (lane < nbox) {
+          uint8_t* dst = smem + L::OFF_KV + st * 2 * L::TB + lane * rows_box * 128;
+          const int row = (kk + lane * rows_box) % p.page_size;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(dst + c * (TILE * 128), &tm_k, &full[st], c * 64, kvh, k0 + t * TILE, b);
-          tma_load_4d(dst + L::TB + c * (TILE * 128), &tm_v, &full[st], c * 64, kvh, k0 + t * TILE, b);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(dst + c * (TILE * 128), &tm_k, &full[st], c * 64, kvh, row, page);
+            tma_load_4d(dst + L::TB + c * (TILE * 128), &tm_v, &full[st], c * 64, kvh, row, page);
+          }
         }
         ++issued;
       }
-      // wait for the copies in flight before the CTA may exit
-      for (int t = imax(0, issued - L::STAGES); t < issued; ++t)
-        mbar_wait(&full[t % L::STAGES], (t / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+      if (lane == 0)
+        for (int t = imax(0, issued - L::STAGES); t < issued; ++t)
+          mbar_wait(&full[t % L::STAGES], (t / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
     }
     __syncthreads();  // pairs with the compute warps' barrier before the merge
     __syncthreads();
@@ -226,7 +298,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-    // O += P V: B fragments of V (16 keys x 8 channels) via transposed ldmatrix
+    // O += P V: B fragments of V (16 keys x 8 channels) via transposed ldmatrix.
+    // Paged: V rows past the split's end may hold anything (stale shared memory or
+    // an unused part of a page); they are zeroed, as their P is.  This thread's
+    // fragment halves cover keys key0 + 2tq (+1) and key0 + 8 + 2tq (+1).
+    uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+    if (PAGED && key0 + 16 > k1) {
+      const int ka = key0 + 2 * tq, kb8 = ka + 8;
+      vmask_lo = (ka < k1 ? 0x0000ffffu : 0u) | (ka + 1 < k1 ? 0xffff0000u : 0u);
+      vmask_hi = (kb8 < k1 ? 0x0000ffffu : 0u) | (kb8 + 1 < k1 ? 0xffff0000u : 0u);
+    }
 #pragma unroll
     for (int np = 0; np < D / 16; ++np) {
       // matrices: (keys 0-7, ch n0..), (keys 8-15, ch n0..), (keys 0-7, ch n0+8..), (keys 8-15, ch n0+8..)
@@ -234,6 +315,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int ch = np * 16 + 8 * (mat >> 1);
       uint32_t v0, v1, v2, v3;
       ldsm_x4_t(vb + swz(key, ch), v0, v1, v2, v3);
+      if (PAGED) {
+        v0 &= vmask_lo;
+        v2 &= vmask_lo;
+        v1 &= vmask_hi;
+        v3 &= vmask_hi;
+      }
       mma_16816(o[2 * np], pa, v0, v1);
       mma_16816(o[2 * np + 1], pa, v2, v3);
     }
@@ -288,7 +375,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       wt[w] = mw == -INFINITY ? 0.f : ex2(mw - mref);
       wsum += wt[w] * sm_l[w * 16 + row];
     }
-    const float inv = 1.f / wsum;
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;  // an empty split: O 0, LSE -inf
     const int qpos = row / g, hq = kvh * g + row % g;
     const int64_t prow = ((static_cast<int64_t>(b) * s.Hq + hq) * s.Nq + qpos) * p.num_splits + split;
 #pragma unroll
@@ -298,7 +385,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int w = 0; w < WARPS; ++w) acc += wt[w] * sm_o[(w * 16 + row) * D + chb + i];
       p.o_part[prow * D + chb + i] = acc * inv;
     }
-    if (chb == 0) p.lse_part[prow] = (mref + __log2f(wsum)) * LN2;
+    if (chb == 0) p.lse_part[prow] = wsum > 0.f ? (mref + __log2f(wsum)) * LN2 : -INFINITY;
   }
 }
 
@@ -316,18 +403,19 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const float* __r
   for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lp[s]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  const float mxs = mx == -INFINITY ? 0.f : mx;  // no split saw a key: O 0, LSE -inf
   float den = 0.f;
-  for (int s = lane; s < S; s += 32) den += __expf(lp[s] - mx);
+  for (int s = lane; s < S; s += 32) den += __expf(lp[s] - mxs);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-  const float lse_row = mx + __logf(den);
+  const float lse_row = mxs + __logf(den);
   constexpr int PER = D / 32;
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   const float* op = o_part + static_cast<int64_t>(row) * S * D;
   for (int s = 0; s < S; ++s) {
-    const float w = __expf(lp[s] - lse_row);
+    const float w = den > 0.f ? __expf(lp[s] - lse_row) : 0.f;
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] += w * op[s * D + lane * PER + i];
   }
@@ -343,7 +431,7 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const float* __r
 template <int D>
 cudaError_t launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
   using L = DecLayout<D>;
-  auto kern = fa_decode_split_kernel<D>;
+  auto kern = a.block_table != nullptr ? fa_decode_split_kernel<D, true> : fa_decode_split_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   DecParams p;
@@ -360,6 +448,11 @@ cudaError_t launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
   p.chunk = a.chunk;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
+  p.block_table = a.block_table;
+  p.max_pages = a.max_pages;
+  p.seqlens = a.seqlens;
+  p.num_pages = a.num_pages;
+  p.page_size = a.page_size;
   dim3 grid(a.num_splits, a.dims.Hkv, a.dims.B);
   kern<<<grid, THREADS, L::ALLOC, st>>>(a.tm_k, a.tm_v, p);
   e = cudaGetLastError();

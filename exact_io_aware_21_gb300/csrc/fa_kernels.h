@@ -59,9 +59,15 @@ struct DecodeLaunch {
   float* lse_part;  // [B, Hq, Nq, S]
   float* o_part;    // [B, Hq, Nq, S, d]
   int num_splits;
-  int chunk;        // keys per split (multiple of 128)
+  int chunk;        // keys per split (multiple of 128); paged: computed per sequence in the kernel
   int* status;
   unsigned long long timeout_ns;
+  // paged, variable-length cache (block_table == nullptr: contiguous [B, Nk, Hkv, d])
+  const int* block_table;  // [B, max_pages] physical page of each logical page
+  int max_pages;
+  const int* seqlens;      // [B] keys of each sequence, 1..Nk
+  int num_pages;
+  int page_size;           // 16, 32, 64, or a multiple of 128
 };
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t st);
 

@@ -158,6 +158,37 @@ int fa_decode(const fa_tensor_t* q, const fa_tensor_t* kcache, const fa_tensor_t
 int fa_decode_partials_layout(const fa_shape_t* shape, int num_splits, size_t* lse_offset, size_t* o_offset);
 
 /* ---------------------------------------------------------------------------
+ * Paged, variable-length decode.  §18.8.2 part 3 and §18.8.3 (PagedAttention):
+ * the KV cache lives in fixed-size physical pages; logical page i of sequence
+ * b is physical page block_table[b * max_pages + i], and sequence b has its own
+ * length seqlens_k[b].  Sequence b's logical key r is row r % page_size of page
+ * block_table[b * max_pages + r / page_size].  Otherwise as fa_decode: the same
+ * q, o, lse, shape (causal 0, Hq/Hkv * Nq <= 16), num_splits and workspace
+ * (fa_decode_workspace_size(shape, num_splits)).
+ *   kcache, vcache [num_pages, page_size, Hkv, d] bf16: stride_b = elements
+ *                  between pages, stride_n between rows of a page, stride_h
+ *                  between heads (16-byte aligned, multiples of 8 elements)
+ *   block_table    device int32 [B, max_pages]; entries for logical pages at or
+ *                  past ceil(seqlens_k[b] / page_size) are never read
+ *   seqlens_k      device int32 [B], each in [1, shape->Nk]
+ *   shape->Nk      the largest seqlens_k (an upper bound is fine); it sizes the
+ *                  split grid; max_pages * page_size must be >= shape->Nk
+ *   page_size      16, 32, 64, or a multiple of 128
+ * Each sequence is cut into whole 128-key tiles by its own length, with the
+ * chunk rule of fa_decode applied to seqlens_k[b]; splits past its end
+ * contribute nothing.  Keys past a sequence's end are never weighted, whatever
+ * the page holds there.  Device-side input errors (a length outside [1, Nk], a
+ * page index outside [0, num_pages)) set a status bit that
+ * fa_get_device_status() returns as FA_ERR_INVALID; such a page reads as zeros.
+ * Host-side: FA_ERR_INVALID for a bad page_size, max_pages, num_pages or null
+ * table/length pointers.
+ * ------------------------------------------------------------------------- */
+int fa_decode_paged(const fa_tensor_t* q, const fa_tensor_t* kcache, const fa_tensor_t* vcache,
+                    const int* block_table, int max_pages, const int* seqlens_k, int num_pages, int page_size,
+                    const fa_tensor_t* o, float* lse, const fa_shape_t* shape, int num_splits, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Decode without allocation.  No counterpart on the pages: this is a service
  * to callers that cannot allocate device memory, such as an inference server
  * that reserves all device memory for its own pool at start-up and forbids
@@ -189,7 +220,8 @@ int fa_decode_noalloc(const fa_tensor_t* q, const fa_tensor_t* kcache, const fa_
 /* ---------------------------------------------------------------------------
  * Device status.  Synchronises `stream`, returns the error bits the kernels
  * recorded in `workspace` (0 = none) through *status, and clears them.
- * Returns FA_ERR_TIMEOUT when a bounded wait ran out, FA_OK otherwise.
+ * Returns FA_ERR_TIMEOUT when a bounded wait ran out, FA_ERR_INVALID when a
+ * kernel found bad device-side input (paged decode), FA_OK otherwise.
  * ------------------------------------------------------------------------- */
 int fa_get_device_status(void* workspace, void* stream, int* status);
 

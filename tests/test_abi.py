@@ -140,6 +140,20 @@ def test_misaligned_and_workspace_errors(lib):
     assert lib.fa_decode(tens(), tens(), tens(), tens(), FAKE, ctypes.byref(sd), 1, FAKE, 1 << 30, None) == 1
 
 
+@pytest.mark.parametrize("page_size,max_pages,table,lens", [
+    (48, 64, FAKE, FAKE),      # neither 16/32/64 nor a multiple of 128
+    (96, 64, FAKE, FAKE),
+    (8, 256, FAKE, FAKE),
+    (16, 4, FAKE, FAKE),       # 4 pages of 16 cannot hold Nk = 1000
+    (16, 64, None, FAKE),      # no page table
+    (16, 64, FAKE, None)])     # no lengths
+def test_paged_decode_arguments_rejected_before_any_gpu_work(lib, page_size, max_pages, table, lens):
+    sd = ctypes.byref(shape(2, 8, 2, 4, 1000, 64))
+    rc = lib.fa_decode_paged(tens(), tens(), tens(), table, max_pages, lens, 100, page_size, tens(), FAKE, sd, 0,
+                             FAKE, 1 << 30, None)
+    assert rc == 1  # FA_ERR_INVALID
+
+
 def test_workspace_sizes(lib):
     s = S(2, 16, 16, 4096, 4096, causal=True)
     assert lib.fa_fwd_workspace_size(s) >= 256

@@ -24,6 +24,10 @@ Definitions followed (one bullet per function below):
   * FlashDecoding: each KV split t yields (m_t, l_t, O_t) with O_t the
     unnormalised local output; the combine is O = sum_t O_t e^{m_t - m} /
     sum_t l_t e^{m_t - m}.  §18.8.2 and lecture slides 57-60.
+  * sliding window: query i sees keys j with i - left <= j <= i + right
+    (``window_size=(left, right)`` of flash_attn_func, §18.7.1; local attention,
+    §18.8.1), a negative bound meaning unbounded; with causal, j <= i as well.
+    Like causal it is defined here for Nq == Nk (top-left aligned).
   * paged, variable-length decode: a sequence's logical KV row r lives in the
     physical page block_table[b, r // page_size], at row r % page_size
     (PagedAttention's page table, §18.8.2 part 3 and §18.8.3); each sequence
@@ -71,10 +75,25 @@ def causal_mask(rows, Nk):
     return np.arange(Nk)[None, :] > rows[:, None]
 
 
-def _scores(Qr, Kh, scale, rows, causal):
+def window_mask(rows, Nk, left, right):
+    """Boolean matrix, True where key j is outside query row i's window
+    [i - left, i + right] (a negative or None bound is unbounded)."""
+    rows = np.asarray(rows)[:, None]
+    j = np.arange(Nk)[None, :]
+    out = np.zeros((rows.shape[0], Nk), dtype=bool)
+    if left is not None and left >= 0:
+        out |= j < rows - left
+    if right is not None and right >= 0:
+        out |= j > rows + right
+    return out
+
+
+def _scores(Qr, Kh, scale, rows, causal, window=None):
     S = scale * (Qr @ Kh.T)
     if causal:
         S = np.where(causal_mask(rows, Kh.shape[0]), NEG_INF, S)
+    if window is not None:
+        S = np.where(window_mask(rows, Kh.shape[0], *window), NEG_INF, S)
     return S
 
 
@@ -88,8 +107,10 @@ def _softmax_rows(S):
     return E / l, m[:, 0], l[:, 0]
 
 
-def attention_forward(q, k, v, scale, causal=False, row_block=2048, heads=None, rows=None):
+def attention_forward(q, k, v, scale, causal=False, row_block=2048, heads=None, rows=None, window=None):
     """Plain attention forward.  Returns (O [B,Nq,Hq,d], LSE [B,Hq,Nq]).
+
+    ``window`` = (left, right) restricts query i to keys [i - left, i + right].
 
     ``heads`` (list of (b, h)) and ``rows`` (array of query rows) restrict which
     outputs are computed; entries not computed are NaN.  Restriction only skips
@@ -97,8 +118,8 @@ def attention_forward(q, k, v, scale, causal=False, row_block=2048, heads=None, 
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Nq, Nk, Hq, Hkv, d = _check_shapes(q, k, v)
-    if causal and Nq != Nk:
-        raise ValueError("causal attention is defined here for Nq == Nk only")
+    if (causal or window is not None) and Nq != Nk:
+        raise ValueError("causal and windowed attention are defined here for Nq == Nk only")
     g = Hq // Hkv
     o = np.full((B, Nq, Hq, d), np.nan)
     lse = np.full((B, Hq, Nq), np.nan)
@@ -108,14 +129,14 @@ def attention_forward(q, k, v, scale, causal=False, row_block=2048, heads=None, 
         Kh, Vh = k[b, :, kv, :], v[b, :, kv, :]
         for r0 in range(0, len(all_rows), row_block):
             rr = all_rows[r0:r0 + row_block]
-            S = _scores(q[b, rr, h, :], Kh, scale, rr, causal)
+            S = _scores(q[b, rr, h, :], Kh, scale, rr, causal, window)
             P, m, l = _softmax_rows(S)
             o[b, rr, h, :] = P @ Vh
             lse[b, h, rr] = m + np.log(l)
     return o, lse
 
 
-def attention_backward(q, k, v, do, scale, causal=False, row_block=1024, heads=None, rows=None):
+def attention_backward(q, k, v, do, scale, causal=False, row_block=1024, heads=None, rows=None, window=None):
     """Plain attention backward with S and P materialised.
 
     Returns (dQ [B,Nq,Hq,d], dK [B,Nk,Hkv,d], dV [B,Nk,Hkv,d]).  With ``heads``
@@ -128,8 +149,8 @@ def attention_backward(q, k, v, do, scale, causal=False, row_block=1024, heads=N
     B, Nq, Nk, Hq, Hkv, d = _check_shapes(q, k, v)
     if do.shape != q.shape:
         raise ValueError("dO must have the shape of O")
-    if causal and Nq != Nk:
-        raise ValueError("causal attention is defined here for Nq == Nk only")
+    if (causal or window is not None) and Nq != Nk:
+        raise ValueError("causal and windowed attention are defined here for Nq == Nk only")
     g = Hq // Hkv
     dq = np.full(q.shape, np.nan)
     dk = np.zeros(k.shape)
@@ -141,7 +162,7 @@ def attention_backward(q, k, v, do, scale, causal=False, row_block=1024, heads=N
         for r0 in range(0, len(all_rows), row_block):
             rr = all_rows[r0:r0 + row_block]
             Qr, dOr = q[b, rr, h, :], do[b, rr, h, :]
-            S = _scores(Qr, Kh, scale, rr, causal)
+            S = _scores(Qr, Kh, scale, rr, causal, window)
             P, _, _ = _softmax_rows(S)
             dv[b, :, kv, :] += P.T @ dOr                 # dV = P^T dO
             dP = dOr @ Vh.T                              # dP = dO V^T
@@ -152,7 +173,7 @@ def attention_backward(q, k, v, do, scale, causal=False, row_block=1024, heads=N
     return dq, dk, dv
 
 
-def attention_backward_sampled(q, k, v, do, scale, causal, b, h, q_rows, k_rows, row_block=1024):
+def attention_backward_sampled(q, k, v, do, scale, causal, b, h, q_rows, k_rows, row_block=1024, window=None):
     """Backward of one query head (b, h), returning only sampled output rows.
 
     Returns (dQ[q_rows], dK_h[k_rows], dV_h[k_rows]) where dK_h/dV_h are the
@@ -172,7 +193,7 @@ def attention_backward_sampled(q, k, v, do, scale, causal, b, h, q_rows, k_rows,
     for r0 in range(0, Nq, row_block):
         rr = np.arange(r0, min(Nq, r0 + row_block))
         Qr, dOr = q[b, rr, h, :], do[b, rr, h, :]
-        S = _scores(Qr, Kh, scale, rr, causal)
+        S = _scores(Qr, Kh, scale, rr, causal, window)
         P, _, _ = _softmax_rows(S)
         dP = dOr @ Vh.T
         D = np.sum(P * dP, axis=1, keepdims=True)

@@ -5,6 +5,9 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).  Pure Python integers.
   * causal tile classes -- "第18章 FlashAttention" §18.5.2: a (Q block, K block)
     pair is fully visible, fully masked (skipped) or partial (masked element by
     element).  Fig. 18-20 shows the 3x3 case.
+  * sliding-window tile classes -- the same three classes under the predicate
+    i - left <= j <= i + right (§18.8.1's block-sparse loop skips the blocks no
+    row of the query block can see; a sliding window is its banded case).
   * longest-first order and greedy list scheduling -- "CMU 11-868 L21
     FlashAttention" notes, slides 27-46 (LPT: schedule the longest work first;
     worked example with 2 batches on 3 SMs: in-order loads [9, 5, 6], longest
@@ -32,6 +35,36 @@ def causal_tile_class(q_start, q_end, k_start, k_end):
     if k_end - 1 <= q_start:
         return FULL
     return PARTIAL
+
+
+def window_tile_class(q_start, q_end, k_start, k_end, left, right, causal):
+    """Class of rows [q_start, q_end) x keys [k_start, k_end) under i - left <= j <= i + right
+    (and j <= i when causal); a negative bound is unbounded.
+
+    Skipped when no (row, key) pair is visible; full when every pair is; else partial.
+    """
+    if causal:
+        right = 0 if right < 0 else min(right, 0)
+    lo_ok = lambda i, j: left < 0 or j >= i - left       # noqa: E731
+    hi_ok = lambda i, j: right < 0 or j <= i + right     # noqa: E731
+    # visible pairs exist iff the band meets the rectangle: the smallest key any row can
+    # see is q_start - left, the largest q_end - 1 + right
+    if (right >= 0 and k_start > q_end - 1 + right) or (left >= 0 and k_end - 1 < q_start - left):
+        return SKIP
+    if lo_ok(q_end - 1, k_start) and hi_ok(q_start, k_end - 1):
+        return FULL
+    return PARTIAL
+
+
+def tile_ranges(Nq, Nk, block, left, right, causal):
+    """For each query tile, the half-open range of key tiles that are not skipped."""
+    out = []
+    for i in range(cdiv(Nq, block)):
+        qs, qe = i * block, min(Nq, (i + 1) * block)
+        vis = [j for j in range(cdiv(Nk, block))
+               if window_tile_class(qs, qe, j * block, min(Nk, (j + 1) * block), left, right, causal) != SKIP]
+        out.append((min(vis), max(vis) + 1) if vis else (0, 0))
+    return out
 
 
 def tile_classes(Nq, Nk, block_m, block_n, causal):

@@ -34,7 +34,8 @@ class FaTensor(ctypes.Structure):
 
 class FaShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("Nq", ctypes.c_int),
-                ("Nk", ctypes.c_int), ("d", ctypes.c_int), ("scale", ctypes.c_float), ("causal", ctypes.c_int)]
+                ("Nk", ctypes.c_int), ("d", ctypes.c_int), ("scale", ctypes.c_float), ("causal", ctypes.c_int),
+                ("window", ctypes.c_int), ("window_left", ctypes.c_int), ("window_right", ctypes.c_int)]
 
 
 # name -> (restype, argtypes); mirrors include/fa.h
@@ -102,8 +103,11 @@ def check(rc):
         raise FAError(rc, msg)
 
 
-def shape(B, Hq, Hkv, Nq, Nk, d, scale=None, causal=False):
-    return FaShape(B, Hq, Hkv, Nq, Nk, d, 1.0 / math.sqrt(d) if scale is None else float(scale), int(bool(causal)))
+def shape(B, Hq, Hkv, Nq, Nk, d, scale=None, causal=False, window=None):
+    """window = (left, right): query i sees keys i - left .. i + right (negative: unbounded)."""
+    w = (0, -1, -1) if window is None else (1, int(window[0]), int(window[1]))
+    return FaShape(B, Hq, Hkv, Nq, Nk, d, 1.0 / math.sqrt(d) if scale is None else float(scale), int(bool(causal)),
+                   *w)
 
 
 def tdesc(t):
@@ -171,19 +175,20 @@ def device_status(workspace):
 
 
 # ---------------------------------------------------------------- convenience API
-def _dims(q, k, scale, causal):
+def _dims(q, k, scale, causal, window=None):
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
-    return shape(B, Hq, Hkv, Nq, Nk, d, scale, causal)
+    return shape(B, Hq, Hkv, Nq, Nk, d, scale, causal, window)
 
 
-def forward(q, k, v, causal=False, scale=None, residual=False):
+def forward(q, k, v, causal=False, scale=None, residual=False, window=None):
     """O, LSE = attention(q, k, v).  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] bf16 on CUDA.
 
     With ``residual=True`` also returns O's bf16 rounding residual, which
     ``backward`` uses to form D accurately (see fa_bwd in include/fa.h).
+    ``window=(left, right)`` restricts query i to keys i - left .. i + right.
     """
-    s = _dims(q, k, scale, causal)
+    s = _dims(q, k, scale, causal, window)
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
     res = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
@@ -192,9 +197,9 @@ def forward(q, k, v, causal=False, scale=None, residual=False):
     return (o, lse, res) if residual else (o, lse)
 
 
-def backward(q, k, v, o, lse, do, causal=False, scale=None, o_residual=None):
+def backward(q, k, v, o, lse, do, causal=False, scale=None, o_residual=None, window=None):
     """dQ, dK, dV of attention given O, LSE (and optionally O's residual) from ``forward``."""
-    s = _dims(q, k, scale, causal)
+    s = _dims(q, k, scale, causal, window)
     dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device)
     dv = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device)

@@ -98,6 +98,8 @@ int check_shape(const fa_shape_t* s) {
   if (!(s->scale > 0.f) || !isfinite(s->scale)) return FA_ERR_INVALID;
   if (s->causal != 0 && s->causal != 1) return FA_ERR_INVALID;
   if (s->causal && s->Nq != s->Nk) return FA_ERR_INVALID;
+  if (s->window != 0 && s->window != 1) return FA_ERR_INVALID;
+  if (s->window && s->Nq != s->Nk) return FA_ERR_INVALID;
   // index arithmetic inside the kernels is 32-bit per (head, row) and 64-bit per element
   if (static_cast<int64_t>(s->B) * s->Hq * s->Nq > (1ll << 31) - 1) return FA_ERR_INVALID;
   if (static_cast<int64_t>(s->Nk) > (1ll << 30)) return FA_ERR_INVALID;
@@ -118,7 +120,15 @@ int check_ws(const void* ws, size_t have, size_t need) {
   return FA_OK;
 }
 
-Dims dims_of(const fa_shape_t* s) { return Dims{s->B, s->Hq, s->Hkv, s->Nq, s->Nk, s->causal}; }
+Dims dims_of(const fa_shape_t* s) {
+  int wl = UNBOUNDED, wr = UNBOUNDED;
+  if (s->window) {
+    if (s->window_left >= 0) wl = imin(s->window_left, UNBOUNDED);
+    if (s->window_right >= 0) wr = imin(s->window_right, UNBOUNDED);
+  }
+  if (s->causal) wr = imin(wr, 0);
+  return Dims{s->B, s->Hq, s->Hkv, s->Nq, s->Nk, s->causal, wl, wr};
+}
 
 OutRows rows_of(const fa_tensor_t* t) { return OutRows{t->ptr, t->stride_b, t->stride_n, t->stride_h}; }
 
@@ -375,7 +385,7 @@ int fa_decode(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor_t* vc
   if ((rc = check_shape(s)) || (rc = check_tensor(q)) || (rc = check_tensor(kc)) || (rc = check_tensor(vc)) ||
       (rc = check_tensor(o)))
     return rc;
-  if (!lse || s->causal) return FA_ERR_INVALID;
+  if (!lse || s->causal || s->window) return FA_ERR_INVALID;
   if ((s->Hq / s->Hkv) * s->Nq > 16) return FA_ERR_INVALID;  // packed rows must fit one 16-row tile
   int sms = 0;
   if ((rc = device_info(&sms))) return rc;
@@ -416,7 +426,8 @@ int fa_decode_paged(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor
   if ((rc = check_shape(s)) || (rc = check_tensor(q)) || (rc = check_tensor(kc)) || (rc = check_tensor(vc)) ||
       (rc = check_tensor(o)))
     return rc;
-  if (!lse || s->causal || !block_table || !seqlens_k || max_pages < 1 || num_pages < 1) return FA_ERR_INVALID;
+  if (!lse || s->causal || s->window || !block_table || !seqlens_k || max_pages < 1 || num_pages < 1)
+    return FA_ERR_INVALID;
   if ((s->Hq / s->Hkv) * s->Nq > 16) return FA_ERR_INVALID;
   // pages of 16, 32 or 64 keys stack into a 128-key tile; larger pages hold whole tiles
   const bool small = page_size == 16 || page_size == 32 || page_size == 64;

@@ -220,16 +220,35 @@ struct DkvUnit {
   int b, kvh, kt, q0, nqi, n_it;
 };
 
+// Key tiles visited by query tile qt: a band's range, else a prefix (causal: up
+// to the diagonal tile, Nq == Nk).
+template <int MASK>
+__device__ __forceinline__ void dq_kv_range(const Dims& s, int qt, int& lo, int& hi) {
+  if (MASK == MASK_BAND) {
+    kv_range(s, qt, lo, hi);
+  } else {
+    lo = 0;
+    hi = MASK == MASK_CAUSAL ? qt + 1 : k_tiles(s);
+  }
+}
+
+// The query tiles visiting key tile kt: a band's range, or under j <= i (where
+// Nq == Nk) the suffix from the diagonal tile.
+template <int MASK>
 __device__ __forceinline__ DkvUnit dkv_decode(const Dims& s, int u) {
   DkvUnit r;
   dkdv_unit(s, u, r.b, r.kvh, r.kt);
-  r.q0 = q_tile_begin(s, r.kt);
-  r.nqi = q_tiles(s) - r.q0;
+  int qhi = q_tiles(s);
+  if (MASK == MASK_BAND)
+    q_range(s, r.kt, r.q0, qhi);
+  else
+    r.q0 = MASK == MASK_CAUSAL ? r.kt : 0;
+  r.nqi = qhi - r.q0;
   r.n_it = (s.Hq / s.Hkv) * r.nqi;
   return r;
 }
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 __global__ void __launch_bounds__(384, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -280,7 +299,7 @@ __global__ void __launch_bounds__(384, 1)
         unit_slot[slot] = u;
         mbar_arrive(&bar.unit_full[slot]);
         if (u >= p.total_units) break;
-        const DkvUnit w = dkv_decode(s, u);
+        const DkvUnit w = dkv_decode<MASK>(s, u);
         if (!mbar_wait(bar.kv_empty, (it & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
         mbar_arrive_expect_tx(bar.kv_full, 2 * L::TB);
         for (int c = 0; c < D / 64; ++c) {
@@ -335,7 +354,7 @@ __global__ void __launch_bounds__(384, 1)
         const int u = unit_slot[slot];
         mbar_arrive(&bar.unit_empty[slot]);
         if (u >= p.total_units) break;
-        const DkvUnit w = dkv_decode(s, u);
+        const DkvUnit w = dkv_decode<MASK>(s, u);
         if (!mbar_wait(bar.kv_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA)) break;
         bool ok = mbar_wait(&bar.st_full[sq % L::STAGES], (sq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
         if (!ok) break;
@@ -409,15 +428,19 @@ __global__ void __launch_bounds__(384, 1)
       const int u = unit_slot[slot];
       warp_arrive(&bar.unit_empty[slot]);
       if (u >= p.total_units) break;
-      const DkvUnit w = dkv_decode(s, u);
+      const DkvUnit w = dkv_decode<MASK>(s, u);
       const int key = w.kt * TILE + r;
+      int qfull_lo = 0, qfull_hi = 0;  // band: query tiles whose rows all see every key of this tile
+      if (MASK == MASK_BAND) q_full_range(s, w.kt, qfull_lo, qfull_hi);
       for (int k = 0; k < w.n_it && ok; ++k) {
         const uint32_t q = sq + k;
         const uint8_t* stage = smem + L::OFF_ST + (q % L::STAGES) * L::STAGE;
         const float* nl2 = reinterpret_cast<const float*>(stage + 2 * L::TB);  // -LSE2[query]
         const float* nd = nl2 + 128;                                            // -D[query]
         const int qi = w.q0 + k % w.nqi;
-        const bool diag = CAUSAL && tile_class(s, qi, w.kt) == 2;
+        // rows (keys) see only part of the tile's queries: the band's edges, or causal's diagonal
+        const bool part = MASK == MASK_BAND ? (qi < qfull_lo || qi > qfull_hi)
+                                            : (MASK == MASK_CAUSAL && qi == w.kt);
         ok = mbar_wait(&bar.st_full[q % L::STAGES], (q / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
         ok = ok && mbar_wait(bar.s_full, sph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
         sph ^= 1;
@@ -449,7 +472,13 @@ __global__ void __launch_bounds__(384, 1)
               pf[e + 2] = ex2(x23.x);
               pf[e + 3] = ex2(x23.y);
             }
-            if (CAUSAL && diag) {  // columns below lim (queries before this key) are masked
+            if (MASK == MASK_BAND && part) {  // query q sees this key iff key - wr <= q <= key + wl
+              const int q_first = qi * TILE + c0 + 32 * cc;
+              const int lo = key - s.wr - q_first, hi = key + s.wl + 1 - q_first;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < lo || i >= hi) pf[32 * cc + i] = 0.f;
+            } else if (MASK == MASK_CAUSAL && part) {  // columns below lim (queries before this key)
               const int lim = key - qi * TILE - c0 - 32 * cc;
 #pragma unroll
               for (int i = 0; i < 32; ++i)
@@ -546,7 +575,7 @@ struct DqLayout {
   static constexpr int ALLOC = (SCRATCH ? OFF_SCR + 8 * ROW_SCRATCH_BYTES : OFF_TMEM + 16) + 1024;
 };
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -614,7 +643,9 @@ __global__ void __launch_bounds__(384, 1)
         if (u >= p.total_units) break;
         int b, h, qt;
         dq_unit(s, u, b, h, qt);
-        const int n = kv_tiles_for_q(s, qt), kvh = h / g;
+        int klo, khi;
+        dq_kv_range<MASK>(s, qt, klo, khi);
+        const int n = khi - klo, kvh = h / g;
         if (!mbar_wait(q_empty, (it & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
         mbar_arrive_expect_tx(q_full, 2 * L::TB);
         for (int c = 0; c < D / 64; ++c) {
@@ -633,7 +664,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&k_full[ks], L::TB);
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(smem + L::OFF_K + ks * L::TB + c * (TILE * 128), &tm_k, &k_full[ks], c * 64, kvh,
-                        j * TILE, b);
+                        (klo + j) * TILE, b);
           // V_j: its slot is free once dP of the tile VST back is done.
           const int vs = kq % L::VST;
           if (!mbar_wait(&v_empty[vs], ((kq / L::VST) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
@@ -643,7 +674,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&v_full[vs], L::TB);
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(smem + L::OFF_V + vs * L::TB + c * (TILE * 128), &tm_v, &v_full[vs], c * 64, kvh,
-                        j * TILE, b);
+                        (klo + j) * TILE, b);
         }
         if (!ok) break;
       }
@@ -682,7 +713,9 @@ __global__ void __launch_bounds__(384, 1)
         if (u >= p.total_units) break;
         int b, h, qt;
         dq_unit(s, u, b, h, qt);
-        const int n = kv_tiles_for_q(s, qt);
+        int klo, khi;
+        dq_kv_range<MASK>(s, qt, klo, khi);
+        const int n = khi - klo;
         bool ok = mbar_wait(q_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA) && kwait(kq);
         if (!ok) break;
         tc_fence_after();
@@ -744,7 +777,13 @@ __global__ void __launch_bounds__(384, 1)
       if (u >= p.total_units) break;
       int b, h, qt;
       dq_unit(s, u, b, h, qt);
-      const int n = kv_tiles_for_q(s, qt);
+      int klo, khi, full_lo = 0, full_hi = 0;
+      dq_kv_range<MASK>(s, qt, klo, khi);
+      if (MASK == MASK_BAND) {
+        kv_full_range(s, qt, full_lo, full_hi);
+        if ((s.Nk % TILE) != 0) full_hi = imin(full_hi, k_tiles(s) - 2);  // the ragged last tile is masked too
+      }
+      const int n = khi - klo;
       const int q_row = qt * TILE + r;
       const int64_t srow = (static_cast<int64_t>(b) * s.Hq + h) * p.nq_pad + q_row;
       const float2 nl2 = make_float2(p.neg_lse2[srow], p.neg_lse2[srow]);
@@ -759,7 +798,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         tc_fence_after();
         // P = exp2(S * scale*log2e - LSE2[row]), on packed f32x2 operations (see the
-        // dK/dV kernel); only the last key tile can hold masked keys.
+        // dK/dV kernel); keys outside the row's band, or past Nk, are masked.
         float pf[64];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -772,9 +811,20 @@ __global__ void __launch_bounds__(384, 1)
             pf[32 * cc + 2 * i + 1] = ex2(x.y);
           }
         }
-        if (j == n - 1) {  // keys at or beyond lim (tile-local) are masked
+        if (MASK == MASK_BAND) {
+          const int kt = klo + j;
+          if (kt < full_lo || kt > full_hi) {
+            // visible keys [lo, hi) relative to this warpgroup's first column
+            const int first = kt * TILE + c0;
+            const int hi = imin(s.Nk, q_row + s.wr + 1) - first;
+            const int lo = q_row - s.wl - first;
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              if (i < lo || i >= hi) pf[i] = 0.f;
+          }
+        } else if (j == n - 1) {  // causal or full: only the last key tile holds masked keys
           int lim = imin(TILE, s.Nk - j * TILE);
-          if (CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
+          if (MASK == MASK_CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
           lim -= c0;
 #pragma unroll
           for (int i = 0; i < 64; ++i)
@@ -829,7 +879,7 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   BwdParams p;
   p.dims = a.dims;
@@ -856,7 +906,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   }
   // 2) dK / dV
   if (a.parts & 2) {
-    auto kern = bwd_dkdv_kernel<D, CAUSAL>;
+    auto kern = bwd_dkdv_kernel<D, MASK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<D>::ALLOC);
     if (e != cudaSuccess) return e;
     p.counter = a.counters;
@@ -867,7 +917,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   }
   // 3) dQ
   if (a.parts & 4) {
-    auto kern = bwd_dq_kernel<D, CAUSAL>;
+    auto kern = bwd_dq_kernel<D, MASK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::ALLOC);
     if (e != cudaSuccess) return e;
     p.counter = a.counters + 1;
@@ -882,8 +932,12 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st) {
-  if (a.d == 64) return a.dims.causal ? launch_bwd_t<64, true>(a, st) : launch_bwd_t<64, false>(a, st);
-  return a.dims.causal ? launch_bwd_t<128, true>(a, st) : launch_bwd_t<128, false>(a, st);
+  const int m = mask_kind(a.dims);
+  if (a.d == 64)
+    return m == MASK_BAND ? launch_bwd_t<64, MASK_BAND>(a, st)
+           : m == MASK_CAUSAL ? launch_bwd_t<64, MASK_CAUSAL>(a, st) : launch_bwd_t<64, MASK_NONE>(a, st);
+  return m == MASK_BAND ? launch_bwd_t<128, MASK_BAND>(a, st)
+         : m == MASK_CAUSAL ? launch_bwd_t<128, MASK_CAUSAL>(a, st) : launch_bwd_t<128, MASK_NONE>(a, st);
 }
 
 }  // namespace fa

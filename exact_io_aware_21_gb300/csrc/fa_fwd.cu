@@ -95,17 +95,54 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   return r;
 }
 
-__device__ __forceinline__ void unit_tiles(const Dims& s, int p, int (&n)[2]) {
+// The key tiles of unit p: each query tile t visits [lo[t], hi[t]) (empty when
+// the tile is past the sequence); the unit streams the union [base, base + nu)
+// once, and tile t is active at local steps [a[t], a[t] + n[t]).
+struct UnitTiles {
+  int base, nu;
+  int a[2], n[2];
+};
+
+// Without a band every range starts at key tile 0 and (under j <= i, where
+// Nq == Nk) ends at the diagonal tile.
+template <int MASK>
+__device__ __forceinline__ UnitTiles unit_tiles(const Dims& s, int p) {
   const int nq = q_tiles(s);
+  int lo[2], hi[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int qt = 2 * p + t;
-    n[t] = qt < nq ? kv_tiles_for_q(s, qt) : 0;
+    lo[t] = hi[t] = 0;
+    if (qt < nq) {
+      if (MASK == MASK_BAND)
+        kv_range(s, qt, lo[t], hi[t]);
+      else
+        hi[t] = MASK == MASK_CAUSAL ? qt + 1 : k_tiles(s);
+    }
   }
+  if (MASK != MASK_BAND) {
+    UnitTiles u;
+    u.base = 0;
+    u.nu = imax(hi[0], hi[1]);
+    u.a[0] = u.a[1] = 0;
+    u.n[0] = hi[0];
+    u.n[1] = hi[1];
+    return u;
+  }
+  UnitTiles u;
+  const bool e1 = hi[1] <= lo[1];  // tile 1 past the sequence (tile 0 never is)
+  u.base = e1 ? lo[0] : imin(lo[0], lo[1]);
+  u.nu = (e1 ? hi[0] : imax(hi[0], hi[1])) - u.base;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    u.n[t] = imax(0, hi[t] - lo[t]);
+    u.a[t] = u.n[t] > 0 ? lo[t] - u.base : 0;
+  }
+  return u;
 }
 
 // ------------------------------------------------------------------ producer
-template <int D>
+template <int D, int MASK>
 __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, const CUtensorMap* tm_q,
                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, const FwdParams& p,
                              const Ctl& ctl) {
@@ -120,10 +157,10 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
     unit_slot[slot] = u;
     mbar_arrive(&bar.unit_full[slot]);
     if (u >= p.total_units) break;
-    int b, h, pr, n[2];
+    int b, h, pr;
     fwd_unit(p.dims, u, b, h, pr);
-    unit_tiles(p.dims, pr, n);
-    const int nmax = imax(n[0], n[1]);
+    const UnitTiles ut = unit_tiles<MASK>(p.dims, pr);
+    const int nmax = ut.nu;
     const int kvh = h / g;
 
     if (!mbar_wait(bar.q_empty, (it & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
@@ -149,9 +186,10 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
 #pragma unroll
       for (int c = 0; c < L::CH; ++c) {
         if (has_v)
-          tma_load_4d(base + c * (TILE * 128), tm_v, &bar.kv_full[gs], c * 64, kvh, (gi - 1) * TILE, b);
+          tma_load_4d(base + c * (TILE * 128), tm_v, &bar.kv_full[gs], c * 64, kvh, (ut.base + gi - 1) * TILE, b);
         if (has_k)
-          tma_load_4d(base + L::TB + c * (TILE * 128), tm_k, &bar.kv_full[gs], c * 64, kvh, gi * TILE, b);
+          tma_load_4d(base + L::TB + c * (TILE * 128), tm_k, &bar.kv_full[gs], c * 64, kvh, (ut.base + gi) * TILE,
+                      b);
       }
     }
     if (!ok) break;
@@ -167,7 +205,7 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D>
+template <int D, int MASK>
 __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
                         const Ctl& ctl) {
   using L = FwdLayout<D>;
@@ -209,18 +247,20 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
     const int u = unit_slot[slot];
     mbar_arrive(&bar.unit_empty[slot]);
     if (u >= p.total_units) return;
-    int b, h, pr, n[2];
+    int b, h, pr;
     fwd_unit(p.dims, u, b, h, pr);
-    unit_tiles(p.dims, pr, n);
-    const int nmax = imax(n[0], n[1]);
+    const UnitTiles ut = unit_tiles<MASK>(p.dims, pr);
+    const int nmax = ut.nu;
+    // tile t is active at local steps [a[t], e[t])
+    const int a[2] = {ut.a[0], ut.a[1]}, e[2] = {ut.a[0] + ut.n[0], ut.a[1] + ut.n[1]};
 
     if (!mbar_wait(bar.q_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
-    // group 0: K_0
+    // group 0: K of local step 0
     {
       if (!group_wait(seq)) return;
       tc_fence_after();
       for (int t = 0; t < 2; ++t)
-        if (n[t] > 0) {
+        if (ut.n[t] > 0 && a[t] == 0) {
           issue_s(t, group_base(seq) + L::TB);
           mma_commit(&bar.s_full[t]);
         }
@@ -232,14 +272,16 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
       if (!group_wait(gq)) return;
       const uint32_t v_addr = group_base(gq), k_addr = v_addr + L::TB;
       for (int t = 0; t < 2; ++t) {
-        if (j >= n[t]) continue;
-        if (j == 0 && !mbar_wait(&bar.o_empty[t], (active[t] & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
-        if (!mbar_wait(&bar.p_full[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
-        pph[t] ^= 1;
-        tc_fence_after();
-        issue_pv(t, v_addr, j > 0);
-        if (j == n[t] - 1) mma_commit(&bar.o_full[t]);
-        if (j + 1 < n[t]) {
+        if (j >= a[t] && j < e[t]) {
+          if (j == a[t] && !mbar_wait(&bar.o_empty[t], (active[t] & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+          if (!mbar_wait(&bar.p_full[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
+          pph[t] ^= 1;
+          tc_fence_after();
+          issue_pv(t, v_addr, j > a[t]);
+          if (j == e[t] - 1) mma_commit(&bar.o_full[t]);
+        }
+        if (j + 1 >= a[t] && j + 1 < e[t]) {  // S of the tile's next step (its first, when it starts late)
+          if (j < a[t]) tc_fence_after();       // no P V of this tile in this step fenced the group wait
           issue_s(t, k_addr);
           mma_commit(&bar.s_full[t]);
         }
@@ -248,13 +290,13 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
       mma_commit(&bar.kv_empty[gq % L::NG]);
     }
     for (int t = 0; t < 2; ++t)
-      if (n[t] > 0) ++active[t];
+      if (ut.n[t] > 0) ++active[t];
     seq += nmax + 1;
   }
 }
 
 // ------------------------------------------------------------------ softmax
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
                             const Ctl& ctl, uint8_t* scratch) {
   const int wq = (threadIdx.x >> 5) & 3;  // warp within the warpgroup = TMEM lane quarter
@@ -274,13 +316,19 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     const int u = unit_slot[slot];
     warp_arrive(&bar.unit_empty[slot]);
     if (u >= p.total_units) return;
-    int b, h, pr, n2[2];
+    int b, h, pr;
     fwd_unit(s, u, b, h, pr);
-    unit_tiles(s, pr, n2);
-    const int n = n2[t];
+    const UnitTiles ut = unit_tiles<MASK>(s, pr);
+    const int n = ut.n[t];
     if (n == 0) continue;
     const int qt = 2 * pr + t;
     const int q_row = qt * TILE + r;
+    const int kt0 = ut.base + ut.a[t];  // first key tile of this query tile
+    int full_lo = 0, full_hi = 0;        // band: key tiles this query tile sees in full
+    if (MASK == MASK_BAND) {
+      kv_full_range(s, qt, full_lo, full_hi);
+      if ((s.Nk % TILE) != 0) full_hi = imin(full_hi, k_tiles(s) - 2);  // the ragged last tile is masked too
+    }
 
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < n; ++j) {
@@ -294,9 +342,20 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
       float sv[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i]);
-      if (j == n - 1 && (CAUSAL || (s.Nk % TILE) != 0)) {
+      if (MASK == MASK_BAND) {
+        const int kt = kt0 + j;
+        if (kt < full_lo || kt > full_hi) {
+          // keys [lo, hi) of this tile are visible to the row: the band i - wl .. i + wr, below Nk
+          const int hi = imin(s.Nk - kt * TILE, imin(TILE, q_row + s.wr + 1 - kt * TILE));
+          const int lo = imax(0, q_row - s.wl - kt * TILE);
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i >= hi || i < lo) sv[i] = -INFINITY;
+        }
+      } else if (j == n - 1 && (MASK == MASK_CAUSAL || (s.Nk % TILE) != 0)) {
+        // the last tile: keys at or past Nk, and under j <= i keys past the row
         int lim = s.Nk - j * TILE;
-        if (CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
+        if (MASK == MASK_CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i >= lim) sv[i] = -INFINITY;
@@ -313,8 +372,13 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
       }
       const float m_tile = fmaxf(fmax3(mx0, mx1, mx2), mx3) * c;
       const float m_new = (m_tile > m_run + TAU) ? m_tile : m_run;
-      const float alpha = ex2(m_run - m_new);
-      const float2 neg_m2 = make_float2(-m_new, -m_new);
+      // Under a band a row may see no key of a tile: while it has seen none at all, m
+      // stays -inf, alpha 1 and every p 0.  (Causal and full rows see a key in their
+      // first tile.  Measured: the guarded form costs the causal kernels 1-2% and saves
+      // the full d = 64 kernel 5%, hence the split.)
+      const float alpha = (MASK == MASK_CAUSAL) ? ex2(m_run - m_new) : (m_new == m_run) ? 1.f : ex2(m_run - m_new);
+      const float m_use = (MASK == MASK_BAND && m_new == -INFINITY) ? 0.f : m_new;
+      const float2 neg_m2 = make_float2(-m_use, -m_use);
       float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
       uint32_t pk[64];
 #pragma unroll
@@ -396,7 +460,7 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -438,11 +502,11 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane_id() == 0) fwd_producer<D>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
+    if (lane_id() == 0) fwd_producer<D, MASK>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
   } else if (warp == 1) {
-    if (lane_id() == 0) fwd_mma<D>(smem, bar, unit_slot, tmem, p, ctl);
+    if (lane_id() == 0) fwd_mma<D, MASK>(smem, bar, unit_slot, tmem, p, ctl);
   } else if (warp >= 4) {
-    fwd_softmax<D, CAUSAL>((warp - 4) >> 2, bar, unit_slot, tmem, p, ctl,
+    fwd_softmax<D, MASK>((warp - 4) >> 2, bar, unit_slot, tmem, p, ctl,
                            smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES);
   }
   tc_fence_before();
@@ -453,10 +517,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   using L = FwdLayout<D>;
-  auto kern = fa_fwd_kernel<D, CAUSAL>;
+  auto kern = fa_fwd_kernel<D, MASK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   FwdParams p;
@@ -477,8 +541,12 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
-  if (a.d == 64) return a.dims.causal ? launch_fwd_t<64, true>(a, st) : launch_fwd_t<64, false>(a, st);
-  return a.dims.causal ? launch_fwd_t<128, true>(a, st) : launch_fwd_t<128, false>(a, st);
+  const int m = mask_kind(a.dims);
+  if (a.d == 64)
+    return m == MASK_BAND ? launch_fwd_t<64, MASK_BAND>(a, st)
+           : m == MASK_CAUSAL ? launch_fwd_t<64, MASK_CAUSAL>(a, st) : launch_fwd_t<64, MASK_NONE>(a, st);
+  return m == MASK_BAND ? launch_fwd_t<128, MASK_BAND>(a, st)
+         : m == MASK_CAUSAL ? launch_fwd_t<128, MASK_CAUSAL>(a, st) : launch_fwd_t<128, MASK_NONE>(a, st);
 }
 
 }  // namespace fa

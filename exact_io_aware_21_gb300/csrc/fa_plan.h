@@ -20,42 +20,91 @@ FA_HD int cdiv(int a, int b) { return (a + b - 1) / b; }
 FA_HD int imin(int a, int b) { return a < b ? a : b; }
 FA_HD int imax(int a, int b) { return a > b ? a : b; }
 
+// Keys visible to query row i: i - wl <= j <= i + wr.  Causal attention is the
+// band with wr = 0 (and wl unbounded); a sliding window sets both; UNBOUNDED
+// (larger than any sequence) leaves a side open.
+constexpr int UNBOUNDED = 1 << 29;
+
 struct Dims {
   int B, Hq, Hkv, Nq, Nk;
   int causal;
+  int wl, wr;  // band of visible keys around each row (causal folded into wr)
 };
 
-// "第18章 FlashAttention" §18.5.2: with rows [qs, qe) and keys [ks, ke) under
-// the rule j <= i, the block is fully masked when ks > qe-1, fully visible
-// when ke-1 <= qs, and partial otherwise.  0 = skip, 1 = full, 2 = partial.
-FA_HD int causal_class(int qs, int qe, int ks, int ke) {
-  if (ks > qe - 1) return 0;
-  if (ke - 1 <= qs) return 1;
+FA_HD bool banded(const Dims& s) { return s.wl < UNBOUNDED || s.wr < UNBOUNDED; }
+
+// Which masking a kernel instantiation handles: none, causal (j <= i only; the
+// last visited tile is the only partial one), or a general band.
+constexpr int MASK_NONE = 0, MASK_CAUSAL = 1, MASK_BAND = 2;
+FA_HD int mask_kind(const Dims& s) {
+  if (s.wl < UNBOUNDED || (!s.causal && s.wr < UNBOUNDED)) return MASK_BAND;
+  return s.causal ? MASK_CAUSAL : MASK_NONE;
+}
+
+// "第18章 FlashAttention" §18.5.2: a block of rows [qs, qe) and keys [ks, ke)
+// is fully masked, fully visible or partial; under j <= i the first happens
+// when ks > qe-1 and the second when ke-1 <= qs.  The same test for the band
+// i - wl <= j <= i + wr: no key of the block is visible to any row when the
+// block lies right of the last row's reach (ks > qe-1 + wr) or left of the first
+// row's (ke-1 < qs - wl); every key is visible to every row when the block's
+// corners are (ke-1 <= qs + wr and ks >= qe-1 - wl).  0 = skip, 1 = full,
+// 2 = partial.  (64-bit: wl and wr may be UNBOUNDED.)
+FA_HD int band_class(int qs, int qe, int ks, int ke, int wl, int wr) {
+  const long long qs_ = qs, qe_ = qe, ks_ = ks, ke_ = ke;
+  if (ks_ > qe_ - 1 + wr || ke_ - 1 < qs_ - wl) return 0;
+  if (ke_ - 1 <= qs_ + wr && ks_ >= qe_ - 1 - wl) return 1;
   return 2;
 }
 
 FA_HD int tile_class(const Dims& s, int qt, int kt) {
-  if (!s.causal) return 1;
-  return causal_class(qt * TILE, imin(s.Nq, (qt + 1) * TILE), kt * TILE, imin(s.Nk, (kt + 1) * TILE));
+  if (!banded(s)) return 1;
+  return band_class(qt * TILE, imin(s.Nq, (qt + 1) * TILE), kt * TILE, imin(s.Nk, (kt + 1) * TILE), s.wl, s.wr);
 }
 
 FA_HD int q_tiles(const Dims& s) { return cdiv(s.Nq, TILE); }
 FA_HD int k_tiles(const Dims& s) { return cdiv(s.Nk, TILE); }
 
-// Key tiles visited by query tile qt: a prefix [0, n).  Under j <= i key tile
-// kt is visited iff its first key is at most the tile's last row (§18.5.2's
-// bound ceil((q_start + B_r) / B_c), clipped to the sequence).
-FA_HD int kv_tiles_for_q(const Dims& s, int qt) {
+// Key tiles visited by query tile qt: the range [lo, hi) of tiles holding a key
+// some row of the tile can see.  Under j <= i that is a prefix ending at the
+// tile of the last row (§18.5.2's bound ceil((q_start + B_r) / B_c), clipped to
+// the sequence); under a band it also starts at the first row's reach.
+FA_HD void kv_range(const Dims& s, int qt, int& lo, int& hi) {
   const int nk = k_tiles(s);
-  if (!s.causal) return nk;
-  const int last_row = imin(s.Nq, (qt + 1) * TILE) - 1;
-  return imin(nk, last_row / TILE + 1);
+  const long long first = static_cast<long long>(qt) * TILE - s.wl;
+  const long long last = static_cast<long long>(imin(s.Nq, (qt + 1) * TILE)) - 1 + s.wr;
+  lo = first <= 0 ? 0 : static_cast<int>(first / TILE);
+  hi = last >= static_cast<long long>(nk) * TILE ? nk : static_cast<int>(last / TILE) + 1;
 }
 
-// Query tiles visited by key tile kt: a suffix [first, nq).
-FA_HD int q_tile_begin(const Dims& s, int kt) {
-  if (!s.causal) return 0;
-  return (kt * TILE) / TILE;  // first query tile whose last row reaches key kt*TILE
+FA_HD int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// Key tiles that query tile qt sees in full are [lo, hi] (a superset of its
+// visited range may result; callers intersect): every row of [qs, qe) must
+// reach the tile's first key (kt*TILE >= qe-1 - wl) and its last key
+// (kt*TILE + TILE-1 <= qs + wr).  Ragged sequence ends are not counted here.
+FA_HD void kv_full_range(const Dims& s, int qt, int& lo, int& hi) {
+  const int qs = qt * TILE, qe = imin(s.Nq, qs + TILE);
+  lo = imax(0, floor_div(qe - 1 - s.wl + TILE - 1, TILE));
+  hi = floor_div(qs + s.wr - (TILE - 1), TILE);
+}
+
+// Query tiles whose rows all see every key of key tile kt are [lo, hi]: rows
+// j - wr .. j + wl see key j, so a query tile is full for keys [ks, ke) when
+// its first row reaches ke-1 - wr and its last row at most ks + wl.
+FA_HD void q_full_range(const Dims& s, int kt, int& lo, int& hi) {
+  const int ks = kt * TILE, ke = imin(s.Nk, ks + TILE);
+  lo = imax(0, floor_div(ke - 1 - s.wr + TILE - 1, TILE));
+  hi = floor_div(ks + s.wl - (TILE - 1), TILE);
+}
+
+// Query tiles visiting key tile kt: the range [lo, hi) of tiles holding a row
+// that sees some key of the tile (rows j - wr .. j + wl see key j).
+FA_HD void q_range(const Dims& s, int kt, int& lo, int& hi) {
+  const int nq = q_tiles(s);
+  const long long first = static_cast<long long>(kt) * TILE - s.wr;
+  const long long last = static_cast<long long>(imin(s.Nk, (kt + 1) * TILE)) - 1 + s.wl;
+  lo = first <= 0 ? 0 : static_cast<int>(first / TILE);
+  hi = last >= static_cast<long long>(nq) * TILE ? nq : static_cast<int>(last / TILE) + 1;
 }
 
 // ---- forward units: (b, h, p) = query tiles 2p and 2p+1 of head h ------------

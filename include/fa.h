@@ -78,6 +78,14 @@ typedef struct {
   int d;        /* head dim: 64 or 128 */
   float scale;  /* softmax scale applied to q.k (e.g. 1/sqrt(d)) */
   int causal;   /* 0 or 1 */
+  /* Sliding window (flash_attn_func's window_size, §18.7.1; local attention,
+   * §18.8.1): with window = 1, query i sees keys i - window_left .. i +
+   * window_right (a negative bound is unbounded; causal still caps at i).
+   * window = 0 (a zero-initialised struct) means no window.  Needs Nq == Nk,
+   * like causal; forward and backward only (decode rejects it). */
+  int window;
+  int window_left;
+  int window_right;
 } fa_shape_t;
 
 /* ---------------------------------------------------------------------------

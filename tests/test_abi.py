@@ -56,6 +56,27 @@ def test_tile_classes_match_oracle(lib, N, causal):
             assert lib.fa_tile_class(S(1, 1, 1, N, N, causal=causal), i, j) == c
 
 
+@pytest.mark.parametrize("N,left,right,causal", [(1000, 100, 50, False), (777, 300, -1, True), (512, 0, 0, False),
+                                                 (640, 128, 128, False), (300, 1000, 3, True), (4096, 1024, 0, True),
+                                                 (640, 128, -1, False), (1000, -1, 200, False)])
+def test_window_tile_classes_match_oracle(lib, N, left, right, causal):
+    s = ctypes.byref(shape(1, 1, 1, N, N, 64, causal=causal, window=(left, right)))
+    nt = -(-N // 128)
+    for i in range(nt):
+        for j in range(nt):
+            want = P.window_tile_class(i * 128, min(N, i * 128 + 128), j * 128, min(N, j * 128 + 128), left, right,
+                                       causal)
+            assert lib.fa_tile_class(s, i, j) == want, (i, j)
+
+
+def test_window_needs_square_shape(lib):
+    s = shape(1, 1, 1, 100, 200, 64, window=(10, 10))
+    assert lib.fa_tile_class(ctypes.byref(s), 0, 0) == -1
+    s.window = 2
+    s.Nk = 100
+    assert lib.fa_tile_class(ctypes.byref(s), 0, 0) == -1
+
+
 def test_noncausal_rectangular_classes(lib):
     assert lib.fa_tile_class(S(1, 1, 1, 100, 700), 0, 5) == P.FULL
     assert lib.fa_tile_class(S(1, 1, 1, 100, 700), 0, 6) == -1   # out of range

@@ -9,10 +9,13 @@ in HBM:
   decode legs    split-KV decode + combine of
                  decode_b8_hq32_hkv8_q1_kv131072_d128 and the q4 variant, and the
                  q1 cache in shuffled pages of 16 keys through fa_decode_paged
+  window leg     forward + backward of window_causal_b1_hq32_hkv8_n16384_w4096_d128
+                 (each query sees itself and the 4095 keys before it)
 ``value`` = counted forward + backward FLOPs of the training legs divided by
 their device time (TFLOPS; forward 4*B*H*Nq*Nk*d, halved when causal, backward
-2.5x that).  Decode legs report KV-read GB/s.  L2 is flushed (256 MiB write)
-before every launch group, outside its events.
+2.5x that).  The window leg is reported beside it with its FLOPs counted over
+the (query, key) pairs inside the window.  Decode legs report KV-read GB/s.  L2
+is flushed (256 MiB write) before every launch group, outside its events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --profile-case WORKLOAD   # two fwd+bwd passes, for ncu captures
@@ -42,8 +45,9 @@ TRAIN = ("causal_b2_h16_n4096_d128", "gqa_causal_b1_hq32_hkv8_n8192_d128_outlier
 DECODE = ("decode_b8_hq32_hkv8_q1_kv131072_d128", "decode_b8_hq32_hkv8_q4_kv131072_d128")
 PAGED = ("decode_b8_hq32_hkv8_q1_kv131072_d128", 16)  # the q1 decode cache in shuffled pages of 16 keys
 PAGED_NAME = PAGED[0] + "_paged16"
+WINDOW = ("window_causal_b1_hq32_hkv8_n16384_w4096_d128",)
 WORKLOAD = (" + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode); " + PAGED_NAME +
-            " (paged decode)")
+            " (paged decode); " + " + ".join(WINDOW) + " (sliding-window fwd+bwd)")
 METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -54,10 +58,25 @@ def workloads():
     from exact_io_aware_21_gb300 import inputs
 
     by = {w.name: w for w in inputs.ALL}
-    return [by[n] for n in TRAIN], [by[n] for n in DECODE] + [by[PAGED[0]]]
+    return [by[n] for n in TRAIN], [by[n] for n in DECODE] + [by[PAGED[0]]], [by[n] for n in WINDOW]
+
+
+def window_pairs(w):
+    """(query, key) pairs inside the window: row i sees keys max(0, i-l) .. min(Nk-1, i+r)."""
+    left, right = w.window
+    n = 0
+    for i in range(w.Nq):
+        lo = 0 if left < 0 else max(0, i - left)
+        hi = w.Nk - 1 if right < 0 else min(w.Nk - 1, i + right)
+        if w.causal:
+            hi = min(hi, i)
+        n += max(0, hi - lo + 1)
+    return n
 
 
 def fwd_flops(w):
+    if w.window is not None:
+        return 4.0 * w.B * w.Hq * w.d * window_pairs(w)
     f = 4.0 * w.B * w.Hq * w.Nq * w.Nk * w.d
     return f / 2 if w.causal else f
 
@@ -233,7 +252,7 @@ def run_reference(args):
     _, rank, _ = dist_env()
     if rank != 0:
         return 0
-    train, _ = workloads()
+    train, _, _ = workloads()
     per_step = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
     value, s_per_step, desc = oracle_run(train, per_step, args.steps, args.warmup)
     cpu = {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
@@ -279,11 +298,11 @@ def make_legs(device, seed):
     from exact_io_aware_21_gb300 import inputs
 
     lib = fa.library()
-    train, dec = workloads()
+    train, dec, win = workloads()
     legs, state = [], {}
-    for w in train:
+    for w in train + win:
         x = inputs.make(w, device=device, seed=w.seed + seed)
-        s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal)
+        s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal, w.window)
         st = dict(x=x, s=s, o=torch.empty_like(x["q"]), ores=torch.empty_like(x["q"]),
                   lse=torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=device),
                   dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
@@ -302,7 +321,7 @@ def make_legs(device, seed):
 
         fns = [("fwd", fwd), ("bwd_pre", lambda part=part: part(0)), ("bwd_dkdv", lambda part=part: part(1)),
                ("bwd_dq", lambda part=part: part(2))]
-        legs.append(Leg(w.name, "train", w, fns, 3.5 * fwd_flops(w)))
+        legs.append(Leg(w.name, "window" if w.window else "train", w, fns, 3.5 * fwd_flops(w)))
     for i, w in enumerate(dec):
         paged = i == len(dec) - 1
         name = PAGED_NAME if paged else w.name
@@ -472,7 +491,10 @@ def run_ours(args):
     for leg, part, e0, e1 in recs:
         leg.ms[part] += e0.elapsed_time(e1) / args.steps
     leg_ms = {l.name: sum(l.ms.values()) for l in legs}
-    step_ms = sum(leg_ms.values())
+    # the step is the training and decode legs; the window leg is timed in the same
+    # loop and reported beside them
+    step_legs = [l for l in legs if l.kind != "window"]
+    step_ms = sum(leg_ms[l.name] for l in step_legs)
     train_ms = sum(leg_ms[l.name] for l in legs if l.kind == "train")
     max_train_ms, total_flops = aggregate(train_ms, sum(l.work for l in legs if l.kind == "train"), world)
     max_step_ms, _ = aggregate(step_ms, 0.0, world)
@@ -480,7 +502,7 @@ def run_ours(args):
 
     legs_out = {}
     for l in legs:
-        if l.kind == "train":
+        if l.kind in ("train", "window"):
             f = fwd_flops(l.w)
             bwd_ms = l.ms["bwd_pre"] + l.ms["bwd_dkdv"] + l.ms["bwd_dq"]
             legs_out[l.name] = {
@@ -489,13 +511,16 @@ def run_ours(args):
                 "bwd_ms": bwd_ms, "bwd_tflops": 2.5 * f / bwd_ms / 1e9,
                 "bwd_frac_of_sustained_peak": 2.5 * f / bwd_ms / 1e9 / sus,
                 "bwd_parts_ms": {k: l.ms[k] for k in ("bwd_pre", "bwd_dkdv", "bwd_dq")}}
+            if l.kind == "window":
+                legs_out[l.name].update({"window": list(l.w.window), "in_step": False,
+                                         "flops_count": "4*B*H*d per visible (query, key) pair, x3.5 fwd+bwd"})
         else:
             ms = l.ms["decode"]
             legs_out[l.name] = {"ms": ms, "gbs": l.work / ms / 1e6, "frac_of_hbm_peak": l.work / ms / 1e6 /
                                 peaks["hbm_gbs"], "num_splits": state[l.name]["S"]}
 
     # roofline of the dominant kernel: the launch with the largest share of the step
-    dl, dp = max(((l, p) for l in legs for p, _ in l.fns if p != "bwd_pre"), key=lambda lp: lp[0].ms[lp[1]])
+    dl, dp = max(((l, p) for l in step_legs for p, _ in l.fns if p != "bwd_pre"), key=lambda lp: lp[0].ms[lp[1]])
     if dp == "decode":
         ach = dl.work / dl.ms[dp] / 1e6
         roof = {"kernel": "fa_decode_split_kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
@@ -561,8 +586,10 @@ def profile_case(name):
     w = {x.name: x for x in inputs.ALL}[name]
     x = inputs.make(w, device="cuda")
     for _ in range(2):
-        o, lse, res = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, residual=True)
-        fa.backward(x["q"], x["k"], x["v"], o, lse, x["do"], causal=w.causal, scale=w.scale, o_residual=res)
+        o, lse, res = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, residual=True,
+                                 window=w.window)
+        fa.backward(x["q"], x["k"], x["v"], o, lse, x["do"], causal=w.causal, scale=w.scale, o_residual=res,
+                    window=w.window)
     torch.cuda.synchronize()
     print("ok")
     return 0

@@ -34,6 +34,7 @@ class Workload:
     outliers: bool = False
     seed: int = 0
     decode: bool = False
+    window: tuple = None  # (left, right): query i sees keys i - left .. i + right (negative: unbounded)
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
     @property
@@ -49,8 +50,11 @@ GQA_N8192_D128 = Workload("gqa_causal_b1_hq32_hkv8_n8192_d128_outliers", 1, 32, 
                           True, outliers=True)
 DECODE_Q1 = Workload("decode_b8_hq32_hkv8_q1_kv131072_d128", 8, 32, 8, 1, 131072, 128, False, decode=True)
 DECODE_Q4 = Workload("decode_b8_hq32_hkv8_q4_kv131072_d128", 8, 32, 8, 4, 131072, 128, False, decode=True)
+# Causal sliding window: every query sees itself and the 4095 keys before it.
+WINDOW_N16384_W4096 = Workload("window_causal_b1_hq32_hkv8_n16384_w4096_d128", 1, 32, 8, 16384, 16384, 128,
+                               True, window=(4095, 0))
 
-ALL = [TINY, MHA_N2048_D64, CAUSAL_N4096_D128, GQA_N8192_D128, DECODE_Q1, DECODE_Q4]
+ALL = [TINY, MHA_N2048_D64, CAUSAL_N4096_D128, GQA_N8192_D128, DECODE_Q1, DECODE_Q4, WINDOW_N16384_W4096]
 
 
 def make(w, device="cpu", with_do=True, seed=None):

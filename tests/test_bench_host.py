@@ -1,0 +1,32 @@
+"""Host logic of the benchmark (no GPU): the counted FLOPs of the sliding-window leg."""
+
+import numpy as np
+import pytest
+
+import bench
+from exact_io_aware_21_gb300 import inputs
+from oracle import attention as A
+
+
+@pytest.mark.parametrize("N,window,causal", [(300, (37, 0), True), (300, (37, 11), False), (257, (0, 0), False),
+                                             (129, (-1, 5), False), (129, (500, 0), True)])
+def test_window_pairs_is_the_visible_pair_count(N, window, causal):
+    w = inputs.Workload("t", 1, 1, 1, N, N, 64, causal, window=window)
+    rows = np.arange(N)
+    hidden = A.window_mask(rows, N, *window)
+    if causal:
+        hidden |= A.causal_mask(rows, N)
+    assert bench.window_pairs(w) == int((~hidden).sum())
+
+
+def test_window_workload_flops():
+    w = inputs.WINDOW_N16384_W4096
+    # 4096 rows still growing (1 + 2 + ... + 4096 keys), then 12288 rows of 4096 keys
+    assert bench.window_pairs(w) == 4096 * 4097 // 2 + 12288 * 4096
+    assert bench.fwd_flops(w) == 4.0 * 32 * 128 * bench.window_pairs(w)
+
+
+def test_window_leg_is_outside_the_step():
+    train, dec, win = bench.workloads()
+    assert [w.name for w in win] == list(bench.WINDOW)
+    assert all(w.window is None for w in train + dec)

@@ -89,6 +89,15 @@ def make(w, device="cpu", with_do=True, seed=None):
     return out
 
 
+def hadamard_signs(d, seed=0):
+    """d random signs (+1.0 / -1.0, float32) for the random Hadamard rotation: a CPU
+    generator seeded with ``seed`` draws d bits."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    bits = torch.randint(0, 2, (d,), generator=gen)
+    return (1.0 - 2.0 * bits).to(torch.float32)
+
+
 def shape_inputs(B, Hq, Hkv, Nq, Nk, d, seed=0, device="cpu", with_do=True):
     """Draw (q, k, v, do) for an arbitrary shape with the same recipe (no outliers)."""
     w = Workload("custom", B, Hq, Hkv, Nq, Nk, d, False, seed=seed)

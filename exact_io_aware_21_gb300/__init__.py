@@ -12,7 +12,11 @@ from .binding import (  # noqa: F401
     fa_decode,
     fa_decode_paged,
     fa_fwd,
+    fa_fwd_fp8,
+    fa_quantize_fp8,
     forward,
+    forward_fp8,
+    quantize_fp8,
     backward,
     decode,
     decode_paged,

@@ -71,6 +71,9 @@ SIGNATURES = {
     "fa_dq_unit": (_I, [_PS, _I, _PI, _PI, _PI]),
     "fa_decode_split_range": (_I, [_PS, _I, _I, _PI, _PI]),
     "fa_selftest_mma": (_I, [_I, _I, _VP, _VP, _VP, _VP, _VP]),
+    "fa_quantize_fp8_workspace_size": (_SZ, [_I, _I]),
+    "fa_quantize_fp8": (_I, [_PT, _I, _I, _I, _I, _I, _VP, _PT, _VP, _VP, _SZ, _VP]),
+    "fa_fwd_fp8": (_I, [_PT, _PT, _PT, _VP, _VP, _VP, _PT, _VP, _PS, _VP, _SZ, _VP]),
 }
 
 
@@ -114,6 +117,13 @@ def tdesc(t):
     """[B, N, H, d] bf16 CUDA tensor -> FaTensor (strides in elements)."""
     if t.dim() != 4 or t.dtype != torch.bfloat16 or not t.is_cuda or t.stride(-1) != 1:
         raise FAError(1, "expected a 4-D bf16 CUDA tensor [B, N, H, d] with unit head-dim stride")
+    return FaTensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
+
+
+def tdesc_u8(t):
+    """[B, N, H, d] uint8 (E4M3 codes) CUDA tensor -> FaTensor (strides in bytes)."""
+    if t.dim() != 4 or t.dtype != torch.uint8 or not t.is_cuda or t.stride(-1) != 1:
+        raise FAError(1, "expected a 4-D uint8 CUDA tensor [B, N, H, d] with unit head-dim stride")
     return FaTensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
 
 
@@ -164,6 +174,24 @@ def fa_decode_paged(q, kc, vc, block_table, seqlens_k, o, lse, s, num_splits, wo
     check(lib.fa_decode_paged(tdesc(q), tdesc(kc), tdesc(vc), block_table.data_ptr(), block_table.shape[1],
                               seqlens_k.data_ptr(), kc.shape[0], kc.shape[1], tdesc(o), lse.data_ptr(),
                               ctypes.byref(s), int(num_splits), workspace.data_ptr(), workspace.numel(), _stream(q)))
+
+
+def fa_quantize_fp8(x, block_rows, signs, out, scales, workspace):
+    """x [B, N, H, d] bf16 -> out uint8 codes and fp32 scales (see fa_quantize_fp8 in include/fa.h)."""
+    lib = library()
+    B, N, H, d = x.shape
+    if signs is not None and (signs.dtype != torch.float32 or not signs.is_cuda or signs.numel() != d):
+        raise FAError(1, "signs must be a float32 CUDA tensor of d values")
+    check(lib.fa_quantize_fp8(tdesc(x), B, N, H, d, int(block_rows), None if signs is None else signs.data_ptr(),
+                              tdesc_u8(out), scales.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                              _stream(x)))
+
+
+def fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, s, workspace):
+    lib = library()
+    check(lib.fa_fwd_fp8(tdesc_u8(q8), tdesc_u8(k8), tdesc_u8(v8), q_scale.data_ptr(), k_scale.data_ptr(),
+                         v_scale.data_ptr(), tdesc(o), lse.data_ptr(), ctypes.byref(s), workspace.data_ptr(),
+                         workspace.numel(), _stream(q8)))
 
 
 def device_status(workspace):
@@ -234,4 +262,27 @@ def decode_paged(q, k_cache, v_cache, block_table, seqlens_k, max_seqlen=None, s
     lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
     ws = _ws(library().fa_decode_workspace_size(ctypes.byref(s), int(num_splits)), q.device)
     fa_decode_paged(q, k_cache, v_cache, block_table, seqlens_k, o, lse, s, num_splits, ws)
+    return o, lse
+
+
+def quantize_fp8(x, block_rows=128, signs=None):
+    """E4M3 codes and scales of x [B, N, H, d] bf16: per 128-row block (``block_rows``
+    = 128, scales [B, H, ceil(N/128)]) or per head (0, scales [B, H]); ``signs``
+    (d float32 +-1 on the device) rotates the rows by the random Hadamard matrix first."""
+    B, N, H, d = x.shape
+    out = torch.empty((B, N, H, d), dtype=torch.uint8, device=x.device)
+    nblk = -(-N // 128)
+    scales = torch.empty((B, H, nblk) if block_rows else (B, H), dtype=torch.float32, device=x.device)
+    ws = _ws(library().fa_quantize_fp8_workspace_size(B, H), x.device)
+    fa_quantize_fp8(x, block_rows, signs, out, scales, ws)
+    return out, scales
+
+
+def forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None, window=None):
+    """O (bf16), LSE from E4M3 operands made by ``quantize_fp8`` (Q, K per block, V per head)."""
+    s = _dims(q8, k8, scale, causal, window)
+    o = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q8.device)
+    ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q8.device)
+    fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, s, ws)
     return o, lse

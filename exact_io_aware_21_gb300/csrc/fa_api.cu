@@ -89,6 +89,23 @@ int make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int64_
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ALIGN;
 }
 
+// The same map over one-byte elements (E4M3 codes): box 128 x 1 x box_rows x 1,
+// the 128-byte inner box matching the 128-byte swizzle.  Strides in elements.
+int make_map_u8(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int64_t sb, int64_t sn, int64_t sh,
+                int box_rows = TILE) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return FA_ERR_CUDA;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sh), static_cast<cuuint64_t>(sn), static_cast<cuuint64_t>(sb)};
+  cuuint32_t box[4] = {128, 1, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ALIGN;
+}
+
 // ---- argument checks ----------------------------------------------------------------
 int check_shape(const fa_shape_t* s) {
   if (!s) return FA_ERR_INVALID;
@@ -111,6 +128,15 @@ int check_tensor(const fa_tensor_t* t) {
   if (t->stride_b < 0 || t->stride_n < 0 || t->stride_h < 0) return FA_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(t->ptr) & 15) != 0) return FA_ERR_ALIGN;
   if ((t->stride_b % 8) || (t->stride_n % 8) || (t->stride_h % 8)) return FA_ERR_ALIGN;
+  return FA_OK;
+}
+
+// one-byte E4M3 codes: TMA and the quantiser's 16-byte row accesses need 16-byte strides
+int check_tensor_u8(const fa_tensor_t* t) {
+  if (!t || !t->ptr) return FA_ERR_INVALID;
+  if (t->stride_b < 0 || t->stride_n < 0 || t->stride_h < 0) return FA_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(t->ptr) & 15) != 0) return FA_ERR_ALIGN;
+  if ((t->stride_b % 16) || (t->stride_n % 16) || (t->stride_h % 16)) return FA_ERR_ALIGN;
   return FA_OK;
 }
 
@@ -278,6 +304,83 @@ int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
   a.o = rows_of(o);
   a.o_res = o_res ? rows_of(o_res) : OutRows{nullptr, 0, 0, 0};
   a.lse = lse;
+  a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
+  a.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_COUNTER_OFFSET);
+  a.timeout_ns = g_timeout_ns;
+  a.num_sms = sms;
+  if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
+  cudaError_t e = launch_fwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
+}
+
+// ------------------------------------------------------------------------ FP8
+size_t fa_quantize_fp8_workspace_size(int B, int H) {
+  if (B <= 0 || H <= 0) return 0;
+  return FA_WS_HEADER_BYTES + round_up(static_cast<size_t>(B) * H * sizeof(unsigned), 256);
+}
+
+int fa_quantize_fp8(const fa_tensor_t* x, int B, int N, int H, int d, int block_rows, const float* signs,
+                    const fa_tensor_t* out, float* scales, void* ws, size_t ws_bytes, void* stream) {
+  int rc;
+  if (B <= 0 || N <= 0 || H <= 0 || (d != 64 && d != 128) || (block_rows != 0 && block_rows != TILE) || !scales)
+    return FA_ERR_INVALID;
+  if (static_cast<int64_t>(cdiv(N, TILE)) > 0x7fffffff || H > 65535 || B > 65535) return FA_ERR_INVALID;
+  if ((rc = check_tensor(x)) || (rc = check_tensor_u8(out))) return rc;
+  if ((rc = check_ws(ws, ws_bytes, fa_quantize_fp8_workspace_size(B, H)))) return rc;
+  QuantLaunch a;
+  memset(&a, 0, sizeof(a));
+  a.x = x->ptr;
+  a.sb = x->stride_b;
+  a.sn = x->stride_n;
+  a.sh = x->stride_h;
+  a.B = B;
+  a.N = N;
+  a.H = H;
+  a.d = d;
+  a.signs = signs;
+  a.out = out->ptr;
+  a.ob = out->stride_b;
+  a.on = out->stride_n;
+  a.oh = out->stride_h;
+  a.scales = scales;
+  a.head_amax = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + FA_WS_HEADER_BYTES);
+  a.nblk = cdiv(N, TILE);
+  a.per_block = block_rows != 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!a.per_block) {
+    cudaError_t e = cudaMemsetAsync(a.head_amax, 0, static_cast<size_t>(B) * H * sizeof(unsigned), st);
+    if (e != cudaSuccess) return cuda_fail(e, FA_ERR_CUDA);
+  }
+  cudaError_t e = launch_quantize(a, st);
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
+}
+
+int fa_fwd_fp8(const fa_tensor_t* q8, const fa_tensor_t* k8, const fa_tensor_t* v8, const float* q_scale,
+               const float* k_scale, const float* v_scale, const fa_tensor_t* o, float* lse, const fa_shape_t* s,
+               void* ws, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_shape(s)) || (rc = check_tensor_u8(q8)) || (rc = check_tensor_u8(k8)) ||
+      (rc = check_tensor_u8(v8)) || (rc = check_tensor(o)))
+    return rc;
+  if (s->d != 128 || !lse || !q_scale || !k_scale || !v_scale) return FA_ERR_INVALID;
+  if ((rc = check_ws(ws, ws_bytes, fa_fwd_workspace_size(s)))) return rc;
+  int sms = 0;
+  if ((rc = device_info(&sms))) return rc;
+  FwdLaunch a;
+  memset(&a, 0, sizeof(a));
+  a.dims = dims_of(s);
+  a.d = s->d;
+  a.scale = s->scale;
+  if ((rc = make_map_u8(&a.tm_q, q8->ptr, s->B, s->Nq, s->Hq, s->d, q8->stride_b, q8->stride_n, q8->stride_h)) ||
+      (rc = make_map_u8(&a.tm_k, k8->ptr, s->B, s->Nk, s->Hkv, s->d, k8->stride_b, k8->stride_n, k8->stride_h)) ||
+      (rc = make_map_u8(&a.tm_v, v8->ptr, s->B, s->Nk, s->Hkv, s->d, v8->stride_b, v8->stride_n, v8->stride_h)))
+    return rc;
+  a.o = rows_of(o);
+  a.o_res = OutRows{nullptr, 0, 0, 0};
+  a.lse = lse;
+  a.sq = q_scale;
+  a.sk = k_scale;
+  a.sv = v_scale;
   a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
   a.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_COUNTER_OFFSET);
   a.timeout_ns = g_timeout_ns;
@@ -474,16 +577,23 @@ int fa_decode_paged(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor
 
 // ------------------------------------------------------------------------ self-test
 int fa_selftest_mma(int mode, int nk, const void* a, const void* b, float* c, void* ws, void* stream) {
-  if ((mode != 0 && mode != 1) || (nk != 64 && nk != 128) || !a || !b || !c) return FA_ERR_INVALID;
+  if (mode < 0 || mode > 3 || (nk != 64 && nk != 128) || (mode >= 2 && nk != 128) || !a || !b || !c)
+    return FA_ERR_INVALID;
   int sms = 0, rc;
   if ((rc = check_ws(ws, FA_WS_HEADER_BYTES, FA_WS_HEADER_BYTES))) return rc;
   if ((rc = device_info(&sms))) return rc;
   CUtensorMap ta, tb;
   // mode 0: a, b are [128 x k] row-major.  mode 1: a [128 x 128] is read by
-  // threads (the map over it is unused), b is [128 x n] row-major.
-  if ((rc = make_map(&ta, mode == 0 ? a : b, 1, 128, 1, nk, 128 * nk, nk, nk)) ||
-      (rc = make_map(&tb, b, 1, 128, 1, nk, 128 * nk, nk, nk)))
+  // threads (the map over it is unused), b is [128 x n] row-major.  Modes 2, 3:
+  // the same with one-byte E4M3 codes.
+  if (mode >= 2) {
+    if ((rc = make_map_u8(&ta, mode == 2 ? a : b, 1, 128, 1, 128, 128 * 128, 128, 128)) ||
+        (rc = make_map_u8(&tb, b, 1, 128, 1, 128, 128 * 128, 128, 128)))
+      return rc;
+  } else if ((rc = make_map(&ta, mode == 0 ? a : b, 1, 128, 1, nk, 128 * nk, nk, nk)) ||
+             (rc = make_map(&tb, b, 1, 128, 1, nk, 128 * nk, nk, nk))) {
     return rc;
+  }
   int* status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
   if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
   cudaError_t e = launch_selftest_mma(mode, nk, ta, tb, a, c, status, static_cast<cudaStream_t>(stream));

@@ -21,6 +21,12 @@
 // TMEM (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,256+d) O_1 [256+d,256+2d);
 // P_t is written as bf16 over the first 64 columns of S_t and read from TMEM by
 // the P V product.
+// FP8 instantiation ("第18章" §18.6.2): Q, K, V arrive as E4M3 codes with
+// per-block scales for Q and K and one scale per head for V; S = Q K^T and O +=
+// P V run as kind::f8f6f4 products (K = 32 per instruction), S is scaled by
+// the product of the two block scales, the softmax stays in fp32, and P goes
+// to TMEM as E4M3 on the scale its bound fixes (448 P, four codes per column);
+// the epilogue applies V's scale with 1 / l.
 // The running max is the exact row max so far (TAU = 0): the dominant P of a
 // nearly one-hot row is then exactly 1.0 in bf16, so O's error scales with the
 // rest of the row, which keeps D = dO . O consistent in the backward.  The
@@ -37,17 +43,20 @@ namespace {
 
 constexpr float TAU = 0.0f;
 constexpr float LN2 = 0.69314718055994530942f;
+constexpr float LOG2_448 = 8.8073549220576041f;  // P is quantised as 448 P = 2^(x - m + log2 448)
 
-template <int D>
+template <int D, bool F8 = false>
 struct FwdLayout {
-  static constexpr int QB = TILE * D * 2;    // one Q tile (bytes)
-  static constexpr int TB = TILE * D * 2;    // one K or V tile
-  static constexpr int STAGES = D == 64 ? 6 : 4;  // K/V tile slots
+  static constexpr int ESZ = F8 ? 1 : 2;     // bytes per element
+  static constexpr int QB = TILE * D * ESZ;  // one Q tile (bytes)
+  static constexpr int TB = TILE * D * ESZ;  // one K or V tile
+  static constexpr int STAGES = F8 ? 8 : (D == 64 ? 6 : 4);  // K/V tile slots
   // Slots are used in pairs: group 0 of a unit holds K_0, group j+1 holds V_j and
   // K_{j+1} (the two tiles the step after S_j reads), so a step costs the MMA
   // thread one wait and one release instead of two of each.
   static constexpr int NG = STAGES / 2;
-  static constexpr int CH = D / 64;          // 64-column swizzle atoms per tile row
+  static constexpr int CH = D * ESZ / 128;   // 128-byte swizzle atoms per tile row
+  static constexpr int ECH = 128 / ESZ;      // elements per atom row (the TMA box width)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = 2 * QB;
   static constexpr int OFF_BAR = OFF_KV + STAGES * TB;
@@ -64,6 +73,10 @@ struct FwdLayout {
 struct FwdParams {
   Dims dims;
   float scale_log2;
+  const float* sq;  // FP8: Q block scales [B, Hq, nqt], K block scales [B, Hkv, nkt], V head scales [B, Hkv]
+  const float* sk;
+  const float* sv;
+  int nqt, nkt;
   OutRows o;
   OutRows o_res;
   float* lse;
@@ -77,9 +90,9 @@ struct Bars {
   uint64_t *unit_full, *unit_empty, *q_full, *q_empty, *kv_full, *kv_empty, *s_full, *p_full, *o_full, *o_empty;
 };
 
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, F8>;
   uint64_t* b = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   Bars r;
   r.unit_full = b;
@@ -142,11 +155,11 @@ __device__ __forceinline__ UnitTiles unit_tiles(const Dims& s, int p) {
 }
 
 // ------------------------------------------------------------------ producer
-template <int D, int MASK>
+template <int D, int MASK, bool F8>
 __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, const CUtensorMap* tm_q,
                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, const FwdParams& p,
                              const Ctl& ctl) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, F8>;
   const int g = p.dims.Hq / p.dims.Hkv;
   uint32_t seq = 0;       // K/V groups issued so far (ring sequence number)
   int q_armed = -1;       // last unit index whose Q load was issued
@@ -169,7 +182,7 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
     for (int t = 0; t < 2; ++t)
 #pragma unroll
       for (int c = 0; c < L::CH; ++c)
-        tma_load_4d(smem + L::OFF_Q + t * L::QB + c * (TILE * 128), tm_q, bar.q_full, c * 64, h,
+        tma_load_4d(smem + L::OFF_Q + t * L::QB + c * (TILE * 128), tm_q, bar.q_full, c * L::ECH, h,
                     (2 * pr + t) * TILE, b);
     q_armed = it;
 
@@ -186,10 +199,11 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
 #pragma unroll
       for (int c = 0; c < L::CH; ++c) {
         if (has_v)
-          tma_load_4d(base + c * (TILE * 128), tm_v, &bar.kv_full[gs], c * 64, kvh, (ut.base + gi - 1) * TILE, b);
-        if (has_k)
-          tma_load_4d(base + L::TB + c * (TILE * 128), tm_k, &bar.kv_full[gs], c * 64, kvh, (ut.base + gi) * TILE,
+          tma_load_4d(base + c * (TILE * 128), tm_v, &bar.kv_full[gs], c * L::ECH, kvh, (ut.base + gi - 1) * TILE,
                       b);
+        if (has_k)
+          tma_load_4d(base + L::TB + c * (TILE * 128), tm_k, &bar.kv_full[gs], c * L::ECH, kvh,
+                      (ut.base + gi) * TILE, b);
       }
     }
     if (!ok) break;
@@ -205,12 +219,14 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D, int MASK>
+template <int D, int MASK, bool F8>
 __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
                         const Ctl& ctl) {
-  using L = FwdLayout<D>;
-  constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);  // Q K^T, both K-major
-  constexpr uint32_t IDESC_O = idesc_bf16(128, D, false, true);     // P V, V is N-major
+  using L = FwdLayout<D, F8>;
+  // Q K^T with both operands K-major; P V with V N-major
+  constexpr uint32_t IDESC_S = F8 ? idesc_e4m3(128, 128, false, false) : idesc_bf16(128, 128, false, false);
+  constexpr uint32_t IDESC_O = F8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
+  constexpr int KS = F8 ? 32 : 16;  // K of one product (32 bytes of a 128-byte swizzle row)
   const uint32_t q_base = smem_u32(smem + L::OFF_Q);
   const uint32_t kv_base = smem_u32(smem + L::OFF_KV);
   uint32_t seq = 0;
@@ -220,20 +236,27 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
   auto issue_s = [&](int t, uint32_t k_addr) {
     const uint32_t d_tmem = tmem + t * 128;
 #pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
+    for (int k = 0; k < D / KS; ++k) {
       const uint32_t off = (k / 4) * (TILE * 128) + (k % 4) * 32;
       const uint64_t a = sdesc_sw128(q_base + t * L::QB + off, 16, 1024);
       const uint64_t bd = sdesc_sw128(k_addr + off, 16, 1024);
-      mma_ss(d_tmem, a, bd, IDESC_S, k > 0);
+      if (F8)
+        mma_ss_f8(d_tmem, a, bd, IDESC_S, k > 0);
+      else
+        mma_ss(d_tmem, a, bd, IDESC_S, k > 0);
     }
   };
+  // P is read from TMEM, 8 columns per product (8 x 2 bf16 or 8 x 4 E4M3 keys)
   auto issue_pv = [&](int t, uint32_t v_addr, bool acc) {
     const uint32_t d_tmem = tmem + 256 + t * D;
     const uint32_t p_tmem = tmem + t * 128;
 #pragma unroll
-    for (int k = 0; k < TILE / 16; ++k) {
-      const uint64_t bd = sdesc_sw128(v_addr + k * 16 * 128, TILE * 128, 1024);
-      mma_ts(d_tmem, p_tmem + k * 8, bd, IDESC_O, (acc || k > 0) ? 1u : 0u);
+    for (int k = 0; k < TILE / KS; ++k) {
+      const uint64_t bd = sdesc_sw128(v_addr + k * KS * 128, TILE * 128, 1024);
+      if (F8)
+        mma_ts_f8(d_tmem, p_tmem + k * 8, bd, IDESC_O, (acc || k > 0) ? 1u : 0u);
+      else
+        mma_ts(d_tmem, p_tmem + k * 8, bd, IDESC_O, (acc || k > 0) ? 1u : 0u);
     }
   };
   auto group_wait = [&](uint32_t gq) {
@@ -296,7 +319,7 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
 }
 
 // ------------------------------------------------------------------ softmax
-template <int D, int MASK>
+template <int D, int MASK, bool F8>
 __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
                             const Ctl& ctl, uint8_t* scratch) {
   const int wq = (threadIdx.x >> 5) & 3;  // warp within the warpgroup = TMEM lane quarter
@@ -305,7 +328,6 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
   const uint32_t tS = tmem + lanes + t * 128;
   const uint32_t tO = tmem + lanes + 256 + t * D;
   const float c = p.scale_log2;
-  const float2 c2 = make_float2(c, c);
   const Dims& s = p.dims;
   uint32_t sph = 0, active = 0;
 
@@ -324,6 +346,11 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     const int qt = 2 * pr + t;
     const int q_row = qt * TILE + r;
     const int kt0 = ut.base + ut.a[t];  // first key tile of this query tile
+    // FP8: logits = S * scale*log2(e) * s_q * s_k[kt]; a zero block scale leaves S = 0
+    // exactly, and the floor keeps masked -inf scores from becoming NaN
+    const int kvh = h / (s.Hq / s.Hkv);
+    const float cq = F8 ? c * p.sq[(static_cast<int64_t>(b) * s.Hq + h) * p.nqt + qt] : c;
+    const float* skp = F8 ? p.sk + (static_cast<int64_t>(b) * s.Hkv + kvh) * p.nkt + kt0 : nullptr;
     int full_lo = 0, full_hi = 0;        // band: key tiles this query tile sees in full
     if (MASK == MASK_BAND) {
       kv_full_range(s, qt, full_lo, full_hi);
@@ -332,6 +359,8 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
 
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < n; ++j) {
+      const float cj = F8 ? fmaxf(cq * __ldg(skp + j), 1.17549435e-38f) : c;
+      const float2 cj2 = make_float2(cj, cj);
       ok = mbar_wait(&bar.s_full[t], sph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
       sph ^= 1;
       if (!__all_sync(0xffffffffu, ok)) return;
@@ -370,7 +399,7 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
         mx2 = fmax3(mx2, sv[i + 4], sv[i + 5]);
         mx3 = fmax3(mx3, sv[i + 6], sv[i + 7]);
       }
-      const float m_tile = fmaxf(fmax3(mx0, mx1, mx2), mx3) * c;
+      const float m_tile = fmaxf(fmax3(mx0, mx1, mx2), mx3) * cj;
       const float m_new = (m_tile > m_run + TAU) ? m_tile : m_run;
       // Under a band a row may see no key of a tile: while it has seen none at all, m
       // stays -inf, alpha 1 and every p 0.  (Causal and full rows see a key in their
@@ -378,23 +407,29 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
       // the full d = 64 kernel 5%, hence the split.)
       const float alpha = (MASK == MASK_CAUSAL) ? ex2(m_run - m_new) : (m_new == m_run) ? 1.f : ex2(m_run - m_new);
       const float m_use = (MASK == MASK_BAND && m_new == -INFINITY) ? 0.f : m_new;
-      const float2 neg_m2 = make_float2(-m_use, -m_use);
+      // FP8: p' = 448 p (P's scale 1/448), and l sums p' alike
+      const float off = F8 ? LOG2_448 - m_use : -m_use;
+      const float2 neg_m2 = make_float2(off, off);
       float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; i += 2) {
-        const float2 x0 = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), c2, neg_m2);
-        const float2 x1 = __ffma2_rn(make_float2(sv[2 * i + 2], sv[2 * i + 3]), c2, neg_m2);
+        const float2 x0 = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), cj2, neg_m2);
+        const float2 x1 = __ffma2_rn(make_float2(sv[2 * i + 2], sv[2 * i + 3]), cj2, neg_m2);
         const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
         const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
         sum0 = __fadd2_rn(sum0, p0);
         sum1 = __fadd2_rn(sum1, p1);
-        pk[i] = pack_bf16(p0.x, p0.y);
-        pk[i + 1] = pack_bf16(p1.x, p1.y);
+        if (F8) {
+          pk[i >> 1] = pack4_e4m3(p0.x, p0.y, p1.x, p1.y);
+        } else {
+          pk[i] = pack_bf16(p0.x, p0.y);
+          pk[i + 1] = pack_bf16(p1.x, p1.y);
+        }
       }
       l_run = l_run * alpha + ((sum0.x + sum0.y) + (sum1.x + sum1.y));
       tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      if (!F8) tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
@@ -421,7 +456,7 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     ++active;
     if (!__all_sync(0xffffffffu, ok)) return;
     tc_fence_after();
-    const float inv_l = 1.f / l_run;
+    const float inv_l = (F8 ? p.sv[static_cast<int64_t>(b) * s.Hkv + kvh] : 1.f) / l_run;
     const float2 il2 = make_float2(inv_l, inv_l);
     const bool live = q_row < s.Nq;
     const int q0 = qt * TILE + wq * 32;  // this warp's first row
@@ -454,20 +489,22 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
         store_rows32_bf16(rz, scratch, r0 + cc * 32, p.o_res.sn, s.Nq - q0);
       }
     }
-    if (live) p.lse[(static_cast<int64_t>(b) * s.Hq + h) * s.Nq + q_row] = (m_run + __log2f(l_run)) * LN2;
+    if (live)
+      p.lse[(static_cast<int64_t>(b) * s.Hq + h) * s.Nq + q_row] =
+          (m_run + __log2f(l_run) - (F8 ? LOG2_448 : 0.f)) * LN2;
     tc_fence_before();
     warp_arrive(&bar.o_empty[t]);
   }
 }
 
-template <int D, int MASK>
+template <int D, int MASK, bool F8>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, F8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Bars bar = carve_bars<D>(smem);
+  const Bars bar = carve_bars<D, F8>(smem);
   int* unit_slot = reinterpret_cast<int*>(smem + L::OFF_UNIT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
   const int warp = threadIdx.x >> 5;
@@ -502,11 +539,11 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane_id() == 0) fwd_producer<D, MASK>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
+    if (lane_id() == 0) fwd_producer<D, MASK, F8>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
   } else if (warp == 1) {
-    if (lane_id() == 0) fwd_mma<D, MASK>(smem, bar, unit_slot, tmem, p, ctl);
+    if (lane_id() == 0) fwd_mma<D, MASK, F8>(smem, bar, unit_slot, tmem, p, ctl);
   } else if (warp >= 4) {
-    fwd_softmax<D, MASK>((warp - 4) >> 2, bar, unit_slot, tmem, p, ctl,
+    fwd_softmax<D, MASK, F8>((warp - 4) >> 2, bar, unit_slot, tmem, p, ctl,
                            smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES);
   }
   tc_fence_before();
@@ -517,15 +554,20 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, int MASK>
+template <int D, int MASK, bool F8 = false>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
-  using L = FwdLayout<D>;
-  auto kern = fa_fwd_kernel<D, MASK>;
+  using L = FwdLayout<D, F8>;
+  auto kern = fa_fwd_kernel<D, MASK, F8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   FwdParams p;
   p.dims = a.dims;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.sq = a.sq;
+  p.sk = a.sk;
+  p.sv = a.sv;
+  p.nqt = q_tiles(a.dims);
+  p.nkt = k_tiles(a.dims);
   p.o = a.o;
   p.o_res = a.o_res;
   p.lse = a.lse;
@@ -542,6 +584,12 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
   const int m = mask_kind(a.dims);
+  if (a.sq != nullptr) {  // E4M3 operands (d = 128 only)
+    if (a.d != 128) return cudaErrorInvalidValue;
+    return m == MASK_BAND     ? launch_fwd_t<128, MASK_BAND, true>(a, st)
+           : m == MASK_CAUSAL ? launch_fwd_t<128, MASK_CAUSAL, true>(a, st)
+                              : launch_fwd_t<128, MASK_NONE, true>(a, st);
+  }
   if (a.d == 64)
     return m == MASK_BAND ? launch_fwd_t<64, MASK_BAND>(a, st)
            : m == MASK_CAUSAL ? launch_fwd_t<64, MASK_CAUSAL>(a, st) : launch_fwd_t<64, MASK_NONE>(a, st);

@@ -26,6 +26,12 @@ struct FwdLaunch {
   int* counter;
   unsigned long long timeout_ns;
   int num_sms;
+  // E4M3 operands (sq != nullptr; maps over one-byte codes, box 128 x 1 x 128 x 1):
+  // Q block scales [B, Hq, ceil(Nq/128)], K block scales [B, Hkv, ceil(Nk/128)],
+  // V scales [B, Hkv]
+  const float* sq;
+  const float* sk;
+  const float* sv;
 };
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
 
@@ -70,6 +76,20 @@ struct DecodeLaunch {
   int page_size;           // 16, 32, 64, or a multiple of 128
 };
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t st);
+
+struct QuantLaunch {       // E4M3 codes of a bf16 [B, N, H, d] tensor
+  const void* x;
+  int64_t sb, sn, sh;      // x strides (elements)
+  int B, N, H, d;
+  const float* signs;      // d signs of the Hadamard rotation, or nullptr
+  void* out;               // uint8 [B, N, H, d]
+  int64_t ob, on, oh;      // out strides (bytes)
+  float* scales;           // per_block: [B, H, nblk]; else [B, H]
+  unsigned* head_amax;     // per-head pass: [B, H] zeroed workspace
+  int nblk;                // ceil(N / 128)
+  int per_block;
+};
+cudaError_t launch_quantize(const QuantLaunch& a, cudaStream_t st);
 
 cudaError_t launch_selftest_mma(int mode, int n_or_k, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                 const void* a_rows, float* c, int* status, cudaStream_t st);

@@ -110,6 +110,39 @@ int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
            void* stream);
 
 /* ---------------------------------------------------------------------------
+ * FP8 forward ("第18章" §18.6.2; lecture notes slide 24).
+ *
+ * fa_quantize_fp8: E4M3 codes of a bf16 tensor x [B, N, H, d] (d = 64 or 128),
+ * X_fp8 = E4M3(X / s), s = max|X| / 448 (round to nearest even, saturating
+ * at 448).  block_rows = 128: one scale per 128 rows of one head (the load
+ * block of the forward; use for Q and K), scales [B, H, ceil(N/128)] fp32;
+ * block_rows = 0: one scale per (batch, head), scales [B, H] (use for V).
+ * signs: NULL, or d device floats (+1 / -1): the rows are first rotated by
+ * J = diag(signs) H_d / sqrt(d) (H_d the Sylvester Hadamard matrix), which
+ * leaves Q K^T unchanged when Q and K get the same signs and spreads outlier
+ * channels; the scale then includes 1 / sqrt(d).  Codes come from the
+ * unnormalised transform y: inv = 448 / max|y|, code = E4M3(y * inv), each an
+ * IEEE round-to-nearest fp32 operation; an all-zero block gets scale 0.
+ *   out [B, N, H, d] uint8 out (strides multiples of 16 bytes)
+ * Needs fa_quantize_fp8_workspace_size(B, H) bytes of workspace.
+ *
+ * fa_fwd_fp8: the forward of fa_fwd on E4M3 operands (d = 128 only): q8, k8
+ * and v8 [.., d] uint8 codes from fa_quantize_fp8 (Q and K per block with the
+ * same signs or none, V per head, unrotated), q_scale [B, Hq, ceil(Nq/128)],
+ * k_scale [B, Hkv, ceil(Nk/128)], v_scale [B, Hkv] (device fp32).  S = Q K^T
+ * on E4M3 tensor-core products with fp32 accumulation, times s_q s_k and the
+ * shape's scale; softmax in fp32; P enters P V as E4M3(448 P) (P <= 1 fixes
+ * its scale at 1/448); O = (sum E4M3(448 P) V_codes) * s_v / l -> bf16; lse as
+ * in fa_fwd.  Causal and sliding windows as in fa_fwd.  Workspace as fa_fwd.
+ * ------------------------------------------------------------------------- */
+size_t fa_quantize_fp8_workspace_size(int B, int H);
+int fa_quantize_fp8(const fa_tensor_t* x, int B, int N, int H, int d, int block_rows, const float* signs,
+                    const fa_tensor_t* out, float* scales, void* workspace, size_t workspace_bytes, void* stream);
+int fa_fwd_fp8(const fa_tensor_t* q8, const fa_tensor_t* k8, const fa_tensor_t* v8, const float* q_scale,
+               const float* k_scale, const float* v_scale, const fa_tensor_t* o, float* lse, const fa_shape_t* shape,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Backward.  §18.4.4: P rebuilt per tile from the saved statistics with no
  * rescaling, dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = scale dS K,
  * dK = scale dS^T Q; Fig. 18-17 (dependency chain).  D_i is the full-row
@@ -268,7 +301,10 @@ int fa_decode_split_range(const fa_shape_t* shape, int num_splits, int s, int* s
  *   mode 0: c[128 x 128] = a[128 x k] * b[128 x k]^T   (both K-major, k = 64|128)
  *   mode 1: c[128 x n]   = a[128 x 128] * b[128 x n]   (a staged in TMEM,
  *                                                       b row-major, n = 64|128)
- * a, b: device bf16, row-major; c: device fp32 row-major.
+ *   modes 2, 3: the forms of modes 0 and 1 with E4M3 operands (one-byte codes,
+ *           k = n = 128), as the FP8 forward uses them.
+ * a, b: device bf16 (modes 0, 1) or E4M3 codes (modes 2, 3), row-major;
+ * c: device fp32 row-major.
  * workspace: at least 256 bytes of device memory (its first word records a
  * timed-out wait, as for the attention calls).
  */

@@ -175,6 +175,31 @@ def test_paged_decode_arguments_rejected_before_any_gpu_work(lib, page_size, max
     assert rc == 1  # FA_ERR_INVALID
 
 
+def test_fp8_arguments_rejected_before_any_gpu_work(lib):
+    s128 = ctypes.byref(shape(1, 2, 2, 256, 256, 128))
+    s64 = ctypes.byref(shape(1, 2, 2, 256, 256, 64))
+    u8 = lambda ptr=FAKE, sn=256: tens(ptr, sb=256 * 256, sn=sn, sh=128)  # noqa: E731
+
+    def fwd8(q=None, s=s128, qs=FAKE, ws_bytes=1 << 20):
+        return lib.fa_fwd_fp8(q or u8(), u8(), u8(), qs, FAKE, FAKE, tens(), FAKE, s, FAKE, ws_bytes, None)
+    assert fwd8(s=s64) == 1                    # d = 128 only
+    assert fwd8(q=u8(sn=264)) == 2             # code rows must be 16-byte multiples
+    assert fwd8(q=u8(FAKE + 8)) == 2
+    assert fwd8(qs=None) == 1
+    assert fwd8(ws_bytes=8) == 3
+
+    def quant(d=128, rows=128, out=None, scales=FAKE, ws_bytes=1 << 20, x=None):
+        return lib.fa_quantize_fp8(x or tens(), 1, 256, 2, d, rows, None, out or u8(), scales, FAKE, ws_bytes, None)
+    assert quant(d=96) == 1
+    assert quant(rows=64) == 1
+    assert quant(scales=None) == 1
+    assert quant(out=u8(sn=136)) == 2
+    assert quant(x=tens(FAKE + 2)) == 2
+    assert quant(ws_bytes=16) == 3
+    assert lib.fa_quantize_fp8_workspace_size(2, 3) >= 256 + 2 * 3 * 4
+    assert lib.fa_quantize_fp8_workspace_size(0, 3) == 0
+
+
 def test_workspace_sizes(lib):
     s = S(2, 16, 16, 4096, 4096, causal=True)
     assert lib.fa_fwd_workspace_size(s) >= 256

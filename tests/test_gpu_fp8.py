@@ -1,0 +1,169 @@
+"""GPU parity of the FP8 path against the oracle: the tensor-core building
+blocks with E4M3 operands, the quantiser (codes bit-exact), and the FP8 forward."""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_21_gb300 as fa
+from exact_io_aware_21_gb300 import inputs
+from oracle import attention as A
+from oracle import fp8 as F
+from parity import assert_fwd, rel_fro
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fa.library().fa_set_wait_timeout_ns(10_000_000_000)
+
+
+def status_ok(ws):
+    rc, st = fa.binding.device_status(ws)
+    assert rc == 0 and st == 0, f"device status {st:#x}"
+
+
+def codes(shape, seed, max_exp=12):
+    """Random finite E4M3 codes with exponent field at most max_exp."""
+    g = np.random.default_rng(seed)
+    c = g.integers(0, 256, shape).astype(np.uint8)
+    e = (c >> 3) & 15
+    c = np.where(e > max_exp, (c & 0x87) | (max_exp << 3), c).astype(np.uint8)
+    return c
+
+
+# ------------------------------------------------------------------ building blocks
+def run_selftest(mode, a, b):
+    c = torch.zeros(128, 128, dtype=torch.float32, device=DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    da, db = torch.from_numpy(a).to(DEV), torch.from_numpy(b).to(DEV)
+    fa.binding.check(fa.library().fa_selftest_mma(mode, 128, da.data_ptr(), db.data_ptr(), c.data_ptr(),
+                                                  ws.data_ptr(), None))
+    torch.cuda.synchronize()
+    status_ok(ws)
+    return c.cpu().double().numpy()
+
+
+def test_selftest_e4m3_qk_form():
+    a, b = codes((128, 128), 1), codes((128, 128), 2)
+    ref = F.e4m3_decode(a) @ F.e4m3_decode(b).T
+    np.testing.assert_allclose(run_selftest(2, a, b), ref, rtol=1e-5, atol=1e-5 * np.abs(ref).max())
+
+
+def test_selftest_e4m3_pv_form():
+    a, b = codes((128, 128), 3), codes((128, 128), 4)
+    ref = F.e4m3_decode(a) @ F.e4m3_decode(b)
+    np.testing.assert_allclose(run_selftest(3, a, b), ref, rtol=1e-5, atol=1e-5 * np.abs(ref).max())
+
+
+# ------------------------------------------------------------------ quantiser
+
+def signs_for(d, use):
+    return inputs.hadamard_signs(d, seed=d).to(DEV) if use else None
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("block_rows", [128, 0])
+@pytest.mark.parametrize("had", [False, True])
+def test_quantize_codes_and_scales_bit_exact(d, block_rows, had):
+    B, N, H = 2, 300, 3                                        # three row blocks, the last ragged
+    x = inputs.shape_inputs(B, H, H, N, N, d, seed=7 + d, with_do=False)["q"]
+    x = x * torch.tensor([0.01, 1.0, 30.0]).view(1, 1, H, 1).to(torch.bfloat16)   # one scale range per head
+    x[1, 128:256, 0] = 0                                       # an all-zero block
+    sg = signs_for(d, had)
+    codes, sc = fa.quantize_fp8(x.to(DEV), block_rows, sg)
+    torch.cuda.synchronize()
+    ref_codes, ref_sc = F.quantize(x.float().numpy(), block_rows, None if sg is None else sg.cpu().numpy())
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
+    assert np.array_equal(sc.cpu().numpy(), ref_sc)
+
+
+def test_quantize_strided_views():
+    x = inputs.shape_inputs(1, 4, 4, 256, 256, 128, seed=3, with_do=False)["q"].to(DEV)
+    xv = x[:, :, 1:3]                                          # a head slice: strided rows
+    out = torch.zeros((1, 256, 4, 128), dtype=torch.uint8, device=DEV)[:, :, 1:3]
+    sc = torch.empty((1, 2, 2), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(fa.library().fa_quantize_fp8_workspace_size(1, 2), dtype=torch.uint8, device=DEV)
+    fa.fa_quantize_fp8(xv, 128, None, out, sc, ws)
+    torch.cuda.synchronize()
+    ref_codes, ref_sc = F.quantize(xv.cpu().float().numpy(), 128)
+    assert np.array_equal(out.cpu().numpy(), ref_codes) and np.array_equal(sc.cpu().numpy(), ref_sc)
+
+
+# ------------------------------------------------------------------ forward
+def fp8_inputs(B, Hq, Hkv, N, seed, had, outliers=False):
+    w = inputs.Workload("t", B, Hq, Hkv, N, N, 128, False, outliers=outliers, seed=seed)
+    x = inputs.make(w, with_do=False)
+    sg = signs_for(128, had)
+    q8, sq = fa.quantize_fp8(x["q"].to(DEV), 128, sg)
+    k8, sk = fa.quantize_fp8(x["k"].to(DEV), 128, sg)
+    v8, sv = fa.quantize_fp8(x["v"].to(DEV), 0, None)
+    return x, (q8, k8, v8, sq, sk, sv)
+
+
+def cpu(t):
+    return t.cpu().numpy()
+
+
+CASES = [  # B, Hq, Hkv, N, causal, window, Hadamard
+    (1, 2, 1, 300, False, None, False),
+    (2, 4, 2, 512, True, None, False),
+    (1, 4, 4, 384, False, (100, 20), True),
+    (1, 8, 2, 1024, True, None, True),
+    (1, 2, 2, 200, True, (64, 0), False),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,causal,window,had", CASES)
+def test_forward_fp8_matches_oracle(B, Hq, Hkv, N, causal, window, had):
+    x, (q8, k8, v8, sq, sk, sv) = fp8_inputs(B, Hq, Hkv, N, seed=N + Hq, had=had)
+    scale = 1 / np.sqrt(128)
+    o, lse = fa.forward_fp8(q8, k8, v8, sq, sk, sv, causal=causal, scale=scale, window=window)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = F.attention_forward_fp8(cpu(q8), cpu(k8), cpu(v8), cpu(sq), cpu(sk), cpu(sv), scale, causal,
+                                             window)
+    tag = f"fp8 {B}x{Hq}/{Hkv}x{N} causal={causal} window={window} hadamard={had}"
+    assert_fwd(o, lse, o_ref, lse_ref, tag)
+    # and the whole FP8 scheme against exact attention on these N(0,1) inputs
+    o_ex, _ = A.attention_forward(x["q"], x["k"], x["v"], scale, causal, window=window)
+    assert rel_fro(o, o_ex) < 0.08, tag
+
+
+def test_forward_fp8_zero_blocks():
+    """An all-zero Q block and an all-zero K block (scale 0): S = 0 there, no NaN."""
+    B, H, N = 1, 2, 384
+    x = inputs.shape_inputs(B, H, H, N, N, 128, seed=5, with_do=False)
+    x["q"][0, 128:256, 0] = 0
+    x["k"][0, 256:384, 1] = 0
+    q8, sq = fa.quantize_fp8(x["q"].to(DEV), 128)
+    k8, sk = fa.quantize_fp8(x["k"].to(DEV), 128)
+    v8, sv = fa.quantize_fp8(x["v"].to(DEV), 0)
+    for causal in (False, True):
+        o, lse = fa.forward_fp8(q8, k8, v8, sq, sk, sv, causal=causal)
+        torch.cuda.synchronize()
+        o_ref, lse_ref = F.attention_forward_fp8(cpu(q8), cpu(k8), cpu(v8), cpu(sq), cpu(sk), cpu(sv),
+                                                 1 / np.sqrt(128), causal)
+        assert_fwd(o, lse, o_ref, lse_ref, f"zero blocks causal={causal}")
+
+
+@pytest.mark.slow
+def test_forward_fp8_full_size_sampled():
+    """The benchmark's FP8 leg: GQA causal N = 8192 with the outlier channel,
+    Hadamard rotation on; oracle on sampled query blocks of a few heads."""
+    w = inputs.GQA_N8192_D128
+    x = inputs.make(w, device=DEV, with_do=False)
+    sg = signs_for(128, True)
+    q8, sq = fa.quantize_fp8(x["q"], 128, sg)
+    k8, sk = fa.quantize_fp8(x["k"], 128, sg)
+    v8, sv = fa.quantize_fp8(x["v"], 0, None)
+    o, lse = fa.forward_fp8(q8, k8, v8, sq, sk, sv, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    heads = [(0, 0), (0, 13), (0, 31)]
+    blocks = [0, 31, 63]
+    o_ref, lse_ref = F.attention_forward_fp8(cpu(q8), cpu(k8), cpu(v8), cpu(sq), cpu(sk), cpu(sv), w.scale, True,
+                                             heads=heads, q_blocks=blocks)
+    rows = np.concatenate([np.arange(b * 128, (b + 1) * 128) for b in blocks])
+    for b, h in heads:
+        assert_fwd(o[b, rows, h], lse[b, h, rows], o_ref[b, rows, h], lse_ref[b, h, rows], f"fp8 full h{h}")

@@ -11,10 +11,15 @@ in HBM:
                  q1 cache in shuffled pages of 16 keys through fa_decode_paged
   window leg     forward + backward of window_causal_b1_hq32_hkv8_n16384_w4096_d128
                  (each query sees itself and the 4095 keys before it)
+  fp8 leg        E4M3 quantisation (Q, K per 128-row block after the random
+                 Hadamard rotation, V per head) and the FP8 forward of the GQA
+                 workload
 ``value`` = counted forward + backward FLOPs of the training legs divided by
 their device time (TFLOPS; forward 4*B*H*Nq*Nk*d, halved when causal, backward
 2.5x that).  The window leg is reported beside it with its FLOPs counted over
-the (query, key) pairs inside the window.  Decode legs report KV-read GB/s.  L2
+the (query, key) pairs inside the window, and the FP8 leg with the forward's
+count (its roofline is FP8's: twice the measured bf16 peak, the nominal ratio of
+the two tensor rates).  Decode legs report KV-read GB/s.  L2
 is flushed (256 MiB write) before every launch group, outside its events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -46,8 +51,12 @@ DECODE = ("decode_b8_hq32_hkv8_q1_kv131072_d128", "decode_b8_hq32_hkv8_q4_kv1310
 PAGED = ("decode_b8_hq32_hkv8_q1_kv131072_d128", 16)  # the q1 decode cache in shuffled pages of 16 keys
 PAGED_NAME = PAGED[0] + "_paged16"
 WINDOW = ("window_causal_b1_hq32_hkv8_n16384_w4096_d128",)
+FP8 = "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers"  # the FP8 leg runs this workload
+FP8_NAME = FP8 + "_fp8_hadamard"
+FP8_TENSOR_RATIO = 2.0  # nominal dense E4M3 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 WORKLOAD = (" + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode); " + PAGED_NAME +
-            " (paged decode); " + " + ".join(WINDOW) + " (sliding-window fwd+bwd)")
+            " (paged decode); " + " + ".join(WINDOW) + " (sliding-window fwd+bwd); " + FP8_NAME +
+            " (FP8 quantise + fwd)")
 METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -278,7 +287,8 @@ class Leg:
         self.ms = {k: 0.0 for k, _ in fns}
 
 
-KERNELS_PER_CALL = {"fwd": 1, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2}
+KERNELS_PER_CALL = {"fwd": 1, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
+                    "quant_v": 2, "fwd_fp8": 1}
 
 
 def kernel_flops(part, w):
@@ -345,6 +355,30 @@ def make_legs(device, seed):
                               st["s"], st["S"], st["ws"])
 
         legs.append(Leg(name, "decode", w, [("decode", paged_fn if paged else dec_fn)], kv_bytes(w)))
+
+    w = {x.name: x for x in train}[FP8]
+    x = inputs.make(w, device=device, with_do=False, seed=w.seed + seed)
+    signs = inputs.hadamard_signs(w.d, seed=w.d).to(device)
+    s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal)
+    nqt, nkt = -(-w.Nq // 128), -(-w.Nk // 128)
+    st = dict(x=x, s=s, signs=signs, o=torch.empty_like(x["q"]),
+              lse=torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=device),
+              q8=torch.empty(x["q"].shape, dtype=torch.uint8, device=device),
+              k8=torch.empty(x["k"].shape, dtype=torch.uint8, device=device),
+              v8=torch.empty(x["v"].shape, dtype=torch.uint8, device=device),
+              sq=torch.empty((w.B, w.Hq, nqt), dtype=torch.float32, device=device),
+              sk=torch.empty((w.B, w.Hkv, nkt), dtype=torch.float32, device=device),
+              sv=torch.empty((w.B, w.Hkv), dtype=torch.float32, device=device),
+              wsq=torch.zeros(lib.fa_quantize_fp8_workspace_size(w.B, w.Hq), dtype=torch.uint8, device=device),
+              wsk=torch.zeros(lib.fa_quantize_fp8_workspace_size(w.B, w.Hkv), dtype=torch.uint8, device=device),
+              wsf=torch.zeros(lib.fa_fwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=device))
+    state[FP8_NAME] = st
+    fns = [("quant_q", lambda st=st: B.fa_quantize_fp8(st["x"]["q"], 128, st["signs"], st["q8"], st["sq"], st["wsq"])),
+           ("quant_k", lambda st=st: B.fa_quantize_fp8(st["x"]["k"], 128, st["signs"], st["k8"], st["sk"], st["wsk"])),
+           ("quant_v", lambda st=st: B.fa_quantize_fp8(st["x"]["v"], 0, None, st["v8"], st["sv"], st["wsk"])),
+           ("fwd_fp8", lambda st=st: B.fa_fwd_fp8(st["q8"], st["k8"], st["v8"], st["sq"], st["sk"], st["sv"], st["o"],
+                                                  st["lse"], st["s"], st["wsf"]))]
+    legs.append(Leg(FP8_NAME, "fp8", w, fns, fwd_flops(w)))
     return legs, state
 
 
@@ -493,7 +527,7 @@ def run_ours(args):
     leg_ms = {l.name: sum(l.ms.values()) for l in legs}
     # the step is the training and decode legs; the window leg is timed in the same
     # loop and reported beside them
-    step_legs = [l for l in legs if l.kind != "window"]
+    step_legs = [l for l in legs if l.kind in ("train", "decode")]
     step_ms = sum(leg_ms[l.name] for l in step_legs)
     train_ms = sum(leg_ms[l.name] for l in legs if l.kind == "train")
     max_train_ms, total_flops = aggregate(train_ms, sum(l.work for l in legs if l.kind == "train"), world)
@@ -514,6 +548,20 @@ def run_ours(args):
             if l.kind == "window":
                 legs_out[l.name].update({"window": list(l.w.window), "in_step": False,
                                          "flops_count": "4*B*H*d per visible (query, key) pair, x3.5 fwd+bwd"})
+        elif l.kind == "fp8":
+            f = fwd_flops(l.w)
+            qb = {"quant_q": (l.w.Hq, l.w.Nq), "quant_k": (l.w.Hkv, l.w.Nk), "quant_v": (l.w.Hkv, l.w.Nk)}
+            # quantiser traffic: bf16 in, one-byte codes out (V's per-head scale reads its rows twice)
+            qbytes = {k: l.w.B * n * h * l.w.d * (5 if k == "quant_v" else 3) for k, (h, n) in qb.items()}
+            fp8_peak = FP8_TENSOR_RATIO * sus
+            legs_out[l.name] = {
+                "fwd_ms": l.ms["fwd_fp8"], "fwd_tflops": f / l.ms["fwd_fp8"] / 1e9,
+                "fwd_frac_of_fp8_peak": f / l.ms["fwd_fp8"] / 1e9 / fp8_peak,
+                "fp8_peak_tflops": fp8_peak, "fp8_peak_source": "2 x measured sustained bf16 (nominal E4M3/BF16 ratio)",
+                "quant_ms": {k: l.ms[k] for k in qb},
+                "quant_gbs": {k: qbytes[k] / l.ms[k] / 1e6 for k in qb},
+                "fwd_plus_quant_tflops": f / sum(l.ms.values()) / 1e9,
+                "hadamard": True, "in_step": False}
         else:
             ms = l.ms["decode"]
             legs_out[l.name] = {"ms": ms, "gbs": l.work / ms / 1e6, "frac_of_hbm_peak": l.work / ms / 1e6 /
@@ -576,15 +624,27 @@ def run_ours(args):
 
 
 def profile_case(name):
-    """Two forward + backward passes of one named workload through the public API.
+    """Two forward + backward passes of one named workload through the public API
+    (a name ending in ``_fp8``: two quantise + FP8 forward passes instead).
 
     A short, fixed program for ncu captures (the first pass warms up; capture the
     second with ``-s``).  Prints nothing but "ok"."""
     import exact_io_aware_21_gb300 as fa
     from exact_io_aware_21_gb300 import inputs
 
-    w = {x.name: x for x in inputs.ALL}[name]
-    x = inputs.make(w, device="cuda")
+    fp8 = name.endswith("_fp8")
+    w = {x.name: x for x in inputs.ALL}[name[:-4] if fp8 else name]
+    x = inputs.make(w, device="cuda", with_do=not fp8)
+    if fp8:  # quantise (Hadamard on Q and K) and run the FP8 forward, twice
+        sg = inputs.hadamard_signs(w.d, seed=w.d).cuda()
+        for _ in range(2):
+            q8, sq = fa.quantize_fp8(x["q"], 128, sg)
+            k8, sk = fa.quantize_fp8(x["k"], 128, sg)
+            v8, sv = fa.quantize_fp8(x["v"], 0, None)
+            fa.forward_fp8(q8, k8, v8, sq, sk, sv, causal=w.causal, scale=w.scale, window=w.window)
+        torch.cuda.synchronize()
+        print("ok")
+        return 0
     for _ in range(2):
         o, lse, res = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, residual=True,
                                  window=w.window)

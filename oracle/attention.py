@@ -28,6 +28,11 @@ Definitions followed (one bullet per function below):
     (``window_size=(left, right)`` of flash_attn_func, §18.7.1; local attention,
     §18.8.1), a negative bound meaning unbounded; with causal, j <= i as well.
     Like causal it is defined here for Nq == Nk (top-left aligned).
+  * packed variable-length sequences (``flash_attn_varlen_func``, §18.7.1):
+    Q [total_q, Hq, d] and K, V [total_k, Hkv, d] hold the sequences one after
+    another; sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1 and attends
+    only within itself (no attention across sequence boundaries; causal is
+    applied with the sequence's own positions).  LSE is [Hq, total_q].
   * paged, variable-length decode: a sequence's logical KV row r lives in the
     physical page block_table[b, r // page_size], at row r % page_size
     (PagedAttention's page table, §18.8.2 part 3 and §18.8.3); each sequence
@@ -302,6 +307,47 @@ def decode_combine(m, l, Ot):
     den = np.sum(l * w, axis=-1)
     O = np.sum(Ot * w[..., None], axis=-2) / den[..., None]
     return O, mg + np.log(den)
+
+
+def _seq_bounds(cu):
+    cu = np.asarray(cu, dtype=np.int64)
+    if cu[0] != 0 or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must start at 0 and be non-decreasing")
+    return cu
+
+
+def attention_varlen_forward(q, k, v, cu_q, cu_k, scale, causal=False):
+    """Packed variable-length forward: each sequence is plain attention over its own
+    rows.  q [total_q, Hq, d], k/v [total_k, Hkv, d]; returns (O [total_q, Hq, d],
+    LSE [Hq, total_q]).  Causal needs equal query and key lengths per sequence."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cq, ck = _seq_bounds(cu_q), _seq_bounds(cu_k)
+    O = np.zeros(q.shape)
+    LSE = np.zeros((q.shape[1], q.shape[0]))
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0:
+            continue
+        if k1 == k0:
+            raise ValueError("a sequence with queries but no keys has no attention")
+        Ob, Lb = attention_forward(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], scale, causal)
+        O[q0:q1], LSE[:, q0:q1] = Ob[0], Lb[0]
+    return O, LSE
+
+
+def attention_varlen_backward(q, k, v, do, cu_q, cu_k, scale, causal=False):
+    """Gradients (dQ, dK, dV) of the packed forward, sequence by sequence; keys of a
+    sequence with no queries get zero gradients."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    cq, ck = _seq_bounds(cu_q), _seq_bounds(cu_k)
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if q1 == q0 or k1 == k0:
+            continue
+        g = attention_backward(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], do[None, q0:q1], scale, causal)
+        dq[q0:q1], dk[k0:k1], dv[k0:k1] = g[0][0], g[1][0], g[2][0]
+    return dq, dk, dv
 
 
 def gather_paged(cache, block_table, b, length):

@@ -11,6 +11,9 @@ in HBM:
                  q1 cache in shuffled pages of 16 keys through fa_decode_paged
   window leg     forward + backward of window_causal_b1_hq32_hkv8_n16384_w4096_d128
                  (each query sees itself and the 4095 keys before it)
+  varlen leg     forward + backward of 24 packed sequences of long-tailed
+                 lengths (32768 tokens, GQA 32/8, d=128, causal) through
+                 fa_fwd_varlen / fa_bwd_varlen
   fp8 leg        E4M3 quantisation (Q, K per 128-row block after the random
                  Hadamard rotation, V per head) and the FP8 forward of the GQA
                  workload
@@ -32,6 +35,7 @@ this host's cores on a bounded sample of the same workloads.
 """
 
 import argparse
+import itertools
 import json
 import os
 import statistics
@@ -51,12 +55,13 @@ DECODE = ("decode_b8_hq32_hkv8_q1_kv131072_d128", "decode_b8_hq32_hkv8_q4_kv1310
 PAGED = ("decode_b8_hq32_hkv8_q1_kv131072_d128", 16)  # the q1 decode cache in shuffled pages of 16 keys
 PAGED_NAME = PAGED[0] + "_paged16"
 WINDOW = ("window_causal_b1_hq32_hkv8_n16384_w4096_d128",)
+VARLEN = "varlen_causal_b24_hq32_hkv8_total32768_d128"
 FP8 = "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers"  # the FP8 leg runs this workload
 FP8_NAME = FP8 + "_fp8_hadamard"
 FP8_TENSOR_RATIO = 2.0  # nominal dense E4M3 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 WORKLOAD = (" + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode); " + PAGED_NAME +
-            " (paged decode); " + " + ".join(WINDOW) + " (sliding-window fwd+bwd); " + FP8_NAME +
-            " (FP8 quantise + fwd)")
+            " (paged decode); " + " + ".join(WINDOW) + " (sliding-window fwd+bwd); " + VARLEN +
+            " (packed variable-length fwd+bwd); " + FP8_NAME + " (FP8 quantise + fwd)")
 METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -83,7 +88,16 @@ def window_pairs(w):
     return n
 
 
+def varlen_lens(w):
+    from exact_io_aware_21_gb300 import inputs
+
+    return inputs.varlen_lengths(w.extra["n_seqs"], w.Nq, seed=w.seed)
+
+
 def fwd_flops(w):
+    if "n_seqs" in w.extra:  # packed sequences: each its own (causal) attention
+        f = sum(4.0 * w.Hq * n * n * w.d for n in varlen_lens(w))
+        return f / 2 if w.causal else f
     if w.window is not None:
         return 4.0 * w.B * w.Hq * w.d * window_pairs(w)
     f = 4.0 * w.B * w.Hq * w.Nq * w.Nk * w.d
@@ -288,7 +302,7 @@ class Leg:
 
 
 KERNELS_PER_CALL = {"fwd": 1, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
-                    "quant_v": 2, "fwd_fp8": 1}
+                    "quant_v": 2, "fwd_fp8": 1, "fwd_varlen": 1, "bwd_varlen": 3}
 
 
 def kernel_flops(part, w):
@@ -355,6 +369,33 @@ def make_legs(device, seed):
                               st["s"], st["S"], st["ws"])
 
         legs.append(Leg(name, "decode", w, [("decode", paged_fn if paged else dec_fn)], kv_bytes(w)))
+
+    by = {x.name: x for x in inputs.ALL}
+    w = by[VARLEN]
+    lens = varlen_lens(w)
+    x = inputs.make(w, device=device, seed=w.seed + seed)
+    packed = {k: x[k][0] for k in ("q", "k", "v", "do")}          # [total, H, d]
+    cu = torch.tensor([0] + list(itertools.accumulate(lens)), dtype=torch.int32, device=device)
+    s = B._varlen_shape(packed["q"], packed["k"], cu, w.scale, w.causal)
+    st = dict(x=packed, cu=cu, s=s, mx=max(lens), o=torch.empty_like(packed["q"]), ores=torch.empty_like(packed["q"]),
+              lse=torch.empty((w.Hq, w.Nq), dtype=torch.float32, device=device),
+              dq=torch.empty_like(packed["q"]), dk=torch.empty_like(packed["k"]), dv=torch.empty_like(packed["v"]),
+              wsf=torch.zeros(lib.fa_fwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=device),
+              wsb=torch.zeros(lib.fa_bwd_varlen_workspace_size(ctypes.byref(s), max(lens)), dtype=torch.uint8,
+                              device=device))
+    state[VARLEN] = st
+
+    def vfwd(st=st):
+        x = st["x"]
+        B.fa_fwd_varlen(x["q"], x["k"], x["v"], st["cu"], st["cu"], st["mx"], st["mx"], st["o"], st["lse"], st["s"],
+                        st["wsf"], st["ores"])
+
+    def vbwd(st=st):
+        x = st["x"]
+        B.fa_bwd_varlen(x["q"], x["k"], x["v"], st["cu"], st["cu"], st["mx"], st["mx"], st["o"], st["lse"], x["do"],
+                        st["dq"], st["dk"], st["dv"], st["s"], st["wsb"], st["ores"])
+
+    legs.append(Leg(VARLEN, "varlen", w, [("fwd_varlen", vfwd), ("bwd_varlen", vbwd)], 3.5 * fwd_flops(w)))
 
     w = {x.name: x for x in train}[FP8]
     x = inputs.make(w, device=device, with_do=False, seed=w.seed + seed)
@@ -548,6 +589,15 @@ def run_ours(args):
             if l.kind == "window":
                 legs_out[l.name].update({"window": list(l.w.window), "in_step": False,
                                          "flops_count": "4*B*H*d per visible (query, key) pair, x3.5 fwd+bwd"})
+        elif l.kind == "varlen":
+            f = fwd_flops(l.w)
+            legs_out[l.name] = {
+                "fwd_ms": l.ms["fwd_varlen"], "fwd_tflops": f / l.ms["fwd_varlen"] / 1e9,
+                "fwd_frac_of_sustained_peak": f / l.ms["fwd_varlen"] / 1e9 / sus,
+                "bwd_ms": l.ms["bwd_varlen"], "bwd_tflops": 2.5 * f / l.ms["bwd_varlen"] / 1e9,
+                "bwd_frac_of_sustained_peak": 2.5 * f / l.ms["bwd_varlen"] / 1e9 / sus,
+                "lens": varlen_lens(l.w), "in_step": False,
+                "flops_count": "per sequence 4*H*L^2*d, halved (causal), x3.5 fwd+bwd"}
         elif l.kind == "fp8":
             f = fwd_flops(l.w)
             qb = {"quant_q": (l.w.Hq, l.w.Nq), "quant_k": (l.w.Hkv, l.w.Nk), "quant_v": (l.w.Hkv, l.w.Nk)}

@@ -16,6 +16,10 @@ from .binding import (  # noqa: F401
     fa_quantize_fp8,
     forward,
     forward_fp8,
+    forward_varlen,
+    backward_varlen,
+    fa_fwd_varlen,
+    fa_bwd_varlen,
     quantize_fp8,
     backward,
     decode,

@@ -71,6 +71,9 @@ SIGNATURES = {
     "fa_dq_unit": (_I, [_PS, _I, _PI, _PI, _PI]),
     "fa_decode_split_range": (_I, [_PS, _I, _I, _PI, _PI]),
     "fa_selftest_mma": (_I, [_I, _I, _VP, _VP, _VP, _VP, _VP]),
+    "fa_fwd_varlen": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _I, _PT, _VP, _PT, _PS, _VP, _SZ, _VP]),
+    "fa_bwd_varlen_workspace_size": (_SZ, [_PS, _I]),
+    "fa_bwd_varlen": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _I, _PT, _VP, _PT, _PT, _PT, _PT, _PT, _PS, _VP, _SZ, _VP]),
     "fa_quantize_fp8_workspace_size": (_SZ, [_I, _I]),
     "fa_quantize_fp8": (_I, [_PT, _I, _I, _I, _I, _I, _VP, _PT, _VP, _VP, _SZ, _VP]),
     "fa_fwd_fp8": (_I, [_PT, _PT, _PT, _VP, _VP, _VP, _PT, _VP, _PS, _VP, _SZ, _VP]),
@@ -118,6 +121,19 @@ def tdesc(t):
     if t.dim() != 4 or t.dtype != torch.bfloat16 or not t.is_cuda or t.stride(-1) != 1:
         raise FAError(1, "expected a 4-D bf16 CUDA tensor [B, N, H, d] with unit head-dim stride")
     return FaTensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
+
+
+def tdesc_packed(t):
+    """[total, H, d] bf16 CUDA tensor (packed sequences) -> FaTensor (stride_b unused)."""
+    if t.dim() != 3 or t.dtype != torch.bfloat16 or not t.is_cuda or t.stride(-1) != 1:
+        raise FAError(1, "expected a 3-D bf16 CUDA tensor [total, H, d] with unit head-dim stride")
+    return FaTensor(t.data_ptr(), 0, t.stride(0), t.stride(1))
+
+
+def _cu(t):
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous() or t.dim() != 1:
+        raise FAError(1, "cu_seqlens must be contiguous 1-D int32 CUDA tensors")
+    return t.data_ptr()
 
 
 def tdesc_u8(t):
@@ -174,6 +190,23 @@ def fa_decode_paged(q, kc, vc, block_table, seqlens_k, o, lse, s, num_splits, wo
     check(lib.fa_decode_paged(tdesc(q), tdesc(kc), tdesc(vc), block_table.data_ptr(), block_table.shape[1],
                               seqlens_k.data_ptr(), kc.shape[0], kc.shape[1], tdesc(o), lse.data_ptr(),
                               ctypes.byref(s), int(num_splits), workspace.data_ptr(), workspace.numel(), _stream(q)))
+
+
+def fa_fwd_varlen(q, k, v, cu_q, cu_k, max_q, max_k, o, lse, s, workspace, o_res=None):
+    lib = library()
+    check(lib.fa_fwd_varlen(tdesc_packed(q), tdesc_packed(k), tdesc_packed(v), _cu(cu_q), _cu(cu_k), int(max_q),
+                            int(max_k), tdesc_packed(o), lse.data_ptr(),
+                            None if o_res is None else ctypes.byref(tdesc_packed(o_res)), ctypes.byref(s),
+                            workspace.data_ptr(), workspace.numel(), _stream(q)))
+
+
+def fa_bwd_varlen(q, k, v, cu_q, cu_k, max_q, max_k, o, lse, do, dq, dk, dv, s, workspace, o_res=None):
+    lib = library()
+    check(lib.fa_bwd_varlen(tdesc_packed(q), tdesc_packed(k), tdesc_packed(v), _cu(cu_q), _cu(cu_k), int(max_q),
+                            int(max_k), tdesc_packed(o), lse.data_ptr(),
+                            None if o_res is None else ctypes.byref(tdesc_packed(o_res)), tdesc_packed(do),
+                            tdesc_packed(dq), tdesc_packed(dk), tdesc_packed(dv), ctypes.byref(s),
+                            workspace.data_ptr(), workspace.numel(), _stream(q)))
 
 
 def fa_quantize_fp8(x, block_rows, signs, out, scales, workspace):
@@ -286,3 +319,36 @@ def forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None,
     ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q8.device)
     fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, s, ws)
     return o, lse
+
+
+def _varlen_shape(q, k, cu_q, scale, causal):
+    total_q, Hq, d = q.shape
+    total_k, Hkv, _ = k.shape
+    return shape(cu_q.numel() - 1, Hq, Hkv, total_q, total_k, d, scale, causal)
+
+
+def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False, scale=None,
+                   residual=False):
+    """Packed variable-length forward (see fa_fwd_varlen in include/fa.h): q [total_q, Hq, d],
+    k/v [total_k, Hkv, d] bf16, cu_seqlens int32 [B + 1] on the device.  Returns O, LSE
+    [Hq, total_q] (and O's residual with ``residual=True``)."""
+    s = _varlen_shape(q, k, cu_seqlens_q, scale, causal)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((s.Hq, s.Nq), dtype=torch.float32, device=q.device)
+    res = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
+    ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q.device)
+    fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, o, lse, s, ws, res)
+    return (o, lse, res) if residual else (o, lse)
+
+
+def backward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, o, lse, do, causal=False,
+                    scale=None, o_residual=None):
+    """dQ, dK, dV of the packed forward."""
+    s = _varlen_shape(q, k, cu_seqlens_q, scale, causal)
+    dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device)
+    dv = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device)
+    ws = _ws(library().fa_bwd_varlen_workspace_size(ctypes.byref(s), int(max_seqlen_q)), q.device)
+    fa_bwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, o, lse, do, dq, dk, dv, s, ws,
+                  o_residual)
+    return dq, dk, dv

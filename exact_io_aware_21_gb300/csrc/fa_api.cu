@@ -282,11 +282,51 @@ int fa_get_device_status(void* ws, void* stream, int* status) {
 // ------------------------------------------------------------------------ forward
 size_t fa_fwd_workspace_size(const fa_shape_t* s) { return check_shape(s) == FA_OK ? FA_WS_HEADER_BYTES : 0; }
 
-int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
-           const fa_tensor_t* o_res, const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
+// Packed variable-length sequences: the cu arrays (device) and the longest
+// lengths; shape Nq / Nk are then the packed tensors' token counts.
+struct Packed {
+  const int* cu_q;
+  const int* cu_k;
+  int max_q, max_k;
+};
+
+int check_packed(const fa_shape_t* s, const Packed* pk) {
+  if (!pk) return FA_OK;
+  if (!pk->cu_q || !pk->cu_k || s->window) return FA_ERR_INVALID;
+  if (pk->max_q < 1 || pk->max_q > s->Nq || pk->max_k < 1 || pk->max_k > s->Nk) return FA_ERR_INVALID;
+  return FA_OK;
+}
+
+// Dims of the kernels: dense, or packed (the unit grid sized by the longest sequence).
+Dims kernel_dims(const fa_shape_t* s, const Packed* pk) {
+  Dims d = dims_of(s);
+  if (pk) {
+    d.Nq = pk->max_q;
+    d.Nk = pk->max_k;
+    d.cu_q = pk->cu_q;
+    d.cu_k = pk->cu_k;
+    d.total_q = s->Nq;
+    d.total_k = s->Nk;
+  }
+  return d;
+}
+
+// TMA map over a dense [B, N, H, d] tensor, or a packed [total, H, d] one (B = 1).
+int map_of(CUtensorMap* m, const fa_tensor_t* t, const fa_shape_t* s, int n, int h, const Packed* pk) {
+  if (pk) return make_map(m, t->ptr, 1, n, h, s->d, static_cast<int64_t>(n) * t->stride_n, t->stride_n, t->stride_h);
+  return make_map(m, t->ptr, s->B, n, h, s->d, t->stride_b, t->stride_n, t->stride_h);
+}
+
+OutRows out_rows(const fa_tensor_t* t, const Packed* pk) {
+  return OutRows{t->ptr, pk ? 0 : t->stride_b, t->stride_n, t->stride_h};
+}
+
+int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
+             const fa_tensor_t* o_res, const fa_shape_t* s, const Packed* pk, void* ws, size_t ws_bytes,
+             void* stream) {
   int rc;
-  if ((rc = check_shape(s)) || (rc = check_tensor(q)) || (rc = check_tensor(k)) || (rc = check_tensor(v)) ||
-      (rc = check_tensor(o)) || (o_res && (rc = check_tensor(o_res))))
+  if ((rc = check_shape(s)) || (rc = check_packed(s, pk)) || (rc = check_tensor(q)) || (rc = check_tensor(k)) ||
+      (rc = check_tensor(v)) || (rc = check_tensor(o)) || (o_res && (rc = check_tensor(o_res))))
     return rc;
   if (!lse) return FA_ERR_INVALID;
   if ((rc = check_ws(ws, ws_bytes, fa_fwd_workspace_size(s)))) return rc;
@@ -294,15 +334,14 @@ int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
   if ((rc = device_info(&sms))) return rc;
   FwdLaunch a;
   memset(&a, 0, sizeof(a));
-  a.dims = dims_of(s);
+  a.dims = kernel_dims(s, pk);
   a.d = s->d;
   a.scale = s->scale;
-  if ((rc = make_map(&a.tm_q, q->ptr, s->B, s->Nq, s->Hq, s->d, q->stride_b, q->stride_n, q->stride_h)) ||
-      (rc = make_map(&a.tm_k, k->ptr, s->B, s->Nk, s->Hkv, s->d, k->stride_b, k->stride_n, k->stride_h)) ||
-      (rc = make_map(&a.tm_v, v->ptr, s->B, s->Nk, s->Hkv, s->d, v->stride_b, v->stride_n, v->stride_h)))
+  if ((rc = map_of(&a.tm_q, q, s, s->Nq, s->Hq, pk)) || (rc = map_of(&a.tm_k, k, s, s->Nk, s->Hkv, pk)) ||
+      (rc = map_of(&a.tm_v, v, s, s->Nk, s->Hkv, pk)))
     return rc;
-  a.o = rows_of(o);
-  a.o_res = o_res ? rows_of(o_res) : OutRows{nullptr, 0, 0, 0};
+  a.o = out_rows(o, pk);
+  a.o_res = o_res ? out_rows(o_res, pk) : OutRows{nullptr, 0, 0, 0};
   a.lse = lse;
   a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
   a.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_COUNTER_OFFSET);
@@ -311,6 +350,18 @@ int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
   if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
   cudaError_t e = launch_fwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
+}
+
+int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
+           const fa_tensor_t* o_res, const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
+  return fwd_impl(q, k, v, o, lse, o_res, s, nullptr, ws, ws_bytes, stream);
+}
+
+int fa_fwd_varlen(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k, const fa_tensor_t* o, float* lse,
+                  const fa_tensor_t* o_res, const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
+  const Packed pk{cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k};
+  return fwd_impl(q, k, v, o, lse, o_res, s, &pk, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------------ FP8
@@ -391,44 +442,52 @@ int fa_fwd_fp8(const fa_tensor_t* q8, const fa_tensor_t* k8, const fa_tensor_t* 
 }
 
 // ------------------------------------------------------------------------ backward
+size_t bwd_ws_bytes(const fa_shape_t* s, int nq_rows) {
+  const size_t rows = static_cast<size_t>(s->B) * s->Hq * (cdiv(nq_rows, TILE) * TILE);
+  return FA_WS_HEADER_BYTES + 2 * round_up(rows * sizeof(float), 256);
+}
+
 size_t fa_bwd_workspace_size(const fa_shape_t* s) {
   if (check_shape(s) != FA_OK) return 0;
-  const size_t rows = static_cast<size_t>(s->B) * s->Hq * nq_pad(s);
-  return FA_WS_HEADER_BYTES + 2 * round_up(rows * sizeof(float), 256);
+  return bwd_ws_bytes(s, s->Nq);
+}
+
+size_t fa_bwd_varlen_workspace_size(const fa_shape_t* s, int max_seqlen_q) {
+  if (check_shape(s) != FA_OK || max_seqlen_q < 1 || max_seqlen_q > s->Nq) return 0;
+  return bwd_ws_bytes(s, max_seqlen_q);
 }
 
 static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v,
                     const fa_tensor_t* o, const float* lse, const fa_tensor_t* o_res, const fa_tensor_t* dout,
                     const fa_tensor_t* dq, const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* s,
-                    void* ws, size_t ws_bytes, void* stream) {
+                    const Packed* pk, void* ws, size_t ws_bytes, void* stream) {
   int rc;
-  if ((rc = check_shape(s)) || (rc = check_tensor(q)) || (rc = check_tensor(k)) || (rc = check_tensor(v)) ||
+  if ((rc = check_shape(s)) || (rc = check_packed(s, pk)) || (rc = check_tensor(q)) || (rc = check_tensor(k)) ||
+      (rc = check_tensor(v)) ||
       (rc = check_tensor(o)) || (rc = check_tensor(dout)) || (rc = check_tensor(dq)) || (rc = check_tensor(dk)) ||
       (rc = check_tensor(dv)) || (o_res && (rc = check_tensor(o_res))))
     return rc;
   if (!lse) return FA_ERR_INVALID;
-  if ((rc = check_ws(ws, ws_bytes, fa_bwd_workspace_size(s)))) return rc;
+  const int nq_rows = pk ? pk->max_q : s->Nq;
+  if ((rc = check_ws(ws, ws_bytes, bwd_ws_bytes(s, nq_rows)))) return rc;
   int sms = 0;
   if ((rc = device_info(&sms))) return rc;
   BwdLaunch a;
   memset(&a, 0, sizeof(a));
-  a.dims = dims_of(s);
+  a.dims = kernel_dims(s, pk);
   a.d = s->d;
   a.scale = s->scale;
-  if ((rc = make_map(&a.tm_q, q->ptr, s->B, s->Nq, s->Hq, s->d, q->stride_b, q->stride_n, q->stride_h)) ||
-      (rc = make_map(&a.tm_k, k->ptr, s->B, s->Nk, s->Hkv, s->d, k->stride_b, k->stride_n, k->stride_h)) ||
-      (rc = make_map(&a.tm_v, v->ptr, s->B, s->Nk, s->Hkv, s->d, v->stride_b, v->stride_n, v->stride_h)) ||
-      (rc = make_map(&a.tm_do, dout->ptr, s->B, s->Nq, s->Hq, s->d, dout->stride_b, dout->stride_n,
-                     dout->stride_h)))
+  if ((rc = map_of(&a.tm_q, q, s, s->Nq, s->Hq, pk)) || (rc = map_of(&a.tm_k, k, s, s->Nk, s->Hkv, pk)) ||
+      (rc = map_of(&a.tm_v, v, s, s->Nk, s->Hkv, pk)) || (rc = map_of(&a.tm_do, dout, s, s->Nq, s->Hq, pk)))
     return rc;
-  a.o = rows_of(o);
-  a.o_res = o_res ? rows_of(o_res) : OutRows{nullptr, 0, 0, 0};
-  a.dout = rows_of(dout);
-  a.dq = rows_of(dq);
-  a.dk = rows_of(dk);
-  a.dv = rows_of(dv);
+  a.o = out_rows(o, pk);
+  a.o_res = o_res ? out_rows(o_res, pk) : OutRows{nullptr, 0, 0, 0};
+  a.dout = out_rows(dout, pk);
+  a.dq = out_rows(dq, pk);
+  a.dk = out_rows(dk, pk);
+  a.dv = out_rows(dv, pk);
   a.lse = lse;
-  a.nq_pad = nq_pad(s);
+  a.nq_pad = cdiv(nq_rows, TILE) * TILE;
   const size_t rows = static_cast<size_t>(s->B) * s->Hq * a.nq_pad;
   char* base = static_cast<char*>(ws);
   a.neg_lse2 = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES);
@@ -447,7 +506,16 @@ int fa_bwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
            const float* lse, const fa_tensor_t* o_res, const fa_tensor_t* dout, const fa_tensor_t* dq,
            const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* s, void* ws, size_t ws_bytes,
            void* stream) {
-  return bwd_impl(7, q, k, v, o, lse, o_res, dout, dq, dk, dv, s, ws, ws_bytes, stream);
+  return bwd_impl(7, q, k, v, o, lse, o_res, dout, dq, dk, dv, s, nullptr, ws, ws_bytes, stream);
+}
+
+int fa_bwd_varlen(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k, const fa_tensor_t* o,
+                  const float* lse, const fa_tensor_t* o_res, const fa_tensor_t* dout, const fa_tensor_t* dq,
+                  const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* s, void* ws, size_t ws_bytes,
+                  void* stream) {
+  const Packed pk{cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k};
+  return bwd_impl(7, q, k, v, o, lse, o_res, dout, dq, dk, dv, s, &pk, ws, ws_bytes, stream);
 }
 
 int fa_bwd_part(int part, const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o,
@@ -455,7 +523,7 @@ int fa_bwd_part(int part, const fa_tensor_t* q, const fa_tensor_t* k, const fa_t
                 const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* s, void* ws, size_t ws_bytes,
                 void* stream) {
   if (part < 0 || part > 2) return FA_ERR_INVALID;
-  return bwd_impl(1 << part, q, k, v, o, lse, o_res, dout, dq, dk, dv, s, ws, ws_bytes, stream);
+  return bwd_impl(1 << part, q, k, v, o, lse, o_res, dout, dq, dk, dv, s, nullptr, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------------ decode

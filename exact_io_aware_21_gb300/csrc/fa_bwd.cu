@@ -62,7 +62,7 @@ struct BwdParams {
 
 // ================================================================== preprocess
 // threads per row = D / 8 (one 16-byte chunk of dO and of O each)
-template <int D>
+template <int D, bool VL>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
   constexpr int TPR = D / 8;
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / TPR;
@@ -72,12 +72,15 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   const int q = static_cast<int>(row % p.nq_pad);
   const int bh = static_cast<int>(row / p.nq_pad);
   const int b = bh / p.dims.Hq, h = bh % p.dims.Hq;
+  const SeqRows sr = seq_rows<VL>(p.dims, b);
+  const int nq = sr.s.Nq;                       // this sequence's rows
+  const int64_t qrow = sr.qoff + static_cast<int64_t>(q);
   float acc = 0.f;
-  if (q < p.dims.Nq) {
-    const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.o.ptr) + b * p.o.sb +
-                             static_cast<int64_t>(q) * p.o.sn + h * p.o.sh + part * 8;
+  if (q < nq) {
+    const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.o.ptr) + b * p.o.sb + qrow * p.o.sn +
+                             h * p.o.sh + part * 8;
     const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout.ptr) + b * p.dout.sb +
-                             static_cast<int64_t>(q) * p.dout.sn + h * p.dout.sh + part * 8;
+                             qrow * p.dout.sn + h * p.dout.sh + part * 8;
     const uint4 ov = *reinterpret_cast<const uint4*>(o);
     const uint4 gv = *reinterpret_cast<const uint4*>(g);
     const uint32_t* ou = reinterpret_cast<const uint32_t*>(&ov);
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
     }
     if (p.o_res.ptr != nullptr) {  // D = dO . (O + residual)
       const __nv_bfloat16* rr = reinterpret_cast<const __nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
-                                static_cast<int64_t>(q) * p.o_res.sn + h * p.o_res.sh + part * 8;
+                                qrow * p.o_res.sn + h * p.o_res.sh + part * 8;
       const uint4 rv = *reinterpret_cast<const uint4*>(rr);
       const uint32_t* ru = reinterpret_cast<const uint32_t*>(&rv);
 #pragma unroll
@@ -105,7 +108,10 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
   if (part == 0) {
     p.neg_delta[row] = -acc;
-    p.neg_lse2[row] = q < p.dims.Nq ? -p.lse[static_cast<int64_t>(bh) * p.dims.Nq + q] * LOG2E : -INFINITY;
+    // LSE [B, Hq, Nq], or [Hq, total_q] for packed sequences
+    const int64_t li = VL ? static_cast<int64_t>(h) * p.dims.total_q + qrow
+                                   : static_cast<int64_t>(bh) * p.dims.Nq + q;
+    p.neg_lse2[row] = q < nq ? -p.lse[li] * LOG2E : -INFINITY;
   }
 }
 
@@ -218,6 +224,9 @@ __device__ __forceinline__ DkvBars dkv_bars(uint8_t* smem) {
 
 struct DkvUnit {
   int b, kvh, kt, q0, nqi, n_it;
+  SeqRows sr;  // the unit's sequence (packed sequences: its own lengths and row offsets)
+  bool work;   // the key tile holds keys that some query sees
+  bool zero;   // the key tile holds keys that no query sees: their gradients are 0
 };
 
 // Key tiles visited by query tile qt: a band's range, else a prefix (causal: up
@@ -234,21 +243,26 @@ __device__ __forceinline__ void dq_kv_range(const Dims& s, int qt, int& lo, int&
 
 // The query tiles visiting key tile kt: a band's range, or under j <= i (where
 // Nq == Nk) the suffix from the diagonal tile.
-template <int MASK>
+template <int MASK, bool VL>
 __device__ __forceinline__ DkvUnit dkv_decode(const Dims& s, int u) {
   DkvUnit r;
   dkdv_unit(s, u, r.b, r.kvh, r.kt);
-  int qhi = q_tiles(s);
+  r.sr = seq_rows<VL>(s, r.b);
+  const Dims& su = r.sr.s;
+  int qhi = q_tiles(su);
   if (MASK == MASK_BAND)
-    q_range(s, r.kt, r.q0, qhi);
+    q_range(su, r.kt, r.q0, qhi);
   else
     r.q0 = MASK == MASK_CAUSAL ? r.kt : 0;
-  r.nqi = qhi - r.q0;
+  const bool keys = r.kt < k_tiles(su);
+  r.nqi = keys ? imax(0, qhi - r.q0) : 0;
   r.n_it = (s.Hq / s.Hkv) * r.nqi;
+  r.work = r.n_it > 0;
+  r.zero = keys && !r.work;
   return r;
 }
 
-template <int D, int MASK>
+template <int D, int MASK, bool VL>
 __global__ void __launch_bounds__(384, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -290,7 +304,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     if (lane_id() == 0) {  // ---------------------------------------------- producer
-      uint32_t sq = 0;
+      uint32_t sq = 0, un = 0;  // un: units with work so far (K/V phase)
       int kv_armed = -1;
       for (int it = 0;; ++it) {
         const int slot = it & 1;
@@ -299,14 +313,16 @@ __global__ void __launch_bounds__(384, 1)
         unit_slot[slot] = u;
         mbar_arrive(&bar.unit_full[slot]);
         if (u >= p.total_units) break;
-        const DkvUnit w = dkv_decode<MASK>(s, u);
-        if (!mbar_wait(bar.kv_empty, (it & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
+        const DkvUnit w = dkv_decode<MASK, VL>(s, u);
+        if (!w.work) continue;
+        const int krow = w.sr.koff + w.kt * TILE, tb = w.sr.tb;
+        if (!mbar_wait(bar.kv_empty, (un & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
         mbar_arrive_expect_tx(bar.kv_full, 2 * L::TB);
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(smem + L::OFF_K + c * (TILE * 128), &tm_k, bar.kv_full, c * 64, w.kvh, w.kt * TILE, w.b);
-          tma_load_4d(smem + L::OFF_V + c * (TILE * 128), &tm_v, bar.kv_full, c * 64, w.kvh, w.kt * TILE, w.b);
+          tma_load_4d(smem + L::OFF_K + c * (TILE * 128), &tm_k, bar.kv_full, c * 64, w.kvh, krow, tb);
+          tma_load_4d(smem + L::OFF_V + c * (TILE * 128), &tm_v, bar.kv_full, c * 64, w.kvh, krow, tb);
         }
-        kv_armed = it;
+        kv_armed = static_cast<int>(un++);
         bool ok = true;
         for (int k = 0; k < w.n_it; ++k, ++sq) {
           const int st = sq % L::STAGES;
@@ -319,16 +335,17 @@ __global__ void __launch_bounds__(384, 1)
           const int64_t row0 = (static_cast<int64_t>(w.b) * s.Hq + hq) * p.nq_pad + qi * TILE;
           mbar_arrive_expect_tx(&bar.st_full[st], 2 * L::TB + 1024);
           for (int c = 0; c < D / 64; ++c) {
-            tma_load_4d(base + c * (TILE * 128), &tm_q, &bar.st_full[st], c * 64, hq, qi * TILE, w.b);
-            tma_load_4d(base + L::TB + c * (TILE * 128), &tm_do, &bar.st_full[st], c * 64, hq, qi * TILE, w.b);
+            tma_load_4d(base + c * (TILE * 128), &tm_q, &bar.st_full[st], c * 64, hq, w.sr.qoff + qi * TILE, tb);
+            tma_load_4d(base + L::TB + c * (TILE * 128), &tm_do, &bar.st_full[st], c * 64, hq,
+                        w.sr.qoff + qi * TILE, tb);
           }
           bulk_load(base + 2 * L::TB, p.neg_lse2 + row0, 512, &bar.st_full[st]);
           bulk_load(base + 2 * L::TB + 512, p.neg_delta + row0, 512, &bar.st_full[st]);
           if (k + 1 < w.n_it) {  // the next iteration's Q and dO into L2 while this stage waits its turn
             const int hq1 = w.kvh * g + (k + 1) / w.nqi, qi1 = w.q0 + (k + 1) % w.nqi;
             for (int c = 0; c < D / 64; ++c) {
-              tma_prefetch_l2_4d(&tm_q, c * 64, hq1, qi1 * TILE, w.b);
-              tma_prefetch_l2_4d(&tm_do, c * 64, hq1, qi1 * TILE, w.b);
+              tma_prefetch_l2_4d(&tm_q, c * 64, hq1, w.sr.qoff + qi1 * TILE, tb);
+              tma_prefetch_l2_4d(&tm_do, c * 64, hq1, w.sr.qoff + qi1 * TILE, tb);
             }
           }
         }
@@ -347,15 +364,16 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t kb = smem_u32(smem + L::OFF_K), vb = smem_u32(smem + L::OFF_V);
       const uint32_t stb = smem_u32(smem + L::OFF_ST);
       const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
-      uint32_t sq = 0, pph = 0, dph = 0;
+      uint32_t sq = 0, pph = 0, dph = 0, un = 0;
       for (int it = 0;; ++it) {
         const int slot = it & 1;
         if (!mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
         const int u = unit_slot[slot];
         mbar_arrive(&bar.unit_empty[slot]);
         if (u >= p.total_units) break;
-        const DkvUnit w = dkv_decode<MASK>(s, u);
-        if (!mbar_wait(bar.kv_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA)) break;
+        const DkvUnit w = dkv_decode<MASK, VL>(s, u);
+        if (!w.work) continue;
+        if (!mbar_wait(bar.kv_full, (un++) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) break;
         bool ok = mbar_wait(&bar.st_full[sq % L::STAGES], (sq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
         if (!ok) break;
         tc_fence_after();
@@ -420,7 +438,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + lanes, tP = tmem + lanes + 128, tdV = tmem + lanes + 256,
                    tdK = tmem + lanes + 256 + D;
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-    uint32_t sq = 0, sph = 0, dph = 0;
+    uint32_t sq = 0, sph = 0, dph = 0, un = 0;
     for (int it = 0;; ++it) {
       const int slot = it & 1;
       bool ok = mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
@@ -428,10 +446,30 @@ __global__ void __launch_bounds__(384, 1)
       const int u = unit_slot[slot];
       warp_arrive(&bar.unit_empty[slot]);
       if (u >= p.total_units) break;
-      const DkvUnit w = dkv_decode<MASK>(s, u);
+      const DkvUnit w = dkv_decode<MASK, VL>(s, u);
+      const Dims& su = w.sr.s;  // this unit's sequence
+      if (!w.sr.ok && warp == 4 && lane_id() == 0) report(ctl, FA_STATUS_BAD_INPUT);
+      if (!w.work) {
+        if (w.zero) {  // keys of a sequence without queries: zero gradients, this thread's row and columns
+          const int key = w.kt * TILE + r;
+          if (key < su.Nk) {
+            const int64_t krow = w.sr.koff + static_cast<int64_t>(key);
+            uint4* v4 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dv.ptr) + w.b * p.dv.sb +
+                                                 krow * p.dv.sn + w.kvh * p.dv.sh + (c0 / 64) * (D / 2));
+            uint4* k4 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dk.ptr) + w.b * p.dk.sb +
+                                                 krow * p.dk.sn + w.kvh * p.dk.sh + (c0 / 64) * (D / 2));
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+              v4[i] = make_uint4(0, 0, 0, 0);
+              k4[i] = make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+        continue;
+      }
       const int key = w.kt * TILE + r;
       int qfull_lo = 0, qfull_hi = 0;  // band: query tiles whose rows all see every key of this tile
-      if (MASK == MASK_BAND) q_full_range(s, w.kt, qfull_lo, qfull_hi);
+      if (MASK == MASK_BAND) q_full_range(su, w.kt, qfull_lo, qfull_hi);
       for (int k = 0; k < w.n_it && ok; ++k) {
         const uint32_t q = sq + k;
         const uint8_t* stage = smem + L::OFF_ST + (q % L::STAGES) * L::STAGE;
@@ -527,16 +565,17 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (!ok) break;
-      ok = mbar_wait(bar.acc_full, it & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+      ok = mbar_wait(bar.acc_full, (un++) & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int key0 = w.kt * TILE + wq * 32;  // this warp's first key row
-      __nv_bfloat16* dv0 = reinterpret_cast<__nv_bfloat16*>(p.dv.ptr) + w.b * p.dv.sb +
-                           static_cast<int64_t>(key0) * p.dv.sn + w.kvh * p.dv.sh;
-      __nv_bfloat16* dk0 = reinterpret_cast<__nv_bfloat16*>(p.dk.ptr) + w.b * p.dk.sb +
-                           static_cast<int64_t>(key0) * p.dk.sn + w.kvh * p.dk.sh;
-      store_acc_rows<D / 2>(tdV, (c0 / 64) * (D / 2), 1.f, dv0, p.dv.sn, s.Nk - key0, scratch);
-      store_acc_rows<D / 2>(tdK, (c0 / 64) * (D / 2), p.scale, dk0, p.dk.sn, s.Nk - key0, scratch);
+      const int key0 = w.kt * TILE + wq * 32;  // this warp's first key row (within its sequence)
+      const int64_t krow0 = w.sr.koff + static_cast<int64_t>(key0);
+      __nv_bfloat16* dv0 = reinterpret_cast<__nv_bfloat16*>(p.dv.ptr) + w.b * p.dv.sb + krow0 * p.dv.sn +
+                           w.kvh * p.dv.sh;
+      __nv_bfloat16* dk0 = reinterpret_cast<__nv_bfloat16*>(p.dk.ptr) + w.b * p.dk.sb + krow0 * p.dk.sn +
+                           w.kvh * p.dk.sh;
+      store_acc_rows<D / 2>(tdV, (c0 / 64) * (D / 2), 1.f, dv0, p.dv.sn, su.Nk - key0, scratch);
+      store_acc_rows<D / 2>(tdK, (c0 / 64) * (D / 2), p.scale, dk0, p.dk.sn, su.Nk - key0, scratch);
       sq += w.n_it;
     }
   }
@@ -575,7 +614,7 @@ struct DqLayout {
   static constexpr int ALLOC = (SCRATCH ? OFF_SCR + 8 * ROW_SCRATCH_BYTES : OFF_TMEM + 16) + 1024;
 };
 
-template <int D, int MASK>
+template <int D, int MASK, bool VL>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -632,7 +671,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     if (lane_id() == 0) {  // ---------------------------------------------- producer
-      uint32_t kq = 0;
+      uint32_t kq = 0, qn = 0;  // qn: units with work so far (Q phase)
       int q_armed = -1;
       for (int it = 0;; ++it) {
         const int slot = it & 1;
@@ -643,16 +682,18 @@ __global__ void __launch_bounds__(384, 1)
         if (u >= p.total_units) break;
         int b, h, qt;
         dq_unit(s, u, b, h, qt);
+        const SeqRows sr = seq_rows<VL>(s, b);
+        if (qt >= q_tiles(sr.s)) continue;  // past its (packed) sequence
         int klo, khi;
-        dq_kv_range<MASK>(s, qt, klo, khi);
+        dq_kv_range<MASK>(sr.s, qt, klo, khi);
         const int n = khi - klo, kvh = h / g;
-        if (!mbar_wait(q_empty, (it & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
+        if (!mbar_wait(q_empty, (qn & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
         mbar_arrive_expect_tx(q_full, 2 * L::TB);
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(smem + L::OFF_Q + c * (TILE * 128), &tm_q, q_full, c * 64, h, qt * TILE, b);
-          tma_load_4d(smem + L::OFF_DO + c * (TILE * 128), &tm_do, q_full, c * 64, h, qt * TILE, b);
+          tma_load_4d(smem + L::OFF_Q + c * (TILE * 128), &tm_q, q_full, c * 64, h, sr.qoff + qt * TILE, sr.tb);
+          tma_load_4d(smem + L::OFF_DO + c * (TILE * 128), &tm_do, q_full, c * 64, h, sr.qoff + qt * TILE, sr.tb);
         }
-        q_armed = it;
+        q_armed = static_cast<int>(qn++);
         bool ok = true;
         for (int j = 0; j < n; ++j, ++kq) {
           // K_j: its slot is free once dQ of the tile KST back is done.
@@ -664,7 +705,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&k_full[ks], L::TB);
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(smem + L::OFF_K + ks * L::TB + c * (TILE * 128), &tm_k, &k_full[ks], c * 64, kvh,
-                        (klo + j) * TILE, b);
+                        sr.koff + (klo + j) * TILE, sr.tb);
           // V_j: its slot is free once dP of the tile VST back is done.
           const int vs = kq % L::VST;
           if (!mbar_wait(&v_empty[vs], ((kq / L::VST) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
@@ -674,7 +715,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&v_full[vs], L::TB);
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(smem + L::OFF_V + vs * L::TB + c * (TILE * 128), &tm_v, &v_full[vs], c * 64, kvh,
-                        (klo + j) * TILE, b);
+                        sr.koff + (klo + j) * TILE, sr.tb);
         }
         if (!ok) break;
       }
@@ -696,7 +737,7 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t qb = smem_u32(smem + L::OFF_Q), dob = smem_u32(smem + L::OFF_DO);
       const uint32_t kb0 = smem_u32(smem + L::OFF_K), vb0 = smem_u32(smem + L::OFF_V);
       const uint32_t tP = tmem + 256, tdQ = tmem + 384;
-      uint32_t kq = 0, dsph = 0;
+      uint32_t kq = 0, dsph = 0, qn = 0;
       auto kwait = [&](uint32_t idx) {
         return mbar_wait(&k_full[idx % L::KST], (idx / L::KST) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
       };
@@ -713,10 +754,12 @@ __global__ void __launch_bounds__(384, 1)
         if (u >= p.total_units) break;
         int b, h, qt;
         dq_unit(s, u, b, h, qt);
+        const Dims su = seq_rows<VL>(s, b).s;
+        if (qt >= q_tiles(su)) continue;  // past its (packed) sequence
         int klo, khi;
-        dq_kv_range<MASK>(s, qt, klo, khi);
+        dq_kv_range<MASK>(su, qt, klo, khi);
         const int n = khi - klo;
-        bool ok = mbar_wait(q_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA) && kwait(kq);
+        bool ok = mbar_wait(q_full, (qn++) & 1, ctl, FA_STATUS_TIMEOUT_MMA) && kwait(kq);
         if (!ok) break;
         tc_fence_after();
         issue_ss<D>(tmem + 0, qb, kbase(kq));            // S_0 = Q K_0^T
@@ -767,7 +810,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tP = tmem + lanes + 256, tdQ = tmem + lanes + 384;
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-    uint32_t sph[2] = {0, 0}, dph = 0, kq = 0;
+    uint32_t sph[2] = {0, 0}, dph = 0, kq = 0, qn = 0;
     for (int it = 0;; ++it) {
       const int slot = it & 1;
       bool ok = mbar_wait(&unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
@@ -777,11 +820,15 @@ __global__ void __launch_bounds__(384, 1)
       if (u >= p.total_units) break;
       int b, h, qt;
       dq_unit(s, u, b, h, qt);
+      const SeqRows sr = seq_rows<VL>(s, b);
+      if (!sr.ok && warp == 4 && lane_id() == 0) report(ctl, FA_STATUS_BAD_INPUT);
+      const Dims& su = sr.s;  // this unit's sequence
+      if (qt >= q_tiles(su)) continue;  // past its (packed) sequence
       int klo, khi, full_lo = 0, full_hi = 0;
-      dq_kv_range<MASK>(s, qt, klo, khi);
+      dq_kv_range<MASK>(su, qt, klo, khi);
       if (MASK == MASK_BAND) {
-        kv_full_range(s, qt, full_lo, full_hi);
-        if ((s.Nk % TILE) != 0) full_hi = imin(full_hi, k_tiles(s) - 2);  // the ragged last tile is masked too
+        kv_full_range(su, qt, full_lo, full_hi);
+        if ((su.Nk % TILE) != 0) full_hi = imin(full_hi, k_tiles(su) - 2);  // the ragged last tile is masked too
       }
       const int n = khi - klo;
       const int q_row = qt * TILE + r;
@@ -816,14 +863,14 @@ __global__ void __launch_bounds__(384, 1)
           if (kt < full_lo || kt > full_hi) {
             // visible keys [lo, hi) relative to this warpgroup's first column
             const int first = kt * TILE + c0;
-            const int hi = imin(s.Nk, q_row + s.wr + 1) - first;
+            const int hi = imin(su.Nk, q_row + s.wr + 1) - first;
             const int lo = q_row - s.wl - first;
 #pragma unroll
             for (int i = 0; i < 64; ++i)
               if (i < lo || i >= hi) pf[i] = 0.f;
           }
         } else if (j == n - 1) {  // causal or full: only the last key tile holds masked keys
-          int lim = imin(TILE, s.Nk - j * TILE);
+          int lim = imin(TILE, su.Nk - j * TILE);
           if (MASK == MASK_CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
           lim -= c0;
 #pragma unroll
@@ -857,13 +904,13 @@ __global__ void __launch_bounds__(384, 1)
         warp_arrive(ds_full);
       }
       if (!ok) break;
-      ok = mbar_wait(acc_full, it & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+      ok = mbar_wait(acc_full, (qn++) & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int q0 = qt * TILE + wq * 32;  // this warp's first query row
+      const int q0 = qt * TILE + wq * 32;  // this warp's first query row (within its sequence)
       __nv_bfloat16* dq0 = reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sb +
-                           static_cast<int64_t>(q0) * p.dq.sn + h * p.dq.sh;
-      store_acc_rows<D / 2>(tdQ, (c0 / 64) * (D / 2), p.scale, dq0, p.dq.sn, s.Nq - q0, scratch);
+                           (sr.qoff + static_cast<int64_t>(q0)) * p.dq.sn + h * p.dq.sh;
+      store_acc_rows<D / 2>(tdQ, (c0 / 64) * (D / 2), p.scale, dq0, p.dq.sn, su.Nq - q0, scratch);
       if (!L::SCRATCH) {  // the Q tile was the scratch: order these accesses before the next TMA write
         fence_proxy_async_smem();
         warp_arrive(q_empty);
@@ -879,7 +926,7 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, int MASK>
+template <int D, int MASK, bool VL = false>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   BwdParams p;
   p.dims = a.dims;
@@ -900,13 +947,13 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   // 1) preprocess
   if (a.parts & 1) {
     const int64_t threads = static_cast<int64_t>(a.dims.B) * a.dims.Hq * a.nq_pad * (D / 8);
-    bwd_preprocess_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(p);
+    bwd_preprocess_kernel<D, VL><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   // 2) dK / dV
   if (a.parts & 2) {
-    auto kern = bwd_dkdv_kernel<D, MASK>;
+    auto kern = bwd_dkdv_kernel<D, MASK, VL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<D>::ALLOC);
     if (e != cudaSuccess) return e;
     p.counter = a.counters;
@@ -917,7 +964,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   }
   // 3) dQ
   if (a.parts & 4) {
-    auto kern = bwd_dq_kernel<D, MASK>;
+    auto kern = bwd_dq_kernel<D, MASK, VL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::ALLOC);
     if (e != cudaSuccess) return e;
     p.counter = a.counters + 1;
@@ -933,6 +980,12 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
 
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st) {
   const int m = mask_kind(a.dims);
+  if (a.dims.cu_q != nullptr) {  // packed sequences: no band
+    if (m == MASK_BAND) return cudaErrorInvalidValue;
+    if (a.d == 64)
+      return m == MASK_CAUSAL ? launch_bwd_t<64, MASK_CAUSAL, true>(a, st) : launch_bwd_t<64, MASK_NONE, true>(a, st);
+    return m == MASK_CAUSAL ? launch_bwd_t<128, MASK_CAUSAL, true>(a, st) : launch_bwd_t<128, MASK_NONE, true>(a, st);
+  }
   if (a.d == 64)
     return m == MASK_BAND ? launch_bwd_t<64, MASK_BAND>(a, st)
            : m == MASK_CAUSAL ? launch_bwd_t<64, MASK_CAUSAL>(a, st) : launch_bwd_t<64, MASK_NONE>(a, st);

@@ -155,14 +155,15 @@ __device__ __forceinline__ UnitTiles unit_tiles(const Dims& s, int p) {
 }
 
 // ------------------------------------------------------------------ producer
-template <int D, int MASK, bool F8>
+template <int D, int MASK, bool F8, bool VL>
 __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, const CUtensorMap* tm_q,
                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, const FwdParams& p,
                              const Ctl& ctl) {
   using L = FwdLayout<D, F8>;
   const int g = p.dims.Hq / p.dims.Hkv;
   uint32_t seq = 0;       // K/V groups issued so far (ring sequence number)
-  int q_armed = -1;       // last unit index whose Q load was issued
+  uint32_t qn = 0;        // units with work so far (Q load phase)
+  int q_armed = -1;       // phase of the last Q load issued
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     if (!mbar_wait(&bar.unit_empty[slot], ((it >> 1) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
@@ -172,19 +173,22 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
     if (u >= p.total_units) break;
     int b, h, pr;
     fwd_unit(p.dims, u, b, h, pr);
-    const UnitTiles ut = unit_tiles<MASK>(p.dims, pr);
+    const SeqRows sr = seq_rows<VL>(p.dims, b);
+    const UnitTiles ut = unit_tiles<MASK>(VL ? sr.s : p.dims, pr);
     const int nmax = ut.nu;
+    if (VL && nmax == 0) continue;  // both query tiles past their packed sequence
     const int kvh = h / g;
+    const int qrow = VL ? sr.qoff : 0, krow = VL ? sr.koff : 0, tb = VL ? 0 : b;
 
-    if (!mbar_wait(bar.q_empty, (it & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
+    if (!mbar_wait(bar.q_empty, ((VL ? qn : it) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
     mbar_arrive_expect_tx(bar.q_full, 2 * L::QB);
 #pragma unroll
     for (int t = 0; t < 2; ++t)
 #pragma unroll
       for (int c = 0; c < L::CH; ++c)
         tma_load_4d(smem + L::OFF_Q + t * L::QB + c * (TILE * 128), tm_q, bar.q_full, c * L::ECH, h,
-                    (2 * pr + t) * TILE, b);
-    q_armed = it;
+                    qrow + (2 * pr + t) * TILE, tb);
+    q_armed = VL ? static_cast<int>(qn++) : it;
 
     bool ok = true;
     for (int gi = 0; gi <= nmax; ++gi, ++seq) {  // group gi: V_{gi-1} (slot A), K_gi (slot B)
@@ -199,11 +203,11 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
 #pragma unroll
       for (int c = 0; c < L::CH; ++c) {
         if (has_v)
-          tma_load_4d(base + c * (TILE * 128), tm_v, &bar.kv_full[gs], c * L::ECH, kvh, (ut.base + gi - 1) * TILE,
-                      b);
+          tma_load_4d(base + c * (TILE * 128), tm_v, &bar.kv_full[gs], c * L::ECH, kvh,
+                      krow + (ut.base + gi - 1) * TILE, tb);
         if (has_k)
           tma_load_4d(base + L::TB + c * (TILE * 128), tm_k, &bar.kv_full[gs], c * L::ECH, kvh,
-                      (ut.base + gi) * TILE, b);
+                      krow + (ut.base + gi) * TILE, tb);
       }
     }
     if (!ok) break;
@@ -219,7 +223,7 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D, int MASK, bool F8>
+template <int D, int MASK, bool F8, bool VL>
 __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
                         const Ctl& ctl) {
   using L = FwdLayout<D, F8>;
@@ -230,6 +234,7 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
   const uint32_t q_base = smem_u32(smem + L::OFF_Q);
   const uint32_t kv_base = smem_u32(smem + L::OFF_KV);
   uint32_t seq = 0;
+  uint32_t qn = 0;  // units with work so far (Q phase)
   uint32_t pph[2] = {0, 0};
   uint32_t active[2] = {0, 0};
 
@@ -272,12 +277,13 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
     if (u >= p.total_units) return;
     int b, h, pr;
     fwd_unit(p.dims, u, b, h, pr);
-    const UnitTiles ut = unit_tiles<MASK>(p.dims, pr);
+    const UnitTiles ut = unit_tiles<MASK>(VL ? seq_rows<VL>(p.dims, b).s : p.dims, pr);
     const int nmax = ut.nu;
+    if (VL && nmax == 0) continue;  // both query tiles past their packed sequence
     // tile t is active at local steps [a[t], e[t])
     const int a[2] = {ut.a[0], ut.a[1]}, e[2] = {ut.a[0] + ut.n[0], ut.a[1] + ut.n[1]};
 
-    if (!mbar_wait(bar.q_full, it & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+    if (!mbar_wait(bar.q_full, (VL ? qn++ : static_cast<uint32_t>(it)) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
     // group 0: K of local step 0
     {
       if (!group_wait(seq)) return;
@@ -319,7 +325,7 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
 }
 
 // ------------------------------------------------------------------ softmax
-template <int D, int MASK, bool F8>
+template <int D, int MASK, bool F8, bool VL>
 __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
                             const Ctl& ctl, uint8_t* scratch) {
   const int wq = (threadIdx.x >> 5) & 3;  // warp within the warpgroup = TMEM lane quarter
@@ -340,9 +346,13 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     if (u >= p.total_units) return;
     int b, h, pr;
     fwd_unit(s, u, b, h, pr);
-    const UnitTiles ut = unit_tiles<MASK>(s, pr);
+    const SeqRows sr = seq_rows<VL>(s, b);
+    if (VL && !sr.ok && t == 0 && wq == 0 && lane_id() == 0) report(ctl, FA_STATUS_BAD_INPUT);
+    const Dims& su = VL ? sr.s : s;  // this unit's sequence (packed), else the problem
+    const UnitTiles ut = unit_tiles<MASK>(su, pr);
     const int n = ut.n[t];
     if (n == 0) continue;
+    const int nq_u = su.Nq, nk_u = su.Nk, qoff = VL ? sr.qoff : 0;
     const int qt = 2 * pr + t;
     const int q_row = qt * TILE + r;
     const int kt0 = ut.base + ut.a[t];  // first key tile of this query tile
@@ -353,8 +363,8 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     const float* skp = F8 ? p.sk + (static_cast<int64_t>(b) * s.Hkv + kvh) * p.nkt + kt0 : nullptr;
     int full_lo = 0, full_hi = 0;        // band: key tiles this query tile sees in full
     if (MASK == MASK_BAND) {
-      kv_full_range(s, qt, full_lo, full_hi);
-      if ((s.Nk % TILE) != 0) full_hi = imin(full_hi, k_tiles(s) - 2);  // the ragged last tile is masked too
+      kv_full_range(su, qt, full_lo, full_hi);
+      if ((nk_u % TILE) != 0) full_hi = imin(full_hi, cdiv(nk_u, TILE) - 2);  // the ragged last tile is masked too
     }
 
     float m_run = -INFINITY, l_run = 0.f;
@@ -375,15 +385,15 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
         const int kt = kt0 + j;
         if (kt < full_lo || kt > full_hi) {
           // keys [lo, hi) of this tile are visible to the row: the band i - wl .. i + wr, below Nk
-          const int hi = imin(s.Nk - kt * TILE, imin(TILE, q_row + s.wr + 1 - kt * TILE));
+          const int hi = imin(nk_u - kt * TILE, imin(TILE, q_row + s.wr + 1 - kt * TILE));
           const int lo = imax(0, q_row - s.wl - kt * TILE);
 #pragma unroll
           for (int i = 0; i < 128; ++i)
             if (i >= hi || i < lo) sv[i] = -INFINITY;
         }
-      } else if (j == n - 1 && (MASK == MASK_CAUSAL || (s.Nk % TILE) != 0)) {
+      } else if (j == n - 1 && (MASK == MASK_CAUSAL || (nk_u % TILE) != 0)) {
         // the last tile: keys at or past Nk, and under j <= i keys past the row
-        int lim = s.Nk - j * TILE;
+        int lim = nk_u - j * TILE;
         if (MASK == MASK_CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
 #pragma unroll
         for (int i = 0; i < 128; ++i)
@@ -458,14 +468,13 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     tc_fence_after();
     const float inv_l = (F8 ? p.sv[static_cast<int64_t>(b) * s.Hkv + kvh] : 1.f) / l_run;
     const float2 il2 = make_float2(inv_l, inv_l);
-    const bool live = q_row < s.Nq;
-    const int q0 = qt * TILE + wq * 32;  // this warp's first row
-    __nv_bfloat16* o0 = reinterpret_cast<__nv_bfloat16*>(p.o.ptr) + b * p.o.sb + static_cast<int64_t>(q0) * p.o.sn +
-                        h * p.o.sh;
-    __nv_bfloat16* r0 = p.o_res.ptr == nullptr
-                            ? nullptr
-                            : reinterpret_cast<__nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
-                                  static_cast<int64_t>(q0) * p.o_res.sn + h * p.o_res.sh;
+    const bool live = q_row < nq_u;
+    const int q0 = qt * TILE + wq * 32;  // this warp's first row (within its sequence)
+    const int64_t orow = qoff + q0;      // ... and in the tensor
+    __nv_bfloat16* o0 = reinterpret_cast<__nv_bfloat16*>(p.o.ptr) + b * p.o.sb + orow * p.o.sn + h * p.o.sh;
+    __nv_bfloat16* r0 = p.o_res.ptr == nullptr ? nullptr
+                                               : reinterpret_cast<__nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
+                                                     orow * p.o_res.sn + h * p.o_res.sh;
 #pragma unroll
     for (int cc = 0; cc < D / 32; ++cc) {
       uint32_t o[32];
@@ -478,7 +487,7 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
         ov[i] = __fmul2_rn(f32x2(o[2 * i], o[2 * i + 1]), il2);
         w[i] = pack_bf16(ov[i].x, ov[i].y);
       }
-      store_rows32_bf16(w, scratch, o0 + cc * 32, p.o.sn, s.Nq - q0);
+      store_rows32_bf16(w, scratch, o0 + cc * 32, p.o.sn, nq_u - q0);
       if (r0 != nullptr) {  // rounding residual: bf16(O - bf16(O))
         uint32_t rz[16];
 #pragma unroll
@@ -486,18 +495,18 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
           const float2 hv = unpack_bf16(w[i]);
           rz[i] = pack_bf16(ov[i].x - hv.x, ov[i].y - hv.y);
         }
-        store_rows32_bf16(rz, scratch, r0 + cc * 32, p.o_res.sn, s.Nq - q0);
+        store_rows32_bf16(rz, scratch, r0 + cc * 32, p.o_res.sn, nq_u - q0);
       }
     }
-    if (live)
-      p.lse[(static_cast<int64_t>(b) * s.Hq + h) * s.Nq + q_row] =
-          (m_run + __log2f(l_run) - (F8 ? LOG2_448 : 0.f)) * LN2;
+    if (live)  // LSE [B, Hq, Nq], or [Hq, total_q] for packed sequences
+      p.lse[(VL ? static_cast<int64_t>(h) * s.total_q + qoff : (static_cast<int64_t>(b) * s.Hq + h) * s.Nq) +
+            q_row] = (m_run + __log2f(l_run) - (F8 ? LOG2_448 : 0.f)) * LN2;
     tc_fence_before();
     warp_arrive(&bar.o_empty[t]);
   }
 }
 
-template <int D, int MASK, bool F8>
+template <int D, int MASK, bool F8, bool VL>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -539,11 +548,11 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane_id() == 0) fwd_producer<D, MASK, F8>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
+    if (lane_id() == 0) fwd_producer<D, MASK, F8, VL>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
   } else if (warp == 1) {
-    if (lane_id() == 0) fwd_mma<D, MASK, F8>(smem, bar, unit_slot, tmem, p, ctl);
+    if (lane_id() == 0) fwd_mma<D, MASK, F8, VL>(smem, bar, unit_slot, tmem, p, ctl);
   } else if (warp >= 4) {
-    fwd_softmax<D, MASK, F8>((warp - 4) >> 2, bar, unit_slot, tmem, p, ctl,
+    fwd_softmax<D, MASK, F8, VL>((warp - 4) >> 2, bar, unit_slot, tmem, p, ctl,
                            smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES);
   }
   tc_fence_before();
@@ -554,10 +563,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, int MASK, bool F8 = false>
+template <int D, int MASK, bool F8 = false, bool VL = false>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   using L = FwdLayout<D, F8>;
-  auto kern = fa_fwd_kernel<D, MASK, F8>;
+  auto kern = fa_fwd_kernel<D, MASK, F8, VL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   FwdParams p;
@@ -584,6 +593,14 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
   const int m = mask_kind(a.dims);
+  if (a.dims.cu_q != nullptr) {  // packed sequences: bf16, no band
+    if (a.sq != nullptr || m == MASK_BAND) return cudaErrorInvalidValue;
+    if (a.d == 64)
+      return m == MASK_CAUSAL ? launch_fwd_t<64, MASK_CAUSAL, false, true>(a, st)
+                              : launch_fwd_t<64, MASK_NONE, false, true>(a, st);
+    return m == MASK_CAUSAL ? launch_fwd_t<128, MASK_CAUSAL, false, true>(a, st)
+                            : launch_fwd_t<128, MASK_NONE, false, true>(a, st);
+  }
   if (a.sq != nullptr) {  // E4M3 operands (d = 128 only)
     if (a.d != 128) return cudaErrorInvalidValue;
     return m == MASK_BAND     ? launch_fwd_t<128, MASK_BAND, true>(a, st)

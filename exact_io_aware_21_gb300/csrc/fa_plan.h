@@ -29,7 +29,44 @@ struct Dims {
   int B, Hq, Hkv, Nq, Nk;
   int causal;
   int wl, wr;  // band of visible keys around each row (causal folded into wr)
+  // Packed variable-length sequences (cu_q == nullptr: dense [B, N, H, d]).
+  // Sequence b is rows cu_q[b] .. cu_q[b+1]-1 of Q (cu_k likewise of K, V),
+  // tensors [total, H, d]; Nq and Nk then hold the longest lengths, which size
+  // the work-unit grid, and every unit works on its own sequence's lengths.
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
 };
+
+#ifdef __CUDACC__
+// The rows a work unit of batch entry b sees: its own lengths (in `s`) and
+// where they start in the tensors.  Dense: b's rows from 0, TMA batch
+// coordinate b.  Packed: rows cu[b].., batch coordinate 0.  `ok` is false for
+// lengths the cu arrays cannot hold (not within [0, total], decreasing, longer
+// than the grid's Nq / Nk, queries without keys, or unequal lengths under a
+// causal mask); such a sequence is given no rows.
+struct SeqRows {
+  Dims s;
+  int qoff, koff, tb;
+  bool ok;
+};
+
+template <bool VL>  // VL: packed sequences (else the dense view, at no cost)
+__device__ __forceinline__ SeqRows seq_rows(const Dims& d, int b) {
+  SeqRows r{d, 0, 0, b, true};
+  if (!VL) return r;
+  const int q0 = __ldg(d.cu_q + b), q1 = __ldg(d.cu_q + b + 1);
+  const int k0 = __ldg(d.cu_k + b), k1 = __ldg(d.cu_k + b + 1);
+  r.ok = 0 <= q0 && q0 <= q1 && q1 <= d.total_q && 0 <= k0 && k0 <= k1 && k1 <= d.total_k &&
+         q1 - q0 <= d.Nq && k1 - k0 <= d.Nk && (q1 == q0 || k1 > k0) && (!d.causal || q1 - q0 == k1 - k0);
+  r.s.Nq = r.ok ? q1 - q0 : 0;
+  r.s.Nk = r.ok ? k1 - k0 : 0;
+  r.qoff = r.ok ? q0 : 0;
+  r.koff = r.ok ? k0 : 0;
+  r.tb = 0;
+  return r;
+}
+#endif
 
 FA_HD bool banded(const Dims& s) { return s.wl < UNBOUNDED || s.wr < UNBOUNDED; }
 

@@ -34,8 +34,10 @@ __device__ __forceinline__ void report(const Ctl& c, int code) {
   atomicOr(c.status, code);
 }
 
+// Another thread gave up on a wait (a timeout bit is set).  Input errors
+// (FA_STATUS_BAD_INPUT) do not stop the kernel: the bad work is skipped.
 __device__ __forceinline__ bool aborted(const Ctl& c) {
-  return *reinterpret_cast<volatile int*>(c.status) != 0;
+  return (*reinterpret_cast<volatile int*>(c.status) & FA_STATUS_TIMEOUT_MASK) != 0;
 }
 
 // ---------------------------------------------------------------------------

@@ -54,7 +54,31 @@ DECODE_Q4 = Workload("decode_b8_hq32_hkv8_q4_kv131072_d128", 8, 32, 8, 4, 131072
 WINDOW_N16384_W4096 = Workload("window_causal_b1_hq32_hkv8_n16384_w4096_d128", 1, 32, 8, 16384, 16384, 128,
                                True, window=(4095, 0))
 
-ALL = [TINY, MHA_N2048_D64, CAUSAL_N4096_D128, GQA_N8192_D128, DECODE_Q1, DECODE_Q4, WINDOW_N16384_W4096]
+# Packed variable-length sequences (SFT-like, long-tailed lengths): extra["n_seqs"]
+# sequences, lengths varlen_lengths(n_seqs, Nq, seed), in [total, H, d] tensors, causal.
+VARLEN_T32768_D128 = Workload("varlen_causal_b24_hq32_hkv8_total32768_d128", 1, 32, 8, 32768, 32768, 128, True,
+                              extra={"n_seqs": 24})
+
+ALL = [TINY, MHA_N2048_D64, CAUSAL_N4096_D128, GQA_N8192_D128, DECODE_Q1, DECODE_Q4, WINDOW_N16384_W4096,
+       VARLEN_T32768_D128]
+
+
+def varlen_lengths(n_seqs, total, lo=64, hi=8192, seed=0):
+    """n_seqs lengths summing to ``total``, long-tailed: Pareto(1.2) draws of a CPU
+    generator seeded with ``seed``, scaled and clipped to [lo, hi], the rounding
+    remainder spread over the sequences below hi."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    u = torch.rand(n_seqs, generator=gen, dtype=torch.float64)
+    raw = (1.0 - u) ** (-1.0 / 1.2)                            # Pareto(1.2) on [1, inf)
+    lens = [int(min(hi, max(lo, round(float(r) * total / float(raw.sum()))))) for r in raw]
+    i = 0
+    while sum(lens) != total:                                  # fix the rounding, one token at a time
+        step = 1 if sum(lens) < total else -1
+        if lo <= lens[i] + step <= hi:
+            lens[i] += step
+        i = (i + 1) % n_seqs
+    return lens
 
 
 def make(w, device="cpu", with_do=True, seed=None):

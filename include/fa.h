@@ -110,6 +110,36 @@ int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
            void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Packed variable-length sequences ("第18章" §18.7.1, flash_attn_varlen_func):
+ * the B sequences of a batch lie one after another along the token axis,
+ * q [total_q, Hq, d], k, v [total_k, Hkv, d] (the fa_tensor_t's stride_b is
+ * ignored); sequence b is rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of q
+ * (cu_seqlens_k likewise of k, v), and attends only within itself, causal
+ * with its own positions.  cu_seqlens_q / _k: device int32 [B + 1], starting
+ * at 0, non-decreasing, ending at most at total; max_seqlen_q / _k: host ints,
+ * at least every sequence's length (they size the kernels' work grid).  The
+ * shape's B is the number of sequences and Nq, Nk the packed token counts
+ * total_q, total_k; windows are not supported.  lse [Hq, total_q].  o,
+ * o_residual, dout, dq: [total_q, Hq, d]; dk, dv: [total_k, Hkv, d].
+ * Lengths the arrays cannot hold (out of range, decreasing, above max_seqlen,
+ * queries with no keys, or unequal lengths under causal) are reported through
+ * the workspace status (fa_get_device_status -> FA_ERR_INVALID) and those
+ * sequences' outputs are not written; keys of a sequence with no queries get
+ * zero gradients.  Workspaces: fa_fwd_workspace_size(shape) and
+ * fa_bwd_varlen_workspace_size(shape, max_seqlen_q).
+ * ------------------------------------------------------------------------- */
+int fa_fwd_varlen(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k, const fa_tensor_t* o, float* lse,
+                  const fa_tensor_t* o_residual, const fa_shape_t* shape, void* workspace, size_t workspace_bytes,
+                  void* stream);
+size_t fa_bwd_varlen_workspace_size(const fa_shape_t* shape, int max_seqlen_q);
+int fa_bwd_varlen(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* cu_seqlens_q,
+                  const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k, const fa_tensor_t* o,
+                  const float* lse, const fa_tensor_t* o_residual, const fa_tensor_t* dout, const fa_tensor_t* dq,
+                  const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* shape, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * FP8 forward ("第18章" §18.6.2; lecture notes slide 24).
  *
  * fa_quantize_fp8: E4M3 codes of a bf16 tensor x [B, N, H, d] (d = 64 or 128),

@@ -30,3 +30,11 @@ def test_window_leg_is_outside_the_step():
     train, dec, win = bench.workloads()
     assert [w.name for w in win] == list(bench.WINDOW)
     assert all(w.window is None for w in train + dec)
+
+
+def test_varlen_leg_lengths_and_flops():
+    w = inputs.VARLEN_T32768_D128
+    lens = bench.varlen_lens(w)
+    assert len(lens) == 24 and sum(lens) == w.Nq and min(lens) >= 64 and max(lens) <= 8192
+    assert lens == inputs.varlen_lengths(24, w.Nq, seed=w.seed)          # seeded: the same every call
+    assert bench.fwd_flops(w) == sum(2.0 * w.Hq * n * n * w.d for n in lens)   # causal: half of 4*H*n^2*d

@@ -33,6 +33,12 @@ Definitions followed (one bullet per function below):
     another; sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1 and attends
     only within itself (no attention across sequence boundaries; causal is
     applied with the sequence's own positions).  LSE is [Hq, total_q].
+  * block-sparse attention (§18.8.1): a CSR table lists, for each query block
+    of ``block`` rows, the key blocks it attends to (row_ptr [nqb + 1],
+    col_idx [nnz], strictly increasing within a row); key j is visible to
+    query i iff j's block is listed for i's block (and, causal, j <= i).
+    Unlisted blocks contribute nothing.  A row that sees no key gets O = 0 and
+    LSE = -inf.  One table serves every batch entry and head.
   * paged, variable-length decode: a sequence's logical KV row r lives in the
     physical page block_table[b, r // page_size], at row r % page_size
     (PagedAttention's page table, §18.8.2 part 3 and §18.8.3); each sequence
@@ -348,6 +354,48 @@ def attention_varlen_backward(q, k, v, do, cu_q, cu_k, scale, causal=False):
         g = attention_backward(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], do[None, q0:q1], scale, causal)
         dq[q0:q1], dk[k0:k1], dv[k0:k1] = g[0][0], g[1][0], g[2][0]
     return dq, dk, dv
+
+
+def block_mask_from_csr(row_ptr, col_idx, n_qblocks, n_kblocks):
+    """Dense boolean [n_qblocks, n_kblocks] of the listed blocks; raises on a table
+    that is not strictly increasing within rows or lists a block out of range."""
+    row_ptr, col_idx = np.asarray(row_ptr, dtype=np.int64), np.asarray(col_idx, dtype=np.int64)
+    if len(row_ptr) != n_qblocks + 1 or row_ptr[0] != 0 or np.any(np.diff(row_ptr) < 0):
+        raise ValueError("row_ptr must have one entry per query block plus one, from 0, non-decreasing")
+    M = np.zeros((n_qblocks, n_kblocks), dtype=bool)
+    for i in range(n_qblocks):
+        cols = col_idx[row_ptr[i]:row_ptr[i + 1]]
+        if np.any(np.diff(cols) <= 0) or np.any(cols < 0) or np.any(cols >= n_kblocks):
+            raise ValueError("column indices must be strictly increasing and within range")
+        M[i, cols] = True
+    return M
+
+
+def attention_blocksparse_forward(q, k, v, row_ptr, col_idx, scale, causal=False, block=128):
+    """Block-sparse forward: O [B, Nq, Hq, d], LSE [B, Hq, Nq].  Plain definition with
+    the element mask taken from the listed blocks; rows that see no key get O = 0,
+    LSE = -inf."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Nq, Nk, Hq, Hkv, d = _check_shapes(q, k, v)
+    if causal and Nq != Nk:
+        raise ValueError("causal attention is defined here for Nq == Nk only")
+    M = block_mask_from_csr(row_ptr, col_idx, -(-Nq // block), -(-Nk // block))
+    visible = np.repeat(np.repeat(M, block, axis=0), block, axis=1)[:Nq, :Nk]
+    if causal:
+        visible &= ~causal_mask(np.arange(Nq), Nk)
+    g = Hq // Hkv
+    O = np.zeros((B, Nq, Hq, d))
+    LSE = np.full((B, Hq, Nq), NEG_INF)
+    seen = visible.any(axis=1)
+    for b in range(B):
+        for h in range(Hq):
+            S = np.where(visible, scale * (q[b, :, h, :] @ k[b, :, h // g, :].T), NEG_INF)
+            m = np.where(seen, S.max(axis=1), 0.0)
+            E = np.where(visible, np.exp(S - m[:, None]), 0.0)
+            l = E.sum(axis=1)
+            O[b, seen, h, :] = (E[seen] @ v[b, :, h // g, :]) / l[seen, None]
+            LSE[b, h, seen] = m[seen] + np.log(l[seen])
+    return O, LSE
 
 
 def gather_paged(cache, block_table, b, length):

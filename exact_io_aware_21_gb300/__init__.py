@@ -17,6 +17,8 @@ from .binding import (  # noqa: F401
     forward,
     forward_fp8,
     forward_varlen,
+    forward_blocksparse,
+    fa_fwd_blocksparse,
     backward_varlen,
     fa_fwd_varlen,
     fa_bwd_varlen,

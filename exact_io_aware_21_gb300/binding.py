@@ -71,6 +71,7 @@ SIGNATURES = {
     "fa_dq_unit": (_I, [_PS, _I, _PI, _PI, _PI]),
     "fa_decode_split_range": (_I, [_PS, _I, _I, _PI, _PI]),
     "fa_selftest_mma": (_I, [_I, _I, _VP, _VP, _VP, _VP, _VP]),
+    "fa_fwd_blocksparse": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _PT, _VP, _PT, _PS, _VP, _SZ, _VP]),
     "fa_fwd_varlen": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _I, _PT, _VP, _PT, _PS, _VP, _SZ, _VP]),
     "fa_bwd_varlen_workspace_size": (_SZ, [_PS, _I]),
     "fa_bwd_varlen": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _I, _PT, _VP, _PT, _PT, _PT, _PT, _PT, _PS, _VP, _SZ, _VP]),
@@ -190,6 +191,18 @@ def fa_decode_paged(q, kc, vc, block_table, seqlens_k, o, lse, s, num_splits, wo
     check(lib.fa_decode_paged(tdesc(q), tdesc(kc), tdesc(vc), block_table.data_ptr(), block_table.shape[1],
                               seqlens_k.data_ptr(), kc.shape[0], kc.shape[1], tdesc(o), lse.data_ptr(),
                               ctypes.byref(s), int(num_splits), workspace.data_ptr(), workspace.numel(), _stream(q)))
+
+
+def fa_fwd_blocksparse(q, k, v, row_ptr, col_idx, o, lse, s, workspace, o_res=None):
+    """row_ptr [ceil(Nq/128) + 1], col_idx [nnz]: contiguous int32 CUDA tensors (the CSR block table)."""
+    lib = library()
+    for t in (row_ptr, col_idx):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise FAError(1, "row_ptr and col_idx must be contiguous int32 CUDA tensors")
+    check(lib.fa_fwd_blocksparse(tdesc(q), tdesc(k), tdesc(v), row_ptr.data_ptr(),
+                                 col_idx.data_ptr() if col_idx.numel() else None, col_idx.numel(), tdesc(o),
+                                 lse.data_ptr(), _opt(o_res), ctypes.byref(s), workspace.data_ptr(),
+                                 workspace.numel(), _stream(q)))
 
 
 def fa_fwd_varlen(q, k, v, cu_q, cu_k, max_q, max_k, o, lse, s, workspace, o_res=None):
@@ -352,3 +365,15 @@ def backward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqle
     fa_bwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, o, lse, do, dq, dk, dv, s, ws,
                   o_residual)
     return dq, dk, dv
+
+
+def forward_blocksparse(q, k, v, row_ptr, col_idx, causal=False, scale=None, residual=False):
+    """Block-sparse forward (see fa_fwd_blocksparse in include/fa.h): q [B,Nq,Hq,d], k/v
+    [B,Nk,Hkv,d] bf16; row_ptr / col_idx the CSR table of 128-key tiles per 128-row query tile."""
+    s = _dims(q, k, scale, causal)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
+    res = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
+    ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q.device)
+    fa_fwd_blocksparse(q, k, v, row_ptr, col_idx, o, lse, s, ws, res)
+    return (o, lse, res) if residual else (o, lse)

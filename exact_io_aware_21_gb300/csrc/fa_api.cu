@@ -321,9 +321,16 @@ OutRows out_rows(const fa_tensor_t* t, const Packed* pk) {
   return OutRows{t->ptr, pk ? 0 : t->stride_b, t->stride_n, t->stride_h};
 }
 
+// Block-sparse table (CSR over 128-row query tiles and 128-key tiles).
+struct Sparse {
+  const int* row_ptr;
+  const int* col_idx;
+  int nnz;
+};
+
 int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
              const fa_tensor_t* o_res, const fa_shape_t* s, const Packed* pk, void* ws, size_t ws_bytes,
-             void* stream) {
+             void* stream, const Sparse* sp = nullptr) {
   int rc;
   if ((rc = check_shape(s)) || (rc = check_packed(s, pk)) || (rc = check_tensor(q)) || (rc = check_tensor(k)) ||
       (rc = check_tensor(v)) || (rc = check_tensor(o)) || (o_res && (rc = check_tensor(o_res))))
@@ -342,6 +349,11 @@ int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, c
     return rc;
   a.o = out_rows(o, pk);
   a.o_res = o_res ? out_rows(o_res, pk) : OutRows{nullptr, 0, 0, 0};
+  if (sp) {
+    a.row_ptr = sp->row_ptr;
+    a.col_idx = sp->col_idx;
+    a.nnz = sp->nnz;
+  }
   a.lse = lse;
   a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
   a.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_COUNTER_OFFSET);
@@ -355,6 +367,16 @@ int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, c
 int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
            const fa_tensor_t* o_res, const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
   return fwd_impl(q, k, v, o, lse, o_res, s, nullptr, ws, ws_bytes, stream);
+}
+
+int fa_fwd_blocksparse(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* row_ptr,
+                       const int* col_idx, int nnz, const fa_tensor_t* o, float* lse, const fa_tensor_t* o_res,
+                       const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_shape(s))) return rc;
+  if (!row_ptr || nnz < 0 || (nnz > 0 && !col_idx) || s->window || cdiv(s->Nk, TILE) > 1024) return FA_ERR_INVALID;
+  const Sparse sp{row_ptr, col_idx, nnz};
+  return fwd_impl(q, k, v, o, lse, o_res, s, nullptr, ws, ws_bytes, stream, &sp);
 }
 
 int fa_fwd_varlen(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* cu_seqlens_q,

@@ -27,6 +27,12 @@
 // the product of the two block scales, the softmax stays in fp32, and P goes
 // to TMEM as E4M3 on the scale its bound fixes (448 P, four codes per column);
 // the epilogue applies V's scale with 1 / l.
+// Block-sparse instantiation (§18.8.1): a CSR table lists the key tiles of each
+// query tile.  Warp 2 turns a unit's two rows of the table into one list in
+// shared memory (the union in key order, with a bit per query tile) and the
+// other roles walk it: K/V of listed tiles only, S and P V of a query tile only
+// at its own tiles.  Consumers release a unit's slot when the unit is done
+// (the list lives there until then).
 // The running max is the exact row max so far (TAU = 0): the dominant P of a
 // nearly one-hot row is then exactly 1.0 in bf16, so O's error scales with the
 // rest of the row, which keeps D = dO . O consistent in the backward.  The
@@ -45,7 +51,7 @@ constexpr float TAU = 0.0f;
 constexpr float LN2 = 0.69314718055994530942f;
 constexpr float LOG2_448 = 8.8073549220576041f;  // P is quantised as 448 P = 2^(x - m + log2 448)
 
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, bool SP = false>
 struct FwdLayout {
   static constexpr int ESZ = F8 ? 1 : 2;     // bytes per element
   static constexpr int QB = TILE * D * ESZ;  // one Q tile (bytes)
@@ -62,13 +68,39 @@ struct FwdLayout {
   static constexpr int OFF_BAR = OFF_KV + STAGES * TB;
   // barriers: unit_full[2] unit_empty[2] q_full q_empty kv_full[NG] kv_empty[NG]
   //           s_full[2] p_full[2] o_full[2] o_empty[2]
-  static constexpr int NBAR = 4 + 2 + 2 * NG + 8;
+  //           list_full[2] (block-sparse)
+  static constexpr int NBAR = 4 + 2 + 2 * NG + 8 + (SP ? 2 : 0);
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
   static constexpr int OFF_SCR = (OFF_TMEM + 16 + 127) / 128 * 128;  // row-store scratch, one per softmax warp
-  static constexpr int BYTES = OFF_SCR + 8 * ROW_SCRATCH_BYTES;
+  // block-sparse unit lists, one per unit slot: header (nu, n[2], first[2],
+  // last[2]), per-key-tile flags of the two rows, then the union (act, kt)
+  static constexpr int MAXL = 1024;  // key tiles (Nk <= 131072)
+  static constexpr int LIST = SP ? (48 + 5 * MAXL + 127) / 128 * 128 : 0;
+  static constexpr int OFF_LIST = OFF_SCR + 8 * ROW_SCRATCH_BYTES;
+  static constexpr int BYTES = OFF_LIST + 2 * LIST;
   static constexpr int ALLOC = BYTES + 1024;
+  static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
+
+// A unit's key-tile list in shared memory (block-sparse).
+struct SpList {
+  int* hdr;       // [0] nu  [1..2] n[t]  [3..4] first step of t  [5..6] last step of t
+  uint8_t* a0;    // key tile c listed for query tile 0 / 1 (build scratch)
+  uint8_t* a1;
+  uint8_t* act;   // union step j: bit t set when query tile t uses it
+  int16_t* kt;    // union step j: key tile
+};
+template <int MAXL>
+__device__ __forceinline__ SpList sp_list(uint8_t* base) {
+  SpList l;
+  l.hdr = reinterpret_cast<int*>(base);
+  l.a0 = base + 48;
+  l.a1 = l.a0 + MAXL;
+  l.act = l.a1 + MAXL;
+  l.kt = reinterpret_cast<int16_t*>(l.act + MAXL);
+  return l;
+}
 
 struct FwdParams {
   Dims dims;
@@ -77,6 +109,9 @@ struct FwdParams {
   const float* sk;
   const float* sv;
   int nqt, nkt;
+  const int* row_ptr;  // block-sparse CSR table: [nqt + 1], col_idx [nnz]
+  const int* col_idx;
+  int nnz;
   OutRows o;
   OutRows o_res;
   float* lse;
@@ -88,11 +123,12 @@ struct FwdParams {
 
 struct Bars {
   uint64_t *unit_full, *unit_empty, *q_full, *q_empty, *kv_full, *kv_empty, *s_full, *p_full, *o_full, *o_empty;
+  uint64_t* list_full;  // block-sparse only
 };
 
-template <int D, bool F8>
+template <int D, bool F8, bool SP>
 __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
-  using L = FwdLayout<D, F8>;
+  using L = FwdLayout<D, F8, SP>;
   uint64_t* b = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   Bars r;
   r.unit_full = b;
@@ -105,6 +141,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   r.p_full = r.s_full + 2;
   r.o_full = r.p_full + 2;
   r.o_empty = r.o_full + 2;
+  r.list_full = r.o_empty + 2;
   return r;
 }
 
@@ -155,11 +192,12 @@ __device__ __forceinline__ UnitTiles unit_tiles(const Dims& s, int p) {
 }
 
 // ------------------------------------------------------------------ producer
-template <int D, int MASK, bool F8, bool VL>
+template <int D, int MASK, bool F8, bool VL, bool SP>
 __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, const CUtensorMap* tm_q,
                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, const FwdParams& p,
                              const Ctl& ctl) {
-  using L = FwdLayout<D, F8>;
+  using L = FwdLayout<D, F8, SP>;
+  constexpr bool SKIP = VL || SP;  // units may have no work
   const int g = p.dims.Hq / p.dims.Hkv;
   uint32_t seq = 0;       // K/V groups issued so far (ring sequence number)
   uint32_t qn = 0;        // units with work so far (Q load phase)
@@ -175,12 +213,19 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
     fwd_unit(p.dims, u, b, h, pr);
     const SeqRows sr = seq_rows<VL>(p.dims, b);
     const UnitTiles ut = unit_tiles<MASK>(VL ? sr.s : p.dims, pr);
-    const int nmax = ut.nu;
-    if (VL && nmax == 0) continue;  // both query tiles past their packed sequence
+    int nmax = ut.nu;
+    SpList sl{};
+    if (SP) {  // the unit's key tiles, from the list warp 2 built
+      if (!mbar_wait(&bar.list_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
+      sl = sp_list<L::MAXL>(smem + L::OFF_LIST + slot * L::LIST);
+      nmax = sl.hdr[0];
+    }
+    if (SKIP && nmax == 0) continue;  // no key tile for either query tile (past a packed sequence, or none listed)
     const int kvh = h / g;
     const int qrow = VL ? sr.qoff : 0, krow = VL ? sr.koff : 0, tb = VL ? 0 : b;
+    auto key_tile = [&](int step) { return SP ? static_cast<int>(sl.kt[step]) : ut.base + step; };
 
-    if (!mbar_wait(bar.q_empty, ((VL ? qn : it) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
+    if (!mbar_wait(bar.q_empty, ((SKIP ? qn : it) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
     mbar_arrive_expect_tx(bar.q_full, 2 * L::QB);
 #pragma unroll
     for (int t = 0; t < 2; ++t)
@@ -188,7 +233,7 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
       for (int c = 0; c < L::CH; ++c)
         tma_load_4d(smem + L::OFF_Q + t * L::QB + c * (TILE * 128), tm_q, bar.q_full, c * L::ECH, h,
                     qrow + (2 * pr + t) * TILE, tb);
-    q_armed = VL ? static_cast<int>(qn++) : it;
+    q_armed = SKIP ? static_cast<int>(qn++) : it;
 
     bool ok = true;
     for (int gi = 0; gi <= nmax; ++gi, ++seq) {  // group gi: V_{gi-1} (slot A), K_gi (slot B)
@@ -204,10 +249,10 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
       for (int c = 0; c < L::CH; ++c) {
         if (has_v)
           tma_load_4d(base + c * (TILE * 128), tm_v, &bar.kv_full[gs], c * L::ECH, kvh,
-                      krow + (ut.base + gi - 1) * TILE, tb);
+                      krow + key_tile(gi - 1) * TILE, tb);
         if (has_k)
           tma_load_4d(base + L::TB + c * (TILE * 128), tm_k, &bar.kv_full[gs], c * L::ECH, kvh,
-                      krow + (ut.base + gi) * TILE, tb);
+                      krow + key_tile(gi) * TILE, tb);
       }
     }
     if (!ok) break;
@@ -223,10 +268,11 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D, int MASK, bool F8, bool VL>
+template <int D, int MASK, bool F8, bool VL, bool SP>
 __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
                         const Ctl& ctl) {
-  using L = FwdLayout<D, F8>;
+  using L = FwdLayout<D, F8, SP>;
+  constexpr bool SKIP = VL || SP;
   // Q K^T with both operands K-major; P V with V N-major
   constexpr uint32_t IDESC_S = F8 ? idesc_e4m3(128, 128, false, false) : idesc_bf16(128, 128, false, false);
   constexpr uint32_t IDESC_O = F8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
@@ -273,23 +319,38 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
     const int slot = it & 1;
     if (!mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) return;
     const int u = unit_slot[slot];
-    mbar_arrive(&bar.unit_empty[slot]);
+    if (!SP || u >= p.total_units) mbar_arrive(&bar.unit_empty[slot]);  // block-sparse: after the unit
     if (u >= p.total_units) return;
     int b, h, pr;
     fwd_unit(p.dims, u, b, h, pr);
     const UnitTiles ut = unit_tiles<MASK>(VL ? seq_rows<VL>(p.dims, b).s : p.dims, pr);
-    const int nmax = ut.nu;
-    if (VL && nmax == 0) continue;  // both query tiles past their packed sequence
-    // tile t is active at local steps [a[t], e[t])
-    const int a[2] = {ut.a[0], ut.a[1]}, e[2] = {ut.a[0] + ut.n[0], ut.a[1] + ut.n[1]};
+    int nmax = ut.nu;
+    // tile t is active at local steps [a[t], e[t]) (block-sparse: the steps its bit marks)
+    int a[2] = {ut.a[0], ut.a[1]}, e[2] = {ut.a[0] + ut.n[0], ut.a[1] + ut.n[1]}, nt[2] = {ut.n[0], ut.n[1]};
+    SpList sl{};
+    if (SP) {
+      if (!mbar_wait(&bar.list_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+      sl = sp_list<L::MAXL>(smem + L::OFF_LIST + slot * L::LIST);
+      nmax = sl.hdr[0];
+      for (int t = 0; t < 2; ++t) {
+        nt[t] = sl.hdr[1 + t];
+        a[t] = sl.hdr[3 + t];
+        e[t] = sl.hdr[5 + t] + 1;
+      }
+    }
+    auto on = [&](int t, int j) { return SP ? ((sl.act[j] >> t) & 1) != 0 : (j >= a[t] && j < e[t]); };
+    if (SKIP && nmax == 0) {  // no key tile for either query tile
+      if (SP) mbar_arrive(&bar.unit_empty[slot]);
+      continue;
+    }
 
-    if (!mbar_wait(bar.q_full, (VL ? qn++ : static_cast<uint32_t>(it)) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+    if (!mbar_wait(bar.q_full, (SKIP ? qn++ : static_cast<uint32_t>(it)) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
     // group 0: K of local step 0
     {
       if (!group_wait(seq)) return;
       tc_fence_after();
       for (int t = 0; t < 2; ++t)
-        if (ut.n[t] > 0 && a[t] == 0) {
+        if (nt[t] > 0 && on(t, 0)) {
           issue_s(t, group_base(seq) + L::TB);
           mma_commit(&bar.s_full[t]);
         }
@@ -301,7 +362,8 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
       if (!group_wait(gq)) return;
       const uint32_t v_addr = group_base(gq), k_addr = v_addr + L::TB;
       for (int t = 0; t < 2; ++t) {
-        if (j >= a[t] && j < e[t]) {
+        const bool now = on(t, j);
+        if (now) {
           if (j == a[t] && !mbar_wait(&bar.o_empty[t], (active[t] & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
           if (!mbar_wait(&bar.p_full[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
           pph[t] ^= 1;
@@ -309,8 +371,8 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
           issue_pv(t, v_addr, j > a[t]);
           if (j == e[t] - 1) mma_commit(&bar.o_full[t]);
         }
-        if (j + 1 >= a[t] && j + 1 < e[t]) {  // S of the tile's next step (its first, when it starts late)
-          if (j < a[t]) tc_fence_after();       // no P V of this tile in this step fenced the group wait
+        if (j + 1 < nmax && on(t, j + 1)) {  // S of the tile's next step (its first, when it starts late)
+          if (!now) tc_fence_after();         // no P V of this tile in this step fenced the group wait
           issue_s(t, k_addr);
           mma_commit(&bar.s_full[t]);
         }
@@ -319,15 +381,17 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
       mma_commit(&bar.kv_empty[gq % L::NG]);
     }
     for (int t = 0; t < 2; ++t)
-      if (ut.n[t] > 0) ++active[t];
+      if (nt[t] > 0) ++active[t];
     seq += nmax + 1;
+    if (SP) mbar_arrive(&bar.unit_empty[slot]);
   }
 }
 
 // ------------------------------------------------------------------ softmax
-template <int D, int MASK, bool F8, bool VL>
-__device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
-                            const Ctl& ctl, uint8_t* scratch) {
+template <int D, int MASK, bool F8, bool VL, bool SP>
+__device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* unit_slot, uint32_t tmem,
+                            const FwdParams& p, const Ctl& ctl, uint8_t* scratch) {
+  using L = FwdLayout<D, F8, SP>;
   const int wq = (threadIdx.x >> 5) & 3;  // warp within the warpgroup = TMEM lane quarter
   const int r = wq * 32 + lane_id();      // row of the query tile
   const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
@@ -342,7 +406,7 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     bool ok = mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
     if (!__all_sync(0xffffffffu, ok)) return;
     const int u = unit_slot[slot];
-    warp_arrive(&bar.unit_empty[slot]);
+    if (!SP || u >= p.total_units) warp_arrive(&bar.unit_empty[slot]);  // block-sparse: after the unit
     if (u >= p.total_units) return;
     int b, h, pr;
     fwd_unit(s, u, b, h, pr);
@@ -350,11 +414,37 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
     if (VL && !sr.ok && t == 0 && wq == 0 && lane_id() == 0) report(ctl, FA_STATUS_BAD_INPUT);
     const Dims& su = VL ? sr.s : s;  // this unit's sequence (packed), else the problem
     const UnitTiles ut = unit_tiles<MASK>(su, pr);
-    const int n = ut.n[t];
+    int n = ut.n[t];
+    const int qt = 2 * pr + t;
+    SpList sl{};
+    if (SP) {
+      ok = mbar_wait(&bar.list_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
+      if (!__all_sync(0xffffffffu, ok)) return;
+      sl = sp_list<L::MAXL>(smem + L::OFF_LIST + slot * L::LIST);
+      n = sl.hdr[1 + t];
+      if (n == 0 && qt < q_tiles(s)) {  // no key tile listed: O = 0, LSE = -inf
+        const int q0 = qt * TILE + wq * 32;
+        __nv_bfloat16* o0 = reinterpret_cast<__nv_bfloat16*>(p.o.ptr) + b * p.o.sb +
+                            static_cast<int64_t>(q0) * p.o.sn + h * p.o.sh;
+        uint32_t zw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) zw[i] = 0u;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) store_rows32_bf16(zw, scratch, o0 + cc * 32, p.o.sn, s.Nq - q0);
+        if (p.o_res.ptr != nullptr) {
+          __nv_bfloat16* r0 = reinterpret_cast<__nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
+                              static_cast<int64_t>(q0) * p.o_res.sn + h * p.o_res.sh;
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) store_rows32_bf16(zw, scratch, r0 + cc * 32, p.o_res.sn, s.Nq - q0);
+        }
+        if (qt * TILE + r < s.Nq) p.lse[(static_cast<int64_t>(b) * s.Hq + h) * s.Nq + qt * TILE + r] = -INFINITY;
+      }
+      if (n == 0) warp_arrive(&bar.unit_empty[slot]);
+    }
     if (n == 0) continue;
     const int nq_u = su.Nq, nk_u = su.Nk, qoff = VL ? sr.qoff : 0;
-    const int qt = 2 * pr + t;
     const int q_row = qt * TILE + r;
+    int jj = 0;  // block-sparse: scan position in the unit's list
     const int kt0 = ut.base + ut.a[t];  // first key tile of this query tile
     // FP8: logits = S * scale*log2(e) * s_q * s_k[kt]; a zero block scale leaves S = 0
     // exactly, and the floor keeps masked -inf scores from becoming NaN
@@ -381,7 +471,17 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
       float sv[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) sv[i] = __uint_as_float(sr[i]);
-      if (MASK == MASK_BAND) {
+      if (SP) {  // this step's key tile: the next list entry marked for this query tile
+        while (((sl.act[jj] >> t) & 1) == 0) ++jj;
+        const int kt = sl.kt[jj++];
+        if ((MASK == MASK_CAUSAL && kt == qt) || (kt == k_tiles(s) - 1 && (nk_u % TILE) != 0)) {
+          int lim = nk_u - kt * TILE;  // keys at or past Nk, and under j <= i keys past the row
+          if (MASK == MASK_CAUSAL) lim = imin(lim, q_row - kt * TILE + 1);
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) sv[i] = -INFINITY;
+        }
+      } else if (MASK == MASK_BAND) {
         const int kt = kt0 + j;
         if (kt < full_lo || kt > full_hi) {
           // keys [lo, hi) of this tile are visible to the row: the band i - wl .. i + wr, below Nk
@@ -503,17 +603,108 @@ __device__ void fwd_softmax(int t, const Bars& bar, const int* unit_slot, uint32
             q_row] = (m_run + __log2f(l_run) - (F8 ? LOG2_448 : 0.f)) * LN2;
     tc_fence_before();
     warp_arrive(&bar.o_empty[t]);
+    if (SP) warp_arrive(&bar.unit_empty[slot]);
   }
 }
 
-template <int D, int MASK, bool F8, bool VL>
+// ------------------------------------------------------------------ block-sparse lists (warp 2)
+// For each unit: mark the key tiles each of its two query tiles lists (entries
+// must increase strictly within a row and lie below k_tiles; others are skipped
+// and reported; under j <= i tiles above the diagonal hide every key and are
+// skipped), then compact the marks into the union in key order.
+template <int D, int MASK>
+__device__ void fwd_sparse_lists(uint8_t* smem, const Bars& bar, const int* unit_slot, const FwdParams& p,
+                                 const Ctl& ctl) {
+  using L = FwdLayout<D, false, true>;
+  const int lane = lane_id();
+  const Dims& s = p.dims;
+  const int nqt = q_tiles(s), nkt = k_tiles(s);
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    const bool ok = mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    const int u = unit_slot[slot];
+    warp_arrive(&bar.unit_empty[slot]);
+    if (u >= p.total_units) return;
+    int b, h, pr;
+    fwd_unit(s, u, b, h, pr);
+    const SpList sl = sp_list<L::MAXL>(smem + L::OFF_LIST + slot * L::LIST);
+    for (int c = lane; c < nkt; c += 32) {
+      sl.a0[c] = 0;
+      sl.a1[c] = 0;
+    }
+    __syncwarp();
+    bool bad = false;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int qt = 2 * pr + t;
+      if (qt >= nqt) continue;
+      const int e0 = __ldg(p.row_ptr + qt), e1 = __ldg(p.row_ptr + qt + 1);
+      if (e0 < 0 || e1 < e0 || e1 > p.nnz) {
+        bad = true;
+        continue;
+      }
+      uint8_t* mark = t ? sl.a1 : sl.a0;
+      for (int e = e0 + lane; e < e1; e += 32) {
+        const int c = __ldg(p.col_idx + e);
+        const int prev = e > e0 ? __ldg(p.col_idx + e - 1) : -1;
+        if (c <= prev || c < 0 || c >= nkt) {
+          bad = true;
+          continue;
+        }
+        if (MASK == MASK_CAUSAL && c > qt) continue;
+        mark[c] = 1;
+      }
+    }
+    __syncwarp();
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report(ctl, FA_STATUS_BAD_INPUT);
+    int nu = 0, n0 = 0, n1 = 0, f0 = -1, f1 = -1, l0 = -1, l1 = -1;
+    for (int base = 0; base < nkt; base += 32) {
+      const int c = base + lane;
+      const int x0 = c < nkt ? sl.a0[c] : 0, x1 = c < nkt ? sl.a1[c] : 0;
+      const unsigned m = __ballot_sync(0xffffffffu, x0 | x1);
+      const unsigned m0 = __ballot_sync(0xffffffffu, x0), m1 = __ballot_sync(0xffffffffu, x1);
+      const unsigned below = (1u << lane) - 1u;
+      if (x0 | x1) {
+        const int pos = nu + __popc(m & below);
+        sl.kt[pos] = static_cast<int16_t>(c);
+        sl.act[pos] = static_cast<uint8_t>(x0 | (x1 << 1));
+      }
+      // union positions of each query tile's first and last key tile
+      if (m0) {
+        if (f0 < 0) f0 = nu + __popc(m & ((1u << (__ffs(m0) - 1)) - 1u));
+        l0 = nu + __popc(m & ((1u << (31 - __clz(m0))) - 1u));
+      }
+      if (m1) {
+        if (f1 < 0) f1 = nu + __popc(m & ((1u << (__ffs(m1) - 1)) - 1u));
+        l1 = nu + __popc(m & ((1u << (31 - __clz(m1))) - 1u));
+      }
+      nu += __popc(m);
+      n0 += __popc(m0);
+      n1 += __popc(m1);
+    }
+    if (lane == 0) {
+      sl.hdr[0] = nu;
+      sl.hdr[1] = n0;
+      sl.hdr[2] = n1;
+      sl.hdr[3] = f0;
+      sl.hdr[4] = f1;
+      sl.hdr[5] = l0;
+      sl.hdr[6] = l1;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar.list_full[slot]);
+  }
+}
+
+template <int D, int MASK, bool F8, bool VL, bool SP>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using L = FwdLayout<D, F8>;
+  using L = FwdLayout<D, F8, SP>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Bars bar = carve_bars<D, F8>(smem);
+  const Bars bar = carve_bars<D, F8, SP>(smem);
   int* unit_slot = reinterpret_cast<int*>(smem + L::OFF_UNIT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
   const int warp = threadIdx.x >> 5;
@@ -522,8 +713,12 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bar.unit_full[0], 1);
     mbar_init(&bar.unit_full[1], 1);
-    mbar_init(&bar.unit_empty[0], 1 + 8);
-    mbar_init(&bar.unit_empty[1], 1 + 8);
+    mbar_init(&bar.unit_empty[0], 1 + 8 + (SP ? 1 : 0));  // MMA, softmax warps (, list warp)
+    mbar_init(&bar.unit_empty[1], 1 + 8 + (SP ? 1 : 0));
+    if (SP) {
+      mbar_init(&bar.list_full[0], 1);
+      mbar_init(&bar.list_full[1], 1);
+    }
     mbar_init(bar.q_full, 1);
     mbar_init(bar.q_empty, 1);
     for (int s = 0; s < L::STAGES; ++s) {
@@ -548,11 +743,13 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane_id() == 0) fwd_producer<D, MASK, F8, VL>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
+    if (lane_id() == 0) fwd_producer<D, MASK, F8, VL, SP>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
   } else if (warp == 1) {
-    if (lane_id() == 0) fwd_mma<D, MASK, F8, VL>(smem, bar, unit_slot, tmem, p, ctl);
+    if (lane_id() == 0) fwd_mma<D, MASK, F8, VL, SP>(smem, bar, unit_slot, tmem, p, ctl);
+  } else if (SP && warp == 2) {
+    fwd_sparse_lists<D, MASK>(smem, bar, unit_slot, p, ctl);
   } else if (warp >= 4) {
-    fwd_softmax<D, MASK, F8, VL>((warp - 4) >> 2, bar, unit_slot, tmem, p, ctl,
+    fwd_softmax<D, MASK, F8, VL, SP>((warp - 4) >> 2, smem, bar, unit_slot, tmem, p, ctl,
                            smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES);
   }
   tc_fence_before();
@@ -563,10 +760,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, int MASK, bool F8 = false, bool VL = false>
+template <int D, int MASK, bool F8 = false, bool VL = false, bool SP = false>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
-  using L = FwdLayout<D, F8>;
-  auto kern = fa_fwd_kernel<D, MASK, F8, VL>;
+  using L = FwdLayout<D, F8, SP>;
+  auto kern = fa_fwd_kernel<D, MASK, F8, VL, SP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   FwdParams p;
@@ -577,6 +774,9 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   p.sv = a.sv;
   p.nqt = q_tiles(a.dims);
   p.nkt = k_tiles(a.dims);
+  p.row_ptr = a.row_ptr;
+  p.col_idx = a.col_idx;
+  p.nnz = a.nnz;
   p.o = a.o;
   p.o_res = a.o_res;
   p.lse = a.lse;
@@ -593,6 +793,15 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
   const int m = mask_kind(a.dims);
+  if (a.row_ptr != nullptr) {  // block-sparse: bf16, dense batch, no band
+    if (a.sq != nullptr || a.dims.cu_q != nullptr || m == MASK_BAND) return cudaErrorInvalidValue;
+    if (k_tiles(a.dims) > FwdLayout<128, false, true>::MAXL) return cudaErrorInvalidValue;
+    if (a.d == 64)
+      return m == MASK_CAUSAL ? launch_fwd_t<64, MASK_CAUSAL, false, false, true>(a, st)
+                              : launch_fwd_t<64, MASK_NONE, false, false, true>(a, st);
+    return m == MASK_CAUSAL ? launch_fwd_t<128, MASK_CAUSAL, false, false, true>(a, st)
+                            : launch_fwd_t<128, MASK_NONE, false, false, true>(a, st);
+  }
   if (a.dims.cu_q != nullptr) {  // packed sequences: bf16, no band
     if (a.sq != nullptr || m == MASK_BAND) return cudaErrorInvalidValue;
     if (a.d == 64)

@@ -32,6 +32,10 @@ struct FwdLaunch {
   const float* sq;
   const float* sk;
   const float* sv;
+  // block-sparse (row_ptr != nullptr): CSR table of key tiles per query tile
+  const int* row_ptr;  // [ceil(Nq/128) + 1]
+  const int* col_idx;  // [nnz]
+  int nnz;
 };
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
 

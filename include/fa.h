@@ -110,6 +110,24 @@ int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
            void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Block-sparse forward ("第18章" §18.8.1): a CSR table over 128-row query tiles
+ * lists the 128-key tiles each one attends to; the kernel loads and computes
+ * only those (the inner loop runs over the list).  row_ptr: device int32
+ * [ceil(Nq/128) + 1], from 0, non-decreasing, ending at nnz; col_idx: device
+ * int32 [nnz], strictly increasing within each row, each below ceil(Nk/128).
+ * Key j is visible to query i iff j's tile is listed for i's tile (and, causal,
+ * j <= i).  Rows that see no key get O = 0 (and a zero residual) and LSE =
+ * -inf.  One table serves every batch entry and head.  Entries that break the
+ * rules are skipped and reported through the workspace status
+ * (fa_get_device_status -> FA_ERR_INVALID).  Nk <= 131072; no window; other
+ * arguments and the workspace as fa_fwd.
+ * ------------------------------------------------------------------------- */
+int fa_fwd_blocksparse(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* row_ptr,
+                       const int* col_idx, int nnz, const fa_tensor_t* o, float* lse,
+                       const fa_tensor_t* o_residual, const fa_shape_t* shape, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Packed variable-length sequences ("第18章" §18.7.1, flash_attn_varlen_func):
  * the B sequences of a batch lie one after another along the token axis,
  * q [total_q, Hq, d], k, v [total_k, Hkv, d] (the fa_tensor_t's stride_b is

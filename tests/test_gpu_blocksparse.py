@@ -1,0 +1,132 @@
+"""GPU parity of the block-sparse forward against the fp64 oracle, through
+fa_fwd_blocksparse.
+
+Covers random tables over ragged shapes (causal and not, grouped heads, d = 64
+and 128, rows with no listed tile), every tile listed against the dense kernel
+(bit for bit), a sliding-window + global-token pattern at N = 8192 on sampled
+query tiles, the residual, and tables that break the rules (reported)."""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_21_gb300 as fa
+from exact_io_aware_21_gb300 import inputs
+from oracle import attention as A
+from parity import assert_fwd, f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fa.library().fa_set_wait_timeout_ns(10_000_000_000)
+
+
+def csr(M):
+    rows = [np.flatnonzero(r) for r in M]
+    rp = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+    ci = np.concatenate(rows).astype(np.int32) if sum(len(r) for r in rows) else np.zeros(0, np.int32)
+    return rp, ci
+
+
+def run(x, M, causal, scale, residual=False):
+    rp, ci = csr(M)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    out = fa.forward_blocksparse(q, k, v, torch.from_numpy(rp).to(DEV), torch.from_numpy(ci).to(DEV),
+                                 causal=causal, scale=scale, residual=residual)
+    torch.cuda.synchronize()
+    return out, rp, ci
+
+
+CASES = [  # B, Hq, Hkv, Nq, Nk, d, causal, density
+    (1, 2, 1, 640, 900, 64, False, 0.4),
+    (2, 4, 2, 1000, 1000, 128, True, 0.5),
+    (1, 2, 2, 384, 384, 128, False, 0.3),
+    (1, 8, 2, 2048, 2048, 128, True, 0.25),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal,density", CASES)
+def test_random_tables(B, Hq, Hkv, Nq, Nk, d, causal, density):
+    g = np.random.default_rng(Nq + Nk + d)
+    nqt, nkt = -(-Nq // 128), -(-Nk // 128)
+    M = g.random((nqt, nkt)) < density
+    M[np.arange(nqt), np.arange(nqt) % nkt] = True              # every query tile lists a tile ...
+    M[1] = False                                               # ... but one
+    x = inputs.shape_inputs(B, Hq, Hkv, Nq, Nk, d, seed=Nq + d, with_do=False)
+    scale = 1 / np.sqrt(d)
+    (o, lse), rp, ci = run(x, M, causal, scale)
+    o_ref, lse_ref = A.attention_blocksparse_forward(x["q"], x["k"], x["v"], rp, ci, scale, causal)
+    seen = np.isfinite(lse_ref[0, 0])
+    tag = f"blocksparse {B}x{Hq}/{Hkv} {Nq}x{Nk} d={d} causal={causal}"
+    assert_fwd(o[:, seen], lse[:, :, seen], o_ref[:, seen], lse_ref[:, :, seen], tag)
+    assert not f64(o[:, ~seen]).any() and np.all(np.isneginf(f64(lse[:, :, ~seen]))), tag
+
+
+@pytest.mark.parametrize("causal,d", [(False, 64), (True, 128)])
+def test_every_tile_listed_equals_the_dense_kernel(causal, d):
+    N = 1000
+    x = inputs.shape_inputs(2, 4, 2, N, N, d, seed=3, with_do=False)
+    nt = -(-N // 128)
+    (o, lse, res), _, _ = run(x, np.ones((nt, nt), bool), causal, 0.1, residual=True)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    o2, lse2, res2 = fa.forward(q, k, v, causal=causal, scale=0.1, residual=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2) and torch.equal(res, res2)
+
+
+@pytest.mark.slow
+def test_window_plus_global_pattern_sampled():
+    """Each query tile lists its own tile, the two before it and tile 0 (a global
+    prefix); causal; GQA 32/8 at N = 8192."""
+    N, d = 8192, 128
+    nt = N // 128
+    M = np.zeros((nt, nt), bool)
+    for i in range(nt):
+        M[i, max(0, i - 2):i + 1] = True
+        M[i, 0] = True
+    w = inputs.Workload("bs", 1, 32, 8, N, N, d, True, seed=5)
+    x = inputs.make(w, device=DEV, with_do=False)
+    rp, ci = csr(M)
+    o, lse = fa.forward_blocksparse(x["q"], x["k"], x["v"], torch.from_numpy(rp).to(DEV),
+                                    torch.from_numpy(ci).to(DEV), causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    q, k, v = (x[n][:, :, :].cpu() for n in ("q", "k", "v"))
+    for qt in (0, 1, 37, nt - 1):
+        rows = np.arange(qt * 128, (qt + 1) * 128)
+        keys = np.concatenate([np.arange(j * 128, (j + 1) * 128) for j in np.flatnonzero(M[qt])])
+        for h in (0, 13, 31):
+            kv = h // 4
+            qq, kk, vv = q[:, rows, h:h + 1], k[:, keys, kv:kv + 1], v[:, keys, kv:kv + 1]
+            # causal within the gathered keys: key keys[j] visible to row rows[i] iff keys[j] <= rows[i]
+            S = (f64(qq)[0, :, 0] @ f64(kk)[0, :, 0].T) * w.scale
+            S = np.where(keys[None, :] <= rows[:, None], S, -np.inf)
+            m = S.max(axis=1, keepdims=True)
+            E = np.exp(S - m)
+            o_ref = (E @ f64(vv)[0, :, 0]) / E.sum(axis=1, keepdims=True)
+            lse_ref = m[:, 0] + np.log(E.sum(axis=1))
+            assert_fwd(o[0, rows, h], lse[0, h, rows], o_ref, lse_ref, f"tile {qt} head {h}")
+
+
+@pytest.mark.parametrize("table", ["decreasing", "out_of_range", "row_ptr_past_nnz"])
+def test_tables_that_break_the_rules_are_reported(table):
+    N = 384
+    x = inputs.shape_inputs(1, 2, 2, N, N, 64, seed=1, with_do=False)
+    rp = np.array([0, 2, 3, 4], np.int32)
+    ci = np.array([0, 1, 1, 2], np.int32)
+    if table == "decreasing":
+        ci = np.array([1, 0, 1, 2], np.int32)
+    elif table == "out_of_range":
+        ci = np.array([0, 3, 1, 2], np.int32)
+    else:
+        rp = np.array([0, 2, 3, 9], np.int32)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    s = fa.binding._dims(q, k, None, False)
+    o = torch.zeros_like(q)
+    lse = torch.zeros((1, 2, N), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(fa.library().fa_fwd_workspace_size(fa.binding.ctypes.byref(s)), dtype=torch.uint8, device=DEV)
+    fa.fa_fwd_blocksparse(q, k, v, torch.from_numpy(rp).to(DEV), torch.from_numpy(ci).to(DEV), o, lse, s, ws)
+    rc, st = fa.binding.device_status(ws)
+    assert rc == 1 and st == 0x100

@@ -14,6 +14,9 @@ in HBM:
   varlen leg     forward + backward of 24 packed sequences of long-tailed
                  lengths (32768 tokens, GQA 32/8, d=128, causal) through
                  fa_fwd_varlen / fa_bwd_varlen
+  blocksparse    forward of blocksparse_causal_b1_hq32_hkv8_n16384_d128_local8_global1
+                 through fa_fwd_blocksparse (each query tile: its own key tile, the
+                 seven before it and tile 0)
   fp8 leg        E4M3 quantisation (Q, K per 128-row block after the random
                  Hadamard rotation, V per head) and the FP8 forward of the GQA
                  workload
@@ -56,12 +59,14 @@ PAGED = ("decode_b8_hq32_hkv8_q1_kv131072_d128", 16)  # the q1 decode cache in s
 PAGED_NAME = PAGED[0] + "_paged16"
 WINDOW = ("window_causal_b1_hq32_hkv8_n16384_w4096_d128",)
 VARLEN = "varlen_causal_b24_hq32_hkv8_total32768_d128"
+BLOCKSPARSE = "blocksparse_causal_b1_hq32_hkv8_n16384_d128_local8_global1"
 FP8 = "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers"  # the FP8 leg runs this workload
 FP8_NAME = FP8 + "_fp8_hadamard"
 FP8_TENSOR_RATIO = 2.0  # nominal dense E4M3 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 WORKLOAD = (" + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode); " + PAGED_NAME +
             " (paged decode); " + " + ".join(WINDOW) + " (sliding-window fwd+bwd); " + VARLEN +
-            " (packed variable-length fwd+bwd); " + FP8_NAME + " (FP8 quantise + fwd)")
+            " (packed variable-length fwd+bwd); " + BLOCKSPARSE + " (block-sparse fwd); " + FP8_NAME +
+            " (FP8 quantise + fwd)")
 METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -94,7 +99,19 @@ def varlen_lens(w):
     return inputs.varlen_lengths(w.extra["n_seqs"], w.Nq, seed=w.seed)
 
 
+def blocksparse_table(w):
+    from exact_io_aware_21_gb300 import inputs
+
+    return inputs.local_global_tiles(-(-w.Nq // 128), w.extra["local_tiles"], w.extra["global_tiles"])
+
+
 def fwd_flops(w):
+    if "local_tiles" in w.extra:  # block-sparse, causal: listed tiles below the diagonal in full, diagonal halves
+        M = blocksparse_table(w)
+        nt = len(M)
+        below = sum(sum(1 for j in range(i) if M[i][j]) for i in range(nt))
+        pairs = below * 128 * 128 + nt * 128 * 129 // 2
+        return 4.0 * w.B * w.Hq * w.d * pairs
     if "n_seqs" in w.extra:  # packed sequences: each its own (causal) attention
         f = sum(4.0 * w.Hq * n * n * w.d for n in varlen_lens(w))
         return f / 2 if w.causal else f
@@ -301,7 +318,7 @@ class Leg:
         self.ms = {k: 0.0 for k, _ in fns}
 
 
-KERNELS_PER_CALL = {"fwd": 1, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
+KERNELS_PER_CALL = {"fwd_bs": 1, "fwd": 1, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
                     "quant_v": 2, "fwd_fp8": 1, "fwd_varlen": 1, "bwd_varlen": 3}
 
 
@@ -396,6 +413,24 @@ def make_legs(device, seed):
                         st["dq"], st["dk"], st["dv"], st["s"], st["wsb"], st["ores"])
 
     legs.append(Leg(VARLEN, "varlen", w, [("fwd_varlen", vfwd), ("bwd_varlen", vbwd)], 3.5 * fwd_flops(w)))
+
+    w = by[BLOCKSPARSE]
+    x = inputs.make(w, device=device, with_do=False, seed=w.seed + seed)
+    M = blocksparse_table(w)
+    rows = [[j for j, on in enumerate(r) if on] for r in M]
+    rp = torch.tensor([0] + list(itertools.accumulate(len(r) for r in rows)), dtype=torch.int32, device=device)
+    ci = torch.tensor([j for r in rows for j in r], dtype=torch.int32, device=device)
+    s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal)
+    st = dict(x=x, s=s, rp=rp, ci=ci, o=torch.empty_like(x["q"]),
+              lse=torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=device),
+              wsf=torch.zeros(lib.fa_fwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=device))
+    state[BLOCKSPARSE] = st
+
+    def bsfwd(st=st):
+        x = st["x"]
+        B.fa_fwd_blocksparse(x["q"], x["k"], x["v"], st["rp"], st["ci"], st["o"], st["lse"], st["s"], st["wsf"])
+
+    legs.append(Leg(BLOCKSPARSE, "blocksparse", w, [("fwd_bs", bsfwd)], fwd_flops(w)))
 
     w = {x.name: x for x in train}[FP8]
     x = inputs.make(w, device=device, with_do=False, seed=w.seed + seed)
@@ -598,6 +633,12 @@ def run_ours(args):
                 "bwd_frac_of_sustained_peak": 2.5 * f / l.ms["bwd_varlen"] / 1e9 / sus,
                 "lens": varlen_lens(l.w), "in_step": False,
                 "flops_count": "per sequence 4*H*L^2*d, halved (causal), x3.5 fwd+bwd"}
+        elif l.kind == "blocksparse":
+            f = fwd_flops(l.w)
+            legs_out[l.name] = {"fwd_ms": l.ms["fwd_bs"], "fwd_tflops": f / l.ms["fwd_bs"] / 1e9,
+                                "fwd_frac_of_sustained_peak": f / l.ms["fwd_bs"] / 1e9 / sus,
+                                "tiles_listed": sum(sum(r) for r in blocksparse_table(l.w)), "in_step": False,
+                                "flops_count": "4*B*H*d per visible (query, key) pair"}
         elif l.kind == "fp8":
             f = fwd_flops(l.w)
             qb = {"quant_q": (l.w.Hq, l.w.Nq), "quant_k": (l.w.Hkv, l.w.Nk), "quant_v": (l.w.Hkv, l.w.Nk)}

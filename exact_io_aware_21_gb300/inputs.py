@@ -59,8 +59,19 @@ WINDOW_N16384_W4096 = Workload("window_causal_b1_hq32_hkv8_n16384_w4096_d128", 1
 VARLEN_T32768_D128 = Workload("varlen_causal_b24_hq32_hkv8_total32768_d128", 1, 32, 8, 32768, 32768, 128, True,
                               extra={"n_seqs": 24})
 
+# Block-sparse: each 128-row query tile lists its own key tile, the seven before it
+# and tile 0 (a local window plus a global prefix), causal.
+BLOCKSPARSE_N16384 = Workload("blocksparse_causal_b1_hq32_hkv8_n16384_d128_local8_global1", 1, 32, 8, 16384, 16384,
+                              128, True, extra={"local_tiles": 8, "global_tiles": 1})
+
 ALL = [TINY, MHA_N2048_D64, CAUSAL_N4096_D128, GQA_N8192_D128, DECODE_Q1, DECODE_Q4, WINDOW_N16384_W4096,
-       VARLEN_T32768_D128]
+       VARLEN_T32768_D128, BLOCKSPARSE_N16384]
+
+
+def local_global_tiles(n_tiles, local, glob):
+    """Block table of the local + global pattern: query tile i lists key tiles
+    max(0, i - local + 1) .. i and 0 .. glob - 1 (as a [n_tiles, n_tiles] bool list of lists)."""
+    return [[(i - local < j <= i) or (j < glob and j <= i) for j in range(n_tiles)] for i in range(n_tiles)]
 
 
 def varlen_lengths(n_seqs, total, lo=64, hi=8192, seed=0):

@@ -38,3 +38,14 @@ def test_varlen_leg_lengths_and_flops():
     assert len(lens) == 24 and sum(lens) == w.Nq and min(lens) >= 64 and max(lens) <= 8192
     assert lens == inputs.varlen_lengths(24, w.Nq, seed=w.seed)          # seeded: the same every call
     assert bench.fwd_flops(w) == sum(2.0 * w.Hq * n * n * w.d for n in lens)   # causal: half of 4*H*n^2*d
+
+
+def test_blocksparse_leg_counts_visible_pairs():
+    w = inputs.Workload("bs", 1, 2, 2, 1280, 1280, 64, True, extra={"local_tiles": 3, "global_tiles": 1})
+    M = np.array(bench.blocksparse_table(w))
+    rows = [np.flatnonzero(r) for r in M]
+    rp = np.concatenate([[0], np.cumsum([len(r) for r in rows])])
+    vis = np.repeat(np.repeat(A.block_mask_from_csr(rp, np.concatenate(rows), 10, 10), 128, 0), 128, 1)
+    vis &= ~A.causal_mask(np.arange(1280), 1280)
+    assert bench.fwd_flops(w) == 4.0 * 2 * 64 * vis.sum()
+    assert M[5].tolist() == [True, False, False, True, True, True, False, False, False, False]

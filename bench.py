@@ -397,7 +397,8 @@ def make_legs(device, seed):
     st = dict(x=packed, cu=cu, s=s, mx=max(lens), o=torch.empty_like(packed["q"]), ores=torch.empty_like(packed["q"]),
               lse=torch.empty((w.Hq, w.Nq), dtype=torch.float32, device=device),
               dq=torch.empty_like(packed["q"]), dk=torch.empty_like(packed["k"]), dv=torch.empty_like(packed["v"]),
-              wsf=torch.zeros(lib.fa_fwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=device),
+              wsf=torch.zeros(lib.fa_fwd_varlen_workspace_size(ctypes.byref(s), max(lens)), dtype=torch.uint8,
+                              device=device),
               wsb=torch.zeros(lib.fa_bwd_varlen_workspace_size(ctypes.byref(s), max(lens)), dtype=torch.uint8,
                               device=device))
     state[VARLEN] = st

@@ -72,6 +72,7 @@ SIGNATURES = {
     "fa_decode_split_range": (_I, [_PS, _I, _I, _PI, _PI]),
     "fa_selftest_mma": (_I, [_I, _I, _VP, _VP, _VP, _VP, _VP]),
     "fa_fwd_blocksparse": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _PT, _VP, _PT, _PS, _VP, _SZ, _VP]),
+    "fa_fwd_varlen_workspace_size": (_SZ, [_PS, _I]),
     "fa_fwd_varlen": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _I, _PT, _VP, _PT, _PS, _VP, _SZ, _VP]),
     "fa_bwd_varlen_workspace_size": (_SZ, [_PS, _I]),
     "fa_bwd_varlen": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _I, _PT, _VP, _PT, _PT, _PT, _PT, _PT, _PS, _VP, _SZ, _VP]),
@@ -349,7 +350,7 @@ def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((s.Hq, s.Nq), dtype=torch.float32, device=q.device)
     res = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
-    ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q.device)
+    ws = _ws(library().fa_fwd_varlen_workspace_size(ctypes.byref(s), int(max_seqlen_q)), q.device)
     fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, o, lse, s, ws, res)
     return (o, lse, res) if residual else (o, lse)
 

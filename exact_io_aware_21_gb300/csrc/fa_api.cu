@@ -328,6 +328,12 @@ struct Sparse {
   int nnz;
 };
 
+// Workspace of the packed forward: the header, then the device-side work plan.
+size_t fwd_varlen_ws_bytes(const fa_shape_t* s, int max_q) {
+  const int levels = cdiv(cdiv(max_q, TILE), 2);
+  return FA_WS_HEADER_BYTES + round_up(static_cast<size_t>(varlen_plan_ints(levels, s->B)) * sizeof(int), 256);
+}
+
 int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
              const fa_tensor_t* o_res, const fa_shape_t* s, const Packed* pk, void* ws, size_t ws_bytes,
              void* stream, const Sparse* sp = nullptr) {
@@ -336,7 +342,7 @@ int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, c
       (rc = check_tensor(v)) || (rc = check_tensor(o)) || (o_res && (rc = check_tensor(o_res))))
     return rc;
   if (!lse) return FA_ERR_INVALID;
-  if ((rc = check_ws(ws, ws_bytes, fa_fwd_workspace_size(s)))) return rc;
+  if ((rc = check_ws(ws, ws_bytes, pk ? fwd_varlen_ws_bytes(s, pk->max_q) : fa_fwd_workspace_size(s)))) return rc;
   int sms = 0;
   if ((rc = device_info(&sms))) return rc;
   FwdLaunch a;
@@ -354,6 +360,7 @@ int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, c
     a.col_idx = sp->col_idx;
     a.nnz = sp->nnz;
   }
+  if (pk) a.plan = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_HEADER_BYTES);
   a.lse = lse;
   a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
   a.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_COUNTER_OFFSET);
@@ -367,6 +374,11 @@ int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, c
 int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
            const fa_tensor_t* o_res, const fa_shape_t* s, void* ws, size_t ws_bytes, void* stream) {
   return fwd_impl(q, k, v, o, lse, o_res, s, nullptr, ws, ws_bytes, stream);
+}
+
+size_t fa_fwd_varlen_workspace_size(const fa_shape_t* s, int max_seqlen_q) {
+  if (check_shape(s) != FA_OK || max_seqlen_q < 1 || max_seqlen_q > s->Nq) return 0;
+  return fwd_varlen_ws_bytes(s, max_seqlen_q);
 }
 
 int fa_fwd_blocksparse(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* row_ptr,
@@ -474,9 +486,16 @@ size_t fa_bwd_workspace_size(const fa_shape_t* s) {
   return bwd_ws_bytes(s, s->Nq);
 }
 
+// The packed backward adds the device-side work plans of its dQ and dK/dV
+// kernels (the latter sized by the packed key count, a bound on the longest).
+size_t bwd_plan_bytes(const fa_shape_t* s, int max_q) {
+  return round_up(static_cast<size_t>(varlen_plan_ints(cdiv(max_q, TILE), s->B)) * sizeof(int), 256) +
+         round_up(static_cast<size_t>(varlen_plan_ints(cdiv(s->Nk, TILE), s->B)) * sizeof(int), 256);
+}
+
 size_t fa_bwd_varlen_workspace_size(const fa_shape_t* s, int max_seqlen_q) {
   if (check_shape(s) != FA_OK || max_seqlen_q < 1 || max_seqlen_q > s->Nq) return 0;
-  return bwd_ws_bytes(s, max_seqlen_q);
+  return bwd_ws_bytes(s, max_seqlen_q) + bwd_plan_bytes(s, max_seqlen_q);
 }
 
 static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v,
@@ -491,7 +510,7 @@ static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const
     return rc;
   if (!lse) return FA_ERR_INVALID;
   const int nq_rows = pk ? pk->max_q : s->Nq;
-  if ((rc = check_ws(ws, ws_bytes, bwd_ws_bytes(s, nq_rows)))) return rc;
+  if ((rc = check_ws(ws, ws_bytes, bwd_ws_bytes(s, nq_rows) + (pk ? bwd_plan_bytes(s, pk->max_q) : 0)))) return rc;
   int sms = 0;
   if ((rc = device_info(&sms))) return rc;
   BwdLaunch a;
@@ -514,6 +533,12 @@ static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const
   char* base = static_cast<char*>(ws);
   a.neg_lse2 = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES);
   a.neg_delta = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES + round_up(rows * sizeof(float), 256));
+  if (pk) {
+    char* plans = base + bwd_ws_bytes(s, nq_rows);
+    a.plan_dq = reinterpret_cast<int*>(plans);
+    a.plan_dkdv = reinterpret_cast<int*>(
+        plans + round_up(static_cast<size_t>(varlen_plan_ints(cdiv(pk->max_q, TILE), s->B)) * sizeof(int), 256));
+  }
   a.status = reinterpret_cast<int*>(base + FA_WS_STATUS_OFFSET);
   a.counters = reinterpret_cast<int*>(base + FA_WS_COUNTER_OFFSET);
   a.timeout_ns = g_timeout_ns;

@@ -58,6 +58,7 @@ struct BwdParams {
   int* counter;
   unsigned long long timeout_ns;
   int total_units;
+  const int* plan;  // packed sequences: the kernel's device-side work plan (units with work only)
 };
 
 // ================================================================== preprocess
@@ -244,10 +245,18 @@ __device__ __forceinline__ void dq_kv_range(const Dims& s, int qt, int& lo, int&
 // The query tiles visiting key tile kt: a band's range, or under j <= i (where
 // Nq == Nk) the suffix from the diagonal tile.
 template <int MASK, bool VL>
-__device__ __forceinline__ DkvUnit dkv_decode(const Dims& s, int u) {
+__device__ __forceinline__ DkvUnit dkv_decode(const BwdParams& p, int u) {
+  const Dims& s = p.dims;
   DkvUnit r;
-  dkdv_unit(s, u, r.b, r.kvh, r.kt);
-  r.sr = seq_rows<VL>(s, r.b);
+  if (VL) {  // plan level m = the key tile counted from the sequence's end
+    int m;
+    plan_unit(p.plan, s.Hkv, u, r.b, r.kvh, m);
+    r.sr = seq_rows<VL>(s, r.b);
+    r.kt = k_tiles(r.sr.s) - 1 - m;
+  } else {
+    dkdv_unit(s, u, r.b, r.kvh, r.kt);
+    r.sr = seq_rows<VL>(s, r.b);
+  }
   const Dims& su = r.sr.s;
   int qhi = q_tiles(su);
   if (MASK == MASK_BAND)
@@ -276,6 +285,7 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const Ctl ctl{p.status, p.timeout_ns};
   const Dims& s = p.dims;
+  const int total = VL ? __ldg(p.plan) : p.total_units;  // units (packed sequences: from the plan)
   const int g = s.Hq / s.Hkv;
 
   if (threadIdx.x == 0) {
@@ -312,8 +322,8 @@ __global__ void __launch_bounds__(384, 1)
         const int u = atomicAdd(p.counter, 1);
         unit_slot[slot] = u;
         mbar_arrive(&bar.unit_full[slot]);
-        if (u >= p.total_units) break;
-        const DkvUnit w = dkv_decode<MASK, VL>(s, u);
+        if (u >= total) break;
+        const DkvUnit w = dkv_decode<MASK, VL>(p, u);
         if (!w.work) continue;
         const int krow = w.sr.koff + w.kt * TILE, tb = w.sr.tb;
         if (!mbar_wait(bar.kv_empty, (un & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
@@ -370,8 +380,8 @@ __global__ void __launch_bounds__(384, 1)
         if (!mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
         const int u = unit_slot[slot];
         mbar_arrive(&bar.unit_empty[slot]);
-        if (u >= p.total_units) break;
-        const DkvUnit w = dkv_decode<MASK, VL>(s, u);
+        if (u >= total) break;
+        const DkvUnit w = dkv_decode<MASK, VL>(p, u);
         if (!w.work) continue;
         if (!mbar_wait(bar.kv_full, (un++) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) break;
         bool ok = mbar_wait(&bar.st_full[sq % L::STAGES], (sq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
@@ -445,8 +455,8 @@ __global__ void __launch_bounds__(384, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       const int u = unit_slot[slot];
       warp_arrive(&bar.unit_empty[slot]);
-      if (u >= p.total_units) break;
-      const DkvUnit w = dkv_decode<MASK, VL>(s, u);
+      if (u >= total) break;
+      const DkvUnit w = dkv_decode<MASK, VL>(p, u);
       const Dims& su = w.sr.s;  // this unit's sequence
       if (!w.sr.ok && warp == 4 && lane_id() == 0) report(ctl, FA_STATUS_BAD_INPUT);
       if (!w.work) {
@@ -587,6 +597,15 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// The dQ unit's (b, h, query tile): dense order, or the packed sequences' plan.
+template <bool VL>
+__device__ __forceinline__ void dq_unit_of(const BwdParams& p, int u, int& b, int& h, int& qt) {
+  if (VL)
+    plan_unit(p.plan, p.dims.Hq, u, b, h, qt);
+  else
+    dq_unit(p.dims, u, b, h, qt);
+}
+
 // ================================================================== dQ
 template <int D>
 struct DqLayout {
@@ -640,6 +659,7 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const Ctl ctl{p.status, p.timeout_ns};
   const Dims& s = p.dims;
+  const int total = VL ? __ldg(p.plan) : p.total_units;  // units (packed sequences: from the plan)
   const int g = s.Hq / s.Hkv;
 
   if (threadIdx.x == 0) {
@@ -679,9 +699,9 @@ __global__ void __launch_bounds__(384, 1)
         const int u = atomicAdd(p.counter, 1);
         unit_slot[slot] = u;
         mbar_arrive(&unit_full[slot]);
-        if (u >= p.total_units) break;
+        if (u >= total) break;
         int b, h, qt;
-        dq_unit(s, u, b, h, qt);
+        dq_unit_of<VL>(p, u, b, h, qt);
         const SeqRows sr = seq_rows<VL>(s, b);
         if (qt >= q_tiles(sr.s)) continue;  // past its (packed) sequence
         int klo, khi;
@@ -751,9 +771,9 @@ __global__ void __launch_bounds__(384, 1)
         if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
         const int u = unit_slot[slot];
         mbar_arrive(&unit_empty[slot]);
-        if (u >= p.total_units) break;
+        if (u >= total) break;
         int b, h, qt;
-        dq_unit(s, u, b, h, qt);
+        dq_unit_of<VL>(p, u, b, h, qt);
         const Dims su = seq_rows<VL>(s, b).s;
         if (qt >= q_tiles(su)) continue;  // past its (packed) sequence
         int klo, khi;
@@ -817,9 +837,9 @@ __global__ void __launch_bounds__(384, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       const int u = unit_slot[slot];
       warp_arrive(&unit_empty[slot]);
-      if (u >= p.total_units) break;
+      if (u >= total) break;
       int b, h, qt;
-      dq_unit(s, u, b, h, qt);
+      dq_unit_of<VL>(p, u, b, h, qt);
       const SeqRows sr = seq_rows<VL>(s, b);
       if (!sr.ok && warp == 4 && lane_id() == 0) report(ctl, FA_STATUS_BAD_INPUT);
       const Dims& su = sr.s;  // this unit's sequence
@@ -929,6 +949,7 @@ __global__ void __launch_bounds__(384, 1)
 template <int D, int MASK, bool VL = false>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   BwdParams p;
+  p.plan = nullptr;
   p.dims = a.dims;
   p.scale = a.scale;
   p.scale_log2 = a.scale * LOG2E;
@@ -958,6 +979,11 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     p.counter = a.counters;
     p.total_units = dkdv_units(a.dims);
+    p.plan = a.plan_dkdv;
+    if (VL) {
+      e = launch_varlen_plan(a.dims, VARLEN_PLAN_DKDV, k_tiles(a.dims), a.dims.Hkv, a.plan_dkdv, a.status, st);
+      if (e != cudaSuccess) return e;
+    }
     kern<<<imax(1, imin(p.total_units, a.num_sms)), 384, DkvLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
                                                                                      a.tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -969,6 +995,11 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     p.counter = a.counters + 1;
     p.total_units = dq_units(a.dims);
+    p.plan = a.plan_dq;
+    if (VL) {
+      e = launch_varlen_plan(a.dims, VARLEN_PLAN_DQ, q_tiles(a.dims), a.dims.Hq, a.plan_dq, a.status, st);
+      if (e != cudaSuccess) return e;
+    }
     kern<<<imax(1, imin(p.total_units, a.num_sms)), 384, DqLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
                                                                                    a.tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -112,6 +112,7 @@ struct FwdParams {
   const int* row_ptr;  // block-sparse CSR table: [nqt + 1], col_idx [nnz]
   const int* col_idx;
   int nnz;
+  const int* plan;     // packed sequences: the device-side work plan (units with work only)
   OutRows o;
   OutRows o_res;
   float* lse;
@@ -191,6 +192,18 @@ __device__ __forceinline__ UnitTiles unit_tiles(const Dims& s, int p) {
   return u;
 }
 
+// The unit's (b, h, pair): dense order, or the packed sequences' plan.
+template <bool VL>
+__device__ __forceinline__ void fwd_unit_of(const FwdParams& p, int u, int& b, int& h, int& pr) {
+  if (VL)
+    plan_unit(p.plan, p.dims.Hq, u, b, h, pr);
+  else
+    fwd_unit(p.dims, u, b, h, pr);
+}
+
+template <bool VL>
+__device__ __forceinline__ int fwd_total(const FwdParams& p) { return VL ? __ldg(p.plan) : p.total_units; }
+
 // ------------------------------------------------------------------ producer
 template <int D, int MASK, bool F8, bool VL, bool SP>
 __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, const CUtensorMap* tm_q,
@@ -202,15 +215,16 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
   uint32_t seq = 0;       // K/V groups issued so far (ring sequence number)
   uint32_t qn = 0;        // units with work so far (Q load phase)
   int q_armed = -1;       // phase of the last Q load issued
+  const int total = fwd_total<VL>(p);
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     if (!mbar_wait(&bar.unit_empty[slot], ((it >> 1) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
     const int u = atomicAdd(p.counter, 1);
     unit_slot[slot] = u;
     mbar_arrive(&bar.unit_full[slot]);
-    if (u >= p.total_units) break;
+    if (u >= total) break;
     int b, h, pr;
-    fwd_unit(p.dims, u, b, h, pr);
+    fwd_unit_of<VL>(p, u, b, h, pr);
     const SeqRows sr = seq_rows<VL>(p.dims, b);
     const UnitTiles ut = unit_tiles<MASK>(VL ? sr.s : p.dims, pr);
     int nmax = ut.nu;
@@ -315,14 +329,15 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
   };
   auto group_base = [&](uint32_t gq) { return kv_base + (gq % L::NG) * 2 * L::TB; };
 
+  const int total = fwd_total<VL>(p);
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     if (!mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) return;
     const int u = unit_slot[slot];
-    if (!SP || u >= p.total_units) mbar_arrive(&bar.unit_empty[slot]);  // block-sparse: after the unit
-    if (u >= p.total_units) return;
+    if (!SP || u >= total) mbar_arrive(&bar.unit_empty[slot]);  // block-sparse: after the unit
+    if (u >= total) return;
     int b, h, pr;
-    fwd_unit(p.dims, u, b, h, pr);
+    fwd_unit_of<VL>(p, u, b, h, pr);
     const UnitTiles ut = unit_tiles<MASK>(VL ? seq_rows<VL>(p.dims, b).s : p.dims, pr);
     int nmax = ut.nu;
     // tile t is active at local steps [a[t], e[t]) (block-sparse: the steps its bit marks)
@@ -400,16 +415,17 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
   const float c = p.scale_log2;
   const Dims& s = p.dims;
   uint32_t sph = 0, active = 0;
+  const int total = fwd_total<VL>(p);
 
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     bool ok = mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
     if (!__all_sync(0xffffffffu, ok)) return;
     const int u = unit_slot[slot];
-    if (!SP || u >= p.total_units) warp_arrive(&bar.unit_empty[slot]);  // block-sparse: after the unit
-    if (u >= p.total_units) return;
+    if (!SP || u >= total) warp_arrive(&bar.unit_empty[slot]);  // block-sparse: after the unit
+    if (u >= total) return;
     int b, h, pr;
-    fwd_unit(s, u, b, h, pr);
+    fwd_unit_of<VL>(p, u, b, h, pr);
     const SeqRows sr = seq_rows<VL>(s, b);
     if (VL && !sr.ok && t == 0 && wq == 0 && lane_id() == 0) report(ctl, FA_STATUS_BAD_INPUT);
     const Dims& su = VL ? sr.s : s;  // this unit's sequence (packed), else the problem
@@ -777,6 +793,11 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   p.row_ptr = a.row_ptr;
   p.col_idx = a.col_idx;
   p.nnz = a.nnz;
+  p.plan = a.plan;
+  if (VL) {  // the units with work, longest first
+    e = launch_varlen_plan(a.dims, VARLEN_PLAN_FWD, fwd_pairs(a.dims), a.dims.Hq, a.plan, a.status, st);
+    if (e != cudaSuccess) return e;
+  }
   p.o = a.o;
   p.o_res = a.o_res;
   p.lse = a.lse;

@@ -36,6 +36,7 @@ struct FwdLaunch {
   const int* row_ptr;  // [ceil(Nq/128) + 1]
   const int* col_idx;  // [nnz]
   int nnz;
+  int* plan;           // packed sequences: workspace for the device-side work plan
 };
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
 
@@ -54,6 +55,8 @@ struct BwdLaunch {
   unsigned long long timeout_ns;
   int num_sms;
   int parts;       // bit 0: preprocess, bit 1: dK/dV, bit 2: dQ
+  int* plan_dkdv;  // packed sequences: workspace for the device-side work plans
+  int* plan_dq;
 };
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st);
 
@@ -94,6 +97,13 @@ struct QuantLaunch {       // E4M3 codes of a bf16 [B, N, H, d] tensor
   int per_block;
 };
 cudaError_t launch_quantize(const QuantLaunch& a, cudaStream_t st);
+
+// Device-side work plan of packed sequences (levels: forward pairs, dQ query
+// tiles, dK/dV key tiles from the end); `plan` holds varlen_plan_ints(nlev, B) ints.
+constexpr int VARLEN_PLAN_FWD = 0, VARLEN_PLAN_DQ = 1, VARLEN_PLAN_DKDV = 2;
+// Sequences the cu arrays cannot hold are reported in *status and get no units.
+cudaError_t launch_varlen_plan(const Dims& d, int mode, int nlev, int heads, int* plan, int* status,
+                               cudaStream_t st);
 
 cudaError_t launch_selftest_mma(int mode, int n_or_k, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                 const void* a_rows, float* c, int* status, cudaStream_t st);

@@ -66,7 +66,36 @@ __device__ __forceinline__ SeqRows seq_rows(const Dims& d, int b) {
   r.tb = 0;
   return r;
 }
+
+// Work plan of packed sequences, built on the device for each call (see
+// launch_varlen_plan): units with work only, longest first.  A unit has a
+// level (forward: the query-tile pair; dQ: the query tile; dK/dV: the key tile
+// counted from the sequence's end) and levels are handed out from the highest
+// down; within a level come the sequences long enough to have it, in
+// descending order of their level count, each with all its heads (adjacent,
+// so heads sharing a K/V head stay together).  Layout (ints): [0] units,
+// [1] levels n, [4 .. 4+n] first unit of each level, highest level first
+// (the last entry = units), then [B] the sequences in order.
+__device__ __forceinline__ void plan_unit(const int* plan, int heads, int u, int& b, int& h, int& level) {
+  const int nlev = __ldg(plan + 1);
+  const int* ls = plan + 4;
+  int lo = 0, hi = nlev;  // ls[lo] <= u < ls[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(ls + mid) <= u)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int r = u - __ldg(ls + lo);
+  b = __ldg(ls + nlev + 1 + r / heads);
+  h = r % heads;
+  level = nlev - 1 - lo;
+}
 #endif
+
+// ints a varlen plan with `levels` levels over B sequences takes
+FA_HD int varlen_plan_ints(int levels, int B) { return 4 + levels + 1 + B; }
 
 FA_HD bool banded(const Dims& s) { return s.wl < UNBOUNDED || s.wr < UNBOUNDED; }
 

@@ -143,9 +143,12 @@ int fa_fwd_blocksparse(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tens
  * queries with no keys, or unequal lengths under causal) are reported through
  * the workspace status (fa_get_device_status -> FA_ERR_INVALID) and those
  * sequences' outputs are not written; keys of a sequence with no queries get
- * zero gradients.  Workspaces: fa_fwd_workspace_size(shape) and
- * fa_bwd_varlen_workspace_size(shape, max_seqlen_q).
+ * zero gradients.  Workspaces: fa_fwd_varlen_workspace_size(shape,
+ * max_seqlen_q) and fa_bwd_varlen_workspace_size(shape, max_seqlen_q); they
+ * hold a work plan the call builds on the device (the units with work,
+ * longest first), so no host copy of the lengths is needed.
  * ------------------------------------------------------------------------- */
+size_t fa_fwd_varlen_workspace_size(const fa_shape_t* shape, int max_seqlen_q);
 int fa_fwd_varlen(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* cu_seqlens_q,
                   const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k, const fa_tensor_t* o, float* lse,
                   const fa_tensor_t* o_residual, const fa_shape_t* shape, void* workspace, size_t workspace_bytes,

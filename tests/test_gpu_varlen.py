@@ -124,7 +124,8 @@ def test_lengths_the_arrays_cannot_hold_are_reported(bad):
     s = fa.binding._varlen_shape(qd, kd, cqd, None, causal)
     o = torch.zeros_like(qd)
     lse = torch.zeros((2, qd.shape[0]), dtype=torch.float32, device=DEV)
-    ws = torch.zeros(fa.library().fa_fwd_workspace_size(fa.binding.ctypes.byref(s)), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(fa.library().fa_fwd_varlen_workspace_size(fa.binding.ctypes.byref(s), max_q), dtype=torch.uint8,
+                     device=DEV)
     fa.fa_fwd_varlen(qd, kd, vd, cqd, ckd, max_q, max_k, o, lse, s, ws)
     rc, st = fa.binding.device_status(ws)
     assert rc == 1 and st == 0x100                             # FA_ERR_INVALID, input error only

@@ -398,6 +398,38 @@ def attention_blocksparse_forward(q, k, v, row_ptr, col_idx, scale, causal=False
     return O, LSE
 
 
+def attention_blocksparse_backward(q, k, v, do, row_ptr, col_idx, scale, causal=False, block=128):
+    """Gradients (dQ, dK, dV) of the block-sparse forward: the plain backward with
+    S = -inf outside the visible pairs (P = 0 there); rows that see no key
+    contribute nothing."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Nq, Nk, Hq, Hkv, d = _check_shapes(q, k, v)
+    if causal and Nq != Nk:
+        raise ValueError("causal attention is defined here for Nq == Nk only")
+    M = block_mask_from_csr(row_ptr, col_idx, -(-Nq // block), -(-Nk // block))
+    visible = np.repeat(np.repeat(M, block, axis=0), block, axis=1)[:Nq, :Nk]
+    if causal:
+        visible &= ~causal_mask(np.arange(Nq), Nk)
+    seen = visible.any(axis=1)
+    g = Hq // Hkv
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // g
+            S = np.where(visible, scale * (q[b, :, h, :] @ k[b, :, kv, :].T), NEG_INF)
+            m = np.where(seen, S.max(axis=1), 0.0)
+            E = np.where(visible, np.exp(S - m[:, None]), 0.0)
+            P = E / np.where(seen, E.sum(axis=1), 1.0)[:, None]
+            dO = do[b, :, h, :]
+            dv[b, :, kv, :] += P.T @ dO
+            dP = dO @ v[b, :, kv, :].T
+            D = (P * dP).sum(axis=1, keepdims=True)
+            dS = P * (dP - D)
+            dq[b, :, h, :] = scale * dS @ k[b, :, kv, :]
+            dk[b, :, kv, :] += scale * dS.T @ q[b, :, h, :]
+    return dq, dk, dv
+
+
 def gather_paged(cache, block_table, b, length):
     """Logical rows [0, length) of sequence b from a paged cache [pages, page_size, H, d]:
     row r is at page block_table[b, r // page_size], row r % page_size."""

@@ -79,3 +79,41 @@ def test_malformed_tables_rejected(rp, ci):
     q, k, v = qkv(1, 1, 1, 16, 24, 4)
     with pytest.raises(ValueError):
         A.attention_blocksparse_forward(q, k, v, rp, ci, 1.0, block=8)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_all_blocks_listed_is_dense(causal):
+    q, k, v = qkv(1, 2, 1, 40, 40, 8)
+    do = RNG.standard_normal(q.shape)
+    rp, ci = csr(np.ones((5, 5), bool))
+    g = A.attention_blocksparse_backward(q, k, v, do, rp, ci, 0.3, causal, block=8)
+    gd = A.attention_backward(q, k, v, do, 0.3, causal)
+    for a, b in zip(g, gd):
+        assert np.allclose(a, b, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_central_differences(causal):
+    block, nb = 4, 4
+    q, k, v = qkv(1, 2, 1, nb * block - 1, nb * block - 1, 3)
+    M = RNG.random((nb, nb)) < 0.5
+    M[np.arange(nb), np.arange(nb)] = True
+    M[2] = False                                                 # a query block that sees nothing
+    rp, ci = csr(M)
+    W = RNG.standard_normal(q.shape)
+    dq, dk, dv = A.attention_blocksparse_backward(q, k, v, W, rp, ci, 0.6, causal, block=block)
+    assert not dq[0, 8:12].any()
+
+    def loss(q_, k_, v_):
+        return np.sum(A.attention_blocksparse_forward(q_, k_, v_, rp, ci, 0.6, causal, block=block)[0] * W)
+
+    eps = 1e-6
+    for name, x, gr in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in [(0, 0, 0, 0), (0, x.shape[1] - 1, x.shape[2] - 1, 2), (0, 6, 0, 1)]:
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            ap = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            am = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            num = (loss(*ap) - loss(*am)) / (2 * eps)
+            assert abs(num - gr[idx]) < 1e-6 * max(1.0, abs(num)), (name, idx, num, gr[idx])

@@ -18,6 +18,8 @@ from .binding import (  # noqa: F401
     forward_fp8,
     forward_varlen,
     forward_blocksparse,
+    backward_blocksparse,
+    fa_bwd_blocksparse,
     fa_fwd_blocksparse,
     backward_varlen,
     fa_fwd_varlen,

@@ -72,6 +72,8 @@ SIGNATURES = {
     "fa_decode_split_range": (_I, [_PS, _I, _I, _PI, _PI]),
     "fa_selftest_mma": (_I, [_I, _I, _VP, _VP, _VP, _VP, _VP]),
     "fa_fwd_blocksparse": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _PT, _VP, _PT, _PS, _VP, _SZ, _VP]),
+    "fa_bwd_blocksparse_workspace_size": (_SZ, [_PS, _I]),
+    "fa_bwd_blocksparse": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _PT, _VP, _PT, _PT, _PT, _PT, _PT, _PS, _VP, _SZ, _VP]),
     "fa_fwd_varlen_workspace_size": (_SZ, [_PS, _I]),
     "fa_fwd_varlen": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _I, _PT, _VP, _PT, _PS, _VP, _SZ, _VP]),
     "fa_bwd_varlen_workspace_size": (_SZ, [_PS, _I]),
@@ -204,6 +206,17 @@ def fa_fwd_blocksparse(q, k, v, row_ptr, col_idx, o, lse, s, workspace, o_res=No
                                  col_idx.data_ptr() if col_idx.numel() else None, col_idx.numel(), tdesc(o),
                                  lse.data_ptr(), _opt(o_res), ctypes.byref(s), workspace.data_ptr(),
                                  workspace.numel(), _stream(q)))
+
+
+def fa_bwd_blocksparse(q, k, v, row_ptr, col_idx, o, lse, do, dq, dk, dv, s, workspace, o_res=None):
+    lib = library()
+    for t in (row_ptr, col_idx):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise FAError(1, "row_ptr and col_idx must be contiguous int32 CUDA tensors")
+    check(lib.fa_bwd_blocksparse(tdesc(q), tdesc(k), tdesc(v), row_ptr.data_ptr(),
+                                 col_idx.data_ptr() if col_idx.numel() else None, col_idx.numel(), tdesc(o),
+                                 lse.data_ptr(), _opt(o_res), tdesc(do), tdesc(dq), tdesc(dk), tdesc(dv),
+                                 ctypes.byref(s), workspace.data_ptr(), workspace.numel(), _stream(q)))
 
 
 def fa_fwd_varlen(q, k, v, cu_q, cu_k, max_q, max_k, o, lse, s, workspace, o_res=None):
@@ -378,3 +391,14 @@ def forward_blocksparse(q, k, v, row_ptr, col_idx, causal=False, scale=None, res
     ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q.device)
     fa_fwd_blocksparse(q, k, v, row_ptr, col_idx, o, lse, s, ws, res)
     return (o, lse, res) if residual else (o, lse)
+
+
+def backward_blocksparse(q, k, v, row_ptr, col_idx, o, lse, do, causal=False, scale=None, o_residual=None):
+    """dQ, dK, dV of ``forward_blocksparse`` (same table)."""
+    s = _dims(q, k, scale, causal)
+    dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device)
+    dv = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device)
+    ws = _ws(library().fa_bwd_blocksparse_workspace_size(ctypes.byref(s), col_idx.numel()), q.device)
+    fa_bwd_blocksparse(q, k, v, row_ptr, col_idx, o, lse, do, dq, dk, dv, s, ws, o_residual)
+    return dq, dk, dv

@@ -498,10 +498,17 @@ size_t fa_bwd_varlen_workspace_size(const fa_shape_t* s, int max_seqlen_q) {
   return bwd_ws_bytes(s, max_seqlen_q) + bwd_plan_bytes(s, max_seqlen_q);
 }
 
+// The block-sparse backward adds the tile bitmap and the two filtered lists.
+size_t bwd_sparse_bytes(const fa_shape_t* s, int nnz) {
+  const size_t nqt = cdiv(s->Nq, TILE), nkt = cdiv(s->Nk, TILE);
+  return round_up(nqt * nkt, 256) + round_up((nqt + 1) * sizeof(int), 256) +
+         round_up((nkt + 1) * sizeof(int), 256) + 2 * round_up(static_cast<size_t>(nnz) * sizeof(int) + 4, 256);
+}
+
 static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v,
                     const fa_tensor_t* o, const float* lse, const fa_tensor_t* o_res, const fa_tensor_t* dout,
                     const fa_tensor_t* dq, const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* s,
-                    const Packed* pk, void* ws, size_t ws_bytes, void* stream) {
+                    const Packed* pk, void* ws, size_t ws_bytes, void* stream, const Sparse* sp = nullptr) {
   int rc;
   if ((rc = check_shape(s)) || (rc = check_packed(s, pk)) || (rc = check_tensor(q)) || (rc = check_tensor(k)) ||
       (rc = check_tensor(v)) ||
@@ -510,7 +517,10 @@ static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const
     return rc;
   if (!lse) return FA_ERR_INVALID;
   const int nq_rows = pk ? pk->max_q : s->Nq;
-  if ((rc = check_ws(ws, ws_bytes, bwd_ws_bytes(s, nq_rows) + (pk ? bwd_plan_bytes(s, pk->max_q) : 0)))) return rc;
+  if ((rc = check_ws(ws, ws_bytes,
+                     bwd_ws_bytes(s, nq_rows) + (pk ? bwd_plan_bytes(s, pk->max_q) : 0) +
+                         (sp ? bwd_sparse_bytes(s, sp->nnz) : 0))))
+    return rc;
   int sms = 0;
   if ((rc = device_info(&sms))) return rc;
   BwdLaunch a;
@@ -533,6 +543,31 @@ static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const
   char* base = static_cast<char*>(ws);
   a.neg_lse2 = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES);
   a.neg_delta = reinterpret_cast<float*>(base + FA_WS_HEADER_BYTES + round_up(rows * sizeof(float), 256));
+  SparseLaunch sl;
+  memset(&sl, 0, sizeof(sl));
+  if (sp) {  // the caller's table -> filtered per-query-tile and per-key-tile lists in the workspace
+    char* w = base + bwd_ws_bytes(s, nq_rows);
+    const int nqt = cdiv(s->Nq, TILE), nkt = cdiv(s->Nk, TILE);
+    sl.row_ptr = sp->row_ptr;
+    sl.col_idx = sp->col_idx;
+    sl.nnz = sp->nnz;
+    sl.nqt = nqt;
+    sl.nkt = nkt;
+    sl.causal = s->causal;
+    sl.bitmap = reinterpret_cast<uint8_t*>(w);
+    w += round_up(static_cast<size_t>(nqt) * nkt, 256);
+    sl.rows_ptr = reinterpret_cast<int*>(w);
+    w += round_up((nqt + 1) * sizeof(int), 256);
+    sl.cols_ptr = reinterpret_cast<int*>(w);
+    w += round_up((nkt + 1) * sizeof(int), 256);
+    sl.rows_idx = reinterpret_cast<int*>(w);
+    w += round_up(static_cast<size_t>(sp->nnz) * sizeof(int) + 4, 256);
+    sl.cols_idx = reinterpret_cast<int*>(w);
+    a.rows_ptr = sl.rows_ptr;
+    a.rows_idx = sl.rows_idx;
+    a.cols_ptr = sl.cols_ptr;
+    a.cols_idx = sl.cols_idx;
+  }
   if (pk) {
     char* plans = base + bwd_ws_bytes(s, nq_rows);
     a.plan_dq = reinterpret_cast<int*>(plans);
@@ -545,8 +580,32 @@ static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const
   a.num_sms = sms;
   a.parts = parts;
   if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
-  cudaError_t e = launch_bwd(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaSuccess;
+  if (sp) {
+    sl.status = a.status;
+    e = launch_sparse_lists(sl, static_cast<cudaStream_t>(stream));
+  }
+  if (e == cudaSuccess) e = launch_bwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
+}
+
+size_t fa_bwd_blocksparse_workspace_size(const fa_shape_t* s, int nnz) {
+  if (check_shape(s) != FA_OK || nnz < 0) return 0;
+  return bwd_ws_bytes(s, s->Nq) + bwd_sparse_bytes(s, nnz);
+}
+
+int fa_bwd_blocksparse(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* row_ptr,
+                       const int* col_idx, int nnz, const fa_tensor_t* o, const float* lse,
+                       const fa_tensor_t* o_res, const fa_tensor_t* dout, const fa_tensor_t* dq,
+                       const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* s, void* ws, size_t ws_bytes,
+                       void* stream) {
+  int rc;
+  if ((rc = check_shape(s))) return rc;
+  if (!row_ptr || nnz < 0 || (nnz > 0 && !col_idx) || s->window || cdiv(s->Nq, TILE) > 1024 ||
+      cdiv(s->Nk, TILE) > 1024)
+    return FA_ERR_INVALID;
+  const Sparse sp{row_ptr, col_idx, nnz};
+  return bwd_impl(7, q, k, v, o, lse, o_res, dout, dq, dk, dv, s, nullptr, ws, ws_bytes, stream, &sp);
 }
 
 int fa_bwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o,

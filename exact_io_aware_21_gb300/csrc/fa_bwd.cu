@@ -59,6 +59,10 @@ struct BwdParams {
   unsigned long long timeout_ns;
   int total_units;
   const int* plan;  // packed sequences: the kernel's device-side work plan (units with work only)
+  const int* rows_ptr;  // block-sparse: key tiles of each query tile (ascending) ...
+  const int* rows_idx;
+  const int* cols_ptr;  // ... and query tiles of each key tile (ascending)
+  const int* cols_idx;
 };
 
 // ================================================================== preprocess
@@ -225,6 +229,7 @@ __device__ __forceinline__ DkvBars dkv_bars(uint8_t* smem) {
 
 struct DkvUnit {
   int b, kvh, kt, q0, nqi, n_it;
+  const int* qlist;  // block-sparse: the key tile's query tiles (else q0, q0 + 1, ...)
   SeqRows sr;  // the unit's sequence (packed sequences: its own lengths and row offsets)
   bool work;   // the key tile holds keys that some query sees
   bool zero;   // the key tile holds keys that no query sees: their gradients are 0
@@ -244,7 +249,7 @@ __device__ __forceinline__ void dq_kv_range(const Dims& s, int qt, int& lo, int&
 
 // The query tiles visiting key tile kt: a band's range, or under j <= i (where
 // Nq == Nk) the suffix from the diagonal tile.
-template <int MASK, bool VL>
+template <int MASK, bool VL, bool SP>
 __device__ __forceinline__ DkvUnit dkv_decode(const BwdParams& p, int u) {
   const Dims& s = p.dims;
   DkvUnit r;
@@ -259,10 +264,16 @@ __device__ __forceinline__ DkvUnit dkv_decode(const BwdParams& p, int u) {
   }
   const Dims& su = r.sr.s;
   int qhi = q_tiles(su);
-  if (MASK == MASK_BAND)
+  r.qlist = nullptr;
+  if (SP) {
+    r.q0 = __ldg(p.cols_ptr + r.kt);
+    qhi = __ldg(p.cols_ptr + r.kt + 1);
+    r.qlist = p.cols_idx + r.q0;
+  } else if (MASK == MASK_BAND) {
     q_range(su, r.kt, r.q0, qhi);
-  else
+  } else {
     r.q0 = MASK == MASK_CAUSAL ? r.kt : 0;
+  }
   const bool keys = r.kt < k_tiles(su);
   r.nqi = keys ? imax(0, qhi - r.q0) : 0;
   r.n_it = (s.Hq / s.Hkv) * r.nqi;
@@ -271,7 +282,7 @@ __device__ __forceinline__ DkvUnit dkv_decode(const BwdParams& p, int u) {
   return r;
 }
 
-template <int D, int MASK, bool VL>
+template <int D, int MASK, bool VL, bool SP>
 __global__ void __launch_bounds__(384, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(384, 1)
         unit_slot[slot] = u;
         mbar_arrive(&bar.unit_full[slot]);
         if (u >= total) break;
-        const DkvUnit w = dkv_decode<MASK, VL>(p, u);
+        const DkvUnit w = dkv_decode<MASK, VL, SP>(p, u);
         if (!w.work) continue;
         const int krow = w.sr.koff + w.kt * TILE, tb = w.sr.tb;
         if (!mbar_wait(bar.kv_empty, (un & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
@@ -340,7 +351,7 @@ __global__ void __launch_bounds__(384, 1)
             ok = false;
             break;
           }
-          const int hq = w.kvh * g + k / w.nqi, qi = w.q0 + k % w.nqi;
+          const int hq = w.kvh * g + k / w.nqi, qi = SP ? __ldg(w.qlist + k % w.nqi) : w.q0 + k % w.nqi;
           uint8_t* base = smem + L::OFF_ST + st * L::STAGE;
           const int64_t row0 = (static_cast<int64_t>(w.b) * s.Hq + hq) * p.nq_pad + qi * TILE;
           mbar_arrive_expect_tx(&bar.st_full[st], 2 * L::TB + 1024);
@@ -352,7 +363,8 @@ __global__ void __launch_bounds__(384, 1)
           bulk_load(base + 2 * L::TB, p.neg_lse2 + row0, 512, &bar.st_full[st]);
           bulk_load(base + 2 * L::TB + 512, p.neg_delta + row0, 512, &bar.st_full[st]);
           if (k + 1 < w.n_it) {  // the next iteration's Q and dO into L2 while this stage waits its turn
-            const int hq1 = w.kvh * g + (k + 1) / w.nqi, qi1 = w.q0 + (k + 1) % w.nqi;
+            const int hq1 = w.kvh * g + (k + 1) / w.nqi;
+            const int qi1 = SP ? __ldg(w.qlist + (k + 1) % w.nqi) : w.q0 + (k + 1) % w.nqi;
             for (int c = 0; c < D / 64; ++c) {
               tma_prefetch_l2_4d(&tm_q, c * 64, hq1, w.sr.qoff + qi1 * TILE, tb);
               tma_prefetch_l2_4d(&tm_do, c * 64, hq1, w.sr.qoff + qi1 * TILE, tb);
@@ -381,7 +393,7 @@ __global__ void __launch_bounds__(384, 1)
         const int u = unit_slot[slot];
         mbar_arrive(&bar.unit_empty[slot]);
         if (u >= total) break;
-        const DkvUnit w = dkv_decode<MASK, VL>(p, u);
+        const DkvUnit w = dkv_decode<MASK, VL, SP>(p, u);
         if (!w.work) continue;
         if (!mbar_wait(bar.kv_full, (un++) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) break;
         bool ok = mbar_wait(&bar.st_full[sq % L::STAGES], (sq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
@@ -456,7 +468,7 @@ __global__ void __launch_bounds__(384, 1)
       const int u = unit_slot[slot];
       warp_arrive(&bar.unit_empty[slot]);
       if (u >= total) break;
-      const DkvUnit w = dkv_decode<MASK, VL>(p, u);
+      const DkvUnit w = dkv_decode<MASK, VL, SP>(p, u);
       const Dims& su = w.sr.s;  // this unit's sequence
       if (!w.sr.ok && warp == 4 && lane_id() == 0) report(ctl, FA_STATUS_BAD_INPUT);
       if (!w.work) {
@@ -485,7 +497,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint8_t* stage = smem + L::OFF_ST + (q % L::STAGES) * L::STAGE;
         const float* nl2 = reinterpret_cast<const float*>(stage + 2 * L::TB);  // -LSE2[query]
         const float* nd = nl2 + 128;                                            // -D[query]
-        const int qi = w.q0 + k % w.nqi;
+        const int qi = SP ? __ldg(w.qlist + k % w.nqi) : w.q0 + k % w.nqi;
         // rows (keys) see only part of the tile's queries: the band's edges, or causal's diagonal
         const bool part = MASK == MASK_BAND ? (qi < qfull_lo || qi > qfull_hi)
                                             : (MASK == MASK_CAUSAL && qi == w.kt);
@@ -597,6 +609,22 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// The key tiles of dQ unit qt: the range [klo, khi) (dense, band, packed), or
+// for block-sparse the query tile's list (klo = 0, khi = its length, *klist).
+template <int MASK, bool SP>
+__device__ __forceinline__ void dq_keys(const BwdParams& p, const Dims& su, int qt, int& klo, int& khi,
+                                        const int*& klist) {
+  klist = nullptr;
+  if (SP) {
+    const int r0 = __ldg(p.rows_ptr + qt);
+    klo = 0;
+    khi = __ldg(p.rows_ptr + qt + 1) - r0;
+    klist = p.rows_idx + r0;
+  } else {
+    dq_kv_range<MASK>(su, qt, klo, khi);
+  }
+}
+
 // The dQ unit's (b, h, query tile): dense order, or the packed sequences' plan.
 template <bool VL>
 __device__ __forceinline__ void dq_unit_of(const BwdParams& p, int u, int& b, int& h, int& qt) {
@@ -633,7 +661,7 @@ struct DqLayout {
   static constexpr int ALLOC = (SCRATCH ? OFF_SCR + 8 * ROW_SCRATCH_BYTES : OFF_TMEM + 16) + 1024;
 };
 
-template <int D, int MASK, bool VL>
+template <int D, int MASK, bool VL, bool SP>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -705,8 +733,10 @@ __global__ void __launch_bounds__(384, 1)
         const SeqRows sr = seq_rows<VL>(s, b);
         if (qt >= q_tiles(sr.s)) continue;  // past its (packed) sequence
         int klo, khi;
-        dq_kv_range<MASK>(sr.s, qt, klo, khi);
+        const int* klist;
+        dq_keys<MASK, SP>(p, sr.s, qt, klo, khi, klist);
         const int n = khi - klo, kvh = h / g;
+        if (SP && n == 0) continue;  // no key tile listed: the dQ warps write zeros
         if (!mbar_wait(q_empty, (qn & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
         mbar_arrive_expect_tx(q_full, 2 * L::TB);
         for (int c = 0; c < D / 64; ++c) {
@@ -725,7 +755,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&k_full[ks], L::TB);
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(smem + L::OFF_K + ks * L::TB + c * (TILE * 128), &tm_k, &k_full[ks], c * 64, kvh,
-                        sr.koff + (klo + j) * TILE, sr.tb);
+                        sr.koff + (SP ? __ldg(klist + j) : klo + j) * TILE, sr.tb);
           // V_j: its slot is free once dP of the tile VST back is done.
           const int vs = kq % L::VST;
           if (!mbar_wait(&v_empty[vs], ((kq / L::VST) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) {
@@ -735,7 +765,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(&v_full[vs], L::TB);
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(smem + L::OFF_V + vs * L::TB + c * (TILE * 128), &tm_v, &v_full[vs], c * 64, kvh,
-                        sr.koff + (klo + j) * TILE, sr.tb);
+                        sr.koff + (SP ? __ldg(klist + j) : klo + j) * TILE, sr.tb);
         }
         if (!ok) break;
       }
@@ -777,8 +807,10 @@ __global__ void __launch_bounds__(384, 1)
         const Dims su = seq_rows<VL>(s, b).s;
         if (qt >= q_tiles(su)) continue;  // past its (packed) sequence
         int klo, khi;
-        dq_kv_range<MASK>(su, qt, klo, khi);
+        const int* klist;
+        dq_keys<MASK, SP>(p, su, qt, klo, khi, klist);
         const int n = khi - klo;
+        if (SP && n == 0) continue;
         bool ok = mbar_wait(q_full, (qn++) & 1, ctl, FA_STATUS_TIMEOUT_MMA) && kwait(kq);
         if (!ok) break;
         tc_fence_after();
@@ -845,13 +877,23 @@ __global__ void __launch_bounds__(384, 1)
       const Dims& su = sr.s;  // this unit's sequence
       if (qt >= q_tiles(su)) continue;  // past its (packed) sequence
       int klo, khi, full_lo = 0, full_hi = 0;
-      dq_kv_range<MASK>(su, qt, klo, khi);
+      const int* klist;
+      dq_keys<MASK, SP>(p, su, qt, klo, khi, klist);
       if (MASK == MASK_BAND) {
         kv_full_range(su, qt, full_lo, full_hi);
         if ((su.Nk % TILE) != 0) full_hi = imin(full_hi, k_tiles(su) - 2);  // the ragged last tile is masked too
       }
       const int n = khi - klo;
       const int q_row = qt * TILE + r;
+      if (SP && n == 0) {  // no key tile listed: dQ = 0 for the tile's rows (this warp's half of the columns)
+        if (q_row < su.Nq) {
+          uint4* z = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.dq.ptr) + b * p.dq.sb +
+                                              static_cast<int64_t>(q_row) * p.dq.sn + h * p.dq.sh + (c0 / 64) * (D / 2));
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
       const int64_t srow = (static_cast<int64_t>(b) * s.Hq + h) * p.nq_pad + q_row;
       const float2 nl2 = make_float2(p.neg_lse2[srow], p.neg_lse2[srow]);
       const float2 nd2 = make_float2(p.neg_delta[srow], p.neg_delta[srow]);
@@ -888,6 +930,16 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int i = 0; i < 64; ++i)
               if (i < lo || i >= hi) pf[i] = 0.f;
+          }
+        } else if (SP) {  // the listed tile: the diagonal, or the ragged last tile, is masked
+          const int kt = __ldg(klist + j);
+          if ((MASK == MASK_CAUSAL && kt == qt) || (kt == k_tiles(su) - 1 && (su.Nk % TILE) != 0)) {
+            int lim = imin(TILE, su.Nk - kt * TILE);
+            if (MASK == MASK_CAUSAL) lim = imin(lim, q_row - kt * TILE + 1);
+            lim -= c0;
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              if (i >= lim) pf[i] = 0.f;
           }
         } else if (j == n - 1) {  // causal or full: only the last key tile holds masked keys
           int lim = imin(TILE, su.Nk - j * TILE);
@@ -946,10 +998,14 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, int MASK, bool VL = false>
+template <int D, int MASK, bool VL = false, bool SP = false>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   BwdParams p;
   p.plan = nullptr;
+  p.rows_ptr = a.rows_ptr;
+  p.rows_idx = a.rows_idx;
+  p.cols_ptr = a.cols_ptr;
+  p.cols_idx = a.cols_idx;
   p.dims = a.dims;
   p.scale = a.scale;
   p.scale_log2 = a.scale * LOG2E;
@@ -974,7 +1030,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   }
   // 2) dK / dV
   if (a.parts & 2) {
-    auto kern = bwd_dkdv_kernel<D, MASK, VL>;
+    auto kern = bwd_dkdv_kernel<D, MASK, VL, SP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkvLayout<D>::ALLOC);
     if (e != cudaSuccess) return e;
     p.counter = a.counters;
@@ -990,7 +1046,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   }
   // 3) dQ
   if (a.parts & 4) {
-    auto kern = bwd_dq_kernel<D, MASK, VL>;
+    auto kern = bwd_dq_kernel<D, MASK, VL, SP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::ALLOC);
     if (e != cudaSuccess) return e;
     p.counter = a.counters + 1;
@@ -1011,6 +1067,14 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
 
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st) {
   const int m = mask_kind(a.dims);
+  if (a.rows_ptr != nullptr) {  // block-sparse: dense batch, no band
+    if (a.dims.cu_q != nullptr || m == MASK_BAND) return cudaErrorInvalidValue;
+    if (a.d == 64)
+      return m == MASK_CAUSAL ? launch_bwd_t<64, MASK_CAUSAL, false, true>(a, st)
+                              : launch_bwd_t<64, MASK_NONE, false, true>(a, st);
+    return m == MASK_CAUSAL ? launch_bwd_t<128, MASK_CAUSAL, false, true>(a, st)
+                            : launch_bwd_t<128, MASK_NONE, false, true>(a, st);
+  }
   if (a.dims.cu_q != nullptr) {  // packed sequences: no band
     if (m == MASK_BAND) return cudaErrorInvalidValue;
     if (a.d == 64)

@@ -57,6 +57,11 @@ struct BwdLaunch {
   int parts;       // bit 0: preprocess, bit 1: dK/dV, bit 2: dQ
   int* plan_dkdv;  // packed sequences: workspace for the device-side work plans
   int* plan_dq;
+  // block-sparse (rows_ptr != nullptr): filtered lists (see SparseLaunch)
+  const int* rows_ptr;
+  const int* rows_idx;
+  const int* cols_ptr;
+  const int* cols_idx;
 };
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st);
 
@@ -97,6 +102,21 @@ struct QuantLaunch {       // E4M3 codes of a bf16 [B, N, H, d] tensor
   int per_block;
 };
 cudaError_t launch_quantize(const QuantLaunch& a, cudaStream_t st);
+
+// Block-sparse backward: the caller's CSR table checked and filtered into
+// per-query-tile and per-key-tile lists (ascending), via a tile bitmap.
+struct SparseLaunch {
+  const int* row_ptr;   // caller's table: [nqt + 1], col_idx [nnz]
+  const int* col_idx;
+  int nnz, nqt, nkt, causal;
+  uint8_t* bitmap;      // workspace [nqt * nkt]
+  int* rows_ptr;        // out [nqt + 1], rows_idx [<= nnz]: key tiles of each query tile
+  int* rows_idx;
+  int* cols_ptr;        // out [nkt + 1], cols_idx [<= nnz]: query tiles of each key tile
+  int* cols_idx;
+  int* status;
+};
+cudaError_t launch_sparse_lists(const SparseLaunch& a, cudaStream_t st);
 
 // Device-side work plan of packed sequences (levels: forward pairs, dQ query
 // tiles, dK/dV key tiles from the end); `plan` holds varlen_plan_ints(nlev, B) ints.

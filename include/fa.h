@@ -126,6 +126,19 @@ int fa_fwd_blocksparse(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tens
                        const int* col_idx, int nnz, const fa_tensor_t* o, float* lse,
                        const fa_tensor_t* o_residual, const fa_shape_t* shape, void* workspace,
                        size_t workspace_bytes, void* stream);
+/* Block-sparse backward: dQ, dK, dV of fa_fwd_blocksparse (same table; o, lse
+ * and o_residual from it).  The call first turns the table into per-query-tile
+ * and per-key-tile lists in the workspace (checked as above, ascending, so the
+ * results are deterministic); the dQ kernel visits each query tile's listed key
+ * tiles, the dK/dV kernel each key tile's listing query tiles.  Rows that see
+ * no key get dQ = 0; keys no query sees get dK = dV = 0.  Nq, Nk <= 131072.
+ * Needs fa_bwd_blocksparse_workspace_size(shape, nnz) bytes. */
+size_t fa_bwd_blocksparse_workspace_size(const fa_shape_t* shape, int nnz);
+int fa_bwd_blocksparse(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* row_ptr,
+                       const int* col_idx, int nnz, const fa_tensor_t* o, const float* lse,
+                       const fa_tensor_t* o_residual, const fa_tensor_t* dout, const fa_tensor_t* dq,
+                       const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* shape, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Packed variable-length sequences ("第18章" §18.7.1, flash_attn_varlen_func):

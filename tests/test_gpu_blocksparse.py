@@ -130,3 +130,52 @@ def test_tables_that_break_the_rules_are_reported(table):
     fa.fa_fwd_blocksparse(q, k, v, torch.from_numpy(rp).to(DEV), torch.from_numpy(ci).to(DEV), o, lse, s, ws)
     rc, st = fa.binding.device_status(ws)
     assert rc == 1 and st == 0x100
+
+
+# ------------------------------------------------------------------ backward
+from parity import assert_grad  # noqa: E402
+
+
+def run_bwd(x, M, causal, scale):
+    rp, ci = csr(M)
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    rpd, cid = torch.from_numpy(rp).to(DEV), torch.from_numpy(ci).to(DEV)
+    o, lse, res = fa.forward_blocksparse(q, k, v, rpd, cid, causal=causal, scale=scale, residual=True)
+    g = fa.backward_blocksparse(q, k, v, rpd, cid, o, lse, do, causal=causal, scale=scale, o_residual=res)
+    torch.cuda.synchronize()
+    return g, rp, ci
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d,causal,density", CASES)
+def test_backward_random_tables(B, Hq, Hkv, Nq, Nk, d, causal, density):
+    g = np.random.default_rng(Nq + Nk + d + 1)
+    nqt, nkt = -(-Nq // 128), -(-Nk // 128)
+    M = g.random((nqt, nkt)) < density
+    M[np.arange(nqt), np.arange(nqt) % nkt] = True
+    M[1] = False                                               # a query tile that sees nothing
+    M[:, nkt - 2] = False                                      # a key tile no query tile lists
+    x = inputs.shape_inputs(B, Hq, Hkv, Nq, Nk, d, seed=Nq + d + 7)
+    scale = 1 / np.sqrt(d)
+    (dq, dk, dv), rp, ci = run_bwd(x, M, causal, scale)
+    rq, rk, rv = A.attention_blocksparse_backward(x["q"], x["k"], x["v"], x["do"], rp, ci, scale, causal)
+    tag = f"blocksparse bwd {B}x{Hq}/{Hkv} {Nq}x{Nk} d={d} causal={causal}"
+    assert_grad(dq, rq, "dQ " + tag)
+    assert_grad(dk, rk, "dK " + tag)
+    assert_grad(dv, rv, "dV " + tag)
+    assert not f64(dq[:, 128:256]).any()                          # the query tile that sees nothing
+    dead = slice((nkt - 2) * 128, (nkt - 1) * 128)
+    assert not f64(dk[:, dead]).any() and not f64(dv[:, dead]).any()
+
+
+@pytest.mark.parametrize("causal,d", [(False, 128), (True, 64)])
+def test_backward_every_tile_listed_equals_the_dense_kernels(causal, d):
+    N = 1000
+    x = inputs.shape_inputs(1, 4, 2, N, N, d, seed=5)
+    nt = -(-N // 128)
+    (dq, dk, dv), _, _ = run_bwd(x, np.ones((nt, nt), bool), causal, 0.1)
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    o, lse, res = fa.forward(q, k, v, causal=causal, scale=0.1, residual=True)
+    g2 = fa.backward(q, k, v, o, lse, do, causal=causal, scale=0.1, o_residual=res)
+    torch.cuda.synchronize()
+    for a, b in zip((dq, dk, dv), g2):
+        assert torch.equal(a, b)

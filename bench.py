@@ -14,9 +14,10 @@ in HBM:
   varlen leg     forward + backward of 24 packed sequences of long-tailed
                  lengths (32768 tokens, GQA 32/8, d=128, causal) through
                  fa_fwd_varlen / fa_bwd_varlen
-  blocksparse    forward of blocksparse_causal_b1_hq32_hkv8_n16384_d128_local8_global1
-                 through fa_fwd_blocksparse (each query tile: its own key tile, the
-                 seven before it and tile 0)
+  blocksparse    forward + backward of
+                 blocksparse_causal_b1_hq32_hkv8_n16384_d128_local8_global1 through
+                 fa_fwd_blocksparse / fa_bwd_blocksparse (each query tile: its own
+                 key tile, the seven before it and tile 0)
   fp8 leg        E4M3 quantisation (Q, K per 128-row block after the random
                  Hadamard rotation, V per head) and the FP8 forward of the GQA
                  workload
@@ -65,7 +66,7 @@ FP8_NAME = FP8 + "_fp8_hadamard"
 FP8_TENSOR_RATIO = 2.0  # nominal dense E4M3 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 WORKLOAD = (" + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode); " + PAGED_NAME +
             " (paged decode); " + " + ".join(WINDOW) + " (sliding-window fwd+bwd); " + VARLEN +
-            " (packed variable-length fwd+bwd); " + BLOCKSPARSE + " (block-sparse fwd); " + FP8_NAME +
+            " (packed variable-length fwd+bwd); " + BLOCKSPARSE + " (block-sparse fwd+bwd); " + FP8_NAME +
             " (FP8 quantise + fwd)")
 METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -318,7 +319,7 @@ class Leg:
         self.ms = {k: 0.0 for k, _ in fns}
 
 
-KERNELS_PER_CALL = {"fwd_bs": 1, "fwd": 1, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
+KERNELS_PER_CALL = {"fwd_bs": 1, "bwd_bs": 5, "fwd": 1, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
                     "quant_v": 2, "fwd_fp8": 1, "fwd_varlen": 1, "bwd_varlen": 3}
 
 
@@ -416,22 +417,31 @@ def make_legs(device, seed):
     legs.append(Leg(VARLEN, "varlen", w, [("fwd_varlen", vfwd), ("bwd_varlen", vbwd)], 3.5 * fwd_flops(w)))
 
     w = by[BLOCKSPARSE]
-    x = inputs.make(w, device=device, with_do=False, seed=w.seed + seed)
+    x = inputs.make(w, device=device, seed=w.seed + seed)
     M = blocksparse_table(w)
     rows = [[j for j, on in enumerate(r) if on] for r in M]
     rp = torch.tensor([0] + list(itertools.accumulate(len(r) for r in rows)), dtype=torch.int32, device=device)
     ci = torch.tensor([j for r in rows for j in r], dtype=torch.int32, device=device)
     s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal)
-    st = dict(x=x, s=s, rp=rp, ci=ci, o=torch.empty_like(x["q"]),
+    st = dict(x=x, s=s, rp=rp, ci=ci, o=torch.empty_like(x["q"]), ores=torch.empty_like(x["q"]),
               lse=torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=device),
-              wsf=torch.zeros(lib.fa_fwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=device))
+              dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
+              wsf=torch.zeros(lib.fa_fwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=device),
+              wsb=torch.zeros(lib.fa_bwd_blocksparse_workspace_size(ctypes.byref(s), ci.numel()), dtype=torch.uint8,
+                              device=device))
     state[BLOCKSPARSE] = st
 
     def bsfwd(st=st):
         x = st["x"]
-        B.fa_fwd_blocksparse(x["q"], x["k"], x["v"], st["rp"], st["ci"], st["o"], st["lse"], st["s"], st["wsf"])
+        B.fa_fwd_blocksparse(x["q"], x["k"], x["v"], st["rp"], st["ci"], st["o"], st["lse"], st["s"], st["wsf"],
+                             st["ores"])
 
-    legs.append(Leg(BLOCKSPARSE, "blocksparse", w, [("fwd_bs", bsfwd)], fwd_flops(w)))
+    def bsbwd(st=st):
+        x = st["x"]
+        B.fa_bwd_blocksparse(x["q"], x["k"], x["v"], st["rp"], st["ci"], st["o"], st["lse"], x["do"], st["dq"],
+                             st["dk"], st["dv"], st["s"], st["wsb"], st["ores"])
+
+    legs.append(Leg(BLOCKSPARSE, "blocksparse", w, [("fwd_bs", bsfwd), ("bwd_bs", bsbwd)], 3.5 * fwd_flops(w)))
 
     w = {x.name: x for x in train}[FP8]
     x = inputs.make(w, device=device, with_do=False, seed=w.seed + seed)
@@ -638,6 +648,8 @@ def run_ours(args):
             f = fwd_flops(l.w)
             legs_out[l.name] = {"fwd_ms": l.ms["fwd_bs"], "fwd_tflops": f / l.ms["fwd_bs"] / 1e9,
                                 "fwd_frac_of_sustained_peak": f / l.ms["fwd_bs"] / 1e9 / sus,
+                                "bwd_ms": l.ms["bwd_bs"], "bwd_tflops": 2.5 * f / l.ms["bwd_bs"] / 1e9,
+                                "bwd_frac_of_sustained_peak": 2.5 * f / l.ms["bwd_bs"] / 1e9 / sus,
                                 "tiles_listed": sum(sum(r) for r in blocksparse_table(l.w)), "in_step": False,
                                 "flops_count": "4*B*H*d per visible (query, key) pair"}
         elif l.kind == "fp8":

@@ -67,16 +67,11 @@ struct BwdParams {
 
 // ================================================================== preprocess
 // threads per row = D / 8 (one 16-byte chunk of dO and of O each)
+// One row's D and -LSE2 (TPR threads; `part` = this thread's 16-byte chunk).
+// Rows at or past the sequence's length get D = 0 and -LSE2 = -inf (P = 0).
 template <int D, bool VL>
-__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
+__device__ __forceinline__ void preprocess_row(const BwdParams& p, int b, int h, int q, int64_t row, int part) {
   constexpr int TPR = D / 8;
-  const int64_t row = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / TPR;
-  const int part = threadIdx.x % TPR;
-  const int64_t rows = static_cast<int64_t>(p.dims.B) * p.dims.Hq * p.nq_pad;
-  if (row >= rows) return;
-  const int q = static_cast<int>(row % p.nq_pad);
-  const int bh = static_cast<int>(row / p.nq_pad);
-  const int b = bh / p.dims.Hq, h = bh % p.dims.Hq;
   const SeqRows sr = seq_rows<VL>(p.dims, b);
   const int nq = sr.s.Nq;                       // this sequence's rows
   const int64_t qrow = sr.qoff + static_cast<int64_t>(q);
@@ -115,8 +110,36 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
     p.neg_delta[row] = -acc;
     // LSE [B, Hq, Nq], or [Hq, total_q] for packed sequences
     const int64_t li = VL ? static_cast<int64_t>(h) * p.dims.total_q + qrow
-                                   : static_cast<int64_t>(bh) * p.dims.Nq + q;
+                          : (static_cast<int64_t>(b) * p.dims.Hq + h) * p.dims.Nq + q;
     p.neg_lse2[row] = q < nq ? -p.lse[li] * LOG2E : -INFINITY;
+  }
+}
+
+// Dense: one thread group per row of the padded [B * Hq, nq_pad] layout.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
+  constexpr int TPR = D / 8;
+  const int64_t row = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / TPR;
+  const int64_t rows = static_cast<int64_t>(p.dims.B) * p.dims.Hq * p.nq_pad;
+  if (row >= rows) return;
+  const int q = static_cast<int>(row % p.nq_pad);
+  const int bh = static_cast<int>(row / p.nq_pad);
+  preprocess_row<D, false>(p, bh / p.dims.Hq, bh % p.dims.Hq, q, row, threadIdx.x % TPR);
+}
+
+// Packed sequences: only the query tiles that exist (the dQ plan's units), a
+// persistent grid striding over them; rows of the max-length padding that no
+// kernel reads are left alone.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_varlen_kernel(const BwdParams p, const int* plan_dq) {
+  constexpr int TPR = D / 8, RPP = 256 / TPR;  // threads per row, rows per pass
+  const int total = __ldg(plan_dq);
+  for (int u = blockIdx.x; u < total; u += gridDim.x) {
+    int b, h, qt;
+    plan_unit(plan_dq, p.dims.Hq, u, b, h, qt);
+    const int64_t row0 = (static_cast<int64_t>(b) * p.dims.Hq + h) * p.nq_pad + qt * TILE;
+    for (int r = threadIdx.x / TPR; r < TILE; r += RPP)
+      preprocess_row<D, true>(p, b, h, qt * TILE + r, row0 + r, threadIdx.x % TPR);
   }
 }
 
@@ -1021,10 +1044,19 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   p.nq_pad = a.nq_pad;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
+  // 0) packed sequences: the dQ plan (the query tiles that exist) serves preprocess and dQ
+  if (VL && (a.parts & 5)) {
+    cudaError_t e = launch_varlen_plan(a.dims, VARLEN_PLAN_DQ, q_tiles(a.dims), a.dims.Hq, a.plan_dq, a.status, st);
+    if (e != cudaSuccess) return e;
+  }
   // 1) preprocess
   if (a.parts & 1) {
-    const int64_t threads = static_cast<int64_t>(a.dims.B) * a.dims.Hq * a.nq_pad * (D / 8);
-    bwd_preprocess_kernel<D, VL><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(p);
+    if (VL) {
+      bwd_preprocess_varlen_kernel<D><<<4 * a.num_sms, 256, 0, st>>>(p, a.plan_dq);
+    } else {
+      const int64_t threads = static_cast<int64_t>(a.dims.B) * a.dims.Hq * a.nq_pad * (D / 8);
+      bwd_preprocess_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(p);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1051,11 +1083,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     p.counter = a.counters + 1;
     p.total_units = dq_units(a.dims);
-    p.plan = a.plan_dq;
-    if (VL) {
-      e = launch_varlen_plan(a.dims, VARLEN_PLAN_DQ, q_tiles(a.dims), a.dims.Hq, a.plan_dq, a.status, st);
-      if (e != cudaSuccess) return e;
-    }
+    p.plan = a.plan_dq;  // built above
     kern<<<imax(1, imin(p.total_units, a.num_sms)), 384, DqLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
                                                                                    a.tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

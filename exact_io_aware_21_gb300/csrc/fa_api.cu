@@ -431,7 +431,14 @@ int fa_quantize_fp8(const fa_tensor_t* x, int B, int N, int H, int d, int block_
   a.head_amax = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + FA_WS_HEADER_BYTES);
   a.nblk = cdiv(N, TILE);
   a.per_block = block_rows != 0;
+  int sms = 0;
+  if ((rc = device_info(&sms))) return rc;
+  a.num_sms = sms;
+  a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
+  a.timeout_ns = g_timeout_ns;
+  if ((rc = make_map(&a.tm_x, x->ptr, B, N, H, d, x->stride_b, x->stride_n, x->stride_h))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((rc = clear_header(ws, st))) return rc;
   if (!a.per_block) {
     cudaError_t e = cudaMemsetAsync(a.head_amax, 0, static_cast<size_t>(B) * H * sizeof(unsigned), st);
     if (e != cudaSuccess) return cuda_fail(e, FA_ERR_CUDA);

@@ -8,8 +8,8 @@
 // at strides 1, 2, ..., d/2), the codes come from it directly (the block scale
 // absorbs any constant factor), and 1 / sqrt(d) goes into the scale.
 //
-// One CTA of 128 threads per block of rows, thread = row (rows staged through
-// shared memory with coalesced loads and stores).  Every rounding that
+// Persistent CTAs of 128 threads stream 128-row blocks, thread = row, the next
+// block's TMA load overlapping the current block's work.  Every rounding that
 // decides a code is an IEEE round-to-nearest fp32 operation (sums, 448 / amax,
 // y * inv) followed by the hardware's round-to-nearest-even E4M3 conversion, so
 // the codes are reproducible operation by operation.  HBM-bound: 2 bytes read
@@ -22,127 +22,176 @@ namespace {
 
 constexpr float E4M3_MAX = 448.f;
 
-// Shared-memory staging: the block's rows are loaded and stored with coalesced
-// 16-byte accesses (a warp covers whole rows), and each thread works on one row
-// from shared memory.  Row pitch padded by 16 bytes so that the row-per-thread
-// accesses of a quarter warp fall in distinct banks.
+// A persistent CTA streams 128-row blocks through three shared-memory stages:
+// the TMA loads of the next two blocks (64-column boxes, 128-byte swizzle) are
+// in flight while all threads transform and encode the current one, thread =
+// row.  Once every row is in registers the block's codes are written over its
+// own stage (row pitch padded by 16 bytes: the row-per-thread writes of a
+// quarter warp fall in distinct banks) and stored with coalesced 16-byte writes.
 template <int D>
 struct QuantSmem {
-  static constexpr int IN_PITCH = D * 2 + 16;   // bf16 row
-  static constexpr int OUT_PITCH = D + 16;      // code row
-  static constexpr int BYTES = 128 * IN_PITCH + 128 * OUT_PITCH;
+  static constexpr int STAGES = 3;
+  static constexpr int BOX = 128 * 128;        // one 64-column box of 128 rows (bytes)
+  static constexpr int STAGE = D * 2 * 128;    // a block of bf16 rows: D / 64 boxes
+  static constexpr int OUT_PITCH = D + 16;     // code row (written over the stage)
+  static_assert(128 * OUT_PITCH <= STAGE, "codes fit in their stage");
+  static constexpr int OFF_BAR = STAGES * STAGE;
+  static constexpr int BYTES = OFF_BAR + 64;
+  static constexpr int ALLOC = BYTES + 1024;   // 1024-byte alignment of the stages
 };
 
 template <int D, bool HAD, int MODE>  // MODE 0: block scales; 1: per-head max pass; 2: per-head codes
-__global__ void __launch_bounds__(128) quantize_kernel(const QuantLaunch p) {
+__global__ void __launch_bounds__(128) quantize_kernel(const __grid_constant__ CUtensorMap tm_x, const QuantLaunch p) {
   using S = QuantSmem<D>;
-  extern __shared__ __align__(16) uint8_t qsm[];
-  uint8_t* s_in = qsm;
-  uint8_t* s_out = qsm + 128 * S::IN_PITCH;
+  extern __shared__ __align__(1024) uint8_t qraw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qraw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);  // [STAGES]
   __shared__ float s_signs[D];
   __shared__ float s_red[4];
-  const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int n0 = blk * 128;
-  const int rows = min(128, p.N - n0);
+  const Ctl ctl{p.status, p.timeout_ns};
+  const int total = p.B * p.H * p.nblk;
+  const int r = threadIdx.x;
   if (HAD)
-    for (int i = threadIdx.x; i < D; i += 128) s_signs[i] = p.signs[i];
-
-  // coalesced load of the block: chunk c = (row, 16-byte piece)
-  constexpr int CPR = D * 2 / 16;  // 16-byte chunks per bf16 row
-  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(p.x) + b * p.sb + h * p.sh;
-#pragma unroll
-  for (int c = threadIdx.x; c < 128 * CPR; c += 128) {  // all of a thread's loads in flight at once
-    const int r = c / CPR, q = c % CPR;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (r < rows) w = *reinterpret_cast<const uint4*>(xb + static_cast<int64_t>(n0 + r) * p.sn + q * 8);
-    *reinterpret_cast<uint4*>(s_in + r * S::IN_PITCH + q * 16) = w;
+    for (int i = r; i < D; i += 128) s_signs[i] = p.signs[i];
+  if (r == 0) {
+    for (int k = 0; k < S::STAGES; ++k) mbar_init(&full[k], 1);
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_x);
   }
   __syncthreads();
+  auto issue = [&](int unit, int stage) {  // unit = (b * H + h) * nblk + blk
+    const int blk = unit % p.nblk, bh = unit / p.nblk;
+    mbar_arrive_expect_tx(&full[stage], S::STAGE);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c)
+      tma_load_4d(smem + stage * S::STAGE + c * S::BOX, &tm_x, &full[stage], c * 64, bh % p.H, blk * 128, bh / p.H);
+  };
+  if (r == 0)
+    for (int k = 0; k < S::STAGES - 1; ++k)
+      if (static_cast<int>(blockIdx.x + k * gridDim.x) < total) issue(blockIdx.x + k * gridDim.x, k);
 
-  const int r = threadIdx.x;
-  float y[D];
+  int i = 0;
+  for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++i) {
+    const int st = i % S::STAGES;
+    const int ahead = unit + (S::STAGES - 1) * gridDim.x;
+    // that stage held the block before this one, released at the end of the last iteration
+    if (r == 0 && ahead < total) issue(ahead, (i + S::STAGES - 1) % S::STAGES);
+    const bool ok = mbar_wait(&full[st], (i / S::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_LOAD);
+    if (!__syncthreads_and(ok)) break;
+    const int blk = unit % p.nblk, bh = unit / p.nblk, b = bh / p.H, h = bh % p.H;
+    const int rows = min(128, p.N - blk * 128);  // rows past N were read as zeros
+
+    // this thread's row, un-swizzled: 16-byte chunk c of a box row sits at chunk c ^ (row & 7)
+    float y[D];
+    const uint8_t* in = smem + st * S::STAGE + r * 128;
 #pragma unroll
-  for (int q = 0; q < D / 8; ++q) {
-    const uint4 w = *reinterpret_cast<const uint4*>(s_in + r * S::IN_PITCH + q * 16);
-    const float2 a = unpack_bf16(w.x), bb = unpack_bf16(w.y), c = unpack_bf16(w.z), d = unpack_bf16(w.w);
-    y[8 * q + 0] = a.x;
-    y[8 * q + 1] = a.y;
-    y[8 * q + 2] = bb.x;
-    y[8 * q + 3] = bb.y;
-    y[8 * q + 4] = c.x;
-    y[8 * q + 5] = c.y;
-    y[8 * q + 6] = d.x;
-    y[8 * q + 7] = d.y;
-  }
-  if (HAD) {
+    for (int q = 0; q < D / 8; ++q) {
+      const uint4 w = *reinterpret_cast<const uint4*>(in + (q / 8) * S::BOX + (((q % 8) ^ (r & 7)) << 4));
+      const float2 a = unpack_bf16(w.x), bb = unpack_bf16(w.y), c = unpack_bf16(w.z), d = unpack_bf16(w.w);
+      y[8 * q + 0] = a.x;
+      y[8 * q + 1] = a.y;
+      y[8 * q + 2] = bb.x;
+      y[8 * q + 3] = bb.y;
+      y[8 * q + 4] = c.x;
+      y[8 * q + 5] = c.y;
+      y[8 * q + 6] = d.x;
+      y[8 * q + 7] = d.y;
+    }
+    if (HAD) {  // the same IEEE operations as the scalar transform, two lanes at a time where they pair up
 #pragma unroll
-    for (int i = 0; i < D; ++i) y[i] *= s_signs[i];  // exact: a sign flip
+      for (int k = 0; k < D; k += 2) {  // exact: a sign flip
+        const float2 v = __fmul2_rn(make_float2(y[k], y[k + 1]), make_float2(s_signs[k], s_signs[k + 1]));
+        y[k] = v.x;
+        y[k + 1] = v.y;
+      }
 #pragma unroll
-    for (int hs = 1; hs < D; hs *= 2) {
+      for (int k = 0; k < D; k += 2) {  // stride 1: the pair is (y[k], y[k+1])
+        const float u = y[k], v = y[k + 1];
+        y[k] = __fadd_rn(u, v);
+        y[k + 1] = __fsub_rn(u, v);
+      }
 #pragma unroll
-      for (int i = 0; i < D; ++i) {
-        if (i & hs) continue;
-        const float u = y[i], v = y[i + hs];
-        y[i] = __fadd_rn(u, v);
-        y[i + hs] = __fsub_rn(u, v);
+      for (int hs = 2; hs < D; hs *= 2) {  // strides >= 2: (y[k], y[k+1]) against (y[k+hs], y[k+hs+1])
+#pragma unroll
+        for (int k = 0; k < D; k += 2) {
+          if (k & hs) continue;
+          const float2 u = make_float2(y[k], y[k + 1]), v = make_float2(y[k + hs], y[k + hs + 1]);
+          const float2 sum = __fadd2_rn(u, v);
+          const float2 dif = __fadd2_rn(u, make_float2(-v.x, -v.y));  // u - v, exactly
+          y[k] = sum.x;
+          y[k + 1] = sum.y;
+          y[k + hs] = dif.x;
+          y[k + hs + 1] = dif.y;
+        }
       }
     }
-  }
 
-  float amax;
-  if (MODE == 2) {
-    amax = __uint_as_float(p.head_amax[static_cast<int64_t>(b) * p.H + h]);
-  } else {
-    float am = 0.f;  // rows past N were loaded as zeros
+    float amax;
+    if (MODE == 2) {
+      amax = __uint_as_float(p.head_amax[static_cast<int64_t>(b) * p.H + h]);
+    } else {
+      float am = 0.f;
 #pragma unroll
-    for (int i = 0; i < D; ++i) am = fmaxf(am, fabsf(y[i]));
+      for (int k = 0; k < D; k += 2) am = fmax3(am, fabsf(y[k]), fabsf(y[k + 1]));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = am;
-    __syncthreads();
-    amax = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      if ((r & 31) == 0) s_red[r >> 5] = am;
+      __syncthreads();
+      amax = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+    }
     if (MODE == 1) {  // non-negative floats order like their bit patterns
-      if (threadIdx.x == 0) atomicMax(p.head_amax + static_cast<int64_t>(b) * p.H + h, __float_as_uint(amax));
-      return;
-    }
-  }
-
-  const float inv = amax > 0.f ? __fdiv_rn(E4M3_MAX, amax) : 0.f;
+      if (r == 0) atomicMax(p.head_amax + static_cast<int64_t>(b) * p.H + h, __float_as_uint(amax));
+    } else {
+      uint8_t* s_out = smem + st * S::STAGE;  // the codes go over the rows just read
+      if (MODE == 2) __syncthreads();         // (blocks with a max already synchronised after reading)
+      const float inv = amax > 0.f ? __fdiv_rn(E4M3_MAX, amax) : 0.f;
 #pragma unroll
-  for (int q = 0; q < D / 16; ++q) {
-    uint32_t w[4];
+      for (int q = 0; q < D / 16; ++q) {
+        uint32_t w[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = 16 * q + 4 * e;
-      w[e] = pack4_e4m3(__fmul_rn(y[i], inv), __fmul_rn(y[i + 1], inv), __fmul_rn(y[i + 2], inv),
-                        __fmul_rn(y[i + 3], inv));
-    }
-    *reinterpret_cast<uint4*>(s_out + r * S::OUT_PITCH + q * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  __syncthreads();
-  constexpr int CPO = D / 16;  // 16-byte chunks per code row
-  uint8_t* ob = static_cast<uint8_t*>(p.out) + b * p.ob + h * p.oh;
+        for (int e = 0; e < 4; ++e) {
+          const int k = 16 * q + 4 * e;
+          const float2 a = __fmul2_rn(make_float2(y[k], y[k + 1]), make_float2(inv, inv));
+          const float2 c = __fmul2_rn(make_float2(y[k + 2], y[k + 3]), make_float2(inv, inv));
+          w[e] = pack4_e4m3(a.x, a.y, c.x, c.y);
+        }
+        *reinterpret_cast<uint4*>(s_out + r * S::OUT_PITCH + q * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      __syncthreads();
+      constexpr int CPO = D / 16;  // 16-byte chunks per code row
+      uint8_t* ob = static_cast<uint8_t*>(p.out) + b * p.ob + h * p.oh;
 #pragma unroll 4
-  for (int c = threadIdx.x; c < rows * CPO; c += 128) {
-    const int rr = c / CPO, q = c % CPO;
-    *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(n0 + rr) * p.on + q * 16) =
-        *reinterpret_cast<const uint4*>(s_out + rr * S::OUT_PITCH + q * 16);
+      for (int c = r; c < rows * CPO; c += 128) {
+        const int rr = c / CPO, q = c % CPO;
+        *reinterpret_cast<uint4*>(ob + static_cast<int64_t>(blk * 128 + rr) * p.on + q * 16) =
+            *reinterpret_cast<const uint4*>(s_out + rr * S::OUT_PITCH + q * 16);
+      }
+      if (r == 0 && (MODE == 0 || blk == 0)) {
+        float sc = amax > 0.f ? __fdiv_rn(amax, E4M3_MAX) : 0.f;
+        if (HAD) sc = __fmul_rn(sc, D == 128 ? 0.0883883476483184405f : 0.125f);  // 1 / sqrt(d)
+        const int64_t bhi = static_cast<int64_t>(b) * p.H + h;
+        p.scales[MODE == 0 ? bhi * p.nblk + blk : bhi] = sc;
+      }
+    }
+    __syncthreads();  // the stage, the code rows and s_red are free for the next block
   }
-  if (threadIdx.x == 0 && (MODE == 0 || blk == 0)) {
-    float sc = amax > 0.f ? __fdiv_rn(amax, E4M3_MAX) : 0.f;
-    if (HAD) sc = __fmul_rn(sc, D == 128 ? 0.0883883476483184405f : 0.125f);  // 1 / sqrt(d)
-    const int64_t bh = static_cast<int64_t>(b) * p.H + h;
-    p.scales[MODE == 0 ? bh * p.nblk + blk : bh] = sc;
+  // loads issued for blocks this CTA gave up on must land before exit
+  if (r == 0) {
+    const int n_issued = total > static_cast<int>(blockIdx.x)
+                             ? (total - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                             : 0;
+    for (int k = i; k < n_issued && k < i + S::STAGES; ++k)
+      mbar_wait(&full[k % S::STAGES], (k / S::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
   }
 }
 
 template <int D, bool HAD, int MODE>
 cudaError_t launch_quantize_mode(const QuantLaunch& a, cudaStream_t st) {
-  const dim3 grid(a.nblk, a.H, a.B);
   auto kern = quantize_kernel<D, HAD, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QuantSmem<D>::BYTES);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QuantSmem<D>::ALLOC);
   if (e != cudaSuccess) return e;
-  kern<<<grid, 128, QuantSmem<D>::BYTES, st>>>(a);
+  const int total = a.B * a.H * a.nblk;
+  kern<<<imax(1, imin(total, 2 * a.num_sms)), 128, QuantSmem<D>::ALLOC, st>>>(a.tm_x, a);
   return cudaGetLastError();
 }
 

@@ -100,6 +100,10 @@ struct QuantLaunch {       // E4M3 codes of a bf16 [B, N, H, d] tensor
   unsigned* head_amax;     // per-head pass: [B, H] zeroed workspace
   int nblk;                // ceil(N / 128)
   int per_block;
+  CUtensorMap tm_x;        // x as 4-D map, box 64 x 1 x 128 x 1, 128-byte swizzle
+  int* status;             // workspace status word (a wait that ran out)
+  unsigned long long timeout_ns;
+  int num_sms;
 };
 cudaError_t launch_quantize(const QuantLaunch& a, cudaStream_t st);
 

@@ -762,15 +762,29 @@ def run_ours(args):
 
 def profile_case(name):
     """Two forward + backward passes of one named workload through the public API
-    (a name ending in ``_fp8``: two quantise + FP8 forward passes instead).
+    (a name ending in ``_fp8``: two quantise + FP8 forward passes instead; a
+    decode workload: two decodes, ``_paged16`` over its cache in pages of 16).
 
     A short, fixed program for ncu captures (the first pass warms up; capture the
     second with ``-s``).  Prints nothing but "ok"."""
     import exact_io_aware_21_gb300 as fa
     from exact_io_aware_21_gb300 import inputs
 
-    fp8 = name.endswith("_fp8")
-    w = {x.name: x for x in inputs.ALL}[name[:-4] if fp8 else name]
+    fp8, paged = name.endswith("_fp8"), name.endswith("_paged16")
+    w = {x.name: x for x in inputs.ALL}[name[:-4] if fp8 else name[:-8] if paged else name]
+    if w.decode:  # two split-KV decodes (contiguous cache, or its shuffled pages of 16 keys)
+        x = inputs.make(w, device="cuda", with_do=False)
+        if paged:
+            pc = paged_cache(x, 16, seed=w.seed)
+            lens = pc["lens"]
+            for _ in range(2):
+                fa.decode_paged(x["q"], pc["kc"], pc["vc"], pc["table"], lens, max_seqlen=w.Nk, scale=w.scale)
+        else:
+            for _ in range(2):
+                fa.decode(x["q"], x["k"], x["v"], scale=w.scale)
+        torch.cuda.synchronize()
+        print("ok")
+        return 0
     x = inputs.make(w, device="cuda", with_do=not fp8)
     if fp8:  # quantise (Hadamard on Q and K) and run the FP8 forward, twice
         sg = inputs.hadamard_signs(w.d, seed=w.d).cuda()

@@ -200,6 +200,39 @@ def test_fp8_arguments_rejected_before_any_gpu_work(lib):
     assert lib.fa_quantize_fp8_workspace_size(0, 3) == 0
 
 
+def test_varlen_arguments_rejected_before_any_gpu_work(lib):
+    s = ctypes.byref(shape(3, 2, 2, 500, 500, 64, causal=True))          # B sequences, packed totals
+    sw = ctypes.byref(shape(3, 2, 2, 500, 500, 64, window=(10, 0)))
+    pk = lambda ptr=FAKE: tens(ptr, sb=0, sn=2 * 64, sh=64)  # noqa: E731
+
+    def fwd(cq=FAKE, ck=FAKE, mq=300, mk=300, sh=s):
+        return lib.fa_fwd_varlen(pk(), pk(), pk(), cq, ck, mq, mk, pk(), FAKE, None, sh, FAKE, 1 << 20, None)
+    assert fwd(cq=None) == 1 and fwd(ck=None) == 1
+    assert fwd(mq=0) == 1 and fwd(mk=501) == 1                           # longest length outside [1, total]
+    assert fwd(sh=sw) == 1                                              # no window with packing
+    assert lib.fa_fwd_varlen(pk(), pk(), pk(), FAKE, FAKE, 300, 300, pk(), FAKE, None, s, FAKE, 64, None) == 3
+    assert lib.fa_fwd_varlen_workspace_size(s, 300) >= 256 + 4 * (4 + 2 + 1 + 3)
+    assert lib.fa_fwd_varlen_workspace_size(s, 0) == 0
+    assert lib.fa_bwd_varlen_workspace_size(s, 300) > lib.fa_bwd_varlen_workspace_size(s, 100) > 0
+    assert lib.fa_bwd_varlen(pk(), pk(), pk(), FAKE, FAKE, 0, 300, pk(), FAKE, None, pk(), pk(), pk(), pk(), s, FAKE,
+                             1 << 30, None) == 1
+
+
+def test_blocksparse_arguments_rejected_before_any_gpu_work(lib):
+    s = ctypes.byref(shape(1, 2, 2, 1000, 1000, 64))
+
+    def fwd(rp=FAKE, ci=FAKE, nnz=5, sh=s):
+        return lib.fa_fwd_blocksparse(tens(), tens(), tens(), rp, ci, nnz, tens(), FAKE, None, sh, FAKE, 1 << 20,
+                                      None)
+    assert fwd(rp=None) == 1 and fwd(ci=None) == 1 and fwd(nnz=-1) == 1
+    assert fwd(sh=ctypes.byref(shape(1, 2, 2, 1000, 131200, 64))) == 1      # more than 1024 key tiles
+    assert fwd(sh=ctypes.byref(shape(1, 2, 2, 1000, 1000, 64, window=(5, 5)))) == 1
+    big = ctypes.byref(shape(1, 2, 2, 131200, 1000, 64))
+    assert lib.fa_bwd_blocksparse(tens(), tens(), tens(), FAKE, FAKE, 5, tens(), FAKE, None, tens(), tens(), tens(),
+                                  tens(), big, FAKE, 1 << 30, None) == 1
+    assert lib.fa_bwd_blocksparse_workspace_size(s, 400) > lib.fa_bwd_blocksparse_workspace_size(s, 0) > 0
+
+
 def test_workspace_sizes(lib):
     s = S(2, 16, 16, 4096, 4096, causal=True)
     assert lib.fa_fwd_workspace_size(s) >= 256

@@ -505,11 +505,22 @@ size_t fa_bwd_varlen_workspace_size(const fa_shape_t* s, int max_seqlen_q) {
   return bwd_ws_bytes(s, max_seqlen_q) + bwd_plan_bytes(s, max_seqlen_q);
 }
 
-// The block-sparse backward adds the tile bitmap and the two filtered lists.
+// The block-sparse backward adds the two filtered lists, the dK/dV segment
+// plan and the pool of partial tiles.  Split key tiles hold fewer than
+// min(2 P, W / 16) partial tiles in all (P = SP_PLAN_PARALLELISM, W = the
+// iterations of all heads, at most B * Hkv * (Hq / Hkv) * nnz; fa_sparse.cu).
+size_t sparse_pool_slots(const fa_shape_t* s, int nnz) {
+  const size_t w = static_cast<size_t>(s->B) * s->Hkv * (s->Hq / s->Hkv) * static_cast<size_t>(nnz);
+  const size_t bound = (w + 15) / 16;
+  return bound < 2 * SP_PLAN_PARALLELISM ? bound : 2 * SP_PLAN_PARALLELISM;
+}
+
 size_t bwd_sparse_bytes(const fa_shape_t* s, int nnz) {
   const size_t nqt = cdiv(s->Nq, TILE), nkt = cdiv(s->Nk, TILE);
-  return round_up(nqt * nkt, 256) + round_up((nqt + 1) * sizeof(int), 256) +
-         round_up((nkt + 1) * sizeof(int), 256) + 2 * round_up(static_cast<size_t>(nnz) * sizeof(int) + 4, 256);
+  return round_up((nqt + 1) * sizeof(int), 256) + round_up((nkt + 1) * sizeof(int), 256) +
+         2 * round_up(static_cast<size_t>(nnz) * sizeof(int) + 4, 256) +
+         round_up(SP_PLAN_INTS * sizeof(int), 256) +
+         sparse_pool_slots(s, nnz) * TILE * 2 * s->d * sizeof(float);
 }
 
 static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v,
@@ -561,8 +572,9 @@ static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const
     sl.nqt = nqt;
     sl.nkt = nkt;
     sl.causal = s->causal;
-    sl.bitmap = reinterpret_cast<uint8_t*>(w);
-    w += round_up(static_cast<size_t>(nqt) * nkt, 256);
+    sl.group = s->Hq / s->Hkv;
+    sl.heads = s->B * s->Hkv;
+    sl.pool_slots = static_cast<int>(sparse_pool_slots(s, sp->nnz));
     sl.rows_ptr = reinterpret_cast<int*>(w);
     w += round_up((nqt + 1) * sizeof(int), 256);
     sl.cols_ptr = reinterpret_cast<int*>(w);
@@ -570,6 +582,11 @@ static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const
     sl.rows_idx = reinterpret_cast<int*>(w);
     w += round_up(static_cast<size_t>(sp->nnz) * sizeof(int) + 4, 256);
     sl.cols_idx = reinterpret_cast<int*>(w);
+    w += round_up(static_cast<size_t>(sp->nnz) * sizeof(int) + 4, 256);
+    sl.dkdv_plan = reinterpret_cast<int*>(w);
+    w += round_up(SP_PLAN_INTS * sizeof(int), 256);
+    a.sp_plan = sl.dkdv_plan;
+    a.sp_pool = reinterpret_cast<float*>(w);
     a.rows_ptr = sl.rows_ptr;
     a.rows_idx = sl.rows_idx;
     a.cols_ptr = sl.cols_ptr;

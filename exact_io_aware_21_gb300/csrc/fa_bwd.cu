@@ -63,6 +63,8 @@ struct BwdParams {
   const int* rows_idx;
   const int* cols_ptr;  // ... and query tiles of each key tile (ascending)
   const int* cols_idx;
+  const int* sp_plan;   // block-sparse: the dK/dV segment plan
+  float* sp_pool;       // ... and the partial tiles of split key tiles
 };
 
 // ================================================================== preprocess
@@ -207,6 +209,19 @@ __device__ __forceinline__ void store_acc_rows(uint32_t t_acc, int col0, float m
   }
 }
 
+// Store accumulator columns [col0, col0 + NC) of this thread's TMEM lane as fp32 at dst.
+template <int NC>
+__device__ __forceinline__ void store_acc_f32(uint32_t t_acc, int col0, float* dst) {
+#pragma unroll
+  for (int cc = 0; cc < NC / 32; ++cc) {
+    uint32_t v[32];
+    tmem_ld32(t_acc + col0 + cc * 32, v);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d4[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+
 // ================================================================== dK / dV
 template <int D>
 struct DkvLayout {
@@ -252,6 +267,9 @@ __device__ __forceinline__ DkvBars dkv_bars(uint8_t* smem) {
 
 struct DkvUnit {
   int b, kvh, kt, q0, nqi, n_it;
+  int k0;            // first iteration (block-sparse segment; else 0): iteration k covers
+                     // query head kvh * g + (k0 + k) / nqi and query tile (k0 + k) % nqi
+  int slot;          // block-sparse split key tile: its partial tile (else -1: write dK, dV)
   const int* qlist;  // block-sparse: the key tile's query tiles (else q0, q0 + 1, ...)
   SeqRows sr;  // the unit's sequence (packed sequences: its own lengths and row offsets)
   bool work;   // the key tile holds keys that some query sees
@@ -276,7 +294,20 @@ template <int MASK, bool VL, bool SP>
 __device__ __forceinline__ DkvUnit dkv_decode(const BwdParams& p, int u) {
   const Dims& s = p.dims;
   DkvUnit r;
-  if (VL) {  // plan level m = the key tile counted from the sequence's end
+  r.k0 = 0;
+  r.slot = -1;
+  int seg_n = 0;
+  if (SP) {  // segment-major: unit u = segment u / (B * Hkv) of head group u % (B * Hkv)
+    const int heads = s.B * s.Hkv, bh = u % heads;
+    const int4 e = __ldg(reinterpret_cast<const int4*>(p.sp_plan + SP_PLAN_SEGS) + u / heads);
+    r.b = bh / s.Hkv;
+    r.kvh = bh % s.Hkv;
+    r.kt = e.x;
+    r.k0 = e.y;
+    seg_n = e.z;
+    r.slot = e.w >= 0 ? bh * __ldg(p.sp_plan + 1) + e.w : -1;
+    r.sr = seq_rows<VL>(s, r.b);
+  } else if (VL) {  // plan level m = the key tile counted from the sequence's end
     int m;
     plan_unit(p.plan, s.Hkv, u, r.b, r.kvh, m);
     r.sr = seq_rows<VL>(s, r.b);
@@ -299,7 +330,7 @@ __device__ __forceinline__ DkvUnit dkv_decode(const BwdParams& p, int u) {
   }
   const bool keys = r.kt < k_tiles(su);
   r.nqi = keys ? imax(0, qhi - r.q0) : 0;
-  r.n_it = (s.Hq / s.Hkv) * r.nqi;
+  r.n_it = SP ? seg_n : (s.Hq / s.Hkv) * r.nqi;
   r.work = r.n_it > 0;
   r.zero = keys && !r.work;
   return r;
@@ -319,7 +350,8 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const Ctl ctl{p.status, p.timeout_ns};
   const Dims& s = p.dims;
-  const int total = VL ? __ldg(p.plan) : p.total_units;  // units (packed sequences: from the plan)
+  // units: packed sequences and block-sparse from their plans
+  const int total = VL ? __ldg(p.plan) : SP ? __ldg(p.sp_plan) * s.B * s.Hkv : p.total_units;
   const int g = s.Hq / s.Hkv;
 
   if (threadIdx.x == 0) {
@@ -374,7 +406,8 @@ __global__ void __launch_bounds__(384, 1)
             ok = false;
             break;
           }
-          const int hq = w.kvh * g + k / w.nqi, qi = SP ? __ldg(w.qlist + k % w.nqi) : w.q0 + k % w.nqi;
+          const int kk = w.k0 + k;
+          const int hq = w.kvh * g + kk / w.nqi, qi = SP ? __ldg(w.qlist + kk % w.nqi) : w.q0 + kk % w.nqi;
           uint8_t* base = smem + L::OFF_ST + st * L::STAGE;
           const int64_t row0 = (static_cast<int64_t>(w.b) * s.Hq + hq) * p.nq_pad + qi * TILE;
           mbar_arrive_expect_tx(&bar.st_full[st], 2 * L::TB + 1024);
@@ -386,8 +419,8 @@ __global__ void __launch_bounds__(384, 1)
           bulk_load(base + 2 * L::TB, p.neg_lse2 + row0, 512, &bar.st_full[st]);
           bulk_load(base + 2 * L::TB + 512, p.neg_delta + row0, 512, &bar.st_full[st]);
           if (k + 1 < w.n_it) {  // the next iteration's Q and dO into L2 while this stage waits its turn
-            const int hq1 = w.kvh * g + (k + 1) / w.nqi;
-            const int qi1 = SP ? __ldg(w.qlist + (k + 1) % w.nqi) : w.q0 + (k + 1) % w.nqi;
+            const int hq1 = w.kvh * g + (kk + 1) / w.nqi;
+            const int qi1 = SP ? __ldg(w.qlist + (kk + 1) % w.nqi) : w.q0 + (kk + 1) % w.nqi;
             for (int c = 0; c < D / 64; ++c) {
               tma_prefetch_l2_4d(&tm_q, c * 64, hq1, w.sr.qoff + qi1 * TILE, tb);
               tma_prefetch_l2_4d(&tm_do, c * 64, hq1, w.sr.qoff + qi1 * TILE, tb);
@@ -520,7 +553,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint8_t* stage = smem + L::OFF_ST + (q % L::STAGES) * L::STAGE;
         const float* nl2 = reinterpret_cast<const float*>(stage + 2 * L::TB);  // -LSE2[query]
         const float* nd = nl2 + 128;                                            // -D[query]
-        const int qi = SP ? __ldg(w.qlist + k % w.nqi) : w.q0 + k % w.nqi;
+        const int qi = SP ? __ldg(w.qlist + (w.k0 + k) % w.nqi) : w.q0 + k % w.nqi;
         // rows (keys) see only part of the tile's queries: the band's edges, or causal's diagonal
         const bool part = MASK == MASK_BAND ? (qi < qfull_lo || qi > qfull_hi)
                                             : (MASK == MASK_CAUSAL && qi == w.kt);
@@ -619,8 +652,14 @@ __global__ void __launch_bounds__(384, 1)
                            w.kvh * p.dv.sh;
       __nv_bfloat16* dk0 = reinterpret_cast<__nv_bfloat16*>(p.dk.ptr) + w.b * p.dk.sb + krow0 * p.dk.sn +
                            w.kvh * p.dk.sh;
-      store_acc_rows<D / 2>(tdV, (c0 / 64) * (D / 2), 1.f, dv0, p.dv.sn, su.Nk - key0, scratch);
-      store_acc_rows<D / 2>(tdK, (c0 / 64) * (D / 2), p.scale, dk0, p.dk.sn, su.Nk - key0, scratch);
+      if (SP && w.slot >= 0) {  // a segment of a split key tile: its fp32 partial, row r = [dV | dK]
+        float* part = p.sp_pool + (static_cast<int64_t>(w.slot) * TILE + r) * (2 * D) + (c0 / 64) * (D / 2);
+        store_acc_f32<D / 2>(tdV, (c0 / 64) * (D / 2), part);
+        store_acc_f32<D / 2>(tdK, (c0 / 64) * (D / 2), part + D);
+      } else {
+        store_acc_rows<D / 2>(tdV, (c0 / 64) * (D / 2), 1.f, dv0, p.dv.sn, su.Nk - key0, scratch);
+        store_acc_rows<D / 2>(tdK, (c0 / 64) * (D / 2), p.scale, dk0, p.dk.sn, su.Nk - key0, scratch);
+      }
       sq += w.n_it;
     }
   }
@@ -1021,6 +1060,47 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// ================================================================== block-sparse reduce
+// dK, dV of the split key tiles: each output element is the sum of its tile's
+// partials in segment order (a fixed order: deterministic), dK times the scale.
+// One float4 of a partial row per thread and step; grid-stride.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_sparse_reduce_kernel(const BwdParams p) {
+  const Dims& s = p.dims;
+  const int sph = __ldg(p.sp_plan + 1), nsplit = __ldg(p.sp_plan + 2);
+  constexpr int ROW4 = 2 * D / 4;          // float4s per partial row
+  constexpr int TILE4 = TILE * ROW4;       // ... per partial tile
+  const int64_t total = static_cast<int64_t>(s.B) * s.Hkv * nsplit * TILE4;
+  const float4* pool = reinterpret_cast<const float4*>(p.sp_pool);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % TILE4);
+    const int64_t t = i / TILE4;
+    const int j = static_cast<int>(t % nsplit), bh = static_cast<int>(t / nsplit);
+    const int4 e = __ldg(reinterpret_cast<const int4*>(p.sp_plan + SP_PLAN_SPLITS) + j);
+    const int row = c / ROW4, col = (c % ROW4) * 4;
+    const int key = e.x * TILE + row;
+    if (key >= s.Nk) continue;
+    const float4* src = pool + (static_cast<int64_t>(bh) * sph + e.y) * TILE4 + c;
+    float4 a = __ldg(src);
+    for (int k = 1; k < e.z; ++k) {
+      const float4 x = __ldg(src + static_cast<int64_t>(k) * TILE4);
+      a.x += x.x;
+      a.y += x.y;
+      a.z += x.z;
+      a.w += x.w;
+    }
+    const int b = bh / s.Hkv, kvh = bh % s.Hkv;
+    const OutRows& o = col < D ? p.dv : p.dk;
+    const float m = col < D ? 1.f : p.scale;
+    const float2 lo = __fmul2_rn(make_float2(a.x, a.y), make_float2(m, m));
+    const float2 hi = __fmul2_rn(make_float2(a.z, a.w), make_float2(m, m));
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(o.ptr) + b * o.sb + static_cast<int64_t>(key) * o.sn +
+                         kvh * o.sh + (col < D ? col : col - D);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(lo.x, lo.y), pack_bf16(hi.x, hi.y));
+  }
+}
+
 template <int D, int MASK, bool VL = false, bool SP = false>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   BwdParams p;
@@ -1029,6 +1109,8 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   p.rows_idx = a.rows_idx;
   p.cols_ptr = a.cols_ptr;
   p.cols_idx = a.cols_idx;
+  p.sp_plan = a.sp_plan;
+  p.sp_pool = a.sp_pool;
   p.dims = a.dims;
   p.scale = a.scale;
   p.scale_log2 = a.scale * LOG2E;
@@ -1072,9 +1154,14 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
       e = launch_varlen_plan(a.dims, VARLEN_PLAN_DKDV, k_tiles(a.dims), a.dims.Hkv, a.plan_dkdv, a.status, st);
       if (e != cudaSuccess) return e;
     }
-    kern<<<imax(1, imin(p.total_units, a.num_sms)), 384, DkvLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
-                                                                                     a.tm_do, p);
+    // block-sparse: the unit count is on the device; fill the GPU and let the plan's count stop the CTAs
+    const int grid = SP ? a.num_sms : imax(1, imin(p.total_units, a.num_sms));
+    kern<<<grid, 384, DkvLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (SP) {
+      bwd_sparse_reduce_kernel<D><<<2 * a.num_sms, 256, 0, st>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
   // 3) dQ
   if (a.parts & 4) {

@@ -57,11 +57,13 @@ struct BwdLaunch {
   int parts;       // bit 0: preprocess, bit 1: dK/dV, bit 2: dQ
   int* plan_dkdv;  // packed sequences: workspace for the device-side work plans
   int* plan_dq;
-  // block-sparse (rows_ptr != nullptr): filtered lists (see SparseLaunch)
+  // block-sparse (rows_ptr != nullptr): filtered lists and the dK/dV plan (see SparseLaunch)
   const int* rows_ptr;
   const int* rows_idx;
   const int* cols_ptr;
   const int* cols_idx;
+  const int* sp_plan;
+  float* sp_pool;  // partial tiles of split key tiles
 };
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st);
 
@@ -113,14 +115,34 @@ struct SparseLaunch {
   const int* row_ptr;   // caller's table: [nqt + 1], col_idx [nnz]
   const int* col_idx;
   int nnz, nqt, nkt, causal;
-  uint8_t* bitmap;      // workspace [nqt * nkt]
+  int group;            // query heads per K/V head
+  int heads;            // B * Hkv: copies of the dK/dV plan's segments
+  int pool_slots;       // partial tiles the workspace holds (all heads)
   int* rows_ptr;        // out [nqt + 1], rows_idx [<= nnz]: key tiles of each query tile
   int* rows_idx;
   int* cols_ptr;        // out [nkt + 1], cols_idx [<= nnz]: query tiles of each key tile
   int* cols_idx;
+  int* dkdv_plan;       // out [SP_PLAN_INTS]: the dK/dV segment plan (layout below)
   int* status;
 };
 cudaError_t launch_sparse_lists(const SparseLaunch& a, cudaStream_t st);
+
+// Block-sparse dK/dV segment plan.  A key tile's iterations (query heads of the
+// group x its listed query tiles, flattened) form one unit, or, when there are
+// more than `seg` of them, near-equal segments of at most `seg`; each segment
+// of a split tile owns a partial tile (fp32 dV | dK, [128][2d]) that a reduce
+// kernel sums in segment order.  The segments of one head group are ordered
+// longest first and repeated for every (batch, K/V head).
+//   [0] segments per head group  [1] partial slots per head group
+//   [2] split key tiles          [3] seg
+//   SP_PLAN_SEGS + 4 i: segment i = {key tile, first iteration, iterations, slot or -1}
+//   SP_PLAN_SPLITS + 4 j: split tile j = {key tile, first slot, segments, 0}
+constexpr int SP_PLAN_PARALLELISM = 152;  // the units' target: one GB300's SMs (the plan is device-independent)
+constexpr int SP_MIN_SEGMENT = 32;
+constexpr int SP_MAX_SEGMENTS = 1024 + 2 * SP_PLAN_PARALLELISM;
+constexpr int SP_PLAN_SEGS = 4;
+constexpr int SP_PLAN_SPLITS = SP_PLAN_SEGS + 4 * SP_MAX_SEGMENTS;
+constexpr int SP_PLAN_INTS = SP_PLAN_SPLITS + 4 * 1024;
 
 // Device-side work plan of packed sequences (levels: forward pairs, dQ query
 // tiles, dK/dV key tiles from the end); `plan` holds varlen_plan_ints(nlev, B) ints.

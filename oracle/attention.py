@@ -430,6 +430,62 @@ def attention_blocksparse_backward(q, k, v, do, row_ptr, col_idx, scale, causal=
     return dq, dk, dv
 
 
+def attention_blocksparse_backward_sampled(q, k, v, do, row_ptr, col_idx, scale, causal, b, h, q_rows, k_rows,
+                                           block=128):
+    """Sampled rows of the block-sparse backward of one query head (b, h).
+
+    Returns (dQ[q_rows], dK_h[k_rows], dV_h[k_rows]), dK_h/dV_h being head h's
+    contributions.  The definition of ``attention_blocksparse_backward`` taken
+    one query block at a time over the key blocks it lists (P is 0 elsewhere,
+    so the other key blocks add nothing): with K_L, V_L the listed keys,
+        P = softmax(scale Q_i K_L^T) (causal: keys after the row masked),
+        dP = dO_i V_L^T, D = rowsum(P o dP), dS = P o (dP - D),
+        dQ_i = scale dS K_L, dK_L += scale dS^T Q_i, dV_L += P^T dO_i.
+    Query blocks that hold no sampled row and list no block of a sampled key
+    row are skipped."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Nq, Nk, Hq, Hkv, d = _check_shapes(q, k, v)
+    if causal and Nq != Nk:
+        raise ValueError("causal attention is defined here for Nq == Nk only")
+    nqb, nkb = -(-Nq // block), -(-Nk // block)
+    M = block_mask_from_csr(row_ptr, col_idx, nqb, nkb)
+    kv = h // (Hq // Hkv)
+    q_rows, k_rows = np.asarray(q_rows), np.asarray(k_rows)
+    dq = np.zeros((len(q_rows), d))
+    dk = np.zeros((len(k_rows), d))
+    dv = np.zeros((len(k_rows), d))
+    k_blocks = set((k_rows // block).tolist())
+    q_blocks = set((q_rows // block).tolist())
+    for i in range(nqb):
+        listed = np.flatnonzero(M[i])
+        if len(listed) == 0 or not (i in q_blocks or k_blocks & set(listed.tolist())):
+            continue
+        rows = np.arange(i * block, min(Nq, (i + 1) * block))
+        keys = np.concatenate([np.arange(j * block, min(Nk, (j + 1) * block)) for j in listed])
+        vis = np.ones((len(rows), len(keys)), dtype=bool)
+        if causal:
+            vis &= keys[None, :] <= rows[:, None]
+        seen = vis.any(axis=1)
+        S = np.where(vis, scale * (q[b, rows, h, :] @ k[b, keys, kv, :].T), NEG_INF)
+        m = np.where(seen, S.max(axis=1), 0.0)
+        E = np.where(vis, np.exp(S - m[:, None]), 0.0)
+        P = E / np.where(seen, E.sum(axis=1), 1.0)[:, None]
+        dO = do[b, rows, h, :]
+        dP = dO @ v[b, keys, kv, :].T
+        D = (P * dP).sum(axis=1, keepdims=True)
+        dS = P * (dP - D)
+        for t, r in enumerate(q_rows):
+            if r // block == i:
+                dq[t] = scale * (dS[r - i * block] @ k[b, keys, kv, :])
+        pos = {int(key): c for c, key in enumerate(keys)}
+        for t, key in enumerate(k_rows):
+            c = pos.get(int(key))
+            if c is not None:
+                dk[t] += scale * (dS[:, c] @ q[b, rows, h, :])
+                dv[t] += P[:, c] @ dO
+    return dq, dk, dv
+
+
 def gather_paged(cache, block_table, b, length):
     """Logical rows [0, length) of sequence b from a paged cache [pages, page_size, H, d]:
     row r is at page block_table[b, r // page_size], row r % page_size."""

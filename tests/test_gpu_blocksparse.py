@@ -1,10 +1,12 @@
-"""GPU parity of the block-sparse forward against the fp64 oracle, through
-fa_fwd_blocksparse.
+"""GPU parity of the block-sparse forward and backward against the fp64 oracle,
+through fa_fwd_blocksparse and fa_bwd_blocksparse.
 
 Covers random tables over ragged shapes (causal and not, grouped heads, d = 64
-and 128, rows with no listed tile), every tile listed against the dense kernel
-(bit for bit), a sliding-window + global-token pattern at N = 8192 on sampled
-query tiles, the residual, and tables that break the rules (reported)."""
+and 128, rows with no listed tile, key tiles no row lists), every tile listed
+against the dense kernels (bit for bit), a sliding-window + global-token
+pattern at N = 8192 on sampled query tiles, the residual, tables that break
+the rules (reported), key tiles long enough for the dK/dV plan to split (plan,
+determinism, parity) and the local + global pattern at N = 16384 sampled."""
 
 import numpy as np
 import pytest
@@ -179,3 +181,111 @@ def test_backward_every_tile_listed_equals_the_dense_kernels(causal, d):
     torch.cuda.synchronize()
     for a, b in zip((dq, dk, dv), g2):
         assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ split key tiles
+def _ru(x, a=256):
+    return -(-x // a) * a
+
+
+def plan_rule(M, causal, B, Hkv, g):
+    """The dK/dV segment rule, written out on the host: per key tile n = g x (query
+    tiles listing it, tiles above the diagonal dropped under causal); seg =
+    max(32, ceil(B Hkv sum(n) / 152)); a tile with n > seg becomes ceil(n / seg)
+    segments, each with its own partial tile."""
+    Mc = M & np.tril(np.ones_like(M)) if causal else M
+    n = g * Mc.sum(axis=0)
+    seg = max(32, -(-(B * Hkv * int(n.sum())) // 152))
+    return seg, np.where(n > seg, -(-n // seg), 1)
+
+
+def plan_header(ws, B, Hq, Nq, Nk, nnz):
+    """[segments, partial slots, split tiles, seg] of the plan in a block-sparse
+    backward workspace (after the status header, the -LSE2 and -D rows, the two
+    list pointer arrays and the two index arrays)."""
+    nqt, nkt = -(-Nq // 128), -(-Nk // 128)
+    off = 256 + 2 * _ru(B * Hq * nqt * 128 * 4) + _ru((nqt + 1) * 4) + _ru((nkt + 1) * 4) + 2 * _ru(nnz * 4 + 4)
+    return ws[off:off + 16].view(torch.int32).cpu().numpy()
+
+
+SPLIT_CASES = [  # B, Hq, Hkv, N, d, causal, local tiles (+ key tile 0 for everyone; not causal: + the last)
+    (1, 4, 1, 4096, 128, True, 3),
+    (2, 8, 2, 2048, 64, False, 2),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,causal,local", SPLIT_CASES)
+def test_backward_split_key_tiles(B, Hq, Hkv, N, d, causal, local):
+    """Key tiles every query tile lists have more iterations than a segment: the
+    plan splits them, their fp32 partial tiles are summed in segment order.
+    Checks the plan against the rule, the gradients against the oracle and that
+    two calls agree bit for bit."""
+    nt = N // 128
+    M = np.array(inputs.local_global_tiles(nt, local, 1))
+    if not causal:
+        M[:, nt - 1] = True
+    seg, nseg = plan_rule(M, causal, B, Hkv, Hq // Hkv)
+    assert (nseg > 1).any()
+    x = inputs.shape_inputs(B, Hq, Hkv, N, N, d, seed=N + d + 11)
+    scale = 1 / np.sqrt(d)
+    rp, ci = csr(M)
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    rpd, cid = torch.from_numpy(rp).to(DEV), torch.from_numpy(ci).to(DEV)
+    o, lse, res = fa.forward_blocksparse(q, k, v, rpd, cid, causal=causal, scale=scale, residual=True)
+    s = fa.binding._dims(q, k, scale, causal)
+    ws = torch.zeros(fa.library().fa_bwd_blocksparse_workspace_size(fa.binding.ctypes.byref(s), len(ci)),
+                     dtype=torch.uint8, device=DEV)
+    grads = []
+    for _ in range(2):
+        g = [torch.empty_like(t) for t in (q, k, v)]
+        fa.fa_bwd_blocksparse(q, k, v, rpd, cid, o, lse, do, *g, s, ws, res)
+        torch.cuda.synchronize()
+        grads.append(g)
+    rc, st = fa.binding.device_status(ws)
+    assert rc == 0 and st == 0
+    hdr = plan_header(ws, B, Hq, N, N, len(ci))
+    assert list(hdr) == [int(nseg.sum()), int(nseg[nseg > 1].sum()), int((nseg > 1).sum()), seg]
+    for a, b in zip(*grads):
+        assert torch.equal(a, b)
+    rq, rk, rv = A.attention_blocksparse_backward(x["q"], x["k"], x["v"], x["do"], rp, ci, scale, causal)
+    tag = f"split blocksparse bwd {B}x{Hq}/{Hkv} N={N} d={d} causal={causal}"
+    dq, dk, dv = grads[0]
+    assert_grad(dq, rq, "dQ " + tag)
+    assert_grad(dk, rk, "dK " + tag)
+    assert_grad(dv, rv, "dV " + tag)
+
+
+@pytest.mark.slow
+def test_backward_local_global_n16384_sampled():
+    """The block-sparse backward at the bench's workload (local 8 + global 1, causal,
+    GQA 32/8, N = 16384, d = 128), where the global key tile is split: sampled rows
+    of dQ and of one K/V head's dK, dV (the global tile's among them) against the
+    oracle."""
+    w = inputs.BLOCKSPARSE_N16384
+    nt = w.Nq // 128
+    M = np.array(inputs.local_global_tiles(nt, w.extra["local_tiles"], w.extra["global_tiles"]))
+    seg, nseg = plan_rule(M, w.causal, w.B, w.Hkv, w.Hq // w.Hkv)
+    assert nseg[0] > 1
+    x = inputs.make(w, device=DEV)
+    rp, ci = csr(M)
+    rpd, cid = torch.from_numpy(rp).to(DEV), torch.from_numpy(ci).to(DEV)
+    o, lse, res = fa.forward_blocksparse(x["q"], x["k"], x["v"], rpd, cid, causal=True, scale=w.scale, residual=True)
+    dq, dk, dv = fa.backward_blocksparse(x["q"], x["k"], x["v"], rpd, cid, o, lse, x["do"], causal=True,
+                                         scale=w.scale, o_residual=res)
+    torch.cuda.synchronize()
+    assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+    rng = np.random.default_rng(23)
+    b, kvh, g = 0, 5, w.Hq // w.Hkv
+    q_rows = np.unique(np.concatenate([[0, 127, 77 * 128 + 3, w.Nq - 1], rng.integers(0, w.Nq, 12)]))
+    k_rows = np.unique(np.concatenate([[0, 5, 127, 77 * 128 + 3, w.Nk - 1], rng.integers(0, w.Nk, 12)]))
+    xc = {n: x[n].cpu() for n in ("q", "k", "v", "do")}
+    sk = np.zeros((len(k_rows), w.d))
+    sv = np.zeros((len(k_rows), w.d))
+    for h in range(kvh * g, (kvh + 1) * g):
+        rq, rk, rv = A.attention_blocksparse_backward_sampled(xc["q"], xc["k"], xc["v"], xc["do"], rp, ci, w.scale,
+                                                              True, b, h, q_rows, k_rows)
+        assert_grad(dq[b, q_rows, h], rq, f"dQ b{b} h{h}")
+        sk += rk
+        sv += rv
+    assert_grad(dk[b, k_rows, kvh], sk, f"dK b{b} kvh{kvh}")
+    assert_grad(dv[b, k_rows, kvh], sv, f"dV b{b} kvh{kvh}")

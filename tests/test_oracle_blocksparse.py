@@ -117,3 +117,30 @@ def test_backward_central_differences(causal):
             am = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
             num = (loss(*ap) - loss(*am)) / (2 * eps)
             assert abs(num - gr[idx]) < 1e-6 * max(1.0, abs(num)), (name, idx, num, gr[idx])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_sampled_equals_the_full_backward(causal):
+    """The per-block sampled backward gives the full backward's rows (head by head;
+    dK, dV as one head's contributions, summed over the group)."""
+    block, nb = 4, 5
+    N = nb * block - 2
+    q, k, v = qkv(2, 4, 2, N, N, 3)
+    do = RNG.standard_normal(q.shape)
+    M = RNG.random((nb, nb)) < 0.5
+    M[np.arange(nb), 0] = True
+    M[3] = False
+    rp, ci = csr(M)
+    dq, dk, dv = A.attention_blocksparse_backward(q, k, v, do, rp, ci, 0.4, causal, block=block)
+    q_rows, k_rows = np.array([0, 5, 13, N - 1]), np.array([0, 3, 9, N - 1])
+    for b in range(2):
+        for kvh in range(2):
+            sk, sv = np.zeros((4, 3)), np.zeros((4, 3))
+            for h in (2 * kvh, 2 * kvh + 1):
+                rq, rk, rv = A.attention_blocksparse_backward_sampled(q, k, v, do, rp, ci, 0.4, causal, b, h,
+                                                                      q_rows, k_rows, block=block)
+                assert np.allclose(rq, dq[b, q_rows, h], atol=1e-12)
+                sk += rk
+                sv += rv
+            assert np.allclose(sk, dk[b, k_rows, kvh], atol=1e-12)
+            assert np.allclose(sv, dv[b, k_rows, kvh], atol=1e-12)

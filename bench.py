@@ -772,7 +772,9 @@ def run_ours(args):
 def profile_case(name):
     """Two forward + backward passes of one named workload through the public API
     (a name ending in ``_fp8``: two quantise + FP8 forward passes instead; a
-    decode workload: two decodes, ``_paged16`` over its cache in pages of 16).
+    decode workload: two decodes, ``_paged16`` over its cache in pages of 16;
+    the packed-sequence and block-sparse workloads through their own entry
+    points).
 
     A short, fixed program for ncu captures (the first pass warms up; capture the
     second with ``-s``).  Prints nothing but "ok"."""
@@ -805,11 +807,30 @@ def profile_case(name):
         torch.cuda.synchronize()
         print("ok")
         return 0
-    for _ in range(2):
-        o, lse, res = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, residual=True,
-                                 window=w.window)
-        fa.backward(x["q"], x["k"], x["v"], o, lse, x["do"], causal=w.causal, scale=w.scale, o_residual=res,
-                    window=w.window)
+    if "n_seqs" in w.extra:  # packed sequences: [total, H, d] and cu_seqlens
+        lens = varlen_lens(w)
+        px = {k: x[k][0] for k in ("q", "k", "v", "do")}
+        cu = torch.tensor([0] + list(itertools.accumulate(lens)), dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            o, lse, res = fa.forward_varlen(px["q"], px["k"], px["v"], cu, cu, max(lens), max(lens), causal=w.causal,
+                                            scale=w.scale, residual=True)
+            fa.backward_varlen(px["q"], px["k"], px["v"], cu, cu, max(lens), max(lens), o, lse, px["do"],
+                               causal=w.causal, scale=w.scale, o_residual=res)
+    elif "local_tiles" in w.extra:  # block-sparse: the local + global table
+        M = blocksparse_table(w)
+        rp = torch.tensor([0] + list(itertools.accumulate(sum(r) for r in M)), dtype=torch.int32, device="cuda")
+        ci = torch.tensor([j for r in M for j, on in enumerate(r) if on], dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            o, lse, res = fa.forward_blocksparse(x["q"], x["k"], x["v"], rp, ci, causal=w.causal, scale=w.scale,
+                                                 residual=True)
+            fa.backward_blocksparse(x["q"], x["k"], x["v"], rp, ci, o, lse, x["do"], causal=w.causal, scale=w.scale,
+                                    o_residual=res)
+    else:
+        for _ in range(2):
+            o, lse, res = fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, residual=True,
+                                     window=w.window)
+            fa.backward(x["q"], x["k"], x["v"], o, lse, x["do"], causal=w.causal, scale=w.scale, o_residual=res,
+                        window=w.window)
     torch.cuda.synchronize()
     print("ok")
     return 0

@@ -374,8 +374,11 @@ def make_legs(device, seed):
                   lse=torch.empty((w.B, w.Hq, w.Nq), dtype=torch.float32, device=device),
                   ws=torch.zeros(lib.fa_decode_workspace_size(ctypes.byref(s), S), dtype=torch.uint8,
                                  device=device))
-        if paged:  # every sequence at full length, its pages scattered over the cache
+        if paged:  # every sequence at full length, its pages scattered over the cache; its own split count
             st.update(paged_cache(x, PAGED[1], seed=w.seed + seed))
+            st["S"] = 0
+            st["ws"] = torch.zeros(lib.fa_decode_paged_workspace_size(ctypes.byref(s), 0, PAGED[1]),
+                                   dtype=torch.uint8, device=device)
         state[name] = st
 
         def dec_fn(st=st):
@@ -711,7 +714,7 @@ def run_ours(args):
         else:
             ms = l.ms["decode"]
             legs_out[l.name] = {"ms": ms, "gbs": l.work / ms / 1e6, "frac_of_hbm_peak": l.work / ms / 1e6 /
-                                peaks["hbm_gbs"], "num_splits": state[l.name]["S"]}
+                                peaks["hbm_gbs"], "num_splits": state[l.name]["S"] or "auto"}
 
     # roofline of the dominant kernel: the launch with the largest share of the step
     dl, dp = max(((l, p) for l in step_legs for p, _ in l.fns if p != "bwd_pre"), key=lambda lp: lp[0].ms[lp[1]])

@@ -56,6 +56,7 @@ SIGNATURES = {
     "fa_decode": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _I, _VP, _SZ, _VP]),
     "fa_decode_partials_layout": (_I, [_PS, _I, ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "fa_decode_paged": (_I, [_PT, _PT, _PT, _VP, _I, _VP, _I, _I, _PT, _VP, _PS, _I, _VP, _SZ, _VP]),
+    "fa_decode_paged_workspace_size": (_SZ, [_PS, _I, _I]),
     "fa_decode_noalloc_max_bytes": (_SZ, []),
     "fa_decode_noalloc": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _I, _VP]),
     "fa_get_device_status": (_I, [_VP, _VP, _PI]),
@@ -320,7 +321,7 @@ def decode_paged(q, k_cache, v_cache, block_table, seqlens_k, max_seqlen=None, s
     s = shape(B, Hq, Hkv, Nq, int(max_seqlen), d, scale, False)
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
-    ws = _ws(library().fa_decode_workspace_size(ctypes.byref(s), int(num_splits)), q.device)
+    ws = _ws(library().fa_decode_paged_workspace_size(ctypes.byref(s), int(num_splits), k_cache.shape[1]), q.device)
     fa_decode_paged(q, k_cache, v_cache, block_table, seqlens_k, o, lse, s, num_splits, ws)
     return o, lse
 

@@ -106,6 +106,25 @@ int make_map_u8(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ALIGN;
 }
 
+// Paged cache [num_pages, page_size, H, d] viewed as (channel, row, head, page)
+// for the head-group decode: boxes of 64 channels x 16 rows x 8 heads, which land
+// in shared memory as 128 rows of 128 bytes, head-major (16 rows per head).
+int make_map_heads(CUtensorMap* m, const void* ptr, int pages, int page_size, int H, int d, int64_t sb, int64_t sn,
+                   int64_t sh) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return FA_ERR_CUDA;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(pages)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn) * 2, static_cast<cuuint64_t>(sh) * 2,
+                           static_cast<cuuint64_t>(sb) * 2};
+  cuuint32_t box[4] = {64, 16, static_cast<cuuint32_t>(DECODE_HEAD_GROUP), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ALIGN;
+}
+
 // ---- argument checks ----------------------------------------------------------------
 int check_shape(const fa_shape_t* s) {
   if (!s) return FA_ERR_INVALID;
@@ -192,6 +211,37 @@ int decode_splits_resolved(const fa_shape_t* s, int requested, int sms) {
   }
   if (S > tiles) S = tiles;
   return decode_nsplits(s->Nk, S);
+}
+
+// The head-group paged decode: does it apply, and its splits per sequence.  The
+// same cost model over 16-key slices, with B * Hkv / 8 CTAs per split.
+bool decode_head_groups(const fa_shape_t* s, int page_size) {
+  return s->Hkv % DECODE_HEAD_GROUP == 0 && page_size % 16 == 0;
+}
+
+int decode_splits_hg(const fa_shape_t* s, int requested, int sms) {
+  const int slices = cdiv(s->Nk, 16);
+  int S = requested;
+  if (S <= 0) {
+    const int units = s->B * (s->Hkv / DECODE_HEAD_GROUP);
+    int best = 1;
+    double best_cost = 1e30;
+    for (int c = 1; c <= 1024 && c <= slices; ++c) {
+      const int waves = cdiv(units * c, sms > 0 ? sms : 1);
+      const double cost = static_cast<double>(waves) * (cdiv(slices, c) + 4) + 0.02 * c;
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = c;
+      }
+    }
+    S = best;
+  }
+  return S > slices ? slices : S;
+}
+
+size_t decode_ws_bytes(const fa_shape_t* s, int S) {
+  const size_t rows = static_cast<size_t>(s->B) * s->Hq * s->Nq * S;
+  return FA_WS_HEADER_BYTES + round_up(rows * sizeof(float), 256) + round_up(rows * s->d * sizeof(float), 256);
 }
 
 }  // namespace
@@ -676,8 +726,21 @@ int fa_decode_partials_layout(const fa_shape_t* s, int num_splits, size_t* lse_o
 size_t fa_decode_workspace_size(const fa_shape_t* s, int num_splits) {
   const int S = fa_decode_num_splits(s, num_splits);
   if (S <= 0) return 0;
-  const size_t rows = static_cast<size_t>(s->B) * s->Hq * s->Nq * S;
-  return FA_WS_HEADER_BYTES + round_up(rows * sizeof(float), 256) + round_up(rows * s->d * sizeof(float), 256);
+  return decode_ws_bytes(s, S);
+}
+
+// The paged decode's split count: the head-group grid's where it applies.
+static int paged_splits(const fa_shape_t* s, int num_splits, int page_size, int sms) {
+  return decode_head_groups(s, page_size) ? decode_splits_hg(s, num_splits, sms)
+                                          : decode_splits_resolved(s, num_splits, sms);
+}
+
+size_t fa_decode_paged_workspace_size(const fa_shape_t* s, int num_splits, int page_size) {
+  if (check_shape(s) != FA_OK || page_size < 1) return 0;
+  int sms = 148;
+  if (num_splits <= 0 && device_info(&sms) != FA_OK) sms = 148;
+  const int S = paged_splits(s, num_splits, page_size, sms);
+  return S > 0 ? decode_ws_bytes(s, S) : 0;
 }
 
 int fa_decode(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor_t* vc, const fa_tensor_t* o,
@@ -736,29 +799,37 @@ int fa_decode_paged(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor
   if (static_cast<int64_t>(max_pages) * page_size < s->Nk) return FA_ERR_INVALID;
   int sms = 0;
   if ((rc = device_info(&sms))) return rc;
-  const int S = decode_splits_resolved(s, num_splits, sms);
-  if ((rc = check_ws(ws, ws_bytes, fa_decode_workspace_size(s, num_splits)))) return rc;
+  const int S = paged_splits(s, num_splits, page_size, sms);
+  if ((rc = check_ws(ws, ws_bytes, decode_ws_bytes(s, S)))) return rc;
   DecodeLaunch a;
   memset(&a, 0, sizeof(a));
   a.dims = dims_of(s);
   a.d = s->d;
   a.scale = s->scale;
-  const int box_rows = small ? page_size : TILE;
-  if ((rc = make_map(&a.tm_k, kc->ptr, num_pages, page_size, s->Hkv, s->d, kc->stride_b, kc->stride_n,
-                     kc->stride_h, box_rows)) ||
-      (rc = make_map(&a.tm_v, vc->ptr, num_pages, page_size, s->Hkv, s->d, vc->stride_b, vc->stride_n,
-                     vc->stride_h, box_rows)))
-    return rc;
+  a.head_groups = decode_head_groups(s, page_size) ? 1 : 0;
+  if (a.head_groups) {
+    if ((rc = make_map_heads(&a.tm_k, kc->ptr, num_pages, page_size, s->Hkv, s->d, kc->stride_b, kc->stride_n,
+                             kc->stride_h)) ||
+        (rc = make_map_heads(&a.tm_v, vc->ptr, num_pages, page_size, s->Hkv, s->d, vc->stride_b, vc->stride_n,
+                             vc->stride_h)))
+      return rc;
+  } else {
+    const int box_rows = small ? page_size : TILE;
+    if ((rc = make_map(&a.tm_k, kc->ptr, num_pages, page_size, s->Hkv, s->d, kc->stride_b, kc->stride_n,
+                       kc->stride_h, box_rows)) ||
+        (rc = make_map(&a.tm_v, vc->ptr, num_pages, page_size, s->Hkv, s->d, vc->stride_b, vc->stride_n,
+                       vc->stride_h, box_rows)))
+      return rc;
+  }
   a.q = q->ptr;
   a.q_sb = q->stride_b;
   a.q_sn = q->stride_n;
   a.q_sh = q->stride_h;
   a.o = rows_of(o);
   a.lse = lse;
-  size_t lo = 0, oo = 0;
-  fa_decode_partials_layout(s, num_splits, &lo, &oo);
-  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(ws) + lo);
-  a.o_part = reinterpret_cast<float*>(static_cast<char*>(ws) + oo);
+  const size_t prow = static_cast<size_t>(s->B) * s->Hq * s->Nq * S;  // partials: [B, Hq, Nq, S]
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(ws) + FA_WS_HEADER_BYTES);
+  a.o_part = reinterpret_cast<float*>(static_cast<char*>(ws) + FA_WS_HEADER_BYTES + round_up(prow * sizeof(float), 256));
   a.num_splits = S;
   a.chunk = 0;  // per sequence, in the kernel
   a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);

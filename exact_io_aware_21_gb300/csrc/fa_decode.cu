@@ -31,6 +31,16 @@
 // the end of a sequence inside its last tile hold whatever the page (or an
 // earlier tile) left in shared memory: their scores are masked and their V rows
 // are zeroed in registers, so even NaN there cannot reach O.
+//
+// Head groups (HG).  A page holds all K/V heads of its rows side by side, so
+// with small pages the per-head kernel needs eight 16-row boxes per 128-key
+// tile and the copy engine's per-box cost, not HBM, sets the pace.  When Hkv
+// is a multiple of 8 and pages are whole 16-row slices, one CTA serves 8 K/V
+// heads instead: a stage is one 16-key slice of a page for all 8 heads (one
+// box of 16 rows x 8 heads x 64 channels per half of d, i.e. four boxes of
+// 16 KB for K and V), laid out exactly as a 128-key tile of one head, and
+// compute warp w works on head 8 g + w.  Each warp keeps its own softmax
+// state and writes its own partial; there is no merge across warps.
 #include <math.h>
 
 #include "fa_kernels.h"
@@ -40,7 +50,8 @@ namespace fa {
 namespace {
 
 constexpr float LN2 = 0.69314718055994530942f;
-constexpr int WARPS = 8;              // compute warps, 16 keys of each tile apiece
+constexpr int WARPS = 8;              // compute warps, 16 keys of each tile apiece (HG: one head each)
+static_assert(WARPS == DECODE_HEAD_GROUP, "a head group is one head per compute warp");
 constexpr int THREADS = 32 * (WARPS + 1);
 
 template <int D>
@@ -102,20 +113,23 @@ __device__ __forceinline__ uint32_t swz(int key, int ch) {
   return (ch >> 6) * (TILE * 128) + key * 128 + ((((ch & 63) >> 3) ^ (key & 7)) << 4) + ((ch & 7) << 1);
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool HG>
 __global__ void __launch_bounds__(THREADS, 1)
     fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecParams p) {
   using L = DecLayout<D>;
+  static_assert(!HG || PAGED, "head groups are a paged layout");
+  constexpr int KT = HG ? 16 : TILE;  // keys per stage: a page slice (all 8 heads) or a tile of one head
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* empty = full + L::STAGES;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = lane_id();
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int kvh = HG ? blockIdx.y * WARPS + (warp < WARPS ? warp : 0) : blockIdx.y;  // this warp's K/V head
   const Dims& s = p.dims;
   const int g = s.Hq / s.Hkv;
   const int rows = g * s.Nq;
-  const int warp = threadIdx.x >> 5, lane = lane_id();
   const Ctl ctl{p.status, p.timeout_ns};
   int len = s.Nk, chunk = p.chunk;  // this sequence's keys and its split length
   if (PAGED) {
@@ -124,11 +138,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (threadIdx.x == 0 && split == 0 && kvh == 0) report(ctl, FA_STATUS_BAD_INPUT);
       len = imax(0, imin(len, s.Nk));
     }
-    chunk = cdiv(cdiv(len, TILE), p.num_splits) * TILE;
+    chunk = cdiv(cdiv(len, KT), p.num_splits) * KT;
   }
   const int k0 = split * chunk;
   const int k1 = imin(len, k0 + chunk);
-  const int ntiles = k1 > k0 ? cdiv(k1 - k0, TILE) : 0;
+  const int ntiles = k1 > k0 ? cdiv(k1 - k0, KT) : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < L::STAGES; ++i) {
@@ -142,7 +156,43 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
 
   if (warp == WARPS) {  // ---------------------------------------------- producer
-    if (!PAGED) {
+    if (HG) {
+      // One lane: slice t is rows [r, r + 16) of one page (page_size is a multiple of
+      // 16), heads 8 blockIdx.y .. + 7; the next slice's page index is read one
+      // slice ahead.  Coordinates of the map: (channel, row, head, page).
+      if (lane == 0) {
+        const int64_t trow = static_cast<int64_t>(b) * p.max_pages;
+        auto page_of = [&](int t) {
+          if (t >= ntiles) return -1;
+          int pg = p.block_table[trow + (k0 + t * KT) / p.page_size];
+          if (pg < 0 || pg >= p.num_pages) {  // reads as zeros (out-of-range TMA box); reported
+            report(ctl, FA_STATUS_BAD_INPUT);
+            pg = p.num_pages;
+          }
+          return pg;
+        };
+        int issued = 0;
+        int next_page = page_of(0);
+        for (int t = 0; t < ntiles; ++t) {
+          const int st = t % L::STAGES;
+          const int page = next_page;
+          next_page = page_of(t + 1);
+          if (!mbar_wait(&empty[st], ((t / L::STAGES) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
+          uint8_t* dst = smem + L::OFF_KV + st * 2 * L::TB;
+          const int row = (k0 + t * KT) % p.page_size;
+          mbar_arrive_expect_tx(&full[st], 2 * L::TB);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(dst + c * (TILE * 128), &tm_k, &full[st], c * 64, row, blockIdx.y * WARPS, page);
+            tma_load_4d(dst + L::TB + c * (TILE * 128), &tm_v, &full[st], c * 64, row, blockIdx.y * WARPS, page);
+          }
+          ++issued;
+        }
+        for (int t = imax(0, issued - L::STAGES); t < issued; ++t)
+          mbar_wait(&full[t % L::STAGES], (t / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
+      }
+      return;  // the compute warps do not merge: no block-wide barrier follows
+    } else if (!PAGED) {
       if (lane == 0) {
         int issued = 0;
         for (int t = 0; t < ntiles; ++t) {
@@ -249,7 +299,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     const uint32_t kb = smem_u32(smem + L::OFF_KV + st * 2 * L::TB);
     const uint32_t vb = kb + L::TB;
-    const int key_base = 16 * warp;  // this warp's 16 keys within the tile
+    // this warp's 16 rows of the stage: keys 16 warp .. + 15 of the tile, or (HG)
+    // the slice's 16 keys of this warp's head
+    const int key_base = 16 * warp;
 
     // S = Q K^T for 16 rows x 16 keys (two n8 tiles)
     float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -264,7 +316,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mma_16816(sacc[1], qa[ks], b10, b11);
     }
     // mask keys outside [k0, k1)
-    const int key0 = k0 + t * TILE + key_base;
+    const int key0 = k0 + t * KT + (HG ? 0 : key_base);
     float sv[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -334,6 +386,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   for (int hr = 0; hr < 2; ++hr) {
     l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
     l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
+  }
+  if (HG) {  // one head per warp: its state is the split's (rows gq and gq + 8)
+    if (!ok) return;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int row = gq + 8 * hr;
+      if (row >= rows) continue;
+      const float l = l_run[hr];
+      const float inv = l > 0.f ? 1.f / l : 0.f;  // an empty split: O 0, LSE -inf
+      const int qpos = row / g, hq = kvh * g + row % g;
+      const int64_t prow = ((static_cast<int64_t>(b) * s.Hq + hq) * s.Nq + qpos) * p.num_splits + split;
+      float* op = p.o_part + prow * D + 2 * tq;
+#pragma unroll
+      for (int nt = 0; nt < D / 8; ++nt)
+        *reinterpret_cast<float2*>(op + nt * 8) = make_float2(o[nt][2 * hr] * inv, o[nt][2 * hr + 1] * inv);
+      if (tq == 0) p.lse_part[prow] = l > 0.f ? (m_run[hr] + __log2f(l)) * LN2 : -INFINITY;
+    }
+    return;
   }
   // all compute warps and the producer must be past the pipeline before the
   // stage memory is reused
@@ -431,7 +501,9 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const float* __r
 template <int D>
 cudaError_t launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
   using L = DecLayout<D>;
-  auto kern = a.block_table != nullptr ? fa_decode_split_kernel<D, true> : fa_decode_split_kernel<D, false>;
+  auto kern = a.block_table == nullptr ? fa_decode_split_kernel<D, false, false>
+               : a.head_groups ? fa_decode_split_kernel<D, true, true>
+                               : fa_decode_split_kernel<D, true, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   DecParams p;
@@ -453,7 +525,7 @@ cudaError_t launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
   p.seqlens = a.seqlens;
   p.num_pages = a.num_pages;
   p.page_size = a.page_size;
-  dim3 grid(a.num_splits, a.dims.Hkv, a.dims.B);
+  dim3 grid(a.num_splits, a.head_groups ? a.dims.Hkv / WARPS : a.dims.Hkv, a.dims.B);
   kern<<<grid, THREADS, L::ALLOC, st>>>(a.tm_k, a.tm_v, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

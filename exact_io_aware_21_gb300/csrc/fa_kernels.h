@@ -88,7 +88,11 @@ struct DecodeLaunch {
   const int* seqlens;      // [B] keys of each sequence, 1..Nk
   int num_pages;
   int page_size;           // 16, 32, 64, or a multiple of 128
+  // paged, Hkv % 8 == 0, page_size % 16 == 0: one CTA per 8 K/V heads, 16-key page
+  // slices; tm_k / tm_v then map (channel, row, head, page) with 64 x 16 x 8 boxes
+  int head_groups;
 };
+constexpr int DECODE_HEAD_GROUP = 8;
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t st);
 
 struct QuantLaunch {       // E4M3 codes of a bf16 [B, N, H, d] tensor

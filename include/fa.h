@@ -268,8 +268,9 @@ int fa_decode_partials_layout(const fa_shape_t* shape, int num_splits, size_t* l
  * b is physical page block_table[b * max_pages + i], and sequence b has its own
  * length seqlens_k[b].  Sequence b's logical key r is row r % page_size of page
  * block_table[b * max_pages + r / page_size].  Otherwise as fa_decode: the same
- * q, o, lse, shape (causal 0, Hq/Hkv * Nq <= 16), num_splits and workspace
- * (fa_decode_workspace_size(shape, num_splits)).
+ * q, o, lse, shape (causal 0, Hq/Hkv * Nq <= 16) and num_splits; the
+ * workspace is fa_decode_paged_workspace_size(shape, num_splits, page_size)
+ * bytes.
  *   kcache, vcache [num_pages, page_size, Hkv, d] bf16: stride_b = elements
  *                  between pages, stride_n between rows of a page, stride_h
  *                  between heads (16-byte aligned, multiples of 8 elements)
@@ -281,7 +282,11 @@ int fa_decode_partials_layout(const fa_shape_t* shape, int num_splits, size_t* l
  *   page_size      16, 32, 64, or a multiple of 128
  * Each sequence is cut into whole 128-key tiles by its own length, with the
  * chunk rule of fa_decode applied to seqlens_k[b]; splits past its end
- * contribute nothing.  Keys past a sequence's end are never weighted, whatever
+ * contribute nothing.  When Hkv is a multiple of 8 and page_size a multiple
+ * of 16, one CTA serves 8 K/V heads over 16-key page slices (the copy engine
+ * then moves 16 KB boxes instead of one 2 KB box per page and head): the
+ * splits are whole 16-key slices, chunk = ceil(ceil(len/16)/S)*16, and S is
+ * chosen for that grid when num_splits is 0.  Keys past a sequence's end are never weighted, whatever
  * the page holds there.  Device-side input errors (a length outside [1, Nk], a
  * page index outside [0, num_pages)) set a status bit that
  * fa_get_device_status() returns as FA_ERR_INVALID; such a page reads as zeros.
@@ -292,6 +297,9 @@ int fa_decode_paged(const fa_tensor_t* q, const fa_tensor_t* kcache, const fa_te
                     const int* block_table, int max_pages, const int* seqlens_k, int num_pages, int page_size,
                     const fa_tensor_t* o, float* lse, const fa_shape_t* shape, int num_splits, void* workspace,
                     size_t workspace_bytes, void* stream);
+/* Workspace bytes fa_decode_paged needs for (shape, num_splits, page_size); 0
+ * for an invalid shape. */
+size_t fa_decode_paged_workspace_size(const fa_shape_t* shape, int num_splits, int page_size);
 
 /* ---------------------------------------------------------------------------
  * Decode without allocation.  No counterpart on the pages: this is a service

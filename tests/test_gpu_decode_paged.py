@@ -5,7 +5,9 @@ page tables do not reference hold junk (NaN in one test), which must never
 reach the output.  Also: the key count recovered bit-exactly from LSE with
 Q = 0, equality with the contiguous decode for an identity layout, device-side
 reporting of bad lengths and page indices, and the full decode workload in
-pages of 16 keys with ragged lengths, on sampled heads.
+pages of 16 keys with ragged lengths, on sampled heads.  Shapes with Hkv a
+multiple of 8 and pages of whole 16-row slices take the head-group kernel
+(one CTA per 8 K/V heads); the others the per-head kernel.
 """
 
 import numpy as np
@@ -55,6 +57,11 @@ CASES = [
     (1, 8, 8, 2, [128], 64, 128, 0),
     (4, 32, 8, 4, [300, 1, 2000, 777], 128, 32, 3),
     (2, 4, 2, 1, [4500, 20], 128, 16, 9),       # more splits than the short sequence has tiles
+    # K/V heads in groups of 8 (one CTA per group, 16-key page slices)
+    (2, 16, 8, 2, [1000, 333], 64, 16, 0),
+    (3, 8, 8, 1, [17, 1, 640], 128, 16, 0),
+    (1, 32, 16, 1, [2049], 128, 256, 5),         # two head groups, pages of two tiles
+    (2, 64, 16, 4, [700, 1500], 128, 32, 40),    # 16 packed rows, more splits than needed
 ]
 
 
@@ -70,8 +77,9 @@ def test_paged_decode_matches_oracle(B, Hq, Hkv, Nq, lens, d, page, S):
     assert_fwd(o, lse, o_ref, lse_ref, f"paged {B}x{Hq}/{Hkv}x{Nq} lens={lens} d={d} page={page} S={S}")
 
 
-def test_nan_in_unreferenced_rows_never_reaches_the_output():
-    B, Hq, Hkv, Nq, d, page = 3, 8, 2, 2, 128, 32
+@pytest.mark.parametrize("Hkv,page", [(2, 32), (8, 16)])
+def test_nan_in_unreferenced_rows_never_reaches_the_output(Hkv, page):
+    B, Hq, Nq, d = 3, 8, 2, 128
     lens = [77, 1, 300]
     x = inputs.shape_inputs(B, Hq, Hkv, Nq, max(lens), d, seed=5, with_do=False)
     kc, vc, table = to_pages(x["k"], x["v"], page, seed=11, junk=float("nan"))
@@ -83,10 +91,10 @@ def test_nan_in_unreferenced_rows_never_reaches_the_output():
     assert_fwd(o, lse, o_ref, lse_ref, "NaN junk")
 
 
-@pytest.mark.parametrize("page", [16, 64, 128])
-def test_zero_query_counts_each_sequence_keys_exactly(page):
+@pytest.mark.parametrize("page,Hkv", [(16, 2), (64, 2), (128, 2), (16, 8)])
+def test_zero_query_counts_each_sequence_keys_exactly(page, Hkv):
     lens = [1, 127, 128, 129, 1000, 4095]
-    B, Hq, Hkv, Nq, d = len(lens), 4, 2, 1, 64
+    B, Hq, Nq, d = len(lens), 2 * Hkv, 1, 64
     x = inputs.shape_inputs(B, Hq, Hkv, Nq, max(lens), d, seed=page, with_do=False)
     kc, vc, table = to_pages(x["k"], x["v"], page, seed=page)
     q = torch.zeros(B, Nq, Hq, d, dtype=torch.bfloat16, device=DEV)
@@ -108,8 +116,9 @@ def test_identity_layout_equals_contiguous_decode():
     assert torch.equal(o_p, o_c) and torch.equal(lse_p, lse_c)
 
 
-def test_bad_lengths_and_pages_are_reported_not_faulted():
-    B, Hq, Hkv, Nq, d, page, N = 3, 4, 1, 1, 64, 64, 512
+@pytest.mark.parametrize("Hq,Hkv,page", [(4, 1, 64), (8, 8, 16)])
+def test_bad_lengths_and_pages_are_reported_not_faulted(Hq, Hkv, page):
+    B, Nq, d, N = 3, 1, 64, 512
     x = inputs.shape_inputs(B, Hq, Hkv, Nq, N, d, seed=3, with_do=False)
     kc, vc, table = to_pages(x["k"], x["v"], page, seed=3)
     q = x["q"].to(DEV)
@@ -118,7 +127,7 @@ def test_bad_lengths_and_pages_are_reported_not_faulted():
     import ctypes
 
     def call(lens, tab):
-        ws = torch.zeros(lib.fa_decode_workspace_size(ctypes.byref(s), 0), dtype=torch.uint8, device=DEV)
+        ws = torch.zeros(lib.fa_decode_paged_workspace_size(ctypes.byref(s), 0, page), dtype=torch.uint8, device=DEV)
         o = torch.empty(q.shape, dtype=torch.bfloat16, device=DEV)
         lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=DEV)
         fa.binding.fa_decode_paged(q, kc, vc, tab, torch.tensor(lens, dtype=torch.int32, device=DEV), o, lse, s, 0,

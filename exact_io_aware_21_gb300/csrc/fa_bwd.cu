@@ -79,30 +79,35 @@ __device__ __forceinline__ void preprocess_row(const BwdParams& p, int b, int h,
   const int64_t qrow = sr.qoff + static_cast<int64_t>(q);
   float acc = 0.f;
   if (q < nq) {
+    // all three loads go out before any use (one memory round trip per row)
     const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(p.o.ptr) + b * p.o.sb + qrow * p.o.sn +
                              h * p.o.sh + part * 8;
     const __nv_bfloat16* g = reinterpret_cast<const __nv_bfloat16*>(p.dout.ptr) + b * p.dout.sb +
                              qrow * p.dout.sn + h * p.dout.sh + part * 8;
-    const uint4 ov = *reinterpret_cast<const uint4*>(o);
+    const bool res = p.o_res.ptr != nullptr;  // D = dO . (O + residual)
+    const __nv_bfloat16* rr = res ? reinterpret_cast<const __nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
+                                        qrow * p.o_res.sn + h * p.o_res.sh + part * 8
+                                  : o;
+    // O and the residual are not read again (streaming loads); dO is, by the
+    // dK/dV and dQ kernels that follow, so it is loaded the ordinary way
+    const uint4 ov = __ldcs(reinterpret_cast<const uint4*>(o));
     const uint4 gv = *reinterpret_cast<const uint4*>(g);
+    const uint4 rv = res ? __ldcs(reinterpret_cast<const uint4*>(rr)) : make_uint4(0, 0, 0, 0);
     const uint32_t* ou = reinterpret_cast<const uint32_t*>(&ov);
     const uint32_t* gu = reinterpret_cast<const uint32_t*>(&gv);
+    const uint32_t* ru = reinterpret_cast<const uint32_t*>(&rv);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 a = unpack_bf16(ou[i]), c = unpack_bf16(gu[i]);
       acc = fmaf(a.x, c.x, acc);
       acc = fmaf(a.y, c.y, acc);
     }
-    if (p.o_res.ptr != nullptr) {  // D = dO . (O + residual)
-      const __nv_bfloat16* rr = reinterpret_cast<const __nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
-                                qrow * p.o_res.sn + h * p.o_res.sh + part * 8;
-      const uint4 rv = *reinterpret_cast<const uint4*>(rr);
-      const uint32_t* ru = reinterpret_cast<const uint32_t*>(&rv);
+    if (res) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 a = unpack_bf16(ru[i]), c = unpack_bf16(gu[i]);
-        acc = fmaf(a.x, c.x, acc);
-        acc = fmaf(a.y, c.y, acc);
+        const float2 e = unpack_bf16(ru[i]), c = unpack_bf16(gu[i]);
+        acc = fmaf(e.x, c.x, acc);
+        acc = fmaf(e.y, c.y, acc);
       }
     }
   }
@@ -129,20 +134,21 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) 
   preprocess_row<D, false>(p, bh / p.dims.Hq, bh % p.dims.Hq, q, row, threadIdx.x % TPR);
 }
 
-// Packed sequences: only the query tiles that exist (the dQ plan's units), a
-// persistent grid striding over them; rows of the max-length padding that no
-// kernel reads are left alone.
+// Packed sequences: only the query tiles that exist (the dQ plan's units); rows
+// of the max-length padding that no kernel reads are left alone.  One block per
+// RPP rows of a unit, over a host-side bound on the unit count: blocks past the
+// plan's count return at once.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_varlen_kernel(const BwdParams p, const int* plan_dq) {
-  constexpr int TPR = D / 8, RPP = 256 / TPR;  // threads per row, rows per pass
-  const int total = __ldg(plan_dq);
-  for (int u = blockIdx.x; u < total; u += gridDim.x) {
-    int b, h, qt;
-    plan_unit(plan_dq, p.dims.Hq, u, b, h, qt);
-    const int64_t row0 = (static_cast<int64_t>(b) * p.dims.Hq + h) * p.nq_pad + qt * TILE;
-    for (int r = threadIdx.x / TPR; r < TILE; r += RPP)
-      preprocess_row<D, true>(p, b, h, qt * TILE + r, row0 + r, threadIdx.x % TPR);
-  }
+  constexpr int TPR = D / 8, RPP = 256 / TPR;  // threads per row, rows per block
+  constexpr int BPU = TILE / RPP;              // blocks per unit
+  const int u = blockIdx.x / BPU;
+  if (u >= __ldg(plan_dq)) return;
+  int b, h, qt;
+  plan_unit(plan_dq, p.dims.Hq, u, b, h, qt);
+  const int r = (blockIdx.x % BPU) * RPP + threadIdx.x / TPR;
+  const int64_t row0 = (static_cast<int64_t>(b) * p.dims.Hq + h) * p.nq_pad + qt * TILE;
+  preprocess_row<D, true>(p, b, h, qt * TILE + r, row0 + r, threadIdx.x % TPR);
 }
 
 // ================================================================== shared helpers
@@ -1134,7 +1140,12 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   // 1) preprocess
   if (a.parts & 1) {
     if (VL) {
-      bwd_preprocess_varlen_kernel<D><<<4 * a.num_sms, 256, 0, st>>>(p, a.plan_dq);
+      // units <= Hq x (query tiles of all sequences) <= Hq x (total_q / 128 + B)
+      const int64_t units = static_cast<int64_t>(a.dims.Hq) * (cdiv(a.dims.total_q, TILE) + a.dims.B);
+      const int64_t blocks = units * (TILE / (256 / (D / 8)));
+      if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+      bwd_preprocess_varlen_kernel<D><<<static_cast<unsigned>(imax(1, static_cast<int>(blocks))), 256, 0, st>>>(
+          p, a.plan_dq);
     } else {
       const int64_t threads = static_cast<int64_t>(a.dims.B) * a.dims.Hq * a.nq_pad * (D / 8);
       bwd_preprocess_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(p);

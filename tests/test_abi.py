@@ -250,3 +250,63 @@ def test_binding_rejects_non_cuda_tensors():
 
     with pytest.raises(fa.FAError):
         fa.binding.tdesc(torch.zeros(1, 2, 2, 64, dtype=torch.bfloat16))
+
+
+# ------------------------------------------------------------------ block-sparse dK/dV plan bounds
+def _segment_rule(M, causal, heads, g, P=152, min_seg=32):
+    """The dK/dV segment rule of the block-sparse backward: per key tile n = g x
+    (query tiles listing it, under causal those at or below the diagonal);
+    seg = max(32, ceil(heads * sum(n) / P)); a tile with n > seg becomes
+    ceil(n / seg) segments (else one), each segment of a split tile a partial tile."""
+    nqt, nkt = len(M), len(M[0])
+    n = [g * sum(1 for i in range(nqt) if M[i][j] and (not causal or j <= i)) for j in range(nkt)]
+    seg = max(min_seg, -(-heads * sum(n) // P))
+    nseg = [(-(-x // seg) if x > seg else 1) for x in n]
+    return sum(nseg), heads * sum(k for k in nseg if k > 1)
+
+
+def test_block_sparse_plan_fits_its_bounds(lib):
+    """On random tables, dense rows, one global column and a full table, the plan
+    holds fewer than nkt + 2P segments per head group and fewer partial tiles
+    (all heads) than the workspace's pool: min(2P, ceil(heads * g * nnz / 16))."""
+    import random
+
+    rng = random.Random(5)
+    cases = []
+    for _ in range(300):
+        nqt, nkt = rng.randint(1, 96), rng.randint(1, 96)
+        dens = rng.choice([0.02, 0.1, 0.5, 1.0])
+        M = [[rng.random() < dens for _ in range(nkt)] for _ in range(nqt)]
+        if rng.random() < 0.3:
+            for i in range(nqt):
+                M[i][0] = True                      # a global column
+        cases.append((M, rng.random() < 0.5 and nqt == nkt, rng.choice([1, 2, 8, 32]), rng.choice([1, 2, 4, 8])))
+    cases.append(([[True] * 1024 for _ in range(1024)], False, 1, 8))   # the largest table, full
+    cases.append(([[j == 0 or j == i for j in range(512)] for i in range(512)], True, 64, 4))
+    for M, causal, heads, g in cases:
+        nnz = sum(map(sum, M))
+        segs, slots = _segment_rule(M, causal, heads, g)
+        assert segs < len(M[0]) + 2 * 152
+        assert slots <= min(2 * 152, -(-heads * g * nnz // 16))
+
+
+def test_paged_decode_workspace_covers_its_splits(lib):
+    """The paged decode's workspace: head-group shapes (Hkv % 8 == 0, pages of whole
+    16-row slices) size the partials for their own split count; the others match
+    the contiguous decode's."""
+    size = lib.fa_decode_paged_workspace_size
+    hdr = 256
+
+    def parts(B, Hq, Nq, S, d=128):
+        rows = B * Hq * Nq * S
+        up = lambda x: -(-x // 256) * 256  # noqa: E731
+        return hdr + up(rows * 4) + up(rows * d * 4)
+
+    s8 = S(8, 32, 8, 1, 131072)
+    assert size(s8, 5, 16) == parts(8, 32, 1, 5)                  # explicit splits, head groups
+    assert size(s8, 5000, 16) == parts(8, 32, 1, 5000)
+    assert size(S(1, 8, 8, 1, 1000), 100, 16) == parts(1, 8, 1, 63)  # capped at one 16-key slice each
+    s2 = S(2, 8, 2, 4, 4096)
+    assert size(s2, 0, 16) == lib.fa_decode_workspace_size(s2, 0)  # per-head kernel
+    assert size(s8, 3, 48) == lib.fa_decode_workspace_size(s8, 3)  # pages not of whole 16-row slices
+    assert size(S(1, 8, 8, 1, 0), 0, 16) == 0                      # invalid shape

@@ -132,7 +132,16 @@ int fa_fwd_blocksparse(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tens
  * results are deterministic); the dQ kernel visits each query tile's listed key
  * tiles, the dK/dV kernel each key tile's listing query tiles.  Rows that see
  * no key get dQ = 0; keys no query sees get dK = dV = 0.  Nq, Nk <= 131072.
- * Needs fa_bwd_blocksparse_workspace_size(shape, nnz) bytes. */
+ * A key tile listed by many query tiles (a global column) is cut into
+ * segments so that no SM carries much more than its share: its g x (listing
+ * query tiles) iterations are split when they exceed
+ * max(32, ceil(all heads' iterations / 152)), each segment writes an fp32
+ * partial tile into the workspace, and a reduce kernel sums them in segment
+ * order (the split depends on the table and the shape only, so results stay
+ * deterministic; unsplit tiles are written directly, as by the dense kernel).
+ * Needs fa_bwd_blocksparse_workspace_size(shape, nnz) bytes (lists, the
+ * segment plan and at most min(304, ceil(B Hkv (Hq/Hkv) nnz / 16)) partial
+ * tiles of 128 x 2d floats). */
 size_t fa_bwd_blocksparse_workspace_size(const fa_shape_t* shape, int nnz);
 int fa_bwd_blocksparse(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const int* row_ptr,
                        const int* col_idx, int nnz, const fa_tensor_t* o, const float* lse,

@@ -211,6 +211,7 @@ def plan_header(ws, B, Hq, Nq, Nk, nnz):
 SPLIT_CASES = [  # B, Hq, Hkv, N, d, causal, local tiles (+ key tile 0 for everyone; not causal: + the last)
     (1, 4, 1, 4096, 128, True, 3),
     (2, 8, 2, 2048, 64, False, 2),
+    (1, 8, 2, 2000, 128, False, 2),   # the split last key tile is ragged (80 of 128 keys)
 ]
 
 
@@ -220,7 +221,7 @@ def test_backward_split_key_tiles(B, Hq, Hkv, N, d, causal, local):
     plan splits them, their fp32 partial tiles are summed in segment order.
     Checks the plan against the rule, the gradients against the oracle and that
     two calls agree bit for bit."""
-    nt = N // 128
+    nt = -(-N // 128)
     M = np.array(inputs.local_global_tiles(nt, local, 1))
     if not causal:
         M[:, nt - 1] = True

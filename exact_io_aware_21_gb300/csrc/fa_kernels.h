@@ -114,7 +114,8 @@ struct QuantLaunch {       // E4M3 codes of a bf16 [B, N, H, d] tensor
 cudaError_t launch_quantize(const QuantLaunch& a, cudaStream_t st);
 
 // Block-sparse backward: the caller's CSR table checked and filtered into
-// per-query-tile and per-key-tile lists (ascending), via a tile bitmap.
+// per-query-tile and per-key-tile lists (ascending), via a tile bitmap in
+// shared memory, and the dK/dV segment plan built from the lists' lengths.
 struct SparseLaunch {
   const int* row_ptr;   // caller's table: [nqt + 1], col_idx [nnz]
   const int* col_idx;

@@ -22,15 +22,16 @@ namespace {
 
 constexpr float E4M3_MAX = 448.f;
 
-// A persistent CTA streams 128-row blocks through three shared-memory stages:
-// the TMA loads of the next two blocks (64-column boxes, 128-byte swizzle) are
-// in flight while all threads transform and encode the current one, thread =
-// row.  Once every row is in registers the block's codes are written over its
+// A persistent CTA streams 128-row blocks through two shared-memory stages:
+// the TMA load of the next block (64-column boxes, 128-byte swizzle) is in
+// flight while all threads transform and encode the current one, thread = row.
+// Two stages leave room for three CTAs per SM, whose interleaving hides more
+// of the per-block latency than a deeper ring in fewer CTAs (measured).  Once every row is in registers the block's codes are written over its
 // own stage (row pitch padded by 16 bytes: the row-per-thread writes of a
 // quarter warp fall in distinct banks) and stored with coalesced 16-byte writes.
 template <int D>
 struct QuantSmem {
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = 2;
   static constexpr int BOX = 128 * 128;        // one 64-column box of 128 rows (bytes)
   static constexpr int STAGE = D * 2 * 128;    // a block of bf16 rows: D / 64 boxes
   static constexpr int OUT_PITCH = D + 16;     // code row (written over the stage)
@@ -191,7 +192,7 @@ cudaError_t launch_quantize_mode(const QuantLaunch& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QuantSmem<D>::ALLOC);
   if (e != cudaSuccess) return e;
   const int total = a.B * a.H * a.nblk;
-  kern<<<imax(1, imin(total, 2 * a.num_sms)), 128, QuantSmem<D>::ALLOC, st>>>(a.tm_x, a);
+  kern<<<imax(1, imin(total, 3 * a.num_sms)), 128, QuantSmem<D>::ALLOC, st>>>(a.tm_x, a);
   return cudaGetLastError();
 }
 

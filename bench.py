@@ -4,6 +4,7 @@
 A step is one pass of the whole hot path over synthetic inputs already resident
 in HBM:
   training legs  forward + backward (preprocess, dK/dV, dQ) of
+                 mha_b4_h16_n2048_d64       (B=4, H=16, N=2048, d=64, non-causal)
                  causal_b2_h16_n4096_d128   (B=2, H=16, N=4096, d=128, causal)
                  gqa_causal_b1_hq32_hkv8_n8192_d128_outliers
   decode legs    split-KV decode + combine of
@@ -21,9 +22,18 @@ in HBM:
   fp8 leg        E4M3 quantisation (Q, K per 128-row block after the random
                  Hadamard rotation, V per head) and the FP8 forward of the GQA
                  workload
+The tiny workload (tiny_b1_h1_n256_d64, the oracle's full-size parity case) is
+timed beside the step.
 ``value`` = counted forward + backward FLOPs of the training legs divided by
 their device time (TFLOPS; forward 4*B*H*Nq*Nk*d, halved when causal, backward
-2.5x that).  The window leg is reported beside it with its FLOPs counted over
+2.5x that).  Tensor-core fractions are against the measured burst bf16 peak
+(every launch is timed on its own, at the held clock of a short timed region);
+the sustained figure is printed beside it.  ``targets`` gives the fractions of
+the two N >= 4096, d = 128 workloads and of the decode legs against the bars,
+and ``configs`` every workload of the benchmark plan beside the fp64 oracle
+timed on this host's cores (forward and backward separately; the tiny workload
+whole, as the median of 20 runs; the others on a bounded sample of query rows
+of head (0, 0), decode on one (batch, K/V head)).  The window leg is reported beside it with its FLOPs counted over
 the (query, key) pairs inside the window, and the FP8 leg with the forward's
 count (its roofline is FP8's: twice the measured bf16 peak, the nominal ratio of
 the two tensor rates).  Decode legs report KV-read GB/s.  L2
@@ -54,7 +64,10 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-TRAIN = ("causal_b2_h16_n4096_d128", "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers")
+TRAIN = ("mha_b4_h16_n2048_d64", "causal_b2_h16_n4096_d128", "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers")
+TINY = "tiny_b1_h1_n256_d64"
+TARGET_TRAIN = ("causal_b2_h16_n4096_d128", "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers")  # N >= 4096, d = 128
+TARGETS = {"fwd_frac": 0.55, "bwd_frac": 0.40, "decode_frac": 0.75}
 DECODE = ("decode_b8_hq32_hkv8_q1_kv131072_d128", "decode_b8_hq32_hkv8_q4_kv131072_d128")
 PAGED = ("decode_b8_hq32_hkv8_q1_kv131072_d128", 16)  # the q1 decode cache in shuffled pages of 16 keys
 PAGED_NAME = PAGED[0] + "_paged16"
@@ -65,9 +78,9 @@ FP8 = "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers"  # the FP8 leg runs this wor
 FP8_NAME = FP8 + "_fp8_hadamard"
 FP8_TENSOR_RATIO = 2.0  # nominal dense E4M3 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 WORKLOAD = (" + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode); " + PAGED_NAME +
-            " (paged decode); " + " + ".join(WINDOW) + " (sliding-window fwd+bwd); " + VARLEN +
-            " (packed variable-length fwd+bwd); " + BLOCKSPARSE + " (block-sparse fwd+bwd); " + FP8_NAME +
-            " (FP8 quantise + fwd)")
+            " (paged decode); beside the step: " + TINY + " (fwd+bwd); " + " + ".join(WINDOW) +
+            " (sliding-window fwd+bwd); " + VARLEN + " (packed variable-length fwd+bwd); " + BLOCKSPARSE +
+            " (block-sparse fwd+bwd); " + FP8_NAME + " (FP8 quantise + fwd)")
 METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
@@ -79,6 +92,12 @@ def workloads():
 
     by = {w.name: w for w in inputs.ALL}
     return [by[n] for n in TRAIN], [by[n] for n in DECODE] + [by[PAGED[0]]], [by[n] for n in WINDOW]
+
+
+def tiny_workload():
+    from exact_io_aware_21_gb300 import inputs
+
+    return {w.name: w for w in inputs.ALL}[TINY]
 
 
 def window_pairs(w):
@@ -221,37 +240,90 @@ def _head_inputs(w):
         from exact_io_aware_21_gb300 import inputs
 
         x = inputs.make(w)
-        kvh = 0
         _SAMPLE_CACHE[w.name] = {
-            "q": x["q"][:1, :, :1].float().numpy(), "k": x["k"][:1, :, kvh:kvh + 1].float().numpy(),
-            "v": x["v"][:1, :, kvh:kvh + 1].float().numpy(), "do": x["do"][:1, :, :1].float().numpy()}
+            "q": x["q"][:1, :, :1].float().numpy(), "k": x["k"][:1, :, :1].float().numpy(),
+            "v": x["v"][:1, :, :1].float().numpy(), "do": x["do"][:1, :, :1].float().numpy()}
     return _SAMPLE_CACHE[w.name]
 
 
-def oracle_sample_step(w, rows):
-    """fp64 oracle forward + backward of head (0, 0) restricted to query ``rows``.
+def visible_pairs(w, rows):
+    """(query, key) pairs the given query rows of one head see (dense or causal workloads)."""
+    return sum(int(r) + 1 for r in rows) if w.causal else len(rows) * w.Nk
 
-    Returns the counted FLOPs of that share of the workload: the workload's
-    counted fwd+bwd FLOPs times the fraction of visible (row, key) pairs covered.
-    """
+
+def sample_flops(w, part, rows):
+    """Counted FLOPs of the forward ('fwd') or backward ('bwd') over query ``rows`` of one head."""
+    f = 4.0 * w.d * visible_pairs(w, rows)
+    return f if part == "fwd" else 2.5 * f
+
+
+def oracle_time(w, part, rows):
+    """Seconds the fp64 oracle takes for the forward or backward of query ``rows`` of head (0, 0)."""
     from oracle import attention as A
 
     x = _head_inputs(w)
-    A.attention_forward(x["q"], x["k"], x["v"], w.scale, w.causal, rows=rows)
-    A.attention_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, rows=rows)
-    vis = sum(int(r) + 1 for r in rows) if w.causal else len(rows) * w.Nk
-    total = (w.Nq * (w.Nq + 1) / 2 if w.causal else w.Nq * w.Nk) * w.B * w.Hq
-    return 3.5 * fwd_flops(w) * vis / total
+    t0 = time.perf_counter()
+    if part == "fwd":
+        A.attention_forward(x["q"], x["k"], x["v"], w.scale, w.causal, rows=rows)
+    else:
+        A.attention_backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal, rows=rows)
+    return time.perf_counter() - t0
 
 
-def rows_for(w, seconds, probe=256):
-    """Number of (longest) query rows of one head whose oracle fwd+bwd takes ~``seconds``."""
+def oracle_rows_for(w, part, seconds, probe=128):
+    """Number of (longest) query rows of head (0, 0) whose oracle ``part`` takes about ``seconds``."""
     import numpy as np
 
-    t0 = time.perf_counter()
-    oracle_sample_step(w, np.arange(w.Nq - probe, w.Nq))
-    dt = time.perf_counter() - t0
-    return int(max(32, min(w.Nq, probe * seconds / max(dt, 1e-6))))
+    p = min(probe, w.Nq)
+    dt = oracle_time(w, part, np.arange(w.Nq - p, w.Nq))
+    return int(max(32, min(w.Nq, p * seconds / max(dt, 1e-6))))
+
+
+def oracle_train_row(w, seconds, whole_reps=0):
+    """The oracle's forward and backward rates on ``w``: the whole workload as the median of
+    ``whole_reps`` runs when given (tiny), else about ``seconds`` of query rows of head (0, 0)."""
+    import numpy as np
+
+    out = {}
+    for part in ("fwd", "bwd"):
+        if whole_reps:
+            rows = np.arange(w.Nq)
+            ts = [oracle_time(w, part, rows) for _ in range(whole_reps)]
+            dt = statistics.median(ts)
+            f = sample_flops(w, part, rows) * w.B * w.Hq
+            out[part] = {"ms": dt * 1e3, "tflops": f / dt / 1e12, "sample": f"whole workload, median of {whole_reps}"}
+        else:
+            m = oracle_rows_for(w, part, seconds)
+            rows = np.arange(w.Nq - m, w.Nq)
+            dt = oracle_time(w, part, rows)
+            if dt < 0.5 * seconds and m < w.Nq:  # the probe's fixed costs made it look slow: once more
+                m = int(min(w.Nq, m * seconds / max(dt, 1e-6)))
+                rows = np.arange(w.Nq - m, w.Nq)
+                dt = oracle_time(w, part, rows)
+            f = sample_flops(w, part, rows)
+            full_s = (fwd_flops(w) * (1.0 if part == "fwd" else 2.5)) / (f / dt)
+            out[part] = {"tflops": f / dt / 1e12, "est_full_s": full_s, "s": dt,
+                         "sample": f"{m} query rows of head (0,0)"}
+    return out
+
+
+def oracle_decode_row(x, w, reps=3):
+    """The oracle's split-free forward for the query heads of K/V head 0 of batch entry 0 of a
+    decode workload (``x``: its q, k, v tensors), as KV-read GB/s of that head's cache."""
+    from oracle import attention as A
+
+    g = w.Hq // w.Hkv
+    q = x["q"][:1, :, :g].float().cpu().numpy()
+    k = x["k"][:1, :, :1].float().cpu().numpy()
+    v = x["v"][:1, :, :1].float().cpu().numpy()
+    ts = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        A.attention_forward(q, k, v, w.scale, False)
+        ts.append(time.perf_counter() - t0)
+    dt = statistics.median(ts)
+    return {"ms_per_kv_head": dt * 1e3, "gbs": 2.0 * w.Nk * w.d * 2 / dt / 1e9,
+            "est_full_s": dt * w.B * w.Hkv, "sample": f"batch 0, K/V head 0 ({g * w.Nq} query rows), median of {reps}"}
 
 
 def cpu_cores():
@@ -262,35 +334,54 @@ def cpu_cores():
 
 
 def oracle_run(train, seconds_per_step, steps, warmup):
-    """Time ``steps`` oracle steps; each step = a row block of head (0,0) of every training workload."""
+    """Time ``steps`` oracle steps; each step = forward + backward of a block of query rows of
+    head (0, 0) of every training workload, about ``seconds_per_step`` in all."""
     import numpy as np
 
-    n = {w.name: rows_for(w, seconds_per_step / len(train)) for w in train}
+    n = {w.name: min(oracle_rows_for(w, "fwd", seconds_per_step / len(train) / 3.5),
+                     oracle_rows_for(w, "bwd", seconds_per_step / len(train) * 2.5 / 3.5)) for w in train}
     times, flops = [], 0.0
     for i in range(warmup + steps):
-        t0 = time.perf_counter()
-        f = 0.0
+        t = f = 0.0
         for w in train:
             m = n[w.name]
             r0 = (w.Nq - m) - (i * m) % max(1, w.Nq - m + 1)
-            f += oracle_sample_step(w, np.arange(r0, r0 + m))
-        dt = time.perf_counter() - t0
+            rows = np.arange(r0, r0 + m)
+            for part in ("fwd", "bwd"):
+                t += oracle_time(w, part, rows)
+                f += sample_flops(w, part, rows)
         if i >= warmup:
-            times.append(dt)
+            times.append(t)
             flops += f
     desc = ", ".join(f"{w.name}: {n[w.name]} query rows of head (0,0)" for w in train)
     return flops / sum(times) / 1e12, sum(times) / steps, desc
 
 
-def run_cpu_baseline(train, budget_s):
-    value, _, desc = oracle_run(train, budget_s, 1, 0)
-    return {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"{desc}; fwd+bwd in fp64 numpy, about {budget_s:.0f} s"}
+def cpu_baseline_from(rows):
+    """The contract's cpu_baseline: counted FLOPs over oracle time, summed over the training rows."""
+    f = t = 0.0
+    for r in rows.values():
+        for part in ("fwd", "bwd"):
+            f += r[part]["tflops"] * 1e12 * r[part]["s"]
+            t += r[part]["s"]
+    desc = "; ".join(f"{name}: fwd {r['fwd']['sample']}, bwd {r['bwd']['sample']}" for name, r in rows.items())
+    return {"value": f / t / 1e12 if t else None, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{desc}; fp64 numpy, forward and backward timed separately"}
+
+
+def bench_config(world):
+    """The ``config`` object of both arms (the same workload, metric and unit)."""
+    return {
+        "workload": WORKLOAD,
+        "value_counts": "fwd+bwd FLOPs of the training workloads (" + ", ".join(TRAIN) + ") / their device time",
+        "l2": "flushed (256 MiB write) before every launch group, outside its events",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
 
 
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
-    _, rank, _ = dist_env()
+    world, rank, _ = dist_env()
     if rank != 0:
         return 0
     train, _, _ = workloads()
@@ -303,8 +394,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": s_per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1), bf16-rounded; outlier channel x20 in the GQA workload)",
-        "config": {"workload": WORKLOAD, "sample": f"per step: {desc}, fwd+bwd (decode legs not sampled)",
-                   "parallelism": "host cores"},
+        "config": bench_config(args.gpus),
+        "sample": f"per step: {desc}, fwd+bwd (decode legs not sampled); host cores",
         "cpu_baseline": cpu,
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -342,7 +433,8 @@ def make_legs(device, seed):
     lib = fa.library()
     train, dec, win = workloads()
     legs, state = [], {}
-    for w in train + win:
+    tiny = tiny_workload()
+    for w in train + win + [tiny]:
         x = inputs.make(w, device=device, seed=w.seed + seed)
         s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal, w.window)
         st = dict(x=x, s=s, o=torch.empty_like(x["q"]), ores=torch.empty_like(x["q"]),
@@ -363,7 +455,8 @@ def make_legs(device, seed):
 
         fns = [("fwd", fwd), ("bwd_pre", lambda part=part: part(0)), ("bwd_dkdv", lambda part=part: part(1)),
                ("bwd_dq", lambda part=part: part(2))]
-        legs.append(Leg(w.name, "window" if w.window else "train", w, fns, 3.5 * fwd_flops(w)))
+        kind = "tiny" if w is tiny else "window" if w.window else "train"
+        legs.append(Leg(w.name, kind, w, fns, 3.5 * fwd_flops(w)))
     for i, w in enumerate(dec):
         paged = i == len(dec) - 1
         name = PAGED_NAME if paged else w.name
@@ -657,64 +750,81 @@ def run_ours(args):
     for leg, part, e0, e1 in recs:
         leg.ms[part] += e0.elapsed_time(e1) / args.steps
     leg_ms = {l.name: sum(l.ms.values()) for l in legs}
-    # the step is the training and decode legs; the window leg is timed in the same
+    # the step is the training and decode legs; the other legs are timed in the same
     # loop and reported beside them
     step_legs = [l for l in legs if l.kind in ("train", "decode")]
     step_ms = sum(leg_ms[l.name] for l in step_legs)
     train_ms = sum(leg_ms[l.name] for l in legs if l.kind == "train")
     max_train_ms, total_flops = aggregate(train_ms, sum(l.work for l in legs if l.kind == "train"), world)
     max_step_ms, _ = aggregate(step_ms, 0.0, world)
-    sus = peaks["bf16_tflops_sustained"]
+    burst, sus = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
+
+    def r4(x):
+        return None if x is None else float(f"{x:.4g}")
+
+    def tc(f, ms):
+        """TFLOPS of f FLOPs in ms, and its fractions of the burst and sustained bf16 peaks."""
+        t = f / ms / 1e9
+        return r4(t), r4(t / burst), r4(t / sus)
 
     legs_out = {}
     for l in legs:
-        if l.kind in ("train", "window"):
-            f = fwd_flops(l.w)
-            bwd_ms = l.ms["bwd_pre"] + l.ms["bwd_dkdv"] + l.ms["bwd_dq"]
-            legs_out[l.name] = {
-                "fwd_ms": l.ms["fwd"], "fwd_tflops": f / l.ms["fwd"] / 1e9,
-                "fwd_frac_of_sustained_peak": f / l.ms["fwd"] / 1e9 / sus,
-                "bwd_ms": bwd_ms, "bwd_tflops": 2.5 * f / bwd_ms / 1e9,
-                "bwd_frac_of_sustained_peak": 2.5 * f / bwd_ms / 1e9 / sus,
-                "bwd_parts_ms": {k: l.ms[k] for k in ("bwd_pre", "bwd_dkdv", "bwd_dq")}}
+        f = fwd_flops(l.w)
+        if l.kind in ("train", "window", "tiny", "varlen", "blocksparse"):
+            fk = {"varlen": "fwd_varlen", "blocksparse": "fwd_bs"}.get(l.kind, "fwd")
+            fwd_ms = l.ms[fk]
+            bwd_ms = (l.ms["bwd_varlen"] if l.kind == "varlen" else l.ms["bwd_bs"] if l.kind == "blocksparse"
+                      else l.ms["bwd_pre"] + l.ms["bwd_dkdv"] + l.ms["bwd_dq"])
+            ft, ff, fs = tc(f, fwd_ms)
+            bt, bf, bs = tc(2.5 * f, bwd_ms)
+            out = {"fwd_ms": r4(fwd_ms), "fwd_tflops": ft, "fwd_frac_of_burst_peak": ff,
+                   "fwd_frac_of_sustained_peak": fs, "bwd_ms": r4(bwd_ms), "bwd_tflops": bt,
+                   "bwd_frac_of_burst_peak": bf, "bwd_frac_of_sustained_peak": bs,
+                   "in_step": l.kind == "train"}
+            if l.kind in ("train", "window", "tiny"):
+                out["bwd_parts_ms"] = {k: r4(l.ms[k]) for k in ("bwd_pre", "bwd_dkdv", "bwd_dq")}
             if l.kind == "window":
-                legs_out[l.name].update({"window": list(l.w.window), "in_step": False,
-                                         "flops_count": "4*B*H*d per visible (query, key) pair, x3.5 fwd+bwd"})
-        elif l.kind == "varlen":
-            f = fwd_flops(l.w)
-            legs_out[l.name] = {
-                "fwd_ms": l.ms["fwd_varlen"], "fwd_tflops": f / l.ms["fwd_varlen"] / 1e9,
-                "fwd_frac_of_sustained_peak": f / l.ms["fwd_varlen"] / 1e9 / sus,
-                "bwd_ms": l.ms["bwd_varlen"], "bwd_tflops": 2.5 * f / l.ms["bwd_varlen"] / 1e9,
-                "bwd_frac_of_sustained_peak": 2.5 * f / l.ms["bwd_varlen"] / 1e9 / sus,
-                "lens": varlen_lens(l.w), "in_step": False,
-                "flops_count": "per sequence 4*H*L^2*d, halved (causal), x3.5 fwd+bwd"}
-        elif l.kind == "blocksparse":
-            f = fwd_flops(l.w)
-            legs_out[l.name] = {"fwd_ms": l.ms["fwd_bs"], "fwd_tflops": f / l.ms["fwd_bs"] / 1e9,
-                                "fwd_frac_of_sustained_peak": f / l.ms["fwd_bs"] / 1e9 / sus,
-                                "bwd_ms": l.ms["bwd_bs"], "bwd_tflops": 2.5 * f / l.ms["bwd_bs"] / 1e9,
-                                "bwd_frac_of_sustained_peak": 2.5 * f / l.ms["bwd_bs"] / 1e9 / sus,
-                                "tiles_listed": sum(sum(r) for r in blocksparse_table(l.w)), "in_step": False,
-                                "flops_count": "4*B*H*d per visible (query, key) pair"}
+                out.update({"window": list(l.w.window),
+                            "flops_count": "4*B*H*d per visible (query, key) pair, x3.5 fwd+bwd"})
+            elif l.kind == "varlen":
+                out.update({"lens": varlen_lens(l.w), "flops_count": "per sequence 4*H*L^2*d, halved (causal)"})
+            elif l.kind == "blocksparse":
+                out.update({"tiles_listed": sum(sum(r) for r in blocksparse_table(l.w)),
+                            "flops_count": "4*B*H*d per visible (query, key) pair"})
+            legs_out[l.name] = out
         elif l.kind == "fp8":
-            f = fwd_flops(l.w)
             qb = {"quant_q": (l.w.Hq, l.w.Nq), "quant_k": (l.w.Hkv, l.w.Nk), "quant_v": (l.w.Hkv, l.w.Nk)}
             # quantiser traffic: bf16 in, one-byte codes out (V's per-head scale reads its rows twice)
             qbytes = {k: l.w.B * n * h * l.w.d * (5 if k == "quant_v" else 3) for k, (h, n) in qb.items()}
-            fp8_peak = FP8_TENSOR_RATIO * sus
+            fp8_peak = FP8_TENSOR_RATIO * burst
+            t = f / l.ms["fwd_fp8"] / 1e9
             legs_out[l.name] = {
-                "fwd_ms": l.ms["fwd_fp8"], "fwd_tflops": f / l.ms["fwd_fp8"] / 1e9,
-                "fwd_frac_of_fp8_peak": f / l.ms["fwd_fp8"] / 1e9 / fp8_peak,
-                "fp8_peak_tflops": fp8_peak, "fp8_peak_source": "2 x measured sustained bf16 (nominal E4M3/BF16 ratio)",
-                "quant_ms": {k: l.ms[k] for k in qb},
-                "quant_gbs": {k: qbytes[k] / l.ms[k] / 1e6 for k in qb},
-                "fwd_plus_quant_tflops": f / sum(l.ms.values()) / 1e9,
-                "hadamard": True, "in_step": False}
+                "fwd_ms": r4(l.ms["fwd_fp8"]), "fwd_tflops": r4(t), "fwd_frac_of_fp8_peak": r4(t / fp8_peak),
+                "fp8_peak_tflops": r4(fp8_peak),
+                "fp8_peak_source": "nominal: 2 x the measured burst bf16 peak (the E4M3/BF16 dense rate ratio, "
+                                   "4.5 / 2.25 PFLOP/s); no E4M3 peak is measured",
+                "quant_ms": {k: r4(l.ms[k]) for k in qb},
+                "quant_gbs": {k: r4(qbytes[k] / l.ms[k] / 1e6) for k in qb},
+                "fwd_plus_quant_tflops": r4(f / sum(l.ms.values()) / 1e9), "hadamard": True, "in_step": False}
         else:
             ms = l.ms["decode"]
-            legs_out[l.name] = {"ms": ms, "gbs": l.work / ms / 1e6, "frac_of_hbm_peak": l.work / ms / 1e6 /
-                                peaks["hbm_gbs"], "num_splits": state[l.name]["S"] or "auto"}
+            legs_out[l.name] = {"ms": r4(ms), "gbs": r4(l.work / ms / 1e6),
+                                "frac_of_hbm_peak": r4(l.work / ms / 1e6 / peaks["hbm_gbs"]),
+                                "num_splits": state[l.name]["S"] or "auto", "in_step": True}
+
+    # the bars: forward and backward of the N >= 4096, d = 128 workloads, decode legs
+    targets = {"peak_bf16_tflops": burst, "peak_hbm_gbs": peaks["hbm_gbs"],
+               "peak_source": f"{peak_src} burst bf16 (kernels timed one launch at a time)", "bars": TARGETS}
+    ok = True
+    for name in TARGET_TRAIN:
+        lo = legs_out[name]
+        targets[name] = {"fwd_frac": lo["fwd_frac_of_burst_peak"], "bwd_frac": lo["bwd_frac_of_burst_peak"]}
+        ok &= lo["fwd_frac_of_burst_peak"] >= TARGETS["fwd_frac"] and lo["bwd_frac_of_burst_peak"] >= TARGETS["bwd_frac"]
+    for l in legs:
+        if l.kind == "decode":
+            targets[l.name] = {"decode_frac": legs_out[l.name]["frac_of_hbm_peak"]}
+            ok &= legs_out[l.name]["frac_of_hbm_peak"] >= TARGETS["decode_frac"]
+    targets["all_met"] = bool(ok)
 
     # roofline of the dominant kernel: the launch with the largest share of the step
     dl, dp = max(((l, p) for l in step_legs for p, _ in l.fns if p != "bwd_pre"), key=lambda lp: lp[0].ms[lp[1]])
@@ -725,17 +835,39 @@ def run_ours(args):
     else:
         ach = kernel_flops(dp, dl.w) / dl.ms[dp] / 1e9
         kname = {"fwd": "fa_fwd_kernel", "bwd_dkdv": "bwd_dkdv_kernel", "bwd_dq": "bwd_dq_kernel"}[dp]
-        roof = {"kernel": kname, "bound": "tensor", "achieved": ach, "peak": sus, "unit": "TFLOP/s",
-                "frac": ach / sus, "frac_of_burst_peak": ach / peaks["bf16_tflops"]}
+        roof = {"kernel": kname, "bound": "tensor", "achieved": ach, "peak": burst, "unit": "TFLOP/s",
+                "frac": ach / burst, "frac_of_sustained_peak": ach / sus}
     roof.update({"workload": dl.name, "share_of_step": dl.ms[dp] / step_ms,
                  "peak_source": f"{peak_src}: " + ("MEASURED_PEAKS.json" if peak_src == "measured"
-                                                   else "profiling-recipe fallback"),
+                                                   else "profiling-recipe fallback") +
+                                (" (burst)" if dp != "decode" else ""),
                  "traffic": traffic_for(roof["kernel"], dl.name)})
 
     e2e = run_e2e(legs, state, device, args.steps, world)
-    cpu = None
+
+    # every workload of the benchmark plan beside the fp64 oracle on this host's cores
+    configs, cpu = {}, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = run_cpu_baseline([l.w for l in legs if l.kind == "train"], args.cpu_seconds)
+        budget = args.cpu_seconds / 6.0  # forward and backward of the three training workloads
+        rows = {}
+        for l in [x for x in legs if x.kind in ("tiny", "train")]:
+            lo = legs_out[l.name]
+            r = oracle_train_row(l.w, budget, whole_reps=20 if l.kind == "tiny" else 0)
+            if l.kind == "train":
+                rows[l.name] = r
+            configs[l.name] = {
+                "fwd_tflops": lo["fwd_tflops"], "bwd_tflops": lo["bwd_tflops"],
+                "fwd_frac": lo["fwd_frac_of_burst_peak"], "bwd_frac": lo["bwd_frac_of_burst_peak"],
+                "oracle_fwd_tflops": r4(r["fwd"]["tflops"]), "oracle_bwd_tflops": r4(r["bwd"]["tflops"]),
+                "oracle": {p: {k: (r4(v) if isinstance(v, float) else v) for k, v in r[p].items() if k != "s"}
+                           for p in ("fwd", "bwd")}}
+        for l in [x for x in legs if x.kind == "decode" and x.name in DECODE]:
+            r = oracle_decode_row(state[l.name]["x"], l.w)
+            configs[l.name] = {"gbs": legs_out[l.name]["gbs"], "frac": legs_out[l.name]["frac_of_hbm_peak"],
+                               "oracle_gbs": r4(r["gbs"]),
+                               "oracle": {k: (r4(v) if isinstance(v, float) else v) for k, v in r.items()}}
+        configs["oracle_cores"] = cpu_cores()
+        cpu = cpu_baseline_from(rows)
 
     line = {
         "metric": METRIC,
@@ -750,18 +882,15 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), bf16-rounded; outlier channel x20 in the GQA workload)",
-        "config": {
-            "workload": WORKLOAD,
-            "value_counts": "fwd+bwd FLOPs of the two training workloads / their device time",
-            "l2": "flushed (256 MiB write) before every launch group, outside its events",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "legs": legs_out,
-        },
+        "targets": targets,
+        "config": bench_config(world),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * sum(KERNELS_PER_CALL[p] for l in legs for p, _ in l.fns),
         "clocks": clocks,
+        "configs": configs,
+        "legs": legs_out,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -174,6 +174,9 @@ __global__ void __launch_bounds__(128) quantize_kernel(const __grid_constant__ C
         p.scales[MODE == 0 ? bhi * p.nblk + blk : bhi] = sc;
       }
     }
+    // The code rows were written over the stage through the generic proxy; a later
+    // TMA load (async proxy) refills it, so order those writes before it.
+    if (MODE != 1) fence_proxy_async_smem();
     __syncthreads();  // the stage, the code rows and s_red are free for the next block
   }
   // loads issued for blocks this CTA gave up on must land before exit

@@ -6,10 +6,11 @@ the oracle side (tests) and the CUDA side may use it.
 Recipe (all workloads): a CPU ``torch.Generator`` seeded with ``seed``; fp32
 standard normal draws in the order Q, K, V, dO; each then rounded to bf16
 (round to nearest even).  Layout ``[B, N, H, d]``.  The grouped-query workload
-adds outliers: one channel index c in [0, d) is drawn from the same generator
-after the four tensors, and Q[..., c] and K[..., c] are multiplied by 20 before
-the bf16 rounding (1% of d=128 channels, rounded to one channel, shared by all
-heads and tokens).
+adds outliers: one channel index c in [0, d) is drawn by a CPU generator of its
+own seeded with the same seed (``outlier_channel``: channel 44 for seed 0 and
+d = 128), and Q[..., c] and K[..., c] are multiplied by 20 before the bf16
+rounding (1% of d=128 channels, rounded to one channel, shared by all heads and
+tokens).
 
 Large workloads can be drawn on the GPU instead (``device='cuda'``, a CUDA
 generator with the same seed); those values differ from the CPU draws and are
@@ -111,7 +112,7 @@ def make(w, device="cpu", with_do=True, seed=None):
     do = draw(w.Nq, w.Hq) if (with_do and not w.decode) else None
     ch = None
     if w.outliers:
-        ch = int(torch.randint(0, w.d, (1,), generator=gen, device=device).item())
+        ch = outlier_channel(w.d, seed)
         q[..., ch] *= 20.0
         k[..., ch] *= 20.0
     out = {
@@ -122,6 +123,15 @@ def make(w, device="cpu", with_do=True, seed=None):
         "outlier_channel": ch,
     }
     return out
+
+
+def outlier_channel(d, seed=0):
+    """The outlier channel of a workload: one index in [0, d) drawn by its own CPU
+    generator seeded with ``seed``, so every draw of the workload (CPU or CUDA
+    tensors, with or without dO) scales the same channel."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    return int(torch.randint(0, d, (1,), generator=gen).item())
 
 
 def hadamard_signs(d, seed=0):

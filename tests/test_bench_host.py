@@ -49,3 +49,30 @@ def test_blocksparse_leg_counts_visible_pairs():
     vis &= ~A.causal_mask(np.arange(1280), 1280)
     assert bench.fwd_flops(w) == 4.0 * 2 * 64 * vis.sum()
     assert M[5].tolist() == [True, False, False, True, True, True, False, False, False, False]
+
+
+def test_outlier_channel_is_one_per_workload():
+    """Every draw of an outlier workload (with or without dO) scales the same channel."""
+    w = inputs.Workload("o", 1, 2, 1, 64, 64, 128, True, outliers=True, seed=3)
+    a, b = inputs.make(w), inputs.make(w, with_do=False)
+    assert a["outlier_channel"] == b["outlier_channel"] == inputs.outlier_channel(128, 3)
+    assert int(a["q"].float().abs().mean(dim=(0, 1, 2)).argmax()) == a["outlier_channel"]
+    assert inputs.outlier_channel(inputs.GQA_N8192_D128.d, inputs.GQA_N8192_D128.seed) == 44
+
+
+def test_oracle_sample_flops_count_visible_pairs():
+    w = inputs.Workload("c", 1, 1, 1, 300, 300, 64, True)
+    rows = np.arange(10, 50)
+    assert bench.visible_pairs(w, rows) == int((~A.causal_mask(rows, 300)).sum())
+    assert bench.sample_flops(w, "fwd", rows) == 4.0 * 64 * bench.visible_pairs(w, rows)
+    assert bench.sample_flops(w, "bwd", rows) == 2.5 * bench.sample_flops(w, "fwd", rows)
+    full = inputs.Workload("f", 1, 1, 1, 300, 200, 64, False)
+    assert bench.visible_pairs(full, rows) == 40 * 200
+
+
+def test_training_legs_are_the_benchmark_plan():
+    train, dec, _ = bench.workloads()
+    assert [w.name for w in train] == ["mha_b4_h16_n2048_d64", "causal_b2_h16_n4096_d128",
+                                       "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers"]
+    assert bench.tiny_workload() is inputs.TINY
+    assert set(bench.TARGET_TRAIN) <= {w.name for w in train}

@@ -21,6 +21,9 @@ Definitions followed (one bullet per function below):
   * tiled forward: the outer/inner loop with running max m and sum l of
     §18.4.1 and the online update of §18.4.2; CMU 11-868 L21 notes slide 12
     (two-block rescaling) and its Algorithm-1 remark.
+  * conditional rescaling (the L21 notes on FA4: an online-softmax variant
+    that skips most rescalings): the same loop with a reference that moves
+    only when a block's max passes it by more than a threshold.
   * FlashDecoding: each KV split t yields (m_t, l_t, O_t) with O_t the
     unnormalised local output; the combine is O = sum_t O_t e^{m_t - m} /
     sum_t l_t e^{m_t - m}.  §18.8.2 and lecture slides 57-60.
@@ -257,6 +260,58 @@ def tiled_forward_head(Qh, Kh, Vh, scale, block_r, block_c, causal=False):
         O[rows] = Oi / l[:, None]
         LSE[rows] = m + np.log(l)
     return O, LSE
+
+
+def tiled_forward_head_conditional(Qh, Kh, Vh, scale, block_r, block_c, threshold, causal=False):
+    """One head of the tiled forward with conditional rescaling.
+
+    "CMU 11-868 L21" notes on FA4: a variant of the online softmax that skips
+    most rescalings.  Each row keeps a reference r in place of the running max;
+    a new block's row max m~ replaces it only when m~ > r + threshold
+    (``threshold`` in log2 units, i.e. r moves when a probability would exceed
+    2^threshold).  Each block contributes P~ = exp(S - r_new) with
+    r_new = m~ if it moved, else r; when r moves, l and O are rescaled by
+    exp(r - r_new), as in the §18.4.2 update.  Final O / l and LSE = r + ln l.
+    In exact arithmetic this is the plain definition for any threshold >= 0
+    (the rescaling identity holds for any reference, not only the max).
+    Returns (O [Nq, d], LSE [Nq], rescalings, p_max): rescalings counts the
+    (row, block) steps after a row's first visible block in which r moved;
+    p_max is the largest P~ entry seen (at most 2^threshold).
+    """
+    Qh, Kh, Vh = _f64(Qh), _f64(Kh), _f64(Vh)
+    Nq, d = Qh.shape
+    Nk = Kh.shape[0]
+    tau = threshold * np.log(2.0)  # the scores are in natural-log units
+    O = np.zeros((Nq, d))
+    LSE = np.zeros(Nq)
+    rescalings, p_max = 0, 0.0
+    for i0 in range(0, Nq, block_r):
+        rows = np.arange(i0, min(Nq, i0 + block_r))
+        Qi = Qh[rows]
+        r = np.full(len(rows), NEG_INF)
+        l = np.zeros(len(rows))
+        Oi = np.zeros((len(rows), d))
+        for j0 in range(0, Nk, block_c):
+            cols = np.arange(j0, min(Nk, j0 + block_c))
+            Sij = scale * (Qi @ Kh[cols].T)
+            if causal:
+                Sij = np.where(cols[None, :] > rows[:, None], NEG_INF, Sij)
+            m_tilde = Sij.max(axis=1)
+            move = m_tilde > r + tau                     # -inf + tau stays -inf: a first visible block moves r
+            rescalings += int(np.sum(move & np.isfinite(r)))
+            r_new = np.where(move, m_tilde, r)
+            seen = np.isfinite(r_new)
+            base = np.where(seen, r_new, 0.0)
+            alpha = np.where(np.isfinite(r), np.exp(r - base), 0.0)
+            P_tilde = np.where(seen[:, None], np.exp(Sij - base[:, None]), 0.0)
+            if P_tilde.size:
+                p_max = max(p_max, float(P_tilde.max()))
+            l = alpha * l + P_tilde.sum(axis=1)
+            Oi = alpha[:, None] * Oi + P_tilde @ Vh[cols]
+            r = r_new
+        O[rows] = Oi / l[:, None]
+        LSE[rows] = r + np.log(l)
+    return O, LSE, rescalings, p_max
 
 
 def two_block_output(Qh, K1, V1, K2, V2, scale):

@@ -19,6 +19,9 @@ in HBM:
                  blocksparse_causal_b1_hq32_hkv8_n16384_d128_local8_global1 through
                  fa_fwd_blocksparse / fa_bwd_blocksparse (each query tile: its own
                  key tile, the seven before it and tile 0)
+  rescale legs   the forward of the two N >= 4096 workloads with conditional
+                 rescaling (rescale_threshold 8: the reference max lags by up to
+                 2^8), beside the exact-max forward
   fp8 leg        E4M3 quantisation (Q, K per 128-row block after the random
                  Hadamard rotation, V per head) and the FP8 forward of the GQA
                  workload
@@ -68,6 +71,8 @@ TRAIN = ("mha_b4_h16_n2048_d64", "causal_b2_h16_n4096_d128", "gqa_causal_b1_hq32
 TINY = "tiny_b1_h1_n256_d64"
 TARGET_TRAIN = ("causal_b2_h16_n4096_d128", "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers")  # N >= 4096, d = 128
 TARGETS = {"fwd_frac": 0.55, "bwd_frac": 0.40, "decode_frac": 0.75}
+RESCALE_THRESHOLD = 8.0  # conditional rescaling leg: the reference max lags by up to 2^8
+RESCALE_SUFFIX = "_cond_rescale8"
 DECODE = ("decode_b8_hq32_hkv8_q1_kv131072_d128", "decode_b8_hq32_hkv8_q4_kv131072_d128")
 PAGED = ("decode_b8_hq32_hkv8_q1_kv131072_d128", 16)  # the q1 decode cache in shuffled pages of 16 keys
 PAGED_NAME = PAGED[0] + "_paged16"
@@ -78,7 +83,8 @@ FP8 = "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers"  # the FP8 leg runs this wor
 FP8_NAME = FP8 + "_fp8_hadamard"
 FP8_TENSOR_RATIO = 2.0  # nominal dense E4M3 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 WORKLOAD = (" + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode); " + PAGED_NAME +
-            " (paged decode); beside the step: " + TINY + " (fwd+bwd); " + " + ".join(WINDOW) +
+            " (paged decode); beside the step: " + TINY + " (fwd+bwd); " + " + ".join(TARGET_TRAIN) +
+            " (fwd with conditional rescaling, threshold 8); " + " + ".join(WINDOW) +
             " (sliding-window fwd+bwd); " + VARLEN + " (packed variable-length fwd+bwd); " + BLOCKSPARSE +
             " (block-sparse fwd+bwd); " + FP8_NAME + " (FP8 quantise + fwd)")
 METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/s"
@@ -457,6 +463,14 @@ def make_legs(device, seed):
                ("bwd_dq", lambda part=part: part(2))]
         kind = "tiny" if w is tiny else "window" if w.window else "train"
         legs.append(Leg(w.name, kind, w, fns, 3.5 * fwd_flops(w)))
+        if w.name in TARGET_TRAIN:  # conditional rescaling beside the exact forward
+            st["s_cr"] = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal, w.window, RESCALE_THRESHOLD)
+
+            def fwd_cr(st=st):
+                x = st["x"]
+                B.fa_fwd(x["q"], x["k"], x["v"], st["o"], st["lse"], st["s_cr"], st["wsf"], st["ores"])
+
+            legs.append(Leg(w.name + RESCALE_SUFFIX, "rescale", w, [("fwd", fwd_cr)], fwd_flops(w)))
     for i, w in enumerate(dec):
         paged = i == len(dec) - 1
         name = PAGED_NAME if paged else w.name
@@ -594,6 +608,49 @@ def traffic_for(kernel, workload):
         return ent["bytes_per_launch"] if sha == ent["source_sha256_16"] else None
     except Exception:
         return None
+
+
+def trace_summary(t, units):
+    """Per-CTA busy spread and per-unit phases of one traced forward (``t``: the int64
+    trace words as numpy; layout in include/fa.h, fa_set_trace).  Times in microseconds."""
+    import numpy as np
+
+    cta = t[:4096].reshape(1024, 4)
+    used = cta[:, 0] > 0
+    st, en, nun = cta[used, 0].astype(np.float64), cta[used, 1].astype(np.float64), cta[used, 3]
+    t0 = st.min()
+    busy = (en - st) / 1e3
+    rec = t[4096:4096 + 16 * units].reshape(units, 16).astype(np.float64)
+    q = lambda x: {"min": r4(float(np.min(x))), "median": r4(float(np.median(x))), "max": r4(float(np.max(x)))}  # noqa: E731
+    return {
+        "ctas": int(used.sum()), "span_us": r4((en.max() - t0) / 1e3), "start_spread_us": r4((st.max() - t0) / 1e3),
+        "busy_us": q(busy), "end_spread_us": r4((en.max() - en.min()) / 1e3), "units_per_cta": q(nun),
+        "unit_claim_to_first_product_us": q((rec[:, 1] - rec[:, 0]) / 1e3),
+        "unit_last_product_to_output_us": q((rec[:, 3] - rec[:, 2]) / 1e3),
+        "unit_issue_span_us": q((rec[:, 2] - rec[:, 1]) / 1e3),
+        "issue_share_of_busy": r4(float(np.sum(rec[:, 2] - rec[:, 1]) / 1e3 / np.sum(busy))),
+    }
+
+
+def r4(x):
+    return None if x is None else float(f"{x:.4g}")
+
+
+def fwd_trace(leg, st, device):
+    """One traced forward of a training leg (outside the timed region)."""
+    import ctypes
+
+    from exact_io_aware_21_gb300 import binding as B
+
+    units = B.library().fa_fwd_num_units(ctypes.byref(st["s"]))
+    buf = torch.zeros(B.TRACE_UNIT0 + B.TRACE_UNIT_WORDS * units, dtype=torch.int64, device=device)
+    B.set_trace(buf)
+    try:
+        dict(leg.fns)["fwd"]()
+        torch.cuda.synchronize()
+    finally:
+        B.set_trace(None)
+    return trace_summary(buf.cpu().numpy(), units)
 
 
 def run_e2e(legs, state, device, steps, world):
@@ -759,15 +816,13 @@ def run_ours(args):
     max_step_ms, _ = aggregate(step_ms, 0.0, world)
     burst, sus = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
 
-    def r4(x):
-        return None if x is None else float(f"{x:.4g}")
-
     def tc(f, ms):
         """TFLOPS of f FLOPs in ms, and its fractions of the burst and sustained bf16 peaks."""
         t = f / ms / 1e9
         return r4(t), r4(t / burst), r4(t / sus)
 
     legs_out = {}
+    legs_by = {l.name: l for l in legs}
     for l in legs:
         f = fwd_flops(l.w)
         if l.kind in ("train", "window", "tiny", "varlen", "blocksparse"):
@@ -792,6 +847,12 @@ def run_ours(args):
                 out.update({"tiles_listed": sum(sum(r) for r in blocksparse_table(l.w)),
                             "flops_count": "4*B*H*d per visible (query, key) pair"})
             legs_out[l.name] = out
+        elif l.kind == "rescale":
+            exact_ms = legs_by[l.name[:-len(RESCALE_SUFFIX)]].ms["fwd"]
+            ft, ff, fs = tc(f, l.ms["fwd"])
+            legs_out[l.name] = {"fwd_ms": r4(l.ms["fwd"]), "fwd_tflops": ft, "fwd_frac_of_burst_peak": ff,
+                                "fwd_frac_of_sustained_peak": fs, "speedup_vs_exact_max": r4(exact_ms / l.ms["fwd"]),
+                                "rescale_threshold": RESCALE_THRESHOLD, "in_step": False}
         elif l.kind == "fp8":
             qb = {"quant_q": (l.w.Hq, l.w.Nq), "quant_k": (l.w.Hkv, l.w.Nk), "quant_v": (l.w.Hkv, l.w.Nk)}
             # quantiser traffic: bf16 in, one-byte codes out (V's per-head scale reads its rows twice)
@@ -842,6 +903,12 @@ def run_ours(args):
                                                    else "profiling-recipe fallback") +
                                 (" (burst)" if dp != "decode" else ""),
                  "traffic": traffic_for(roof["kernel"], dl.name)})
+
+    # where a forward launch spends its time: per-CTA and per-unit timestamps of one
+    # extra traced launch of each N >= 4096 workload (outside the timed region)
+    for l in legs:
+        if l.name in TARGET_TRAIN:
+            legs_out[l.name]["fwd_trace"] = fwd_trace(l, state[l.name], device)
 
     e2e = run_e2e(legs, state, device, args.steps, world)
 

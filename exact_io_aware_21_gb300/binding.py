@@ -35,7 +35,8 @@ class FaTensor(ctypes.Structure):
 class FaShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("Nq", ctypes.c_int),
                 ("Nk", ctypes.c_int), ("d", ctypes.c_int), ("scale", ctypes.c_float), ("causal", ctypes.c_int),
-                ("window", ctypes.c_int), ("window_left", ctypes.c_int), ("window_right", ctypes.c_int)]
+                ("window", ctypes.c_int), ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("rescale_threshold", ctypes.c_float)]
 
 
 # name -> (restype, argtypes); mirrors include/fa.h
@@ -59,8 +60,11 @@ SIGNATURES = {
     "fa_decode_paged_workspace_size": (_SZ, [_PS, _I, _I]),
     "fa_decode_noalloc_max_bytes": (_SZ, []),
     "fa_decode_noalloc": (_I, [_PT, _PT, _PT, _PT, _VP, _PS, _I, _VP]),
+    "fa_decode_noalloc_status": (_I, [_VP, _PI]),
     "fa_get_device_status": (_I, [_VP, _VP, _PI]),
     "fa_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
+    "fa_set_trace": (None, [_VP, _SZ]),
+    "fa_test_withhold_arrive": (None, []),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_last_cuda_error": (_I, []),
     "fa_tile_class": (_I, [_PS, _I, _I]),
@@ -114,11 +118,12 @@ def check(rc):
         raise FAError(rc, msg)
 
 
-def shape(B, Hq, Hkv, Nq, Nk, d, scale=None, causal=False, window=None):
-    """window = (left, right): query i sees keys i - left .. i + right (negative: unbounded)."""
+def shape(B, Hq, Hkv, Nq, Nk, d, scale=None, causal=False, window=None, rescale_threshold=0.0):
+    """window = (left, right): query i sees keys i - left .. i + right (negative: unbounded).
+    rescale_threshold: conditional rescaling of the forward, log2 units (0 = exact running max)."""
     w = (0, -1, -1) if window is None else (1, int(window[0]), int(window[1]))
     return FaShape(B, Hq, Hkv, Nq, Nk, d, 1.0 / math.sqrt(d) if scale is None else float(scale), int(bool(causal)),
-                   *w)
+                   *w, float(rescale_threshold))
 
 
 def tdesc(t):
@@ -150,6 +155,18 @@ def tdesc_u8(t):
 
 def _stream(t):
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+# Tests set OUTPUT_CANARY to NaN so that any output element a kernel leaves
+# unwritten shows up (E4M3 code outputs then start as 0xFF, a NaN code); the
+# default leaves outputs uninitialised, as torch.empty does.
+OUTPUT_CANARY = None
+
+
+def _out(shape, dtype, device):
+    if OUTPUT_CANARY is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    return torch.full(shape, 0xFF if dtype == torch.uint8 else OUTPUT_CANARY, dtype=dtype, device=device)
 
 
 def _ws(nbytes, device):
@@ -263,24 +280,38 @@ def device_status(workspace):
     return rc, st.value
 
 
+TRACE_MAX_CTAS, TRACE_UNIT0, TRACE_UNIT_WORDS = 1024, 4096, 16
+
+
+def set_trace(buf):
+    """Record the dense forward's timestamps into ``buf`` (a CUDA int64 tensor of at
+    least TRACE_UNIT0 + TRACE_UNIT_WORDS * units elements), or stop (None)."""
+    lib = library()
+    if buf is None:
+        lib.fa_set_trace(None, 0)
+    else:
+        lib.fa_set_trace(buf.data_ptr(), buf.numel() * buf.element_size())
+
+
 # ---------------------------------------------------------------- convenience API
-def _dims(q, k, scale, causal, window=None):
+def _dims(q, k, scale, causal, window=None, rescale_threshold=0.0):
     B, Nq, Hq, d = q.shape
     _, Nk, Hkv, _ = k.shape
-    return shape(B, Hq, Hkv, Nq, Nk, d, scale, causal, window)
+    return shape(B, Hq, Hkv, Nq, Nk, d, scale, causal, window, rescale_threshold)
 
 
-def forward(q, k, v, causal=False, scale=None, residual=False, window=None):
+def forward(q, k, v, causal=False, scale=None, residual=False, window=None, rescale_threshold=0.0):
     """O, LSE = attention(q, k, v).  q [B,Nq,Hq,d], k/v [B,Nk,Hkv,d] bf16 on CUDA.
 
     With ``residual=True`` also returns O's bf16 rounding residual, which
     ``backward`` uses to form D accurately (see fa_bwd in include/fa.h).
     ``window=(left, right)`` restricts query i to keys i - left .. i + right.
+    ``rescale_threshold`` > 0 turns on conditional rescaling (fa_shape_t in include/fa.h).
     """
-    s = _dims(q, k, scale, causal, window)
-    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
-    res = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
+    s = _dims(q, k, scale, causal, window, rescale_threshold)
+    o = _out(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = _out((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
+    res = _out(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
     ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q.device)
     fa_fwd(q, k, v, o, lse, s, ws, res)
     return (o, lse, res) if residual else (o, lse)
@@ -289,9 +320,9 @@ def forward(q, k, v, causal=False, scale=None, residual=False, window=None):
 def backward(q, k, v, o, lse, do, causal=False, scale=None, o_residual=None, window=None):
     """dQ, dK, dV of attention given O, LSE (and optionally O's residual) from ``forward``."""
     s = _dims(q, k, scale, causal, window)
-    dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device)
-    dv = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device)
+    dq = _out(q.shape, dtype=torch.bfloat16, device=q.device)
+    dk = _out(k.shape, dtype=torch.bfloat16, device=q.device)
+    dv = _out(v.shape, dtype=torch.bfloat16, device=q.device)
     ws = _ws(library().fa_bwd_workspace_size(ctypes.byref(s)), q.device)
     fa_bwd(q, k, v, o, lse, do, dq, dk, dv, s, ws, o_residual)
     return dq, dk, dv
@@ -300,8 +331,8 @@ def backward(q, k, v, o, lse, do, causal=False, scale=None, o_residual=None, win
 def decode(q, k_cache, v_cache, scale=None, num_splits=0):
     """Split-KV decode: O, LSE for a short query q [B,Nq,Hq,d] against the cache."""
     s = _dims(q, k_cache, scale, False)
-    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
+    o = _out(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = _out((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
     ws = _ws(library().fa_decode_workspace_size(ctypes.byref(s), int(num_splits)), q.device)
     fa_decode(q, k_cache, v_cache, o, lse, s, num_splits, ws)
     return o, lse
@@ -319,8 +350,8 @@ def decode_paged(q, k_cache, v_cache, block_table, seqlens_k, max_seqlen=None, s
     if max_seqlen is None:
         max_seqlen = int(seqlens_k.max().item())
     s = shape(B, Hq, Hkv, Nq, int(max_seqlen), d, scale, False)
-    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    o = _out(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = _out((B, Hq, Nq), dtype=torch.float32, device=q.device)
     ws = _ws(library().fa_decode_paged_workspace_size(ctypes.byref(s), int(num_splits), k_cache.shape[1]), q.device)
     fa_decode_paged(q, k_cache, v_cache, block_table, seqlens_k, o, lse, s, num_splits, ws)
     return o, lse
@@ -331,39 +362,39 @@ def quantize_fp8(x, block_rows=128, signs=None):
     = 128, scales [B, H, ceil(N/128)]) or per head (0, scales [B, H]); ``signs``
     (d float32 +-1 on the device) rotates the rows by the random Hadamard matrix first."""
     B, N, H, d = x.shape
-    out = torch.empty((B, N, H, d), dtype=torch.uint8, device=x.device)
+    out = _out((B, N, H, d), dtype=torch.uint8, device=x.device)
     nblk = -(-N // 128)
-    scales = torch.empty((B, H, nblk) if block_rows else (B, H), dtype=torch.float32, device=x.device)
+    scales = _out((B, H, nblk) if block_rows else (B, H), dtype=torch.float32, device=x.device)
     ws = _ws(library().fa_quantize_fp8_workspace_size(B, H), x.device)
     fa_quantize_fp8(x, block_rows, signs, out, scales, ws)
     return out, scales
 
 
-def forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None, window=None):
+def forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None, window=None, rescale_threshold=0.0):
     """O (bf16), LSE from E4M3 operands made by ``quantize_fp8`` (Q, K per block, V per head)."""
-    s = _dims(q8, k8, scale, causal, window)
-    o = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device)
-    lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q8.device)
+    s = _dims(q8, k8, scale, causal, window, rescale_threshold)
+    o = _out(q8.shape, dtype=torch.bfloat16, device=q8.device)
+    lse = _out((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q8.device)
     ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q8.device)
     fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, s, ws)
     return o, lse
 
 
-def _varlen_shape(q, k, cu_q, scale, causal):
+def _varlen_shape(q, k, cu_q, scale, causal, rescale_threshold=0.0):
     total_q, Hq, d = q.shape
     total_k, Hkv, _ = k.shape
-    return shape(cu_q.numel() - 1, Hq, Hkv, total_q, total_k, d, scale, causal)
+    return shape(cu_q.numel() - 1, Hq, Hkv, total_q, total_k, d, scale, causal, None, rescale_threshold)
 
 
 def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, causal=False, scale=None,
-                   residual=False):
+                   residual=False, rescale_threshold=0.0):
     """Packed variable-length forward (see fa_fwd_varlen in include/fa.h): q [total_q, Hq, d],
     k/v [total_k, Hkv, d] bf16, cu_seqlens int32 [B + 1] on the device.  Returns O, LSE
     [Hq, total_q] (and O's residual with ``residual=True``)."""
-    s = _varlen_shape(q, k, cu_seqlens_q, scale, causal)
-    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty((s.Hq, s.Nq), dtype=torch.float32, device=q.device)
-    res = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
+    s = _varlen_shape(q, k, cu_seqlens_q, scale, causal, rescale_threshold)
+    o = _out(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = _out((s.Hq, s.Nq), dtype=torch.float32, device=q.device)
+    res = _out(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
     ws = _ws(library().fa_fwd_varlen_workspace_size(ctypes.byref(s), int(max_seqlen_q)), q.device)
     fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, o, lse, s, ws, res)
     return (o, lse, res) if residual else (o, lse)
@@ -373,22 +404,23 @@ def backward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqle
                     scale=None, o_residual=None):
     """dQ, dK, dV of the packed forward."""
     s = _varlen_shape(q, k, cu_seqlens_q, scale, causal)
-    dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device)
-    dv = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device)
+    dq = _out(q.shape, dtype=torch.bfloat16, device=q.device)
+    dk = _out(k.shape, dtype=torch.bfloat16, device=q.device)
+    dv = _out(v.shape, dtype=torch.bfloat16, device=q.device)
     ws = _ws(library().fa_bwd_varlen_workspace_size(ctypes.byref(s), int(max_seqlen_q)), q.device)
     fa_bwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, o, lse, do, dq, dk, dv, s, ws,
                   o_residual)
     return dq, dk, dv
 
 
-def forward_blocksparse(q, k, v, row_ptr, col_idx, causal=False, scale=None, residual=False):
+def forward_blocksparse(q, k, v, row_ptr, col_idx, causal=False, scale=None, residual=False,
+                        rescale_threshold=0.0):
     """Block-sparse forward (see fa_fwd_blocksparse in include/fa.h): q [B,Nq,Hq,d], k/v
     [B,Nk,Hkv,d] bf16; row_ptr / col_idx the CSR table of 128-key tiles per 128-row query tile."""
-    s = _dims(q, k, scale, causal)
-    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
-    res = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
+    s = _dims(q, k, scale, causal, None, rescale_threshold)
+    o = _out(q.shape, dtype=torch.bfloat16, device=q.device)
+    lse = _out((s.B, s.Hq, s.Nq), dtype=torch.float32, device=q.device)
+    res = _out(q.shape, dtype=torch.bfloat16, device=q.device) if residual else None
     ws = _ws(library().fa_fwd_workspace_size(ctypes.byref(s)), q.device)
     fa_fwd_blocksparse(q, k, v, row_ptr, col_idx, o, lse, s, ws, res)
     return (o, lse, res) if residual else (o, lse)
@@ -397,9 +429,9 @@ def forward_blocksparse(q, k, v, row_ptr, col_idx, causal=False, scale=None, res
 def backward_blocksparse(q, k, v, row_ptr, col_idx, o, lse, do, causal=False, scale=None, o_residual=None):
     """dQ, dK, dV of ``forward_blocksparse`` (same table)."""
     s = _dims(q, k, scale, causal)
-    dq = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    dk = torch.empty(k.shape, dtype=torch.bfloat16, device=q.device)
-    dv = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device)
+    dq = _out(q.shape, dtype=torch.bfloat16, device=q.device)
+    dk = _out(k.shape, dtype=torch.bfloat16, device=q.device)
+    dv = _out(v.shape, dtype=torch.bfloat16, device=q.device)
     ws = _ws(library().fa_bwd_blocksparse_workspace_size(ctypes.byref(s), col_idx.numel()), q.device)
     fa_bwd_blocksparse(q, k, v, row_ptr, col_idx, o, lse, do, dq, dk, dv, s, ws, o_residual)
     return dq, dk, dv

@@ -18,6 +18,9 @@ namespace {
 
 unsigned long long g_timeout_ns = 10ull * 1000 * 1000 * 1000;
 int g_last_cuda_error = 0;
+void* g_trace = nullptr;  // forward timestamps (fa_set_trace)
+size_t g_trace_bytes = 0;
+bool g_withhold = false;  // the next dense d = 128 forward runs the withheld-hand-off test kernel
 
 int cuda_fail(cudaError_t e, int code) {
   g_last_cuda_error = static_cast<int>(e);
@@ -136,6 +139,7 @@ int check_shape(const fa_shape_t* s) {
   if (s->causal && s->Nq != s->Nk) return FA_ERR_INVALID;
   if (s->window != 0 && s->window != 1) return FA_ERR_INVALID;
   if (s->window && s->Nq != s->Nk) return FA_ERR_INVALID;
+  if (!(s->rescale_threshold >= 0.f && s->rescale_threshold <= 16.f)) return FA_ERR_INVALID;
   // index arithmetic inside the kernels is 32-bit per (head, row) and 64-bit per element
   if (static_cast<int64_t>(s->B) * s->Hq * s->Nq > (1ll << 31) - 1) return FA_ERR_INVALID;
   if (static_cast<int64_t>(s->Nk) > (1ll << 30)) return FA_ERR_INVALID;
@@ -266,6 +270,13 @@ const char* fa_strerror(int code) {
 int fa_last_cuda_error(void) { return g_last_cuda_error; }
 
 void fa_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns > 0 ? ns : 1; }
+
+void fa_test_withhold_arrive(void) { g_withhold = true; }
+
+void fa_set_trace(void* buf, size_t bytes) {
+  g_trace = bytes > 0 ? buf : nullptr;
+  g_trace_bytes = buf ? bytes : 0;
+}
 
 // ------------------------------------------------------------------------ plans
 int fa_tile_class(const fa_shape_t* s, int qt, int kt) {
@@ -400,6 +411,7 @@ int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, c
   a.dims = kernel_dims(s, pk);
   a.d = s->d;
   a.scale = s->scale;
+  a.tau = s->rescale_threshold;
   if ((rc = map_of(&a.tm_q, q, s, s->Nq, s->Hq, pk)) || (rc = map_of(&a.tm_k, k, s, s->Nk, s->Hkv, pk)) ||
       (rc = map_of(&a.tm_v, v, s, s->Nk, s->Hkv, pk)))
     return rc;
@@ -411,6 +423,16 @@ int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, c
     a.nnz = sp->nnz;
   }
   if (pk) a.plan = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_HEADER_BYTES);
+  if (g_trace && !pk && !sp && s->d == 128 && sms <= TRACE_MAX_CTAS &&
+      g_trace_bytes >= sizeof(unsigned long long) *
+                           (TRACE_UNIT0 + static_cast<size_t>(fwd_units(a.dims)) * TRACE_UNIT_WORDS)) {
+    a.trace = static_cast<unsigned long long*>(g_trace);
+    a.diag = DG_TRACE;
+  }
+  if (g_withhold && !pk && !sp && s->d == 128 && !s->window) {
+    a.diag = DG_WITHHOLD;
+    g_withhold = false;
+  }
   a.lse = lse;
   a.status = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_STATUS_OFFSET);
   a.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_COUNTER_OFFSET);
@@ -513,6 +535,7 @@ int fa_fwd_fp8(const fa_tensor_t* q8, const fa_tensor_t* k8, const fa_tensor_t* 
   a.dims = dims_of(s);
   a.d = s->d;
   a.scale = s->scale;
+  a.tau = s->rescale_threshold;
   if ((rc = make_map_u8(&a.tm_q, q8->ptr, s->B, s->Nq, s->Hq, s->d, q8->stride_b, q8->stride_n, q8->stride_h)) ||
       (rc = make_map_u8(&a.tm_k, k8->ptr, s->B, s->Nk, s->Hkv, s->d, k8->stride_b, k8->stride_n, k8->stride_h)) ||
       (rc = make_map_u8(&a.tm_v, v8->ptr, s->B, s->Nk, s->Hkv, s->d, v8->stride_b, v8->stride_n, v8->stride_h)))

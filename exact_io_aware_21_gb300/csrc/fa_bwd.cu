@@ -669,6 +669,10 @@ __global__ void __launch_bounds__(384, 1)
       sq += w.n_it;
     }
   }
+  // Lanes 1-31 of the producer and MMA warps had no role: they wait here for their
+  // lane 0, so that every warp reaches the block barrier converged (a barrier met by
+  // part of a warp does not hold the rest) and TMEM is freed only after all its users.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -1058,6 +1062,10 @@ __global__ void __launch_bounds__(384, 1)
       kq += n;
     }
   }
+  // Lanes 1-31 of the producer and MMA warps had no role: they wait here for their
+  // lane 0, so that every warp reaches the block barrier converged (a barrier met by
+  // part of a warp does not hold the rest) and TMEM is freed only after all its users.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int t = imax(0, issued - L::STAGES); t < issued; ++t)
           mbar_wait(&full[t % L::STAGES], (t / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
     }
+    __syncwarp();     // lanes 1-31 wait for lane 0's drain: the barrier needs the whole warp
     __syncthreads();  // pairs with the compute warps' barrier before the merge
     __syncthreads();
     return;

@@ -33,12 +33,15 @@
 // other roles walk it: K/V of listed tiles only, S and P V of a query tile only
 // at its own tiles.  Consumers release a unit's slot when the unit is done
 // (the list lives there until then).
-// The running max is the exact row max so far (TAU = 0): the dominant P of a
-// nearly one-hot row is then exactly 1.0 in bf16, so O's error scales with the
-// rest of the row, which keeps D = dO . O consistent in the backward.  The
-// rescale of O is skipped for a warp whose 32 rows kept their max.  (A stale
-// reference within TAU > 0 of the max, as lecture slides 51-52 describe, is
-// exact for O / l but rounds the dominant P; see the design notes.)
+// The reference of the exponent is the running max.  By default (tau = 0) it
+// is the exact row max so far: the dominant P of a nearly one-hot row is then
+// exactly 1.0 in bf16, so O's error scales with the rest of the row, which keeps
+// D = dO . O consistent in the backward.  The rescale of O is skipped for a warp
+// whose 32 rows kept their reference.  Conditional rescaling (lecture notes,
+// FA4: most rescalings skipped) is the opt-in tau > 0: the reference moves
+// only when a tile's max exceeds it by more than tau (log2 units), so P may
+// reach 2^tau and most tiles keep alpha = 1; O / l is still exact, but the
+// dominant P is rounded (to bf16, or as E4M3 with P's scale 2^tau / 448).
 #include <math.h>
 
 #include "fa_kernels.h"
@@ -47,7 +50,6 @@
 namespace fa {
 namespace {
 
-constexpr float TAU = 0.0f;
 constexpr float LN2 = 0.69314718055994530942f;
 constexpr float LOG2_448 = 8.8073549220576041f;  // P is quantised as 448 P = 2^(x - m + log2 448)
 
@@ -105,6 +107,7 @@ __device__ __forceinline__ SpList sp_list(uint8_t* base) {
 struct FwdParams {
   Dims dims;
   float scale_log2;
+  float tau;        // conditional rescaling threshold, log2 units (0: exact running max)
   const float* sq;  // FP8: Q block scales [B, Hq, nqt], K block scales [B, Hkv, nkt], V head scales [B, Hkv]
   const float* sk;
   const float* sv;
@@ -120,6 +123,7 @@ struct FwdParams {
   int* counter;
   unsigned long long timeout_ns;
   int total_units;
+  unsigned long long* trace;  // optional timestamps (see TRACE_UNIT0)
 };
 
 struct Bars {
@@ -192,6 +196,12 @@ __device__ __forceinline__ UnitTiles unit_tiles(const Dims& s, int p) {
   return u;
 }
 
+// A work unit's trace record (dense units; the index from (b, h, pair), so that no
+// register has to keep it alive across the unit).
+__device__ __forceinline__ unsigned long long* trace_unit(const FwdParams& p, int b, int h, int pr) {
+  return p.trace + TRACE_UNIT0 + static_cast<int64_t>(fwd_unit_index(p.dims, b, h, pr)) * TRACE_UNIT_WORDS;
+}
+
 // The unit's (b, h, pair): dense order, or the packed sequences' plan.
 template <bool VL>
 __device__ __forceinline__ void fwd_unit_of(const FwdParams& p, int u, int& b, int& h, int& pr) {
@@ -205,7 +215,7 @@ template <bool VL>
 __device__ __forceinline__ int fwd_total(const FwdParams& p) { return VL ? __ldg(p.plan) : p.total_units; }
 
 // ------------------------------------------------------------------ producer
-template <int D, int MASK, bool F8, bool VL, bool SP>
+template <int D, int MASK, bool F8, bool VL, bool SP, int DG>
 __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, const CUtensorMap* tm_q,
                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, const FwdParams& p,
                              const Ctl& ctl) {
@@ -220,6 +230,13 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
     const int slot = it & 1;
     if (!mbar_wait(&bar.unit_empty[slot], ((it >> 1) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
     const int u = atomicAdd(p.counter, 1);
+    if (DG == DG_TRACE && u < total) {
+      unsigned long long* rec = p.trace + TRACE_UNIT0 + static_cast<int64_t>(u) * TRACE_UNIT_WORDS;
+      rec[0] = globaltimer();
+      rec[3] = 0;
+      rec[4] = blockIdx.x;
+      p.trace[4 * blockIdx.x + 3] += 1;
+    }
     unit_slot[slot] = u;
     mbar_arrive(&bar.unit_full[slot]);
     if (u >= total) break;
@@ -239,6 +256,12 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
     const int qrow = VL ? sr.qoff : 0, krow = VL ? sr.koff : 0, tb = VL ? 0 : b;
     auto key_tile = [&](int step) { return SP ? static_cast<int>(sl.kt[step]) : ut.base + step; };
 
+    // The Q load must wait until the previous unit's last S has read the buffer;
+    // bring the tiles into L2 now, so that the load then comes from L2.
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int c = 0; c < L::CH; ++c) tma_prefetch_l2_4d(tm_q, c * L::ECH, h, qrow + (2 * pr + t) * TILE, tb);
     if (!mbar_wait(bar.q_empty, ((SKIP ? qn : it) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
     mbar_arrive_expect_tx(bar.q_full, 2 * L::QB);
 #pragma unroll
@@ -282,7 +305,7 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D, int MASK, bool F8, bool VL, bool SP>
+template <int D, int MASK, bool F8, bool VL, bool SP, int DG>
 __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
                         const Ctl& ctl) {
   using L = FwdLayout<D, F8, SP>;
@@ -360,9 +383,11 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
     }
 
     if (!mbar_wait(bar.q_full, (SKIP ? qn++ : static_cast<uint32_t>(it)) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+    unsigned long long* rec = DG == DG_TRACE ? p.trace + TRACE_UNIT0 + static_cast<int64_t>(u) * TRACE_UNIT_WORDS : nullptr;
     // group 0: K of local step 0
     {
       if (!group_wait(seq)) return;
+      if (rec) rec[1] = globaltimer();
       tc_fence_after();
       for (int t = 0; t < 2; ++t)
         if (nt[t] > 0 && on(t, 0)) {
@@ -395,6 +420,7 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
       if (j + 1 == nmax - 1) mma_commit(bar.q_empty);
       mma_commit(&bar.kv_empty[gq % L::NG]);
     }
+    if (rec) rec[2] = globaltimer();
     for (int t = 0; t < 2; ++t)
       if (nt[t] > 0) ++active[t];
     seq += nmax + 1;
@@ -403,7 +429,7 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
 }
 
 // ------------------------------------------------------------------ softmax
-template <int D, int MASK, bool F8, bool VL, bool SP>
+template <int D, int MASK, bool F8, bool VL, bool SP, int DG>
 __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* unit_slot, uint32_t tmem,
                             const FwdParams& p, const Ctl& ctl, uint8_t* scratch) {
   using L = FwdLayout<D, F8, SP>;
@@ -480,6 +506,7 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
       ok = mbar_wait(&bar.s_full[t], sph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
       sph ^= 1;
       if (!__all_sync(0xffffffffu, ok)) return;
+      if (DG == DG_TRACE && j == 0 && wq == 0 && lane_id() == 0) trace_unit(p, b, h, pr)[5 + t] = globaltimer();
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld128(tS, sr);
@@ -526,15 +553,15 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
         mx3 = fmax3(mx3, sv[i + 6], sv[i + 7]);
       }
       const float m_tile = fmaxf(fmax3(mx0, mx1, mx2), mx3) * cj;
-      const float m_new = (m_tile > m_run + TAU) ? m_tile : m_run;
+      const float m_new = (m_tile > m_run + p.tau) ? m_tile : m_run;
       // Under a band a row may see no key of a tile: while it has seen none at all, m
       // stays -inf, alpha 1 and every p 0.  (Causal and full rows see a key in their
       // first tile.  Measured: the guarded form costs the causal kernels 1-2% and saves
       // the full d = 64 kernel 5%, hence the split.)
       const float alpha = (MASK == MASK_CAUSAL) ? ex2(m_run - m_new) : (m_new == m_run) ? 1.f : ex2(m_run - m_new);
       const float m_use = (MASK == MASK_BAND && m_new == -INFINITY) ? 0.f : m_new;
-      // FP8: p' = 448 p (P's scale 1/448), and l sums p' alike
-      const float off = F8 ? LOG2_448 - m_use : -m_use;
+      // FP8: p' = 448 p / 2^tau (P <= 2^tau fixes P's scale at 2^tau / 448), and l sums p' alike
+      const float off = F8 ? (LOG2_448 - p.tau) - m_use : -m_use;
       const float2 neg_m2 = make_float2(off, off);
       float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
       uint32_t pk[64];
@@ -573,7 +600,10 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
       }
       tmem_wait_st();
       tc_fence_before();
-      warp_arrive(&bar.p_full[t]);
+      // (test instantiation: the first warp of query tile 0 of work unit 0 withholds its first hand-off)
+      if (DG != DG_WITHHOLD || u != 0 || j != 0 || t != 0 || wq != 0)
+        warp_arrive(&bar.p_full[t]);
+      if (DG == DG_TRACE && j == n - 1 && wq == 0 && lane_id() == 0) trace_unit(p, b, h, pr)[7 + t] = globaltimer();
       m_run = m_new;
     }
 
@@ -581,6 +611,7 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
     ok = mbar_wait(&bar.o_full[t], active & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
     ++active;
     if (!__all_sync(0xffffffffu, ok)) return;
+    if (DG == DG_TRACE && wq == 0 && lane_id() == 0) trace_unit(p, b, h, pr)[9 + t] = globaltimer();
     tc_fence_after();
     const float inv_l = (F8 ? p.sv[static_cast<int64_t>(b) * s.Hkv + kvh] : 1.f) / l_run;
     const float2 il2 = make_float2(inv_l, inv_l);
@@ -616,9 +647,15 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
     }
     if (live)  // LSE [B, Hq, Nq], or [Hq, total_q] for packed sequences
       p.lse[(VL ? static_cast<int64_t>(h) * s.total_q + qoff : (static_cast<int64_t>(b) * s.Hq + h) * s.Nq) +
-            q_row] = (m_run + __log2f(l_run) - (F8 ? LOG2_448 : 0.f)) * LN2;
+            q_row] = (m_run + __log2f(l_run) - (F8 ? LOG2_448 - p.tau : 0.f)) * LN2;
     tc_fence_before();
     warp_arrive(&bar.o_empty[t]);
+    if (DG == DG_TRACE && wq == 0 && lane_id() == 0) {
+      unsigned long long* rec = trace_unit(p, b, h, pr);
+      const unsigned long long now = globaltimer();
+      rec[11 + t] = now;
+      atomicMax(rec + 3, now);
+    }
     if (SP) warp_arrive(&bar.unit_empty[slot]);
   }
 }
@@ -713,7 +750,7 @@ __device__ void fwd_sparse_lists(uint8_t* smem, const Bars& bar, const int* unit
   }
 }
 
-template <int D, int MASK, bool F8, bool VL, bool SP>
+template <int D, int MASK, bool F8, bool VL, bool SP, int DG>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -757,34 +794,48 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (DG == DG_TRACE) {
+    if (threadIdx.x == 0) {
+      p.trace[4 * blockIdx.x] = globaltimer();
+      p.trace[4 * blockIdx.x + 2] = smid();
+      p.trace[4 * blockIdx.x + 3] = 0;
+    }
+    __syncthreads();
+  }
 
   if (warp == 0) {
-    if (lane_id() == 0) fwd_producer<D, MASK, F8, VL, SP>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
+    if (lane_id() == 0) fwd_producer<D, MASK, F8, VL, SP, DG>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
   } else if (warp == 1) {
-    if (lane_id() == 0) fwd_mma<D, MASK, F8, VL, SP>(smem, bar, unit_slot, tmem, p, ctl);
+    if (lane_id() == 0) fwd_mma<D, MASK, F8, VL, SP, DG>(smem, bar, unit_slot, tmem, p, ctl);
   } else if (SP && warp == 2) {
     fwd_sparse_lists<D, MASK>(smem, bar, unit_slot, p, ctl);
   } else if (warp >= 4) {
-    fwd_softmax<D, MASK, F8, VL, SP>((warp - 4) >> 2, smem, bar, unit_slot, tmem, p, ctl,
+    fwd_softmax<D, MASK, F8, VL, SP, DG>((warp - 4) >> 2, smem, bar, unit_slot, tmem, p, ctl,
                            smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES);
   }
+  // Lanes 1-31 of the producer and MMA warps had no role: they wait here for their
+  // lane 0, so that every warp reaches the block barrier converged (a barrier met by
+  // part of a warp does not hold the rest) and TMEM is freed only after all its users.
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (DG == DG_TRACE && threadIdx.x == 0) p.trace[4 * blockIdx.x + 1] = globaltimer();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
-template <int D, int MASK, bool F8 = false, bool VL = false, bool SP = false>
+template <int D, int MASK, bool F8 = false, bool VL = false, bool SP = false, int DG = DG_NONE>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   using L = FwdLayout<D, F8, SP>;
-  auto kern = fa_fwd_kernel<D, MASK, F8, VL, SP>;
+  auto kern = fa_fwd_kernel<D, MASK, F8, VL, SP, DG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   FwdParams p;
   p.dims = a.dims;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.tau = a.tau;
   p.sq = a.sq;
   p.sk = a.sk;
   p.sv = a.sv;
@@ -806,6 +857,7 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   p.timeout_ns = a.timeout_ns;
   p.total_units = fwd_units(a.dims);
   const int grid = imax(1, imin(p.total_units, a.num_sms));
+  p.trace = DG == DG_TRACE ? a.trace : nullptr;  // the host sets a.trace only when the grid fits TRACE_MAX_CTAS
   kern<<<grid, 384, L::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v, p);
   return cudaGetLastError();
 }
@@ -836,6 +888,16 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
     return m == MASK_BAND     ? launch_fwd_t<128, MASK_BAND, true>(a, st)
            : m == MASK_CAUSAL ? launch_fwd_t<128, MASK_CAUSAL, true>(a, st)
                               : launch_fwd_t<128, MASK_NONE, true>(a, st);
+  }
+  if (a.diag != DG_NONE) {  // timestamps, or the withheld hand-off: dense bf16 d = 128 only
+    if (a.d != 128 || (a.diag == DG_TRACE && imin(fwd_units(a.dims), a.num_sms) > TRACE_MAX_CTAS))
+      return cudaErrorInvalidValue;
+    if (a.diag == DG_WITHHOLD)
+      return m == MASK_CAUSAL ? launch_fwd_t<128, MASK_CAUSAL, false, false, false, DG_WITHHOLD>(a, st)
+                              : launch_fwd_t<128, MASK_NONE, false, false, false, DG_WITHHOLD>(a, st);
+    return m == MASK_BAND     ? launch_fwd_t<128, MASK_BAND, false, false, false, DG_TRACE>(a, st)
+           : m == MASK_CAUSAL ? launch_fwd_t<128, MASK_CAUSAL, false, false, false, DG_TRACE>(a, st)
+                              : launch_fwd_t<128, MASK_NONE, false, false, false, DG_TRACE>(a, st);
   }
   if (a.d == 64)
     return m == MASK_BAND ? launch_fwd_t<64, MASK_BAND>(a, st)

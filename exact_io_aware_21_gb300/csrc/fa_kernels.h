@@ -18,6 +18,7 @@ struct FwdLaunch {
   Dims dims;
   int d;
   float scale;
+  float tau;  // conditional rescaling: the reference max moves only past this margin (log2 units)
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps, box 64 x 1 x 128 x 1, 128B swizzle
   OutRows o;
   OutRows o_res;   // ptr == nullptr: residual not written
@@ -37,8 +38,24 @@ struct FwdLaunch {
   const int* col_idx;  // [nnz]
   int nnz;
   int* plan;           // packed sequences: workspace for the device-side work plan
+  unsigned long long* trace;  // timestamps (diag == DG_TRACE); layout below
+  int diag;                   // DG_NONE, or a diagnostic instantiation (below)
 };
+// Diagnostic instantiations of the dense bf16 d = 128 forward: DG_TRACE writes
+// timestamps into `trace`; DG_WITHHOLD (tests of the bounded waits) has one softmax
+// warp of work unit 0 skip its first P hand-off, so that CTA's MMA issuer's wait runs out.
+constexpr int DG_NONE = 0, DG_TRACE = 1, DG_WITHHOLD = 2;
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
+
+// Forward trace (diagnostics), %globaltimer nanoseconds.  Per CTA c < TRACE_MAX_CTAS:
+// [4c] start (after set-up), [4c+1] end, [4c+2] SM id, [4c+3] units run.  Per work
+// unit u: [TRACE_UNIT0 + 16u + k], k = 0 claimed, 1 first product issued, 2 last
+// product issued, 3 output written (the later query tile), 4 CTA; per query tile t
+// of the unit (softmax warps): 5 + t its first S received, 7 + t its last P handed
+// over, 9 + t its final O ready (products done), 11 + t its output written.
+constexpr int TRACE_MAX_CTAS = 1024;
+constexpr int TRACE_UNIT0 = 4 * TRACE_MAX_CTAS;
+constexpr int TRACE_UNIT_WORDS = 16;
 
 struct BwdLaunch {
   Dims dims;

@@ -57,4 +57,13 @@ int fa_decode_noalloc(const fa_tensor_t* q, const fa_tensor_t* kcache, const fa_
   return fa_decode(q, kcache, vcache, o, lse, shape, num_splits, scratch, FA_DECODE_SCRATCH_BYTES, stream);
 }
 
+int fa_decode_noalloc_status(void* stream, int* status) {
+  if (!status) return FA_ERR_INVALID;
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != FA_OK) return rc;
+  // the array starts with the same header as a workspace, status word first
+  return fa_get_device_status(scratch, stream, status);
+}
+
 }  // extern "C"

@@ -194,6 +194,12 @@ FA_HD void fwd_unit(const Dims& s, int u, int& b, int& h, int& p) {
   h = bh % s.Hq;
 }
 
+// The unit index of (b, h, p): the inverse of fwd_unit.
+FA_HD int fwd_unit_index(const Dims& s, int b, int h, int p) {
+  const int P = fwd_pairs(s), BH = s.B * s.Hq, bh = b * s.Hq + h;
+  return s.causal ? (P - 1 - p) * BH + bh : bh * P + p;
+}
+
 // ---- dK/dV units: (b, kvh, kt) -------------------------------------------------
 FA_HD int dkdv_units(const Dims& s) { return s.B * s.Hkv * k_tiles(s); }
 

@@ -86,6 +86,19 @@ typedef struct {
   int window;
   int window_left;
   int window_right;
+  /* Conditional rescaling (lecture notes, FA4: a variant of the online softmax
+   * that skips most rescalings of O).  The forward exponentiates each key tile
+   * against a reference max that moves only when the tile's row max exceeds it
+   * by more than rescale_threshold, in log2 units of the probabilities (P then
+   * reaches at most 2^rescale_threshold before normalisation); O and l keep
+   * their scale while it stays, so most O rescalings are skipped.  O / l and the
+   * LSE stay exact up to rounding; what changes is the rounding of P: the
+   * dominant P of a nearly one-hot row is no longer exactly 1.0, which costs
+   * the backward accuracy there (D = dO . O from a forward O that carries that
+   * rounding).  0 (a zero-initialised struct) = the exact running max; range
+   * [0, 16]; FA4 uses 8.  Read by the forward calls (fa_fwd, fa_fwd_varlen,
+   * fa_fwd_blocksparse, fa_fwd_fp8); the backward and decode calls ignore it. */
+  float rescale_threshold;
 } fa_shape_t;
 
 /* ---------------------------------------------------------------------------
@@ -331,13 +344,20 @@ size_t fa_decode_paged_workspace_size(const fa_shape_t* shape, int num_splits, i
  *  - All calls share the one array, which keeps the last call's contents.
  *    Calls whose work overlaps on the GPU (other streams, other host threads)
  *    race on it: order them on one stream.
- *  - fa_get_device_status() cannot reach this array; a timed-out wait still
- *    ends the kernels, but its status bit is not reported.
+ *  - Errors found on the GPU (a bounded wait that ran out) are recorded in
+ *    the array's header, as in a workspace: fa_decode_noalloc_status() reads
+ *    and clears them (fa_get_device_status() cannot reach the array).
  * ------------------------------------------------------------------------- */
 #define FA_DECODE_SCRATCH_BYTES ((size_t)8 << 20)
 size_t fa_decode_noalloc_max_bytes(void);
 int fa_decode_noalloc(const fa_tensor_t* q, const fa_tensor_t* kcache, const fa_tensor_t* vcache,
                       const fa_tensor_t* o, float* lse, const fa_shape_t* shape, int num_splits, void* stream);
+/* Device status of the latest fa_decode_noalloc call on the current device:
+ * synchronises `stream`, returns the error bits its kernels recorded in the
+ * fixed array (0 = none) through *status and clears them; the return value is
+ * as fa_get_device_status's (FA_ERR_TIMEOUT when a bounded wait ran out).
+ * Allocates nothing. */
+int fa_decode_noalloc_status(void* stream, int* status);
 
 /* ---------------------------------------------------------------------------
  * Device status.  Synchronises `stream`, returns the error bits the kernels
@@ -350,6 +370,36 @@ int fa_get_device_status(void* workspace, void* stream, int* status);
 /* Time budget of every device-side wait, in nanoseconds (default 10 s).  A
  * wait that runs out records an error and the kernel returns early.  */
 void fa_set_wait_timeout_ns(unsigned long long ns);
+
+/* Test hook for the bounded waits (no counterpart on the pages).  The next
+ * fa_fwd call with d = 128 on dense tensors without a window runs a test
+ * instantiation of the forward kernel in which one softmax warp of the CTA
+ * that runs work unit 0 skips its first hand-off of P (one software mbarrier
+ * arrive; no copy and no tensor-core operation is touched).  The tensor-core
+ * issuer of that CTA then
+ * waits until the wait budget (fa_set_wait_timeout_ns) runs out, records
+ * FA_STATUS_TIMEOUT_MMA, and every role of the CTA leaves early: copies in
+ * flight land, TMEM is freed, and the units it held are not written.
+ * fa_get_device_status then returns FA_ERR_TIMEOUT.  One-shot: later calls run
+ * the normal kernels.  Not thread-safe; for tests. */
+void fa_test_withhold_arrive(void);
+
+/* Diagnostics (no counterpart on the pages): timestamps of the dense forward
+ * kernel, to see how its persistent CTAs spend the launch.  With a buffer set
+ * (device memory, 8-byte aligned), every later fa_fwd call with d = 128 (dense
+ * tensors; not the packed, block-sparse or FP8 calls) runs an instantiation of
+ * the kernel that also writes %globaltimer nanoseconds into it:
+ *   per CTA c < 1024:  buf[4c] start (after set-up), buf[4c+1] end, buf[4c+2]
+ *                      SM id, buf[4c+3] work units it ran;
+ *   per work unit u:   buf[4096 + 16u + k], k = 0 claimed, 1 first product
+ *                      issued, 2 last product issued, 3 output written, 4 CTA;
+ *                      per query tile t = 0, 1 of the unit: 5 + t its first S
+ *                      received, 7 + t its last P handed over, 9 + t its final
+ *                      O ready, 11 + t its output written.
+ * bytes must cover 8 * (4096 + 16 * units) (units: fa_fwd_num_units); otherwise
+ * nothing is written.  buf = NULL or bytes = 0 turns it off.  The buffer is the
+ * caller's and is overwritten by every traced call. */
+void fa_set_trace(void* buf, size_t bytes);
 
 const char* fa_strerror(int code);
 /* The last CUDA runtime error code seen by the library (cudaError_t value). */

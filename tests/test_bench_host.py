@@ -76,3 +76,19 @@ def test_training_legs_are_the_benchmark_plan():
                                        "gqa_causal_b1_hq32_hkv8_n8192_d128_outliers"]
     assert bench.tiny_workload() is inputs.TINY
     assert set(bench.TARGET_TRAIN) <= {w.name for w in train}
+
+
+def test_trace_summary_of_a_synthetic_trace():
+    """Two CTAs; CTA 0 runs units 0 and 2, CTA 1 runs unit 1 (times in ns)."""
+    t = np.zeros(4096 + 16 * 3, dtype=np.int64)
+    t[0:4] = [1000, 11000, 5, 2]
+    t[4:8] = [2000, 9000, 7, 1]
+    for u, r in enumerate([[1000, 1500, 5000, 6000, 0], [2000, 2500, 8000, 9000, 1], [5000, 6000, 10000, 11000, 0]]):
+        t[4096 + 16 * u:4096 + 16 * u + 5] = r
+    s = bench.trace_summary(t, 3)
+    assert s["ctas"] == 2 and s["span_us"] == 10.0 and s["start_spread_us"] == 1.0
+    assert s["busy_us"] == {"min": 7.0, "median": 8.5, "max": 10.0} and s["end_spread_us"] == 2.0
+    assert s["units_per_cta"] == {"min": 1.0, "median": 1.5, "max": 2.0}
+    assert s["unit_claim_to_first_product_us"]["max"] == 1.0
+    assert s["unit_last_product_to_output_us"] == {"min": 1.0, "median": 1.0, "max": 1.0}
+    assert s["issue_share_of_busy"] == round((3.5 + 5.5 + 4.0) / 17.0, 4)

@@ -238,7 +238,7 @@ def test_backward_split_key_tiles(B, Hq, Hkv, N, d, causal, local):
                      dtype=torch.uint8, device=DEV)
     grads = []
     for _ in range(2):
-        g = [torch.empty_like(t) for t in (q, k, v)]
+        g = [torch.full_like(t, float("nan")) for t in (q, k, v)]
         fa.fa_bwd_blocksparse(q, k, v, rpd, cid, o, lse, do, *g, s, ws, res)
         torch.cuda.synchronize()
         grads.append(g)

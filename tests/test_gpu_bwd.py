@@ -82,7 +82,7 @@ def test_bwd_parts_equal_bwd():
     a = fa.backward(q, k, v, o, lse, do, causal=True, o_residual=res)
     s = fa.binding._dims(q, k, None, True)
     ws = torch.zeros(fa.library().fa_bwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=DEV)
-    g = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+    g = [torch.full_like(t, float("nan")) for t in (q, k, v)]
     for part in range(3):
         fa.binding.fa_bwd_part(part, q, k, v, o, lse, do, *g, s, ws, res)
     torch.cuda.synchronize()

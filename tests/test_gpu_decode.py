@@ -35,8 +35,8 @@ def run_decode(q, k, v, S):
     s = fa.binding._dims(q, k, None, False)
     n_used = fa.library().fa_decode_num_splits(ctypes.byref(s), S)
     ws = torch.zeros(fa.library().fa_decode_workspace_size(ctypes.byref(s), S), dtype=torch.uint8, device=DEV)
-    o = torch.empty(q.shape, dtype=torch.bfloat16, device=DEV)
-    lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=DEV)
+    o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((s.B, s.Hq, s.Nq), float("nan"), dtype=torch.float32, device=DEV)
     fa.binding.fa_decode(q, k, v, o, lse, s, S, ws)
     rc, st = fa.binding.device_status(ws)
     assert rc == 0 and st == 0

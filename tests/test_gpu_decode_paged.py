@@ -128,8 +128,8 @@ def test_bad_lengths_and_pages_are_reported_not_faulted(Hq, Hkv, page):
 
     def call(lens, tab):
         ws = torch.zeros(lib.fa_decode_paged_workspace_size(ctypes.byref(s), 0, page), dtype=torch.uint8, device=DEV)
-        o = torch.empty(q.shape, dtype=torch.bfloat16, device=DEV)
-        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=DEV)
+        o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=DEV)
+        lse = torch.full((B, Hq, Nq), float("nan"), dtype=torch.float32, device=DEV)
         fa.binding.fa_decode_paged(q, kc, vc, tab, torch.tensor(lens, dtype=torch.int32, device=DEV), o, lse, s, 0,
                                    ws)
         return fa.binding.device_status(ws), o, lse

@@ -84,7 +84,7 @@ def test_quantize_strided_views():
     x = inputs.shape_inputs(1, 4, 4, 256, 256, 128, seed=3, with_do=False)["q"].to(DEV)
     xv = x[:, :, 1:3]                                          # a head slice: strided rows
     out = torch.zeros((1, 256, 4, 128), dtype=torch.uint8, device=DEV)[:, :, 1:3]
-    sc = torch.empty((1, 2, 2), dtype=torch.float32, device=DEV)
+    sc = torch.full((1, 2, 2), float("nan"), dtype=torch.float32, device=DEV)
     ws = torch.zeros(fa.library().fa_quantize_fp8_workspace_size(1, 2), dtype=torch.uint8, device=DEV)
     fa.fa_quantize_fp8(xv, 128, None, out, sc, ws)
     torch.cuda.synchronize()

@@ -179,3 +179,34 @@ def sampled_check(w, n_heads=3, n_rows=96, seed=11):
                          ids=lambda w: w.name)
 def test_full_workload_sampled(w):
     sampled_check(w)
+
+
+# ------------------------------------------------------------------ forward trace (diagnostics)
+def test_forward_trace_stamps_every_unit_and_leaves_results_unchanged():
+    """A traced launch writes consistent timestamps for every CTA and unit (claimed <=
+    first product <= last product <= output written, inside its CTA's span) and
+    computes the same output, bit for bit, as an untraced launch."""
+    x = inputs.shape_inputs(2, 4, 2, 1000, 1000, 128, seed=31, with_do=False)
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    o_ref, lse_ref = fa.forward(q, k, v, causal=True)
+    s = fa.binding.shape(2, 4, 2, 1000, 1000, 128, None, True)
+    units = fa.library().fa_fwd_num_units(ctypes.byref(s))
+    buf = torch.zeros(fa.binding.TRACE_UNIT0 + fa.binding.TRACE_UNIT_WORDS * units, dtype=torch.int64, device=DEV)
+    fa.binding.set_trace(buf)
+    try:
+        o, lse = fa.forward(q, k, v, causal=True)
+        torch.cuda.synchronize()
+    finally:
+        fa.binding.set_trace(None)
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+    t = buf.cpu().numpy()
+    cta = t[:4096].reshape(1024, 4)
+    grid = int((cta[:, 0] > 0).sum())
+    assert grid == min(units, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert (cta[:grid, 1] >= cta[:grid, 0]).all() and int(cta[:grid, 3].sum()) == units
+    rec = t[4096:4096 + 16 * units].reshape(units, 16)
+    assert (rec[:, 0] > 0).all() and (rec[:, 1] >= rec[:, 0]).all() and (rec[:, 2] >= rec[:, 1]).all()
+    assert (rec[:, 3] >= rec[:, 2]).all()
+    c = rec[:, 4]
+    assert ((c >= 0) & (c < grid)).all()
+    assert (rec[:, 0] >= cta[c, 0]).all() and (rec[:, 3] <= cta[c, 1]).all()

@@ -5,8 +5,10 @@ reserves all device memory for its own pool at start-up, or a plug-in that
 only receives the call's tensors.  fa_decode_noalloc gives them the same
 decode as fa_decode, with its scratch in a fixed array inside the library.
 These tests call both entry points through the C ABI on the same inputs and
-require the outputs to agree within the parity tolerances, on two calls in a
-row (the second call reuses the array the first one left behind).
+require the outputs to agree within the parity tolerances, and both to match
+the fp64 oracle, on two calls in a row (the second call reuses the array the
+first one left behind); after each call the array's status header, read with
+fa_decode_noalloc_status, must report no error.
 
 This file is collected last, so a run that stops at the first failure has
 already run every other test; it also passes when run alone.
@@ -21,6 +23,7 @@ import torch
 import exact_io_aware_21_gb300 as fa
 from exact_io_aware_21_gb300 import inputs
 from exact_io_aware_21_gb300.binding import check, tdesc
+from oracle import attention as A
 from parity import assert_fwd
 
 pytestmark = pytest.mark.gpu
@@ -34,7 +37,9 @@ def noalloc(q, k, v, num_splits):
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     check(fa.library().fa_decode_noalloc(tdesc(q), tdesc(k), tdesc(v), tdesc(o), lse.data_ptr(), ctypes.byref(s),
                                          int(num_splits), stream))
-    torch.cuda.synchronize()
+    bits = ctypes.c_int(-1)
+    rc = fa.library().fa_decode_noalloc_status(stream, ctypes.byref(bits))
+    assert rc == 0 and bits.value == 0, f"status {bits.value:#x}"
     return o, lse
 
 
@@ -51,6 +56,8 @@ def test_matches_fa_decode_on_two_calls_in_a_row(num_splits):
         o_ref, lse_ref = fa.decode(q, k, v, num_splits=num_splits)
         o, lse = noalloc(q, k, v, num_splits)
         assert_fwd(o, lse, o_ref, lse_ref, f"noalloc vs fa_decode {B}x{Hq}/{Hkv}x{Nq}x{Nk}")
+        o_or, lse_or = A.attention_forward(q.cpu(), k.cpu(), v.cpu(), 1 / np.sqrt(128))
+        assert_fwd(o, lse, o_or, lse_or, f"noalloc vs the oracle {B}x{Hq}/{Hkv}x{Nq}x{Nk}")
     # and the same problem twice: identical results
     q, k, v = draw(2, 8, 2, 4, 3000, 11)
     a = noalloc(q, k, v, num_splits)

@@ -92,6 +92,23 @@ int make_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int64_
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ALIGN;
 }
 
+// Map for TMA stores of a bf16 [B, N, H, d] output: boxes of 32 channels x 32 rows
+// (one warp's rows, 64 bytes each), 64-byte swizzle; rows past N are dropped.
+int make_store_map(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int64_t sb, int64_t sn, int64_t sh) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return FA_ERR_CUDA;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(sn) * 2,
+                           static_cast<cuuint64_t>(sb) * 2};
+  cuuint32_t box[4] = {32, 1, 32, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_ALIGN;
+}
+
 // The same map over one-byte elements (E4M3 codes): box 128 x 1 x box_rows x 1,
 // the 128-byte inner box matching the 128-byte swizzle.  Strides in elements.
 int make_map_u8(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int64_t sb, int64_t sn, int64_t sh,
@@ -220,7 +237,7 @@ int decode_splits_resolved(const fa_shape_t* s, int requested, int sms) {
 // The head-group paged decode: does it apply, and its splits per sequence.  The
 // same cost model over 16-key slices, with B * Hkv / 8 CTAs per split.
 bool decode_head_groups(const fa_shape_t* s, int page_size) {
-  return s->Hkv % DECODE_HEAD_GROUP == 0 && page_size % 16 == 0;
+  return s->Hkv % DECODE_HEAD_GROUP == 0 && page_size % 16 == 0 && (s->Hq / s->Hkv) * s->Nq <= 16;
 }
 
 int decode_splits_hg(const fa_shape_t* s, int requested, int sms) {
@@ -311,6 +328,15 @@ int fa_dq_unit(const fa_shape_t* s, int i, int* b, int* h, int* qt) {
   const Dims d = dims_of(s);
   if (i < 0 || i >= dq_units(d)) return FA_ERR_INVALID;
   dq_unit(d, i, *b, *h, *qt);
+  return FA_OK;
+}
+
+int fa_fwd_schedule(const fa_shape_t* s, int grid, int* start, int* ord) {
+  if (check_shape(s) != FA_OK || !start || !ord) return FA_ERR_INVALID;
+  const FwdSched* sc = causal_schedule(dims_of(s), s->d, false, grid);
+  if (!sc) return FA_ERR_INVALID;
+  for (int c = 0; c <= grid; ++c) start[c] = sc->start[c];
+  for (int k = 0; k < sc->start[grid]; ++k) ord[k] = sc->ord[k];
   return FA_OK;
 }
 
@@ -417,12 +443,21 @@ int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, c
     return rc;
   a.o = out_rows(o, pk);
   a.o_res = o_res ? out_rows(o_res, pk) : OutRows{nullptr, 0, 0, 0};
+  if (!pk && !sp) {  // dense: the outputs leave through TMA stores
+    if ((rc = make_store_map(&a.tm_o, o->ptr, s->B, s->Nq, s->Hq, s->d, o->stride_b, o->stride_n, o->stride_h)))
+      return rc;
+    if (o_res && (rc = make_store_map(&a.tm_r, o_res->ptr, s->B, s->Nq, s->Hq, s->d, o_res->stride_b,
+                                      o_res->stride_n, o_res->stride_h)))
+      return rc;
+    a.tma_out = 1;
+  }
   if (sp) {
     a.row_ptr = sp->row_ptr;
     a.col_idx = sp->col_idx;
     a.nnz = sp->nnz;
   }
   if (pk) a.plan = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_HEADER_BYTES);
+  if (!pk && !sp) a.sched = causal_schedule(a.dims, s->d, false, imax(1, imin(fwd_units(a.dims), sms)));
   if (g_trace && !pk && !sp && s->d == 128 && sms <= TRACE_MAX_CTAS &&
       g_trace_bytes >= sizeof(unsigned long long) *
                            (TRACE_UNIT0 + static_cast<size_t>(fwd_units(a.dims)) * TRACE_UNIT_WORDS)) {
@@ -542,6 +577,9 @@ int fa_fwd_fp8(const fa_tensor_t* q8, const fa_tensor_t* k8, const fa_tensor_t* 
     return rc;
   a.o = rows_of(o);
   a.o_res = OutRows{nullptr, 0, 0, 0};
+  if ((rc = make_store_map(&a.tm_o, o->ptr, s->B, s->Nq, s->Hq, s->d, o->stride_b, o->stride_n, o->stride_h)))
+    return rc;
+  a.tma_out = 1;
   a.lse = lse;
   a.sq = q_scale;
   a.sk = k_scale;
@@ -550,6 +588,7 @@ int fa_fwd_fp8(const fa_tensor_t* q8, const fa_tensor_t* k8, const fa_tensor_t* 
   a.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_COUNTER_OFFSET);
   a.timeout_ns = g_timeout_ns;
   a.num_sms = sms;
+  a.sched = causal_schedule(a.dims, s->d, true, imax(1, imin(fwd_units(a.dims), sms)));
   if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
   cudaError_t e = launch_fwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
@@ -773,7 +812,7 @@ int fa_decode(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor_t* vc
       (rc = check_tensor(o)))
     return rc;
   if (!lse || s->causal || s->window) return FA_ERR_INVALID;
-  if ((s->Hq / s->Hkv) * s->Nq > 16) return FA_ERR_INVALID;  // packed rows must fit one 16-row tile
+  if ((s->Hq / s->Hkv) * s->Nq > 64) return FA_ERR_INVALID;  // packed rows: at most four 16-row tiles
   int sms = 0;
   if ((rc = device_info(&sms))) return rc;
   const int S = decode_splits_resolved(s, num_splits, sms);
@@ -815,7 +854,7 @@ int fa_decode_paged(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor
     return rc;
   if (!lse || s->causal || s->window || !block_table || !seqlens_k || max_pages < 1 || num_pages < 1)
     return FA_ERR_INVALID;
-  if ((s->Hq / s->Hkv) * s->Nq > 16) return FA_ERR_INVALID;
+  if ((s->Hq / s->Hkv) * s->Nq > 64) return FA_ERR_INVALID;
   // pages of 16, 32 or 64 keys stack into a 128-key tile; larger pages hold whole tiles
   const bool small = page_size == 16 || page_size == 32 || page_size == 64;
   if (!small && (page_size < TILE || page_size % TILE != 0)) return FA_ERR_INVALID;

@@ -12,13 +12,16 @@
 // built around the copy engine: one CTA per (split, K/V head, batch); a
 // producer warp streams 128-key K and V tiles with TMA (16-byte aligned,
 // 128-byte-swizzled boxes of 64 channels x 128 keys) through a ring of
-// shared-memory stages; 8 compute warps each own 16 keys of every tile.  The
-// packed rows (Hq/Hkv * Nq <= 16) form exactly one 16-row matrix tile, which
-// is what the warp-level mma.sync m16n8k16 handles: the scores, the online
-// softmax and P stay in registers, and no cross-warp exchange is needed until
-// the split ends.  (A 128-row tcgen05 product would be 87% padding here.)
-// The warps' states are merged through shared memory into the split's
-// (LSE_s, O_s); the combine kernel then merges the splits.
+// shared-memory stages; 8 compute warps share every tile.  The packed rows
+// (Hq/Hkv * Nq of them) form RT = 1, 2 or 4 matrix tiles of 16 rows, which is
+// what the warp-level mma.sync m16n8k16 handles: the warps split into RT
+// groups, one per 16-row tile, and each warp of a group owns 16 RT keys of
+// every 128-key tile; the scores, the online softmax and P stay in registers,
+// and no cross-warp exchange is needed until the split ends.  (A 128-row
+// tcgen05 product would be 50-87% padding here; lecture slides 57-60 pack the
+// heads and the query positions into the rows in the same way.)  The warps'
+// states are merged through shared memory into the split's (LSE_s, O_s); the
+// combine kernel then merges the splits.
 //
 // Paged, variable-length cache (§18.8.2 part 3, §18.8.3: PagedAttention keeps
 // the cache in fixed-size physical pages and maps each sequence's logical pages
@@ -50,7 +53,8 @@ namespace fa {
 namespace {
 
 constexpr float LN2 = 0.69314718055994530942f;
-constexpr int WARPS = 8;              // compute warps, 16 keys of each tile apiece (HG: one head each)
+constexpr int WARPS = 8;              // compute warps (HG: one head each)
+constexpr int MAX_ROW_TILES = 4;      // packed rows Hq/Hkv * Nq <= 64
 static_assert(WARPS == DECODE_HEAD_GROUP, "a head group is one head per compute warp");
 constexpr int THREADS = 32 * (WARPS + 1);
 
@@ -113,12 +117,15 @@ __device__ __forceinline__ uint32_t swz(int key, int ch) {
   return (ch >> 6) * (TILE * 128) + key * 128 + ((((ch & 63) >> 3) ^ (key & 7)) << 4) + ((ch & 7) << 1);
 }
 
-template <int D, bool PAGED, bool HG>
+template <int D, bool PAGED, bool HG, int RT>
 __global__ void __launch_bounds__(THREADS, 1)
     fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecParams p) {
   using L = DecLayout<D>;
   static_assert(!HG || PAGED, "head groups are a paged layout");
+  static_assert(!HG || RT == 1, "a head group has one 16-row tile per head");
+  constexpr int WPR = WARPS / RT;  // warps per 16-row tile
+  constexpr int KW = TILE / WPR;   // keys of each 128-key tile per warp (16 RT), in RT chunks of 16
   constexpr int KT = HG ? 16 : TILE;  // keys per stage: a page slice (all 8 heads) or a tile of one head
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -265,10 +272,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   // -------------------------------------------------------------- compute warps
   const int gq = lane >> 2, tq = lane & 3;  // fragment row group / column pair
+  const int rt = warp / WPR;                // this warp's 16-row tile (HG: 0)
   // Q as m16n8k16 A fragments (rows r = qpos * g + head-in-group, zero above `rows`).
   uint32_t qa[D / 16][4];
   {
-    const int ra = gq, rb = gq + 8;
+    const int ra = rt * 16 + gq, rb = ra + 8;
     const __nv_bfloat16* qpa = nullptr;
     const __nv_bfloat16* qpb = nullptr;
     if (ra < rows) qpa = p.q + b * p.q_sb + (ra / g) * p.q_sn + (kvh * g + ra % g) * p.q_sh;
@@ -300,49 +308,61 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     const uint32_t kb = smem_u32(smem + L::OFF_KV + st * 2 * L::TB);
     const uint32_t vb = kb + L::TB;
-    // this warp's 16 rows of the stage: keys 16 warp .. + 15 of the tile, or (HG)
-    // the slice's 16 keys of this warp's head
-    const int key_base = 16 * warp;
+    // this warp's rows of the stage: keys KW (warp % WPR) .. + KW-1 of the tile, or
+    // (HG) the slice's 16 keys of this warp's head
+    const int key_base = KW * (warp % WPR);
 
-    // S = Q K^T for 16 rows x 16 keys (two n8 tiles)
-    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // S = Q K^T for 16 rows x KW keys (2 RT n8 tiles)
+    float sacc[2 * RT][4];
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      // matrices: (keys 0-7, ch lo), (keys 0-7, ch hi), (keys 8-15, ch lo), (keys 8-15, ch hi)
-      const int key = key_base + 8 * (mat >> 1) + mrow;
-      const int ch = ks * 16 + 8 * (mat & 1);
-      uint32_t b00, b01, b10, b11;
-      ldsm_x4(kb + swz(key, ch), b00, b01, b10, b11);
-      mma_16816(sacc[0], qa[ks], b00, b01);
-      mma_16816(sacc[1], qa[ks], b10, b11);
-    }
+    for (int nt = 0; nt < 2 * RT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+    for (int cq = 0; cq < RT; ++cq)
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        // matrices: (keys 0-7, ch lo), (keys 0-7, ch hi), (keys 8-15, ch lo), (keys 8-15, ch hi)
+        const int key = key_base + 16 * cq + 8 * (mat >> 1) + mrow;
+        const int ch = ks * 16 + 8 * (mat & 1);
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(kb + swz(key, ch), b00, b01, b10, b11);
+        mma_16816(sacc[2 * cq], qa[ks], b00, b01);
+        mma_16816(sacc[2 * cq + 1], qa[ks], b10, b11);
+      }
     // mask keys outside [k0, k1)
     const int key0 = k0 + t * KT + (HG ? 0 : key_base);
-    float sv[2][4];
+    float sv[2 * RT][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < 2 * RT; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int key = key0 + 8 * nt + 2 * tq + (i & 1);
         sv[nt][i] = key < k1 ? sacc[nt][i] : -INFINITY;
       }
-    // online softmax for rows gq (i = 0,1) and gq+8 (i = 2,3)
-    uint32_t pa[4];
+    // online softmax for rows gq (i = 0,1) and gq+8 (i = 2,3), over the warp's KW keys
+    uint32_t pa[RT][4];
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
-      float mx = fmaxf(fmaxf(sv[0][2 * hr], sv[0][2 * hr + 1]), fmaxf(sv[1][2 * hr], sv[1][2 * hr + 1]));
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2 * RT; ++nt) mx = fmax3(mx, sv[nt][2 * hr], sv[nt][2 * hr + 1]);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       const float m_tile = mx * c;
       const float m_new = fmaxf(m_run[hr], m_tile);
       const float alpha = (m_new == m_run[hr]) ? 1.f : ex2(m_run[hr] - m_new);
       const float mu = (m_new == -INFINITY) ? 0.f : m_new;
-      const float p00 = ex2(fmaf(sv[0][2 * hr], c, -mu)), p01 = ex2(fmaf(sv[0][2 * hr + 1], c, -mu));
-      const float p10 = ex2(fmaf(sv[1][2 * hr], c, -mu)), p11 = ex2(fmaf(sv[1][2 * hr + 1], c, -mu));
-      l_run[hr] = l_run[hr] * alpha + (p00 + p01 + p10 + p11);
+      float lsum = 0.f;
+#pragma unroll
+      for (int cq = 0; cq < RT; ++cq) {
+        const float p00 = ex2(fmaf(sv[2 * cq][2 * hr], c, -mu)), p01 = ex2(fmaf(sv[2 * cq][2 * hr + 1], c, -mu));
+        const float p10 = ex2(fmaf(sv[2 * cq + 1][2 * hr], c, -mu));
+        const float p11 = ex2(fmaf(sv[2 * cq + 1][2 * hr + 1], c, -mu));
+        lsum += (p00 + p01 + p10 + p11);
+        pa[cq][hr] = pack_bf16(p00, p01);      // a0 (row gq) / a1 (row gq+8): keys 2tq, 2tq+1 of the chunk
+        pa[cq][2 + hr] = pack_bf16(p10, p11);  // a2 / a3: keys 8+2tq, 9+2tq
+      }
+      l_run[hr] = l_run[hr] * alpha + lsum;
       m_run[hr] = m_new;
-      pa[hr] = pack_bf16(p00, p01);      // a0 (row gq) / a1 (row gq+8): keys 2tq, 2tq+1
-      pa[2 + hr] = pack_bf16(p10, p11);  // a2 / a3: keys 8+2tq, 9+2tq
       if (alpha != 1.f) {
 #pragma unroll
         for (int nt = 0; nt < D / 8; ++nt) {
@@ -351,31 +371,36 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     }
-    // O += P V: B fragments of V (16 keys x 8 channels) via transposed ldmatrix.
-    // Paged: V rows past the split's end may hold anything (stale shared memory or
-    // an unused part of a page); they are zeroed, as their P is.  This thread's
-    // fragment halves cover keys key0 + 2tq (+1) and key0 + 8 + 2tq (+1).
-    uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
-    if (PAGED && key0 + 16 > k1) {
-      const int ka = key0 + 2 * tq, kb8 = ka + 8;
-      vmask_lo = (ka < k1 ? 0x0000ffffu : 0u) | (ka + 1 < k1 ? 0xffff0000u : 0u);
-      vmask_hi = (kb8 < k1 ? 0x0000ffffu : 0u) | (kb8 + 1 < k1 ? 0xffff0000u : 0u);
-    }
+    // O += P V: B fragments of V (16 keys x 8 channels) via transposed ldmatrix,
+    // one 16-key chunk at a time.  Paged: V rows past the split's end may hold
+    // anything (stale shared memory or an unused part of a page); they are zeroed,
+    // as their P is.  This thread's fragment halves cover keys kc + 2tq (+1) and
+    // kc + 8 + 2tq (+1) of chunk kc.
 #pragma unroll
-    for (int np = 0; np < D / 16; ++np) {
-      // matrices: (keys 0-7, ch n0..), (keys 8-15, ch n0..), (keys 0-7, ch n0+8..), (keys 8-15, ch n0+8..)
-      const int key = key_base + 8 * (mat & 1) + mrow;
-      const int ch = np * 16 + 8 * (mat >> 1);
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(vb + swz(key, ch), v0, v1, v2, v3);
-      if (PAGED) {
-        v0 &= vmask_lo;
-        v2 &= vmask_lo;
-        v1 &= vmask_hi;
-        v3 &= vmask_hi;
+    for (int cq = 0; cq < RT; ++cq) {
+      uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+      const int kc = key0 + 16 * cq;
+      if (PAGED && kc + 16 > k1) {
+        const int ka = kc + 2 * tq, kb8 = ka + 8;
+        vmask_lo = (ka < k1 ? 0x0000ffffu : 0u) | (ka + 1 < k1 ? 0xffff0000u : 0u);
+        vmask_hi = (kb8 < k1 ? 0x0000ffffu : 0u) | (kb8 + 1 < k1 ? 0xffff0000u : 0u);
       }
-      mma_16816(o[2 * np], pa, v0, v1);
-      mma_16816(o[2 * np + 1], pa, v2, v3);
+#pragma unroll
+      for (int np = 0; np < D / 16; ++np) {
+        // matrices: (keys 0-7, ch n0..), (keys 8-15, ch n0..), (keys 0-7, ch n0+8..), (keys 8-15, ch n0+8..)
+        const int key = key_base + 16 * cq + 8 * (mat & 1) + mrow;
+        const int ch = np * 16 + 8 * (mat >> 1);
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(vb + swz(key, ch), v0, v1, v2, v3);
+        if (PAGED) {
+          v0 &= vmask_lo;
+          v2 &= vmask_lo;
+          v1 &= vmask_hi;
+          v3 &= vmask_hi;
+        }
+        mma_16816(o[2 * np], pa[cq], v0, v1);
+        mma_16816(o[2 * np + 1], pa[cq], v2, v3);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
@@ -429,22 +454,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   __syncthreads();
   if (!ok) return;
-  // 256 threads: thread -> (row, channel range)
+  // 256 threads: thread -> (row, channel range); row r's state is in the WPR warps
+  // of its 16-row tile, at their local row r % 16
   const int tid = threadIdx.x;  // < 256
-  constexpr int PER = 16 * D / 256;  // channels per thread
+  constexpr int PER = RT * 16 * D / 256;  // channels per thread
   const int row = tid / (D / PER);
   const int chb = (tid % (D / PER)) * PER;
   if (row < rows) {
+    const int w0 = (row / 16) * WPR, lr = row % 16;
     float mstar = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < WARPS; ++w) mstar = fmaxf(mstar, sm_m[w * 16 + row]);
+    for (int w = 0; w < WPR; ++w) mstar = fmaxf(mstar, sm_m[(w0 + w) * 16 + lr]);
     const float mref = mstar == -INFINITY ? 0.f : mstar;
-    float wsum = 0.f, wt[WARPS];
+    float wsum = 0.f, wt[WPR];
 #pragma unroll
-    for (int w = 0; w < WARPS; ++w) {
-      const float mw = sm_m[w * 16 + row];
+    for (int w = 0; w < WPR; ++w) {
+      const float mw = sm_m[(w0 + w) * 16 + lr];
       wt[w] = mw == -INFINITY ? 0.f : ex2(mw - mref);
-      wsum += wt[w] * sm_l[w * 16 + row];
+      wsum += wt[w] * sm_l[(w0 + w) * 16 + lr];
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;  // an empty split: O 0, LSE -inf
     const int qpos = row / g, hq = kvh * g + row % g;
@@ -453,7 +480,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < PER; ++i) {
       float acc = 0.f;
 #pragma unroll
-      for (int w = 0; w < WARPS; ++w) acc += wt[w] * sm_o[(w * 16 + row) * D + chb + i];
+      for (int w = 0; w < WPR; ++w) acc += wt[w] * sm_o[((w0 + w) * 16 + lr) * D + chb + i];
       p.o_part[prow * D + chb + i] = acc * inv;
     }
     if (chb == 0) p.lse_part[prow] = wsum > 0.f ? (mref + __log2f(wsum)) * LN2 : -INFINITY;
@@ -499,12 +526,12 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const float* __r
   if (lane == 0) lse[row] = lse_row;
 }
 
-template <int D>
+template <int D, int RT>
 cudaError_t launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
   using L = DecLayout<D>;
-  auto kern = a.block_table == nullptr ? fa_decode_split_kernel<D, false, false>
-               : a.head_groups ? fa_decode_split_kernel<D, true, true>
-                               : fa_decode_split_kernel<D, true, false>;
+  auto kern = a.block_table == nullptr ? fa_decode_split_kernel<D, false, false, RT>
+               : a.head_groups ? fa_decode_split_kernel<D, true, true, 1>
+                               : fa_decode_split_kernel<D, true, false, RT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   DecParams p;
@@ -538,8 +565,15 @@ cudaError_t launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
 
 }  // namespace
 
+// Packed rows Hq/Hkv * Nq in 16-row tiles: 1, 2 or 4 (head groups: 1).
+int decode_row_tiles(const Dims& d) { return cdiv((d.Hq / d.Hkv) * d.Nq, 16); }
+
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t st) {
-  return a.d == 64 ? launch_decode_t<64>(a, st) : launch_decode_t<128>(a, st);
+  const int rt = decode_row_tiles(a.dims);
+  if (rt > MAX_ROW_TILES || (a.head_groups && rt != 1)) return cudaErrorInvalidValue;
+  if (a.d == 64)
+    return rt == 1 ? launch_decode_t<64, 1>(a, st) : rt == 2 ? launch_decode_t<64, 2>(a, st) : launch_decode_t<64, 4>(a, st);
+  return rt == 1 ? launch_decode_t<128, 1>(a, st) : rt == 2 ? launch_decode_t<128, 2>(a, st) : launch_decode_t<128, 4>(a, st);
 }
 
 }  // namespace fa

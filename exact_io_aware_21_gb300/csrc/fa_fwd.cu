@@ -16,6 +16,9 @@
 //               O_t += P_t V_j with tcgen05.mma, accumulators in TMEM.
 //   warps 4-7   softmax for query tile 0 of the unit (thread = row = TMEM lane)
 //   warps 8-11  softmax for query tile 1
+// Each softmax warp also writes its rows' output: O / l in 32-column boxes staged
+// in shared memory and stored by the copy engine (TMA), so the warp only fills a
+// 2 KB buffer per box and can start the next unit while the stores drain.
 // The two query tiles share every K/V stage and ping-pong on the tensor core:
 // while one warpgroup exponentiates S_0, the tensor core computes S_1 or P_0 V.
 // TMEM (512 columns): S_0 [0,128) S_1 [128,256) O_0 [256,256+d) O_1 [256+d,256+2d);
@@ -74,12 +77,14 @@ struct FwdLayout {
   static constexpr int NBAR = 4 + 2 + 2 * NG + 8 + (SP ? 2 : 0);
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
-  static constexpr int OFF_SCR = (OFF_TMEM + 16 + 127) / 128 * 128;  // row-store scratch, one per softmax warp
+  static constexpr int OFF_SCR = (OFF_TMEM + 16 + 1023) / 1024 * 1024;  // output staging, one per softmax warp
+  // two 2 KB boxes per warp for TMA stores (block-sparse: the row-store scratch)
+  static constexpr int SCR = SP ? ROW_SCRATCH_BYTES : 4096;
   // block-sparse unit lists, one per unit slot: header (nu, n[2], first[2],
   // last[2]), per-key-tile flags of the two rows, then the union (act, kt)
   static constexpr int MAXL = 1024;  // key tiles (Nk <= 131072)
   static constexpr int LIST = SP ? (48 + 5 * MAXL + 127) / 128 * 128 : 0;
-  static constexpr int OFF_LIST = OFF_SCR + 8 * ROW_SCRATCH_BYTES;
+  static constexpr int OFF_LIST = OFF_SCR + 8 * SCR;
   static constexpr int BYTES = OFF_LIST + 2 * LIST;
   static constexpr int ALLOC = BYTES + 1024;
   static_assert(ALLOC <= 227 * 1024, "shared memory");
@@ -124,6 +129,7 @@ struct FwdParams {
   unsigned long long timeout_ns;
   int total_units;
   unsigned long long* trace;  // optional timestamps (see TRACE_UNIT0)
+  int tma_out;                // O (and its residual) leave through TMA stores (dense)
 };
 
 struct Bars {
@@ -218,7 +224,7 @@ __device__ __forceinline__ int fwd_total(const FwdParams& p) { return VL ? __ldg
 template <int D, int MASK, bool F8, bool VL, bool SP, int DG>
 __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, const CUtensorMap* tm_q,
                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, const FwdParams& p,
-                             const Ctl& ctl) {
+                             const FwdSched& sched, const Ctl& ctl) {
   using L = FwdLayout<D, F8, SP>;
   constexpr bool SKIP = VL || SP;  // units may have no work
   const int g = p.dims.Hq / p.dims.Hkv;
@@ -229,7 +235,13 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     if (!mbar_wait(&bar.unit_empty[slot], ((it >> 1) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
-    const int u = atomicAdd(p.counter, 1);
+    int u;
+    if (sched.on) {  // this CTA's list of the static schedule
+      const int k = sched.start[blockIdx.x] + it;
+      u = k < sched.start[blockIdx.x + 1] ? sched.ord[k] : total;
+    } else {
+      u = atomicAdd(p.counter, 1);
+    }
     if (DG == DG_TRACE && u < total) {
       unsigned long long* rec = p.trace + TRACE_UNIT0 + static_cast<int64_t>(u) * TRACE_UNIT_WORDS;
       rec[0] = globaltimer();
@@ -428,10 +440,34 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
   }
 }
 
+// One warp's 32 rows x 32 bf16 columns (w: this lane's row, packed in pairs) leave
+// through a TMA store of a 64-byte-swizzled box staged in `buf` (2 KB, 512-byte
+// aligned): 16-byte chunk q of row r sits at chunk q ^ ((r / 2) % 4).  Rows past the
+// tensor's end are dropped by the copy engine.  Each warp alternates two buffers;
+// before one is refilled, the store made from it two boxes ago must have read it
+// (at most one group, the previous box's, may still be reading).
+__device__ __forceinline__ void stage_box_store(const uint32_t (&w)[16], uint8_t* buf, const CUtensorMap* map,
+                                                int c0, int c1, int c2, int c3) {
+  const int lr = lane_id();
+  if (lr == 0) bulk_wait_read<1>();
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(buf + lr * 64 + ((q ^ ((lr >> 1) & 3)) << 4)) =
+        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lr == 0) {
+    tma_store_4d(map, buf, c0, c1, c2, c3);
+    bulk_commit();
+  }
+}
+
 // ------------------------------------------------------------------ softmax
 template <int D, int MASK, bool F8, bool VL, bool SP, int DG>
 __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* unit_slot, uint32_t tmem,
-                            const FwdParams& p, const Ctl& ctl, uint8_t* scratch) {
+                            const FwdParams& p, const Ctl& ctl, uint8_t* scratch, const CUtensorMap* tm_o,
+                            const CUtensorMap* tm_r) {
   using L = FwdLayout<D, F8, SP>;
   const int wq = (threadIdx.x >> 5) & 3;  // warp within the warpgroup = TMEM lane quarter
   const int r = wq * 32 + lane_id();      // row of the query tile
@@ -441,6 +477,7 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
   const float c = p.scale_log2;
   const Dims& s = p.dims;
   uint32_t sph = 0, active = 0;
+  uint32_t nbox = 0;  // output boxes staged so far (TMA stores alternate two buffers)
   const int total = fwd_total<VL>(p);
 
   for (int it = 0;; ++it) {
@@ -634,6 +671,20 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
         ov[i] = __fmul2_rn(f32x2(o[2 * i], o[2 * i + 1]), il2);
         w[i] = pack_bf16(ov[i].x, ov[i].y);
       }
+      if (!VL && !SP && p.tma_out) {  // TMA stores: this warp's 32 rows x 32 channels as one box
+        if (q0 >= nq_u) continue;     // every row of this warp lies past the end
+        stage_box_store(w, scratch + (nbox++ & 1) * 2048, tm_o, cc * 32, h, q0, b);
+        if (p.o_res.ptr != nullptr) {  // rounding residual: bf16(O - bf16(O))
+          uint32_t rz[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 hv = unpack_bf16(w[i]);
+            rz[i] = pack_bf16(ov[i].x - hv.x, ov[i].y - hv.y);
+          }
+          stage_box_store(rz, scratch + (nbox++ & 1) * 2048, tm_r, cc * 32, h, q0, b);
+        }
+        continue;
+      }
       store_rows32_bf16(w, scratch, o0 + cc * 32, p.o.sn, nq_u - q0);
       if (r0 != nullptr) {  // rounding residual: bf16(O - bf16(O))
         uint32_t rz[16];
@@ -753,7 +804,9 @@ __device__ void fwd_sparse_lists(uint8_t* smem, const Bars& bar, const int* unit
 template <int D, int MASK, bool F8, bool VL, bool SP, int DG>
 __global__ void __launch_bounds__(384, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p,
+                  const __grid_constant__ FwdSched sched, const __grid_constant__ CUtensorMap tm_o,
+                  const __grid_constant__ CUtensorMap tm_r) {
   using L = FwdLayout<D, F8, SP>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -797,6 +850,7 @@ __global__ void __launch_bounds__(384, 1)
   if (DG == DG_TRACE) {
     if (threadIdx.x == 0) {
       p.trace[4 * blockIdx.x] = globaltimer();
+      p.trace[4 * blockIdx.x + 1] = 0;
       p.trace[4 * blockIdx.x + 2] = smid();
       p.trace[4 * blockIdx.x + 3] = 0;
     }
@@ -804,22 +858,24 @@ __global__ void __launch_bounds__(384, 1)
   }
 
   if (warp == 0) {
-    if (lane_id() == 0) fwd_producer<D, MASK, F8, VL, SP, DG>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, ctl);
+    if (lane_id() == 0) fwd_producer<D, MASK, F8, VL, SP, DG>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, sched, ctl);
   } else if (warp == 1) {
     if (lane_id() == 0) fwd_mma<D, MASK, F8, VL, SP, DG>(smem, bar, unit_slot, tmem, p, ctl);
   } else if (SP && warp == 2) {
     fwd_sparse_lists<D, MASK>(smem, bar, unit_slot, p, ctl);
   } else if (warp >= 4) {
     fwd_softmax<D, MASK, F8, VL, SP, DG>((warp - 4) >> 2, smem, bar, unit_slot, tmem, p, ctl,
-                           smem + L::OFF_SCR + (warp - 4) * ROW_SCRATCH_BYTES);
+                                         smem + L::OFF_SCR + (warp - 4) * L::SCR, &tm_o, &tm_r);
+    if (!VL && !SP && p.tma_out && lane_id() == 0) bulk_wait<0>();  // the output stores have finished
   }
+  // the CTA's end: the last role to finish (each warp's lane 0 stamps its exit)
+  if (DG == DG_TRACE && lane_id() == 0) atomicMax(p.trace + 4 * blockIdx.x + 1, globaltimer());
   // Lanes 1-31 of the producer and MMA warps had no role: they wait here for their
-  // lane 0, so that every warp reaches the block barrier converged (a barrier met by
-  // part of a warp does not hold the rest) and TMEM is freed only after all its users.
+  // lane 0, so that every warp reaches the block barrier converged (the barrier is
+  // the aligned form, which assumes whole warps) and TMEM is freed after all its users.
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (DG == DG_TRACE && threadIdx.x == 0) p.trace[4 * blockIdx.x + 1] = globaltimer();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -836,6 +892,7 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   p.dims = a.dims;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.tau = a.tau;
+  p.tma_out = (!VL && !SP) ? a.tma_out : 0;
   p.sq = a.sq;
   p.sk = a.sk;
   p.sv = a.sv;
@@ -858,7 +915,11 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   p.total_units = fwd_units(a.dims);
   const int grid = imax(1, imin(p.total_units, a.num_sms));
   p.trace = DG == DG_TRACE ? a.trace : nullptr;  // the host sets a.trace only when the grid fits TRACE_MAX_CTAS
-  kern<<<grid, 384, L::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v, p);
+  FwdSched sched;
+  sched.on = 0;
+  sched.grid = grid;
+  if (a.sched != nullptr && a.sched->on && a.sched->grid == grid && !VL && !SP) sched = *a.sched;
+  kern<<<grid, 384, L::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v, p, sched, a.tm_o, a.tm_r);
   return cudaGetLastError();
 }
 

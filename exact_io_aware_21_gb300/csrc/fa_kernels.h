@@ -14,12 +14,32 @@ struct OutRows {           // a bf16 [B, N, H, d] tensor written row by row
   int64_t sb, sn, sh;
 };
 
+// Static schedule of the causal forward: the work units of each CTA, balanced on the
+// host (fa_sched.cu).  Units of a causal forward differ in cost by up to 20x, and the
+// longest-first order handed out dynamically still leaves the last CTAs idle for about
+// one small unit; a balanced assignment computed once per shape closes most of that.
+// on = 0: units are claimed dynamically (an atomic counter), longest first.
+constexpr int SCHED_MAX_CTAS = 160;
+constexpr int SCHED_MAX_UNITS = 2048;
+struct FwdSched {
+  int on;
+  int grid;                              // the launch's CTAs (the plan is for exactly this grid)
+  uint16_t start[SCHED_MAX_CTAS + 1];    // CTA c runs ord[start[c] .. start[c + 1]) in order
+  uint16_t ord[SCHED_MAX_UNITS];
+};
+// The balanced schedule of a dense causal forward on `grid` CTAs, or nullptr (not
+// causal, packed, too many units or CTAs).  Cached per shape; thread-safe.
+const FwdSched* causal_schedule(const Dims& s, int d, bool fp8, int grid);
+
 struct FwdLaunch {
   Dims dims;
   int d;
   float scale;
   float tau;  // conditional rescaling: the reference max moves only past this margin (log2 units)
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps, box 64 x 1 x 128 x 1, 128B swizzle
+  // output maps for TMA stores (dense bf16 forward): box 32 x 1 x 32 x 1, 64B swizzle
+  CUtensorMap tm_o, tm_r;
+  int tma_out;      // 1: O (and its residual) leave through tm_o / tm_r
   OutRows o;
   OutRows o_res;   // ptr == nullptr: residual not written
   float* lse;
@@ -40,6 +60,7 @@ struct FwdLaunch {
   int* plan;           // packed sequences: workspace for the device-side work plan
   unsigned long long* trace;  // timestamps (diag == DG_TRACE); layout below
   int diag;                   // DG_NONE, or a diagnostic instantiation (below)
+  const FwdSched* sched;      // static schedule (causal), or nullptr: dynamic claims
 };
 // Diagnostic instantiations of the dense bf16 d = 128 forward: DG_TRACE writes
 // timestamps into `trace`; DG_WITHHOLD (tests of the bounded waits) has one softmax
@@ -48,7 +69,8 @@ constexpr int DG_NONE = 0, DG_TRACE = 1, DG_WITHHOLD = 2;
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
 
 // Forward trace (diagnostics), %globaltimer nanoseconds.  Per CTA c < TRACE_MAX_CTAS:
-// [4c] start (after set-up), [4c+1] end, [4c+2] SM id, [4c+3] units run.  Per work
+// [4c] start (after set-up), [4c+1] end (its last role's exit), [4c+2] SM id,
+// [4c+3] units run.  Per work
 // unit u: [TRACE_UNIT0 + 16u + k], k = 0 claimed, 1 first product issued, 2 last
 // product issued, 3 output written (the later query tile), 4 CTA; per query tile t
 // of the unit (softmax warps): 5 + t its first S received, 7 + t its last P handed

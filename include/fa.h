@@ -265,8 +265,10 @@ int fa_bwd_part(int part, const fa_tensor_t* q, const fa_tensor_t* k, const fa_t
  * length into chunks processed in parallel, each producing (m_t, l_t, O_t),
  * merged by O = sum_t O_t e^{m_t-m} / sum_t l_t e^{m_t-m}; lecture slides
  * 57-60: the query heads sharing a K/V head (and the query positions) are
- * packed into one matrix tile.  Non-causal: every query row sees all Nk keys.
- *   q      [B, Nq, Hq, d]   in  (Nq small: Hq/Hkv * Nq <= 16)
+ * packed into the rows of matrix tiles.  Non-causal: every query row sees all
+ * Nk keys.
+ *   q      [B, Nq, Hq, d]   in  (Nq small: Hq/Hkv * Nq <= 64, packed into one,
+ *                               two or four 16-row tiles)
  *   kcache [B, Nk, Hkv, d]  in;  vcache likewise
  *   o      [B, Nq, Hq, d]   out (bf16);  lse [B, Hq, Nq] out (fp32)
  * num_splits: requested number of KV splits, 0 = choose from the GPU's SM
@@ -290,7 +292,7 @@ int fa_decode_partials_layout(const fa_shape_t* shape, int num_splits, size_t* l
  * b is physical page block_table[b * max_pages + i], and sequence b has its own
  * length seqlens_k[b].  Sequence b's logical key r is row r % page_size of page
  * block_table[b * max_pages + r / page_size].  Otherwise as fa_decode: the same
- * q, o, lse, shape (causal 0, Hq/Hkv * Nq <= 16) and num_splits; the
+ * q, o, lse, shape (causal 0, Hq/Hkv * Nq <= 64) and num_splits; the
  * workspace is fa_decode_paged_workspace_size(shape, num_splits, page_size)
  * bytes.
  *   kcache, vcache [num_pages, page_size, Hkv, d] bf16: stride_b = elements
@@ -304,8 +306,8 @@ int fa_decode_partials_layout(const fa_shape_t* shape, int num_splits, size_t* l
  *   page_size      16, 32, 64, or a multiple of 128
  * Each sequence is cut into whole 128-key tiles by its own length, with the
  * chunk rule of fa_decode applied to seqlens_k[b]; splits past its end
- * contribute nothing.  When Hkv is a multiple of 8 and page_size a multiple
- * of 16, one CTA serves 8 K/V heads over 16-key page slices (the copy engine
+ * contribute nothing.  When Hkv is a multiple of 8, page_size a multiple of
+ * 16 and Hq/Hkv * Nq <= 16, one CTA serves 8 K/V heads over 16-key page slices (the copy engine
  * then moves 16 KB boxes instead of one 2 KB box per page and head): the
  * splits are whole 16-key slices, chunk = ceil(ceil(len/16)/S)*16, and S is
  * chosen for that grid when num_splits is 0.  Keys past a sequence's end are never weighted, whatever
@@ -376,10 +378,11 @@ void fa_set_wait_timeout_ns(unsigned long long ns);
  * instantiation of the forward kernel in which one softmax warp of the CTA
  * that runs work unit 0 skips its first hand-off of P (one software mbarrier
  * arrive; no copy and no tensor-core operation is touched).  The tensor-core
- * issuer of that CTA then
- * waits until the wait budget (fa_set_wait_timeout_ns) runs out, records
- * FA_STATUS_TIMEOUT_MMA, and every role of the CTA leaves early: copies in
- * flight land, TMEM is freed, and the units it held are not written.
+ * issuer of that CTA then waits for it, and its producer for a stage the issuer
+ * never frees; the first of those waits to exceed the budget
+ * (fa_set_wait_timeout_ns) records its FA_STATUS_TIMEOUT_* bit, and every role
+ * of the CTA leaves early: copies in flight land, TMEM is freed, and the units
+ * it held are not written.
  * fa_get_device_status then returns FA_ERR_TIMEOUT.  One-shot: later calls run
  * the normal kernels.  Not thread-safe; for tests. */
 void fa_test_withhold_arrive(void);
@@ -389,8 +392,9 @@ void fa_test_withhold_arrive(void);
  * (device memory, 8-byte aligned), every later fa_fwd call with d = 128 (dense
  * tensors; not the packed, block-sparse or FP8 calls) runs an instantiation of
  * the kernel that also writes %globaltimer nanoseconds into it:
- *   per CTA c < 1024:  buf[4c] start (after set-up), buf[4c+1] end, buf[4c+2]
- *                      SM id, buf[4c+3] work units it ran;
+ *   per CTA c < 1024:  buf[4c] start (after set-up), buf[4c+1] end (the last
+ *                      of its warps to leave its role), buf[4c+2] SM id,
+ *                      buf[4c+3] work units it ran;
  *   per work unit u:   buf[4096 + 16u + k], k = 0 claimed, 1 first product
  *                      issued, 2 last product issued, 3 output written, 4 CTA;
  *                      per query tile t = 0, 1 of the unit: 5 + t its first S
@@ -422,6 +426,16 @@ int fa_dkdv_num_units(const fa_shape_t* shape);
 int fa_dkdv_unit(const fa_shape_t* shape, int index, int* b, int* kvh, int* kv_tile);
 int fa_dq_num_units(const fa_shape_t* shape);
 int fa_dq_unit(const fa_shape_t* shape, int index, int* b, int* h, int* q_tile);
+/* The static schedule of a causal bf16 forward on `grid` CTAs (the launch uses
+ * grid = min(units, SMs)): CTA c runs units ord[start[c] .. start[c+1]) in that
+ * order.  A causal unit's cost grows with its query tiles, so instead of handing
+ * units out longest first from a counter, the host assigns them once per shape:
+ * longest first onto the least loaded CTA, then moves and swaps that lower the
+ * largest load (cost = the unit's 128 x 128 x d products plus a fixed cost per
+ * unit measured on GB300).  start: grid + 1 ints, ord: fa_fwd_num_units ints.
+ * FA_ERR_INVALID when the forward does not use one (not causal, more than 2048
+ * units or 160 CTAs); it then claims units from a counter, longest first. */
+int fa_fwd_schedule(const fa_shape_t* shape, int grid, int* start, int* ord);
 /* Key range [start, end) of decode split s. */
 int fa_decode_split_range(const fa_shape_t* shape, int num_splits, int s, int* start, int* end);
 

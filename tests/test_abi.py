@@ -156,8 +156,8 @@ def test_misaligned_and_workspace_errors(lib):
     # bwd_part: unknown part
     assert lib.fa_bwd_part(3, tens(), tens(), tens(), tens(), FAKE, None, tens(), tens(), tens(), tens(), s, FAKE,
                            1 << 20, None) == 1
-    # decode: causal and too many packed rows are rejected
-    sd = shape(1, 32, 1, 1, 100, 64)
+    # decode: more than 64 packed rows (four 16-row tiles) are rejected
+    sd = shape(1, 80, 1, 1, 100, 64)
     assert lib.fa_decode(tens(), tens(), tens(), tens(), FAKE, ctypes.byref(sd), 1, FAKE, 1 << 30, None) == 1
 
 
@@ -310,3 +310,50 @@ def test_paged_decode_workspace_covers_its_splits(lib):
     assert size(s2, 0, 16) == lib.fa_decode_workspace_size(s2, 0)  # per-head kernel
     assert size(s8, 3, 48) == lib.fa_decode_workspace_size(s8, 3)  # pages not of whole 16-row slices
     assert size(S(1, 8, 8, 1, 0), 0, 16) == 0                      # invalid shape
+
+
+def _pair_products(N, p):
+    """Tensor-core products of causal forward unit p: two per key tile visited by each of
+    its query tiles (S and P V), counted from the causal tile classes."""
+    nt = P.cdiv(N, 128)
+    n = 0
+    for t in (2 * p, 2 * p + 1):
+        if t < nt:
+            n += sum(1 for j in range(nt)
+                     if P.causal_tile_class(t * 128, min(N, t * 128 + 128), j * 128, min(N, j * 128 + 128)) != P.SKIP)
+    return 2 * n
+
+
+@pytest.mark.parametrize("B,Hq,N,d,grid", [(2, 16, 4096, 128, 152), (1, 32, 8192, 128, 152), (2, 4, 1000, 128, 16),
+                                           (1, 6, 1100, 64, 24), (3, 5, 3000, 64, 152)])
+def test_fwd_schedule_is_a_balanced_partition(lib, B, Hq, N, d, grid):
+    """The static schedule of a causal forward runs every unit exactly once, each CTA's
+    units longest first, and its largest CTA load (products plus a fixed 16 x 128 / d per
+    unit) is no worse than handing the units out longest first."""
+    s = S(B, Hq, Hq, N, N, d=d, causal=True)
+    n = lib.fa_fwd_num_units(s)
+    grid = min(grid, n)
+    start = (ctypes.c_int * (grid + 1))()
+    ord_ = (ctypes.c_int * n)()
+    assert lib.fa_fwd_schedule(s, grid, start, ord_) == 0
+    st, od = list(start), list(ord_)
+    assert st[0] == 0 and st[-1] == n and all(a <= b for a, b in zip(st, st[1:]))
+    assert sorted(od) == list(range(n))
+    cost = []
+    for u in range(n):
+        b, h, p = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        assert lib.fa_fwd_unit(s, u, ctypes.byref(b), ctypes.byref(h), ctypes.byref(p)) == 0
+        cost.append(_pair_products(N, p.value) + 16 * 128 // d)
+    loads = []
+    for c in range(grid):
+        mine = [cost[u] for u in od[st[c]:st[c + 1]]]
+        assert mine == sorted(mine, reverse=True)
+        loads.append(sum(mine))
+    assert max(loads) <= max(P.greedy_loads(cost, grid, True))
+    assert max(loads) >= sum(cost) / grid
+
+
+def test_fwd_schedule_only_for_causal(lib):
+    start = (ctypes.c_int * 153)()
+    ord_ = (ctypes.c_int * 4096)()
+    assert lib.fa_fwd_schedule(S(2, 16, 16, 4096, 4096), 152, start, ord_) == 1

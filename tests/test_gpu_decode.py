@@ -52,6 +52,12 @@ CASES = [
     (1, 16, 1, 1, 300, 128, 1),    # 16 heads on one K/V head
     (1, 4, 1, 3, 4096, 128, 0),    # automatic split count
     (1, 1, 1, 1, 1, 128, 1),
+    # more than 16 packed rows: two or four 16-row tiles per CTA
+    (2, 8, 1, 4, 3000, 128, 4),    # 32 rows
+    (1, 16, 2, 4, 1500, 128, 0),   # 32 rows, automatic splits
+    (2, 16, 1, 4, 2000, 128, 3),   # 64 rows
+    (1, 8, 1, 5, 777, 64, 2),      # 40 rows (a partly empty fourth tile), d = 64
+    (1, 4, 4, 9, 300, 64, 1),      # 36 rows of 4 heads x 9 positions, ragged keys
 ]
 
 
@@ -87,6 +93,32 @@ def test_split_boundaries_bit_exact(Nk, S):
     got = np.rint(np.exp(f64(lse_p))).astype(np.int64)
     assert np.array_equal(got, np.broadcast_to(np.array(lengths), got.shape))
     assert np.array_equal(np.rint(np.exp(f64(lse))).astype(np.int64), np.full((B, Hq, 1), Nk))
+
+
+def test_more_than_64_packed_rows_is_rejected():
+    s = fa.binding.shape(1, 16, 1, 5, 1000, 128)   # 80 packed rows
+    q = torch.zeros(1, 5, 16, 128, dtype=torch.bfloat16, device=DEV)
+    kv = torch.zeros(1, 1000, 1, 128, dtype=torch.bfloat16, device=DEV)
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 16, 5, dtype=torch.float32, device=DEV)
+    ws = torch.zeros(fa.library().fa_decode_workspace_size(ctypes.byref(s), 2), dtype=torch.uint8, device=DEV)
+    with pytest.raises(fa.binding.FAError) as e:
+        fa.binding.fa_decode(q, kv, kv, o, lse, s, 2, ws)
+    assert e.value.code == 1
+
+
+@pytest.mark.slow
+def test_speculative_decode_64_rows_sampled():
+    """Grouped heads x query positions = 64 packed rows (8 heads per K/V head, 8 positions)
+    against a long cache: four 16-row tiles per CTA."""
+    w = inputs.Workload("spec", 2, 32, 4, 8, 65536, 128, False, decode=True, seed=5)
+    x = inputs.make(w, device=DEV, with_do=False)
+    o, lse, _, _, _ = run_decode(x["q"], x["k"], x["v"], 0)
+    for b, kvh in [(0, 0), (1, 3)]:
+        hs = slice(kvh * 8, (kvh + 1) * 8)
+        o_ref, lse_ref = A.attention_forward(x["q"][b:b + 1, :, hs].cpu(), x["k"][b:b + 1, :, kvh:kvh + 1].cpu(),
+                                             x["v"][b:b + 1, :, kvh:kvh + 1].cpu(), w.scale)
+        assert_fwd(o[b:b + 1, :, hs], lse[b:b + 1, hs], o_ref, lse_ref, f"64 rows b{b} kvh{kvh}")
 
 
 @pytest.mark.slow

@@ -62,6 +62,11 @@ CASES = [
     (3, 8, 8, 1, [17, 1, 640], 128, 16, 0),
     (1, 32, 16, 1, [2049], 128, 256, 5),         # two head groups, pages of two tiles
     (2, 64, 16, 4, [700, 1500], 128, 32, 40),    # 16 packed rows, more splits than needed
+    # more than 16 packed rows: the per-head kernel with two or four 16-row tiles
+    (2, 16, 2, 4, [900, 2500], 128, 16, 0),      # 32 rows, pages of 16
+    (2, 32, 8, 8, [300, 1200], 128, 16, 0),      # 32 rows with Hkv = 8 (no head groups past 16 rows)
+    (1, 16, 2, 8, [4096], 64, 64, 3),            # 64 rows, d = 64
+    (2, 8, 1, 6, [129, 2000], 128, 256, 0),      # 48 rows, pages of two tiles
 ]
 
 

@@ -42,7 +42,10 @@ of head (0, 0), decode on one (batch, K/V head)).  The window leg is reported be
 the (query, key) pairs inside the window, and the FP8 leg with the forward's
 count (its roofline is FP8's: twice the measured bf16 peak, the nominal ratio of
 the two tensor rates).  Decode legs report KV-read GB/s.  L2
-is flushed (256 MiB write) before every launch group, outside its events.
+is flushed (256 MiB write) before every launch group, outside its events, and a
+short spin kernel after the flush holds the stream while the host enqueues the
+start event and the group's launches, so that the events bracket device work and
+not the host's launch latency (the blocking-kernel method of NVIDIA's nvbench).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --profile-case WORKLOAD   # two fwd+bwd passes, for ncu captures
@@ -93,6 +96,7 @@ WORKLOAD = (" + ".join(TRAIN) + " (fwd+bwd); " + " + ".join(DECODE) + " (decode)
 METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
+HOLD_CYCLES = 200_000  # the spin kernel before each timed group: about 0.1 ms at 2 GHz
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -384,6 +388,7 @@ def bench_config(world):
         "workload": WORKLOAD,
         "value_counts": "fwd+bwd FLOPs of the training workloads (" + ", ".join(TRAIN) + ") / their device time",
         "l2": "flushed (256 MiB write) before every launch group, outside its events",
+        "launch_latency": "hidden: a 0.1 ms spin kernel holds the stream while each group is enqueued",
         "residual": "O's optional rounding residual is written (and read by the backward) for the outlier "
                     "workload only, where it takes dQ from 4.2e-2 to 1.3e-2; on the N(0,1) workloads dQ is "
                     "2.5e-3 with or without it (the *_with_residual leg times the forward with it)",
@@ -422,8 +427,8 @@ class Leg:
         self.ms = {k: 0.0 for k, _ in fns}
 
 
-KERNELS_PER_CALL = {"fwd_bs": 1, "bwd_bs": 5, "fwd": 1, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
-                    "quant_v": 2, "fwd_fp8": 1, "fwd_varlen": 1, "bwd_varlen": 3}
+KERNELS_PER_CALL = {"fwd_bs": 2, "bwd_bs": 5, "fwd": 2, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
+                    "quant_v": 2, "fwd_fp8": 2, "fwd_varlen": 3, "bwd_varlen": 3}
 
 
 def kernel_flops(part, w):
@@ -785,6 +790,7 @@ def run_ours(args):
         for leg in legs:
             for part, fn in leg.fns:
                 flush.fill_(1)
+                torch.cuda._sleep(HOLD_CYCLES)
                 if record is None:
                     fn()
                     continue

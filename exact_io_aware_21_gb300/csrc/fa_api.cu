@@ -130,14 +130,14 @@ int make_map_u8(CUtensorMap* m, const void* ptr, int B, int N, int H, int d, int
 // for the head-group decode: boxes of 64 channels x 16 rows x 8 heads, which land
 // in shared memory as 128 rows of 128 bytes, head-major (16 rows per head).
 int make_map_heads(CUtensorMap* m, const void* ptr, int pages, int page_size, int H, int d, int64_t sb, int64_t sn,
-                   int64_t sh) {
+                   int64_t sh, int box_rows, int box_heads) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return FA_ERR_CUDA;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(pages)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(sn) * 2, static_cast<cuuint64_t>(sh) * 2,
                            static_cast<cuuint64_t>(sb) * 2};
-  cuuint32_t box[4] = {64, 16, static_cast<cuuint32_t>(DECODE_HEAD_GROUP), 1};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(box_heads), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -234,17 +234,24 @@ int decode_splits_resolved(const fa_shape_t* s, int requested, int sms) {
   return decode_nsplits(s->Nk, S);
 }
 
-// The head-group paged decode: does it apply, and its splits per sequence.  The
-// same cost model over 16-key slices, with B * Hkv / 8 CTAs per split.
-bool decode_head_groups(const fa_shape_t* s, int page_size) {
-  return s->Hkv % DECODE_HEAD_GROUP == 0 && page_size % 16 == 0 && (s->Hq / s->Hkv) * s->Nq <= 16;
+// The head-group paged decode: K/V heads per CTA (0: the per-head kernel).  Eight
+// when Hkv is a multiple of 8 and pages are whole 16-row slices; four or two when
+// pages hold 16, 32 or 64 rows (with pages of whole tiles the per-head kernel's
+// boxes are already 16 KB).  One 16-row tile of packed rows per head.
+int decode_head_group(const fa_shape_t* s, int page_size) {
+  if ((s->Hq / s->Hkv) * s->Nq > 16 || page_size % 16 != 0) return 0;
+  if (s->Hkv % DECODE_HEAD_GROUP == 0) return DECODE_HEAD_GROUP;
+  if (page_size >= TILE) return 0;
+  return s->Hkv % 4 == 0 ? 4 : s->Hkv % 2 == 0 ? 2 : 0;
 }
 
-int decode_splits_hg(const fa_shape_t* s, int requested, int sms) {
-  const int slices = cdiv(s->Nk, 16);
+// Its splits per sequence: the same cost model over stages of 128 / hg keys, with
+// B * Hkv / hg CTAs per split.
+int decode_splits_hg(const fa_shape_t* s, int requested, int sms, int hg) {
+  const int slices = cdiv(s->Nk, TILE / hg);
   int S = requested;
   if (S <= 0) {
-    const int units = s->B * (s->Hkv / DECODE_HEAD_GROUP);
+    const int units = s->B * (s->Hkv / hg);
     int best = 1;
     double best_cost = 1e30;
     for (int c = 1; c <= 1024 && c <= slices; ++c) {
@@ -473,8 +480,9 @@ int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, c
   a.counter = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_COUNTER_OFFSET);
   a.timeout_ns = g_timeout_ns;
   a.num_sms = sms;
-  if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
-  cudaError_t e = launch_fwd(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_header_clear(ws, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, FA_ERR_LAUNCH);
+  e = launch_fwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
 }
 
@@ -589,8 +597,9 @@ int fa_fwd_fp8(const fa_tensor_t* q8, const fa_tensor_t* k8, const fa_tensor_t* 
   a.timeout_ns = g_timeout_ns;
   a.num_sms = sms;
   a.sched = causal_schedule(a.dims, s->d, true, imax(1, imin(fwd_units(a.dims), sms)));
-  if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
-  cudaError_t e = launch_fwd(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_header_clear(ws, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, FA_ERR_LAUNCH);
+  e = launch_fwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e, FA_ERR_LAUNCH);
 }
 
@@ -793,8 +802,8 @@ size_t fa_decode_workspace_size(const fa_shape_t* s, int num_splits) {
 
 // The paged decode's split count: the head-group grid's where it applies.
 static int paged_splits(const fa_shape_t* s, int num_splits, int page_size, int sms) {
-  return decode_head_groups(s, page_size) ? decode_splits_hg(s, num_splits, sms)
-                                          : decode_splits_resolved(s, num_splits, sms);
+  const int hg = decode_head_group(s, page_size);
+  return hg ? decode_splits_hg(s, num_splits, sms, hg) : decode_splits_resolved(s, num_splits, sms);
 }
 
 size_t fa_decode_paged_workspace_size(const fa_shape_t* s, int num_splits, int page_size) {
@@ -868,12 +877,13 @@ int fa_decode_paged(const fa_tensor_t* q, const fa_tensor_t* kc, const fa_tensor
   a.dims = dims_of(s);
   a.d = s->d;
   a.scale = s->scale;
-  a.head_groups = decode_head_groups(s, page_size) ? 1 : 0;
-  if (a.head_groups) {
+  a.head_group = decode_head_group(s, page_size);
+  if (a.head_group) {
+    const int rb = imin(page_size, TILE / a.head_group);  // box rows: a stage's keys, or a whole page
     if ((rc = make_map_heads(&a.tm_k, kc->ptr, num_pages, page_size, s->Hkv, s->d, kc->stride_b, kc->stride_n,
-                             kc->stride_h)) ||
+                             kc->stride_h, rb, a.head_group)) ||
         (rc = make_map_heads(&a.tm_v, vc->ptr, num_pages, page_size, s->Hkv, s->d, vc->stride_b, vc->stride_n,
-                             vc->stride_h)))
+                             vc->stride_h, rb, a.head_group)))
       return rc;
   } else {
     const int box_rows = small ? page_size : TILE;

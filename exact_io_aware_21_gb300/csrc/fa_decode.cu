@@ -37,13 +37,16 @@
 //
 // Head groups (HG).  A page holds all K/V heads of its rows side by side, so
 // with small pages the per-head kernel needs eight 16-row boxes per 128-key
-// tile and the copy engine's per-box cost, not HBM, sets the pace.  When Hkv
-// is a multiple of 8 and pages are whole 16-row slices, one CTA serves 8 K/V
-// heads instead: a stage is one 16-key slice of a page for all 8 heads (one
-// box of 16 rows x 8 heads x 64 channels per half of d, i.e. four boxes of
-// 16 KB for K and V), laid out exactly as a 128-key tile of one head, and
-// compute warp w works on head 8 g + w.  Each warp keeps its own softmax
-// state and writes its own partial; there is no merge across warps.
+// tile and the copy engine's per-box cost, not HBM, sets the pace.  With HG =
+// 8, 4 or 2 heads per CTA (Hkv a multiple of 8 and pages of whole 16-row
+// slices; or Hkv a multiple of 4 or 2 and pages of 16-64 rows) one CTA serves
+// HG K/V heads instead: a stage holds 128 / HG keys of all HG heads, loaded as
+// boxes of rb = min(page, 128 / HG) rows x HG heads x 64 channels (lines
+// head-major inside a box), so the stage has the size and the swizzle of a
+// 128-key tile of one head.  Compute warp w works on head w % HG and on the
+// 16-key slice w / HG of every stage, with its own softmax state; with HG = 8
+// each warp's state is its head's partial, with HG = 4 or 2 the 2 or 4 warps of
+// a head merge through shared memory as the per-head kernel's do.
 #include <math.h>
 
 #include "fa_kernels.h"
@@ -53,9 +56,9 @@ namespace fa {
 namespace {
 
 constexpr float LN2 = 0.69314718055994530942f;
-constexpr int WARPS = 8;              // compute warps (HG: one head each)
+constexpr int WARPS = 8;              // compute warps
 constexpr int MAX_ROW_TILES = 4;      // packed rows Hq/Hkv * Nq <= 64
-static_assert(WARPS == DECODE_HEAD_GROUP, "a head group is one head per compute warp");
+static_assert(WARPS == DECODE_HEAD_GROUP, "the largest head group is one head per compute warp");
 constexpr int THREADS = 32 * (WARPS + 1);
 
 template <int D>
@@ -117,23 +120,29 @@ __device__ __forceinline__ uint32_t swz(int key, int ch) {
   return (ch >> 6) * (TILE * 128) + key * 128 + ((((ch & 63) >> 3) ^ (key & 7)) << 4) + ((ch & 7) << 1);
 }
 
-template <int D, bool PAGED, bool HG, int RT>
+template <int D, bool PAGED, int HGK, int RT>
 __global__ void __launch_bounds__(THREADS, 1)
     fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                            const DecParams p) {
   using L = DecLayout<D>;
+  constexpr bool HG = HGK > 0;  // HGK K/V heads per CTA, or one head (0)
   static_assert(!HG || PAGED, "head groups are a paged layout");
   static_assert(!HG || RT == 1, "a head group has one 16-row tile per head");
+  static_assert(HGK == 0 || HGK == 2 || HGK == 4 || HGK == WARPS, "heads per CTA");
   constexpr int WPR = WARPS / RT;  // warps per 16-row tile
   constexpr int KW = TILE / WPR;   // keys of each 128-key tile per warp (16 RT), in RT chunks of 16
-  constexpr int KT = HG ? 16 : TILE;  // keys per stage: a page slice (all 8 heads) or a tile of one head
+  constexpr int SPS = HG ? WARPS / HGK : 1;  // (HG) 16-key slices per stage = warps per head
+  constexpr int KT = HG ? 16 * SPS : TILE;   // keys per stage (of each head of the CTA)
+  constexpr bool MERGE = !HG || SPS > 1;     // several warps hold parts of one row
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* empty = full + L::STAGES;
   const int warp = threadIdx.x >> 5, lane = lane_id();
   const int split = blockIdx.x, b = blockIdx.z;
-  const int kvh = HG ? blockIdx.y * WARPS + (warp < WARPS ? warp : 0) : blockIdx.y;  // this warp's K/V head
+  const int hw = HG && warp < WARPS ? warp % HGK : 0;  // (HG) this warp's head in the group
+  const int js = HG && warp < WARPS ? warp / HGK : 0;  // (HG) this warp's 16-key slice of each stage
+  const int kvh = HG ? blockIdx.y * HGK + hw : blockIdx.y;  // this warp's K/V head
   const Dims& s = p.dims;
   const int g = s.Hq / s.Hkv;
   const int rows = g * s.Nq;
@@ -147,6 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     chunk = cdiv(cdiv(len, KT), p.num_splits) * KT;
   }
+  const int rb = HG ? imin(p.page_size, KT) : 0;  // (HG) rows of a box: KT, or a whole page
   const int k0 = split * chunk;
   const int k1 = imin(len, k0 + chunk);
   const int ntiles = k1 > k0 ? cdiv(k1 - k0, KT) : 0;
@@ -164,41 +174,50 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == WARPS) {  // ---------------------------------------------- producer
     if (HG) {
-      // One lane: slice t is rows [r, r + 16) of one page (page_size is a multiple of
-      // 16), heads 8 blockIdx.y .. + 7; the next slice's page index is read one
-      // slice ahead.  Coordinates of the map: (channel, row, head, page).
-      if (lane == 0) {
-        const int64_t trow = static_cast<int64_t>(b) * p.max_pages;
-        auto page_of = [&](int t) {
-          if (t >= ntiles) return -1;
-          int pg = p.block_table[trow + (k0 + t * KT) / p.page_size];
-          if (pg < 0 || pg >= p.num_pages) {  // reads as zeros (out-of-range TMA box); reported
-            report(ctl, FA_STATUS_BAD_INPUT);
-            pg = p.num_pages;
-          }
-          return pg;
-        };
-        int issued = 0;
-        int next_page = page_of(0);
-        for (int t = 0; t < ntiles; ++t) {
-          const int st = t % L::STAGES;
-          const int page = next_page;
-          next_page = page_of(t + 1);
-          if (!mbar_wait(&empty[st], ((t / L::STAGES) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD)) break;
-          uint8_t* dst = smem + L::OFF_KV + st * 2 * L::TB;
-          const int row = (k0 + t * KT) % p.page_size;
-          mbar_arrive_expect_tx(&full[st], 2 * L::TB);
+      // Stage t: keys [k0 + t KT, + KT) of heads HGK blockIdx.y .. + HGK-1, as boxes of rb
+      // rows (a page's rows r .. r + rb - 1; rb divides the page) x HGK heads x 64
+      // channels; lane i reads the page of box i one stage ahead and loads it.  No box
+      // is loaded past the split's end, where the table need not be valid.
+      // Coordinates of the map: (channel, row, head, page).
+      const int64_t trow = static_cast<int64_t>(b) * p.max_pages;
+      auto page_of = [&](int t) {
+        const int key = k0 + t * KT + lane * rb;
+        if (t >= ntiles || lane * rb >= KT || key >= k1) return -1;
+        int pg = p.block_table[trow + key / p.page_size];
+        if (pg < 0 || pg >= p.num_pages) {  // reads as zeros (out-of-range TMA box); reported
+          report(ctl, FA_STATUS_BAD_INPUT);
+          pg = p.num_pages;
+        }
+        return pg;
+      };
+      int issued = 0;
+      int next_page = page_of(0);
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t % L::STAGES;
+        const int page = next_page;
+        next_page = page_of(t + 1);
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&empty[st], ((t / L::STAGES) & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_LOAD);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        const int kk = k0 + t * KT;
+        const int nbox = imin(KT / rb, cdiv(k1 - kk, rb));
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], 4 * nbox * rb * HGK * D);  // K and V boxes
+        __syncwarp();
+        if (lane < nbox) {
+          uint8_t* dst = smem + L::OFF_KV + st * 2 * L::TB + lane * rb * HGK * 128;
+          const int row = (kk + lane * rb) % p.page_size;
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
-            tma_load_4d(dst + c * (TILE * 128), &tm_k, &full[st], c * 64, row, blockIdx.y * WARPS, page);
-            tma_load_4d(dst + L::TB + c * (TILE * 128), &tm_v, &full[st], c * 64, row, blockIdx.y * WARPS, page);
+            tma_load_4d(dst + c * (TILE * 128), &tm_k, &full[st], c * 64, row, blockIdx.y * HGK, page);
+            tma_load_4d(dst + L::TB + c * (TILE * 128), &tm_v, &full[st], c * 64, row, blockIdx.y * HGK, page);
           }
-          ++issued;
         }
+        ++issued;
+      }
+      if (lane == 0)
         for (int t = imax(0, issued - L::STAGES); t < issued; ++t)
           mbar_wait(&full[t % L::STAGES], (t / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
-      }
-      return;  // the compute warps do not merge: no block-wide barrier follows
+      if (!MERGE) return;  // one warp per head: the compute warps do not merge, no block barrier follows
     } else if (!PAGED) {
       if (lane == 0) {
         int issued = 0;
@@ -308,9 +327,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     const uint32_t kb = smem_u32(smem + L::OFF_KV + st * 2 * L::TB);
     const uint32_t vb = kb + L::TB;
-    // this warp's rows of the stage: keys KW (warp % WPR) .. + KW-1 of the tile, or
-    // (HG) the slice's 16 keys of this warp's head
-    const int key_base = KW * (warp % WPR);
+    // this warp's lines of the stage: keys KW (warp % WPR) .. + KW-1 of the tile, or
+    // (HG) the 16 keys of slice js of head hw, inside box (16 js) / rb
+    const int key_base = HG ? (16 * js / rb) * rb * HGK + hw * rb + (16 * js) % rb : KW * (warp % WPR);
 
     // S = Q K^T for 16 rows x KW keys (2 RT n8 tiles)
     float sacc[2 * RT][4];
@@ -329,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mma_16816(sacc[2 * cq + 1], qa[ks], b10, b11);
       }
     // mask keys outside [k0, k1)
-    const int key0 = k0 + t * KT + (HG ? 0 : key_base);
+    const int key0 = k0 + t * KT + (HG ? 16 * js : key_base);
     float sv[2 * RT][4];
 #pragma unroll
     for (int nt = 0; nt < 2 * RT; ++nt)
@@ -413,7 +432,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
     l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
   }
-  if (HG) {  // one head per warp: its state is the split's (rows gq and gq + 8)
+  if (!MERGE) {  // one warp per head: its state is the split's (rows gq and gq + 8)
     if (!ok) return;
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
@@ -454,33 +473,39 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   __syncthreads();
   if (!ok) return;
-  // 256 threads: thread -> (row, channel range); row r's state is in the WPR warps
-  // of its 16-row tile, at their local row r % 16
-  const int tid = threadIdx.x;  // < 256
-  constexpr int PER = RT * 16 * D / 256;  // channels per thread
-  const int row = tid / (D / PER);
+  // 256 threads: thread -> (16-row group, local row, channel range).  A group is a
+  // 16-row tile of the packed rows (its state in the WPR warps of that tile) or
+  // (HG) one head (its state in warps head, head + HGK, ...), at local row lr.
+  constexpr int NW = HG ? SPS : WPR;         // warps holding parts of one row
+  constexpr int GROUPS = HG ? HGK : RT;
+  constexpr int PER = GROUPS * 16 * D / 256;  // channels per thread
+  const int tid = threadIdx.x;               // < 256
+  const int grow = tid / (D / PER);
+  const int grp = grow / 16, lr = grow % 16;
+  const int row = HG ? lr : grow;            // the packed row of the group's head
   const int chb = (tid % (D / PER)) * PER;
+  auto wid = [&](int w) { return HG ? grp + HGK * w : grp * WPR + w; };
   if (row < rows) {
-    const int w0 = (row / 16) * WPR, lr = row % 16;
     float mstar = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < WPR; ++w) mstar = fmaxf(mstar, sm_m[(w0 + w) * 16 + lr]);
+    for (int w = 0; w < NW; ++w) mstar = fmaxf(mstar, sm_m[wid(w) * 16 + lr]);
     const float mref = mstar == -INFINITY ? 0.f : mstar;
-    float wsum = 0.f, wt[WPR];
+    float wsum = 0.f, wt[NW];
 #pragma unroll
-    for (int w = 0; w < WPR; ++w) {
-      const float mw = sm_m[(w0 + w) * 16 + lr];
+    for (int w = 0; w < NW; ++w) {
+      const float mw = sm_m[wid(w) * 16 + lr];
       wt[w] = mw == -INFINITY ? 0.f : ex2(mw - mref);
-      wsum += wt[w] * sm_l[(w0 + w) * 16 + lr];
+      wsum += wt[w] * sm_l[wid(w) * 16 + lr];
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;  // an empty split: O 0, LSE -inf
-    const int qpos = row / g, hq = kvh * g + row % g;
+    const int head = HG ? blockIdx.y * HGK + grp : kvh;
+    const int qpos = row / g, hq = head * g + row % g;
     const int64_t prow = ((static_cast<int64_t>(b) * s.Hq + hq) * s.Nq + qpos) * p.num_splits + split;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       float acc = 0.f;
 #pragma unroll
-      for (int w = 0; w < WPR; ++w) acc += wt[w] * sm_o[((w0 + w) * 16 + lr) * D + chb + i];
+      for (int w = 0; w < NW; ++w) acc += wt[w] * sm_o[(wid(w) * 16 + lr) * D + chb + i];
       p.o_part[prow * D + chb + i] = acc * inv;
     }
     if (chb == 0) p.lse_part[prow] = wsum > 0.f ? (mref + __log2f(wsum)) * LN2 : -INFINITY;
@@ -529,9 +554,11 @@ __global__ void __launch_bounds__(128) fa_decode_combine_kernel(const float* __r
 template <int D, int RT>
 cudaError_t launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
   using L = DecLayout<D>;
-  auto kern = a.block_table == nullptr ? fa_decode_split_kernel<D, false, false, RT>
-               : a.head_groups ? fa_decode_split_kernel<D, true, true, 1>
-                               : fa_decode_split_kernel<D, true, false, RT>;
+  auto kern = a.block_table == nullptr ? fa_decode_split_kernel<D, false, 0, RT>
+               : a.head_group == 8   ? fa_decode_split_kernel<D, true, 8, 1>
+               : a.head_group == 4   ? fa_decode_split_kernel<D, true, 4, 1>
+               : a.head_group == 2   ? fa_decode_split_kernel<D, true, 2, 1>
+                                     : fa_decode_split_kernel<D, true, 0, RT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   DecParams p;
@@ -553,7 +580,7 @@ cudaError_t launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
   p.seqlens = a.seqlens;
   p.num_pages = a.num_pages;
   p.page_size = a.page_size;
-  dim3 grid(a.num_splits, a.head_groups ? a.dims.Hkv / WARPS : a.dims.Hkv, a.dims.B);
+  dim3 grid(a.num_splits, a.head_group ? a.dims.Hkv / a.head_group : a.dims.Hkv, a.dims.B);
   kern<<<grid, THREADS, L::ALLOC, st>>>(a.tm_k, a.tm_v, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -570,7 +597,10 @@ int decode_row_tiles(const Dims& d) { return cdiv((d.Hq / d.Hkv) * d.Nq, 16); }
 
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t st) {
   const int rt = decode_row_tiles(a.dims);
-  if (rt > MAX_ROW_TILES || (a.head_groups && rt != 1)) return cudaErrorInvalidValue;
+  if (rt > MAX_ROW_TILES) return cudaErrorInvalidValue;
+  if (a.head_group && (rt != 1 || a.block_table == nullptr || a.dims.Hkv % a.head_group != 0 ||
+                       (a.head_group != 2 && a.head_group != 4 && a.head_group != WARPS)))
+    return cudaErrorInvalidValue;
   if (a.d == 64)
     return rt == 1 ? launch_decode_t<64, 1>(a, st) : rt == 2 ? launch_decode_t<64, 2>(a, st) : launch_decode_t<64, 4>(a, st);
   return rt == 1 ? launch_decode_t<128, 1>(a, st) : rt == 2 ? launch_decode_t<128, 2>(a, st) : launch_decode_t<128, 4>(a, st);

@@ -847,6 +847,9 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the set-up above touches only this CTA's own memory; from here on the kernel
+  // reads the workspace header the previous kernel cleared, and the inputs
+  griddep_wait();
   if (DG == DG_TRACE) {
     if (threadIdx.x == 0) {
       p.trace[4 * blockIdx.x] = globaltimer();
@@ -919,11 +922,34 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   sched.on = 0;
   sched.grid = grid;
   if (a.sched != nullptr && a.sched->on && a.sched->grid == grid && !VL && !SP) sched = *a.sched;
-  kern<<<grid, 384, L::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v, p, sched, a.tm_o, a.tm_r);
-  return cudaGetLastError();
+  // launched with programmatic stream serialisation: the CTAs set up their barriers
+  // and TMEM while the header-clearing kernel before them still runs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(384);
+  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, p, sched, a.tm_o, a.tm_r);
+}
+
+// Zero a workspace header (status word, counters) and let the kernel after it
+// start its set-up at once.
+__global__ void __launch_bounds__(32) header_clear_kernel(uint4* h) {
+  griddep_launch_dependents();
+  if (threadIdx.x < FA_WS_HEADER_BYTES / 16) h[threadIdx.x] = make_uint4(0, 0, 0, 0);
 }
 
 }  // namespace
+
+cudaError_t launch_header_clear(void* ws, cudaStream_t st) {
+  header_clear_kernel<<<1, 32, 0, st>>>(static_cast<uint4*>(ws));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st) {
   const int m = mask_kind(a.dims);

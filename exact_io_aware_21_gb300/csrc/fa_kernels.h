@@ -66,6 +66,8 @@ struct FwdLaunch {
 // timestamps into `trace`; DG_WITHHOLD (tests of the bounded waits) has one softmax
 // warp of work unit 0 skip its first P hand-off, so that CTA's MMA issuer's wait runs out.
 constexpr int DG_NONE = 0, DG_TRACE = 1, DG_WITHHOLD = 2;
+// Zero a workspace header; a forward launched next may start its set-up meanwhile.
+cudaError_t launch_header_clear(void* ws, cudaStream_t st);
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t st);
 
 // Forward trace (diagnostics), %globaltimer nanoseconds.  Per CTA c < TRACE_MAX_CTAS:
@@ -127,11 +129,12 @@ struct DecodeLaunch {
   const int* seqlens;      // [B] keys of each sequence, 1..Nk
   int num_pages;
   int page_size;           // 16, 32, 64, or a multiple of 128
-  // paged, Hkv % 8 == 0, page_size % 16 == 0: one CTA per 8 K/V heads, 16-key page
-  // slices; tm_k / tm_v then map (channel, row, head, page) with 64 x 16 x 8 boxes
-  int head_groups;
+  // paged head groups: K/V heads per CTA (8, 4 or 2; 0 = one head per CTA).  A stage
+  // holds 128 / head_group keys of each head; tm_k / tm_v then map (channel, row,
+  // head, page) with boxes of 64 x min(page_size, 128 / head_group) x head_group
+  int head_group;
 };
-constexpr int DECODE_HEAD_GROUP = 8;
+constexpr int DECODE_HEAD_GROUP = 8;  // the largest head group
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t st);
 
 struct QuantLaunch {       // E4M3 codes of a bf16 [B, N, H, d] tensor

@@ -32,6 +32,16 @@ __device__ __forceinline__ uint32_t smid() {
   return r;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream still runs;
+// griddep_wait() holds the calling thread until that kernel has finished and its
+// writes are visible (a no-op for an ordinary launch).  griddep_launch_dependents()
+// lets the next such kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -116,6 +116,10 @@ typedef struct {
  *       rounding residual of O, i.e. bf16(O_fp32 - O).  O + o_residual carries
  *       about 16 significant bits; fa_bwd uses it for D (see there).
  * Needs fa_fwd_workspace_size(shape) bytes of workspace (16-byte aligned).
+ * Enqueues two kernels: one that clears the workspace header, then the forward,
+ * launched with programmatic stream serialisation so that its CTAs set up
+ * shared memory and TMEM while the first still runs (they touch global memory
+ * only after it has finished).  The forward calls below do the same.
  * ------------------------------------------------------------------------- */
 size_t fa_fwd_workspace_size(const fa_shape_t* shape);
 int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,

@@ -291,9 +291,10 @@ def test_block_sparse_plan_fits_its_bounds(lib):
 
 
 def test_paged_decode_workspace_covers_its_splits(lib):
-    """The paged decode's workspace: head-group shapes (Hkv % 8 == 0, pages of whole
-    16-row slices) size the partials for their own split count; the others match
-    the contiguous decode's."""
+    """The paged decode's workspace: head-group shapes (8 K/V heads per CTA when Hkv %
+    8 == 0 and pages are whole 16-row slices; 4 or 2 when pages hold 16-64 rows) size
+    the partials for their own split count, capped at one stage (128 / heads-per-CTA
+    keys) each; the others match the contiguous decode's."""
     size = lib.fa_decode_paged_workspace_size
     hdr = 256
 
@@ -307,7 +308,12 @@ def test_paged_decode_workspace_covers_its_splits(lib):
     assert size(s8, 5000, 16) == parts(8, 32, 1, 5000)
     assert size(S(1, 8, 8, 1, 1000), 100, 16) == parts(1, 8, 1, 63)  # capped at one 16-key slice each
     s2 = S(2, 8, 2, 4, 4096)
-    assert size(s2, 0, 16) == lib.fa_decode_workspace_size(s2, 0)  # per-head kernel
+    assert size(s2, 5, 16) == parts(2, 8, 4, 5)                    # two heads per CTA
+    assert size(S(1, 8, 2, 1, 1000), 100, 64) == parts(1, 8, 1, 16)  # capped at 64-key stages
+    assert size(S(1, 8, 4, 1, 1000), 100, 32) == parts(1, 8, 1, 32)  # four heads: 32-key stages
+    assert size(s2, 0, 128) == lib.fa_decode_workspace_size(s2, 0)  # pages of whole tiles: per-head kernel
+    s1 = S(2, 8, 1, 2, 4096)
+    assert size(s1, 0, 16) == lib.fa_decode_workspace_size(s1, 0)  # one K/V head: per-head kernel
     assert size(s8, 3, 48) == lib.fa_decode_workspace_size(s8, 3)  # pages not of whole 16-row slices
     assert size(S(1, 8, 8, 1, 0), 0, 16) == 0                      # invalid shape
 

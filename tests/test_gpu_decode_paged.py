@@ -6,8 +6,10 @@ reach the output.  Also: the key count recovered bit-exactly from LSE with
 Q = 0, equality with the contiguous decode for an identity layout, device-side
 reporting of bad lengths and page indices, and the full decode workload in
 pages of 16 keys with ragged lengths, on sampled heads.  Shapes with Hkv a
-multiple of 8 and pages of whole 16-row slices take the head-group kernel
-(one CTA per 8 K/V heads); the others the per-head kernel.
+multiple of 8 and pages of whole 16-row slices take the head-group kernel with
+one CTA per 8 K/V heads; with Hkv a multiple of 4 or 2 and pages of 16-64 rows,
+the same kernel with 4 or 2 heads per CTA (their warps merged per head); the
+others the per-head kernel.
 """
 
 import numpy as np
@@ -56,12 +58,18 @@ CASES = [
     (2, 16, 4, 4, [5000, 4097], 128, 256, 5),   # pages holding two tiles
     (1, 8, 8, 2, [128], 64, 128, 0),
     (4, 32, 8, 4, [300, 1, 2000, 777], 128, 32, 3),
-    (2, 4, 2, 1, [4500, 20], 128, 16, 9),       # more splits than the short sequence has tiles
+    (2, 4, 2, 1, [4500, 20], 128, 16, 9),       # more splits than the short sequence has stages
     # K/V heads in groups of 8 (one CTA per group, 16-key page slices)
     (2, 16, 8, 2, [1000, 333], 64, 16, 0),
     (3, 8, 8, 1, [17, 1, 640], 128, 16, 0),
     (1, 32, 16, 1, [2049], 128, 256, 5),         # two head groups, pages of two tiles
     (2, 64, 16, 4, [700, 1500], 128, 32, 40),    # 16 packed rows, more splits than needed
+    # 4 or 2 K/V heads per CTA (pages of 16-64 rows): 32- or 64-key stages, warps merged per head
+    (2, 16, 4, 2, [3000, 77], 128, 32, 0),       # four heads, page = stage
+    (1, 8, 4, 1, [2049], 64, 64, 3),             # four heads, two 32-row boxes per page
+    (3, 12, 6, 2, [100, 1, 1500], 128, 16, 0),   # Hkv = 6: three groups of two, four boxes a stage
+    (2, 4, 2, 8, [600, 1300], 64, 64, 2),        # two heads, 16 packed rows, page = stage
+    (2, 8, 4, 2, [5000, 333], 128, 16, 50),      # more splits than the short sequence has stages
     # more than 16 packed rows: the per-head kernel with two or four 16-row tiles
     (2, 16, 2, 4, [900, 2500], 128, 16, 0),      # 32 rows, pages of 16
     (2, 32, 8, 8, [300, 1200], 128, 16, 0),      # 32 rows with Hkv = 8 (no head groups past 16 rows)
@@ -82,7 +90,7 @@ def test_paged_decode_matches_oracle(B, Hq, Hkv, Nq, lens, d, page, S):
     assert_fwd(o, lse, o_ref, lse_ref, f"paged {B}x{Hq}/{Hkv}x{Nq} lens={lens} d={d} page={page} S={S}")
 
 
-@pytest.mark.parametrize("Hkv,page", [(2, 32), (8, 16)])
+@pytest.mark.parametrize("Hkv,page", [(2, 32), (8, 16), (4, 64), (1, 16)])
 def test_nan_in_unreferenced_rows_never_reaches_the_output(Hkv, page):
     B, Hq, Nq, d = 3, 8, 2, 128
     lens = [77, 1, 300]
@@ -96,7 +104,7 @@ def test_nan_in_unreferenced_rows_never_reaches_the_output(Hkv, page):
     assert_fwd(o, lse, o_ref, lse_ref, "NaN junk")
 
 
-@pytest.mark.parametrize("page,Hkv", [(16, 2), (64, 2), (128, 2), (16, 8)])
+@pytest.mark.parametrize("page,Hkv", [(16, 2), (64, 2), (128, 2), (16, 8), (32, 4)])
 def test_zero_query_counts_each_sequence_keys_exactly(page, Hkv):
     lens = [1, 127, 128, 129, 1000, 4095]
     B, Hq, Nq, d = len(lens), 2 * Hkv, 1, 64
@@ -121,7 +129,7 @@ def test_identity_layout_equals_contiguous_decode():
     assert torch.equal(o_p, o_c) and torch.equal(lse_p, lse_c)
 
 
-@pytest.mark.parametrize("Hq,Hkv,page", [(4, 1, 64), (8, 8, 16)])
+@pytest.mark.parametrize("Hq,Hkv,page", [(4, 1, 64), (8, 8, 16), (8, 2, 32)])
 def test_bad_lengths_and_pages_are_reported_not_faulted(Hq, Hkv, page):
     B, Nq, d, N = 3, 1, 64, 512
     x = inputs.shape_inputs(B, Hq, Hkv, Nq, N, d, seed=3, with_do=False)

@@ -428,7 +428,7 @@ class Leg:
 
 
 KERNELS_PER_CALL = {"fwd_bs": 2, "bwd_bs": 5, "fwd": 2, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
-                    "quant_v": 2, "fwd_fp8": 2, "fwd_varlen": 3, "bwd_varlen": 3}
+                    "quant_v": 2, "fwd_fp8": 2, "fwd_fp8_cr": 2, "fwd_varlen": 3, "bwd_varlen": 3}
 
 
 def kernel_flops(part, w):
@@ -589,13 +589,17 @@ def make_legs(device, seed):
               sv=torch.empty((w.B, w.Hkv), dtype=torch.float32, device=device),
               wsq=torch.zeros(lib.fa_quantize_fp8_workspace_size(w.B, w.Hq), dtype=torch.uint8, device=device),
               wsk=torch.zeros(lib.fa_quantize_fp8_workspace_size(w.B, w.Hkv), dtype=torch.uint8, device=device),
-              wsf=torch.zeros(lib.fa_fwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=device))
+              wsf=torch.zeros(lib.fa_fwd_workspace_size(ctypes.byref(s)), dtype=torch.uint8, device=device),
+              s_cr=B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal, None, RESCALE_THRESHOLD))
     state[FP8_NAME] = st
     fns = [("quant_q", lambda st=st: B.fa_quantize_fp8(st["x"]["q"], 128, st["signs"], st["q8"], st["sq"], st["wsq"])),
            ("quant_k", lambda st=st: B.fa_quantize_fp8(st["x"]["k"], 128, st["signs"], st["k8"], st["sk"], st["wsk"])),
            ("quant_v", lambda st=st: B.fa_quantize_fp8(st["x"]["v"], 0, None, st["v8"], st["sv"], st["wsk"])),
            ("fwd_fp8", lambda st=st: B.fa_fwd_fp8(st["q8"], st["k8"], st["v8"], st["sq"], st["sk"], st["sv"], st["o"],
-                                                  st["lse"], st["s"], st["wsf"]))]
+                                                  st["lse"], st["s"], st["wsf"])),
+           # the same forward with conditional rescaling (opt-in, threshold 8), reported beside it
+           ("fwd_fp8_cr", lambda st=st: B.fa_fwd_fp8(st["q8"], st["k8"], st["v8"], st["sq"], st["sk"], st["sv"],
+                                                     st["o"], st["lse"], st["s_cr"], st["wsf"]))]
     legs.append(Leg(FP8_NAME, "fp8", w, fns, fwd_flops(w)))
     return legs, state
 
@@ -888,6 +892,7 @@ def run_ours(args):
             qbytes = {k: l.w.B * n * h * l.w.d * (5 if k == "quant_v" else 3) for k, (h, n) in qb.items()}
             fp8_peak = FP8_TENSOR_RATIO * burst
             t = f / l.ms["fwd_fp8"] / 1e9
+            t_cr = f / l.ms["fwd_fp8_cr"] / 1e9
             legs_out[l.name] = {
                 "fwd_ms": r4(l.ms["fwd_fp8"]), "fwd_tflops": r4(t), "fwd_frac_of_fp8_peak": r4(t / fp8_peak),
                 "fp8_peak_tflops": r4(fp8_peak),
@@ -895,7 +900,12 @@ def run_ours(args):
                                    "4.5 / 2.25 PFLOP/s); no E4M3 peak is measured",
                 "quant_ms": {k: r4(l.ms[k]) for k in qb},
                 "quant_gbs": {k: r4(qbytes[k] / l.ms[k] / 1e6) for k in qb},
-                "fwd_plus_quant_tflops": r4(f / sum(l.ms.values()) / 1e9), "hadamard": True, "in_step": False}
+                "fwd_plus_quant_tflops": r4(f / (l.ms["fwd_fp8"] + sum(l.ms[k] for k in qb)) / 1e9),
+                "cond_rescale8": {"fwd_ms": r4(l.ms["fwd_fp8_cr"]), "fwd_tflops": r4(t_cr),
+                                  "fwd_frac_of_fp8_peak": r4(t_cr / fp8_peak),
+                                  "speedup_vs_exact_max": r4(l.ms["fwd_fp8"] / l.ms["fwd_fp8_cr"]),
+                                  "rescale_threshold": RESCALE_THRESHOLD},
+                "hadamard": True, "in_step": False}
         else:
             ms = l.ms["decode"]
             legs_out[l.name] = {"ms": r4(ms), "gbs": r4(l.work / ms / 1e6),

@@ -676,6 +676,14 @@ static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const
   a.dq = out_rows(dq, pk);
   a.dk = out_rows(dk, pk);
   a.dv = out_rows(dv, pk);
+  if (!pk && !sp) {  // dense: dK and dV leave through TMA stores
+    if ((rc = make_store_map(&a.tm_dk, dk->ptr, s->B, s->Nk, s->Hkv, s->d, dk->stride_b, dk->stride_n,
+                             dk->stride_h)) ||
+        (rc = make_store_map(&a.tm_dv, dv->ptr, s->B, s->Nk, s->Hkv, s->d, dv->stride_b, dv->stride_n,
+                             dv->stride_h)))
+      return rc;
+    a.tma_out = 1;
+  }
   a.lse = lse;
   a.nq_pad = cdiv(nq_rows, TILE) * TILE;
   const size_t rows = static_cast<size_t>(s->B) * s->Hq * a.nq_pad;

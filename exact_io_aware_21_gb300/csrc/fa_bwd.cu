@@ -65,6 +65,7 @@ struct BwdParams {
   const int* cols_idx;
   const int* sp_plan;   // block-sparse: the dK/dV segment plan
   float* sp_pool;       // ... and the partial tiles of split key tiles
+  int tma_out;          // dense: dK and dV leave through TMA stores
 };
 
 // ================================================================== preprocess
@@ -228,6 +229,42 @@ __device__ __forceinline__ void store_acc_f32(uint32_t t_acc, int col0, float* d
   }
 }
 
+// Accumulator columns [col0, col0 + NC) of the warp's 32 TMEM lanes as bf16 (times
+// mul), leaving through TMA stores of 32 x 32 boxes at (col0 + 32 c, c1, c2, c3) of
+// `map`: each box is staged in `buf` (2 KB, 512-byte aligned) in the 64-byte-swizzled
+// layout (16-byte chunk q of row r at chunk q ^ ((r / 2) % 4)); the store made from the
+// buffer before must have read it first.  Rows past the tensor's end are dropped by
+// the copy engine.
+template <int NC>
+__device__ __forceinline__ void store_acc_boxes(uint32_t t_acc, int col0, float mul, const CUtensorMap* map,
+                                                int c1, int c2, int c3, uint8_t* buf) {
+  const float2 m2 = make_float2(mul, mul);
+  const int lr = lane_id();
+#pragma unroll 1
+  for (int cc = 0; cc < NC / 32; ++cc) {
+    uint32_t v[32];
+    tmem_ld32(t_acc + col0 + cc * 32, v);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 f = __fmul2_rn(f32x2(v[2 * i], v[2 * i + 1]), m2);
+      w[i] = pack_bf16(f.x, f.y);
+    }
+    if (lr == 0) bulk_wait_read<0>();
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(buf + lr * 64 + ((q ^ ((lr >> 1) & 3)) << 4)) =
+          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lr == 0) {
+      tma_store_4d(map, buf, col0 + cc * 32, c1, c2, c3);
+      bulk_commit();
+    }
+  }
+}
+
 // ================================================================== dK / dV
 template <int D>
 struct DkvLayout {
@@ -243,8 +280,12 @@ struct DkvLayout {
   static constexpr int NBAR = 4 + 2 + 2 * STAGES + 6;
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
-  static constexpr int OFF_SCR = (OFF_TMEM + 16 + 127) / 128 * 128;  // row-store scratch, one per gradient warp
+  // row-store scratch, one per gradient warp; 1024-byte aligned, so that each warp's
+  // first 2 KB (at a multiple of 2560 bytes) can stage a swizzled TMA-store box
+  static constexpr int OFF_SCR = (OFF_TMEM + 16 + 1023) / 1024 * 1024;
   static constexpr int ALLOC = OFF_SCR + 8 * ROW_SCRATCH_BYTES + 1024;
+  static_assert(ROW_SCRATCH_BYTES % 512 == 0 && ROW_SCRATCH_BYTES >= 2048, "a box per warp");
+  static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
 struct DkvBars {
@@ -346,7 +387,8 @@ template <int D, int MASK, bool VL, bool SP>
 __global__ void __launch_bounds__(384, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdParams p) {
+                    const BwdParams p, const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv) {
   using L = DkvLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -662,12 +704,18 @@ __global__ void __launch_bounds__(384, 1)
         float* part = p.sp_pool + (static_cast<int64_t>(w.slot) * TILE + r) * (2 * D) + (c0 / 64) * (D / 2);
         store_acc_f32<D / 2>(tdV, (c0 / 64) * (D / 2), part);
         store_acc_f32<D / 2>(tdK, (c0 / 64) * (D / 2), part + D);
+      } else if (!VL && !SP && p.tma_out) {  // dense: 32 x 32 boxes through the copy engine
+        if (key0 < su.Nk) {                   // (a warp whose rows all lie past the end stores nothing)
+          store_acc_boxes<D / 2>(tdV, (c0 / 64) * (D / 2), 1.f, &tm_dv, w.kvh, key0, w.b, scratch);
+          store_acc_boxes<D / 2>(tdK, (c0 / 64) * (D / 2), p.scale, &tm_dk, w.kvh, key0, w.b, scratch);
+        }
       } else {
         store_acc_rows<D / 2>(tdV, (c0 / 64) * (D / 2), 1.f, dv0, p.dv.sn, su.Nk - key0, scratch);
         store_acc_rows<D / 2>(tdK, (c0 / 64) * (D / 2), p.scale, dk0, p.dk.sn, su.Nk - key0, scratch);
       }
       sq += w.n_it;
     }
+    if (!VL && !SP && p.tma_out && lane_id() == 0) bulk_wait<0>();  // the gradient stores have finished
   }
   // Lanes 1-31 of the producer and MMA warps had no role: they wait here for their
   // lane 0, so that every warp reaches the block barrier converged (a barrier met by
@@ -1119,6 +1167,7 @@ template <int D, int MASK, bool VL = false, bool SP = false>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   BwdParams p;
   p.plan = nullptr;
+  p.tma_out = 0;
   p.rows_ptr = a.rows_ptr;
   p.rows_idx = a.rows_idx;
   p.cols_ptr = a.cols_ptr;
@@ -1175,7 +1224,8 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
     }
     // block-sparse: the unit count is on the device; fill the GPU and let the plan's count stop the CTAs
     const int grid = SP ? a.num_sms : imax(1, imin(p.total_units, a.num_sms));
-    kern<<<grid, 384, DkvLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, p);
+    p.tma_out = (!VL && !SP) ? a.tma_out : 0;
+    kern<<<grid, 384, DkvLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, p, a.tm_dk, a.tm_dv);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (SP) {
       bwd_sparse_reduce_kernel<D><<<2 * a.num_sms, 256, 0, st>>>(p);

@@ -105,6 +105,9 @@ struct BwdLaunch {
   const int* cols_idx;
   const int* sp_plan;
   float* sp_pool;  // partial tiles of split key tiles
+  // dense bf16 (tma_out = 1): dK and dV leave through TMA stores (maps as the forward's output)
+  CUtensorMap tm_dk, tm_dv;
+  int tma_out;
 };
 cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t st);
 

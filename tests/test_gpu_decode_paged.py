@@ -70,6 +70,9 @@ CASES = [
     (3, 12, 6, 2, [100, 1, 1500], 128, 16, 0),   # Hkv = 6: three groups of two, four boxes a stage
     (2, 4, 2, 8, [600, 1300], 64, 64, 2),        # two heads, 16 packed rows, page = stage
     (2, 8, 4, 2, [5000, 333], 128, 16, 50),      # more splits than the short sequence has stages
+    (2, 8, 4, 1, [1000, 2000], 128, 16, 0),      # four heads, two 16-row boxes a stage
+    (2, 4, 2, 2, [777, 64], 64, 16, 0),          # two heads, d = 64, four 16-row boxes a stage
+    (1, 16, 4, 4, [1500], 64, 32, 2),            # four heads, d = 64, page = stage
     # more than 16 packed rows: the per-head kernel with two or four 16-row tiles
     (2, 16, 2, 4, [900, 2500], 128, 16, 0),      # 32 rows, pages of 16
     (2, 32, 8, 8, [300, 1200], 128, 16, 0),      # 32 rows with Hkv = 8 (no head groups past 16 rows)

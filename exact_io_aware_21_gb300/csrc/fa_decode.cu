@@ -295,11 +295,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   // Q as m16n8k16 A fragments (rows r = qpos * g + head-in-group, zero above `rows`).
   uint32_t qa[D / 16][4];
   {
-    const int ra = rt * 16 + gq, rb = ra + 8;
+    const int row_a = rt * 16 + gq, row_b = row_a + 8;  // this thread's two fragment rows
     const __nv_bfloat16* qpa = nullptr;
     const __nv_bfloat16* qpb = nullptr;
-    if (ra < rows) qpa = p.q + b * p.q_sb + (ra / g) * p.q_sn + (kvh * g + ra % g) * p.q_sh;
-    if (rb < rows) qpb = p.q + b * p.q_sb + (rb / g) * p.q_sn + (kvh * g + rb % g) * p.q_sh;
+    if (row_a < rows) qpa = p.q + b * p.q_sb + (row_a / g) * p.q_sn + (kvh * g + row_a % g) * p.q_sh;
+    if (row_b < rows) qpb = p.q + b * p.q_sb + (row_b / g) * p.q_sn + (kvh * g + row_b % g) * p.q_sh;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       const int c0 = ks * 16 + 2 * tq;

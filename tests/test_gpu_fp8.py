@@ -13,6 +13,7 @@ from parity import assert_fwd, rel_fro
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
+GRAD_BOUND_MIXED = 0.05  # twice the largest measured (0.025 on GB300)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -95,7 +96,7 @@ def test_quantize_strided_views():
 # ------------------------------------------------------------------ forward
 def fp8_inputs(B, Hq, Hkv, N, seed, had, outliers=False, causal=False):
     w = inputs.Workload("t", B, Hq, Hkv, N, N, 128, causal, outliers=outliers, seed=seed)
-    x = inputs.make(w, with_do=False)
+    x = inputs.make(w, with_do=True)
     sg = signs_for(128, had)
     q8, sq = fa.quantize_fp8(x["q"].to(DEV), 128, sg)
     k8, sk = fa.quantize_fp8(x["k"].to(DEV), 128, sg)
@@ -191,3 +192,33 @@ def test_forward_fp8_error_at_the_pages_level(had):
     for b, h in heads:
         mse = float(np.mean((o[b, rows, h].float().cpu().numpy() - o_ex[b, rows, h]) ** 2))
         assert mse < 5e-5, f"fp8 vs exact attention h{h} hadamard={had}: MSE {mse:.2e}"
+
+
+@pytest.mark.parametrize("had", [True, False])
+def test_fp8_forward_then_bf16_backward(had):
+    """The pages' mixed mode ("第18章" §18.6.2, after Table 18-21): the forward in FP8,
+    the backward in bf16.  The bf16 backward takes the FP8 forward's O and LSE with the
+    bf16 Q, K, V, so P rebuilt from bf16 scores carries the FP8 forward's LSE error.
+    On N(0, 1) inputs every gradient stays within a relative Frobenius distance of
+    0.05 of the exact gradients (fp64 oracle), the FP8 output within 0.08.  (With the
+    outlier channel the FP8 LSE is off by whole units for peaky rows and P rebuilt
+    from exact scores no longer sums to one there: dQ was 2.8x off in relative
+    Frobenius distance.  The mixed mode needs statistics consistent with the
+    backward's own scores, which the FP8 forward does not give on such data.)"""
+    outliers = False
+    B_, Hq, Hkv, N = 1, 4, 2, 768
+    x, (q8, k8, v8, sq, sk, sv) = fp8_inputs(B_, Hq, Hkv, N, seed=77, had=had, outliers=outliers, causal=True)
+    scale = 1 / np.sqrt(128)
+    o, lse = fa.forward_fp8(q8, k8, v8, sq, sk, sv, causal=True, scale=scale)
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    o_ex, _ = A.attention_forward(x["q"], x["k"], x["v"], scale, True)
+    dq_ex, dk_ex, dv_ex = A.attention_backward(x["q"], x["k"], x["v"], x["do"], scale, True)
+    errs = {"O": rel_fro(o, o_ex), "dQ": rel_fro(dq, dq_ex), "dK": rel_fro(dk, dk_ex), "dV": rel_fro(dv, dv_ex)}
+    print("fp8 forward + bf16 backward, hadamard", had, "outliers", outliers, {n: f"{e:.3g}" for n, e in errs.items()})
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
+    assert errs["O"] < 0.08
+    for n in ("dQ", "dK", "dV"):
+        assert errs[n] < GRAD_BOUND_MIXED, (n, errs)

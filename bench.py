@@ -428,7 +428,7 @@ class Leg:
 
 
 KERNELS_PER_CALL = {"fwd_bs": 2, "bwd_bs": 5, "fwd": 2, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
-                    "quant_v": 2, "fwd_fp8": 2, "fwd_fp8_cr": 2, "fwd_varlen": 3, "bwd_varlen": 3}
+                    "quant_v": 2, "fwd_fp8": 2, "fwd_fp8_cr": 2, "fwd_varlen": 3, "bwd_varlen": 5}
 
 
 def kernel_flops(part, w):

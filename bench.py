@@ -3,7 +3,7 @@
 
 A step is one pass of the whole hot path over synthetic inputs already resident
 in HBM:
-  training legs  forward + backward (preprocess, dK/dV, dQ) of
+  training legs  forward + backward (one fa_bwd call: preprocess, dK/dV, dQ) of
                  mha_b4_h16_n2048_d64       (B=4, H=16, N=2048, d=64, non-causal)
                  causal_b2_h16_n4096_d128   (B=2, H=16, N=4096, d=128, causal)
                  gqa_causal_b1_hq32_hkv8_n8192_d128_outliers
@@ -28,7 +28,10 @@ in HBM:
                  Hadamard rotation, V per head) and the FP8 forward of the GQA
                  workload
 The tiny workload (tiny_b1_h1_n256_d64, the oracle's full-size parity case) is
-timed beside the step.
+timed beside the step.  The backward of the training, window and tiny legs is
+timed as the one call a user makes (its kernels overlap across their
+boundaries); each of its three kernels is also timed alone, for the breakdown
+and the dominant kernel's roofline.
 ``value`` = counted forward + backward FLOPs of the training legs divided by
 their device time (TFLOPS; forward 4*B*H*Nq*Nk*d, halved when causal, backward
 2.5x that).  Tensor-core fractions are against the measured burst bf16 peak
@@ -97,6 +100,7 @@ METRIC = "fwd/bwd attention TFLOPS and % of BF16 tensor peak; decode KV-read GB/
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 HOLD_CYCLES = 200_000  # the spin kernel before each timed group: about 0.1 ms at 2 GHz
+BWD_KERNELS = ("bwd_pre", "bwd_dkdv", "bwd_dq")  # the backward's kernels, each also timed alone
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -427,7 +431,8 @@ class Leg:
         self.ms = {k: 0.0 for k, _ in fns}
 
 
-KERNELS_PER_CALL = {"fwd_bs": 2, "bwd_bs": 5, "fwd": 2, "bwd_pre": 1, "bwd_dkdv": 1, "bwd_dq": 1, "decode": 2, "quant_q": 1, "quant_k": 1,
+KERNELS_PER_CALL = {"fwd_bs": 2, "bwd_bs": 5, "fwd": 2, "bwd": 4, "bwd_pre": 2, "bwd_dkdv": 2, "bwd_dq": 2, "decode": 2,
+                    "quant_q": 1, "quant_k": 1,
                     "quant_v": 2, "fwd_fp8": 2, "fwd_fp8_cr": 2, "fwd_varlen": 3, "bwd_varlen": 5}
 
 
@@ -472,8 +477,14 @@ def make_legs(device, seed):
             B.fa_bwd_part(i, x["q"], x["k"], x["v"], st["o"], st["lse"], x["do"], st["dq"], st["dk"], st["dv"],
                           st["s"], st["wsb"], st["ores"])
 
-        fns = [("fwd", fwd), ("bwd_pre", lambda part=part: part(0)), ("bwd_dkdv", lambda part=part: part(1)),
-               ("bwd_dq", lambda part=part: part(2))]
+        def bwd(st=st):
+            x = st["x"]
+            B.fa_bwd(x["q"], x["k"], x["v"], st["o"], st["lse"], x["do"], st["dq"], st["dk"], st["dv"], st["s"],
+                     st["wsb"], st["ores"])
+
+        # the whole backward (the step's), then each of its kernels alone (the breakdown)
+        fns = [("fwd", fwd), ("bwd", bwd), ("bwd_pre", lambda part=part: part(0)),
+               ("bwd_dkdv", lambda part=part: part(1)), ("bwd_dq", lambda part=part: part(2))]
         kind = "tiny" if w is tiny else "window" if w.window else "train"
         legs.append(Leg(w.name, kind, w, fns, 3.5 * fwd_flops(w)))
         if w.name in TARGET_TRAIN:  # conditional rescaling beside the exact forward
@@ -832,7 +843,8 @@ def run_ours(args):
 
     for leg, part, e0, e1 in recs:
         leg.ms[part] += e0.elapsed_time(e1) / args.steps
-    leg_ms = {l.name: sum(l.ms.values()) for l in legs}
+    # a leg's time: its parts, without the backward's per-kernel breakdown (timed again alone)
+    leg_ms = {l.name: sum(v for k, v in l.ms.items() if not ("bwd" in l.ms and k in BWD_KERNELS)) for l in legs}
     # the step is the training and decode legs; the other legs are timed in the same
     # loop and reported beside them
     step_legs = [l for l in legs if l.kind in ("train", "decode")]
@@ -855,7 +867,7 @@ def run_ours(args):
             fk = {"varlen": "fwd_varlen", "blocksparse": "fwd_bs"}.get(l.kind, "fwd")
             fwd_ms = l.ms[fk]
             bwd_ms = (l.ms["bwd_varlen"] if l.kind == "varlen" else l.ms["bwd_bs"] if l.kind == "blocksparse"
-                      else l.ms["bwd_pre"] + l.ms["bwd_dkdv"] + l.ms["bwd_dq"])
+                      else l.ms["bwd"])
             ft, ff, fs = tc(f, fwd_ms)
             bt, bf, bs = tc(2.5 * f, bwd_ms)
             out = {"fwd_ms": r4(fwd_ms), "fwd_tflops": ft, "fwd_frac_of_burst_peak": ff,
@@ -863,7 +875,8 @@ def run_ours(args):
                    "bwd_frac_of_burst_peak": bf, "bwd_frac_of_sustained_peak": bs,
                    "in_step": l.kind == "train"}
             if l.kind in ("train", "window", "tiny"):
-                out["bwd_parts_ms"] = {k: r4(l.ms[k]) for k in ("bwd_pre", "bwd_dkdv", "bwd_dq")}
+                out["bwd_parts_ms"] = {k: r4(l.ms[k]) for k in BWD_KERNELS}
+                out["bwd_parts_sum_ms"] = r4(sum(l.ms[k] for k in BWD_KERNELS))
             if l.kind == "window":
                 out.update({"window": list(l.w.window),
                             "flops_count": "4*B*H*d per visible (query, key) pair, x3.5 fwd+bwd"})
@@ -927,7 +940,8 @@ def run_ours(args):
     targets["all_met"] = bool(ok)
 
     # roofline of the dominant kernel: the launch with the largest share of the step
-    dl, dp = max(((l, p) for l in step_legs for p, _ in l.fns if p != "bwd_pre"), key=lambda lp: lp[0].ms[lp[1]])
+    dl, dp = max(((l, p) for l in step_legs for p, _ in l.fns if p not in ("bwd_pre", "bwd")),
+                 key=lambda lp: lp[0].ms[lp[1]])
     if dp == "decode":
         ach = dl.work / dl.ms[dp] / 1e6
         roof = {"kernel": "fa_decode_split_kernel", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],

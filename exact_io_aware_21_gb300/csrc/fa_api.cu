@@ -732,9 +732,8 @@ static int bwd_impl(int parts, const fa_tensor_t* q, const fa_tensor_t* k, const
   a.timeout_ns = g_timeout_ns;
   a.num_sms = sms;
   a.parts = parts;
-  if ((rc = clear_header(ws, static_cast<cudaStream_t>(stream)))) return rc;
-  cudaError_t e = cudaSuccess;
-  if (sp) {
+  cudaError_t e = launch_header_clear(ws, static_cast<cudaStream_t>(stream));
+  if (sp && e == cudaSuccess) {
     sl.status = a.status;
     e = launch_sparse_lists(sl, static_cast<cudaStream_t>(stream));
   }

@@ -18,6 +18,12 @@
 //               P^T and dS^T are written back over S^T and dP^T as bf16 and
 //               feed the dV and dK products from TMEM.
 //   dQ          a unit is one 128-row query tile; it loops over key tiles.
+//   Dense path: the three follow a header-clearing kernel, each launched with
+//   programmatic stream serialisation: it sets up while the one before it
+//   finishes and waits (griddepcontrol) before reading that one's results.  The
+//   dK/dV kernel lets the dQ kernel launch as soon as its own wait is over, so
+//   dQ CTAs take over SMs as dK/dV CTAs finish; dQ reads only the preprocess
+//   kernel's output, complete by then, and skips its wait in that case.
 //               TMEM: S double-buffered [0,256), dP [256,384), dQ [384,384+d);
 //               dS is written over dP as bf16 and feeds dQ += dS K.
 // Warp roles: warp 0 loads with TMA, one thread of warp 1 issues tcgen05 MMAs,
@@ -29,6 +35,8 @@
 // 64, so the two warpgroups never wait for each other; the MMAs that read that
 // operand from TMEM address its second half 64 columns on.
 #include <math.h>
+
+#include <utility>
 
 #include "fa_kernels.h"
 #include "sm103.cuh"
@@ -66,6 +74,7 @@ struct BwdParams {
   const int* sp_plan;   // block-sparse: the dK/dV segment plan
   float* sp_pool;       // ... and the partial tiles of split key tiles
   int tma_out;          // dense: dK and dV leave through TMA stores
+  int dq_after_dkdv;    // dQ launched right after the dK/dV kernel of the same call (see launch_bwd_t)
 };
 
 // ================================================================== preprocess
@@ -126,6 +135,8 @@ __device__ __forceinline__ void preprocess_row(const BwdParams& p, int b, int h,
 // Dense: one thread group per row of the padded [B * Hq, nq_pad] layout.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const BwdParams p) {
+  griddep_wait();  // launched with programmatic serialisation after the header clear
+  griddep_launch_dependents();
   constexpr int TPR = D / 8;
   const int64_t row = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / TPR;
   const int64_t rows = static_cast<int64_t>(p.dims.B) * p.dims.Hq * p.nq_pad;
@@ -425,6 +436,8 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // the preprocess kernel's statistics (and the cleared header) are complete
+  griddep_launch_dependents();  // the dQ kernel may take over SMs as this kernel's CTAs finish
 
   if (warp == 0) {
     if (lane_id() == 0) {  // ---------------------------------------------- producer
@@ -836,6 +849,9 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the preprocess kernel's statistics are complete (dQ launched right after dK/dV: they
+  // were before the dK/dV kernel let it start, and dQ reads nothing dK/dV writes)
+  if (!p.dq_after_dkdv) griddep_wait();
 
   if (warp == 0) {
     if (lane_id() == 0) {  // ---------------------------------------------- producer
@@ -1163,11 +1179,30 @@ __global__ void __launch_bounds__(256) bwd_sparse_reduce_kernel(const BwdParams 
   }
 }
 
+// Launch with programmatic stream serialisation: the kernel may start while the one
+// before it in the stream finishes (it waits with griddepcontrol before depending on it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int D, int MASK, bool VL = false, bool SP = false>
 cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
   BwdParams p;
   p.plan = nullptr;
   p.tma_out = 0;
+  p.dq_after_dkdv = 0;
   p.rows_ptr = a.rows_ptr;
   p.rows_idx = a.rows_idx;
   p.cols_ptr = a.cols_ptr;
@@ -1205,7 +1240,8 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
           p, a.plan_dq);
     } else {
       const int64_t threads = static_cast<int64_t>(a.dims.B) * a.dims.Hq * a.nq_pad * (D / 8);
-      bwd_preprocess_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(p);
+      cudaError_t e = launch_pdl(bwd_preprocess_kernel<D>, static_cast<unsigned>((threads + 255) / 256), 256, 0, st, p);
+      if (e != cudaSuccess) return e;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1225,7 +1261,12 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
     // block-sparse: the unit count is on the device; fill the GPU and let the plan's count stop the CTAs
     const int grid = SP ? a.num_sms : imax(1, imin(p.total_units, a.num_sms));
     p.tma_out = (!VL && !SP) ? a.tma_out : 0;
-    kern<<<grid, 384, DkvLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, p, a.tm_dk, a.tm_dv);
+    if (!VL && !SP) {
+      e = launch_pdl(kern, grid, 384, DkvLayout<D>::ALLOC, st, a.tm_q, a.tm_k, a.tm_v, a.tm_do, p, a.tm_dk, a.tm_dv);
+      if (e != cudaSuccess) return e;
+    } else {
+      kern<<<grid, 384, DkvLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, p, a.tm_dk, a.tm_dv);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (SP) {
       bwd_sparse_reduce_kernel<D><<<2 * a.num_sms, 256, 0, st>>>(p);
@@ -1240,8 +1281,15 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t st) {
     p.counter = a.counters + 1;
     p.total_units = dq_units(a.dims);
     p.plan = a.plan_dq;  // built above
-    kern<<<imax(1, imin(p.total_units, a.num_sms)), 384, DqLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
-                                                                                   a.tm_do, p);
+    p.dq_after_dkdv = (!VL && !SP && (a.parts & 2)) ? 1 : 0;
+    if (!VL && !SP) {
+      e = launch_pdl(kern, imax(1, imin(p.total_units, a.num_sms)), 384, DqLayout<D>::ALLOC, st, a.tm_q, a.tm_k,
+                     a.tm_v, a.tm_do, p);
+      if (e != cudaSuccess) return e;
+    } else {
+      kern<<<imax(1, imin(p.total_units, a.num_sms)), 384, DqLayout<D>::ALLOC, st>>>(a.tm_q, a.tm_k, a.tm_v,
+                                                                                     a.tm_do, p);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -240,7 +240,11 @@ int fa_fwd_fp8(const fa_tensor_t* q8, const fa_tensor_t* k8, const fa_tensor_t* 
  * tile loops (the per-block D of the printed pseudocode is not used).  dK/dV
  * of a shared K/V head sum the contributions of its query heads.  Three
  * kernels, no atomics: preprocess (D), dK/dV (one key tile per work unit),
- * dQ (one query tile per work unit); results are deterministic.
+ * dQ (one query tile per work unit); results are deterministic.  On the dense
+ * path they follow a header-clearing kernel and are launched with programmatic
+ * stream serialisation: each starts while the one before it finishes and waits
+ * (griddepcontrol) before it reads what that one wrote; dQ, which reads nothing
+ * dK/dV writes, takes over each SM as the dK/dV kernel's CTA there finishes.
  *   q, o, dout [B, Nq, Hq, d] in;  k, v [B, Nk, Hkv, d] in;  lse in (from fa_fwd)
  *   o_residual  optional in (NULL = none): the residual written by fa_fwd.
  *       D is then dO . (O + o_residual).  Without it D is dO . O with O in
@@ -257,8 +261,9 @@ int fa_bwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, con
 /* The three backward launches one at a time, for callers that time or
  * schedule them separately: part 0 = preprocess (D and the padded LSE, kept in
  * the workspace), 1 = dK/dV, 2 = dQ.  Parts 1 and 2 read what part 0 left in
- * the same workspace; running parts 0, 1, 2 in order on one stream is exactly
- * fa_bwd.  Same arguments and errors as fa_bwd; FA_ERR_INVALID for another part. */
+ * the same workspace; running parts 0, 1, 2 in order on one stream gives
+ * exactly fa_bwd's results (without the overlap between its kernels).  Same
+ * arguments and errors as fa_bwd; FA_ERR_INVALID for another part. */
 int fa_bwd_part(int part, const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o,
                 const float* lse, const fa_tensor_t* o_residual, const fa_tensor_t* dout, const fa_tensor_t* dq,
                 const fa_tensor_t* dk, const fa_tensor_t* dv, const fa_shape_t* shape, void* workspace,

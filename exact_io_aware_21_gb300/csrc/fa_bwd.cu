@@ -164,13 +164,16 @@ __global__ void __launch_bounds__(256) bwd_preprocess_varlen_kernel(const BwdPar
 }
 
 // ================================================================== shared helpers
-template <int D>
+// EW: called by a whole converged warp, one elected lane issuing each MMA (else
+// by a single lane).
+template <int D, bool EW = false>
 __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a_base, uint32_t b_base) {
   constexpr uint32_t IDESC = idesc_bf16(128, 128, false, false);
 #pragma unroll
   for (int k = 0; k < D / 16; ++k) {
     const uint32_t off = (k / 4) * (TILE * 128) + (k % 4) * 32;
-    mma_ss(d_tmem, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), IDESC, k > 0);
+    const uint64_t ad = sdesc_sw128(a_base + off, 16, 1024), bd = sdesc_sw128(b_base + off, 16, 1024);
+    if (!EW || elect_one()) mma_ss(d_tmem, ad, bd, IDESC, k > 0);
   }
 }
 
@@ -189,14 +192,14 @@ __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint3
 // Half of issue_ts: the four K steps whose A columns come from chunk `half` of
 // each elementwise warpgroup (K steps 0,1,4,5 for half 0; 2,3,6,7 for half 1),
 // so the product can start on the columns written first.
-template <int D, int HALF>
+template <int D, int HALF, bool EW = false>
 __device__ __forceinline__ void issue_ts_half(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, bool acc) {
   constexpr uint32_t IDESC = idesc_bf16(128, D, false, true);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int k = (i & 1) + 2 * HALF + (i >> 1) * 4;
-    mma_ts(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), sdesc_sw128(b_base + k * 16 * 128, TILE * 128, 1024),
-           IDESC, (acc || i > 0) ? 1u : 0u);
+    const uint64_t bd = sdesc_sw128(b_base + k * 16 * 128, TILE * 128, 1024);
+    if (!EW || elect_one()) mma_ts(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), bd, IDESC, (acc || i > 0) ? 1u : 0u);
   }
 }
 
@@ -498,75 +501,79 @@ __global__ void __launch_bounds__(384, 1)
         }
       if (kv_armed >= 0) mbar_wait(bar.kv_full, kv_armed & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
     }
-  } else if (warp == 1) {
-    if (lane_id() == 0) {  // ---------------------------------------------- MMA issuer
-      const uint32_t kb = smem_u32(smem + L::OFF_K), vb = smem_u32(smem + L::OFF_V);
-      const uint32_t stb = smem_u32(smem + L::OFF_ST);
-      const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
-      uint32_t sq = 0, pph = 0, dph = 0, un = 0;
-      for (int it = 0;; ++it) {
-        const int slot = it & 1;
-        if (!mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
-        const int u = unit_slot[slot];
-        mbar_arrive(&bar.unit_empty[slot]);
-        if (u >= total) break;
-        const DkvUnit w = dkv_decode<MASK, VL, SP>(p, u);
-        if (!w.work) continue;
-        if (!mbar_wait(bar.kv_full, (un++) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) break;
-        bool ok = mbar_wait(&bar.st_full[sq % L::STAGES], (sq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
-        if (!ok) break;
-        tc_fence_after();
-        {
-          const uint32_t qb = stb + (sq % L::STAGES) * L::STAGE;
-          issue_ss<D>(tS, kb, qb);           // S^T = K Q^T
-          mma_commit(bar.s_full);
-          issue_ss<D>(tP, vb, qb + L::TB);   // dP^T = V dO^T
+  } else if (warp == 1) {  // -------------------------------------------------- MMA issuer
+    // The whole warp runs the issue loop converged; one elected lane issues each
+    // MMA and commit, so descriptors are formed in uniform registers.
+    const uint32_t kb = smem_u32(smem + L::OFF_K), vb = smem_u32(smem + L::OFF_V);
+    const uint32_t stb = smem_u32(smem + L::OFF_ST);
+    const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+    uint32_t sq = 0, pph = 0, dph = 0, un = 0;
+    for (int it = 0;; ++it) {
+      const int slot = it & 1;
+      if (!warp_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
+      const int u = unit_slot[slot];
+      if (elect_one()) mbar_arrive(&bar.unit_empty[slot]);
+      if (u >= total) break;
+      const DkvUnit w = dkv_decode<MASK, VL, SP>(p, u);
+      if (!w.work) continue;
+      if (!warp_wait(bar.kv_full, (un++) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) break;
+      bool ok = warp_wait(&bar.st_full[sq % L::STAGES], (sq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+      if (!ok) break;
+      tc_fence_after();
+      {
+        const uint32_t qb = stb + (sq % L::STAGES) * L::STAGE;
+        issue_ss<D, true>(tS, kb, qb);           // S^T = K Q^T
+        if (elect_one()) mma_commit(bar.s_full);
+        issue_ss<D, true>(tP, vb, qb + L::TB);   // dP^T = V dO^T
+        if (elect_one()) {
           mma_commit(bar.dp_full);
           if (w.n_it == 1) mma_commit(bar.kv_empty);  // K and V are read by S and dP only
         }
-        for (int k = 0; k < w.n_it && ok; ++k) {
-          const uint32_t cur = stb + ((sq + k) % L::STAGES) * L::STAGE;
-          // dV += P^T dO, each half as soon as its P columns are in TMEM
-          ok = mbar_wait(&bar.p_full[0], pph, ctl, FA_STATUS_TIMEOUT_MMA);
+      }
+      for (int k = 0; k < w.n_it && ok; ++k) {
+        const uint32_t cur = stb + ((sq + k) % L::STAGES) * L::STAGE;
+        // dV += P^T dO, each half as soon as its P columns are in TMEM
+        ok = warp_wait(&bar.p_full[0], pph, ctl, FA_STATUS_TIMEOUT_MMA);
+        if (!ok) break;
+        tc_fence_after();
+        issue_ts_half<D, 0, true>(tdV, tS, cur + L::TB, k > 0);
+        ok = warp_wait(&bar.p_full[1], pph, ctl, FA_STATUS_TIMEOUT_MMA);
+        pph ^= 1;
+        if (!ok) break;
+        tc_fence_after();
+        issue_ts_half<D, 1, true>(tdV, tS, cur + L::TB, true);
+        const bool more = k + 1 < w.n_it;
+        uint32_t nxt = 0;
+        if (more) {
+          const uint32_t nsq = sq + k + 1;
+          ok = warp_wait(&bar.st_full[nsq % L::STAGES], (nsq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
           if (!ok) break;
           tc_fence_after();
-          issue_ts_half<D, 0>(tdV, tS, cur + L::TB, k > 0);
-          ok = mbar_wait(&bar.p_full[1], pph, ctl, FA_STATUS_TIMEOUT_MMA);
-          pph ^= 1;
-          if (!ok) break;
-          tc_fence_after();
-          issue_ts_half<D, 1>(tdV, tS, cur + L::TB, true);
-          const bool more = k + 1 < w.n_it;
-          uint32_t nxt = 0;
-          if (more) {
-            const uint32_t nsq = sq + k + 1;
-            ok = mbar_wait(&bar.st_full[nsq % L::STAGES], (nsq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
-            if (!ok) break;
-            tc_fence_after();
-            nxt = stb + (nsq % L::STAGES) * L::STAGE;
-            issue_ss<D>(tS, kb, nxt);
-            mma_commit(bar.s_full);
-          }
-          // dK += dS^T Q (whole: a second hand-off here costs more than it overlaps)
-          ok = mbar_wait(bar.ds_full, dph, ctl, FA_STATUS_TIMEOUT_MMA);
-          dph ^= 1;
-          if (!ok) break;
-          tc_fence_after();
-          issue_ts_half<D, 0>(tdK, tP, cur, k > 0);
-          issue_ts_half<D, 1>(tdK, tP, cur, true);
-          mma_commit(&bar.st_empty[(sq + k) % L::STAGES]);
-          if (more) {
-            issue_ss<D>(tP, vb, nxt + L::TB);
+          nxt = stb + (nsq % L::STAGES) * L::STAGE;
+          issue_ss<D, true>(tS, kb, nxt);
+          if (elect_one()) mma_commit(bar.s_full);
+        }
+        // dK += dS^T Q (whole: a second hand-off here costs more than it overlaps)
+        ok = warp_wait(bar.ds_full, dph, ctl, FA_STATUS_TIMEOUT_MMA);
+        dph ^= 1;
+        if (!ok) break;
+        tc_fence_after();
+        issue_ts_half<D, 0, true>(tdK, tP, cur, k > 0);
+        issue_ts_half<D, 1, true>(tdK, tP, cur, true);
+        if (elect_one()) mma_commit(&bar.st_empty[(sq + k) % L::STAGES]);
+        if (more) {
+          issue_ss<D, true>(tP, vb, nxt + L::TB);
+          // The unit's last S and dP are issued: K and V can be refilled with the
+          // next unit's tiles while its last dV and dK run.
+          if (elect_one()) {
             mma_commit(bar.dp_full);
-            // The unit's last S and dP are issued: K and V can be refilled with the
-            // next unit's tiles while its last dV and dK run.
             if (k + 2 == w.n_it) mma_commit(bar.kv_empty);
           }
         }
-        if (!ok) break;
-        mma_commit(bar.acc_full);
-        sq += w.n_it;
       }
+      if (!ok) break;
+      if (elect_one()) mma_commit(bar.acc_full);
+      sq += w.n_it;
     }
   } else if (warp >= 4) {  // -------------------------------------------------- gradient warps
     const int wq = warp & 3;
@@ -730,9 +737,9 @@ __global__ void __launch_bounds__(384, 1)
     }
     if (!VL && !SP && p.tma_out && lane_id() == 0) bulk_wait<0>();  // the gradient stores have finished
   }
-  // Lanes 1-31 of the producer and MMA warps had no role: they wait here for their
-  // lane 0, so that every warp reaches the block barrier converged (a barrier met by
-  // part of a warp does not hold the rest) and TMEM is freed only after all its users.
+  // Lanes 1-31 of the producer warp had no role: they wait here for their lane 0,
+  // so that every warp reaches the block barrier converged (a barrier met by part
+  // of a warp does not hold the rest) and TMEM is freed only after all its users.
   __syncwarp();
   tc_fence_before();
   __syncthreads();

@@ -117,6 +117,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   return mbar_wait_slow(a, parity, c, code);
 }
 
+// mbar_wait by a whole converged warp; every lane gets the same answer.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctl& c, int code) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, c, code));
+}
+
 // ---------------------------------------------------------------------------
 // TMA: 4-D tiled tensor load into shared memory, completing on an mbarrier.
 // ---------------------------------------------------------------------------
@@ -398,6 +403,16 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
 }
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
+
+// True in exactly one lane of the (converged, full) warp: the lowest.  Issuing
+// tcgen05 MMAs from converged warp code, one elected lane per instruction, lets
+// their descriptors be formed once per warp in uniform registers instead of in
+// a single diverged lane.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile("{\n .reg .pred q;\n elect.sync _|q, 0xffffffff;\n selp.u32 %0, 1, 0, q;\n}\n" : "=r"(p));
+  return p != 0;
+}
 
 // ---------------------------------------------------------------------------
 // Row stores through shared memory.  A warp that owns 32 rows (one per lane)

@@ -180,13 +180,14 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a_base, uint3
 // D[128 x D] (+)= A[tmem, 128 x 128 bf16] * B[smem tile 128 x D, N-major].
 // A's K columns 0-63 are packed at TMEM columns [0, 32), K columns 64-127 at
 // [64, 96) (one half per elementwise warpgroup).
-template <int D>
+template <int D, bool EW = false>
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_base, bool acc) {
   constexpr uint32_t IDESC = idesc_bf16(128, D, false, true);
 #pragma unroll
-  for (int k = 0; k < TILE / 16; ++k)
-    mma_ts(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), sdesc_sw128(b_base + k * 16 * 128, TILE * 128, 1024),
-           IDESC, (acc || k > 0) ? 1u : 0u);
+  for (int k = 0; k < TILE / 16; ++k) {
+    const uint64_t bd = sdesc_sw128(b_base + k * 16 * 128, TILE * 128, 1024);
+    if (!EW || elect_one()) mma_ts(d_tmem, a_tmem + k * 8 + (k >= 4 ? 32 : 0), bd, IDESC, (acc || k > 0) ? 1u : 0u);
+  }
 }
 
 // Half of issue_ts: the four K steps whose A columns come from chunk `half` of
@@ -925,77 +926,80 @@ __global__ void __launch_bounds__(384, 1)
         }
       if (q_armed >= 0) mbar_wait(q_full, q_armed & 1, ctl, FA_STATUS_TIMEOUT_DRAIN);
     }
-  } else if (warp == 1) {
-    if (lane_id() == 0) {  // ---------------------------------------------- MMA issuer
-      const uint32_t qb = smem_u32(smem + L::OFF_Q), dob = smem_u32(smem + L::OFF_DO);
-      const uint32_t kb0 = smem_u32(smem + L::OFF_K), vb0 = smem_u32(smem + L::OFF_V);
-      const uint32_t tP = tmem + 256, tdQ = tmem + 384;
-      uint32_t kq = 0, dsph = 0, qn = 0;
-      auto kwait = [&](uint32_t idx) {
-        return mbar_wait(&k_full[idx % L::KST], (idx / L::KST) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
-      };
-      auto vwait = [&](uint32_t idx) {
-        return mbar_wait(&v_full[idx % L::VST], (idx / L::VST) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
-      };
-      auto kbase = [&](uint32_t idx) { return kb0 + (idx % L::KST) * L::TB; };
-      auto vbase = [&](uint32_t idx) { return vb0 + (idx % L::VST) * L::TB; };
-      for (int it = 0;; ++it) {
-        const int slot = it & 1;
-        if (!mbar_wait(&unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
-        const int u = unit_slot[slot];
-        mbar_arrive(&unit_empty[slot]);
-        if (u >= total) break;
-        int b, h, qt;
-        dq_unit_of<VL>(p, u, b, h, qt);
-        const Dims su = seq_rows<VL>(s, b).s;
-        if (qt >= q_tiles(su)) continue;  // past its (packed) sequence
-        int klo, khi;
-        const int* klist;
-        dq_keys<MASK, SP>(p, su, qt, klo, khi, klist);
-        const int n = khi - klo;
-        if (SP && n == 0) continue;
-        bool ok = mbar_wait(q_full, (qn++) & 1, ctl, FA_STATUS_TIMEOUT_MMA) && kwait(kq);
+  } else if (warp == 1) {  // -------------------------------------------------- MMA issuer
+    // The whole warp runs the issue loop converged; one elected lane issues each
+    // MMA and commit, so descriptors are formed in uniform registers.
+    const uint32_t qb = smem_u32(smem + L::OFF_Q), dob = smem_u32(smem + L::OFF_DO);
+    const uint32_t kb0 = smem_u32(smem + L::OFF_K), vb0 = smem_u32(smem + L::OFF_V);
+    const uint32_t tP = tmem + 256, tdQ = tmem + 384;
+    uint32_t kq = 0, dsph = 0, qn = 0;
+    auto kwait = [&](uint32_t idx) {
+      return warp_wait(&k_full[idx % L::KST], (idx / L::KST) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+    };
+    auto vwait = [&](uint32_t idx) {
+      return warp_wait(&v_full[idx % L::VST], (idx / L::VST) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+    };
+    auto kbase = [&](uint32_t idx) { return kb0 + (idx % L::KST) * L::TB; };
+    auto vbase = [&](uint32_t idx) { return vb0 + (idx % L::VST) * L::TB; };
+    for (int it = 0;; ++it) {
+      const int slot = it & 1;
+      if (!warp_wait(&unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) break;
+      const int u = unit_slot[slot];
+      if (elect_one()) mbar_arrive(&unit_empty[slot]);
+      if (u >= total) break;
+      int b, h, qt;
+      dq_unit_of<VL>(p, u, b, h, qt);
+      const Dims su = seq_rows<VL>(s, b).s;
+      if (qt >= q_tiles(su)) continue;  // past its (packed) sequence
+      int klo, khi;
+      const int* klist;
+      dq_keys<MASK, SP>(p, su, qt, klo, khi, klist);
+      const int n = khi - klo;
+      if (SP && n == 0) continue;
+      bool ok = warp_wait(q_full, (qn++) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+      ok = ok && kwait(kq);
+      if (!ok) break;
+      tc_fence_after();
+      issue_ss<D, true>(tmem + 0, qb, kbase(kq));            // S_0 = Q K_0^T
+      if (elect_one()) mma_commit(&s_full[0]);
+      if (!vwait(kq)) break;
+      tc_fence_after();
+      issue_ss<D, true>(tP, dob, vbase(kq));                  // dP_0 = dO V_0^T
+      if (elect_one()) mma_commit(dp_full);
+      if (n > 1) {
+        if (!kwait(kq + 1)) break;
+        tc_fence_after();
+        issue_ss<D, true>(tmem + 128, qb, kbase(kq + 1));
+        if (elect_one()) mma_commit(&s_full[1]);
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        ok = warp_wait(ds_full, dsph, ctl, FA_STATUS_TIMEOUT_MMA);
+        dsph ^= 1;
         if (!ok) break;
         tc_fence_after();
-        issue_ss<D>(tmem + 0, qb, kbase(kq));            // S_0 = Q K_0^T
-        mma_commit(&s_full[0]);
-        if (!vwait(kq)) break;
-        tc_fence_after();
-        issue_ss<D>(tP, dob, vbase(kq));                  // dP_0 = dO V_0^T
-        mma_commit(dp_full);
-        if (n > 1) {
-          if (!kwait(kq + 1)) break;
-          tc_fence_after();
-          issue_ss<D>(tmem + 128, qb, kbase(kq + 1));
-          mma_commit(&s_full[1]);
-        }
-        for (int j = 0; j < n && ok; ++j) {
-          ok = mbar_wait(ds_full, dsph, ctl, FA_STATUS_TIMEOUT_MMA);
-          dsph ^= 1;
+        issue_ts<D, true>(tdQ, tP, kbase(kq + j), j > 0);       // dQ += dS K_j
+        if (elect_one()) mma_commit(&k_empty[(kq + j) % L::KST]);
+        if (j + 1 < n) {
+          ok = vwait(kq + j + 1);
           if (!ok) break;
           tc_fence_after();
-          issue_ts<D>(tdQ, tP, kbase(kq + j), j > 0);       // dQ += dS K_j
-          mma_commit(&k_empty[(kq + j) % L::KST]);
-          if (j + 1 < n) {
-            ok = vwait(kq + j + 1);
-            if (!ok) break;
-            tc_fence_after();
-            issue_ss<D>(tP, dob, vbase(kq + j + 1));          // dP_{j+1}
-            mma_commit(dp_full);
-          }
-          if (j + 2 < n) {
-            ok = kwait(kq + j + 2);
-            if (!ok) break;
-            tc_fence_after();
-            issue_ss<D>(tmem + (j & 1) * 128, qb, kbase(kq + j + 2));
-            mma_commit(&s_full[j & 1]);
-          }
+          issue_ss<D, true>(tP, dob, vbase(kq + j + 1));          // dP_{j+1}
+          if (elect_one()) mma_commit(dp_full);
         }
-        if (!ok) break;
+        if (j + 2 < n) {
+          ok = kwait(kq + j + 2);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ss<D, true>(tmem + (j & 1) * 128, qb, kbase(kq + j + 2));
+          if (elect_one()) mma_commit(&s_full[j & 1]);
+        }
+      }
+      if (!ok) break;
+      if (elect_one()) {
         mma_commit(acc_full);
         if (L::SCRATCH) mma_commit(q_empty);
-        kq += n;
       }
+      kq += n;
     }
   } else if (warp >= 4) {  // -------------------------------------------------- gradient warps
     const int wq = warp & 3;
@@ -1133,9 +1137,9 @@ __global__ void __launch_bounds__(384, 1)
       kq += n;
     }
   }
-  // Lanes 1-31 of the producer and MMA warps had no role: they wait here for their
-  // lane 0, so that every warp reaches the block barrier converged (a barrier met by
-  // part of a warp does not hold the rest) and TMEM is freed only after all its users.
+  // Lanes 1-31 of the producer warp had no role: they wait here for their lane 0,
+  // so that every warp reaches the block barrier converged (a barrier met by part
+  // of a warp does not hold the rest) and TMEM is freed only after all its users.
   __syncwarp();
   tc_fence_before();
   __syncthreads();

@@ -317,6 +317,9 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// Run by the whole warp, converged: every wait is the warp's, and one elected
+// lane issues each MMA and commit, so the descriptors are formed once per warp in
+// uniform registers (a single diverged lane forming them issues far slower).
 template <int D, int MASK, bool F8, bool VL, bool SP, int DG>
 __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, uint32_t tmem, const FwdParams& p,
                         const Ctl& ctl) {
@@ -340,10 +343,12 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
       const uint32_t off = (k / 4) * (TILE * 128) + (k % 4) * 32;
       const uint64_t a = sdesc_sw128(q_base + t * L::QB + off, 16, 1024);
       const uint64_t bd = sdesc_sw128(k_addr + off, 16, 1024);
-      if (F8)
-        mma_ss_f8(d_tmem, a, bd, IDESC_S, k > 0);
-      else
-        mma_ss(d_tmem, a, bd, IDESC_S, k > 0);
+      if (elect_one()) {
+        if (F8)
+          mma_ss_f8(d_tmem, a, bd, IDESC_S, k > 0);
+        else
+          mma_ss(d_tmem, a, bd, IDESC_S, k > 0);
+      }
     }
   };
   // P is read from TMEM, 8 columns per product (8 x 2 bf16 or 8 x 4 E4M3 keys)
@@ -353,23 +358,25 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
 #pragma unroll
     for (int k = 0; k < TILE / KS; ++k) {
       const uint64_t bd = sdesc_sw128(v_addr + k * KS * 128, TILE * 128, 1024);
-      if (F8)
-        mma_ts_f8(d_tmem, p_tmem + k * 8, bd, IDESC_O, (acc || k > 0) ? 1u : 0u);
-      else
-        mma_ts(d_tmem, p_tmem + k * 8, bd, IDESC_O, (acc || k > 0) ? 1u : 0u);
+      if (elect_one()) {
+        if (F8)
+          mma_ts_f8(d_tmem, p_tmem + k * 8, bd, IDESC_O, (acc || k > 0) ? 1u : 0u);
+        else
+          mma_ts(d_tmem, p_tmem + k * 8, bd, IDESC_O, (acc || k > 0) ? 1u : 0u);
+      }
     }
   };
   auto group_wait = [&](uint32_t gq) {
-    return mbar_wait(&bar.kv_full[gq % L::NG], (gq / L::NG) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+    return warp_wait(&bar.kv_full[gq % L::NG], (gq / L::NG) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
   };
   auto group_base = [&](uint32_t gq) { return kv_base + (gq % L::NG) * 2 * L::TB; };
 
   const int total = fwd_total<VL>(p);
   for (int it = 0;; ++it) {
     const int slot = it & 1;
-    if (!mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) return;
+    if (!warp_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT)) return;
     const int u = unit_slot[slot];
-    if (!SP || u >= total) mbar_arrive(&bar.unit_empty[slot]);  // block-sparse: after the unit
+    if ((!SP || u >= total) && elect_one()) mbar_arrive(&bar.unit_empty[slot]);  // block-sparse: after the unit
     if (u >= total) return;
     int b, h, pr;
     fwd_unit_of<VL>(p, u, b, h, pr);
@@ -379,7 +386,7 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
     int a[2] = {ut.a[0], ut.a[1]}, e[2] = {ut.a[0] + ut.n[0], ut.a[1] + ut.n[1]}, nt[2] = {ut.n[0], ut.n[1]};
     SpList sl{};
     if (SP) {
-      if (!mbar_wait(&bar.list_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+      if (!warp_wait(&bar.list_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
       sl = sp_list<L::MAXL>(smem + L::OFF_LIST + slot * L::LIST);
       nmax = sl.hdr[0];
       for (int t = 0; t < 2; ++t) {
@@ -390,24 +397,26 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
     }
     auto on = [&](int t, int j) { return SP ? ((sl.act[j] >> t) & 1) != 0 : (j >= a[t] && j < e[t]); };
     if (SKIP && nmax == 0) {  // no key tile for either query tile
-      if (SP) mbar_arrive(&bar.unit_empty[slot]);
+      if (SP && elect_one()) mbar_arrive(&bar.unit_empty[slot]);
       continue;
     }
 
-    if (!mbar_wait(bar.q_full, (SKIP ? qn++ : static_cast<uint32_t>(it)) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+    if (!warp_wait(bar.q_full, (SKIP ? qn++ : static_cast<uint32_t>(it)) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
     unsigned long long* rec = DG == DG_TRACE ? p.trace + TRACE_UNIT0 + static_cast<int64_t>(u) * TRACE_UNIT_WORDS : nullptr;
     // group 0: K of local step 0
     {
       if (!group_wait(seq)) return;
-      if (rec) rec[1] = globaltimer();
+      if (rec && lane_id() == 0) rec[1] = globaltimer();
       tc_fence_after();
       for (int t = 0; t < 2; ++t)
         if (nt[t] > 0 && on(t, 0)) {
           issue_s(t, group_base(seq) + L::TB);
-          mma_commit(&bar.s_full[t]);
+          if (elect_one()) mma_commit(&bar.s_full[t]);
         }
-      if (nmax == 1) mma_commit(bar.q_empty);
-      mma_commit(&bar.kv_empty[seq % L::NG]);
+      if (elect_one()) {
+        if (nmax == 1) mma_commit(bar.q_empty);
+        mma_commit(&bar.kv_empty[seq % L::NG]);
+      }
     }
     for (int j = 0; j < nmax; ++j) {
       const uint32_t gq = seq + 1 + j;  // group j+1: V_j, and K_{j+1} unless this is the last step
@@ -416,27 +425,29 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
       for (int t = 0; t < 2; ++t) {
         const bool now = on(t, j);
         if (now) {
-          if (j == a[t] && !mbar_wait(&bar.o_empty[t], (active[t] & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
-          if (!mbar_wait(&bar.p_full[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
+          if (j == a[t] && !warp_wait(&bar.o_empty[t], (active[t] & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+          if (!warp_wait(&bar.p_full[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
           pph[t] ^= 1;
           tc_fence_after();
           issue_pv(t, v_addr, j > a[t]);
-          if (j == e[t] - 1) mma_commit(&bar.o_full[t]);
+          if (j == e[t] - 1 && elect_one()) mma_commit(&bar.o_full[t]);
         }
         if (j + 1 < nmax && on(t, j + 1)) {  // S of the tile's next step (its first, when it starts late)
           if (!now) tc_fence_after();         // no P V of this tile in this step fenced the group wait
           issue_s(t, k_addr);
-          mma_commit(&bar.s_full[t]);
+          if (elect_one()) mma_commit(&bar.s_full[t]);
         }
       }
-      if (j + 1 == nmax - 1) mma_commit(bar.q_empty);
-      mma_commit(&bar.kv_empty[gq % L::NG]);
+      if (elect_one()) {
+        if (j + 1 == nmax - 1) mma_commit(bar.q_empty);
+        mma_commit(&bar.kv_empty[gq % L::NG]);
+      }
     }
-    if (rec) rec[2] = globaltimer();
+    if (rec && lane_id() == 0) rec[2] = globaltimer();
     for (int t = 0; t < 2; ++t)
       if (nt[t] > 0) ++active[t];
     seq += nmax + 1;
-    if (SP) mbar_arrive(&bar.unit_empty[slot]);
+    if (SP && elect_one()) mbar_arrive(&bar.unit_empty[slot]);
   }
 }
 
@@ -867,7 +878,7 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     if (lane_id() == 0) fwd_producer<D, MASK, F8, VL, SP, DG>(smem, bar, unit_slot, &tm_q, &tm_k, &tm_v, p, sched, ctl);
   } else if (warp == 1) {
-    if (lane_id() == 0) fwd_mma<D, MASK, F8, VL, SP, DG>(smem, bar, unit_slot, tmem, p, ctl);
+    fwd_mma<D, MASK, F8, VL, SP, DG>(smem, bar, unit_slot, tmem, p, ctl);
   } else if (SP && warp == 2) {
     fwd_sparse_lists<D, MASK>(smem, bar, unit_slot, p, ctl);
   } else if (warp >= 4) {
@@ -877,9 +888,9 @@ __global__ void __launch_bounds__(384, 1)
   }
   // the CTA's end: the last role to finish (each warp's lane 0 stamps its exit)
   if (DG == DG_TRACE && lane_id() == 0) atomicMax(p.trace + 4 * blockIdx.x + 1, globaltimer());
-  // Lanes 1-31 of the producer and MMA warps had no role: they wait here for their
-  // lane 0, so that every warp reaches the block barrier converged (the barrier is
-  // the aligned form, which assumes whole warps) and TMEM is freed after all its users.
+  // Lanes 1-31 of the producer warp had no role: they wait here for their lane 0,
+  // so that every warp reaches the block barrier converged (the barrier is the
+  // aligned form, which assumes whole warps) and TMEM is freed after all its users.
   __syncwarp();
   tc_fence_before();
   __syncthreads();

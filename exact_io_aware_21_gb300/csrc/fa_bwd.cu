@@ -289,10 +289,13 @@ struct DkvLayout {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TB;
   static constexpr int OFF_ST = 2 * TB;
+  // S^T buffers: at d = 64, TMEM's last 128 columns hold a second one, so the
+  // S^T of an iteration two ahead is computed while this one's P^T is still in use
+  static constexpr int SB = D == 64 ? 2 : 1;
   static constexpr int OFF_BAR = OFF_ST + STAGES * STAGE;
-  // unit_full[2] unit_empty[2] kv_full kv_empty st_full[S] st_empty[S] s_full dp_full p_full[2] ds_full
+  // unit_full[2] unit_empty[2] kv_full kv_empty st_full[S] st_empty[S] s_full[2] dp_full p_full[2] ds_full
   // acc_full
-  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 6;
+  static constexpr int NBAR = 4 + 2 + 2 * STAGES + 7;
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
   // row-store scratch, one per gradient warp; 1024-byte aligned, so that each warp's
@@ -319,11 +322,11 @@ __device__ __forceinline__ DkvBars dkv_bars(uint8_t* smem) {
   r.kv_empty = b + 5;
   r.st_full = b + 6;
   r.st_empty = r.st_full + L::STAGES;
-  r.s_full = r.st_empty + L::STAGES;
-  r.dp_full = r.s_full + 1;
-  r.p_full = r.s_full + 2;   // [2]: one per 32-column chunk of each warpgroup's half
-  r.ds_full = r.s_full + 4;
-  r.acc_full = r.s_full + 5;
+  r.s_full = r.st_empty + L::STAGES;  // [2]: one per S^T buffer
+  r.dp_full = r.s_full + 2;
+  r.p_full = r.s_full + 3;   // [2]: one per 32-column chunk of each warpgroup's half
+  r.ds_full = r.s_full + 5;
+  r.acc_full = r.s_full + 6;
   return r;
 }
 
@@ -428,7 +431,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar.st_full[i], 1);
       mbar_init(&bar.st_empty[i], 1);
     }
-    mbar_init(bar.s_full, 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&bar.s_full[i], 1);
     mbar_init(bar.dp_full, 1);
     for (int i = 0; i < 2; ++i) mbar_init(&bar.p_full[i], 8);
     mbar_init(bar.ds_full, 8);
@@ -507,7 +510,8 @@ __global__ void __launch_bounds__(384, 1)
     // MMA and commit, so descriptors are formed in uniform registers.
     const uint32_t kb = smem_u32(smem + L::OFF_K), vb = smem_u32(smem + L::OFF_V);
     const uint32_t stb = smem_u32(smem + L::OFF_ST);
-    const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+    const uint32_t tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 256 + D;
+    auto tS = [&](uint32_t q) { return tmem + ((L::SB == 2 && (q & 1)) ? 384u : 0u); };  // S^T of iteration q
     uint32_t sq = 0, pph = 0, dph = 0, un = 0;
     for (int it = 0;; ++it) {
       const int slot = it & 1;
@@ -523,12 +527,19 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       {
         const uint32_t qb = stb + (sq % L::STAGES) * L::STAGE;
-        issue_ss<D, true>(tS, kb, qb);           // S^T = K Q^T
-        if (elect_one()) mma_commit(bar.s_full);
+        issue_ss<D, true>(tS(sq), kb, qb);       // S^T = K Q^T
+        if (elect_one()) mma_commit(&bar.s_full[sq & (L::SB - 1)]);
         issue_ss<D, true>(tP, vb, qb + L::TB);   // dP^T = V dO^T
         if (elect_one()) {
           mma_commit(bar.dp_full);
           if (w.n_it == 1) mma_commit(bar.kv_empty);  // K and V are read by S and dP only
+        }
+        if (L::SB == 2 && w.n_it > 1) {  // the second iteration's S^T, into the other buffer
+          ok = warp_wait(&bar.st_full[(sq + 1) % L::STAGES], ((sq + 1) / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
+          if (!ok) break;
+          tc_fence_after();
+          issue_ss<D, true>(tS(sq + 1), kb, stb + ((sq + 1) % L::STAGES) * L::STAGE);
+          if (elect_one()) mma_commit(&bar.s_full[(sq + 1) & 1]);
         }
       }
       for (int k = 0; k < w.n_it && ok; ++k) {
@@ -537,22 +548,21 @@ __global__ void __launch_bounds__(384, 1)
         ok = warp_wait(&bar.p_full[0], pph, ctl, FA_STATUS_TIMEOUT_MMA);
         if (!ok) break;
         tc_fence_after();
-        issue_ts_half<D, 0, true>(tdV, tS, cur + L::TB, k > 0);
+        issue_ts_half<D, 0, true>(tdV, tS(sq + k), cur + L::TB, k > 0);
         ok = warp_wait(&bar.p_full[1], pph, ctl, FA_STATUS_TIMEOUT_MMA);
         pph ^= 1;
         if (!ok) break;
         tc_fence_after();
-        issue_ts_half<D, 1, true>(tdV, tS, cur + L::TB, true);
+        issue_ts_half<D, 1, true>(tdV, tS(sq + k), cur + L::TB, true);
         const bool more = k + 1 < w.n_it;
-        uint32_t nxt = 0;
-        if (more) {
-          const uint32_t nsq = sq + k + 1;
+        const uint32_t nxt = stb + ((sq + k + 1) % L::STAGES) * L::STAGE;  // (used when more)
+        if (k + L::SB < w.n_it) {  // S^T of the iteration SB ahead, into the buffer this dV has read
+          const uint32_t nsq = sq + k + L::SB;
           ok = warp_wait(&bar.st_full[nsq % L::STAGES], (nsq / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_MMA);
           if (!ok) break;
           tc_fence_after();
-          nxt = stb + (nsq % L::STAGES) * L::STAGE;
-          issue_ss<D, true>(tS, kb, nxt);
-          if (elect_one()) mma_commit(bar.s_full);
+          issue_ss<D, true>(tS(nsq), kb, stb + (nsq % L::STAGES) * L::STAGE);
+          if (elect_one()) mma_commit(&bar.s_full[nsq & (L::SB - 1)]);
         }
         // dK += dS^T Q (whole: a second hand-off here costs more than it overlaps)
         ok = warp_wait(bar.ds_full, dph, ctl, FA_STATUS_TIMEOUT_MMA);
@@ -582,10 +592,9 @@ __global__ void __launch_bounds__(384, 1)
     const int c0 = ((warp - 4) >> 2) * 64;  // this warpgroup's first column
     const int r = wq * 32 + lane_id();      // key row within the tile
     const uint32_t lanes = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lanes, tP = tmem + lanes + 128, tdV = tmem + lanes + 256,
-                   tdK = tmem + lanes + 256 + D;
+    const uint32_t tP = tmem + lanes + 128, tdV = tmem + lanes + 256, tdK = tmem + lanes + 256 + D;
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
-    uint32_t sq = 0, sph = 0, dph = 0, un = 0;
+    uint32_t sq = 0, sph[2] = {0, 0}, dph = 0, un = 0;
     for (int it = 0;; ++it) {
       const int slot = it & 1;
       bool ok = mbar_wait(&bar.unit_full[slot], (it >> 1) & 1, ctl, FA_STATUS_TIMEOUT_UNIT);
@@ -626,9 +635,11 @@ __global__ void __launch_bounds__(384, 1)
         // rows (keys) see only part of the tile's queries: the band's edges, or causal's diagonal
         const bool part = MASK == MASK_BAND ? (qi < qfull_lo || qi > qfull_hi)
                                             : (MASK == MASK_CAUSAL && qi == w.kt);
+        const int sb = q & (L::SB - 1);  // this iteration's S^T buffer
+        const uint32_t tS = tmem + lanes + (sb ? 384u : 0u);
         ok = mbar_wait(&bar.st_full[q % L::STAGES], (q / L::STAGES) & 1, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
-        ok = ok && mbar_wait(bar.s_full, sph, ctl, FA_STATUS_TIMEOUT_SOFTMAX);
-        sph ^= 1;
+        ok = ok && mbar_wait(&bar.s_full[sb], sph[sb], ctl, FA_STATUS_TIMEOUT_SOFTMAX);
+        sph[sb] ^= 1;
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;

@@ -15,8 +15,9 @@
 //               K/V head; it loops over the query heads of the group and their
 //               query tiles (causal: only tiles at or below the diagonal).
 //               TMEM: S^T [0,128) dP^T [128,256) dV [256,256+d) dK [256+d,..);
-//               P^T and dS^T are written back over S^T and dP^T as bf16 and
-//               feed the dV and dK products from TMEM.
+//               at d = 64 a second S^T buffer [384,512) takes every other
+//               iteration.  P^T and dS^T are written back over S^T and dP^T as
+//               bf16 and feed the dV and dK products from TMEM.
 //   dQ          a unit is one 128-row query tile; it loops over key tiles.
 //   Dense path: the three follow a header-clearing kernel, each launched with
 //   programmatic stream serialisation: it sets up while the one before it

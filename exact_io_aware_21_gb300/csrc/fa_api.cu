@@ -374,7 +374,23 @@ int fa_get_device_status(void* ws, void* stream, int* status) {
 }
 
 // ------------------------------------------------------------------------ forward
-size_t fa_fwd_workspace_size(const fa_shape_t* s) { return check_shape(s) == FA_OK ? FA_WS_HEADER_BYTES : 0; }
+// Bytes of key-split partials an unmasked dense forward needs on this device (0:
+// it runs no split units), and the plan they come from.
+size_t fwd_split_bytes(const fa_shape_t* s, FwdSplit* plan) {
+  const Dims dm = dims_of(s);
+  if (mask_kind(dm) != MASK_NONE) return 0;
+  int sms = 0;
+  if (device_info(&sms) != FA_OK) return 0;
+  const FwdSplit sp = fwd_split_plan(dm, sms);
+  if (sp.nsplit < 2) return 0;
+  if (plan) *plan = sp;
+  const size_t rows = static_cast<size_t>(fwd_units(dm) - sp.split0) * sp.nsplit * 2 * TILE;
+  return round_up(rows * sizeof(float), 256) + rows * s->d * sizeof(float);
+}
+
+size_t fa_fwd_workspace_size(const fa_shape_t* s) {
+  return check_shape(s) == FA_OK ? FA_WS_HEADER_BYTES + fwd_split_bytes(s, nullptr) : 0;
+}
 
 // Packed variable-length sequences: the cu arrays (device) and the longest
 // lengths; shape Nq / Nk are then the packed tensors' token counts.
@@ -465,6 +481,15 @@ int fwd_impl(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, c
   }
   if (pk) a.plan = reinterpret_cast<int*>(static_cast<char*>(ws) + FA_WS_HEADER_BYTES);
   if (!pk && !sp) a.sched = causal_schedule(a.dims, s->d, false, imax(1, imin(fwd_units(a.dims), sms)));
+  FwdSplit split{0, 1};
+  if (!pk && !sp && fwd_split_bytes(s, &split) > 0) {  // the last wave's units run as key-split parts
+    const size_t rows = static_cast<size_t>(fwd_units(a.dims) - split.split0) * split.nsplit * 2 * TILE;
+    char* base = static_cast<char*>(ws) + FA_WS_HEADER_BYTES;
+    a.split0 = split.split0;
+    a.nsplit = split.nsplit;
+    a.part_lse = reinterpret_cast<float*>(base);
+    a.part_o = reinterpret_cast<float*>(base + round_up(rows * sizeof(float), 256));
+  }
   if (g_trace && !pk && !sp && s->d == 128 && sms <= TRACE_MAX_CTAS &&
       g_trace_bytes >= sizeof(unsigned long long) *
                            (TRACE_UNIT0 + static_cast<size_t>(fwd_units(a.dims)) * TRACE_UNIT_WORDS)) {

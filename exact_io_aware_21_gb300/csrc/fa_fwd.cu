@@ -130,6 +130,9 @@ struct FwdParams {
   int total_units;
   unsigned long long* trace;  // optional timestamps (see TRACE_UNIT0)
   int tma_out;                // O (and its residual) leave through TMA stores (dense)
+  int split0, nsplit;         // key-split units: items from split0 on are parts (see FwdLaunch)
+  float* part_o;
+  float* part_lse;
 };
 
 struct Bars {
@@ -208,13 +211,28 @@ __device__ __forceinline__ unsigned long long* trace_unit(const FwdParams& p, in
   return p.trace + TRACE_UNIT0 + static_cast<int64_t>(fwd_unit_index(p.dims, b, h, pr)) * TRACE_UNIT_WORDS;
 }
 
-// The unit's (b, h, pair): dense order, or the packed sequences' plan.
+// The unit's (b, h, pair): dense order (a key-split part: its unit's), or the
+// packed sequences' plan.
 template <bool VL>
 __device__ __forceinline__ void fwd_unit_of(const FwdParams& p, int u, int& b, int& h, int& pr) {
   if (VL)
     plan_unit(p.plan, p.dims.Hq, u, b, h, pr);
   else
-    fwd_unit(p.dims, u, b, h, pr);
+    fwd_unit(p.dims, u < p.split0 ? u : p.split0 + (u - p.split0) / p.nsplit, b, h, pr);
+}
+
+// A key-split part (work item u >= split0 of an unmasked dense forward) streams
+// only its share of the key tiles: part k of nsplit covers [k nk / nsplit,
+// (k + 1) nk / nsplit) of the unit's nk.
+template <int MASK, bool VL, bool SP>
+__device__ __forceinline__ void split_tiles(const FwdParams& p, int u, UnitTiles& ut) {
+  if (MASK != MASK_NONE || VL || SP || u < p.split0) return;
+  const int k = (u - p.split0) % p.nsplit, nk = ut.nu;
+  const int lo = k * nk / p.nsplit, hi = (k + 1) * nk / p.nsplit;
+  ut.base = lo;
+  ut.nu = hi - lo;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) ut.n[t] = ut.n[t] > 0 ? hi - lo : 0;
 }
 
 template <bool VL>
@@ -242,7 +260,7 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
     } else {
       u = atomicAdd(p.counter, 1);
     }
-    if (DG == DG_TRACE && u < total) {
+    if (DG == DG_TRACE && u < total && u < p.split0) {  // (key-split parts are not traced)
       unsigned long long* rec = p.trace + TRACE_UNIT0 + static_cast<int64_t>(u) * TRACE_UNIT_WORDS;
       rec[0] = globaltimer();
       rec[3] = 0;
@@ -255,7 +273,8 @@ __device__ void fwd_producer(uint8_t* smem, const Bars& bar, int* unit_slot, con
     int b, h, pr;
     fwd_unit_of<VL>(p, u, b, h, pr);
     const SeqRows sr = seq_rows<VL>(p.dims, b);
-    const UnitTiles ut = unit_tiles<MASK>(VL ? sr.s : p.dims, pr);
+    UnitTiles ut = unit_tiles<MASK>(VL ? sr.s : p.dims, pr);
+    split_tiles<MASK, VL, SP>(p, u, ut);
     int nmax = ut.nu;
     SpList sl{};
     if (SP) {  // the unit's key tiles, from the list warp 2 built
@@ -380,7 +399,8 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
     if (u >= total) return;
     int b, h, pr;
     fwd_unit_of<VL>(p, u, b, h, pr);
-    const UnitTiles ut = unit_tiles<MASK>(VL ? seq_rows<VL>(p.dims, b).s : p.dims, pr);
+    UnitTiles ut = unit_tiles<MASK>(VL ? seq_rows<VL>(p.dims, b).s : p.dims, pr);
+    split_tiles<MASK, VL, SP>(p, u, ut);
     int nmax = ut.nu;
     // tile t is active at local steps [a[t], e[t]) (block-sparse: the steps its bit marks)
     int a[2] = {ut.a[0], ut.a[1]}, e[2] = {ut.a[0] + ut.n[0], ut.a[1] + ut.n[1]}, nt[2] = {ut.n[0], ut.n[1]};
@@ -402,7 +422,8 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
     }
 
     if (!warp_wait(bar.q_full, (SKIP ? qn++ : static_cast<uint32_t>(it)) & 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
-    unsigned long long* rec = DG == DG_TRACE ? p.trace + TRACE_UNIT0 + static_cast<int64_t>(u) * TRACE_UNIT_WORDS : nullptr;
+    unsigned long long* rec =
+        DG == DG_TRACE && u < p.split0 ? p.trace + TRACE_UNIT0 + static_cast<int64_t>(u) * TRACE_UNIT_WORDS : nullptr;
     // group 0: K of local step 0
     {
       if (!group_wait(seq)) return;
@@ -503,7 +524,9 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
     const SeqRows sr = seq_rows<VL>(s, b);
     if (VL && !sr.ok && t == 0 && wq == 0 && lane_id() == 0) report(ctl, FA_STATUS_BAD_INPUT);
     const Dims& su = VL ? sr.s : s;  // this unit's sequence (packed), else the problem
-    const UnitTiles ut = unit_tiles<MASK>(su, pr);
+    UnitTiles ut = unit_tiles<MASK>(su, pr);
+    split_tiles<MASK, VL, SP>(p, u, ut);
+    const bool part = MASK == MASK_NONE && !VL && !SP && u >= p.split0;  // a key-split part
     int n = ut.n[t];
     const int qt = 2 * pr + t;
     SpList sl{};
@@ -582,9 +605,10 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
           for (int i = 0; i < 128; ++i)
             if (i >= hi || i < lo) sv[i] = -INFINITY;
         }
-      } else if (j == n - 1 && (MASK == MASK_CAUSAL || (nk_u % TILE) != 0)) {
-        // the last tile: keys at or past Nk, and under j <= i keys past the row
-        int lim = nk_u - j * TILE;
+      } else if (MASK == MASK_CAUSAL ? j == n - 1 : ((nk_u % TILE) != 0 && kt0 + j == cdiv(nk_u, TILE) - 1)) {
+        // the last tile: keys at or past Nk, and under j <= i keys past the row (a
+        // key-split part starts at key tile kt0 and holds the last tile only if it ends there)
+        int lim = nk_u - (kt0 + j) * TILE;
         if (MASK == MASK_CAUSAL) lim = imin(lim, q_row - j * TILE + 1);
 #pragma unroll
         for (int i = 0; i < 128; ++i)
@@ -663,6 +687,25 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
     tc_fence_after();
     const float inv_l = (F8 ? p.sv[static_cast<int64_t>(b) * s.Hkv + kvh] : 1.f) / l_run;
     const float2 il2 = make_float2(inv_l, inv_l);
+    if (part) {  // a key-split part: its O / l (fp32) and LSE go to the workspace for the combine
+      const int64_t prow = (static_cast<int64_t>(u - p.split0) * 2 + t) * TILE + r;
+      float4* po = reinterpret_cast<float4*>(p.part_o + prow * D);
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 a = __fmul2_rn(f32x2(o[4 * i], o[4 * i + 1]), il2);
+          const float2 c2 = __fmul2_rn(f32x2(o[4 * i + 2], o[4 * i + 3]), il2);
+          po[cc * 8 + i] = make_float4(a.x, a.y, c2.x, c2.y);
+        }
+      }
+      p.part_lse[prow] = (m_run + __log2f(l_run)) * LN2;
+      tc_fence_before();
+      warp_arrive(&bar.o_empty[t]);
+      continue;
+    }
     const bool live = q_row < nq_u;
     const int q0 = qt * TILE + wq * 32;  // this warp's first row (within its sequence)
     const int64_t orow = qoff + q0;      // ... and in the tensor
@@ -865,6 +908,9 @@ __global__ void __launch_bounds__(384, 1)
   // the set-up above touches only this CTA's own memory; from here on the kernel
   // reads the workspace header the previous kernel cleared, and the inputs
   griddep_wait();
+  // a kernel queued behind this one with programmatic serialisation (the key-split
+  // combine) may be scheduled now; it waits for this grid's completion itself
+  griddep_launch_dependents();
   if (DG == DG_TRACE) {
     if (threadIdx.x == 0) {
       p.trace[4 * blockIdx.x] = globaltimer();
@@ -900,6 +946,78 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// ------------------------------------------------------------------ key-split combine
+// The nsplit parts' LSE-weighted sum (each part's O is normalised by its own sum),
+// as the decode path combines its splits: LSE = log sum_k e^{LSE_k},
+// O = sum_k e^{LSE_k - LSE} O_k.  A thread takes 8 columns of one row, so its
+// loads (every part's LSE and columns) are all in flight at once.  Writes O
+// (bf16), its rounding residual when asked for, and LSE.  Launched right behind
+// the forward with programmatic serialisation: it waits for the forward's results.
+template <int D>
+__global__ void __launch_bounds__(128) fwd_split_combine_kernel(const FwdParams p) {
+  constexpr int CPR = D / 8, RPB = 128 / CPR;  // 8-column chunks per row, rows per block
+  griddep_wait();
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * RPB + threadIdx.x / CPR;  // (unit, tile, row) of the splits
+  const int c = (threadIdx.x % CPR) * 8;
+  const int su = static_cast<int>(g / (2 * TILE)), t = static_cast<int>((g / TILE) & 1), r = static_cast<int>(g % TILE);
+  int b, h, pr;
+  fwd_unit(p.dims, p.split0 + su, b, h, pr);
+  const int row = (2 * pr + t) * TILE + r;
+  if (row >= p.dims.Nq) return;
+  const int ns = p.nsplit;
+  float l[4], w[4];
+  float4 x0[4], x1[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // nsplit <= 4
+    if (k < ns) {
+      const int64_t pr_k = (static_cast<int64_t>(su * ns + k) * 2 + t) * TILE + r;
+      l[k] = p.part_lse[pr_k];
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + pr_k * D + c);
+      x0[k] = src[0];
+      x1[k] = src[1];
+    }
+  }
+  float mx = l[0];
+#pragma unroll
+  for (int k = 1; k < 4; ++k)
+    if (k < ns) mx = fmaxf(mx, l[k]);
+  float wsum = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (k < ns) {
+      w[k] = expf(l[k] - mx);
+      wsum += w[k];
+      acc[0] += w[k] * x0[k].x;
+      acc[1] += w[k] * x0[k].y;
+      acc[2] += w[k] * x0[k].z;
+      acc[3] += w[k] * x0[k].w;
+      acc[4] += w[k] * x1[k].x;
+      acc[5] += w[k] * x1[k].y;
+      acc[6] += w[k] * x1[k].z;
+      acc[7] += w[k] * x1[k].w;
+    }
+  }
+  const float inv = 1.f / wsum;
+  uint32_t ob[4], rb[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float v0 = acc[2 * i] * inv, v1 = acc[2 * i + 1] * inv;
+    ob[i] = pack_bf16(v0, v1);
+    const float2 hv = unpack_bf16(ob[i]);
+    rb[i] = pack_bf16(v0 - hv.x, v1 - hv.y);
+  }
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.o.ptr) + b * p.o.sb + static_cast<int64_t>(row) * p.o.sn +
+                     h * p.o.sh + c;
+  *reinterpret_cast<uint4*>(o) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  if (p.o_res.ptr != nullptr) {
+    __nv_bfloat16* res = reinterpret_cast<__nv_bfloat16*>(p.o_res.ptr) + b * p.o_res.sb +
+                         static_cast<int64_t>(row) * p.o_res.sn + h * p.o_res.sh + c;
+    *reinterpret_cast<uint4*>(res) = make_uint4(rb[0], rb[1], rb[2], rb[3]);
+  }
+  if (c == 0) p.lse[(static_cast<int64_t>(b) * p.dims.Hq + h) * p.dims.Nq + row] = mx + logf(wsum);
+}
+
 template <int D, int MASK, bool F8 = false, bool VL = false, bool SP = false, int DG = DG_NONE>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   using L = FwdLayout<D, F8, SP>;
@@ -931,6 +1049,12 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   p.counter = a.counter;
   p.timeout_ns = a.timeout_ns;
   p.total_units = fwd_units(a.dims);
+  const bool split = MASK == MASK_NONE && !F8 && !VL && !SP && a.nsplit > 1;
+  p.split0 = split ? a.split0 : p.total_units;
+  p.nsplit = split ? a.nsplit : 1;
+  p.part_o = a.part_o;
+  p.part_lse = a.part_lse;
+  if (split) p.total_units = a.split0 + (p.total_units - a.split0) * a.nsplit;
   const int grid = imax(1, imin(p.total_units, a.num_sms));
   p.trace = DG == DG_TRACE ? a.trace : nullptr;  // the host sets a.trace only when the grid fits TRACE_MAX_CTAS
   FwdSched sched;
@@ -949,7 +1073,14 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, p, sched, a.tm_o, a.tm_r);
+  e = cudaLaunchKernelEx(&cfg, kern, a.tm_q, a.tm_k, a.tm_v, p, sched, a.tm_o, a.tm_r);
+  if (e != cudaSuccess || !split) return e;
+  // the combine, queued behind the forward with programmatic serialisation (its
+  // CTAs wait in griddepcontrol.wait until the forward's parts are written)
+  cfg.gridDim = dim3((fwd_units(a.dims) - a.split0) * 2 * TILE / (128 / (D / 8)));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&cfg, fwd_split_combine_kernel<D>, p);
 }
 
 // Zero a workspace header (status word, counters) and let the kernel after it

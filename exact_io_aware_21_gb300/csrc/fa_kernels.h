@@ -61,7 +61,21 @@ struct FwdLaunch {
   unsigned long long* trace;  // timestamps (diag == DG_TRACE); layout below
   int diag;                   // DG_NONE, or a diagnostic instantiation (below)
   const FwdSched* sched;      // static schedule (causal), or nullptr: dynamic claims
+  // key-split units (dense bf16 forward without a mask, nsplit > 1): units from
+  // split0 on run as nsplit parts along the keys, each writing its O (normalised
+  // by its own sum, fp32 [part][2 tiles][128 rows][d]) and LSE ([part][2][128])
+  // to part_o / part_lse; a combine kernel then writes O, its residual and LSE
+  int split0, nsplit;
+  float* part_o;
+  float* part_lse;
 };
+// The key-split plan of a forward (dense, bf16, no mask, no block-sparse table):
+// the units of the last, partial wave of SMs (all units when there are fewer
+// than SMs) split into nsplit parts of whole key tiles.  nsplit = 1: none.
+struct FwdSplit {
+  int split0, nsplit;
+};
+FwdSplit fwd_split_plan(const Dims& s, int sms);
 // Diagnostic instantiations of the dense bf16 d = 128 forward: DG_TRACE writes
 // timestamps into `trace`; DG_WITHHOLD (tests of the bounded waits) has one softmax
 // warp of work unit 0 skip its first P hand-off, so that CTA's MMA issuer's wait runs out.

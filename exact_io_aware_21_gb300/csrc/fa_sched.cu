@@ -112,6 +112,25 @@ void build(const Dims& s, int d, bool fp8, int grid, FwdSched* out) {
 
 }  // namespace
 
+// Key-split plan of an unmasked forward.  Its units all cost the same, so with U
+// units on `sms` SMs the last wave holds R = U mod sms of them (all U when U <
+// sms) and the launch lasts ceil(U / sms) units while the SMs average U / sms.
+// Splitting those R units along the keys into f = floor(sms / R) parts (at most
+// 4, each of at least two key tiles) lets the last wave fill the SMs: it then
+// lasts 1/f of a unit.  The parts' outputs are merged by LSE afterwards.
+FwdSplit fwd_split_plan(const Dims& s, int sms) {
+  const int U = fwd_units(s), nk = k_tiles(s);
+  FwdSplit r{U, 1};
+  if (mask_kind(s) != MASK_NONE || s.cu_q != nullptr || sms < 2 || U < 1) return r;
+  const int R = U >= sms ? U % sms : U;
+  if (R == 0) return r;
+  const int f = std::min(std::min(sms / R, 4), nk / 2);
+  if (f < 2) return r;
+  r.split0 = U - R;
+  r.nsplit = f;
+  return r;
+}
+
 const FwdSched* causal_schedule(const Dims& s, int d, bool fp8, int grid) {
   if (mask_kind(s) != MASK_CAUSAL || s.cu_q != nullptr) return nullptr;
   const int n = fwd_units(s);

@@ -115,11 +115,18 @@ typedef struct {
  *   o_residual [B, Nq, Hq, d]  optional out (NULL = not written): the bf16
  *       rounding residual of O, i.e. bf16(O_fp32 - O).  O + o_residual carries
  *       about 16 significant bits; fa_bwd uses it for D (see there).
- * Needs fa_fwd_workspace_size(shape) bytes of workspace (16-byte aligned).
- * Enqueues two kernels: one that clears the workspace header, then the forward,
- * launched with programmatic stream serialisation so that its CTAs set up
- * shared memory and TMEM while the first still runs (they touch global memory
- * only after it has finished).  The forward calls below do the same.
+ * Needs fa_fwd_workspace_size(shape) bytes of workspace (16-byte aligned); for
+ * a shape without a mask (not causal, no window) the size depends on the
+ * current device's SM count, so size the workspace on the device that runs the
+ * call.  Enqueues two kernels: one that clears the workspace header, then the
+ * forward, launched with programmatic stream serialisation so that its CTAs set
+ * up shared memory and TMEM while the first still runs (they touch global
+ * memory only after it has finished).  The forward calls below do the same.
+ * Without a mask, when the work units do not fill the last wave of SMs (or
+ * there are fewer units than SMs), the units of that wave run as 2-4 parts
+ * along the keys (flash-decoding's split, here for a prefill), each writing its
+ * normalised O and LSE to the workspace, and a third kernel merges the parts
+ * by their LSE into O, the residual and LSE.
  * ------------------------------------------------------------------------- */
 size_t fa_fwd_workspace_size(const fa_shape_t* shape);
 int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,

@@ -69,6 +69,10 @@ def test_random_tables(B, Hq, Hkv, Nq, Nk, d, causal, density):
 
 @pytest.mark.parametrize("causal,d", [(False, 64), (True, 128)])
 def test_every_tile_listed_equals_the_dense_kernel(causal, d):
+    """With every tile listed the block-sparse kernel does the dense kernel's work:
+    bit for bit where the dense call runs whole units (causal).  Without a mask the
+    dense call splits this small grid's units along the keys and merges the parts
+    by their LSE, so there both are held to the exact result instead."""
     N = 1000
     x = inputs.shape_inputs(2, 4, 2, N, N, d, seed=3, with_do=False)
     nt = -(-N // 128)
@@ -76,7 +80,12 @@ def test_every_tile_listed_equals_the_dense_kernel(causal, d):
     q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
     o2, lse2, res2 = fa.forward(q, k, v, causal=causal, scale=0.1, residual=True)
     torch.cuda.synchronize()
-    assert torch.equal(o, o2) and torch.equal(lse, lse2) and torch.equal(res, res2)
+    if causal:
+        assert torch.equal(o, o2) and torch.equal(lse, lse2) and torch.equal(res, res2)
+    else:
+        o_ref, lse_ref = A.attention_forward(x["q"], x["k"], x["v"], 0.1, False)
+        assert_fwd(o, lse, o_ref, lse_ref, "block-sparse, every tile listed", o_res=res)
+        assert_fwd(o2, lse2, o_ref, lse_ref, "dense, key-split units", o_res=res2)
 
 
 @pytest.mark.slow
@@ -171,15 +180,20 @@ def test_backward_random_tables(B, Hq, Hkv, Nq, Nk, d, causal, density):
 
 @pytest.mark.parametrize("causal,d", [(False, 128), (True, 64)])
 def test_backward_every_tile_listed_equals_the_dense_kernels(causal, d):
+    """Both backward calls take the block-sparse forward's O, LSE and residual (the
+    dense forward without a mask may split keys and round O differently), so the
+    two backward paths see the same inputs and must agree bit for bit."""
     N = 1000
     x = inputs.shape_inputs(1, 4, 2, N, N, d, seed=5)
     nt = -(-N // 128)
-    (dq, dk, dv), _, _ = run_bwd(x, np.ones((nt, nt), bool), causal, 0.1)
+    rp, ci = csr(np.ones((nt, nt), bool))
     q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "do"))
-    o, lse, res = fa.forward(q, k, v, causal=causal, scale=0.1, residual=True)
+    rpd, cid = torch.from_numpy(rp).to(DEV), torch.from_numpy(ci).to(DEV)
+    o, lse, res = fa.forward_blocksparse(q, k, v, rpd, cid, causal=causal, scale=0.1, residual=True)
+    g1 = fa.backward_blocksparse(q, k, v, rpd, cid, o, lse, do, causal=causal, scale=0.1, o_residual=res)
     g2 = fa.backward(q, k, v, o, lse, do, causal=causal, scale=0.1, o_residual=res)
     torch.cuda.synchronize()
-    for a, b in zip((dq, dk, dv), g2):
+    for a, b in zip(g1, g2):
         assert torch.equal(a, b)
 
 

@@ -153,6 +153,20 @@ def test_residual_output(d):
     assert np.abs(r).max() > 0
 
 
+@pytest.mark.parametrize("B,H,N,d", [(1, 2, 1000, 128), (2, 2, 513, 64), (1, 8, 2048, 128)])
+def test_key_split_units(B, H, N, d):
+    """Without a mask the units of a partial last wave run as parts along the keys,
+    merged by their LSE: O (with its residual) and LSE still meet the bound, the
+    part holding the ragged last key tile included, and the workspace holds the
+    parts.  (The full MHA workload, split in its last wave, is checked below.)"""
+    x = inputs.shape_inputs(B, H, H, N, N, d, seed=N + d, with_do=False)
+    s = fa.binding.shape(B, H, H, N, N, d, None, False)
+    assert fa.library().fa_fwd_workspace_size(ctypes.byref(s)) > 256  # room for the parts' O and LSE
+    o, lse, res = run_fwd(x, False, 1 / np.sqrt(d), residual=True)
+    o_ref, lse_ref = A.attention_forward(x["q"], x["k"], x["v"], 1 / np.sqrt(d), False)
+    assert_fwd(o, lse, o_ref, lse_ref, f"key-split {B}x{H}x{N} d={d}", o_res=res)
+
+
 def test_deterministic():
     x = inputs.shape_inputs(1, 4, 2, 1000, 1000, 128, seed=3, with_do=False)
     a = run_fwd(x, True, 0.1)

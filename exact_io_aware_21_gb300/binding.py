@@ -76,6 +76,7 @@ SIGNATURES = {
     "fa_dq_unit": (_I, [_PS, _I, _PI, _PI, _PI]),
     "fa_decode_split_range": (_I, [_PS, _I, _I, _PI, _PI]),
     "fa_fwd_schedule": (_I, [_PS, _I, _PI, _PI]),
+    "fa_fwd_split_plan": (_I, [_PS, _I, _PI, _PI]),
     "fa_selftest_mma": (_I, [_I, _I, _VP, _VP, _VP, _VP, _VP]),
     "fa_fwd_blocksparse": (_I, [_PT, _PT, _PT, _VP, _VP, _I, _PT, _VP, _PT, _PS, _VP, _SZ, _VP]),
     "fa_bwd_blocksparse_workspace_size": (_SZ, [_PS, _I]),

@@ -347,6 +347,16 @@ int fa_fwd_schedule(const fa_shape_t* s, int grid, int* start, int* ord) {
   return FA_OK;
 }
 
+int fa_fwd_split_plan(const fa_shape_t* s, int sms, int* split0, int* nsplit) {
+  if (check_shape(s) != FA_OK || sms < 1 || !split0 || !nsplit) return FA_ERR_INVALID;
+  const Dims d = dims_of(s);
+  if (mask_kind(d) != MASK_NONE) return FA_ERR_INVALID;
+  const FwdSplit sp = fwd_split_plan(d, sms);
+  *split0 = sp.split0;
+  *nsplit = sp.nsplit;
+  return FA_OK;
+}
+
 int fa_decode_split_range(const fa_shape_t* s, int num_splits, int i, int* start, int* end) {
   if (check_shape(s) != FA_OK || num_splits <= 0 || !start || !end) return FA_ERR_INVALID;
   const int n = decode_nsplits(s->Nk, num_splits);

@@ -452,6 +452,15 @@ int fa_dq_unit(const fa_shape_t* shape, int index, int* b, int* h, int* q_tile);
  * FA_ERR_INVALID when the forward does not use one (not causal, more than 2048
  * units or 160 CTAs); it then claims units from a counter, longest first. */
 int fa_fwd_schedule(const fa_shape_t* shape, int grid, int* start, int* ord);
+/* The key-split plan of an unmasked bf16 forward on `sms` SMs: units split0 ..
+ * fa_fwd_num_units - 1 (those of the last, partial wave; all units when there are
+ * fewer than SMs) each run as *nsplit parts of whole key tiles, part k covering
+ * key tiles [k n / nsplit, (k + 1) n / nsplit) of the n = ceil(Nk / 128), and a
+ * combine merges the parts by their LSE.  *nsplit = 1 (and *split0 = the unit
+ * count): no split.  The rule: R = U mod sms (U when U < sms) units in the last
+ * wave, nsplit = min(floor(sms / R), 4, floor(n / 2)), used when at least 2.
+ * FA_ERR_INVALID for a masked (causal or windowed) shape: those never split. */
+int fa_fwd_split_plan(const fa_shape_t* shape, int sms, int* split0, int* nsplit);
 /* Key range [start, end) of decode split s. */
 int fa_decode_split_range(const fa_shape_t* shape, int num_splits, int s, int* start, int* end);
 

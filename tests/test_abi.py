@@ -359,6 +359,38 @@ def test_fwd_schedule_is_a_balanced_partition(lib, B, Hq, N, d, grid):
     assert max(loads) >= sum(cost) / grid
 
 
+@pytest.mark.parametrize("B,H,N,d,sms", [(4, 16, 2048, 64, 152), (1, 8, 2048, 128, 152), (2, 2, 513, 64, 152),
+                                         (1, 2, 200, 128, 152), (1, 16, 4096, 128, 152), (1, 1, 256, 64, 152),
+                                         (3, 5, 3000, 64, 16), (1, 4, 8192, 128, 152)])
+def test_fwd_split_plan(lib, B, H, N, d, sms):
+    """The unmasked forward's key-split plan: only the last wave's units are split (all of
+    them when there are fewer than SMs), into 2-4 parts of at least two key tiles, and the
+    split wave then fits on the SMs, so the launch's length in unit times drops from
+    ceil(U / sms) to floor(U / sms) + 1 / nsplit."""
+    s = S(B, H, H, N, N, d=d)
+    U = lib.fa_fwd_num_units(s)
+    nk = -(-N // 128)
+    s0, ns = ctypes.c_int(), ctypes.c_int()
+    assert lib.fa_fwd_split_plan(s, sms, ctypes.byref(s0), ctypes.byref(ns)) == 0
+    R = U % sms if U >= sms else U
+    if ns.value == 1:
+        assert s0.value == U
+        assert R == 0 or min(sms // R, 4, nk // 2) < 2
+        return
+    assert s0.value == U - R and 2 <= ns.value <= 4 and ns.value * 2 <= nk
+    assert R * ns.value <= sms                        # the split wave fits on the SMs
+    assert ns.value == min(sms // R, 4, nk // 2)
+    waves_before = -(-U // sms)
+    assert U // sms + 1 / ns.value < waves_before     # shorter in unit times
+
+
+def test_fwd_split_plan_only_without_a_mask(lib):
+    s0, ns = ctypes.c_int(), ctypes.c_int()
+    assert lib.fa_fwd_split_plan(S(1, 2, 2, 1000, 1000, causal=True), 152, ctypes.byref(s0), ctypes.byref(ns)) == 1
+    windowed = ctypes.byref(shape(1, 2, 2, 1000, 1000, 128, window=(5, 5)))
+    assert lib.fa_fwd_split_plan(windowed, 152, ctypes.byref(s0), ctypes.byref(ns)) == 1
+
+
 def test_fwd_schedule_only_for_causal(lib):
     start = (ctypes.c_int * 153)()
     ord_ = (ctypes.c_int * 4096)()

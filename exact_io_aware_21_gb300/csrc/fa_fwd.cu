@@ -72,9 +72,9 @@ struct FwdLayout {
   static constexpr int OFF_KV = 2 * QB;
   static constexpr int OFF_BAR = OFF_KV + STAGES * TB;
   // barriers: unit_full[2] unit_empty[2] q_full q_empty kv_full[NG] kv_empty[NG]
-  //           s_full[2] p_full[2] o_full[2] o_empty[2]
+  //           s_full[2] p_full[2] o_full[2] o_empty[2] p_full2[2]
   //           list_full[2] (block-sparse)
-  static constexpr int NBAR = 4 + 2 + 2 * NG + 8 + (SP ? 2 : 0);
+  static constexpr int NBAR = 4 + 2 + 2 * NG + 10 + (SP ? 2 : 0);
   static constexpr int OFF_UNIT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_TMEM = OFF_UNIT + 16;
   static constexpr int OFF_SCR = (OFF_TMEM + 16 + 1023) / 1024 * 1024;  // output staging, one per softmax warp
@@ -137,6 +137,7 @@ struct FwdParams {
 
 struct Bars {
   uint64_t *unit_full, *unit_empty, *q_full, *q_empty, *kv_full, *kv_empty, *s_full, *p_full, *o_full, *o_empty;
+  uint64_t* p_full2;    // [2]: the second half of a tile's P (keys 64-127; p_full: keys 0-63)
   uint64_t* list_full;  // block-sparse only
 };
 
@@ -156,6 +157,7 @@ __device__ __forceinline__ Bars carve_bars(uint8_t* smem) {
   r.o_full = r.p_full + 2;
   r.o_empty = r.o_full + 2;
   r.list_full = r.o_empty + 2;
+  r.p_full2 = r.list_full + (SP ? 2 : 0);
   return r;
 }
 
@@ -371,11 +373,11 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
     }
   };
   // P is read from TMEM, 8 columns per product (8 x 2 bf16 or 8 x 4 E4M3 keys)
-  auto issue_pv = [&](int t, uint32_t v_addr, bool acc) {
+  auto issue_pv = [&](int t, uint32_t v_addr, bool acc, int half) {  // half: the keys 64 h .. 64 h + 63
     const uint32_t d_tmem = tmem + 256 + t * D;
     const uint32_t p_tmem = tmem + t * 128;
 #pragma unroll
-    for (int k = 0; k < TILE / KS; ++k) {
+    for (int k = half * (TILE / KS / 2); k < (half + 1) * (TILE / KS / 2); ++k) {
       const uint64_t bd = sdesc_sw128(v_addr + k * KS * 128, TILE * 128, 1024);
       if (elect_one()) {
         if (F8)
@@ -447,10 +449,14 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
         const bool now = on(t, j);
         if (now) {
           if (j == a[t] && !warp_wait(&bar.o_empty[t], (active[t] & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
+          // P V in two halves of the keys, each as soon as its half of P is in TMEM
           if (!warp_wait(&bar.p_full[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
+          tc_fence_after();
+          issue_pv(t, v_addr, j > a[t], 0);
+          if (!warp_wait(&bar.p_full2[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
           pph[t] ^= 1;
           tc_fence_after();
-          issue_pv(t, v_addr, j > a[t]);
+          issue_pv(t, v_addr, true, 1);
           if (j == e[t] - 1 && elect_one()) mma_commit(&bar.o_full[t]);
         }
         if (j + 1 < nmax && on(t, j + 1)) {  // S of the tile's next step (its first, when it starts late)
@@ -637,44 +643,69 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
       const float2 neg_m2 = make_float2(off, off);
       float2 sum0 = make_float2(0.f, 0.f), sum1 = make_float2(0.f, 0.f);
       uint32_t pk[64];
+      // P in two halves of the keys: the first half's P V starts while the second
+      // half's exponentials run (E4M3: one store of all 128 keys, both halves at once)
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        const float2 x0 = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), cj2, neg_m2);
-        const float2 x1 = __ffma2_rn(make_float2(sv[2 * i + 2], sv[2 * i + 3]), cj2, neg_m2);
-        const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
-        const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
-        sum0 = __fadd2_rn(sum0, p0);
-        sum1 = __fadd2_rn(sum1, p1);
-        if (F8) {
-          pk[i >> 1] = pack4_e4m3(p0.x, p0.y, p1.x, p1.y);
-        } else {
-          pk[i] = pack_bf16(p0.x, p0.y);
-          pk[i + 1] = pack_bf16(p1.x, p1.y);
+      for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+        for (int i = 32 * hf; i < 32 * hf + 32; i += 2) {
+          const float2 x0 = __ffma2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), cj2, neg_m2);
+          const float2 x1 = __ffma2_rn(make_float2(sv[2 * i + 2], sv[2 * i + 3]), cj2, neg_m2);
+          const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+          const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+          sum0 = __fadd2_rn(sum0, p0);
+          sum1 = __fadd2_rn(sum1, p1);
+          if (F8) {
+            pk[i >> 1] = pack4_e4m3(p0.x, p0.y, p1.x, p1.y);
+          } else {
+            pk[i] = pack_bf16(p0.x, p0.y);
+            pk[i + 1] = pack_bf16(p1.x, p1.y);
+          }
         }
+        if (F8 && hf == 0) continue;
+        if (F8)
+          tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        else
+          tmem_st32(tS + 32 * hf, *reinterpret_cast<uint32_t(*)[32]>(&pk[32 * hf]));
+        if (hf == 0 && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {  // O *= alpha before its P V
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 v = __fmul2_rn(f32x2(o[2 * i], o[2 * i + 1]), a2);
+              o[2 * i] = __float_as_uint(v.x);
+              o[2 * i + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(tO + cc * 32, o);
+          }
+        }
+        if (F8 && j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 v = __fmul2_rn(f32x2(o[2 * i], o[2 * i + 1]), a2);
+              o[2 * i] = __float_as_uint(v.x);
+              o[2 * i + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(tO + cc * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        if (hf == 0 || F8) {
+          // (test instantiation: the first warp of query tile 0 of work unit 0 withholds its first hand-off)
+          if (DG != DG_WITHHOLD || u != 0 || j != 0 || t != 0 || wq != 0) warp_arrive(&bar.p_full[t]);
+        }
+        if (hf == 1) warp_arrive(&bar.p_full2[t]);
       }
       l_run = l_run * alpha + ((sum0.x + sum0.y) + (sum1.x + sum1.y));
-      tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      if (!F8) tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tO + cc * 32, o);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 v = __fmul2_rn(f32x2(o[2 * i], o[2 * i + 1]), a2);
-            o[2 * i] = __float_as_uint(v.x);
-            o[2 * i + 1] = __float_as_uint(v.y);
-          }
-          tmem_st32(tO + cc * 32, o);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      // (test instantiation: the first warp of query tile 0 of work unit 0 withholds its first hand-off)
-      if (DG != DG_WITHHOLD || u != 0 || j != 0 || t != 0 || wq != 0)
-        warp_arrive(&bar.p_full[t]);
       if (DG == DG_TRACE && j == n - 1 && wq == 0 && lane_id() == 0) trace_unit(p, b, h, pr)[7 + t] = globaltimer();
       m_run = m_new;
     }
@@ -892,6 +923,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar.s_full[t], 1);
       mbar_init(&bar.p_full[t], 4);
+      mbar_init(&bar.p_full2[t], 4);
       mbar_init(&bar.o_full[t], 1);
       mbar_init(&bar.o_empty[t], 4);
     }

@@ -450,12 +450,15 @@ __device__ void fwd_mma(uint8_t* smem, const Bars& bar, const int* unit_slot, ui
         if (now) {
           if (j == a[t] && !warp_wait(&bar.o_empty[t], (active[t] & 1) ^ 1, ctl, FA_STATUS_TIMEOUT_MMA)) return;
           // P V in two halves of the keys, each as soon as its half of P is in TMEM
+          // (E4M3: one hand-off; half a P V is two products, too short to overlap)
           if (!warp_wait(&bar.p_full[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
           tc_fence_after();
           issue_pv(t, v_addr, j > a[t], 0);
-          if (!warp_wait(&bar.p_full2[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
+          if (!F8) {
+            if (!warp_wait(&bar.p_full2[t], pph[t], ctl, FA_STATUS_TIMEOUT_MMA)) return;
+            tc_fence_after();
+          }
           pph[t] ^= 1;
-          tc_fence_after();
           issue_pv(t, v_addr, true, 1);
           if (j == e[t] - 1 && elect_one()) mma_commit(&bar.o_full[t]);
         }
@@ -703,7 +706,7 @@ __device__ void fwd_softmax(int t, uint8_t* smem, const Bars& bar, const int* un
           // (test instantiation: the first warp of query tile 0 of work unit 0 withholds its first hand-off)
           if (DG != DG_WITHHOLD || u != 0 || j != 0 || t != 0 || wq != 0) warp_arrive(&bar.p_full[t]);
         }
-        if (hf == 1) warp_arrive(&bar.p_full2[t]);
+        if (hf == 1 && !F8) warp_arrive(&bar.p_full2[t]);
       }
       l_run = l_run * alpha + ((sum0.x + sum0.y) + (sum1.x + sum1.y));
       if (DG == DG_TRACE && j == n - 1 && wq == 0 && lane_id() == 0) trace_unit(p, b, h, pr)[7 + t] = globaltimer();

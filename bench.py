@@ -60,6 +60,7 @@ this host's cores on a bounded sample of the same workloads.
 """
 
 import argparse
+import ctypes
 import itertools
 import json
 import os
@@ -426,14 +427,27 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- our arm
 class Leg:
-    def __init__(self, name, kind, w, fns, work):
+    def __init__(self, name, kind, w, fns, work, launches=None):
         self.name, self.kind, self.w, self.fns, self.work = name, kind, w, fns, work
         self.ms = {k: 0.0 for k, _ in fns}
+        self.launches = launches or {}  # kernels per call where a shape differs from KERNELS_PER_CALL
+
+    def kernels(self, part):
+        return self.launches.get(part, KERNELS_PER_CALL[part])
 
 
 KERNELS_PER_CALL = {"fwd_bs": 2, "bwd_bs": 5, "fwd": 2, "bwd": 4, "bwd_pre": 2, "bwd_dkdv": 2, "bwd_dq": 2, "decode": 2,
                     "quant_q": 1, "quant_k": 1,
                     "quant_v": 2, "fwd_fp8": 2, "fwd_fp8_cr": 2, "fwd_varlen": 3, "bwd_varlen": 5}
+
+
+def fwd_kernels(lib, s, sms):
+    """Kernels one bf16 forward call launches: the header clear and the forward, plus
+    the combine of the key-split parts when the shape's plan splits (unmasked only)."""
+    s0, ns = ctypes.c_int(), ctypes.c_int()
+    if lib.fa_fwd_split_plan(ctypes.byref(s), sms, ctypes.byref(s0), ctypes.byref(ns)) != 0:
+        return KERNELS_PER_CALL["fwd"]
+    return KERNELS_PER_CALL["fwd"] + (1 if ns.value > 1 else 0)
 
 
 def kernel_flops(part, w):
@@ -446,8 +460,6 @@ def kernel_flops(part, w):
 
 
 def make_legs(device, seed):
-    import ctypes
-
     import exact_io_aware_21_gb300 as fa
     from exact_io_aware_21_gb300 import binding as B
     from exact_io_aware_21_gb300 import inputs
@@ -456,6 +468,7 @@ def make_legs(device, seed):
     train, dec, win = workloads()
     legs, state = [], {}
     tiny = tiny_workload()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
     for w in train + win + [tiny]:
         x = inputs.make(w, device=device, seed=w.seed + seed)
         s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal, w.window)
@@ -486,7 +499,7 @@ def make_legs(device, seed):
         fns = [("fwd", fwd), ("bwd", bwd), ("bwd_pre", lambda part=part: part(0)),
                ("bwd_dkdv", lambda part=part: part(1)), ("bwd_dq", lambda part=part: part(2))]
         kind = "tiny" if w is tiny else "window" if w.window else "train"
-        legs.append(Leg(w.name, kind, w, fns, 3.5 * fwd_flops(w)))
+        legs.append(Leg(w.name, kind, w, fns, 3.5 * fwd_flops(w), {"fwd": fwd_kernels(lib, s, sms)}))
         if w.name in TARGET_TRAIN:  # conditional rescaling beside the exact forward
             st["s_cr"] = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal, w.window, RESCALE_THRESHOLD)
 
@@ -494,7 +507,8 @@ def make_legs(device, seed):
                 x = st["x"]
                 B.fa_fwd(x["q"], x["k"], x["v"], st["o"], st["lse"], st["s_cr"], st["wsf"], st["ores"])
 
-            legs.append(Leg(w.name + RESCALE_SUFFIX, "rescale", w, [("fwd", fwd_cr)], fwd_flops(w)))
+            legs.append(Leg(w.name + RESCALE_SUFFIX, "rescale", w, [("fwd", fwd_cr)], fwd_flops(w),
+                            {"fwd": fwd_kernels(lib, st["s_cr"], sms)}))
         if w.name in TARGET_TRAIN and not w.outliers:  # the forward with the residual written anyway
             st["ores_x"] = torch.empty_like(x["q"])
 
@@ -502,7 +516,8 @@ def make_legs(device, seed):
                 x = st["x"]
                 B.fa_fwd(x["q"], x["k"], x["v"], st["o"], st["lse"], st["s"], st["wsf"], st["ores_x"])
 
-            legs.append(Leg(w.name + RESIDUAL_SUFFIX, "residual", w, [("fwd", fwd_res)], fwd_flops(w)))
+            legs.append(Leg(w.name + RESIDUAL_SUFFIX, "residual", w, [("fwd", fwd_res)], fwd_flops(w),
+                            {"fwd": fwd_kernels(lib, s, sms)}))
     for i, w in enumerate(dec):
         paged = i == len(dec) - 1
         name = PAGED_NAME if paged else w.name
@@ -674,8 +689,6 @@ def r4(x):
 
 def fwd_trace(leg, st, device):
     """One traced forward of a training leg (outside the timed region)."""
-    import ctypes
-
     from exact_io_aware_21_gb300 import binding as B
 
     units = B.library().fa_fwd_num_units(ctypes.byref(st["s"]))
@@ -1007,7 +1020,7 @@ def run_ours(args):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * sum(KERNELS_PER_CALL[p] for l in legs for p, _ in l.fns),
+        "gpu_launches": args.steps * sum(l.kernels(p) for l in legs for p, _ in l.fns),
         "clocks": clocks,
         "configs": configs,
         "legs": legs_out,

@@ -92,3 +92,25 @@ def test_trace_summary_of_a_synthetic_trace():
     assert s["unit_claim_to_first_product_us"]["max"] == 1.0
     assert s["unit_last_product_to_output_us"] == {"min": 1.0, "median": 1.0, "max": 1.0}
     assert s["issue_share_of_busy"] == round((3.5 + 5.5 + 4.0) / 17.0, 4)
+
+
+def test_forward_launch_count_follows_the_split_plan():
+    """A forward call launches the header clear and the forward, plus the combine
+    kernel exactly when the shape's key-split plan splits (unmasked shapes only)."""
+    import exact_io_aware_21_gb300 as fa
+    from exact_io_aware_21_gb300 import binding as B
+
+    lib = fa.library()
+    train, dec, win = bench.workloads()
+    counts = {}
+    for w in train + win + [bench.tiny_workload()]:
+        s = B.shape(w.B, w.Hq, w.Hkv, w.Nq, w.Nk, w.d, w.scale, w.causal, w.window)
+        counts[w.name] = bench.fwd_kernels(lib, s, 152)
+        if w.causal or w.window:
+            assert counts[w.name] == 2
+    # B4 H16 N2048 d64: 512 units of two query tiles, 56 in the last wave of 152 SMs
+    assert counts["mha_b4_h16_n2048_d64"] == 3
+    assert counts["tiny_b1_h1_n256_d64"] == 2  # one unit of two key tiles: too short to split
+    # the same shape on an SM count that divides its units does not split
+    s = B.shape(4, 16, 16, 2048, 2048, 64, 0.125, False)
+    assert bench.fwd_kernels(lib, s, 128) == 2

@@ -153,18 +153,27 @@ def test_residual_output(d):
     assert np.abs(r).max() > 0
 
 
-@pytest.mark.parametrize("B,H,N,d", [(1, 2, 1000, 128), (2, 2, 513, 64), (1, 8, 2048, 128)])
-def test_key_split_units(B, H, N, d):
+@pytest.mark.parametrize("B,Hq,Hkv,Nq,Nk,d", [
+    (1, 2, 2, 1000, 1000, 128), (2, 2, 2, 513, 513, 64), (1, 8, 8, 2048, 2048, 128),
+    (1, 8, 2, 1024, 1024, 128),   # grouped heads, 4 parts
+    (1, 4, 1, 777, 777, 64),      # one K/V head, 3 parts, the last holding the ragged tile
+    (1, 2, 2, 300, 1500, 64),     # Nq != Nk, 4 parts of 3 key tiles each
+])
+def test_key_split_units(B, Hq, Hkv, Nq, Nk, d):
     """Without a mask the units of a partial last wave run as parts along the keys,
     merged by their LSE: O (with its residual) and LSE still meet the bound, the
     part holding the ragged last key tile included, and the workspace holds the
     parts.  (The full MHA workload, split in its last wave, is checked below.)"""
-    x = inputs.shape_inputs(B, H, H, N, N, d, seed=N + d, with_do=False)
-    s = fa.binding.shape(B, H, H, N, N, d, None, False)
+    s = fa.binding.shape(B, Hq, Hkv, Nq, Nk, d, None, False)
+    s0, ns = ctypes.c_int(), ctypes.c_int()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert fa.library().fa_fwd_split_plan(ctypes.byref(s), sms, ctypes.byref(s0), ctypes.byref(ns)) == 0
+    assert ns.value >= 2  # the shape does split
     assert fa.library().fa_fwd_workspace_size(ctypes.byref(s)) > 256  # room for the parts' O and LSE
+    x = inputs.shape_inputs(B, Hq, Hkv, Nq, Nk, d, seed=Nq + Nk + d, with_do=False)
     o, lse, res = run_fwd(x, False, 1 / np.sqrt(d), residual=True)
     o_ref, lse_ref = A.attention_forward(x["q"], x["k"], x["v"], 1 / np.sqrt(d), False)
-    assert_fwd(o, lse, o_ref, lse_ref, f"key-split {B}x{H}x{N} d={d}", o_res=res)
+    assert_fwd(o, lse, o_ref, lse_ref, f"key-split {B}x{Hq}/{Hkv}x{Nq}x{Nk} d={d} parts={ns.value}", o_res=res)
 
 
 @pytest.mark.parametrize("causal", [True, False])

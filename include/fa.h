@@ -126,7 +126,10 @@ typedef struct {
  * there are fewer units than SMs), the units of that wave run as 2-4 parts
  * along the keys (flash-decoding's split, here for a prefill), each writing its
  * normalised O and LSE to the workspace, and a third kernel merges the parts
- * by their LSE into O, the residual and LSE.
+ * by their LSE into O, the residual and LSE.  Results are bitwise the same on
+ * every call for one shape on one device; on a device with another SM count
+ * an unmasked shape may split differently (fa_fwd_split_plan), which changes
+ * the rounding of O and LSE but not their error bound.
  * ------------------------------------------------------------------------- */
 size_t fa_fwd_workspace_size(const fa_shape_t* shape);
 int fa_fwd(const fa_tensor_t* q, const fa_tensor_t* k, const fa_tensor_t* v, const fa_tensor_t* o, float* lse,
